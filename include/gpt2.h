@@ -1,0 +1,172 @@
+/*
+ * gpt2.h -- C-ABI of libgpt2b300, one GPT-2 training step on one B300 (sm_103a).
+ *
+ * The step is the one described on "Karpathy's llm.c: understanding LLM
+ * training from scratch in C/CUDA", section "Code anatomy": token+position
+ * embedding, pre-LN transformer blocks (LayerNorm, fused QKV projection,
+ * causal multi-head softmax attention, output projection + residual, 4C MLP
+ * with tanh-GELU + residual), final LayerNorm, a classifier tied to the token
+ * embedding with softmax cross-entropy, the hand-derived backward pass in
+ * reverse graph order, and one AdamW update over fp32 master weights
+ * ("Karpathy reproduces GPT-2 (1.6B) in llm.c", section "Training" and its
+ * flag guide: AdamW, weight decay 0.1 on 2-D weights, gradient clipping,
+ * gradient accumulation, vocabulary padded 50257 -> 50304).
+ *
+ * Conventions shared by every call
+ *  - Every call takes the handle made by gpt2_create and returns an int status
+ *    (GPT2_OK or a negative GPT2_ERR_*); gpt2_last_error() gives a sentence.
+ *  - All GPU work is enqueued on the handle's CUDA stream (the `stream`
+ *    argument of gpt2_create, a cudaStream_t; NULL = the legacy default
+ *    stream).  Calls return without waiting unless stated otherwise.
+ *  - Device pointers ("d_" prefix) must point to memory on the handle's
+ *    device; host pointers ("h_" prefix) to ordinary or pinned host memory.
+ *  - A handle is not thread-safe: one host thread at a time.
+ *  - The handle owns all model state: parameters, gradients, optimizer state
+ *    and activations live in one device workspace, either allocated once by
+ *    gpt2_create or supplied by the caller.  Token buffers stay the caller's.
+ *
+ * Canonical parameter order (weights out x in, row-major), used by every
+ * get/set call:  wte[Vp,C] wpe[T,C] ln1w[L,C] ln1b[L,C] qkvw[L,3C,C]
+ * qkvb[L,3C] projw[L,C,C] projb[L,C] ln2w[L,C] ln2b[L,C] fcw[L,4C,C]
+ * fcb[L,4C] fcprojw[L,C,4C] fcprojb[L,C] lnfw[C] lnfb[C],
+ * where Vp = V rounded up to a multiple of 128 (padded rows are 0 and stay 0).
+ */
+#ifndef GPT2_B300_H
+#define GPT2_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gpt2 gpt2_t;
+
+/* Arithmetic modes.
+ *  GPT2_FP32: parameters, activations and gradients in fp32, every matmul and
+ *             attention product with fp32 FFMA (no TF32).  This is the parity
+ *             mode, checked against the CPU oracle.
+ *  GPT2_BF16: fp32 master weights, AdamW state and gradients; bf16 compute
+ *             copies of the weights and bf16 activations; tensor-core
+ *             contractions with fp32 accumulation; fp32 LayerNorm statistics,
+ *             softmax, loss.  This is the mixed-precision training mode of
+ *             "Karpathy's llm.c ...", section "Code anatomy", item 3. */
+enum { GPT2_FP32 = 0, GPT2_BF16 = 1 };
+
+enum {
+    GPT2_OK = 0,
+    GPT2_ERR_ARG = -1,          /* bad argument or unsupported shape            */
+    GPT2_ERR_CUDA = -2,         /* a CUDA runtime/driver call failed            */
+    GPT2_ERR_OOM = -3,          /* device allocation failed                     */
+    GPT2_ERR_STATE = -4,        /* call out of order (e.g. backward w/o forward)*/
+    GPT2_ERR_TOKEN_RANGE = -5,  /* a token or target id outside [0, V)          */
+    GPT2_ERR_NONFINITE = -6,    /* gradient norm not finite: update skipped     */
+    GPT2_ERR_TIMEOUT = -7       /* a bounded device-side wait ran out           */
+};
+
+/* Bytes of device workspace a handle of this shape needs (0 if the shape is
+ * rejected).  Shape limits: C % H == 0; in GPT2_BF16 mode C % 8 == 0; the
+ * attention head size C/H is at most 128. */
+size_t gpt2_workspace_bytes(int L, int H, int C, int V, int T, int B, int mode);
+
+/* Make a model with L layers, H heads, width C, vocabulary V (padded
+ * internally to Vp), context T and micro-batch B.  Parameters are initialised
+ * from `seed`: matrices and both embeddings ~ N(0, 0.02), the two residual
+ * projections (projw, fcprojw) ~ N(0, 0.02/sqrt(2L)), biases 0, LayerNorm
+ * gains 1; element i of the canonical vector uses SplitMix64 outputs 2i and
+ * 2i+1 for a Box-Muller normal.
+ *   workspace: NULL -> the library cudaMallocs gpt2_workspace_bytes() once and
+ *              frees it in gpt2_destroy; else a device buffer of ws_bytes
+ *              (>= gpt2_workspace_bytes, 256-byte aligned) that the caller
+ *              keeps alive until gpt2_destroy.
+ *   stream:    cudaStream_t to enqueue on.
+ * Synchronises the stream once (initialisation).  On failure *out = NULL. */
+int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int B, uint64_t seed,
+                int mode, void* workspace, size_t ws_bytes, void* stream);
+
+void gpt2_destroy(gpt2_t* g);
+const char* gpt2_last_error(gpt2_t* g);
+
+/* Change the stream later calls enqueue on. */
+int gpt2_set_stream(gpt2_t* g, void* stream);
+
+/* Forward pass over one micro-batch: d_tokens and d_targets are int32 [B,T]
+ * on the device.  d_targets NULL: logits only (readable by gpt2_get_logits),
+ * no loss, and gpt2_backward is refused.  With targets the mean
+ * cross-entropy over the B*T positions is computed and the logits buffer is
+ * overwritten in place by d(loss)/d(logits) for the backward pass (the
+ * probabilities are never stored).  h_loss NULL: stay asynchronous (the loss
+ * stays on the device, gpt2_get_loss reads it); else synchronise and write
+ * the loss.  Out-of-range ids are flagged on the device and reported as
+ * GPT2_ERR_TOKEN_RANGE at the next synchronising call. */
+int gpt2_forward(gpt2_t* g, const int32_t* d_tokens, const int32_t* d_targets, float* h_loss);
+
+/* As gpt2_forward, with tokens/targets in host memory: copies them into the
+ * handle's own device buffers (cudaMemcpyAsync on the handle's stream), then
+ * runs the same forward pass. h_targets may be NULL. */
+int gpt2_forward_host(gpt2_t* g, const int32_t* h_tokens, const int32_t* h_targets,
+                      float* h_loss);
+
+/* Backward pass of the last forward (which must have had targets):
+ * gradients += d(mean micro-batch loss)/d(params); the micro-batch counter
+ * n_accum is incremented.  Asynchronous. */
+int gpt2_backward(gpt2_t* g);
+
+/* One AdamW step on the accumulated gradients.  The gradient used is the mean
+ * over the n_accum micro-batches, g/n_accum; its global L2 norm n over all
+ * parameters is computed; if clip > 0 and n > clip every gradient is scaled
+ * by clip/n.  Then m = b1 m + (1-b1) g, v = b2 v + (1-b2) g^2, and
+ * w -= lr (m_hat / (sqrt(v_hat) + eps) + wd w [w is a 2-D weight: wte, wpe,
+ * qkvw, projw, fcw, fcprojw]), with bias corrections 1-b1^t, 1-b2^t and t the
+ * 1-based step count.  In GPT2_BF16 mode the bf16 compute copy is refreshed
+ * (round to nearest even).  Synchronises.  A non-finite n leaves every state
+ * unchanged and returns GPT2_ERR_NONFINITE.  h_grad_norm (optional) gets n.
+ * Gradients are left as they are (call gpt2_zero_grad). */
+int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float eps, float wd, float clip,
+                    float* h_grad_norm);
+
+/* gradients = 0, n_accum = 0.  Asynchronous. */
+int gpt2_zero_grad(gpt2_t* g);
+
+/* Wait for the stream, then report any error flagged on the device. */
+int gpt2_sync(gpt2_t* g);
+
+/* ---- inspection (synchronise; fp32 host buffers, canonical order) ---- */
+size_t gpt2_num_params(gpt2_t* g);      /* stored count, padded vocabulary */
+int gpt2_padded_vocab(gpt2_t* g);
+int gpt2_get_params(gpt2_t* g, float* h_buf);       /* master weights        */
+int gpt2_set_params(gpt2_t* g, const float* h_buf); /* also refreshes bf16   */
+int gpt2_get_grads(gpt2_t* g, float* h_buf);        /* accumulated, not /n   */
+int gpt2_set_grads(gpt2_t* g, const float* h_buf);
+int gpt2_get_opt_state(gpt2_t* g, float* h_m, float* h_v, int* h_step);
+/* AdamW first/second moments and the step count t (m, v: fp32, canonical
+ * order, either may be NULL to leave it unchanged; step >= 0). */
+int gpt2_set_opt_state(gpt2_t* g, const float* h_m, const float* h_v, int step);
+/* logits [B,T,V] of the last forward WITHOUT targets (real columns only) */
+int gpt2_get_logits(gpt2_t* g, float* h_buf);
+int gpt2_get_loss(gpt2_t* g, float* h_loss);        /* mean loss, last fwd  */
+int gpt2_get_losses(gpt2_t* g, float* h_buf);       /* per position [B,T]   */
+
+/* ---- per-kernel timing (CUDA events on the handle's stream) ----
+ * gpt2_prof_enable(g, mask): bit c of mask turns on timing of class c (0 turns
+ * all timing off).  Every launch of an enabled class is bracketed by events;
+ * gpt2_prof_read sums the elapsed times since the last reset.  Classes are
+ * numbered 0..gpt2_prof_num_classes()-1 and named by gpt2_prof_name().
+ * flops / bytes are the ALGORITHMIC work of the counted launches (model
+ * flops for contractions; compulsory HBM bytes for the rest). */
+int gpt2_prof_enable(gpt2_t* g, unsigned class_mask);
+int gpt2_prof_reset(gpt2_t* g);
+int gpt2_prof_num_classes(void);
+const char* gpt2_prof_name(int cls);
+int gpt2_prof_read(gpt2_t* g, int cls, double* ms, long long* launches, double* flops,
+                   double* bytes);
+
+/* Number of CUDA kernels this handle has launched since gpt2_create
+ * (memsets and copies are not counted). */
+long long gpt2_launch_count(gpt2_t* g);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

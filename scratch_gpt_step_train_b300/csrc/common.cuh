@@ -1,0 +1,67 @@
+// common.cuh -- small device helpers shared by the kernels of libgpt2b300.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+typedef __nv_bfloat16 bf16;
+
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// Butterfly reductions over the 32 lanes of a warp (__shfl_xor_sync), the
+// primitive named in "Karpathy's llm.c ...", section "Code anatomy", item 2.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Vector of N elements of T moved as one 16-byte (or smaller) access.
+template <typename T, int N>
+struct alignas(sizeof(T) * N) Vec {
+    T v[N];
+};
+
+template <typename T, int N>
+__device__ __forceinline__ void load_vec_f(float* dst, const T* src) {
+    Vec<T, N> x = *reinterpret_cast<const Vec<T, N>*>(src);
+#pragma unroll
+    for (int i = 0; i < N; i++) dst[i] = to_f(x.v[i]);
+}
+template <typename T, int N>
+__device__ __forceinline__ void store_vec_f(T* dst, const float* src) {
+    Vec<T, N> x;
+#pragma unroll
+    for (int i = 0; i < N; i++) x.v[i] = from_f<T>(src[i]);
+    *reinterpret_cast<Vec<T, N>*>(dst) = x;
+}
+
+// tanh-form GELU (Hendrycks & Gimpel 2016) and its analytic derivative.
+__device__ __forceinline__ float gelu_f(float x) {
+    const float k = 0.7978845608028654f;  // sqrt(2/pi)
+    float u = k * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.0f + tanhf(u));
+}
+__device__ __forceinline__ float gelu_grad_f(float x) {
+    const float k = 0.7978845608028654f;
+    float x2 = x * x;
+    float u = k * (x + 0.044715f * x2 * x);
+    float th = tanhf(u);
+    float du = k * (1.0f + 3.0f * 0.044715f * x2);
+    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
+}

@@ -1,0 +1,789 @@
+// gpt2.cu -- host orchestration of the GPT-2 training step behind the C-ABI
+// declared in include/gpt2.h: workspace planning (one allocation), the launch
+// sequence of the forward pass, the backward pass in reverse graph order,
+// the AdamW step, error reporting and per-kernel event timing.
+//
+// The order of operations follows "Karpathy's llm.c: understanding LLM
+// training from scratch in C/CUDA", "Code anatomy" (encoder -> per-layer
+// layernorm / attention / MLP -> classifier; backward from d(loss)/d(logits)
+// back through every layer; one parameter-update kernel), and the gradient
+// accumulation / AdamW / clipping of "Karpathy reproduces GPT-2 (1.6B) in
+// llm.c", "Training".
+#include "../../include/gpt2.h"
+#include "kernels.h"
+#include "gemm_tc.h"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+using namespace gk;
+
+// ---------------------------------------------------------------------------
+// kernel classes for event timing
+// ---------------------------------------------------------------------------
+enum {
+    K_MM_FWD, K_MM_CLS_FWD, K_MM_DX, K_MM_DW, K_ATTN_FWD, K_ATTN_BWD, K_LN_FWD, K_LN_BWD,
+    K_XENT, K_EMB_FWD, K_EMB_BWD, K_BIAS, K_ADAM, K_ZERO, K_NCLASS
+};
+static const char* kClassNames[K_NCLASS] = {
+    "matmul_fwd", "matmul_classifier_fwd", "matmul_bwd_dx", "matmul_bwd_dw", "attention_fwd",
+    "attention_bwd", "layernorm_fwd", "layernorm_bwd", "crossentropy", "embedding_fwd",
+    "embedding_bwd", "bias_grad", "adamw", "zero_grad"};
+
+struct ProfRec {
+    int cls;
+    cudaEvent_t a, b;
+    double flops, bytes;
+};
+
+struct gpt2 {
+    int L, H, C, V, Vp, T, B, mode, act;
+    size_t BT;
+    ParamLayout lay;
+    size_t nparams;
+    cudaStream_t stream;
+    void* ws;
+    bool own_ws;
+    size_t ws_bytes;
+    bool use_tc;  // tensor-core GEMMs (bf16 mode)
+    int device;   // CUDA device of the workspace
+
+    float *master, *grads, *m, *v;
+    void* pc;  // compute copy of the parameters (== master in fp32 mode)
+    // activations
+    void *encoded, *ln1, *qkv, *atty, *x1, *ln2, *fch, *fchg, *x2, *lnf, *logits;
+    float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lnf_mean, *lnf_rstd, *lse, *losses;
+    float* loss;
+    // backward buffers
+    void *dres, *dbig, *dln, *datty, *dqkv;
+    void* scratch;
+    size_t scratch_bytes;
+    int32_t *tok, *tgt;
+    unsigned* err;
+    float* adam_state;
+
+    int n_accum, t, have_targets, logits_valid, have_fwd;
+    std::string last_err;
+
+    long long launches;  // kernels launched by this handle
+    unsigned prof_mask;  // classes timed with events
+    bool prof_on, prof_cur;
+    std::vector<ProfRec> prof;
+    size_t prof_used;
+    double prof_ms[K_NCLASS], prof_flops[K_NCLASS], prof_bytes[K_NCLASS];
+    long long prof_n[K_NCLASS];
+};
+
+static int fail(gpt2* g, int code, const char* fmt, ...) {
+    if (g) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        g->last_err = buf;
+    }
+    return code;
+}
+
+#define CK(expr)                                                                         \
+    do {                                                                                 \
+        cudaError_t e_ = (expr);                                                         \
+        if (e_ != cudaSuccess)                                                           \
+            return fail(g, GPT2_ERR_CUDA, "%s: %s (%s:%d)", #expr, cudaGetErrorString(e_), \
+                        __FILE__, __LINE__);                                             \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// event timing around one launch group
+// ---------------------------------------------------------------------------
+static void prof_begin(gpt2* g, int cls, double flops, double bytes) {
+    g->prof_cur = g->prof_on && ((g->prof_mask >> cls) & 1u);
+    if (!g->prof_cur) return;
+    if (g->prof_used == g->prof.size()) {
+        ProfRec r;
+        cudaEventCreate(&r.a);
+        cudaEventCreate(&r.b);
+        g->prof.push_back(r);
+    }
+    ProfRec& r = g->prof[g->prof_used];
+    r.cls = cls;
+    r.flops = flops;
+    r.bytes = bytes;
+    cudaEventRecord(r.a, g->stream);
+}
+static void prof_end(gpt2* g) {
+    if (!g->prof_cur) return;
+    cudaEventRecord(g->prof[g->prof_used].b, g->stream);
+    g->prof_used++;
+}
+static void prof_collect(gpt2* g) {
+    if (g->prof_used == 0) return;
+    cudaEventSynchronize(g->prof[g->prof_used - 1].b);
+    for (size_t i = 0; i < g->prof_used; i++) {
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, g->prof[i].a, g->prof[i].b);
+        int c = g->prof[i].cls;
+        g->prof_ms[c] += ms;
+        g->prof_flops[c] += g->prof[i].flops;
+        g->prof_bytes[c] += g->prof[i].bytes;
+        g->prof_n[c] += 1;
+    }
+    g->prof_used = 0;
+}
+
+// ---------------------------------------------------------------------------
+// workspace plan
+// ---------------------------------------------------------------------------
+struct Planner {
+    char* base;
+    size_t off;
+    void* take(size_t bytes) {
+        void* p = base ? base + off : nullptr;
+        off += (bytes + 255) & ~(size_t)255;
+        return p;
+    }
+};
+
+static size_t scratch_need(int L, int H, int C, int Vp, int T, int B) {
+    size_t BT = (size_t)B * T;
+    size_t s = layernorm_backward_scratch((int)BT, C);
+    size_t x;
+    if ((x = bias_grad_scratch((int)BT, 4 * C)) > s) s = x;
+    if ((x = encoder_backward_scratch(B, T, C, Vp)) > s) s = x;
+    if ((x = attention_backward_scratch(B, T, H)) > s) s = x;
+    if ((x = adamw_scratch()) > s) s = x;
+    return s;
+}
+
+static void plan(gpt2* g, char* base, size_t* total) {
+    Planner p{base, 0};
+    size_t N = g->nparams, BT = g->BT, C = g->C, L = g->L;
+    size_t as = act_size(g->act);
+    g->master = (float*)p.take(N * 4);
+    g->grads = (float*)p.take(N * 4);
+    g->m = (float*)p.take(N * 4);
+    g->v = (float*)p.take(N * 4);
+    g->pc = g->act == ACT_BF16 ? p.take(N * 2) : (void*)g->master;
+    g->encoded = p.take(BT * C * as);
+    g->ln1 = p.take(L * BT * C * as);
+    g->qkv = p.take(L * BT * 3 * C * as);
+    g->atty = p.take(L * BT * C * as);
+    g->x1 = p.take(L * BT * C * as);
+    g->ln2 = p.take(L * BT * C * as);
+    g->fch = p.take(L * BT * 4 * C * as);
+    g->fchg = p.take(L * BT * 4 * C * as);
+    g->x2 = p.take(L * BT * C * as);
+    g->lnf = p.take(BT * C * as);
+    g->logits = p.take(BT * (size_t)g->Vp * as);
+    g->ln1_mean = (float*)p.take(L * BT * 4);
+    g->ln1_rstd = (float*)p.take(L * BT * 4);
+    g->ln2_mean = (float*)p.take(L * BT * 4);
+    g->ln2_rstd = (float*)p.take(L * BT * 4);
+    g->lnf_mean = (float*)p.take(BT * 4);
+    g->lnf_rstd = (float*)p.take(BT * 4);
+    g->lse = (float*)p.take(L * (size_t)g->B * g->H * g->T * 4);
+    g->losses = (float*)p.take(BT * 4);
+    g->loss = (float*)p.take(16);
+    g->dres = p.take(BT * C * as);
+    g->dbig = p.take(BT * 4 * C * as);
+    g->dln = p.take(BT * C * as);
+    g->datty = p.take(BT * C * as);
+    g->dqkv = p.take(BT * 3 * C * as);
+    g->scratch_bytes = scratch_need(g->L, g->H, g->C, g->Vp, g->T, g->B);
+    g->scratch = p.take(g->scratch_bytes);
+    g->tok = (int32_t*)p.take(BT * 4);
+    g->tgt = (int32_t*)p.take(BT * 4);
+    g->err = (unsigned*)p.take(16);
+    g->adam_state = (float*)p.take(16);
+    *total = p.off;
+}
+
+static bool shape_ok(int L, int H, int C, int V, int T, int B, int mode) {
+    if (L < 1 || H < 1 || C < 1 || V < 1 || T < 1 || B < 1) return false;
+    if (C % H) return false;
+    int hd = C / H;
+    if (hd != 8 && hd != 16 && hd != 32 && hd != 64 && hd != 128) return false;
+    if (mode != GPT2_FP32 && mode != GPT2_BF16) return false;
+    if (mode == GPT2_BF16 && C % 8) return false;
+    if ((long)B * T > (1L << 30) / 4) return false;
+    if (V >= (1 << 21) - 128) return false;
+    if (C > 2048 || (C % 4 && C > 512)) return false;  // LayerNorm register tiling
+    return true;
+}
+
+extern "C" size_t gpt2_workspace_bytes(int L, int H, int C, int V, int T, int B, int mode) {
+    if (!shape_ok(L, H, C, V, T, B, mode)) return 0;
+    gpt2 tmp;
+    tmp.L = L; tmp.H = H; tmp.C = C; tmp.V = V; tmp.T = T; tmp.B = B; tmp.mode = mode;
+    tmp.act = mode == GPT2_BF16 ? ACT_BF16 : ACT_F32;
+    tmp.Vp = ((V + 127) / 128) * 128;
+    tmp.BT = (size_t)B * T;
+    make_layout(&tmp.lay, L, C, V, T);
+    tmp.nparams = tmp.lay.off[P_NUM];
+    size_t total;
+    plan(&tmp, nullptr, &total);
+    return total;
+}
+
+// ---------------------------------------------------------------------------
+// create / destroy
+// ---------------------------------------------------------------------------
+extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int B, uint64_t seed,
+                           int mode, void* workspace, size_t ws_bytes, void* stream) {
+    if (!out) return GPT2_ERR_ARG;
+    *out = nullptr;
+    if (!shape_ok(L, H, C, V, T, B, mode)) return GPT2_ERR_ARG;
+    gpt2* g = new gpt2();
+    g->L = L; g->H = H; g->C = C; g->V = V; g->T = T; g->B = B; g->mode = mode;
+    g->act = mode == GPT2_BF16 ? ACT_BF16 : ACT_F32;
+    g->Vp = ((V + 127) / 128) * 128;
+    g->BT = (size_t)B * T;
+    make_layout(&g->lay, L, C, V, T);
+    g->nparams = g->lay.off[P_NUM];
+    g->stream = (cudaStream_t)stream;
+    g->prof_on = false;
+    g->prof_cur = false;
+    g->prof_mask = 0;
+    g->prof_used = 0;
+    g->launches = 0;
+    size_t need;
+    plan(g, nullptr, &need);
+    g->device = 0;
+    if (workspace) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, workspace) != cudaSuccess ||
+            pa.type != cudaMemoryTypeDevice) {
+            cudaGetLastError();
+            delete g;
+            return GPT2_ERR_ARG;
+        }
+        g->device = pa.device;
+    } else {
+        cudaGetDevice(&g->device);
+    }
+    cudaSetDevice(g->device);
+    if (workspace) {
+        if (ws_bytes < need || ((uintptr_t)workspace & 255)) {
+            delete g;
+            return GPT2_ERR_ARG;
+        }
+        g->ws = workspace;
+        g->own_ws = false;
+    } else {
+        if (cudaMalloc(&g->ws, need) != cudaSuccess) {
+            cudaGetLastError();
+            delete g;
+            return GPT2_ERR_OOM;
+        }
+        g->own_ws = true;
+    }
+    g->ws_bytes = need;
+    plan(g, (char*)g->ws, &need);
+    g->use_tc = (g->act == ACT_BF16) && gemm_tc_available();
+    cudaError_t e;
+    do {
+        if ((e = cudaMemsetAsync(g->grads, 0, g->nparams * 4, g->stream))) break;
+        if ((e = cudaMemsetAsync(g->m, 0, g->nparams * 4, g->stream))) break;
+        if ((e = cudaMemsetAsync(g->v, 0, g->nparams * 4, g->stream))) break;
+        if ((e = cudaMemsetAsync(g->err, 0, 16, g->stream))) break;
+        if ((e = init_params(g->master, g->lay, seed, g->stream))) break;
+        if (g->act == ACT_BF16 && (e = cast_to_bf16(g->pc, g->master, g->nparams, g->stream)))
+            break;
+        e = cudaStreamSynchronize(g->stream);
+    } while (0);
+    if (e != cudaSuccess) {
+        if (g->own_ws) cudaFree(g->ws);
+        delete g;
+        return GPT2_ERR_CUDA;
+    }
+    *out = g;
+    return GPT2_OK;
+}
+
+extern "C" void gpt2_destroy(gpt2_t* g) {
+    if (!g) return;
+    cudaStreamSynchronize(g->stream);
+    for (auto& r : g->prof) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    if (g->own_ws) cudaFree(g->ws);
+    delete g;
+}
+
+extern "C" const char* gpt2_last_error(gpt2_t* g) { return g ? g->last_err.c_str() : "null handle"; }
+
+extern "C" int gpt2_set_stream(gpt2_t* g, void* stream) {
+    if (!g) return GPT2_ERR_ARG;
+    g->stream = (cudaStream_t)stream;
+    return GPT2_OK;
+}
+
+// Read and clear the device error word (synchronises).
+static int check_dev_err(gpt2* g) {
+    unsigned e = 0;
+    CK(cudaMemcpyAsync(&e, g->err, 4, cudaMemcpyDeviceToHost, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    if (e) {
+        CK(cudaMemsetAsync(g->err, 0, 4, g->stream));
+        if (e & GPT2_DEVERR_TOKEN)
+            return fail(g, GPT2_ERR_TOKEN_RANGE, "a token or target id is outside [0, V)");
+        if (e & GPT2_DEVERR_TIMEOUT)
+            return fail(g, GPT2_ERR_TIMEOUT, "a bounded device wait ran out");
+        return fail(g, GPT2_ERR_CUDA, "device error word 0x%x", e);
+    }
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_sync(gpt2_t* g) {
+    if (!g) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    return check_dev_err(g);
+}
+
+// ---------------------------------------------------------------------------
+// building blocks
+// ---------------------------------------------------------------------------
+static void* pc_tensor(gpt2* g, int k, int l) {
+    size_t per = g->lay.off[k + 1] - g->lay.off[k];
+    if (k >= P_LN1W && k <= P_FCPROJB) per /= g->L;
+    return (char*)g->pc + (g->lay.off[k] + (size_t)l * per) * act_size(g->act);
+}
+static float* grad_tensor(gpt2* g, int k, int l) {
+    size_t per = g->lay.off[k + 1] - g->lay.off[k];
+    if (k >= P_LN1W && k <= P_FCPROJB) per /= g->L;
+    return g->grads + g->lay.off[k] + (size_t)l * per;
+}
+static void* act_at(gpt2* g, void* base, size_t elems_per_layer, int l) {
+    return (char*)base + (size_t)l * elems_per_layer * act_size(g->act);
+}
+
+// D[M,N] (epilogue) A[M,K] . B[N,K]^T
+static int mm(gpt2* g, int cls, GemmDesc d) {
+    d.act = g->act;
+    double fl = 2.0 * d.M * d.N * d.K;
+    double as = (double)act_size(g->act);
+    double by = as * ((double)d.M * d.K + (double)d.N * d.K) +
+                (d.epi == EPI_ACCUM_F32 ? 8.0 : as) * d.M * d.N;
+    g->launches += 1;
+    prof_begin(g, cls, fl, by);
+    cudaError_t e;
+    if (g->use_tc && gemm_tc_supported(d)) e = gemm_tc(d, g->stream);
+    else e = gemm_simt(d, g->stream);
+    prof_end(g);
+    if (e != cudaSuccess)
+        return fail(g, GPT2_ERR_CUDA, "matmul M=%d N=%d K=%d epi=%d: %s", d.M, d.N, d.K, d.epi,
+                    cudaGetErrorString(e));
+    return GPT2_OK;
+}
+
+static GemmDesc gd(int M, int N, int K, const void* A, long lda, int akm, const void* Bm, long ldb,
+                   int bkm, void* D, long ldd, int epi) {
+    GemmDesc d;
+    memset(&d, 0, sizeof d);
+    d.M = M; d.N = N; d.K = K;
+    d.A = A; d.lda = lda; d.a_kmajor = akm;
+    d.B = Bm; d.ldb = ldb; d.b_kmajor = bkm;
+    d.D = D; d.ldd = ldd; d.epi = epi;
+    return d;
+}
+
+#define RUN(expr)                      \
+    do {                               \
+        int rc_ = (expr);              \
+        if (rc_ != GPT2_OK) return rc_; \
+    } while (0)
+
+#define LAUNCH(cls, nk, fl, by, expr)                                                        \
+    do {                                                                                     \
+        g->launches += (nk);                                                                 \
+        prof_begin(g, cls, fl, by);                                                          \
+        cudaError_t e_ = (expr);                                                             \
+        prof_end(g);                                                                         \
+        if (e_ != cudaSuccess)                                                               \
+            return fail(g, GPT2_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));           \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// forward
+// ---------------------------------------------------------------------------
+static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
+    int B = g->B, T = g->T, C = g->C, L = g->L, H = g->H, Vp = g->Vp;
+    int BT = (int)g->BT;
+    size_t as = act_size(g->act);
+    size_t c = C, bt = g->BT;
+    LAUNCH(K_EMB_FWD, 1, 0, as * 3.0 * bt * c,
+           encoder_forward(g->act, g->encoded, g->tok, pc_tensor(g, P_WTE, 0),
+                           pc_tensor(g, P_WPE, 0), B, T, C, g->V, g->err, g->stream));
+    const void* resid = g->encoded;
+    double ln_bytes = as * 2.0 * bt * c + 8.0 * bt;
+    for (int l = 0; l < L; l++) {
+        void* ln1 = act_at(g, g->ln1, bt * c, l);
+        void* qkv = act_at(g, g->qkv, bt * 3 * c, l);
+        void* atty = act_at(g, g->atty, bt * c, l);
+        void* x1 = act_at(g, g->x1, bt * c, l);
+        void* ln2 = act_at(g, g->ln2, bt * c, l);
+        void* fch = act_at(g, g->fch, bt * 4 * c, l);
+        void* fchg = act_at(g, g->fchg, bt * 4 * c, l);
+        void* x2 = act_at(g, g->x2, bt * c, l);
+        float* lse = g->lse + (size_t)l * B * H * T;
+        LAUNCH(K_LN_FWD, 1, 0, ln_bytes,
+               layernorm_forward(g->act, ln1, g->ln1_mean + l * bt, g->ln1_rstd + l * bt, resid,
+                                 pc_tensor(g, P_LN1W, l), pc_tensor(g, P_LN1B, l), BT, C,
+                                 g->stream));
+        GemmDesc d = gd(BT, 3 * C, C, ln1, C, 1, pc_tensor(g, P_QKVW, l), C, 1, qkv, 3 * C,
+                        EPI_STORE);
+        d.bias = pc_tensor(g, P_QKVB, l);
+        RUN(mm(g, K_MM_FWD, d));
+        // causal attention flops: QK^T and PV over the lower triangle
+        double afl = 2.0 * 2.0 * B * H * ((double)T * (T + 1) / 2) * (C / H);
+        LAUNCH(K_ATTN_FWD, 1, afl, as * 4.0 * bt * c + 4.0 * B * H * T,
+               attention_forward(g->act, atty, lse, qkv, B, T, C, H, g->stream));
+        d = gd(BT, C, C, atty, C, 1, pc_tensor(g, P_PROJW, l), C, 1, x1, C, EPI_RESID);
+        d.bias = pc_tensor(g, P_PROJB, l);
+        d.resid = resid;
+        d.ldr = C;
+        RUN(mm(g, K_MM_FWD, d));
+        LAUNCH(K_LN_FWD, 1, 0, ln_bytes,
+               layernorm_forward(g->act, ln2, g->ln2_mean + l * bt, g->ln2_rstd + l * bt, x1,
+                                 pc_tensor(g, P_LN2W, l), pc_tensor(g, P_LN2B, l), BT, C,
+                                 g->stream));
+        d = gd(BT, 4 * C, C, ln2, C, 1, pc_tensor(g, P_FCW, l), C, 1, fchg, 4 * C, EPI_GELU);
+        d.bias = pc_tensor(g, P_FCB, l);
+        d.aux = fch;
+        d.ldx = 4 * C;
+        RUN(mm(g, K_MM_FWD, d));
+        d = gd(BT, C, 4 * C, fchg, 4 * C, 1, pc_tensor(g, P_FCPROJW, l), 4 * C, 1, x2, C,
+               EPI_RESID);
+        d.bias = pc_tensor(g, P_FCPROJB, l);
+        d.resid = x1;
+        d.ldr = C;
+        RUN(mm(g, K_MM_FWD, d));
+        resid = x2;
+    }
+    LAUNCH(K_LN_FWD, 1, 0, ln_bytes,
+           layernorm_forward(g->act, g->lnf, g->lnf_mean, g->lnf_rstd, resid,
+                             pc_tensor(g, P_LNFW, 0), pc_tensor(g, P_LNFB, 0), BT, C, g->stream));
+    GemmDesc d = gd(BT, Vp, C, g->lnf, C, 1, pc_tensor(g, P_WTE, 0), C, 1, g->logits, Vp,
+                    EPI_STORE);
+    RUN(mm(g, K_MM_CLS_FWD, d));
+    g->have_targets = with_targets ? 1 : 0;
+    g->logits_valid = with_targets ? 0 : 1;
+    g->have_fwd = 1;
+    if (with_targets) {
+        LAUNCH(K_XENT, 1, 0, as * 2.0 * bt * Vp,
+               crossentropy_fused(g->act, g->logits, g->losses, g->tgt, BT, g->V, Vp,
+                                  1.0f / (float)BT, g->err, g->stream));
+        LAUNCH(K_XENT, 1, 0, 4.0 * bt, mean_reduce(g->loss, g->losses, BT, g->stream));
+        if (h_loss) {
+            RUN(check_dev_err(g));
+            CK(cudaMemcpy(h_loss, g->loss, 4, cudaMemcpyDeviceToHost));
+        }
+    } else if (h_loss) {
+        *h_loss = NAN;
+        RUN(check_dev_err(g));
+    }
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_forward(gpt2_t* g, const int32_t* d_tokens, const int32_t* d_targets,
+                            float* h_loss) {
+    if (!g || !d_tokens) return fail(g, GPT2_ERR_ARG, "null handle or tokens");
+    cudaSetDevice(g->device);
+    CK(cudaMemcpyAsync(g->tok, d_tokens, g->BT * 4, cudaMemcpyDeviceToDevice, g->stream));
+    if (d_targets)
+        CK(cudaMemcpyAsync(g->tgt, d_targets, g->BT * 4, cudaMemcpyDeviceToDevice, g->stream));
+    return forward_impl(g, d_targets != nullptr, h_loss);
+}
+
+extern "C" int gpt2_forward_host(gpt2_t* g, const int32_t* h_tokens, const int32_t* h_targets,
+                                 float* h_loss) {
+    if (!g || !h_tokens) return fail(g, GPT2_ERR_ARG, "null handle or tokens");
+    cudaSetDevice(g->device);
+    CK(cudaMemcpyAsync(g->tok, h_tokens, g->BT * 4, cudaMemcpyHostToDevice, g->stream));
+    if (h_targets)
+        CK(cudaMemcpyAsync(g->tgt, h_targets, g->BT * 4, cudaMemcpyHostToDevice, g->stream));
+    return forward_impl(g, h_targets != nullptr, h_loss);
+}
+
+// ---------------------------------------------------------------------------
+// backward (reverse graph order)
+// ---------------------------------------------------------------------------
+extern "C" int gpt2_backward(gpt2_t* g) {
+    if (!g) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    if (!g->have_fwd || !g->have_targets)
+        return fail(g, GPT2_ERR_STATE, "backward needs a preceding forward with targets");
+    int B = g->B, T = g->T, C = g->C, L = g->L, H = g->H, Vp = g->Vp;
+    int BT = (int)g->BT;
+    size_t as = act_size(g->act);
+    size_t c = C, bt = g->BT;
+    void* dres = g->dres;
+    // classifier: dlogits sit in the logits buffer
+    GemmDesc d = gd(BT, C, Vp, g->logits, Vp, 1, pc_tensor(g, P_WTE, 0), C, 0, g->dln, C,
+                    EPI_STORE);
+    RUN(mm(g, K_MM_DX, d));
+    d = gd(Vp, C, BT, g->logits, Vp, 0, g->lnf, C, 0, grad_tensor(g, P_WTE, 0), C,
+           EPI_ACCUM_F32);
+    RUN(mm(g, K_MM_DW, d));
+    CK(cudaMemsetAsync(dres, 0, bt * c * as, g->stream));
+    const void* xL = L > 0 ? act_at(g, g->x2, bt * c, L - 1) : g->encoded;
+    double lnb_bytes = as * 4.0 * bt * c + 8.0 * bt;
+    LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
+           layernorm_backward(g->act, dres, grad_tensor(g, P_LNFW, 0), grad_tensor(g, P_LNFB, 0),
+                              g->dln, xL, pc_tensor(g, P_LNFW, 0), g->lnf_mean, g->lnf_rstd, BT,
+                              C, g->scratch, g->stream));
+    for (int l = L - 1; l >= 0; l--) {
+        const void* rin = l == 0 ? g->encoded : act_at(g, g->x2, bt * c, l - 1);
+        void* ln1 = act_at(g, g->ln1, bt * c, l);
+        void* qkv = act_at(g, g->qkv, bt * 3 * c, l);
+        void* atty = act_at(g, g->atty, bt * c, l);
+        void* x1 = act_at(g, g->x1, bt * c, l);
+        void* ln2 = act_at(g, g->ln2, bt * c, l);
+        void* fch = act_at(g, g->fch, bt * 4 * c, l);
+        void* fchg = act_at(g, g->fchg, bt * 4 * c, l);
+        float* lse = g->lse + (size_t)l * B * H * T;
+        // MLP: x2 = x1 + fcproj(gelu(fc(ln2(x1))))
+        d = gd(C, 4 * C, BT, dres, C, 0, fchg, 4 * C, 0, grad_tensor(g, P_FCPROJW, l), 4 * C,
+               EPI_ACCUM_F32);
+        RUN(mm(g, K_MM_DW, d));
+        LAUNCH(K_BIAS, 2, 0, as * bt * c,
+               bias_grad(g->act, grad_tensor(g, P_FCPROJB, l), dres, BT, C, g->scratch,
+                         g->stream));
+        d = gd(BT, 4 * C, C, dres, C, 1, pc_tensor(g, P_FCPROJW, l), 4 * C, 0, g->dbig, 4 * C,
+               EPI_GELU_BWD);
+        d.aux = fch;
+        d.ldx = 4 * C;
+        RUN(mm(g, K_MM_DX, d));
+        d = gd(4 * C, C, BT, g->dbig, 4 * C, 0, ln2, C, 0, grad_tensor(g, P_FCW, l), C,
+               EPI_ACCUM_F32);
+        RUN(mm(g, K_MM_DW, d));
+        LAUNCH(K_BIAS, 2, 0, as * bt * 4 * c,
+               bias_grad(g->act, grad_tensor(g, P_FCB, l), g->dbig, BT, 4 * C, g->scratch,
+                         g->stream));
+        d = gd(BT, C, 4 * C, g->dbig, 4 * C, 1, pc_tensor(g, P_FCW, l), C, 0, g->dln, C,
+               EPI_STORE);
+        RUN(mm(g, K_MM_DX, d));
+        LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
+               layernorm_backward(g->act, dres, grad_tensor(g, P_LN2W, l),
+                                  grad_tensor(g, P_LN2B, l), g->dln, x1, pc_tensor(g, P_LN2W, l),
+                                  g->ln2_mean + l * bt, g->ln2_rstd + l * bt, BT, C, g->scratch,
+                                  g->stream));
+        // attention: x1 = rin + proj(attn(qkv(ln1(rin))))
+        d = gd(C, C, BT, dres, C, 0, atty, C, 0, grad_tensor(g, P_PROJW, l), C, EPI_ACCUM_F32);
+        RUN(mm(g, K_MM_DW, d));
+        LAUNCH(K_BIAS, 2, 0, as * bt * c,
+               bias_grad(g->act, grad_tensor(g, P_PROJB, l), dres, BT, C, g->scratch,
+                         g->stream));
+        d = gd(BT, C, C, dres, C, 1, pc_tensor(g, P_PROJW, l), C, 0, g->datty, C, EPI_STORE);
+        RUN(mm(g, K_MM_DX, d));
+        double afl = 2.5 * 2.0 * 2.0 * B * H * ((double)T * (T + 1) / 2) * (C / H);
+        LAUNCH(K_ATTN_BWD, 3, afl, as * 8.0 * bt * c,
+               attention_backward(g->act, g->dqkv, g->datty, qkv, atty, lse, B, T, C, H,
+                                  g->scratch, g->stream));
+        d = gd(3 * C, C, BT, g->dqkv, 3 * C, 0, ln1, C, 0, grad_tensor(g, P_QKVW, l), C,
+               EPI_ACCUM_F32);
+        RUN(mm(g, K_MM_DW, d));
+        LAUNCH(K_BIAS, 2, 0, as * bt * 3 * c,
+               bias_grad(g->act, grad_tensor(g, P_QKVB, l), g->dqkv, BT, 3 * C, g->scratch,
+                         g->stream));
+        d = gd(BT, C, 3 * C, g->dqkv, 3 * C, 1, pc_tensor(g, P_QKVW, l), C, 0, g->dln, C,
+               EPI_STORE);
+        RUN(mm(g, K_MM_DX, d));
+        LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
+               layernorm_backward(g->act, dres, grad_tensor(g, P_LN1W, l),
+                                  grad_tensor(g, P_LN1B, l), g->dln, rin, pc_tensor(g, P_LN1W, l),
+                                  g->ln1_mean + l * bt, g->ln1_rstd + l * bt, BT, C, g->scratch,
+                                  g->stream));
+    }
+    LAUNCH(K_EMB_BWD, 9, 0, as * bt * c + 8.0 * T * c,
+           encoder_backward(g->act, grad_tensor(g, P_WTE, 0), grad_tensor(g, P_WPE, 0), dres,
+                            g->tok, B, T, C, Vp, g->scratch, g->stream));
+    g->n_accum++;
+    g->have_fwd = 0;
+    return GPT2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// optimizer
+// ---------------------------------------------------------------------------
+extern "C" int gpt2_zero_grad(gpt2_t* g) {
+    if (!g) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    prof_begin(g, K_ZERO, 0, 4.0 * g->nparams);
+    cudaError_t e = cudaMemsetAsync(g->grads, 0, g->nparams * 4, g->stream);
+    prof_end(g);
+    if (e) return fail(g, GPT2_ERR_CUDA, "zero_grad: %s", cudaGetErrorString(e));
+    g->n_accum = 0;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float eps, float wd,
+                               float clip, float* h_grad_norm) {
+    if (!g) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    if (g->n_accum < 1) return fail(g, GPT2_ERR_STATE, "adamw_step without accumulated grads");
+    int t = g->t + 1;
+    AdamArgs a;
+    a.lr = lr; a.b1 = b1; a.b2 = b2; a.eps = eps; a.wd = wd;
+    a.bc1 = (float)(1.0 - pow((double)b1, t));
+    a.bc2 = (float)(1.0 - pow((double)b2, t));
+    a.inv_accum = 1.0f / (float)g->n_accum;
+    a.clip = clip;
+    const size_t* o = g->lay.off;
+    a.dec_lo[0] = o[P_WTE];     a.dec_hi[0] = o[P_LN1W];
+    a.dec_lo[1] = o[P_QKVW];    a.dec_hi[1] = o[P_QKVB];
+    a.dec_lo[2] = o[P_PROJW];   a.dec_hi[2] = o[P_PROJB];
+    a.dec_lo[3] = o[P_FCW];     a.dec_hi[3] = o[P_FCB];
+    a.dec_lo[4] = o[P_FCPROJW]; a.dec_hi[4] = o[P_FCPROJB];
+    LAUNCH(K_ADAM, 3, 0, 34.0 * g->nparams + (g->act == ACT_BF16 ? 2.0 * g->nparams : 0.0),
+           adamw_step(g->master, g->m, g->v, g->grads, g->act == ACT_BF16 ? g->pc : nullptr,
+                      g->nparams, a, g->adam_state, g->scratch, g->stream));
+    float st[3];
+    CK(cudaMemcpyAsync(st, g->adam_state, 12, cudaMemcpyDeviceToHost, g->stream));
+    RUN(check_dev_err(g));
+    if (h_grad_norm) *h_grad_norm = st[0];
+    if (st[2] == 0.f) return fail(g, GPT2_ERR_NONFINITE, "gradient norm is not finite (%g)", st[0]);
+    g->t = t;
+    return GPT2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// inspection
+// ---------------------------------------------------------------------------
+extern "C" size_t gpt2_num_params(gpt2_t* g) { return g ? g->nparams : 0; }
+extern "C" int gpt2_padded_vocab(gpt2_t* g) { return g ? g->Vp : 0; }
+
+extern "C" int gpt2_get_params(gpt2_t* g, float* h) {
+    if (!g || !h) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    CK(cudaMemcpyAsync(h, g->master, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    return GPT2_OK;
+}
+extern "C" int gpt2_set_params(gpt2_t* g, const float* h) {
+    if (!g || !h) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    CK(cudaMemcpyAsync(g->master, h, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
+    if (g->act == ACT_BF16) CK(cast_to_bf16(g->pc, g->master, g->nparams, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    return GPT2_OK;
+}
+extern "C" int gpt2_get_grads(gpt2_t* g, float* h) {
+    if (!g || !h) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    CK(cudaMemcpyAsync(h, g->grads, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    return GPT2_OK;
+}
+extern "C" int gpt2_set_grads(gpt2_t* g, const float* h) {
+    if (!g || !h) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    CK(cudaMemcpyAsync(g->grads, h, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    if (g->n_accum < 1) g->n_accum = 1;
+    return GPT2_OK;
+}
+extern "C" int gpt2_get_opt_state(gpt2_t* g, float* hm, float* hv, int* step) {
+    if (!g) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    if (hm) CK(cudaMemcpyAsync(hm, g->m, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
+    if (hv) CK(cudaMemcpyAsync(hv, g->v, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    if (step) *step = g->t;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_set_opt_state(gpt2_t* g, const float* hm, const float* hv, int step) {
+    if (!g || step < 0) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    if (hm) CK(cudaMemcpyAsync(g->m, hm, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
+    if (hv) CK(cudaMemcpyAsync(g->v, hv, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    g->t = step;
+    return GPT2_OK;
+}
+
+static float bf16_bits_to_float(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+extern "C" int gpt2_get_logits(gpt2_t* g, float* h) {
+    if (!g || !h) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    if (!g->logits_valid)
+        return fail(g, GPT2_ERR_STATE, "logits are kept only after a forward without targets");
+    size_t as = act_size(g->act);
+    std::vector<char> tmp(g->BT * g->V * as);
+    CK(cudaMemcpy2DAsync(tmp.data(), g->V * as, g->logits, (size_t)g->Vp * as, g->V * as, g->BT,
+                         cudaMemcpyDeviceToHost, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    size_t n = g->BT * g->V;
+    if (g->act == ACT_BF16) {
+        const uint16_t* s = (const uint16_t*)tmp.data();
+        for (size_t i = 0; i < n; i++) h[i] = bf16_bits_to_float(s[i]);
+    } else {
+        memcpy(h, tmp.data(), n * 4);
+    }
+    return GPT2_OK;
+}
+extern "C" int gpt2_get_loss(gpt2_t* g, float* h) {
+    if (!g || !h) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    RUN(check_dev_err(g));
+    CK(cudaMemcpy(h, g->loss, 4, cudaMemcpyDeviceToHost));
+    return GPT2_OK;
+}
+extern "C" int gpt2_get_losses(gpt2_t* g, float* h) {
+    if (!g || !h) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    CK(cudaMemcpyAsync(h, g->losses, g->BT * 4, cudaMemcpyDeviceToHost, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    return GPT2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// profiling
+// ---------------------------------------------------------------------------
+extern "C" int gpt2_prof_enable(gpt2_t* g, unsigned class_mask) {
+    if (!g) return GPT2_ERR_ARG;
+    if (!class_mask) prof_collect(g);
+    g->prof_on = class_mask != 0;
+    g->prof_mask = class_mask;
+    return GPT2_OK;
+}
+extern "C" long long gpt2_launch_count(gpt2_t* g) { return g ? g->launches : -1; }
+extern "C" int gpt2_prof_reset(gpt2_t* g) {
+    if (!g) return GPT2_ERR_ARG;
+    prof_collect(g);
+    for (int i = 0; i < K_NCLASS; i++) {
+        g->prof_ms[i] = g->prof_flops[i] = g->prof_bytes[i] = 0;
+        g->prof_n[i] = 0;
+    }
+    return GPT2_OK;
+}
+extern "C" int gpt2_prof_num_classes(void) { return K_NCLASS; }
+extern "C" const char* gpt2_prof_name(int c) {
+    return (c >= 0 && c < K_NCLASS) ? kClassNames[c] : "";
+}
+extern "C" int gpt2_prof_read(gpt2_t* g, int c, double* ms, long long* n, double* fl,
+                              double* by) {
+    if (!g || c < 0 || c >= K_NCLASS) return GPT2_ERR_ARG;
+    prof_collect(g);
+    if (ms) *ms = g->prof_ms[c];
+    if (n) *n = g->prof_n[c];
+    if (fl) *fl = g->prof_flops[c];
+    if (by) *by = g->prof_bytes[c];
+    return GPT2_OK;
+}

@@ -1,0 +1,970 @@
+// k_misc.cu -- the memory-bound kernels of the GPT-2 step: parameter init,
+// embedding forward/backward, LayerNorm forward/backward, bias gradients,
+// fused softmax cross-entropy, and the AdamW update with global-norm clipping.
+//
+// Sources (page title, section):
+//  * "Karpathy's llm.c: understanding LLM training from scratch in C/CUDA",
+//    "Code anatomy": encoder_forward / encoder_backward, layernorm_forward,
+//    warp_reduce_max / warp_reduce_sum shuffle reductions, the single-kernel
+//    update_params, explicit bf16 compute copies of fp32 master weights.
+//  * "Karpathy reproduces GPT-2 (1.6B) in llm.c", "Training" and the flag
+//    guide: AdamW with weight decay on 2-D weights only, gradient-norm clip,
+//    gradient accumulation; "PyTorch comparison": the fused classifier that
+//    never materialises the probabilities, vocabulary padded to 50304.
+// Every reduction below runs in a fixed order (no float atomics), so a rerun
+// on the same inputs gives the same bits.
+#include "common.cuh"
+#include "kernels.h"
+
+#include <math.h>
+
+namespace gk {
+
+static inline int cdiv(long a, long b) { return (int)((a + b - 1) / b); }
+
+void make_layout(ParamLayout* lay, int L, int C, int V, int T) {
+    size_t c = (size_t)C, l = (size_t)L;
+    int Vp = ((V + 127) / 128) * 128;
+    size_t sz[P_NUM] = {(size_t)Vp * c, (size_t)T * c, l * c, l * c, l * 3 * c * c, l * 3 * c,
+                        l * c * c, l * c, l * c, l * c, l * 4 * c * c, l * 4 * c,
+                        l * 4 * c * c, l * c, c, c};
+    size_t o = 0;
+    for (int k = 0; k < P_NUM; k++) {
+        lay->off[k] = o;
+        o += sz[k];
+    }
+    lay->off[P_NUM] = o;
+    lay->L = L; lay->C = C; lay->V = V; lay->Vp = Vp; lay->T = T;
+}
+
+// ===========================================================================
+// Parameter init: SplitMix64 (Steele, Lea & Flood 2014) counter stream and the
+// Box-Muller transform (Box & Muller 1958) in double, rounded to fp32.
+// ===========================================================================
+__device__ __forceinline__ uint64_t sm64_at(uint64_t seed, uint64_t j) {
+    // state after j+1 increments of the Weyl sequence, then the output mix
+    uint64_t z = seed + (j + 1ull) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+__device__ __forceinline__ double unit_open(uint64_t x) {
+    return ((double)(x >> 11) + 0.5) * 0x1.0p-53;
+}
+
+__global__ void k_init_params(float* p, ParamLayout lay, uint64_t seed, double sd, double sd_res) {
+    size_t n = lay.off[P_NUM];
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        int k = 0;
+        while (k + 1 < P_NUM && lay.off[k + 1] <= i) k++;
+        double std = 0.0;
+        float fixed = 0.0f;
+        switch (k) {
+            case P_WTE:
+                if ((i - lay.off[P_WTE]) / (size_t)lay.C < (size_t)lay.V) std = sd;
+                break;
+            case P_WPE: case P_QKVW: case P_FCW: std = sd; break;
+            case P_PROJW: case P_FCPROJW: std = sd_res; break;
+            case P_LN1W: case P_LN2W: case P_LNFW: fixed = 1.0f; break;
+            default: break;
+        }
+        if (std > 0.0) {
+            double u1 = unit_open(sm64_at(seed, 2 * (uint64_t)i));
+            double u2 = unit_open(sm64_at(seed, 2 * (uint64_t)i + 1));
+            double z = sqrt(-2.0 * log(u1)) * cos(6.283185307179586476925 * u2);
+            p[i] = (float)(z * std);
+        } else {
+            p[i] = fixed;
+        }
+    }
+}
+
+cudaError_t init_params(float* master, const ParamLayout& lay, uint64_t seed, cudaStream_t s) {
+    k_init_params<<<148 * 8, 256, 0, s>>>(master, lay, seed, 0.02, 0.02 / sqrt(2.0 * lay.L));
+    return cudaGetLastError();
+}
+
+__global__ void k_cast_bf16(bf16* dst, const float* src, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = __float2bfloat16_rn(src[i]);
+}
+cudaError_t cast_to_bf16(void* dst, const float* src, size_t n, cudaStream_t s) {
+    k_cast_bf16<<<148 * 8, 256, 0, s>>>((bf16*)dst, src, n);
+    return cudaGetLastError();
+}
+
+// ===========================================================================
+// Embedding forward: one thread per VEC-wide chunk of a row.
+// ===========================================================================
+template <typename T, int VEC>
+__global__ void k_encoder_fwd(T* out, const int* tok, const T* wte, const T* wpe, int BT, int T_,
+                              int C, int V, unsigned* err) {
+    int cv = C / VEC;
+    long total = (long)BT * cv;
+    for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long)gridDim.x * blockDim.x) {
+        int row = (int)(idx / cv), c = (int)(idx % cv) * VEC;
+        int id = tok[row];
+        if (id < 0 || id >= V) {
+            if (c == 0) atomicOr(err, GPT2_DEVERR_TOKEN);
+            id = 0;
+        }
+        int t = row % T_;
+        float a[VEC], b[VEC];
+        load_vec_f<T, VEC>(a, wte + (size_t)id * C + c);
+        load_vec_f<T, VEC>(b, wpe + (size_t)t * C + c);
+#pragma unroll
+        for (int j = 0; j < VEC; j++) a[j] += b[j];
+        store_vec_f<T, VEC>(out + (size_t)row * C + c, a);
+    }
+}
+
+template <typename T>
+static cudaError_t enc_fwd_t(void* out, const int* tok, const void* wte, const void* wpe, int B,
+                             int T_, int C, int V, unsigned* err, cudaStream_t s) {
+    int BT = B * T_;
+    constexpr int VM = 16 / sizeof(T);
+    if (C % VM == 0) {
+        long total = (long)BT * (C / VM);
+        k_encoder_fwd<T, VM><<<cdiv(total, 256) < 148 * 16 ? cdiv(total, 256) : 148 * 16, 256, 0,
+                              s>>>((T*)out, tok, (const T*)wte, (const T*)wpe, BT, T_, C, V, err);
+    } else {
+        long total = (long)BT * C;
+        k_encoder_fwd<T, 1><<<cdiv(total, 256) < 148 * 16 ? cdiv(total, 256) : 148 * 16, 256, 0,
+                             s>>>((T*)out, tok, (const T*)wte, (const T*)wpe, BT, T_, C, V, err);
+    }
+    return cudaGetLastError();
+}
+cudaError_t encoder_forward(int act, void* out, const int* tok, const void* wte, const void* wpe,
+                            int B, int T_, int C, int V, unsigned* err, cudaStream_t s) {
+    if (act == ACT_BF16) return enc_fwd_t<bf16>(out, tok, wte, wpe, B, T_, C, V, err, s);
+    return enc_fwd_t<float>(out, tok, wte, wpe, B, T_, C, V, err, s);
+}
+
+// ===========================================================================
+// LayerNorm forward: one warp per row, row cached in registers, VEC-wide loads.
+// mean, rstd = 1/sqrt(var + 1e-5) with the biased variance.
+// ===========================================================================
+template <typename T, int VEC, int IT>
+__global__ void __launch_bounds__(256) k_ln_fwd(T* out, float* mean, float* rstd, const T* x,
+                                                const T* w, const T* b, int N, int C) {
+    int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const T* xr = x + (size_t)row * C;
+    float v[IT][VEC];
+    float s = 0.f;
+#pragma unroll
+    for (int it = 0; it < IT; it++) {
+        int c = (it * 32 + lane) * VEC;
+        if (c < C) {
+            load_vec_f<T, VEC>(v[it], xr + c);
+#pragma unroll
+            for (int j = 0; j < VEC; j++) s += v[it][j];
+        }
+    }
+    float m = warp_sum(s) / C;
+    float ss = 0.f;
+#pragma unroll
+    for (int it = 0; it < IT; it++) {
+        int c = (it * 32 + lane) * VEC;
+        if (c < C) {
+#pragma unroll
+            for (int j = 0; j < VEC; j++) {
+                float d = v[it][j] - m;
+                ss += d * d;
+            }
+        }
+    }
+    float r = rsqrtf(warp_sum(ss) / C + 1e-5f);
+    T* yr = out + (size_t)row * C;
+#pragma unroll
+    for (int it = 0; it < IT; it++) {
+        int c = (it * 32 + lane) * VEC;
+        if (c < C) {
+            float wv[VEC], bv[VEC], y[VEC];
+            load_vec_f<T, VEC>(wv, w + c);
+            load_vec_f<T, VEC>(bv, b + c);
+#pragma unroll
+            for (int j = 0; j < VEC; j++) y[j] = (v[it][j] - m) * r * wv[j] + bv[j];
+            store_vec_f<T, VEC>(yr + c, y);
+        }
+    }
+    if (lane == 0) {
+        mean[row] = m;
+        rstd[row] = r;
+    }
+}
+
+template <typename T, int VEC>
+static cudaError_t ln_fwd_vec(void* out, float* mean, float* rstd, const void* x, const void* w,
+                              const void* b, int N, int C, cudaStream_t s) {
+    int it = cdiv(C, 32 * VEC);
+    dim3 grid(cdiv(N, 8)), blk(256);
+#define LNF(I)                                                                                   \
+    k_ln_fwd<T, VEC, I><<<grid, blk, 0, s>>>((T*)out, mean, rstd, (const T*)x, (const T*)w,     \
+                                            (const T*)b, N, C)
+    if (it <= 1) LNF(1);
+    else if (it <= 2) LNF(2);
+    else if (it <= 4) LNF(4);
+    else if (it <= 8) LNF(8);
+    else if (it <= 16) LNF(16);
+    else return cudaErrorInvalidValue;
+#undef LNF
+    return cudaGetLastError();
+}
+template <typename T>
+static cudaError_t ln_fwd_t(void* out, float* mean, float* rstd, const void* x, const void* w,
+                            const void* b, int N, int C, cudaStream_t s) {
+    constexpr int VM = 16 / sizeof(T);
+    if (C % VM == 0) return ln_fwd_vec<T, VM>(out, mean, rstd, x, w, b, N, C, s);
+    return ln_fwd_vec<T, 1>(out, mean, rstd, x, w, b, N, C, s);
+}
+cudaError_t layernorm_forward(int act, void* out, float* mean, float* rstd, const void* x,
+                              const void* w, const void* b, int N, int C, cudaStream_t s) {
+    if (act == ACT_BF16) return ln_fwd_t<bf16>(out, mean, rstd, x, w, b, N, C, s);
+    return ln_fwd_t<float>(out, mean, rstd, x, w, b, N, C, s);
+}
+
+// ===========================================================================
+// LayerNorm backward.  Per row (xhat = (x-mean)*rstd, g = dy*w):
+//   dx += rstd * (g - mean(g) - xhat * mean(g*xhat))
+// dw, db column sums: each warp accumulates its rows into its own shared
+// memory slice, the block folds its 8 slices in order into one partial row,
+// and a second kernel sums the block partials in order.
+// ===========================================================================
+#define LNB_WARPS 8
+#define LNB_MAX_BLOCKS 296
+
+template <typename T, int VEC, int IT>
+__global__ void __launch_bounds__(256) k_ln_bwd(T* dx, float* part, const T* dout, const T* x,
+                                                const T* w, const float* mean,
+                                                const float* rstd, int N, int C) {
+    extern __shared__ float sm[];  // [LNB_WARPS][2C]
+    int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    float* acc = sm + (size_t)warp * 2 * C;
+    for (int i = threadIdx.x; i < LNB_WARPS * 2 * C; i += blockDim.x) sm[i] = 0.f;
+    __syncthreads();
+    for (int row = blockIdx.x * LNB_WARPS + warp; row < N; row += gridDim.x * LNB_WARPS) {
+        const T* xr = x + (size_t)row * C;
+        const T* dyr = dout + (size_t)row * C;
+        float m = mean[row], r = rstd[row];
+        float xh[IT][VEC], g[IT][VEC];
+        float sg = 0.f, sgx = 0.f;
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            int c = (it * 32 + lane) * VEC;
+            if (c < C) {
+                float xv[VEC], dy[VEC], wv[VEC];
+                load_vec_f<T, VEC>(xv, xr + c);
+                load_vec_f<T, VEC>(dy, dyr + c);
+                load_vec_f<T, VEC>(wv, w + c);
+#pragma unroll
+                for (int j = 0; j < VEC; j++) {
+                    xh[it][j] = (xv[j] - m) * r;
+                    g[it][j] = dy[j] * wv[j];
+                    sg += g[it][j];
+                    sgx += g[it][j] * xh[it][j];
+                    acc[c + j] += dy[j] * xh[it][j];
+                    acc[C + c + j] += dy[j];
+                }
+            }
+        }
+        sg = warp_sum(sg) / C;
+        sgx = warp_sum(sgx) / C;
+        T* dxr = dx + (size_t)row * C;
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            int c = (it * 32 + lane) * VEC;
+            if (c < C) {
+                float d[VEC];
+                load_vec_f<T, VEC>(d, dxr + c);
+#pragma unroll
+                for (int j = 0; j < VEC; j++) d[j] += r * (g[it][j] - sg - xh[it][j] * sgx);
+                store_vec_f<T, VEC>(dxr + c, d);
+            }
+        }
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+        float a = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < LNB_WARPS; wi++) a += sm[(size_t)wi * 2 * C + c];
+        part[(size_t)blockIdx.x * 2 * C + c] = a;
+    }
+}
+
+__global__ void k_colsum_partials(float* dw, float* db, const float* part, int nb, int C) {
+    int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float a = 0.f, b = 0.f;
+    for (int i = 0; i < nb; i++) {
+        a += part[(size_t)i * 2 * C + c];
+        b += part[(size_t)i * 2 * C + C + c];
+    }
+    dw[c] += a;
+    db[c] += b;
+}
+
+size_t layernorm_backward_scratch(int N, int C) {
+    return (size_t)LNB_MAX_BLOCKS * 2 * C * sizeof(float);
+}
+
+template <typename T, int VEC>
+static cudaError_t ln_bwd_vec(void* dx, float* dw, float* db, const void* dout, const void* x,
+                              const void* w, const float* mean, const float* rstd, int N, int C,
+                              void* scratch, cudaStream_t s) {
+    int it = cdiv(C, 32 * VEC);
+    int nb = cdiv(N, LNB_WARPS);
+    if (nb > LNB_MAX_BLOCKS) nb = LNB_MAX_BLOCKS;
+    size_t smem = (size_t)LNB_WARPS * 2 * C * sizeof(float);
+    float* part = (float*)scratch;
+#define LNB(I)                                                                                   \
+    do {                                                                                         \
+        auto kf = k_ln_bwd<T, VEC, I>;                                                           \
+        cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);        \
+        kf<<<nb, 256, smem, s>>>((T*)dx, part, (const T*)dout, (const T*)x, (const T*)w, mean,  \
+                                 rstd, N, C);                                                    \
+    } while (0)
+    if (it <= 1) LNB(1);
+    else if (it <= 2) LNB(2);
+    else if (it <= 4) LNB(4);
+    else if (it <= 8) LNB(8);
+    else if (it <= 16) LNB(16);
+    else return cudaErrorInvalidValue;
+#undef LNB
+    k_colsum_partials<<<cdiv(C, 256), 256, 0, s>>>(dw, db, part, nb, C);
+    return cudaGetLastError();
+}
+template <typename T>
+static cudaError_t ln_bwd_t(void* dx, float* dw, float* db, const void* dout, const void* x,
+                            const void* w, const float* mean, const float* rstd, int N, int C,
+                            void* scratch, cudaStream_t s) {
+    constexpr int VM = 16 / sizeof(T);
+    if (C % VM == 0) return ln_bwd_vec<T, VM>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
+    return ln_bwd_vec<T, 1>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
+}
+cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, const void* dout,
+                               const void* x, const void* w, const float* mean,
+                               const float* rstd, int N, int C, void* scratch, cudaStream_t s) {
+    if ((size_t)C * 2 * LNB_WARPS * sizeof(float) > 200 * 1024) return cudaErrorInvalidValue;
+    if (act == ACT_BF16)
+        return ln_bwd_t<bf16>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
+    return ln_bwd_t<float>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
+}
+
+// ===========================================================================
+// Bias gradient: db[o] += sum_n dout[n,o].  Stage 1: each block sums a chunk
+// of BG_ROWS rows for VEC-wide column groups; stage 2 sums chunks in order.
+// ===========================================================================
+#define BG_ROWS 32
+
+template <typename T, int VEC>
+__global__ void k_bias_part(float* part, const T* dout, int N, int OC) {
+    int cg = blockIdx.x * blockDim.x + threadIdx.x;
+    int c = cg * VEC;
+    if (c >= OC) return;
+    int r0 = blockIdx.y * BG_ROWS, r1 = min(N, r0 + BG_ROWS);
+    float a[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; j++) a[j] = 0.f;
+    for (int r = r0; r < r1; r++) {
+        float v[VEC];
+        load_vec_f<T, VEC>(v, dout + (size_t)r * OC + c);
+#pragma unroll
+        for (int j = 0; j < VEC; j++) a[j] += v[j];
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; j++) part[(size_t)blockIdx.y * OC + c + j] = a[j];
+}
+__global__ void k_bias_final(float* db, const float* part, int nch, int OC) {
+    int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= OC) return;
+    float a = 0.f;
+    for (int i = 0; i < nch; i++) a += part[(size_t)i * OC + c];
+    db[c] += a;
+}
+size_t bias_grad_scratch(int N, int OC) { return (size_t)cdiv(N, BG_ROWS) * OC * sizeof(float); }
+
+template <typename T>
+static cudaError_t bias_grad_t(float* db, const void* dout, int N, int OC, void* scratch,
+                               cudaStream_t s) {
+    constexpr int VM = 16 / sizeof(T);
+    int nch = cdiv(N, BG_ROWS);
+    float* part = (float*)scratch;
+    if (OC % VM == 0) {
+        dim3 grid(cdiv(OC / VM, 128), nch);
+        k_bias_part<T, VM><<<grid, 128, 0, s>>>(part, (const T*)dout, N, OC);
+    } else {
+        dim3 grid(cdiv(OC, 128), nch);
+        k_bias_part<T, 1><<<grid, 128, 0, s>>>(part, (const T*)dout, N, OC);
+    }
+    k_bias_final<<<cdiv(OC, 256), 256, 0, s>>>(db, part, nch, OC);
+    return cudaGetLastError();
+}
+cudaError_t bias_grad(int act, float* db, const void* dout, int N, int OC, void* scratch,
+                      cudaStream_t s) {
+    if (act == ACT_BF16) return bias_grad_t<bf16>(db, dout, N, OC, scratch, s);
+    return bias_grad_t<float>(db, dout, N, OC, scratch, s);
+}
+
+// ===========================================================================
+// Fused classifier loss.  One block per row: an online (max, sum-exp) pass over
+// the V real columns, lse = max + log(sum); loss = lse - z[target]; then, when
+// dloss != 0, the row is overwritten in place by (softmax - onehot) * dloss
+// with the padded columns set to 0.  The probabilities are never stored.
+// ===========================================================================
+__device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
+    float M = fmaxf(m, m2);
+    float a = (m == -INFINITY) ? 0.f : s * __expf(m - M);
+    float b = (m2 == -INFINITY) ? 0.f : s2 * __expf(m2 - M);
+    m = M;
+    s = a + b;
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(512) k_xent(T* logits, float* losses, const int* tgt, int V,
+                                              int Vp, float dloss, unsigned* err) {
+    __shared__ float sm_m[32], sm_s[32];
+    __shared__ float sh_lse;
+    int row = blockIdx.x;
+    T* z = logits + (size_t)row * Vp;
+    int y = tgt[row];
+    if (y < 0 || y >= V) {
+        if (threadIdx.x == 0) atomicOr(err, GPT2_DEVERR_TOKEN);
+        y = 0;
+    }
+    float zy = to_f(z[y]);
+    float m = -INFINITY, s = 0.f;
+    for (int j = threadIdx.x * VEC; j < V; j += blockDim.x * VEC) {
+        float v[VEC];
+        load_vec_f<T, VEC>(v, z + j);
+#pragma unroll
+        for (int e = 0; e < VEC; e++) {
+            if (j + e < V) {
+                float x = v[e];
+                if (x > m) {
+                    s = s * __expf(m - x) + 1.f;
+                    m = x;
+                } else {
+                    s += __expf(x - m);
+                }
+            }
+        }
+    }
+    // warp then block combine of (m, s) pairs
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        ms_combine(m, s, m2, s2);
+    }
+    int warp = threadIdx.x / 32, lane = threadIdx.x & 31, nw = blockDim.x / 32;
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_s[warp] = s;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < nw ? sm_m[lane] : -INFINITY;
+        s = lane < nw ? sm_s[lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            ms_combine(m, s, m2, s2);
+        }
+        if (lane == 0) {
+            float lse = m + logf(s);
+            sh_lse = lse;
+            losses[row] = lse - zy;
+        }
+    }
+    __syncthreads();
+    if (dloss == 0.f) return;
+    float lse = sh_lse;
+    for (int j = threadIdx.x * VEC; j < Vp; j += blockDim.x * VEC) {
+        float v[VEC];
+        load_vec_f<T, VEC>(v, z + j);
+#pragma unroll
+        for (int e = 0; e < VEC; e++) {
+            int col = j + e;
+            float p = __expf(v[e] - lse);
+            v[e] = col < V ? (p - (col == y ? 1.f : 0.f)) * dloss : 0.f;
+        }
+        store_vec_f<T, VEC>(z + j, v);
+    }
+}
+
+cudaError_t crossentropy_fused(int act, void* logits, float* losses, const int* tgt, int N,
+                               int V, int Vp, float dloss, unsigned* err, cudaStream_t s) {
+    if (Vp % 8) return cudaErrorInvalidValue;
+    if (act == ACT_BF16)
+        k_xent<bf16, 8><<<N, 512, 0, s>>>((bf16*)logits, losses, tgt, V, Vp, dloss, err);
+    else
+        k_xent<float, 4><<<N, 512, 0, s>>>((float*)logits, losses, tgt, V, Vp, dloss, err);
+    return cudaGetLastError();
+}
+
+__global__ void k_mean(float* out, const float* x, int n) {
+    __shared__ double sh[32];
+    double a = 0.0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) a += (double)x[i];
+    a = warp_sum_d(a);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x / 32] = a;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        a = threadIdx.x < blockDim.x / 32 ? sh[threadIdx.x] : 0.0;
+        a = warp_sum_d(a);
+        if (threadIdx.x == 0) out[0] = (float)(a / n);
+    }
+}
+cudaError_t mean_reduce(float* out, const float* x, int n, cudaStream_t s) {
+    k_mean<<<1, 1024, 0, s>>>(out, x, n);
+    return cudaGetLastError();
+}
+
+// ===========================================================================
+// Embedding backward without float atomics.
+//  1. k_emb_rank: each 1024-position block sorts its (token, position) keys in
+//     shared memory (bitonic), giving each position its rank among equal
+//     tokens of the block and the block's count per token.
+//  2. k_emb_blockprefix: per token, exclusive prefix of the block counts.
+//  3. k_emb_scan: one block scans the per-token totals -> bucket starts, and
+//     the chunk counts (buckets split in chunks of EMB_R rows).
+//  4. k_emb_place: stable placement -> positions sorted by (token, position).
+//  5. k_emb_items: list the (token, chunk) work items.
+//  6. k_emb_reduce: one warp per item sums its <= EMB_R rows in position
+//     order; single-chunk tokens add into dwte directly, the others write a
+//     partial row; k_emb_fold adds those partials to dwte in chunk order.
+//  7. k_wpe_bwd: dwpe[t] += sum over b (in order).
+// ===========================================================================
+#define EMB_BLK 1024
+#define EMB_R 32
+
+struct EmbScratch {
+    int* blkcnt;   // [nb][Vp]
+    int* cnt;      // [Vp]
+    int* start;    // [Vp+1]
+    int* itemoff;  // [Vp+1]
+    int* poff;     // [Vp+1]
+    int* lrank;    // [BT]
+    int* sorted;   // [BT]
+    int2* items;   // [max_items]
+    float* part;   // [max_part][C]
+    int nb, max_items, max_part;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static EmbScratch emb_carve(void* base, int BT, int C, int Vp, size_t* total) {
+    EmbScratch e;
+    e.nb = cdiv(BT, EMB_BLK);
+    e.max_items = cdiv(BT, EMB_R) + (BT < Vp ? BT : Vp);
+    e.max_part = 2 * cdiv(BT, EMB_R) + 1;
+    char* p = (char*)base;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        char* r = p ? p + o : nullptr;
+        o += align256(bytes);
+        return r;
+    };
+    e.blkcnt = (int*)take((size_t)e.nb * Vp * 4);
+    e.cnt = (int*)take((size_t)Vp * 4);
+    e.start = (int*)take((size_t)(Vp + 1) * 4);
+    e.itemoff = (int*)take((size_t)(Vp + 1) * 4);
+    e.poff = (int*)take((size_t)(Vp + 1) * 4);
+    e.lrank = (int*)take((size_t)BT * 4);
+    e.sorted = (int*)take((size_t)BT * 4);
+    e.items = (int2*)take((size_t)e.max_items * 8);
+    e.part = (float*)take((size_t)e.max_part * C * 4);
+    if (total) *total = o;
+    return e;
+}
+
+size_t encoder_backward_scratch(int B, int T_, int C, int Vp) {
+    size_t t;
+    emb_carve(nullptr, B * T_, C, Vp, &t);
+    return t;
+}
+
+__global__ void __launch_bounds__(EMB_BLK) k_emb_rank(const int* tok, int BT, int Vp, int* lrank,
+                                                      int* blkcnt) {
+    __shared__ unsigned key[EMB_BLK];
+    __shared__ int rs[EMB_BLK];
+    int i = threadIdx.x, pos = blockIdx.x * EMB_BLK + i;
+    unsigned k = 0xffffffffu;
+    if (pos < BT) {
+        int t = tok[pos];
+        if (t < 0 || t >= Vp) t = 0;
+        k = ((unsigned)t << 11) | (unsigned)i;
+    }
+    key[i] = k;
+    __syncthreads();
+    // bitonic sort, ascending
+    for (int size = 2; size <= EMB_BLK; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            int j = i ^ stride;
+            if (j > i) {
+                unsigned a = key[i], b = key[j];
+                bool up = (i & size) == 0;
+                if ((a > b) == up) {
+                    key[i] = b;
+                    key[j] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    unsigned ki = key[i];
+    bool valid = ki != 0xffffffffu;
+    unsigned ti = ki >> 11;
+    bool head = valid && (i == 0 || (key[i - 1] >> 11) != ti);
+    rs[i] = head ? i : 0;
+    __syncthreads();
+    // inclusive max-scan: start index of each run
+    for (int off = 1; off < EMB_BLK; off <<= 1) {
+        int v = rs[i];
+        if (i >= off) v = max(v, rs[i - off]);
+        __syncthreads();
+        rs[i] = v;
+        __syncthreads();
+    }
+    if (valid) {
+        int st = rs[i];
+        int li = (int)(ki & 2047u);
+        lrank[blockIdx.x * EMB_BLK + li] = i - st;
+        bool tail = (i == EMB_BLK - 1) || (key[i + 1] >> 11) != ti;
+        if (tail) blkcnt[(size_t)blockIdx.x * Vp + ti] = i - st + 1;
+    }
+}
+
+__global__ void k_emb_blockprefix(int* blkcnt, int* cnt, int nb, int Vp) {
+    int v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= Vp) return;
+    int run = 0;
+    for (int b = 0; b < nb; b++) {
+        int c = blkcnt[(size_t)b * Vp + v];
+        blkcnt[(size_t)b * Vp + v] = run;
+        run += c;
+    }
+    cnt[v] = run;
+}
+
+// One block of 1024 threads: exclusive scans of n_v, chunks_v, multi-chunk
+// chunks_v over v in [0, Vp).
+__global__ void __launch_bounds__(1024) k_emb_scan(const int* cnt, int* start, int* itemoff,
+                                                   int* poff, int Vp) {
+    __shared__ int s0[1024], s1[1024], s2[1024];
+    int per = (Vp + 1023) / 1024;
+    int lo = threadIdx.x * per, hi = min(Vp, lo + per);
+    int a = 0, b = 0, c = 0;
+    for (int v = lo; v < hi; v++) {
+        int n = cnt[v], ch = (n + EMB_R - 1) / EMB_R;
+        a += n;
+        b += ch;
+        c += ch > 1 ? ch : 0;
+    }
+    s0[threadIdx.x] = a;
+    s1[threadIdx.x] = b;
+    s2[threadIdx.x] = c;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        int x0 = s0[threadIdx.x], x1 = s1[threadIdx.x], x2 = s2[threadIdx.x];
+        if (threadIdx.x >= off) {
+            x0 += s0[threadIdx.x - off];
+            x1 += s1[threadIdx.x - off];
+            x2 += s2[threadIdx.x - off];
+        }
+        __syncthreads();
+        s0[threadIdx.x] = x0;
+        s1[threadIdx.x] = x1;
+        s2[threadIdx.x] = x2;
+        __syncthreads();
+    }
+    a = threadIdx.x ? s0[threadIdx.x - 1] : 0;
+    b = threadIdx.x ? s1[threadIdx.x - 1] : 0;
+    c = threadIdx.x ? s2[threadIdx.x - 1] : 0;
+    for (int v = lo; v < hi; v++) {
+        int n = cnt[v], ch = (n + EMB_R - 1) / EMB_R;
+        start[v] = a;
+        itemoff[v] = b;
+        poff[v] = c;
+        a += n;
+        b += ch;
+        c += ch > 1 ? ch : 0;
+    }
+    if (threadIdx.x == 1023) {
+        start[Vp] = s0[1023];
+        itemoff[Vp] = s1[1023];
+        poff[Vp] = s2[1023];
+    }
+}
+
+__global__ void k_emb_place(const int* tok, int BT, int Vp, const int* start, const int* blkcnt,
+                            const int* lrank, int* sorted) {
+    int pos = blockIdx.x * blockDim.x + threadIdx.x;
+    if (pos >= BT) return;
+    int t = tok[pos];
+    if (t < 0 || t >= Vp) t = 0;
+    int b = pos / EMB_BLK;
+    sorted[start[t] + blkcnt[(size_t)b * Vp + t] + lrank[pos]] = pos;
+}
+
+__global__ void k_emb_items(const int* cnt, const int* itemoff, int2* items, int Vp) {
+    int v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= Vp) return;
+    int n = cnt[v];
+    int ch = (n + EMB_R - 1) / EMB_R, o = itemoff[v];
+    for (int c = 0; c < ch; c++) items[o + c] = make_int2(v, c);
+}
+
+template <typename T, int VEC, int IT>
+__global__ void k_emb_reduce2(float* dwte, float* part, const T* dx, const int* sorted,
+                              const int* cnt, const int* start, const int* n_items,
+                              const int* poff, const int2* items, int C) {
+    int item = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    int lane = threadIdx.x & 31;
+    if (item >= *n_items) return;
+    int2 vc = items[item];
+    int v = vc.x, c = vc.y;
+    int n = cnt[v];
+    int r0 = c * EMB_R, r1 = min(n, r0 + EMB_R);
+    float acc[IT][VEC];
+#pragma unroll
+    for (int it = 0; it < IT; it++)
+#pragma unroll
+        for (int j = 0; j < VEC; j++) acc[it][j] = 0.f;
+    const int* rows = sorted + start[v];
+    for (int r = r0; r < r1; r++) {
+        const T* src = dx + (size_t)rows[r] * C;
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            int col = (it * 32 + lane) * VEC;
+            if (col < C) {
+                float x[VEC];
+                load_vec_f<T, VEC>(x, src + col);
+#pragma unroll
+                for (int j = 0; j < VEC; j++) acc[it][j] += x[j];
+            }
+        }
+    }
+    bool single = n <= EMB_R;
+    float* dst = single ? dwte + (size_t)v * C : part + (size_t)(poff[v] + c) * C;
+#pragma unroll
+    for (int it = 0; it < IT; it++) {
+        int col = (it * 32 + lane) * VEC;
+        if (col < C) {
+#pragma unroll
+            for (int j = 0; j < VEC; j++) {
+                if (single) dst[col + j] += acc[it][j];
+                else dst[col + j] = acc[it][j];
+            }
+        }
+    }
+}
+
+__global__ void k_emb_fold(float* dwte, const float* part, const int* cnt, const int* poff,
+                           const int* n_items, const int2* items, int C) {
+    int item = blockIdx.x;
+    if (item >= *n_items) return;
+    int2 vc = items[item];
+    if (vc.y != 0) return;
+    int v = vc.x, n = cnt[v];
+    if (n <= EMB_R) return;
+    int ch = (n + EMB_R - 1) / EMB_R;
+    const float* p = part + (size_t)poff[v] * C;
+    for (int col = threadIdx.x; col < C; col += blockDim.x) {
+        float a = 0.f;
+        for (int k = 0; k < ch; k++) a += p[(size_t)k * C + col];
+        dwte[(size_t)v * C + col] += a;
+    }
+}
+
+template <typename T, int VEC>
+__global__ void k_wpe_bwd(float* dwpe, const T* dx, int B, int T_, int C) {
+    long idx = blockIdx.x * (long)blockDim.x + threadIdx.x;
+    int cv = C / VEC;
+    if (idx >= (long)T_ * cv) return;
+    int t = (int)(idx / cv), c = (int)(idx % cv) * VEC;
+    float a[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; j++) a[j] = 0.f;
+    for (int b = 0; b < B; b++) {
+        float x[VEC];
+        load_vec_f<T, VEC>(x, dx + ((size_t)b * T_ + t) * C + c);
+#pragma unroll
+        for (int j = 0; j < VEC; j++) a[j] += x[j];
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; j++) dwpe[(size_t)t * C + c + j] += a[j];
+}
+
+template <typename T, int VEC>
+static cudaError_t emb_bwd_vec(float* dwte, float* dwpe, const void* dx, const int* tok, int B,
+                               int T_, int C, int Vp, void* scratch, cudaStream_t s) {
+    int BT = B * T_;
+    EmbScratch e = emb_carve(scratch, BT, C, Vp, nullptr);
+    cudaMemsetAsync(e.blkcnt, 0, (size_t)e.nb * Vp * 4, s);
+    k_emb_rank<<<e.nb, EMB_BLK, 0, s>>>(tok, BT, Vp, e.lrank, e.blkcnt);
+    k_emb_blockprefix<<<cdiv(Vp, 256), 256, 0, s>>>(e.blkcnt, e.cnt, e.nb, Vp);
+    k_emb_scan<<<1, 1024, 0, s>>>(e.cnt, e.start, e.itemoff, e.poff, Vp);
+    k_emb_place<<<cdiv(BT, 256), 256, 0, s>>>(tok, BT, Vp, e.start, e.blkcnt, e.lrank, e.sorted);
+    k_emb_items<<<cdiv(Vp, 256), 256, 0, s>>>(e.cnt, e.itemoff, e.items, Vp);
+    int it = cdiv(C, 32 * VEC);
+    const int* n_items = e.itemoff + Vp;
+    dim3 g(cdiv(e.max_items, 8));
+#define EMR(I)                                                                                   \
+    k_emb_reduce2<T, VEC, I><<<g, 256, 0, s>>>(dwte, e.part, (const T*)dx, e.sorted, e.cnt,      \
+                                               e.start, n_items, e.poff, e.items, C)
+    if (it <= 1) EMR(1);
+    else if (it <= 2) EMR(2);
+    else if (it <= 4) EMR(4);
+    else if (it <= 8) EMR(8);
+    else if (it <= 16) EMR(16);
+    else return cudaErrorInvalidValue;
+#undef EMR
+    k_emb_fold<<<e.max_items, 256, 0, s>>>(dwte, e.part, e.cnt, e.poff, n_items, e.items, C);
+    k_wpe_bwd<T, VEC><<<cdiv((long)T_ * (C / VEC), 256), 256, 0, s>>>(dwpe, (const T*)dx, B, T_,
+                                                                       C);
+    return cudaGetLastError();
+}
+template <typename T>
+static cudaError_t emb_bwd_t(float* dwte, float* dwpe, const void* dx, const int* tok, int B,
+                             int T_, int C, int Vp, void* scratch, cudaStream_t s) {
+    constexpr int VM = 16 / sizeof(T);
+    if (C % VM == 0) return emb_bwd_vec<T, VM>(dwte, dwpe, dx, tok, B, T_, C, Vp, scratch, s);
+    return emb_bwd_vec<T, 1>(dwte, dwpe, dx, tok, B, T_, C, Vp, scratch, s);
+}
+cudaError_t encoder_backward(int act, float* dwte, float* dwpe, const void* dx, const int* tok,
+                             int B, int T_, int C, int Vp, void* scratch, cudaStream_t s) {
+    if (Vp >= (1 << 21)) return cudaErrorInvalidValue;
+    if (act == ACT_BF16) return emb_bwd_t<bf16>(dwte, dwpe, dx, tok, B, T_, C, Vp, scratch, s);
+    return emb_bwd_t<float>(dwte, dwpe, dx, tok, B, T_, C, Vp, scratch, s);
+}
+
+// ===========================================================================
+// AdamW with global-norm clipping ("update_params" in one pass over the
+// parameters after a norm pass).
+//  k_sumsq:     fixed grid; block b sums squares of its contiguous range.
+//  k_adam_norm: one block folds the block partials in order (fp64),
+//               n = sqrt(S)/n_accum, scale = (1/n_accum) * min(1, clip/n).
+//  k_adam:      per element update; skipped entirely if n is not finite.
+// ===========================================================================
+#define ADAM_NB 1184
+
+__global__ void __launch_bounds__(256) k_sumsq(const float* g, size_t n, double* part) {
+    __shared__ double sh[8];
+    size_t chunk = ((n + ADAM_NB - 1) / ADAM_NB + 3) & ~(size_t)3;
+    size_t lo = (size_t)blockIdx.x * chunk, hi = lo + chunk < n ? lo + chunk : n;
+    float a = 0.f;
+    if (lo < hi) {
+        size_t nv = (hi - lo) / 4;
+        const float4* g4 = reinterpret_cast<const float4*>(g + lo);
+        for (size_t i = threadIdx.x; i < nv; i += blockDim.x) {
+            float4 x = g4[i];
+            a += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+        }
+        for (size_t i = lo + nv * 4 + threadIdx.x; i < hi; i += blockDim.x) a += g[i] * g[i];
+    }
+    double d = warp_sum_d((double)a);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x / 32] = d;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < 8; w++) t += sh[w];
+        part[blockIdx.x] = t;
+    }
+}
+
+__global__ void k_adam_norm(const double* part, float* state, float inv_accum, float clip) {
+    __shared__ double sh[32];
+    double a = 0.0;
+    for (int i = threadIdx.x; i < ADAM_NB; i += blockDim.x) a += part[i];
+    a = warp_sum_d(a);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x / 32] = a;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < (int)(blockDim.x / 32); w++) t += sh[w];
+        float norm = (float)(sqrt(t) * (double)inv_accum);
+        int finite = isfinite(norm) ? 1 : 0;
+        float sc = inv_accum;
+        if (finite && clip > 0.f && norm > clip) sc = inv_accum * (clip / norm);
+        state[0] = norm;
+        state[1] = sc;
+        state[2] = (float)finite;
+    }
+}
+
+__device__ __forceinline__ bool decayed(size_t i, const AdamArgs& a) {
+#pragma unroll
+    for (int k = 0; k < 5; k++)
+        if (i >= a.dec_lo[k] && i < a.dec_hi[k]) return true;
+    return false;
+}
+
+__device__ __forceinline__ float adam_one(float& w, float& m, float& v, float g, float sc,
+                                          const AdamArgs& a, bool dec) {
+    float gi = g * sc;
+    m = a.b1 * m + (1.f - a.b1) * gi;
+    v = a.b2 * v + (1.f - a.b2) * gi * gi;
+    float mh = m / a.bc1, vh = v / a.bc2;
+    w = w - a.lr * (mh / (sqrtf(vh) + a.eps) + (dec ? a.wd * w : 0.f));
+    return w;
+}
+
+__global__ void __launch_bounds__(256) k_adam(float* w, float* m, float* v, const float* g,
+                                              bf16* wb, size_t n, AdamArgs a,
+                                              const float* state) {
+    if (state[2] == 0.f) return;
+    float sc = state[1];
+    size_t nv = n / 4;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nv;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float4 W = reinterpret_cast<float4*>(w)[i];
+        float4 M = reinterpret_cast<float4*>(m)[i];
+        float4 Vv = reinterpret_cast<float4*>(v)[i];
+        float4 G = reinterpret_cast<const float4*>(g)[i];
+        size_t e = i * 4;
+        adam_one(W.x, M.x, Vv.x, G.x, sc, a, decayed(e, a));
+        adam_one(W.y, M.y, Vv.y, G.y, sc, a, decayed(e + 1, a));
+        adam_one(W.z, M.z, Vv.z, G.z, sc, a, decayed(e + 2, a));
+        adam_one(W.w, M.w, Vv.w, G.w, sc, a, decayed(e + 3, a));
+        reinterpret_cast<float4*>(w)[i] = W;
+        reinterpret_cast<float4*>(m)[i] = M;
+        reinterpret_cast<float4*>(v)[i] = Vv;
+        if (wb) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(W.x, W.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(W.z, W.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<unsigned*>(&lo);
+            pk.y = *reinterpret_cast<unsigned*>(&hi);
+            reinterpret_cast<uint2*>(wb)[i] = pk;
+        }
+    }
+    for (size_t e = nv * 4 + blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
+         e += (size_t)gridDim.x * blockDim.x) {
+        float W = w[e], M = m[e], Vv = v[e];
+        adam_one(W, M, Vv, g[e], sc, a, decayed(e, a));
+        w[e] = W;
+        m[e] = M;
+        v[e] = Vv;
+        if (wb) wb[e] = __float2bfloat16_rn(W);
+    }
+}
+
+size_t adamw_scratch() { return ADAM_NB * sizeof(double); }
+
+cudaError_t adamw_step(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
+                       const AdamArgs& a, float* state, void* scratch, cudaStream_t s) {
+    double* part = (double*)scratch;
+    k_sumsq<<<ADAM_NB, 256, 0, s>>>(g, n, part);
+    k_adam_norm<<<1, 1024, 0, s>>>(part, state, a.inv_accum, a.clip);
+    k_adam<<<148 * 8, 256, 0, s>>>(w, m, v, g, (bf16*)wbf16, n, a, state);
+    return cudaGetLastError();
+}
+
+}  // namespace gk

@@ -1,0 +1,112 @@
+// kernels.h -- host-side launchers of the libgpt2b300 kernels (internal).
+//
+// Every launcher enqueues on the given stream and returns the launch status.
+// `act` selects the activation / compute-copy element type: ACT_F32 (fp32)
+// or ACT_BF16 (bf16).  Gradients of parameters are always fp32.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+// Device error word bits (OR-ed by kernels, read by the host at sync points).
+#define GPT2_DEVERR_TOKEN 1u    // a token/target id outside [0, V)
+#define GPT2_DEVERR_TIMEOUT 2u  // a bounded wait in a pipelined kernel ran out
+#define GPT2_DEVERR_SHAPE 4u    // a kernel was launched with a shape it cannot do
+
+namespace gk {
+
+enum { ACT_F32 = 0, ACT_BF16 = 1 };
+inline size_t act_size(int act) { return act == ACT_BF16 ? 2 : 4; }
+
+// Canonical tensor indices (weights are out x in, row-major).
+enum {
+    P_WTE, P_WPE, P_LN1W, P_LN1B, P_QKVW, P_QKVB, P_PROJW, P_PROJB,
+    P_LN2W, P_LN2B, P_FCW, P_FCB, P_FCPROJW, P_FCPROJB, P_LNFW, P_LNFB, P_NUM
+};
+
+struct ParamLayout {
+    size_t off[P_NUM + 1];  // element offsets; off[P_NUM] = total
+    int L, C, V, Vp, T;
+};
+void make_layout(ParamLayout* lay, int L, int C, int V, int T);
+
+// ---- parameters -----------------------------------------------------------
+cudaError_t init_params(float* master, const ParamLayout& lay, uint64_t seed, cudaStream_t s);
+cudaError_t cast_to_bf16(void* dst, const float* src, size_t n, cudaStream_t s);
+
+// ---- embedding ------------------------------------------------------------
+// out[b,t,:] = wte[tok[b,t],:] + wpe[t,:]; ids outside [0,V) set err bit.
+cudaError_t encoder_forward(int act, void* out, const int* tok, const void* wte, const void* wpe,
+                            int B, int T, int C, int V, unsigned* err, cudaStream_t s);
+// Scratch for the deterministic embedding backward (bytes).
+size_t encoder_backward_scratch(int B, int T, int C, int Vp);
+// dwte[tok] += dx rows (each row sum taken in position order), dwpe[t] += sum_b dx[b,t].
+cudaError_t encoder_backward(int act, float* dwte, float* dwpe, const void* dx, const int* tok,
+                             int B, int T, int C, int Vp, void* scratch, cudaStream_t s);
+
+// ---- layernorm ------------------------------------------------------------
+cudaError_t layernorm_forward(int act, void* out, float* mean, float* rstd, const void* x,
+                              const void* w, const void* b, int N, int C, cudaStream_t s);
+size_t layernorm_backward_scratch(int N, int C);
+// dx (+=), dw (+=), db (+=); partial column sums go through scratch.
+cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, const void* dout,
+                               const void* x, const void* w, const float* mean,
+                               const float* rstd, int N, int C, void* scratch, cudaStream_t s);
+
+// ---- bias gradient: db[o] += sum_n dout[n,o] (deterministic, two stage) ---
+size_t bias_grad_scratch(int N, int OC);
+cudaError_t bias_grad(int act, float* db, const void* dout, int N, int OC, void* scratch,
+                      cudaStream_t s);
+
+// ---- classifier: loss per row + dlogits in place ----------------------------
+// logits [N,Vp]; losses[n] = lse(logits[n,:V]) - logits[n,tgt]; if dloss != 0
+// the row is overwritten by (softmax - onehot)*dloss (pad columns -> 0).
+cudaError_t crossentropy_fused(int act, void* logits, float* losses, const int* tgt, int N,
+                               int V, int Vp, float dloss, unsigned* err, cudaStream_t s);
+// out[0] = mean(x[0..n)) in a fixed summation order (one block).
+cudaError_t mean_reduce(float* out, const float* x, int n, cudaStream_t s);
+
+// ---- AdamW ------------------------------------------------------------------
+struct AdamArgs {
+    float lr, b1, b2, eps, wd;
+    float bc1, bc2;          // 1 - b1^t, 1 - b2^t
+    float inv_accum, clip;
+    size_t dec_lo[5], dec_hi[5];  // decayed index ranges [lo, hi)
+};
+size_t adamw_scratch();
+// state[0] = norm, state[1] = total gradient scale, state[2] = finite flag
+cudaError_t adamw_step(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
+                       const AdamArgs& a, float* state, void* scratch, cudaStream_t s);
+
+// ---- SIMT matmul (fp32 FFMA) ----------------------------------------------
+enum Epi {
+    EPI_STORE = 0,      // D = acc (+ bias)
+    EPI_GELU = 1,       // aux = acc + bias; D = gelu(aux)
+    EPI_RESID = 2,      // D = resid + acc + bias
+    EPI_ACCUM_F32 = 3,  // D(fp32) += acc
+    EPI_GELU_BWD = 4    // D = acc * gelu'(aux)
+};
+struct GemmDesc {
+    int M, N, K;
+    const void* A; long lda; int a_kmajor;  // A[m,k] at m*lda+k (K-major) or k*lda+m
+    const void* B; long ldb; int b_kmajor;  // B[n,k] at n*ldb+k (K-major) or k*ldb+n
+    void* D; long ldd;                      // D[m,n] at m*ldd+n
+    const void* bias;                       // [N] act type, or NULL
+    const void* resid; long ldr;            // EPI_RESID
+    void* aux; long ldx;                    // EPI_GELU out / EPI_GELU_BWD in
+    int epi;
+    int act;                                // element type of A, B, bias, resid, aux, D (non-accum)
+};
+cudaError_t gemm_simt(const GemmDesc& d, cudaStream_t s);
+
+// ---- attention (causal, softmax(Q K^T / sqrt(hd)) V) --------------------------
+// qkv [B,T,3C]; out [B,T,C]; lse [B,H,T] fp32
+cudaError_t attention_forward(int act, void* out, float* lse, const void* qkv, int B, int T,
+                              int C, int H, cudaStream_t s);
+size_t attention_backward_scratch(int B, int T, int H);
+// dqkv [B,T,3C] is overwritten
+cudaError_t attention_backward(int act, void* dqkv, const void* dout, const void* qkv,
+                               const void* out, const float* lse, int B, int T, int C, int H,
+                               void* scratch, cudaStream_t s);
+
+}  // namespace gk

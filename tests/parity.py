@@ -1,0 +1,49 @@
+"""Comparison helpers for the GPU-vs-oracle parity tests.
+
+Relative error on a tensor (the reading of "rel 1e-4 on every gradient
+tensor"): the tensor passes when ||got - ref||_2 <= tol * ||ref||_2 AND
+max|got - ref| <= tol * max|ref|.  Elementwise relative error is not used
+because it is ill-posed for entries that are 0 in exact arithmetic.
+"""
+import numpy as np
+
+from oracle.pyoracle import TENSOR_NAMES
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, np.float64).reshape(-1)
+    ref = np.asarray(ref, np.float64).reshape(-1)
+    d = got - ref
+    nr = np.linalg.norm(ref)
+    mr = np.abs(ref).max() if ref.size else 0.0
+    e2 = np.linalg.norm(d) / nr if nr > 0 else np.linalg.norm(d)
+    emax = np.abs(d).max() / mr if mr > 0 else (np.abs(d).max() if d.size else 0.0)
+    return max(e2, emax)
+
+
+def assert_close(got, ref, tol, what=""):
+    e = rel_err(got, ref)
+    assert e <= tol, f"{what}: relative error {e:.3e} > {tol:.1e}"
+
+
+def key_bias_mask(m):
+    """Boolean mask over the canonical vector: True everywhere except the key
+    bias of every layer.  The loss does not depend on the key bias (adding a
+    constant to every key score of a query leaves its softmax unchanged), so
+    its exact gradient is 0 and what an implementation computes there is
+    rounding noise, which Adam turns into O(lr) steps of arbitrary sign."""
+    keep = np.ones(m.n, bool)
+    sl = m.tensor_slices()["qkvb"]
+    C, L = m.C, m.L
+    for l in range(L):
+        o = sl.start + l * 3 * C + C
+        keep[o:o + C] = False
+    return keep
+
+
+def compare_tensors(got_vec, ref_vec, m, tol, what="", skip=()):
+    sl = m.tensor_slices()
+    for k in TENSOR_NAMES:
+        if k in skip:
+            continue
+        assert_close(got_vec[sl[k]], ref_vec[sl[k]], tol, f"{what} {k}")
