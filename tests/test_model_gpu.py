@@ -120,20 +120,26 @@ def test_fp32_toy_50_adamw_steps_stepwise():
     """the toy binary GPT, lr 1e-2, wd 0, torch-default betas/eps, no clip"""
     cfg = dict(TOY, B=12)
     om, gm = _pair(cfg, FP32, seed=0)
+    o32 = Model(**cfg, seed=0, real="float")
     keep = key_bias_mask(om)
     tok, tgt = inputs.toy_windows(0)
     hp = dict(lr=1e-2, b1=0.9, b2=0.999, eps=1e-8, wd=0.0, clip=0.0)
     for step in range(50):
         gm.set_params(om.params())
         gm.set_opt_state(om.m(), om.v(), om.step_count())
+        o32.set_params(om.params())
         om.zero_grad()
         gm.zero_grad()
+        o32.zero_grad()
         lo = om.forward(tok, tgt)
         om.backward()
+        o32.forward(tok, tgt)
+        o32.backward()
         lg = gm.forward(tok, tgt, sync_loss=True)
         gm.backward()
         assert abs(lg - lo) <= 1e-4 * abs(lo)
-        compare_tensors(gm.get_grads(), om.grads(), om, 1e-4, f"step {step} grad")
+        compare_tensors(gm.get_grads(), om.grads(), om, 1e-4, f"step {step} grad",
+                        f32_vec=o32.grads())
         om.adamw_step(**hp)
         gm.adamw_step(**hp)
         assert_close(gm.get_params()[keep], om.params()[keep], 1e-4, f"step {step} params")
