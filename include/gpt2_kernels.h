@@ -1,0 +1,100 @@
+/*
+ * gpt2_kernels.h -- kernel-level C-ABI of libgpt2b300: each hot-path
+ * operation of the GPT-2 training step as one call on caller-owned device
+ * buffers, so that every operation can be checked on its own (at full size)
+ * against an independent reference.  The model-level calls in gpt2.h run
+ * exactly these kernels.
+ *
+ * Common rules
+ *  - dtype: 0 = fp32 elements, 1 = bf16 elements, for every activation /
+ *    weight buffer of the call (statistics, lse and losses are always fp32).
+ *  - All pointers are device pointers on the current device; all work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *    the call returns without waiting.  Buffers are owned by the caller and
+ *    must not overlap unless stated.
+ *  - `scratch` is caller-owned device memory of at least the size the
+ *    matching *_scratch_bytes call returns (256-byte aligned).
+ *  - `err` (where present) is a device unsigned word the kernels OR error
+ *    bits into: 1 = an id outside [0, V), 2 = a bounded wait ran out.
+ *  - Return: 0 on success, -1 (GPT2_ERR_ARG) for a shape / alignment the
+ *    kernels do not take, -2 (GPT2_ERR_CUDA) if a launch failed.
+ */
+#ifndef GPT2_B300_KERNELS_H
+#define GPT2_B300_KERNELS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Linear layer, forward and backward ("Karpathy's llm.c: understanding LLM
+ * training from scratch in C/CUDA", "Code anatomy": the QKV / projection /
+ * MLP / classifier matmuls):  D[M,N] = epi(sum_k A[m,k] B[n,k]).
+ *   A[m,k] is at A[m*lda + k] if a_kmajor else A[k*lda + m]; same for B with n.
+ *   epi 0: D = acc (+ bias[n])                      (bias may be NULL)
+ *   epi 1: aux = acc + bias[n]; D = gelu_tanh(aux)
+ *   epi 2: D = resid[m,n] + acc (+ bias[n])
+ *   epi 3: D (fp32) += acc                          (weight-gradient accumulate)
+ *   epi 4: D = acc * gelu_tanh'(aux[m,n])           (MLP backward)
+ * impl: 0 = automatic (tensor cores for bf16 when the shape fits, else the
+ * fp32-FFMA kernel), 1 = fp32-FFMA kernel, 2 = tensor cores (bf16 only;
+ * returns -1 if the shape does not fit: N % 8, 16-byte aligned bases,
+ * leading dimensions % 8). */
+size_t gpt2k_matmul_scratch_bytes(void);
+int gpt2k_matmul(int dtype, int impl, int M, int N, int K, const void* A, long lda, int a_kmajor,
+                 const void* B, long ldb, int b_kmajor, void* D, long ldd, const void* bias,
+                 const void* resid, long ldr, void* aux, long ldx, int epi, void* scratch,
+                 size_t scratch_bytes, unsigned* err, void* stream);
+
+/* Causal self-attention ("Getting started with LLMs from Andrej Karpathy's
+ * talk", self-attention: softmax(Q K^T / sqrt(d_k)) V), query t attending to
+ * keys 0..t.  qkv [B,T,3C] = Q | K | V with head h at columns h*hd.. of each
+ * C block; out [B,T,C]; lse [B,H,T] = log-sum-exp of each score row. */
+int gpt2k_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T,
+                            int C, int H, void* stream);
+size_t gpt2k_attention_backward_scratch_bytes(int B, int T, int C, int H);
+/* dqkv [B,T,3C] (overwritten) from dout [B,T,C], qkv, out and lse of the forward. */
+int gpt2k_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv,
+                             const void* out, const float* lse, int B, int T, int C, int H,
+                             void* scratch, void* stream);
+
+/* LayerNorm over rows of C (eps 1e-5, biased variance): out = (x-mean)*rstd*w + b,
+ * mean/rstd [N] fp32 saved.  Backward ACCUMULATES into dx [N,C] (dtype) and
+ * into dw, db [C] (fp32). */
+int gpt2k_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* x,
+                            const void* w, const void* b, int N, int C, void* stream);
+size_t gpt2k_layernorm_backward_scratch_bytes(int N, int C);
+int gpt2k_layernorm_backward(int dtype, void* dx, float* dw, float* db, const void* dout,
+                             const void* x, const void* w, const float* mean, const float* rstd,
+                             int N, int C, void* scratch, void* stream);
+
+/* Token + position embedding: out[b,t,:] = wte[tok[b,t],:] + wpe[t,:].
+ * Backward ACCUMULATES dwte[tok[b,t],:] += dx[b,t,:] (each row's sum taken
+ * in position order, no atomics) and dwpe[t,:] += sum_b dx[b,t,:]. */
+int gpt2k_encoder_forward(int dtype, void* out, const int32_t* tok, const void* wte,
+                          const void* wpe, int B, int T, int C, int V, unsigned* err,
+                          void* stream);
+size_t gpt2k_encoder_backward_scratch_bytes(int B, int T, int C, int Vp);
+int gpt2k_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx,
+                           const int32_t* tok, int B, int T, int C, int Vp, void* scratch,
+                           void* stream);
+
+/* Softmax cross-entropy over the first V of Vp columns of logits [N,Vp]:
+ * losses[n] = logsumexp(logits[n,:V]) - logits[n,tgt[n]]; if dloss != 0 the
+ * row is overwritten in place by (softmax - onehot(tgt)) * dloss, pad
+ * columns set to 0 ("Karpathy reproduces GPT-2 (1.6B) in llm.c", "PyTorch
+ * comparison": the fused classifier). */
+int gpt2k_crossentropy(int dtype, void* logits, float* losses, const int32_t* tgt, int N, int V,
+                       int Vp, float dloss, unsigned* err, void* stream);
+
+/* Bias gradient: db[o] += sum_n dout[n,o] (fixed summation order). */
+size_t gpt2k_bias_grad_scratch_bytes(int N, int OC);
+int gpt2k_bias_grad(int dtype, float* db, const void* dout, int N, int OC, void* scratch,
+                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

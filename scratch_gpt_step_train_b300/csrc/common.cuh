@@ -51,17 +51,21 @@ __device__ __forceinline__ void store_vec_f(T* dst, const float* src) {
     *reinterpret_cast<Vec<T, N>*>(dst) = x;
 }
 
-// tanh-form GELU (Hendrycks & Gimpel 2016) and its analytic derivative.
+// tanh-form GELU (Hendrycks & Gimpel 2016), 0.5 x (1 + tanh(u)) with
+// u = sqrt(2/pi) (x + 0.044715 x^3), and its analytic derivative.  Both are
+// evaluated through the exact identity 0.5 (1 + tanh(u)) = 1 / (1 + e^{-2u}),
+// which keeps full relative precision in the negative tail where 1 + tanh(u)
+// would cancel in fp32 (and 1 - tanh(u)^2 = 4 s (1 - s) with s that sigmoid).
 __device__ __forceinline__ float gelu_f(float x) {
     const float k = 0.7978845608028654f;  // sqrt(2/pi)
     float u = k * (x + 0.044715f * x * x * x);
-    return 0.5f * x * (1.0f + tanhf(u));
+    return x / (1.0f + expf(-2.0f * u));
 }
 __device__ __forceinline__ float gelu_grad_f(float x) {
     const float k = 0.7978845608028654f;
     float x2 = x * x;
     float u = k * (x + 0.044715f * x2 * x);
-    float th = tanhf(u);
+    float sg = 1.0f / (1.0f + expf(-2.0f * u));
     float du = k * (1.0f + 3.0f * 0.044715f * x2);
-    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
+    return sg + 2.0f * x * sg * (1.0f - sg) * du;
 }

@@ -160,6 +160,7 @@ static size_t scratch_need(int L, int H, int C, int Vp, int T, int B) {
     if ((x = encoder_backward_scratch(B, T, C, Vp)) > s) s = x;
     if ((x = attention_backward_scratch(B, T, H)) > s) s = x;
     if ((x = adamw_scratch()) > s) s = x;
+    if ((x = gemm_tc_scratch_bytes()) > s) s = x;
     return s;
 }
 
@@ -373,11 +374,16 @@ static int mm(gpt2* g, int cls, GemmDesc d) {
     double as = (double)act_size(g->act);
     double by = as * ((double)d.M * d.K + (double)d.N * d.K) +
                 (d.epi == EPI_ACCUM_F32 ? 8.0 : as) * d.M * d.N;
-    g->launches += 1;
     prof_begin(g, cls, fl, by);
     cudaError_t e;
-    if (g->use_tc && gemm_tc_supported(d)) e = gemm_tc(d, g->stream);
-    else e = gemm_simt(d, g->stream);
+    if (g->use_tc && gemm_tc_supported(d)) {
+        int nl = 0;
+        e = gemm_tc(d, g->scratch, g->scratch_bytes, g->err, g->stream, &nl);
+        g->launches += nl;
+    } else {
+        e = gemm_simt(d, g->stream);
+        g->launches += 1;
+    }
     prof_end(g);
     if (e != cudaSuccess)
         return fail(g, GPT2_ERR_CUDA, "matmul M=%d N=%d K=%d epi=%d: %s", d.M, d.N, d.K, d.epi,

@@ -1,7 +1,624 @@
-// k_gemm_tc.cu -- placeholder until the tcgen05 kernel lands.
+// k_gemm_tc.cu -- bf16 x bf16 -> fp32 matmul on the 5th-generation tensor cores
+// of sm_103a (tcgen05.mma, accumulator in tensor memory), operands staged in
+// shared memory by TMA, with the fused epilogues of the GPT-2 step.
+//
+// These are the dense contractions of the step -- the QKV, attention-output,
+// MLP and tied-classifier linear layers of "Karpathy's llm.c: understanding
+// LLM training from scratch in C/CUDA", "Code anatomy", forward and backward
+// (the pages run them through cuBLAS/cuBLASLt with a GELU epilogue,
+// "Karpathy reproduces GPT-2 (1.6B) in llm.c", flag guide; here they are
+// written directly for the B300).
+//
+// D[M,N] = A[M,K] . B[N,K]^T.  Each operand is either K-major (rows of K
+// contiguous) or M/N-major (the transpose is stored); the instruction
+// descriptor's transpose bits select the smem layout, so dX = dY W and
+// dW = dY^T X run without transposed copies.
+//
+// Kernel organisation (one persistent CTA per SM, 192 threads):
+//   warp 0    TMA producer: 2-D tiled loads, 128-byte swizzle, STAGES-deep
+//             ring of (A, B) stages guarded by full/empty mbarriers
+//   warp 1    allocates 2*BN TMEM columns; lane 0 issues tcgen05.mma
+//             (M=128, N=BN, K=16) and tcgen05.commit to free stages and to
+//             publish a finished accumulator
+//   warps 2-5 epilogue: tcgen05.ld of their 32-lane quarter of the
+//             accumulator, bias / GELU / residual / fp32 accumulate, stores
+// Two TMEM accumulators let the epilogue of tile i overlap the mainloop of
+// tile i+1.  Every mbarrier wait is bounded (clock64 budget): on expiry the
+// CTA raises an abort flag, sets GPT2_DEVERR_TIMEOUT in the device error
+// word, lets every role leave its loop, waits for its own TMA loads, frees
+// its TMEM and returns.
+//
+// Weight-gradient products have K = B*T (16384) and few output tiles; they
+// are split along K into fp32 partial tiles summed in a fixed order by a
+// second kernel (deterministic; no float atomics).
+#include <cuda.h>
+
+#include "common.cuh"
 #include "gemm_tc.h"
+
 namespace gk {
-bool gemm_tc_available() { return false; }
-bool gemm_tc_supported(const GemmDesc&) { return false; }
-cudaError_t gemm_tc(const GemmDesc&, cudaStream_t) { return cudaErrorNotSupported; }
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int NUM_THREADS = 192;
+constexpr long long WAIT_LIMIT = 4000000000LL;  // ~2 s of SM clock
+
+template <int BN>
+struct Cfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+};
+
+struct TcParams {
+    int M, N, K;
+    int tiles_m, tiles_n, splits, k_per_split, num_tiles;
+    int epi;
+    void* D;
+    long ldd;
+    const bf16* bias;
+    const bf16* resid;
+    long ldr;
+    bf16* aux;
+    long ldx;
+    float* part;
+    unsigned* err;
+};
+
+enum { EPI_PART_F32 = 100 };
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of parity `parity` to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* err) {
+    if (mbar_try(bar, parity)) return true;
+    long long t0 = clock64();
+    while (true) {
+        if (mbar_try(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > WAIT_LIMIT) {
+            *abort_flag = 1;
+            atomicOr(err, GPT2_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// 32 TMEM lanes x 32 consecutive 32-bit columns -> 32 registers per thread
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, version 1 (sm_100 family).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ epilogue
+__device__ __forceinline__ void ld8_bf16(float* f, const bf16* p) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+__device__ __forceinline__ void st8_bf16(bf16* p, const float* f) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+
+// one thread: 32 accumulator columns [col, col+32) of row `row`; nv valid
+// columns (a multiple of 8)
+__device__ __forceinline__ void epilogue32(const TcParams& p, int row, int col, int nv, float* v,
+                                           int split) {
+    switch (p.epi) {
+        case EPI_ACCUM_F32: {
+            float* d = (float*)p.D + (size_t)row * p.ldd + col;
+            for (int j = 0; j < nv; j += 4) {
+                float4 o = *reinterpret_cast<float4*>(d + j);
+                o.x += v[j]; o.y += v[j + 1]; o.z += v[j + 2]; o.w += v[j + 3];
+                *reinterpret_cast<float4*>(d + j) = o;
+            }
+            break;
+        }
+        case EPI_PART_F32: {
+            float* d = p.part + ((size_t)split * p.M + row) * p.N + col;
+            for (int j = 0; j < nv; j += 4)
+                *reinterpret_cast<float4*>(d + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            break;
+        }
+        case EPI_GELU_BWD: {
+            const bf16* a = p.aux + (size_t)row * p.ldx + col;
+            bf16* d = (bf16*)p.D + (size_t)row * p.ldd + col;
+            for (int j = 0; j < nv; j += 8) {
+                float pre[8];
+                ld8_bf16(pre, a + j);
+#pragma unroll
+                for (int i = 0; i < 8; i++) pre[i] = v[j + i] * gelu_grad_f(pre[i]);
+                st8_bf16(d + j, pre);
+            }
+            break;
+        }
+        default: {
+            bf16* d = (bf16*)p.D + (size_t)row * p.ldd + col;
+            for (int j = 0; j < nv; j += 8) {
+                float x[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) x[i] = v[j + i];
+                if (p.bias) {
+                    float b[8];
+                    ld8_bf16(b, p.bias + col + j);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) x[i] += b[i];
+                }
+                if (p.epi == EPI_RESID) {
+                    float r[8];
+                    ld8_bf16(r, p.resid + (size_t)row * p.ldr + col + j);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) x[i] += r[i];
+                } else if (p.epi == EPI_GELU) {
+                    st8_bf16(p.aux + (size_t)row * p.ldx + col + j, x);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) x[i] = gelu_f(x[i]);
+                }
+                st8_bf16(d + j, x);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------- kernel
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+              TcParams p) {
+    using CF = Cfg<BN>;
+    constexpr int S = CF::STAGES;
+    constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t tiles = (raw + 1023u) & ~1023u;
+    uint8_t* tiles_gen = smem_raw + (tiles - raw);
+    const uint32_t bars = tiles + S * CF::STAGE_BYTES;
+    const uint32_t full = bars, empty = bars + 8 * S, tfull = bars + 16 * S,
+                   tempty = tfull + 16;
+    uint32_t* tmem_slot = (uint32_t*)(tiles_gen + S * CF::STAGE_BYTES + 16 * S + 32);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full + 8 * s, 1);
+            mbar_init(empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(tfull + 8 * b, 1);
+            mbar_init(tempty + 8 * b, 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&mapA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&mapB) : "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int tiles_mn = p.tiles_m * p.tiles_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------------- producer
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;  // bit s: stage s has a load in flight or landed
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                const int split = tile / tiles_mn, r = tile % tiles_mn;
+                const int tm = r % p.tiles_m, tn = r / p.tiles_m;
+                const int k0 = split * p.k_per_split;
+                const int k1 = min(p.K, k0 + p.k_per_split);
+                const int nkb = (k1 - k0 + BK - 1) / BK;
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!mbar_wait(empty + 8 * s, ph ^ 1u, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = tiles + s * CF::STAGE_BYTES, sb = sa + CF::A_BYTES;
+                    const uint32_t fb = full + 8 * s;
+                    mbar_expect_tx(fb, CF::STAGE_BYTES);
+                    const int kk = k0 + kb * BK;
+                    if (!A_MN) {
+                        tma_load_2d(sa, &mapA, fb, kk, tm * BM);
+                    } else {
+                        tma_load_2d(sa, &mapA, fb, tm * BM, kk);
+                        tma_load_2d(sa + 8192, &mapA, fb, tm * BM + 64, kk);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(sb, &mapB, fb, kk, tn * BN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; j++)
+                            tma_load_2d(sb + j * 8192, &mapB, fb, tn * BN + 64 * j, kk);
+                    }
+                    issued |= 1u << s;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // drain: wait (bounded, ignoring the abort flag) for every
+                // stage's most recent load so no copy lands after exit
+                for (int i = 0; i < S; i++) {
+                    if (!((issued >> i) & 1u)) continue;
+                    // the last issue of stage i used parity (ph if i < s else ph^1)
+                    uint32_t par = i < s ? ph : ph ^ 1u;
+                    long long t0 = clock64();
+                    while (!mbar_try(full + 8 * i, par) && clock64() - t0 < WAIT_LIMIT) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // --------------------------------------------------------- MMA
+            int s = 0;
+            uint32_t ph = 0;
+            int lt = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, lt++) {
+                const int split = tile / tiles_mn;
+                const int k0 = split * p.k_per_split;
+                const int k1 = min(p.K, k0 + p.k_per_split);
+                const int nkb = (k1 - k0 + BK - 1) / BK;
+                const int b = lt & 1;
+                const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+                if (!mbar_wait(tempty + 8 * b, aph ^ 1u, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dt = tmem_base + (uint32_t)(b * BN);
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!mbar_wait(full + 8 * s, ph, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = tiles + s * CF::STAGE_BYTES, sb = sa + CF::A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; k++) {
+                        const uint64_t ad =
+                            A_MN ? sdesc(sa + k * 2048, 8192, 1024) : sdesc(sa + k * 32, 0, 1024);
+                        const uint64_t bd =
+                            B_MN ? sdesc(sb + k * 2048, 8192, 1024) : sdesc(sb + k * 32, 0, 1024);
+                        umma_bf16(dt, ad, bd, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty + 8 * s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull + 8 * b);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int lt = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, lt++) {
+            const int split = tile / tiles_mn, r = tile % tiles_mn;
+            const int tm = r % p.tiles_m, tn = r / p.tiles_m;
+            const int b = lt & 1;
+            const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(tfull + 8 * b, aph, abort_flag, p.err);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            tc_fence_after();
+            const int row = tm * BM + q * 32 + lane;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(taddr + (uint32_t)c0, v);
+                const int col = tn * BN + c0;
+                if (row < p.M && col < p.N) {
+                    const int nv = min(32, p.N - col);
+                    epilogue32(p, row, col, nv, v, split);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty + 8 * b);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 2 * BN);
+    }
+}
+
+// split-K: D[m,n] += sum_s part[s][m][n], s in order
+__global__ void k_splitk_reduce(float* D, long ldd, const float* part, int M, int N, int splits) {
+    long idx = blockIdx.x * (long)blockDim.x + threadIdx.x;
+    long nv = (long)M * (N / 4);
+    if (idx >= nv) return;
+    int m = (int)(idx / (N / 4)), n = (int)(idx % (N / 4)) * 4;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < splits; s++) {
+        float4 x = *reinterpret_cast<const float4*>(part + ((size_t)s * M + m) * N + n);
+        a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+    }
+    float4* d = reinterpret_cast<float4*>(D + (size_t)m * ldd + n);
+    float4 o = *d;
+    o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
+    *d = o;
+}
+
+// ----------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+int g_num_sms = 148;
+int g_state = -1;  // -1 unknown, 0 unavailable, 1 ready
+
+template <int BN, bool AM, bool BMN>
+void set_smem_attr() {
+    cudaFuncSetAttribute(k_gemm_tc<BN, AM, BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg<BN>::SMEM);
+}
+
+// 2-D bf16 tensor map: inner extent `inner` (contiguous), `outer` rows of
+// `ld` elements; box = 64 x box_outer; 128-byte swizzle; OOB reads give 0.
+bool make_map(CUtensorMap* m, const void* base, long inner, long outer, long ld, int box_outer) {
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool AM, bool BMN>
+cudaError_t launch(const GemmDesc& d, const TcParams& tp, int grid, cudaStream_t s) {
+    CUtensorMap ma, mb;
+    // A: K-major -> [M rows][K], box 64(K) x 128(M);  MN-major -> [K rows][M], box 64(M) x 64(K)
+    bool ok = AM ? make_map(&ma, d.A, d.M, d.K, d.lda, 64)
+                 : make_map(&ma, d.A, d.K, d.M, d.lda, BM);
+    ok = ok && (BMN ? make_map(&mb, d.B, d.N, d.K, d.ldb, 64)
+                    : make_map(&mb, d.B, d.K, d.N, d.ldb, BN));
+    if (!ok) return cudaErrorInvalidValue;
+    k_gemm_tc<BN, AM, BMN><<<grid, NUM_THREADS, Cfg<BN>::SMEM, s>>>(ma, mb, tp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_tc_available() {
+    if (g_state >= 0) return g_state == 1;
+    g_state = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return false;
+    if (prop.major != 10 || prop.minor != 3) return false;
+    g_num_sms = prop.multiProcessorCount;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return false;
+    }
+    g_encode = (EncodeTiledFn)fn;
+    set_smem_attr<256, false, false>();
+    set_smem_attr<256, false, true>();
+    set_smem_attr<256, true, false>();
+    set_smem_attr<256, true, true>();
+    set_smem_attr<128, false, false>();
+    set_smem_attr<128, false, true>();
+    set_smem_attr<128, true, false>();
+    set_smem_attr<128, true, true>();
+    if (cudaGetLastError() != cudaSuccess) return false;
+    g_state = 1;
+    return true;
+}
+
+static bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+bool gemm_tc_supported(const GemmDesc& d) {
+    if (d.act != ACT_BF16 || d.M < 1 || d.N < 1 || d.K < 1) return false;
+    if (d.N % 8) return false;
+    if (!al16(d.A) || !al16(d.B) || !al16(d.D)) return false;
+    if ((d.lda % 8) || (d.ldb % 8) || (d.ldd % 8)) return false;
+    if (d.a_kmajor ? d.lda < d.K : d.lda < d.M) return false;
+    if (d.b_kmajor ? d.ldb < d.K : d.ldb < d.N) return false;
+    if (d.epi == EPI_RESID && (!d.resid || !al16(d.resid) || d.ldr % 8)) return false;
+    if ((d.epi == EPI_GELU || d.epi == EPI_GELU_BWD) && (!d.aux || !al16(d.aux) || d.ldx % 8))
+        return false;
+    if (d.bias && !al16(d.bias)) return false;
+    return true;
+}
+
+size_t gemm_tc_scratch_bytes() { return (size_t)64 << 20; }
+
+cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsigned* err,
+                    cudaStream_t s, int* nlaunch) {
+    if (nlaunch) *nlaunch = 0;
+    if (!gemm_tc_available()) return cudaErrorNotSupported;
+    if (!gemm_tc_supported(d)) return cudaErrorInvalidValue;
+    const int tiles_m = (d.M + BM - 1) / BM;
+    int BN = 256;
+    if ((long)tiles_m * ((d.N + 255) / 256) < 2L * g_num_sms || d.N <= 128) BN = 128;
+    const int tiles_n = (d.N + BN - 1) / BN;
+    TcParams tp;
+    tp.M = d.M; tp.N = d.N; tp.K = d.K;
+    tp.tiles_m = tiles_m;
+    tp.tiles_n = tiles_n;
+    tp.splits = 1;
+    tp.k_per_split = ((d.K + BK - 1) / BK) * BK;
+    tp.epi = d.epi;
+    tp.D = d.D; tp.ldd = d.ldd;
+    tp.bias = (const bf16*)d.bias;
+    tp.resid = (const bf16*)d.resid; tp.ldr = d.ldr;
+    tp.aux = (bf16*)d.aux; tp.ldx = d.ldx;
+    tp.part = (float*)scratch;
+    tp.err = err;
+    const long tiles = (long)tiles_m * tiles_n;
+    if (d.epi == EPI_ACCUM_F32 && tiles < g_num_sms && d.K >= 8 * BK && scratch) {
+        int splits = (int)((2L * g_num_sms + tiles - 1) / tiles);
+        int kb = (d.K + BK - 1) / BK;
+        if (splits > kb / 4) splits = kb / 4;
+        if (splits > 16) splits = 16;
+        while (splits > 1 && (size_t)splits * d.M * d.N * 4 > scratch_bytes) splits--;
+        if (splits > 1) {
+            int kbs = (kb + splits - 1) / splits;
+            tp.k_per_split = kbs * BK;
+            tp.splits = (kb + kbs - 1) / kbs;
+            tp.epi = EPI_PART_F32;
+        }
+    }
+    tp.num_tiles = (int)(tiles * tp.splits);
+    const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
+    const bool am = !d.a_kmajor, bm = !d.b_kmajor;
+    cudaError_t e;
+    if (BN == 256) {
+        if (!am && !bm) e = launch<256, false, false>(d, tp, grid, s);
+        else if (!am && bm) e = launch<256, false, true>(d, tp, grid, s);
+        else if (am && !bm) e = launch<256, true, false>(d, tp, grid, s);
+        else e = launch<256, true, true>(d, tp, grid, s);
+    } else {
+        if (!am && !bm) e = launch<128, false, false>(d, tp, grid, s);
+        else if (!am && bm) e = launch<128, false, true>(d, tp, grid, s);
+        else if (am && !bm) e = launch<128, true, false>(d, tp, grid, s);
+        else e = launch<128, true, true>(d, tp, grid, s);
+    }
+    if (e != cudaSuccess) return e;
+    if (nlaunch) *nlaunch = 1;
+    if (tp.splits > 1) {
+        if (nlaunch) *nlaunch = 2;
+        long nv = (long)d.M * (d.N / 4);
+        k_splitk_reduce<<<(int)((nv + 255) / 256), 256, 0, s>>>((float*)d.D, d.ldd, tp.part, d.M,
+                                                                d.N, tp.splits);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
 }  // namespace gk
