@@ -452,7 +452,7 @@ static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
         // causal attention flops: QK^T and PV over the lower triangle
         double afl = 2.0 * 2.0 * B * H * ((double)T * (T + 1) / 2) * (C / H);
         LAUNCH(K_ATTN_FWD, 1, afl, as * 4.0 * bt * c + 4.0 * B * H * T,
-               attention_forward(g->act, atty, lse, qkv, B, T, C, H, g->stream));
+               attention_forward(g->act, atty, lse, qkv, B, T, C, H, g->err, g->stream));
         d = gd(BT, C, C, atty, C, 1, pc_tensor(g, P_PROJW, l), C, 1, x1, C, EPI_RESID);
         d.bias = pc_tensor(g, P_PROJB, l);
         d.resid = resid;
@@ -594,7 +594,7 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         double afl = 2.5 * 2.0 * 2.0 * B * H * ((double)T * (T + 1) / 2) * (C / H);
         LAUNCH(K_ATTN_BWD, 3, afl, as * 8.0 * bt * c,
                attention_backward(g->act, g->dqkv, g->datty, qkv, atty, lse, B, T, C, H,
-                                  g->scratch, g->stream));
+                                  g->scratch, g->err, g->stream));
         d = gd(3 * C, C, BT, g->dqkv, 3 * C, 0, ln1, C, 0, grad_tensor(g, P_QKVW, l), C,
                EPI_ACCUM_F32);
         RUN(mm(g, K_MM_DW, d));

@@ -263,7 +263,9 @@ static cudaError_t attn_bwd_hd(void* dqkv, const void* dout, const void* qkv, co
     }
 
 cudaError_t attention_forward(int act, void* out, float* lse, const void* qkv, int B, int T_,
-                              int C, int H, cudaStream_t s) {
+                              int C, int H, unsigned* err, cudaStream_t s) {
+    if (attention_tc_supported(act, B, T_, C, H, qkv))
+        return attention_forward_tc(out, lse, qkv, B, T_, C, H, err, s);
     if (act == ACT_BF16) {
         HD_DISPATCH(attn_fwd_hd, bf16, out, lse, qkv, B, T_, C, H, s)
     } else {
@@ -277,8 +279,16 @@ size_t attention_backward_scratch(int B, int T_, int H) {
 
 cudaError_t attention_backward(int act, void* dqkv, const void* dout, const void* qkv,
                                const void* out, const float* lse, int B, int T_, int C, int H,
-                               void* scratch, cudaStream_t s) {
+                               void* scratch, unsigned* err, cudaStream_t s) {
     float* Dv = (float*)scratch;
+    if (attention_tc_supported(act, B, T_, C, H, qkv)) {
+        long n = (long)B * H * T_;
+        k_attn_D<bf16><<<(int)((n + 255) / 256), 256, 0, s>>>(Dv, (const bf16*)dout,
+                                                              (const bf16*)out, B, T_, C, H, 64);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return attention_backward_tc(dqkv, dout, qkv, lse, Dv, B, T_, C, H, err, s);
+    }
     if (act == ACT_BF16) {
         HD_DISPATCH(attn_bwd_hd, bf16, dqkv, dout, qkv, out, lse, B, T_, C, H, Dv, s)
     } else {

@@ -1,0 +1,794 @@
+// k_attn_tc.cu -- causal multi-head attention on the sm_103a tensor cores
+// (tcgen05.mma with accumulators in tensor memory, TMA tile loads), head size 64.
+//
+// Definition ("Getting started with LLMs from Andrej Karpathy's talk",
+// self-attention section): O = softmax(Q K^T / sqrt(d_k)) V per head, causal
+// (query t sees keys 0..t; later keys are left out of the softmax).  The
+// pages run attention as cuDNN FlashAttention or as two llm.c kernels
+// ("Karpathy's llm.c: understanding LLM training from scratch in C/CUDA",
+// "Code anatomy" item 2 and "Performance comparison"); here it is one fused
+// kernel per direction, written for tcgen05.
+//
+// Forward (one CTA per 128-query tile of one (batch, head); 192 threads):
+//   warp 0    TMA: the Q tile once, then K_j and V_j tiles (128 keys x 64)
+//   warp 1    TMEM (256 columns) + tcgen05.mma issue:
+//               S_j = Q K_j^T          M=128 N=128 K=64   -> TMEM cols [0,128)
+//               O_j = P_j V_j          M=128 N=64  K=128  -> TMEM cols [128,192)
+//   warps 2-5 one query row per thread: tcgen05.ld of S_j, online softmax in
+//             base 2 (running max m, sum l), P_j = exp2(S_j c - m) written as
+//             bf16 into a 128-byte-swizzled smem tile that is the A operand of
+//             the second product; O_j is read back and accumulated in
+//             registers as O = O * exp2(m_old - m_new) + O_j.
+// Keys are visited in tiles 0..q (q = the query tile); only the diagonal tile
+// needs the causal mask.  Two CTAs fit on one SM (~82 KB smem, 256 TMEM
+// columns each), so one CTA's softmax overlaps the other's products.
+// Outputs: O [B,T,C] (bf16) and the row log-sum-exp [B,H,T] (fp32, natural
+// log), which the backward pass uses to recompute P.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace gk {
+
+namespace {
+
+using namespace tc;
+
+constexpr int HD = 64;
+constexpr int TILE = 128;               // queries per CTA = keys per tile
+constexpr int TILE_BYTES = TILE * 128;  // 128 rows of 64 bf16
+constexpr int F_Q = 0, F_K = 16384, F_V = 32768, F_P = 49152, F_BAR = 81920;
+constexpr int F_SMEM = F_BAR + 256 + 1024;
+constexpr int ATT_THREADS = 192;
+
+struct AttnParams {
+    int B, T, C, H, nqt;
+    bf16* out;
+    float* lse;
+    unsigned* err;
+    float scale_log2;  // log2(e) / sqrt(hd)
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// lane 0 waits, the warp learns the outcome
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* err, int lane) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(bar, parity, abort_flag, err);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+__global__ void __launch_bounds__(ATT_THREADS) k_attn_fwd_tc(const __grid_constant__ CUtensorMap map,
+                                                             AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_gen = smem_raw + (base - raw);
+    const uint32_t sQ = base + F_Q, sK = base + F_K, sV = base + F_V, sP = base + F_P;
+    const uint32_t bar = base + F_BAR;
+    const uint32_t b_kfull = bar, b_vfull = bar + 8, b_sfull = bar + 16, b_kempty = bar + 24,
+                   b_pfull = bar + 32, b_ofull = bar + 40, b_vempty = bar + 48;
+    uint32_t* tmem_slot = (uint32_t*)(base_gen + F_BAR + 64);
+    volatile int* abort_flag = (volatile int*)(base_gen + F_BAR + 68);
+
+    const int qt = p.nqt - 1 - (int)blockIdx.x;  // longest rows first
+    const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+    const int nkt = qt + 1;
+    const int row0 = b * p.T;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_kfull, 1);
+        mbar_init(b_vfull, 1);
+        mbar_init(b_sfull, 1);
+        mbar_init(b_kempty, 1);
+        mbar_init(b_pfull, 4);
+        mbar_init(b_ofull, 1);
+        mbar_init(b_vempty, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map) : "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + 128;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------ producer
+            const int cq = h * HD, ck = p.C + h * HD, cv = 2 * p.C + h * HD;
+            mbar_expect_tx(b_kfull, 2 * TILE_BYTES);
+            tma_load_2d(sQ, &map, b_kfull, cq, row0 + qt * TILE);
+            tma_load_2d(sK, &map, b_kfull, ck, row0);
+            mbar_expect_tx(b_vfull, TILE_BYTES);
+            tma_load_2d(sV, &map, b_vfull, cv, row0);
+            int kdone = 0, vdone = 0;  // loads issued beyond the first
+            for (int j = 0; j + 1 < nkt; j++) {
+                if (!mbar_wait(b_kempty, j & 1, abort_flag, p.err)) break;
+                mbar_expect_tx(b_kfull, TILE_BYTES);
+                tma_load_2d(sK, &map, b_kfull, ck, row0 + (j + 1) * TILE);
+                kdone = j + 1;
+                if (!mbar_wait(b_vempty, j & 1, abort_flag, p.err)) break;
+                mbar_expect_tx(b_vfull, TILE_BYTES);
+                tma_load_2d(sV, &map, b_vfull, cv, row0 + (j + 1) * TILE);
+                vdone = j + 1;
+            }
+            if (*abort_flag) {
+                // let the last issued loads land before the CTA exits
+                long long t0 = clock64();
+                while (!mbar_try(b_kfull, kdone & 1) && clock64() - t0 < WAIT_LIMIT) {
+                }
+                t0 = clock64();
+                while (!mbar_try(b_vfull, vdone & 1) && clock64() - t0 < WAIT_LIMIT) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ----------------------------------------------------------- MMA
+            constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
+            constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
+            bool ok = mbar_wait(b_kfull, 0, abort_flag, p.err);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < HD / 16; k++)
+                    umma_bf16(tS, sdesc(sQ + k * 32, 0, 1024), sdesc(sK + k * 32, 0, 1024), ID_S,
+                              k > 0);
+                umma_commit(b_sfull);
+                umma_commit(b_kempty);
+            }
+            for (int j = 0; ok && j < nkt; j++) {
+                if (!mbar_wait(b_pfull, j & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                if (j + 1 < nkt) {
+                    if (!mbar_wait(b_kfull, (j + 1) & 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < HD / 16; k++)
+                        umma_bf16(tS, sdesc(sQ + k * 32, 0, 1024), sdesc(sK + k * 32, 0, 1024),
+                                  ID_S, k > 0);
+                    umma_commit(b_sfull);
+                    umma_commit(b_kempty);
+                }
+                if (!mbar_wait(b_vfull, j & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < TILE / 16; k++)
+                    umma_bf16(tO, sdesc(sP + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024),
+                              sdesc(sV + k * 2048, 8192, 1024), ID_O, k > 0);
+                umma_commit(b_ofull);
+                umma_commit(b_vempty);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- softmax
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const int qi = qt * TILE + r;
+        const uint32_t loff = (uint32_t)(q * 32) << 16;
+        float o[HD];
+#pragma unroll
+        for (int i = 0; i < HD; i++) o[i] = 0.f;
+        float m2 = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt; j++) {
+            if (j > 0 && !warp_wait(b_ofull, (j - 1) & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
+            }
+            if (!warp_wait(b_sfull, j & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (j > 0) {
+                float t[32];
+                tmem_ld32(tO + loff, t);
+#pragma unroll
+                for (int i = 0; i < 32; i++) o[i] += t[i];
+                tmem_ld32(tO + loff + 32, t);
+#pragma unroll
+                for (int i = 0; i < 32; i++) o[32 + i] += t[i];
+            }
+            const bool diag = (j == qt);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c0 = 0; c0 < TILE; c0 += 32) {
+                float s[32];
+                tmem_ld32(tS + loff + c0, s);
+#pragma unroll
+                for (int i = 0; i < 32; i++)
+                    if (!diag || c0 + i <= r) mx = fmaxf(mx, s[i] * p.scale_log2);
+            }
+            const float mn = fmaxf(m2, mx);
+            const float corr = exp2f(m2 - mn);
+            l *= corr;
+#pragma unroll
+            for (int i = 0; i < HD; i++) o[i] *= corr;
+            m2 = mn;
+#pragma unroll
+            for (int c0 = 0; c0 < TILE; c0 += 32) {
+                float s[32];
+                tmem_ld32(tS + loff + c0, s);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const int k0 = c0 + 2 * i;
+                    float a = (!diag || k0 <= r) ? exp2f(s[2 * i] * p.scale_log2 - mn) : 0.f;
+                    float c = (!diag || k0 + 1 <= r) ? exp2f(s[2 * i + 1] * p.scale_log2 - mn) : 0.f;
+                    l += a + c;
+                    pk[i] = pack_bf16x2(a, c);
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; cc++) {
+                    const int chunk = ((c0 & 63) >> 3) + cc;
+                    const uint32_t addr =
+                        sP + (c0 >> 6) * 16384 + r * 128 + ((uint32_t)(chunk ^ (r & 7)) << 4);
+                    st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pfull);
+        }
+        if (ok && warp_wait(b_ofull, (nkt - 1) & 1, abort_flag, p.err, lane)) {
+            tc_fence_after();
+            float t[32];
+            tmem_ld32(tO + loff, t);
+#pragma unroll
+            for (int i = 0; i < 32; i++) o[i] += t[i];
+            tmem_ld32(tO + loff + 32, t);
+#pragma unroll
+            for (int i = 0; i < 32; i++) o[32 + i] += t[i];
+            if (qi < p.T) {
+                const float inv = 1.f / l;
+                bf16* dst = p.out + ((size_t)(row0 + qi)) * p.C + h * HD;
+#pragma unroll
+                for (int i = 0; i < HD; i += 8) {
+                    uint4 u;
+                    u.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+                    u.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
+                    u.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
+                    u.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
+                    *reinterpret_cast<uint4*>(dst + i) = u;
+                }
+                p.lse[(size_t)bh * p.T + qi] = (m2 + log2f(l)) * 0.6931471805599453f;
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// Backward.  With P = exp(S/sqrt(hd) - lse) recomputed from the saved lse and
+// D = rowsum(dO o O):  dP = dO V^T, dS = P o (dP - D),
+//   dV = P^T dO,  dK = dS^T Q / sqrt(hd),  dQ = dS K / sqrt(hd).
+// k_attn_dkv_tc: one CTA per (128-key tile, batch, head), visiting query tiles
+//   i >= key tile.  S^T = K Q_i^T and dP^T = V dO_i^T land in TMEM; one thread
+//   per key row forms P^T and dS^T (bf16, swizzled smem), then
+//   dV += P^T dO_i and dK += dS^T Q_i accumulate in TMEM (Q_i and dO_i tiles
+//   are read K-major for the first products and MN-major for the second).
+// k_attn_dq_tc: one CTA per (128-query tile, batch, head), visiting key tiles
+//   j <= query tile: S = Q K_j^T, dP = dO V_j^T, dS -> smem, dQ += dS K_j.
+// Each CTA owns its outputs: no atomics, deterministic.  TMEM: 512 columns
+// (one CTA per SM).
+// ---------------------------------------------------------------------------
+constexpr int B_K = 0, B_V = 16384, B_Q0 = 32768, B_DO0 = 49152, B_Q1 = 65536, B_DO1 = 81920,
+              B_PT = 98304, B_DST = 131072, B_LSE = 163840, B_D = 164352, B_BAR = 164864;
+constexpr int B_SMEM = B_BAR + 256 + 1024;
+
+struct AttnBwdParams {
+    int B, T, C, H, nqt;
+    const float* lse;  // [B,H,T] natural log
+    const float* Dv;   // [B,H,T]
+    bf16* dqkv;
+    unsigned* err;
+    float scale_log2;  // log2(e)/sqrt(hd)
+    float scale;       // 1/sqrt(hd)
+};
+
+__device__ __forceinline__ void named_sync_softmax() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// write 32 values (as 16 packed bf16 pairs) of row r into a 128x128 bf16
+// K-major swizzled tile (two 64-column atoms of 16 KB)
+__device__ __forceinline__ void st_row32(uint32_t tile, int r, int c0, const uint32_t* pk) {
+#pragma unroll
+    for (int cc = 0; cc < 4; cc++) {
+        const int chunk = ((c0 & 63) >> 3) + cc;
+        const uint32_t addr = tile + (c0 >> 6) * 16384 + r * 128 + ((uint32_t)(chunk ^ (r & 7)) << 4);
+        st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+    }
+}
+
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    k_attn_dkv_tc(const __grid_constant__ CUtensorMap map_qkv,
+                  const __grid_constant__ CUtensorMap map_do, AttnBwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_gen = smem_raw + (base - raw);
+    const uint32_t sK = base + B_K, sV = base + B_V, sPT = base + B_PT, sDST = base + B_DST;
+    float* lse_s = (float*)(base_gen + B_LSE);
+    float* d_s = (float*)(base_gen + B_D);
+    const uint32_t bar = base + B_BAR;
+    const uint32_t b_kv = bar, b_qdf0 = bar + 8, b_qdf1 = bar + 16, b_qde0 = bar + 24,
+                   b_qde1 = bar + 32, b_sfull = bar + 40, b_psfull = bar + 48,
+                   b_psfree = bar + 56, b_acc = bar + 64;
+    uint32_t* tmem_slot = (uint32_t*)(base_gen + B_BAR + 128);
+    volatile int* abort_flag = (volatile int*)(base_gen + B_BAR + 132);
+
+    const int kt = p.nqt - 1 - (int)blockIdx.x;  // fewest query tiles last
+    const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+    const int nq = p.nqt - kt;  // query tiles kt..nqt-1
+    const int row0 = b * p.T;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_kv, 1);
+        mbar_init(b_qdf0, 1);
+        mbar_init(b_qdf1, 1);
+        mbar_init(b_qde0, 1);
+        mbar_init(b_qde1, 1);
+        mbar_init(b_sfull, 1);
+        mbar_init(b_psfull, 4);
+        mbar_init(b_psfree, 1);
+        mbar_init(b_acc, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tST = tmem, tDPT = tmem + 128, tDV = tmem + 256, tDK = tmem + 320;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const int cq = h * HD, ck = p.C + h * HD, cv = 2 * p.C + h * HD;
+            mbar_expect_tx(b_kv, 2 * TILE_BYTES);
+            tma_load_2d(sK, &map_qkv, b_kv, ck, row0 + kt * TILE);
+            tma_load_2d(sV, &map_qkv, b_kv, cv, row0 + kt * TILE);
+            int issued[2] = {-1, -1};
+            for (int n = 0; n < nq; n++) {
+                const int s = n & 1, u = n >> 1;
+                const uint32_t fe = s ? b_qde1 : b_qde0, ff = s ? b_qdf1 : b_qdf0;
+                if (!mbar_wait(fe, (u & 1) ^ 1, abort_flag, p.err)) break;
+                const uint32_t sq = base + (s ? B_Q1 : B_Q0), sd = base + (s ? B_DO1 : B_DO0);
+                const int qrow = row0 + (kt + n) * TILE;
+                mbar_expect_tx(ff, 2 * TILE_BYTES);
+                tma_load_2d(sq, &map_qkv, ff, cq, qrow);
+                tma_load_2d(sd, &map_do, ff, h * HD, qrow);
+                issued[s] = u;
+            }
+            if (*abort_flag) {
+                for (int s = 0; s < 2; s++) {
+                    if (issued[s] < 0) continue;
+                    long long t0 = clock64();
+                    while (!mbar_try(s ? b_qdf1 : b_qdf0, issued[s] & 1) &&
+                           clock64() - t0 < WAIT_LIMIT) {
+                    }
+                }
+                long long t0 = clock64();
+                while (!mbar_try(b_kv, 0) && clock64() - t0 < WAIT_LIMIT) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
+            constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
+            bool ok = mbar_wait(b_kv, 0, abort_flag, p.err);
+            for (int n = 0; ok && n < nq; n++) {
+                const int s = n & 1, u = n >> 1;
+                if (!mbar_wait(s ? b_qdf1 : b_qdf0, u & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t sq = base + (s ? B_Q1 : B_Q0), sd = base + (s ? B_DO1 : B_DO0);
+#pragma unroll
+                for (int k = 0; k < HD / 16; k++)
+                    umma_bf16(tST, sdesc(sK + k * 32, 0, 1024), sdesc(sq + k * 32, 0, 1024), ID_S,
+                              k > 0);
+#pragma unroll
+                for (int k = 0; k < HD / 16; k++)
+                    umma_bf16(tDPT, sdesc(sV + k * 32, 0, 1024), sdesc(sd + k * 32, 0, 1024),
+                              ID_S, k > 0);
+                umma_commit(b_sfull);
+                if (!mbar_wait(b_psfull, n & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < TILE / 16; k++) {
+                    const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
+                    umma_bf16(tDV, sdesc(sPT + aoff, 0, 1024), sdesc(sd + k * 2048, 8192, 1024),
+                              ID_O, (n > 0 || k > 0));
+                    umma_bf16(tDK, sdesc(sDST + aoff, 0, 1024), sdesc(sq + k * 2048, 8192, 1024),
+                              ID_O, (n > 0 || k > 0));
+                }
+                umma_commit(s ? b_qde1 : b_qde0);
+                umma_commit(b_psfree);
+            }
+            if (ok) umma_commit(b_acc);
+        }
+    } else {
+        const int q = warp & 3;
+        const int r = q * 32 + lane;   // key row within the tile
+        const int kj = kt * TILE + r;  // key index in the sequence
+        const int tid = threadIdx.x - 64;
+        const uint32_t loff = (uint32_t)(q * 32) << 16;
+        bool ok = true;
+        for (int n = 0; n < nq; n++) {
+            const int i = kt + n;
+            named_sync_softmax();  // everyone is done with the previous lse/D
+            {
+                const int qi = i * TILE + tid;
+                lse_s[tid] = qi < p.T ? p.lse[(size_t)bh * p.T + qi] * 1.4426950408889634f : 0.f;
+                d_s[tid] = qi < p.T ? p.Dv[(size_t)bh * p.T + qi] : 0.f;
+            }
+            named_sync_softmax();
+            if (!warp_wait(b_sfull, n & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
+            }
+            if (n > 0 && !warp_wait(b_psfree, (n - 1) & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int qbase = i * TILE;
+#pragma unroll 1
+            for (int c0 = 0; c0 < TILE; c0 += 32) {
+                float sv[32], dp[32];
+                tmem_ld32(tST + loff + c0, sv);
+                tmem_ld32(tDPT + loff + c0, dp);
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int z = 0; z < 2; z++) {
+                        const int c = c0 + 2 * e + z;
+                        const int qi = qbase + c;
+                        const bool live = qi < p.T && kj <= qi;
+                        const float pr = live ? exp2f(sv[2 * e + z] * p.scale_log2 - lse_s[c]) : 0.f;
+                        pv[z] = pr;
+                        dv[z] = live ? pr * (dp[2 * e + z] - d_s[c]) : 0.f;
+                    }
+                    pp[e] = pack_bf16x2(pv[0], pv[1]);
+                    dd[e] = pack_bf16x2(dv[0], dv[1]);
+                }
+                st_row32(sPT, r, c0, pp);
+                st_row32(sDST, r, c0, dd);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_psfull);
+        }
+        if (ok && warp_wait(b_acc, 0, abort_flag, p.err, lane)) {
+            tc_fence_after();
+            bf16* dst = p.dqkv + (size_t)(row0 + kj) * 3 * p.C + h * HD;
+#pragma unroll 1
+            for (int half = 0; half < 2; half++) {
+                float v[32], k[32];
+                tmem_ld32(tDV + loff + half * 32, v);
+                tmem_ld32(tDK + loff + half * 32, k);
+                if (kj < p.T) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 uv, uk;
+                        uv.x = pack_bf16x2(v[e], v[e + 1]);
+                        uv.y = pack_bf16x2(v[e + 2], v[e + 3]);
+                        uv.z = pack_bf16x2(v[e + 4], v[e + 5]);
+                        uv.w = pack_bf16x2(v[e + 6], v[e + 7]);
+                        uk.x = pack_bf16x2(k[e] * p.scale, k[e + 1] * p.scale);
+                        uk.y = pack_bf16x2(k[e + 2] * p.scale, k[e + 3] * p.scale);
+                        uk.z = pack_bf16x2(k[e + 4] * p.scale, k[e + 5] * p.scale);
+                        uk.w = pack_bf16x2(k[e + 6] * p.scale, k[e + 7] * p.scale);
+                        *reinterpret_cast<uint4*>(dst + 2 * p.C + half * 32 + e) = uv;
+                        *reinterpret_cast<uint4*>(dst + p.C + half * 32 + e) = uk;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+constexpr int Q_Q = 0, Q_DO = 16384, Q_K0 = 32768, Q_V0 = 49152, Q_K1 = 65536, Q_V1 = 81920,
+              Q_DS = 98304, Q_BAR = 131072;
+constexpr int Q_SMEM = Q_BAR + 256 + 1024;
+
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    k_attn_dq_tc(const __grid_constant__ CUtensorMap map_qkv,
+                 const __grid_constant__ CUtensorMap map_do, AttnBwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_gen = smem_raw + (base - raw);
+    const uint32_t sQ = base + Q_Q, sDO = base + Q_DO, sDS = base + Q_DS;
+    const uint32_t bar = base + Q_BAR;
+    const uint32_t b_q = bar, b_kvf0 = bar + 8, b_kvf1 = bar + 16, b_kve0 = bar + 24,
+                   b_kve1 = bar + 32, b_sfull = bar + 40, b_dsfull = bar + 48,
+                   b_dsfree = bar + 56, b_acc = bar + 64;
+    uint32_t* tmem_slot = (uint32_t*)(base_gen + Q_BAR + 128);
+    volatile int* abort_flag = (volatile int*)(base_gen + Q_BAR + 132);
+
+    const int qt = p.nqt - 1 - (int)blockIdx.x;
+    const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+    const int nkt = qt + 1;
+    const int row0 = b * p.T;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_q, 1);
+        mbar_init(b_kvf0, 1);
+        mbar_init(b_kvf1, 1);
+        mbar_init(b_kve0, 1);
+        mbar_init(b_kve1, 1);
+        mbar_init(b_sfull, 1);
+        mbar_init(b_dsfull, 4);
+        mbar_init(b_dsfree, 1);
+        mbar_init(b_acc, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const int cq = h * HD, ck = p.C + h * HD, cv = 2 * p.C + h * HD;
+            mbar_expect_tx(b_q, 2 * TILE_BYTES);
+            tma_load_2d(sQ, &map_qkv, b_q, cq, row0 + qt * TILE);
+            tma_load_2d(sDO, &map_do, b_q, h * HD, row0 + qt * TILE);
+            int issued[2] = {-1, -1};
+            for (int j = 0; j < nkt; j++) {
+                const int s = j & 1, u = j >> 1;
+                const uint32_t fe = s ? b_kve1 : b_kve0, ff = s ? b_kvf1 : b_kvf0;
+                if (!mbar_wait(fe, (u & 1) ^ 1, abort_flag, p.err)) break;
+                const uint32_t sk = base + (s ? Q_K1 : Q_K0), sv = base + (s ? Q_V1 : Q_V0);
+                mbar_expect_tx(ff, 2 * TILE_BYTES);
+                tma_load_2d(sk, &map_qkv, ff, ck, row0 + j * TILE);
+                tma_load_2d(sv, &map_qkv, ff, cv, row0 + j * TILE);
+                issued[s] = u;
+            }
+            if (*abort_flag) {
+                for (int s = 0; s < 2; s++) {
+                    if (issued[s] < 0) continue;
+                    long long t0 = clock64();
+                    while (!mbar_try(s ? b_kvf1 : b_kvf0, issued[s] & 1) &&
+                           clock64() - t0 < WAIT_LIMIT) {
+                    }
+                }
+                long long t0 = clock64();
+                while (!mbar_try(b_q, 0) && clock64() - t0 < WAIT_LIMIT) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
+            constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
+            bool ok = mbar_wait(b_q, 0, abort_flag, p.err);
+            for (int j = 0; ok && j < nkt; j++) {
+                const int s = j & 1, u = j >> 1;
+                if (!mbar_wait(s ? b_kvf1 : b_kvf0, u & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t sk = base + (s ? Q_K1 : Q_K0), sv = base + (s ? Q_V1 : Q_V0);
+#pragma unroll
+                for (int k = 0; k < HD / 16; k++)
+                    umma_bf16(tS, sdesc(sQ + k * 32, 0, 1024), sdesc(sk + k * 32, 0, 1024), ID_S,
+                              k > 0);
+#pragma unroll
+                for (int k = 0; k < HD / 16; k++)
+                    umma_bf16(tDP, sdesc(sDO + k * 32, 0, 1024), sdesc(sv + k * 32, 0, 1024),
+                              ID_S, k > 0);
+                umma_commit(b_sfull);
+                if (!mbar_wait(b_dsfull, j & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < TILE / 16; k++)
+                    umma_bf16(tDQ, sdesc(sDS + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024),
+                              sdesc(sk + k * 2048, 8192, 1024), ID_O, (j > 0 || k > 0));
+                umma_commit(s ? b_kve1 : b_kve0);
+                umma_commit(b_dsfree);
+            }
+            if (ok) umma_commit(b_acc);
+        }
+    } else {
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const int qi = qt * TILE + r;
+        const uint32_t loff = (uint32_t)(q * 32) << 16;
+        const bool qlive = qi < p.T;
+        const float lse2 = qlive ? p.lse[(size_t)bh * p.T + qi] * 1.4426950408889634f : 0.f;
+        const float Dq = qlive ? p.Dv[(size_t)bh * p.T + qi] : 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt; j++) {
+            if (!warp_wait(b_sfull, j & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
+            }
+            if (j > 0 && !warp_wait(b_dsfree, (j - 1) & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int kbase = j * TILE;
+#pragma unroll 1
+            for (int c0 = 0; c0 < TILE; c0 += 32) {
+                float sv[32], dp[32];
+                tmem_ld32(tS + loff + c0, sv);
+                tmem_ld32(tDP + loff + c0, dp);
+                uint32_t dd[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    float dv[2];
+#pragma unroll
+                    for (int z = 0; z < 2; z++) {
+                        const int kk = kbase + c0 + 2 * e + z;
+                        const bool live = qlive && kk <= qi;
+                        const float pr = live ? exp2f(sv[2 * e + z] * p.scale_log2 - lse2) : 0.f;
+                        dv[z] = live ? pr * (dp[2 * e + z] - Dq) : 0.f;
+                    }
+                    dd[e] = pack_bf16x2(dv[0], dv[1]);
+                }
+                st_row32(sDS, r, c0, dd);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_dsfull);
+        }
+        if (ok && warp_wait(b_acc, 0, abort_flag, p.err, lane)) {
+            tc_fence_after();
+            bf16* dst = p.dqkv + (size_t)(row0 + qi) * 3 * p.C + h * HD;
+#pragma unroll 1
+            for (int half = 0; half < 2; half++) {
+                float v[32];
+                tmem_ld32(tDQ + loff + half * 32, v);
+                if (qlive) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 u;
+                        u.x = pack_bf16x2(v[e] * p.scale, v[e + 1] * p.scale);
+                        u.y = pack_bf16x2(v[e + 2] * p.scale, v[e + 3] * p.scale);
+                        u.z = pack_bf16x2(v[e + 4] * p.scale, v[e + 5] * p.scale);
+                        u.w = pack_bf16x2(v[e + 6] * p.scale, v[e + 7] * p.scale);
+                        *reinterpret_cast<uint4*>(dst + half * 32 + e) = u;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace
+
+bool attention_tc_supported(int act, int B, int T, int C, int H, const void* qkv) {
+    if (act != ACT_BF16 || H < 1 || C % H || C / H != HD || C % 8) return false;
+    if (((uintptr_t)qkv & 15) != 0) return false;
+    if ((long)B * T >= (1L << 31) - 256) return false;
+    return tc_encode_fn() != nullptr;
+}
+
+static bool map_rows(CUtensorMap* m, const void* base, long width, long rows) {
+    EncodeTiledFn enc = (EncodeTiledFn)tc_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)width * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const float* lse,
+                                  const float* Dv, int B, int T, int C, int H, unsigned* err,
+                                  cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_attn_dkv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM);
+        cudaFuncSetAttribute(k_attn_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM);
+        attr = true;
+    }
+    if (((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15)) return cudaErrorInvalidValue;
+    CUtensorMap mq, md;
+    if (!map_rows(&mq, qkv, 3L * C, (long)B * T) || !map_rows(&md, dout, C, (long)B * T))
+        return cudaErrorInvalidValue;
+    AttnBwdParams p;
+    p.B = B; p.T = T; p.C = C; p.H = H;
+    p.nqt = (T + TILE - 1) / TILE;
+    p.lse = lse;
+    p.Dv = Dv;
+    p.dqkv = (bf16*)dqkv;
+    p.err = err;
+    p.scale = 1.0f / sqrtf((float)HD);
+    p.scale_log2 = 1.4426950408889634f * p.scale;
+    dim3 grid(p.nqt, B * H);
+    k_attn_dkv_tc<<<grid, ATT_THREADS, B_SMEM, s>>>(mq, md, p);
+    k_attn_dq_tc<<<grid, ATT_THREADS, Q_SMEM, s>>>(mq, md, p);
+    return cudaGetLastError();
+}
+
+cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C,
+                                 int H, unsigned* err, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+        attr = true;
+    }
+    EncodeTiledFn enc = (EncodeTiledFn)tc_encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap map;
+    cuuint64_t dims[2] = {(cuuint64_t)3 * C, (cuuint64_t)B * T};
+    cuuint64_t strides[1] = {(cuuint64_t)3 * C * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    AttnParams p;
+    p.B = B; p.T = T; p.C = C; p.H = H;
+    p.nqt = (T + TILE - 1) / TILE;
+    p.out = (bf16*)out;
+    p.lse = lse;
+    p.err = err;
+    p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+    dim3 grid(p.nqt, B * H);
+    k_attn_fwd_tc<<<grid, ATT_THREADS, F_SMEM, s>>>(map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace gk

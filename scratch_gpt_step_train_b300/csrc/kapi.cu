@@ -46,7 +46,7 @@ extern "C" int gpt2k_matmul(int dtype, int impl, int M, int N, int K, const void
 extern "C" int gpt2k_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B,
                                        int T, int C, int H, void* stream) {
     if (!dt_ok(dtype) || B < 1 || T < 1 || H < 1 || C % H) return GPT2_ERR_ARG;
-    return rc_of(attention_forward(dtype, out, lse, qkv, B, T, C, H, (cudaStream_t)stream));
+    return rc_of(attention_forward(dtype, out, lse, qkv, B, T, C, H, nullptr, (cudaStream_t)stream));
 }
 
 extern "C" size_t gpt2k_attention_backward_scratch_bytes(int B, int T, int C, int H) {
@@ -59,7 +59,7 @@ extern "C" int gpt2k_attention_backward(int dtype, void* dqkv, const void* dout,
                                         int H, void* scratch, void* stream) {
     if (!dt_ok(dtype) || B < 1 || T < 1 || H < 1 || C % H || !scratch) return GPT2_ERR_ARG;
     return rc_of(attention_backward(dtype, dqkv, dout, qkv, out, lse, B, T, C, H, scratch,
-                                    (cudaStream_t)stream));
+                                    nullptr, (cudaStream_t)stream));
 }
 
 extern "C" int gpt2k_layernorm_forward(int dtype, void* out, float* mean, float* rstd,

@@ -100,13 +100,22 @@ struct GemmDesc {
 cudaError_t gemm_simt(const GemmDesc& d, cudaStream_t s);
 
 // ---- attention (causal, softmax(Q K^T / sqrt(hd)) V) --------------------------
-// qkv [B,T,3C]; out [B,T,C]; lse [B,H,T] fp32
+// qkv [B,T,3C]; out [B,T,C]; lse [B,H,T] fp32.  bf16 with head size 64 runs
+// on the tensor cores (k_attn_tc.cu), everything else on the FFMA kernels.
+// err (may be NULL) receives GPT2_DEVERR_TIMEOUT from a bounded wait.
 cudaError_t attention_forward(int act, void* out, float* lse, const void* qkv, int B, int T,
-                              int C, int H, cudaStream_t s);
+                              int C, int H, unsigned* err, cudaStream_t s);
+bool attention_tc_supported(int act, int B, int T, int C, int H, const void* qkv);
+cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C,
+                                 int H, unsigned* err, cudaStream_t s);
+cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const float* lse,
+                                  const float* Dv, int B, int T, int C, int H, unsigned* err,
+                                  cudaStream_t s);
+void* tc_encode_fn();
 size_t attention_backward_scratch(int B, int T, int H);
 // dqkv [B,T,3C] is overwritten
 cudaError_t attention_backward(int act, void* dqkv, const void* dout, const void* qkv,
                                const void* out, const float* lse, int B, int T, int C, int H,
-                               void* scratch, cudaStream_t s);
+                               void* scratch, unsigned* err, cudaStream_t s);
 
 }  // namespace gk

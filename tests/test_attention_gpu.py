@@ -1,0 +1,157 @@
+"""Parity of causal attention (forward and backward) against the oracle's
+attention (fp64) on the same bf16-rounded qkv.
+
+bf16 path (tensor cores, head size 64): the probabilities P pass through bf16
+before the P.V product and the output is rounded to bf16, so the per-element
+bound is 2^-8 (sum_j a_ij |v_j|) + 2^-8 |o_i| (a = the exact attention
+weights).  fp32 path: rel 1e-4 (see tests/parity.py)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.pyoracle import Ops
+from scratch_gpt_step_train_b300 import kernels as K
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+ops = Ops("double")
+
+
+def _qkv(B, T, C, seed, qscale=1.0, dtype=torch.bfloat16):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0, 1, (B, T, 3 * C))
+    x[..., :C] *= qscale
+    t = torch.from_numpy(x.astype(np.float32)).to(dtype).cuda()
+    return t, t.double().cpu().numpy()
+
+
+def _fwd(qkv, B, T, C, H):
+    out = torch.empty(B, T, C, dtype=qkv.dtype, device="cuda")
+    lse = torch.empty(B, H, T, dtype=torch.float32, device="cuda")
+    K.attention_forward(out, lse, qkv, B, T, C, H)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _lse_ref(q64, att, C, H):
+    """lse_t = s_tt - log(a_tt): the diagonal score is always in the softmax"""
+    B, T, _ = q64.shape
+    hd = C // H
+    out = np.zeros((B, H, T))
+    for h in range(H):
+        q = q64[..., h * hd:(h + 1) * hd]
+        k = q64[..., C + h * hd:C + (h + 1) * hd]
+        s = (q * k).sum(-1) / np.sqrt(hd)
+        d = np.diagonal(att[:, h], axis1=1, axis2=2)
+        out[:, h] = s - np.log(d)
+    return out
+
+
+SHAPES = [(2, 200, 192, 3), (1, 128, 64, 1), (3, 37, 128, 2), (1, 300, 64, 1)]
+
+
+@pytest.mark.parametrize("B,T,C,H", SHAPES, ids=["ragged", "one-tile", "short", "three-tiles"])
+@pytest.mark.parametrize("qscale", [1.0, 4.0], ids=["mild", "peaky"])
+def test_attention_forward_bf16(B, T, C, H, qscale):
+    qkv, q64 = _qkv(B, T, C, 1, qscale)
+    out, lse = _fwd(qkv, B, T, C, H)
+    ref, att = ops.attention_forward(q64, H)
+    a = q64.copy()
+    a[..., 2 * C:] = np.abs(a[..., 2 * C:])
+    refabs, _ = ops.attention_forward(a, H)
+    got = out.double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * (refabs + np.abs(ref)) + 1e-7)
+    assert np.abs(lse.double().cpu().numpy() - _lse_ref(q64, att, C, H)).max() < 2e-4
+
+
+@pytest.mark.parametrize("B,T,C,H", SHAPES[:3], ids=["ragged", "one-tile", "short"])
+def test_attention_forward_fp32(B, T, C, H):
+    qkv, q64 = _qkv(B, T, C, 2, 1.0, torch.float32)
+    out, lse = _fwd(qkv, B, T, C, H)
+    ref, att = ops.attention_forward(q64, H)
+    assert_close(out.double().cpu().numpy(), ref, 1e-4, "out")
+    assert np.abs(lse.double().cpu().numpy() - _lse_ref(q64, att, C, H)).max() < 1e-4
+
+
+def test_attention_forward_full_size_sampled():
+    """GPT-2 124M shape at micro-batch 16 x 1024: the oracle recomputes one
+    sequence (all 12 heads)"""
+    B, T, C, H = 16, 1024, 768, 12
+    qkv, _ = _qkv(B, T, C, 3)
+    out, lse = _fwd(qkv, B, T, C, H)
+    b = 9
+    q64 = qkv[b:b + 1].double().cpu().numpy()
+    ref, att = ops.attention_forward(q64, H)
+    a = q64.copy()
+    a[..., 2 * C:] = np.abs(a[..., 2 * C:])
+    refabs, _ = ops.attention_forward(a, H)
+    got = out[b:b + 1].double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * (refabs + np.abs(ref)) + 1e-7)
+    assert np.abs(lse[b:b + 1].double().cpu().numpy() - _lse_ref(q64, att, C, H)).max() < 2e-4
+
+
+def _bwd(qkv, dout, out, lse, B, T, C, H):
+    dqkv = torch.full_like(qkv, float("nan"))
+    K.attention_backward(dqkv, dout, qkv, out, lse, B, T, C, H)
+    torch.cuda.synchronize()
+    return dqkv
+
+
+def _check_bwd_bf16(got, ref, C, what):
+    """P and dS pass through bf16 before their products and the outputs are
+    rounded to bf16: each of dQ, dK, dV within 1e-2 of the oracle in L2 norm
+    and 3e-2 of its largest entry elementwise"""
+    for part, sl in (("dq", slice(0, C)), ("dk", slice(C, 2 * C)), ("dv", slice(2 * C, 3 * C))):
+        g, r = got[..., sl], ref[..., sl]
+        e2 = np.linalg.norm(g - r) / np.linalg.norm(r)
+        emax = np.abs(g - r).max() / np.abs(r).max()
+        assert e2 <= 1e-2 and emax <= 3e-2, (what, part, e2, emax)
+
+
+@pytest.mark.parametrize("B,T,C,H", SHAPES, ids=["ragged", "one-tile", "short", "three-tiles"])
+def test_attention_backward_bf16(B, T, C, H):
+    qkv, q64 = _qkv(B, T, C, 4, 2.0)
+    out, lse = _fwd(qkv, B, T, C, H)
+    dout = torch.from_numpy(np.random.default_rng(5).normal(0, 1, (B, T, C)).astype(np.float32))
+    dout = dout.to(torch.bfloat16).cuda()
+    dqkv = _bwd(qkv, dout, out, lse, B, T, C, H)
+    _, att = ops.attention_forward(q64, H)
+    ref = ops.attention_backward(dout.double().cpu().numpy(), q64, att, H)
+    got = dqkv.double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    _check_bwd_bf16(got, ref, C, (B, T, C, H))
+
+
+@pytest.mark.parametrize("B,T,C,H", SHAPES[:3], ids=["ragged", "one-tile", "short"])
+def test_attention_backward_fp32(B, T, C, H):
+    qkv, q64 = _qkv(B, T, C, 6, 1.0, torch.float32)
+    out, lse = _fwd(qkv, B, T, C, H)
+    dout = torch.from_numpy(np.random.default_rng(7).normal(0, 1, (B, T, C)).astype(np.float32)).cuda()
+    dqkv = _bwd(qkv, dout, out, lse, B, T, C, H)
+    _, att = ops.attention_forward(q64, H)
+    ref = ops.attention_backward(dout.double().cpu().numpy(), q64, att, H)
+    assert_close(dqkv.double().cpu().numpy(), ref, 1e-4, "dqkv")
+
+
+def test_attention_backward_full_size_sampled():
+    B, T, C, H = 16, 1024, 768, 12
+    qkv, _ = _qkv(B, T, C, 8)
+    out, lse = _fwd(qkv, B, T, C, H)
+    dout = (torch.randn(B, T, C, generator=torch.Generator(device="cuda").manual_seed(9),
+                        device="cuda")).to(torch.bfloat16)
+    dqkv = _bwd(qkv, dout, out, lse, B, T, C, H)
+    b = 13
+    q64 = qkv[b:b + 1].double().cpu().numpy()
+    _, att = ops.attention_forward(q64, H)
+    ref = ops.attention_backward(dout[b:b + 1].double().cpu().numpy(), q64, att, H)
+    _check_bwd_bf16(dqkv[b:b + 1].double().cpu().numpy(), ref, C, "full")
+
+
+def test_attention_backward_deterministic():
+    B, T, C, H = 2, 300, 128, 2
+    qkv, _ = _qkv(B, T, C, 10)
+    out, lse = _fwd(qkv, B, T, C, H)
+    dout = torch.randn(B, T, C, device="cuda").to(torch.bfloat16)
+    a = _bwd(qkv, dout, out, lse, B, T, C, H)
+    b = _bwd(qkv, dout, out, lse, B, T, C, H)
+    assert torch.equal(a, b)
