@@ -37,9 +37,12 @@ using namespace tc;
 constexpr int HD = 64;
 constexpr int TILE = 128;               // queries per CTA = keys per tile
 constexpr int TILE_BYTES = TILE * 128;  // 128 rows of 64 bf16
-constexpr int F_Q = 0, F_K = 16384, F_V = 32768, F_P = 49152, F_BAR = 81920;
+constexpr int ATT_THREADS = 320;        // TMA warp, MMA warp, 8 softmax warps
+// forward smem: Q, a ring of 3 K/V slots (K_0 V_0 K_1 V_1 ... in order), P,
+// then the row-max exchange, the final row-sum exchange and the barriers
+constexpr int F_Q = 0, F_RING = 16384, F_P = 65536, F_RED = 98304, F_LS = 99328,
+              F_BAR = 100352;
 constexpr int F_SMEM = F_BAR + 256 + 1024;
-constexpr int ATT_THREADS = 192;
 
 struct AttnParams {
     int B, T, C, H, nqt;
@@ -62,18 +65,37 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-__global__ void __launch_bounds__(ATT_THREADS) k_attn_fwd_tc(const __grid_constant__ CUtensorMap map,
+// the 8 softmax warps (256 threads) synchronise among themselves
+__device__ __forceinline__ void named_sync_softmax() {
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// write 32 values (16 packed bf16 pairs) of row r, columns [c0, c0+32), into a
+// 128x128 bf16 K-major tile with 128-byte swizzle (two 64-column atoms)
+__device__ __forceinline__ void st_row32(uint32_t tile, int r, int c0, const uint32_t* pk) {
+#pragma unroll
+    for (int cc = 0; cc < 4; cc++) {
+        const int chunk = ((c0 & 63) >> 3) + cc;
+        const uint32_t addr = tile + (c0 >> 6) * 16384 + r * 128 + ((uint32_t)(chunk ^ (r & 7)) << 4);
+        st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+    }
+}
+
+__global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_constant__ CUtensorMap map,
                                                              AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw);
-    const uint32_t sQ = base + F_Q, sK = base + F_K, sV = base + F_V, sP = base + F_P;
+    const uint32_t sQ = base + F_Q, sRing = base + F_RING, sP = base + F_P;
+    float* red = (float*)(base_gen + F_RED);  // [2 buffers][2 halves][128 rows]
+    float* lsum = (float*)(base_gen + F_LS);  // [2 halves][128 rows]
     const uint32_t bar = base + F_BAR;
-    const uint32_t b_kfull = bar, b_vfull = bar + 8, b_sfull = bar + 16, b_kempty = bar + 24,
-                   b_pfull = bar + 32, b_ofull = bar + 40, b_vempty = bar + 48;
-    uint32_t* tmem_slot = (uint32_t*)(base_gen + F_BAR + 64);
-    volatile int* abort_flag = (volatile int*)(base_gen + F_BAR + 68);
+    // full[3], empty[3] for the ring; q; s (S ready); pf (P ready); o (O_j ready)
+    const uint32_t b_full = bar, b_empty = bar + 24, b_q = bar + 48, b_sfull = bar + 56,
+                   b_pfull = bar + 64, b_ofull = bar + 72;
+    uint32_t* tmem_slot = (uint32_t*)(base_gen + F_BAR + 128);
+    volatile int* abort_flag = (volatile int*)(base_gen + F_BAR + 132);
 
     const int qt = p.nqt - 1 - (int)blockIdx.x;  // longest rows first
     const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
@@ -82,13 +104,14 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_fwd_tc(const __grid_consta
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(b_kfull, 1);
-        mbar_init(b_vfull, 1);
+        for (int i = 0; i < 3; i++) {
+            mbar_init(b_full + 8 * i, 1);
+            mbar_init(b_empty + 8 * i, 1);
+        }
+        mbar_init(b_q, 1);
         mbar_init(b_sfull, 1);
-        mbar_init(b_kempty, 1);
-        mbar_init(b_pfull, 4);
+        mbar_init(b_pfull, 8);
         mbar_init(b_ofull, 1);
-        mbar_init(b_vempty, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map) : "memory");
@@ -106,30 +129,30 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_fwd_tc(const __grid_consta
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------ producer
-            const int cq = h * HD, ck = p.C + h * HD, cv = 2 * p.C + h * HD;
-            mbar_expect_tx(b_kfull, 2 * TILE_BYTES);
-            tma_load_2d(sQ, &map, b_kfull, cq, row0 + qt * TILE);
-            tma_load_2d(sK, &map, b_kfull, ck, row0);
-            mbar_expect_tx(b_vfull, TILE_BYTES);
-            tma_load_2d(sV, &map, b_vfull, cv, row0);
-            int kdone = 0, vdone = 0;  // loads issued beyond the first
-            for (int j = 0; j + 1 < nkt; j++) {
-                if (!mbar_wait(b_kempty, j & 1, abort_flag, p.err)) break;
-                mbar_expect_tx(b_kfull, TILE_BYTES);
-                tma_load_2d(sK, &map, b_kfull, ck, row0 + (j + 1) * TILE);
-                kdone = j + 1;
-                if (!mbar_wait(b_vempty, j & 1, abort_flag, p.err)) break;
-                mbar_expect_tx(b_vfull, TILE_BYTES);
-                tma_load_2d(sV, &map, b_vfull, cv, row0 + (j + 1) * TILE);
-                vdone = j + 1;
+            const int ck = p.C + h * HD, cv = 2 * p.C + h * HD;
+            mbar_expect_tx(b_q, TILE_BYTES);
+            tma_load_2d(sQ, &map, b_q, h * HD, row0 + qt * TILE);
+            int last0 = -1, last1 = -1, last2 = -1;  // use count of each slot's last load
+            for (int it = 0; it < 2 * nkt; it++) {
+                const int s = it % 3, u = it / 3;
+                if (!mbar_wait(b_empty + 8 * s, (u & 1) ^ 1, abort_flag, p.err)) break;
+                mbar_expect_tx(b_full + 8 * s, TILE_BYTES);
+                tma_load_2d(sRing + s * TILE_BYTES, &map, b_full + 8 * s, (it & 1) ? cv : ck,
+                            row0 + (it >> 1) * TILE);
+                if (s == 0) last0 = u;
+                else if (s == 1) last1 = u;
+                else last2 = u;
             }
             if (*abort_flag) {
-                // let the last issued loads land before the CTA exits
-                long long t0 = clock64();
-                while (!mbar_try(b_kfull, kdone & 1) && clock64() - t0 < WAIT_LIMIT) {
+                for (int s = 0; s < 3; s++) {
+                    const int ls = s == 0 ? last0 : (s == 1 ? last1 : last2);
+                    if (ls < 0) continue;
+                    long long t0 = clock64();
+                    while (!mbar_try(b_full + 8 * s, ls & 1) && clock64() - t0 < WAIT_LIMIT) {
+                    }
                 }
-                t0 = clock64();
-                while (!mbar_try(b_vfull, vdone & 1) && clock64() - t0 < WAIT_LIMIT) {
+                long long t0 = clock64();
+                while (!mbar_try(b_q, 0) && clock64() - t0 < WAIT_LIMIT) {
                 }
             }
         }
@@ -138,48 +161,48 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_fwd_tc(const __grid_consta
             // ----------------------------------------------------------- MMA
             constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
-            bool ok = mbar_wait(b_kfull, 0, abort_flag, p.err);
-            if (ok) {
+            auto issue_s = [&](int j) -> bool {
+                const int it = 2 * j, s = it % 3;
+                if (!mbar_wait(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
+                const uint32_t sk = sRing + s * TILE_BYTES;
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
-                    umma_bf16(tS, sdesc(sQ + k * 32, 0, 1024), sdesc(sK + k * 32, 0, 1024), ID_S,
+                    umma_bf16(tS, sdesc(sQ + k * 32, 0, 1024), sdesc(sk + k * 32, 0, 1024), ID_S,
                               k > 0);
                 umma_commit(b_sfull);
-                umma_commit(b_kempty);
-            }
+                umma_commit(b_empty + 8 * s);
+                return true;
+            };
+            bool ok = mbar_wait(b_q, 0, abort_flag, p.err) && issue_s(0);
             for (int j = 0; ok && j < nkt; j++) {
                 if (!mbar_wait(b_pfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                if (j + 1 < nkt) {
-                    if (!mbar_wait(b_kfull, (j + 1) & 1, abort_flag, p.err)) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < HD / 16; k++)
-                        umma_bf16(tS, sdesc(sQ + k * 32, 0, 1024), sdesc(sK + k * 32, 0, 1024),
-                                  ID_S, k > 0);
-                    umma_commit(b_sfull);
-                    umma_commit(b_kempty);
-                }
-                if (!mbar_wait(b_vfull, j & 1, abort_flag, p.err)) break;
+                if (j + 1 < nkt && !issue_s(j + 1)) break;
+                const int it = 2 * j + 1, s = it % 3;
+                if (!mbar_wait(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) break;
                 tc_fence_after();
+                const uint32_t sv = sRing + s * TILE_BYTES;
 #pragma unroll
                 for (int k = 0; k < TILE / 16; k++)
                     umma_bf16(tO, sdesc(sP + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024),
-                              sdesc(sV + k * 2048, 8192, 1024), ID_O, k > 0);
+                              sdesc(sv + k * 2048, 8192, 1024), ID_O, k > 0);
                 umma_commit(b_ofull);
-                umma_commit(b_vempty);
+                umma_commit(b_empty + 8 * s);
             }
         }
     } else {
         // ------------------------------------------------------- softmax
-        const int q = warp & 3;
+        // warp pair (w, w+4) shares TMEM lane quarter w & 3: half 0 takes keys
+        // [0,64) of each tile and output columns [0,32), half 1 the rest
+        const int q = warp & 3, hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;
         const int qi = qt * TILE + r;
         const uint32_t loff = (uint32_t)(q * 32) << 16;
-        float o[HD];
+        const int kb = hf * 64;
+        float o[32];
 #pragma unroll
-        for (int i = 0; i < HD; i++) o[i] = 0.f;
+        for (int i = 0; i < 32; i++) o[i] = 0.f;
         float m2 = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkt; j++) {
@@ -193,79 +216,85 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_fwd_tc(const __grid_consta
             }
             tc_fence_after();
             if (j > 0) {
-                float t[32];
-                tmem_ld32(tO + loff, t);
+                uint32_t t[32];
+                tmem_ld32_async(tO + loff + hf * 32, t);
+                tmem_wait32(t);
 #pragma unroll
-                for (int i = 0; i < 32; i++) o[i] += t[i];
-                tmem_ld32(tO + loff + 32, t);
-#pragma unroll
-                for (int i = 0; i < 32; i++) o[32 + i] += t[i];
+                for (int i = 0; i < 32; i++) o[i] += __uint_as_float(t[i]);
             }
             const bool diag = (j == qt);
             float mx = -INFINITY;
 #pragma unroll
-            for (int c0 = 0; c0 < TILE; c0 += 32) {
-                float s[32];
-                tmem_ld32(tS + loff + c0, s);
+            for (int c = 0; c < 2; c++) {
+                uint32_t sv[32];
+                tmem_ld32_async(tS + loff + kb + 32 * c, sv);
+                tmem_wait32(sv);
 #pragma unroll
                 for (int i = 0; i < 32; i++)
-                    if (!diag || c0 + i <= r) mx = fmaxf(mx, s[i] * p.scale_log2);
+                    if (!diag || kb + 32 * c + i <= r)
+                        mx = fmaxf(mx, __uint_as_float(sv[i]) * p.scale_log2);
             }
+            float* rb = red + (j & 1) * 256;
+            rb[hf * 128 + r] = mx;
+            named_sync_softmax();
+            mx = fmaxf(rb[r], rb[128 + r]);
             const float mn = fmaxf(m2, mx);
             const float corr = exp2f(m2 - mn);
             l *= corr;
 #pragma unroll
-            for (int i = 0; i < HD; i++) o[i] *= corr;
+            for (int i = 0; i < 32; i++) o[i] *= corr;
             m2 = mn;
 #pragma unroll
-            for (int c0 = 0; c0 < TILE; c0 += 32) {
-                float s[32];
-                tmem_ld32(tS + loff + c0, s);
+            for (int c = 0; c < 2; c++) {
+                uint32_t sv[32];
+                tmem_ld32_async(tS + loff + kb + 32 * c, sv);
+                tmem_wait32(sv);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
-                    const int k0 = c0 + 2 * i;
-                    float a = (!diag || k0 <= r) ? exp2f(s[2 * i] * p.scale_log2 - mn) : 0.f;
-                    float c = (!diag || k0 + 1 <= r) ? exp2f(s[2 * i + 1] * p.scale_log2 - mn) : 0.f;
-                    l += a + c;
-                    pk[i] = pack_bf16x2(a, c);
+                    const int k0 = kb + 32 * c + 2 * i;
+                    float a = (!diag || k0 <= r)
+                                  ? exp2f(__uint_as_float(sv[2 * i]) * p.scale_log2 - mn)
+                                  : 0.f;
+                    float e = (!diag || k0 + 1 <= r)
+                                  ? exp2f(__uint_as_float(sv[2 * i + 1]) * p.scale_log2 - mn)
+                                  : 0.f;
+                    l += a + e;
+                    pk[i] = pack_bf16x2(a, e);
                 }
-#pragma unroll
-                for (int cc = 0; cc < 4; cc++) {
-                    const int chunk = ((c0 & 63) >> 3) + cc;
-                    const uint32_t addr =
-                        sP + (c0 >> 6) * 16384 + r * 128 + ((uint32_t)(chunk ^ (r & 7)) << 4);
-                    st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                }
+                st_row32(sP, r, kb + 32 * c, pk);
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_pfull);
         }
-        if (ok && warp_wait(b_ofull, (nkt - 1) & 1, abort_flag, p.err, lane)) {
+        bool fin = ok && warp_wait(b_ofull, (nkt - 1) & 1, abort_flag, p.err, lane);
+        if (fin) {
             tc_fence_after();
-            float t[32];
-            tmem_ld32(tO + loff, t);
+            uint32_t t[32];
+            tmem_ld32_async(tO + loff + hf * 32, t);
+            tmem_wait32(t);
 #pragma unroll
-            for (int i = 0; i < 32; i++) o[i] += t[i];
-            tmem_ld32(tO + loff + 32, t);
+            for (int i = 0; i < 32; i++) o[i] += __uint_as_float(t[i]);
+        }
+        // fold the two halves' row sums (every softmax thread reaches this)
+        lsum[hf * 128 + r] = l;
+        named_sync_softmax();
+        if (fin && qi < p.T) {
+            const float lt = lsum[r] + lsum[128 + r];
+            const float inv = 1.f / lt;
+            bf16* dst = p.out + ((size_t)(row0 + qi)) * p.C + h * HD + hf * 32;
 #pragma unroll
-            for (int i = 0; i < 32; i++) o[32 + i] += t[i];
-            if (qi < p.T) {
-                const float inv = 1.f / l;
-                bf16* dst = p.out + ((size_t)(row0 + qi)) * p.C + h * HD;
-#pragma unroll
-                for (int i = 0; i < HD; i += 8) {
-                    uint4 u;
-                    u.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
-                    u.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
-                    u.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
-                    u.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
-                    *reinterpret_cast<uint4*>(dst + i) = u;
-                }
-                p.lse[(size_t)bh * p.T + qi] = (m2 + log2f(l)) * 0.6931471805599453f;
+            for (int i = 0; i < 32; i += 8) {
+                uint4 u;
+                u.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+                u.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
+                u.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
+                u.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
+                *reinterpret_cast<uint4*>(dst + i) = u;
             }
+            if (hf == 0) p.lse[(size_t)bh * p.T + qi] = (m2 + log2f(lt)) * 0.6931471805599453f;
         }
         tc_fence_before();
     }
@@ -276,7 +305,6 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_fwd_tc(const __grid_consta
         tmem_dealloc(tmem, 256);
     }
 }
-
 
 // ---------------------------------------------------------------------------
 // Backward.  With P = exp(S/sqrt(hd) - lse) recomputed from the saved lse and
@@ -305,21 +333,6 @@ struct AttnBwdParams {
     float scale_log2;  // log2(e)/sqrt(hd)
     float scale;       // 1/sqrt(hd)
 };
-
-__device__ __forceinline__ void named_sync_softmax() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-// write 32 values (as 16 packed bf16 pairs) of row r into a 128x128 bf16
-// K-major swizzled tile (two 64-column atoms of 16 KB)
-__device__ __forceinline__ void st_row32(uint32_t tile, int r, int c0, const uint32_t* pk) {
-#pragma unroll
-    for (int cc = 0; cc < 4; cc++) {
-        const int chunk = ((c0 & 63) >> 3) + cc;
-        const uint32_t addr = tile + (c0 >> 6) * 16384 + r * 128 + ((uint32_t)(chunk ^ (r & 7)) << 4);
-        st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-    }
-}
 
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     k_attn_dkv_tc(const __grid_constant__ CUtensorMap map_qkv,
@@ -351,7 +364,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         mbar_init(b_qde0, 1);
         mbar_init(b_qde1, 1);
         mbar_init(b_sfull, 1);
-        mbar_init(b_psfull, 4);
+        mbar_init(b_psfull, 8);
         mbar_init(b_psfree, 1);
         mbar_init(b_acc, 1);
         *abort_flag = 0;
@@ -433,7 +446,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             if (ok) umma_commit(b_acc);
         }
     } else {
-        const int q = warp & 3;
+        // warp pair (w, w+4) shares TMEM lane quarter w & 3; half hf takes
+        // query columns [64 hf, 64 hf + 64) and output columns [32 hf, 32 hf + 32)
+        const int q = warp & 3, hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;   // key row within the tile
         const int kj = kt * TILE + r;  // key index in the sequence
         const int tid = threadIdx.x - 64;
@@ -442,7 +457,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (int n = 0; n < nq; n++) {
             const int i = kt + n;
             named_sync_softmax();  // everyone is done with the previous lse/D
-            {
+            if (tid < TILE) {
                 const int qi = i * TILE + tid;
                 lse_s[tid] = qi < p.T ? p.lse[(size_t)bh * p.T + qi] * 1.4426950408889634f : 0.f;
                 d_s[tid] = qi < p.T ? p.Dv[(size_t)bh * p.T + qi] : 0.f;
@@ -459,10 +474,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             tc_fence_after();
             const int qbase = i * TILE;
 #pragma unroll 1
-            for (int c0 = 0; c0 < TILE; c0 += 32) {
-                float sv[32], dp[32];
-                tmem_ld32(tST + loff + c0, sv);
-                tmem_ld32(tDPT + loff + c0, dp);
+            for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 32) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32_async(tST + loff + c0, sv);
+                tmem_ld32_async(tDPT + loff + c0, dp);
+                tmem_wait32(sv);
+                tmem_wait32(dp);
                 uint32_t pp[16], dd[16];
 #pragma unroll
                 for (int e = 0; e < 16; e++) {
@@ -472,9 +489,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         const int c = c0 + 2 * e + z;
                         const int qi = qbase + c;
                         const bool live = qi < p.T && kj <= qi;
-                        const float pr = live ? exp2f(sv[2 * e + z] * p.scale_log2 - lse_s[c]) : 0.f;
+                        const float pr =
+                            live ? exp2f(__uint_as_float(sv[2 * e + z]) * p.scale_log2 - lse_s[c])
+                                 : 0.f;
                         pv[z] = pr;
-                        dv[z] = live ? pr * (dp[2 * e + z] - d_s[c]) : 0.f;
+                        dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - d_s[c]) : 0.f;
                     }
                     pp[e] = pack_bf16x2(pv[0], pv[1]);
                     dd[e] = pack_bf16x2(dv[0], dv[1]);
@@ -489,27 +508,32 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         if (ok && warp_wait(b_acc, 0, abort_flag, p.err, lane)) {
             tc_fence_after();
-            bf16* dst = p.dqkv + (size_t)(row0 + kj) * 3 * p.C + h * HD;
-#pragma unroll 1
-            for (int half = 0; half < 2; half++) {
-                float v[32], k[32];
-                tmem_ld32(tDV + loff + half * 32, v);
-                tmem_ld32(tDK + loff + half * 32, k);
-                if (kj < p.T) {
+            bf16* dst = p.dqkv + (size_t)(row0 + kj) * 3 * p.C + h * HD + hf * 32;
+            uint32_t v[32], k[32];
+            tmem_ld32_async(tDV + loff + hf * 32, v);
+            tmem_ld32_async(tDK + loff + hf * 32, k);
+            tmem_wait32(v);
+            tmem_wait32(k);
+            if (kj < p.T) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 uv, uk;
-                        uv.x = pack_bf16x2(v[e], v[e + 1]);
-                        uv.y = pack_bf16x2(v[e + 2], v[e + 3]);
-                        uv.z = pack_bf16x2(v[e + 4], v[e + 5]);
-                        uv.w = pack_bf16x2(v[e + 6], v[e + 7]);
-                        uk.x = pack_bf16x2(k[e] * p.scale, k[e + 1] * p.scale);
-                        uk.y = pack_bf16x2(k[e + 2] * p.scale, k[e + 3] * p.scale);
-                        uk.z = pack_bf16x2(k[e + 4] * p.scale, k[e + 5] * p.scale);
-                        uk.w = pack_bf16x2(k[e + 6] * p.scale, k[e + 7] * p.scale);
-                        *reinterpret_cast<uint4*>(dst + 2 * p.C + half * 32 + e) = uv;
-                        *reinterpret_cast<uint4*>(dst + p.C + half * 32 + e) = uk;
+                for (int e = 0; e < 32; e += 8) {
+                    uint4 uv, uk;
+                    float f[8], g[8];
+#pragma unroll
+                    for (int z = 0; z < 8; z++) {
+                        f[z] = __uint_as_float(v[e + z]);
+                        g[z] = __uint_as_float(k[e + z]) * p.scale;
                     }
+                    uv.x = pack_bf16x2(f[0], f[1]);
+                    uv.y = pack_bf16x2(f[2], f[3]);
+                    uv.z = pack_bf16x2(f[4], f[5]);
+                    uv.w = pack_bf16x2(f[6], f[7]);
+                    uk.x = pack_bf16x2(g[0], g[1]);
+                    uk.y = pack_bf16x2(g[2], g[3]);
+                    uk.z = pack_bf16x2(g[4], g[5]);
+                    uk.w = pack_bf16x2(g[6], g[7]);
+                    *reinterpret_cast<uint4*>(dst + 2 * p.C + e) = uv;
+                    *reinterpret_cast<uint4*>(dst + p.C + e) = uk;
                 }
             }
         }
@@ -555,7 +579,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         mbar_init(b_kve0, 1);
         mbar_init(b_kve1, 1);
         mbar_init(b_sfull, 1);
-        mbar_init(b_dsfull, 4);
+        mbar_init(b_dsfull, 8);
         mbar_init(b_dsfree, 1);
         mbar_init(b_acc, 1);
         *abort_flag = 0;
@@ -632,7 +656,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             if (ok) umma_commit(b_acc);
         }
     } else {
-        const int q = warp & 3;
+        const int q = warp & 3, hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;
         const int qi = qt * TILE + r;
         const uint32_t loff = (uint32_t)(q * 32) << 16;
@@ -652,10 +676,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             tc_fence_after();
             const int kbase = j * TILE;
 #pragma unroll 1
-            for (int c0 = 0; c0 < TILE; c0 += 32) {
-                float sv[32], dp[32];
-                tmem_ld32(tS + loff + c0, sv);
-                tmem_ld32(tDP + loff + c0, dp);
+            for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 32) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32_async(tS + loff + c0, sv);
+                tmem_ld32_async(tDP + loff + c0, dp);
+                tmem_wait32(sv);
+                tmem_wait32(dp);
                 uint32_t dd[16];
 #pragma unroll
                 for (int e = 0; e < 16; e++) {
@@ -664,8 +690,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     for (int z = 0; z < 2; z++) {
                         const int kk = kbase + c0 + 2 * e + z;
                         const bool live = qlive && kk <= qi;
-                        const float pr = live ? exp2f(sv[2 * e + z] * p.scale_log2 - lse2) : 0.f;
-                        dv[z] = live ? pr * (dp[2 * e + z] - Dq) : 0.f;
+                        const float pr =
+                            live ? exp2f(__uint_as_float(sv[2 * e + z]) * p.scale_log2 - lse2) : 0.f;
+                        dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - Dq) : 0.f;
                     }
                     dd[e] = pack_bf16x2(dv[0], dv[1]);
                 }
@@ -678,21 +705,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         if (ok && warp_wait(b_acc, 0, abort_flag, p.err, lane)) {
             tc_fence_after();
-            bf16* dst = p.dqkv + (size_t)(row0 + qi) * 3 * p.C + h * HD;
-#pragma unroll 1
-            for (int half = 0; half < 2; half++) {
-                float v[32];
-                tmem_ld32(tDQ + loff + half * 32, v);
-                if (qlive) {
+            bf16* dst = p.dqkv + (size_t)(row0 + qi) * 3 * p.C + h * HD + hf * 32;
+            uint32_t v[32];
+            tmem_ld32_async(tDQ + loff + hf * 32, v);
+            tmem_wait32(v);
+            if (qlive) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 u;
-                        u.x = pack_bf16x2(v[e] * p.scale, v[e + 1] * p.scale);
-                        u.y = pack_bf16x2(v[e + 2] * p.scale, v[e + 3] * p.scale);
-                        u.z = pack_bf16x2(v[e + 4] * p.scale, v[e + 5] * p.scale);
-                        u.w = pack_bf16x2(v[e + 6] * p.scale, v[e + 7] * p.scale);
-                        *reinterpret_cast<uint4*>(dst + half * 32 + e) = u;
-                    }
+                for (int e = 0; e < 32; e += 8) {
+                    float f[8];
+#pragma unroll
+                    for (int z = 0; z < 8; z++) f[z] = __uint_as_float(v[e + z]) * p.scale;
+                    uint4 u;
+                    u.x = pack_bf16x2(f[0], f[1]);
+                    u.y = pack_bf16x2(f[2], f[3]);
+                    u.z = pack_bf16x2(f[4], f[5]);
+                    u.w = pack_bf16x2(f[6], f[7]);
+                    *reinterpret_cast<uint4*>(dst + e) = u;
                 }
             }
         }

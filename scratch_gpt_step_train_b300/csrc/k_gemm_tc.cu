@@ -45,7 +45,7 @@ using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;  // producer, MMA, 8 epilogue warps
 
 template <int BN>
 struct Cfg {
@@ -93,6 +93,24 @@ __device__ __forceinline__ void st8_bf16(bf16* p, const float* f) {
     *reinterpret_cast<uint4*>(p) = u;
 }
 
+// GELU and GELU' for the bf16 epilogues: the same sigmoid form as gelu_f /
+// gelu_grad_f with the fast exp and divide intrinsics (a few fp32 ulp, far
+// below the bf16 rounding of the stored result); u is clamped at -40 so the
+// divisor stays finite.
+__device__ __forceinline__ float gelu_fast(float x) {
+    const float k = 0.7978845608028654f;
+    float u = fmaxf(k * (x + 0.044715f * x * x * x), -40.0f);
+    return __fdividef(x, 1.0f + __expf(-2.0f * u));
+}
+__device__ __forceinline__ float gelu_grad_fast(float x) {
+    const float k = 0.7978845608028654f;
+    float x2 = x * x;
+    float u = fmaxf(k * (x + 0.044715f * x2 * x), -40.0f);
+    float sg = __fdividef(1.0f, 1.0f + __expf(-2.0f * u));
+    float du = k * (1.0f + 3.0f * 0.044715f * x2);
+    return sg + 2.0f * x * sg * (1.0f - sg) * du;
+}
+
 // one thread: 32 accumulator columns [col, col+32) of row `row`; nv valid
 // columns (a multiple of 8)
 __device__ __forceinline__ void epilogue32(const TcParams& p, int row, int col, int nv, float* v,
@@ -120,7 +138,7 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int row, int col, 
                 float pre[8];
                 ld8_bf16(pre, a + j);
 #pragma unroll
-                for (int i = 0; i < 8; i++) pre[i] = v[j + i] * gelu_grad_f(pre[i]);
+                for (int i = 0; i < 8; i++) pre[i] = v[j + i] * gelu_grad_fast(pre[i]);
                 st8_bf16(d + j, pre);
             }
             break;
@@ -145,7 +163,7 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int row, int col, 
                 } else if (p.epi == EPI_GELU) {
                     st8_bf16(p.aux + (size_t)row * p.ldx + col + j, x);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) x[i] = gelu_f(x[i]);
+                    for (int i = 0; i < 8; i++) x[i] = gelu_fast(x[i]);
                 }
                 st8_bf16(d + j, x);
             }
@@ -179,7 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(tfull + 8 * b, 1);
-            mbar_init(tempty + 8 * b, 4);
+            mbar_init(tempty + 8 * b, 8);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -298,7 +316,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ------------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // warps 2..9: TMEM lane quarter (warp % 4) x column half
+        const int q = warp & 3;
+        const int cbeg = ((warp - 2) >> 2) * (BN / 2);
+        constexpr int NCH = BN / 64;  // 32-column chunks per half
         int lt = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, lt++) {
             const int split = tile / tiles_mn, r = tile % tiles_mn;
@@ -311,16 +332,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const int row = tm * BM + q * 32 + lane;
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                float v[32];
-                tmem_ld32(taddr + (uint32_t)c0, v);
-                const int col = tn * BN + c0;
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cbeg);
+            uint32_t buf[2][32];
+            tmem_ld32_async(taddr, buf[0]);
+            tmem_wait32(buf[0]);
+#pragma unroll
+            for (int c = 0; c < NCH; c++) {
+                if (c + 1 < NCH) tmem_ld32_async(taddr + (uint32_t)(32 * (c + 1)), buf[(c + 1) & 1]);
+                const int col = tn * BN + cbeg + 32 * c;
                 if (row < p.M && col < p.N) {
-                    const int nv = min(32, p.N - col);
-                    epilogue32(p, row, col, nv, v, split);
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(buf[c & 1][i]);
+                    epilogue32(p, row, col, min(32, p.N - col), v, split);
                 }
+                if (c + 1 < NCH) tmem_wait32(buf[(c + 1) & 1]);
             }
             tc_fence_before();
             __syncwarp();

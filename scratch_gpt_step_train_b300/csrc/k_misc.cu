@@ -296,16 +296,26 @@ __global__ void __launch_bounds__(256) k_ln_bwd(T* dx, float* part, const T* dou
     }
 }
 
-__global__ void k_colsum_partials(float* dw, float* db, const float* part, int nb, int C) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= C) return;
-    float a = 0.f, b = 0.f;
-    for (int i = 0; i < nb; i++) {
-        a += part[(size_t)i * 2 * C + c];
-        b += part[(size_t)i * 2 * C + C + c];
+// out0[c] (c < n0) / out1[c - n0] (c >= n0) += sum_i part[i*ld + c], i in a
+// fixed order: thread row ty sums i = ty, ty+8, ..., then row 0 adds the 8
+// row sums in order.  32 consecutive columns per block (coalesced).
+__global__ void __launch_bounds__(256) k_colsum(float* out0, float* out1, int n0, int ncols,
+                                                const float* part, int nparts, long ld) {
+    __shared__ float sh[8][33];
+    int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    int c = blockIdx.x * 32 + tx;
+    float a = 0.f;
+    if (c < ncols)
+        for (int i = ty; i < nparts; i += 8) a += part[(size_t)i * ld + c];
+    sh[ty][tx] = a;
+    __syncthreads();
+    if (ty == 0 && c < ncols) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; k++) t += sh[k][tx];
+        if (c < n0) out0[c] += t;
+        else out1[c - n0] += t;
     }
-    dw[c] += a;
-    db[c] += b;
 }
 
 size_t layernorm_backward_scratch(int N, int C) {
@@ -335,7 +345,7 @@ static cudaError_t ln_bwd_vec(void* dx, float* dw, float* db, const void* dout, 
     else if (it <= 16) LNB(16);
     else return cudaErrorInvalidValue;
 #undef LNB
-    k_colsum_partials<<<cdiv(C, 256), 256, 0, s>>>(dw, db, part, nb, C);
+    k_colsum<<<cdiv(2 * C, 32), 256, 0, s>>>(dw, db, C, 2 * C, part, nb, 2 * C);
     return cudaGetLastError();
 }
 template <typename T>
@@ -359,7 +369,7 @@ cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, const vo
 // Bias gradient: db[o] += sum_n dout[n,o].  Stage 1: each block sums a chunk
 // of BG_ROWS rows for VEC-wide column groups; stage 2 sums chunks in order.
 // ===========================================================================
-#define BG_ROWS 32
+#define BG_ROWS 64
 
 template <typename T, int VEC>
 __global__ void k_bias_part(float* part, const T* dout, int N, int OC) {
@@ -379,13 +389,6 @@ __global__ void k_bias_part(float* part, const T* dout, int N, int OC) {
 #pragma unroll
     for (int j = 0; j < VEC; j++) part[(size_t)blockIdx.y * OC + c + j] = a[j];
 }
-__global__ void k_bias_final(float* db, const float* part, int nch, int OC) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= OC) return;
-    float a = 0.f;
-    for (int i = 0; i < nch; i++) a += part[(size_t)i * OC + c];
-    db[c] += a;
-}
 size_t bias_grad_scratch(int N, int OC) { return (size_t)cdiv(N, BG_ROWS) * OC * sizeof(float); }
 
 template <typename T>
@@ -401,7 +404,7 @@ static cudaError_t bias_grad_t(float* db, const void* dout, int N, int OC, void*
         dim3 grid(cdiv(OC, 128), nch);
         k_bias_part<T, 1><<<grid, 128, 0, s>>>(part, (const T*)dout, N, OC);
     }
-    k_bias_final<<<cdiv(OC, 256), 256, 0, s>>>(db, part, nch, OC);
+    k_colsum<<<cdiv(OC, 32), 256, 0, s>>>(db, db, OC, OC, part, nch, OC);
     return cudaGetLastError();
 }
 cudaError_t bias_grad(int act, float* db, const void* dout, int N, int OC, void* scratch,
