@@ -57,6 +57,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 2^x with one MUFU instruction (ex2.approx: ~2 ulp; P is rounded to bf16 next)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // lane 0 waits, the warp learns the outcome
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* err, int lane) {
@@ -222,6 +229,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
 #pragma unroll
                 for (int i = 0; i < 32; i++) o[i] += __uint_as_float(t[i]);
             }
+            // Only the diagonal tile needs the causal mask; the max is taken on
+            // raw scores (the scale is positive) and scaled once.
             const bool diag = (j == qt);
             float mx = -INFINITY;
 #pragma unroll
@@ -229,17 +238,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
                 uint32_t sv[32];
                 tmem_ld32_async(tS + loff + kb + 32 * c, sv);
                 tmem_wait32(sv);
+                if (!diag) {
 #pragma unroll
-                for (int i = 0; i < 32; i++)
-                    if (!diag || kb + 32 * c + i <= r)
-                        mx = fmaxf(mx, __uint_as_float(sv[i]) * p.scale_log2);
+                    for (int i = 0; i < 32; i++) mx = fmaxf(mx, __uint_as_float(sv[i]));
+                } else {
+                    const int lim = r - (kb + 32 * c);  // keys i <= lim are visible
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        mx = fmaxf(mx, i <= lim ? __uint_as_float(sv[i]) : -INFINITY);
+                }
             }
             float* rb = red + (j & 1) * 256;
             rb[hf * 128 + r] = mx;
             named_sync_softmax();
-            mx = fmaxf(rb[r], rb[128 + r]);
+            mx = fmaxf(rb[r], rb[128 + r]) * p.scale_log2;
             const float mn = fmaxf(m2, mx);
-            const float corr = exp2f(m2 - mn);
+            const float corr = ex2(m2 - mn);
             l *= corr;
 #pragma unroll
             for (int i = 0; i < 32; i++) o[i] *= corr;
@@ -250,15 +264,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
                 tmem_ld32_async(tS + loff + kb + 32 * c, sv);
                 tmem_wait32(sv);
                 uint32_t pk[16];
+                const int lim = diag ? r - (kb + 32 * c) : 64;
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
-                    const int k0 = kb + 32 * c + 2 * i;
-                    float a = (!diag || k0 <= r)
-                                  ? exp2f(__uint_as_float(sv[2 * i]) * p.scale_log2 - mn)
-                                  : 0.f;
-                    float e = (!diag || k0 + 1 <= r)
-                                  ? exp2f(__uint_as_float(sv[2 * i + 1]) * p.scale_log2 - mn)
-                                  : 0.f;
+                    float a = ex2(fmaf(__uint_as_float(sv[2 * i]), p.scale_log2, -mn));
+                    float e = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), p.scale_log2, -mn));
+                    if (diag) {
+                        a = 2 * i <= lim ? a : 0.f;
+                        e = 2 * i + 1 <= lim ? e : 0.f;
+                    }
                     l += a + e;
                     pk[i] = pack_bf16x2(a, e);
                 }
@@ -473,6 +487,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             }
             tc_fence_after();
             const int qbase = i * TILE;
+            // off-diagonal query tiles that lie inside the sequence need no mask
+            const bool full = i > kt && qbase + TILE <= p.T;
 #pragma unroll 1
             for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 32) {
                 uint32_t sv[32], dp[32];
@@ -481,22 +497,36 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 tmem_wait32(sv);
                 tmem_wait32(dp);
                 uint32_t pp[16], dd[16];
+                if (full) {
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int z = 0; z < 2; z++) {
-                        const int c = c0 + 2 * e + z;
-                        const int qi = qbase + c;
-                        const bool live = qi < p.T && kj <= qi;
-                        const float pr =
-                            live ? exp2f(__uint_as_float(sv[2 * e + z]) * p.scale_log2 - lse_s[c])
-                                 : 0.f;
-                        pv[z] = pr;
-                        dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - d_s[c]) : 0.f;
+                    for (int e = 0; e < 16; e++) {
+                        const int c = c0 + 2 * e;
+                        const float p0 =
+                            ex2(fmaf(__uint_as_float(sv[2 * e]), p.scale_log2, -lse_s[c]));
+                        const float p1 =
+                            ex2(fmaf(__uint_as_float(sv[2 * e + 1]), p.scale_log2, -lse_s[c + 1]));
+                        pp[e] = pack_bf16x2(p0, p1);
+                        dd[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - d_s[c]),
+                                            p1 * (__uint_as_float(dp[2 * e + 1]) - d_s[c + 1]));
                     }
-                    pp[e] = pack_bf16x2(pv[0], pv[1]);
-                    dd[e] = pack_bf16x2(dv[0], dv[1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        float pv[2], dv[2];
+#pragma unroll
+                        for (int z = 0; z < 2; z++) {
+                            const int c = c0 + 2 * e + z;
+                            const int qi = qbase + c;
+                            const bool live = qi < p.T && kj <= qi;
+                            const float pr = live ? ex2(fmaf(__uint_as_float(sv[2 * e + z]),
+                                                             p.scale_log2, -lse_s[c]))
+                                                  : 0.f;
+                            pv[z] = pr;
+                            dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - d_s[c]) : 0.f;
+                        }
+                        pp[e] = pack_bf16x2(pv[0], pv[1]);
+                        dd[e] = pack_bf16x2(dv[0], dv[1]);
+                    }
                 }
                 st_row32(sPT, r, c0, pp);
                 st_row32(sDST, r, c0, dd);
@@ -683,18 +713,30 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 tmem_wait32(sv);
                 tmem_wait32(dp);
                 uint32_t dd[16];
+                if (j < qt) {
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
-                    float dv[2];
-#pragma unroll
-                    for (int z = 0; z < 2; z++) {
-                        const int kk = kbase + c0 + 2 * e + z;
-                        const bool live = qlive && kk <= qi;
-                        const float pr =
-                            live ? exp2f(__uint_as_float(sv[2 * e + z]) * p.scale_log2 - lse2) : 0.f;
-                        dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - Dq) : 0.f;
+                    for (int e = 0; e < 16; e++) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), p.scale_log2, -lse2));
+                        const float p1 =
+                            ex2(fmaf(__uint_as_float(sv[2 * e + 1]), p.scale_log2, -lse2));
+                        dd[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - Dq),
+                                            p1 * (__uint_as_float(dp[2 * e + 1]) - Dq));
                     }
-                    dd[e] = pack_bf16x2(dv[0], dv[1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        float dv[2];
+#pragma unroll
+                        for (int z = 0; z < 2; z++) {
+                            const int kk = kbase + c0 + 2 * e + z;
+                            const bool live = qlive && kk <= qi;
+                            const float pr = live ? ex2(fmaf(__uint_as_float(sv[2 * e + z]),
+                                                             p.scale_log2, -lse2))
+                                                  : 0.f;
+                            dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - Dq) : 0.f;
+                        }
+                        dd[e] = pack_bf16x2(dv[0], dv[1]);
+                    }
                 }
                 st_row32(sDS, r, c0, dd);
             }
