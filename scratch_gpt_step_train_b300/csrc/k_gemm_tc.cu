@@ -32,6 +32,7 @@
 // are split along K into fp32 partial tiles summed in a fixed order by a
 // second kernel (deterministic; no float atomics).
 #include <cuda.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "gemm_tc.h"
@@ -53,8 +54,9 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STG_BYTES = 8 * 4096;  // epilogue staging: 4 KB per epilogue warp
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + STG_BYTES + 1024 + BAR_BYTES;
 };
 
 struct TcParams {
@@ -75,6 +77,10 @@ struct TcParams {
 enum { EPI_PART_F32 = 100 };
 
 // ------------------------------------------------------------------ epilogue
+__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
 __device__ __forceinline__ void ld8_bf16(float* f, const bf16* p) {
     uint4 u = *reinterpret_cast<const uint4*>(p);
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -111,63 +117,121 @@ __device__ __forceinline__ float gelu_grad_fast(float x) {
     return sg + 2.0f * x * sg * (1.0f - sg) * du;
 }
 
-// one thread: 32 accumulator columns [col, col+32) of row `row`; nv valid
-// columns (a multiple of 8)
-__device__ __forceinline__ void epilogue32(const TcParams& p, int row, int col, int nv, float* v,
-                                           int split) {
-    switch (p.epi) {
-        case EPI_ACCUM_F32: {
-            float* d = (float*)p.D + (size_t)row * p.ldd + col;
-            for (int j = 0; j < nv; j += 4) {
-                float4 o = *reinterpret_cast<float4*>(d + j);
-                o.x += v[j]; o.y += v[j + 1]; o.z += v[j + 2]; o.w += v[j + 3];
-                *reinterpret_cast<float4*>(d + j) = o;
-            }
-            break;
-        }
-        case EPI_PART_F32: {
-            float* d = p.part + ((size_t)split * p.M + row) * p.N + col;
-            for (int j = 0; j < nv; j += 4)
-                *reinterpret_cast<float4*>(d + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-            break;
-        }
-        case EPI_GELU_BWD: {
-            const bf16* a = p.aux + (size_t)row * p.ldx + col;
-            bf16* d = (bf16*)p.D + (size_t)row * p.ldd + col;
-            for (int j = 0; j < nv; j += 8) {
-                float pre[8];
-                ld8_bf16(pre, a + j);
+// TMA bulk-store helpers (smem -> global through a tensor map)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"((uint64_t)map), "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"((uint64_t)map), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int c0,
+                                                  int c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+        ::"l"((uint64_t)map), "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// row r of a 32 x 32 bf16 staging tile (64-byte rows, 64-byte swizzle)
+__device__ __forceinline__ void stage_bf16_row(uint32_t stg, int r, const float* x) {
 #pragma unroll
-                for (int i = 0; i < 8; i++) pre[i] = v[j + i] * gelu_grad_fast(pre[i]);
-                st8_bf16(d + j, pre);
-            }
-            break;
-        }
-        default: {
-            bf16* d = (bf16*)p.D + (size_t)row * p.ldd + col;
-            for (int j = 0; j < nv; j += 8) {
-                float x[8];
+    for (int k = 0; k < 4; k++) {
+        const float* f = x + 8 * k;
+        st_shared_v4(stg + r * 64 + ((uint32_t)(k ^ ((r >> 1) & 3)) << 4),
+                     pack2_bf16(f[0], f[1]), pack2_bf16(f[2], f[3]), pack2_bf16(f[4], f[5]),
+                     pack2_bf16(f[6], f[7]));
+    }
+}
+// row r of a 32 x 32 fp32 staging tile (128-byte rows, 128-byte swizzle)
+__device__ __forceinline__ void stage_f32_row(uint32_t stg, int r, const float* x) {
 #pragma unroll
-                for (int i = 0; i < 8; i++) x[i] = v[j + i];
+    for (int k = 0; k < 8; k++)
+        st_shared_v4(stg + r * 128 + ((uint32_t)(k ^ (r & 7)) << 4), __float_as_uint(x[4 * k]),
+                     __float_as_uint(x[4 * k + 1]), __float_as_uint(x[4 * k + 2]),
+                     __float_as_uint(x[4 * k + 3]));
+}
+
+struct EpiMaps {
+    CUtensorMap d;    // bf16 [M,N] box 32x32 SW64, or fp32 [M,N] box 32x32 SW128 (accumulate)
+    CUtensorMap aux;  // bf16 [M,N] box 32x32 SW64 (GELU pre-activation)
+    CUtensorMap part; // fp32 [splits,M,N] box 32x32x1 SW128 (split-K partials)
+};
+
+// One warp: the 32 x 32 chunk at rows [row0, row0+32), columns [col, col+32);
+// lane = row within the chunk; v = this lane's 32 accumulator values.
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps& m, int row0,
+                                               int col, int lane, float* v, int split,
+                                               uint32_t stg) {
+    const int row = row0 + lane;
+    const bool rin = row < p.M;
+    const int nv = min(32, p.N - col);  // multiple of 8
+    if (p.epi == EPI_GELU_BWD) {
+        const bf16* a = p.aux + (size_t)row * p.ldx + col;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            float pre[8];
+            if (rin && j < nv) ld8_bf16(pre, a + j);
+            else
+#pragma unroll
+                for (int i = 0; i < 8; i++) pre[i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[j + i] *= gelu_grad_fast(pre[i]);
+        }
+    } else if (p.epi != EPI_ACCUM_F32 && p.epi != EPI_PART_F32) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            if (j < nv) {
                 if (p.bias) {
                     float b[8];
                     ld8_bf16(b, p.bias + col + j);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) x[i] += b[i];
+                    for (int i = 0; i < 8; i++) v[j + i] += b[i];
                 }
-                if (p.epi == EPI_RESID) {
-                    float r[8];
-                    ld8_bf16(r, p.resid + (size_t)row * p.ldr + col + j);
+                if (p.epi == EPI_RESID && rin) {
+                    float r8[8];
+                    ld8_bf16(r8, p.resid + (size_t)row * p.ldr + col + j);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) x[i] += r[i];
-                } else if (p.epi == EPI_GELU) {
-                    st8_bf16(p.aux + (size_t)row * p.ldx + col + j, x);
-#pragma unroll
-                    for (int i = 0; i < 8; i++) x[i] = gelu_fast(x[i]);
+                    for (int i = 0; i < 8; i++) v[j + i] += r8[i];
                 }
-                st8_bf16(d + j, x);
             }
         }
+    }
+    // the previous chunk's bulk stores must have finished reading the staging tile
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+    if (p.epi == EPI_ACCUM_F32 || p.epi == EPI_PART_F32) {
+        stage_f32_row(stg, lane, v);
+    } else if (p.epi == EPI_GELU) {
+        stage_bf16_row(stg + 2048, lane, v);  // pre-activation
+#pragma unroll
+        for (int i = 0; i < 32; i++) v[i] = gelu_fast(v[i]);
+        stage_bf16_row(stg, lane, v);
+    } else {
+        stage_bf16_row(stg, lane, v);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (p.epi == EPI_ACCUM_F32) tma_reduce_add_2d(&m.d, stg, col, row0);
+        else if (p.epi == EPI_PART_F32) tma_store_3d(&m.part, stg, col, row0, split);
+        else {
+            tma_store_2d(&m.d, stg, col, row0);
+            if (p.epi == EPI_GELU) tma_store_2d(&m.aux, stg + 2048, col, row0);
+        }
+        bulk_commit();
     }
 }
 
@@ -175,7 +239,7 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int row, int col, 
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-              TcParams p) {
+              const __grid_constant__ EpiMaps maps, TcParams p) {
     using CF = Cfg<BN>;
     constexpr int S = CF::STAGES;
     constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
@@ -183,10 +247,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t tiles = (raw + 1023u) & ~1023u;
     uint8_t* tiles_gen = smem_raw + (tiles - raw);
-    const uint32_t bars = tiles + S * CF::STAGE_BYTES;
+    const uint32_t stg_base = tiles + S * CF::STAGE_BYTES;  // 1024-aligned
+    const uint32_t bars = stg_base + CF::STG_BYTES;
     const uint32_t full = bars, empty = bars + 8 * S, tfull = bars + 16 * S,
                    tempty = tfull + 16;
-    uint32_t* tmem_slot = (uint32_t*)(tiles_gen + S * CF::STAGE_BYTES + 16 * S + 32);
+    uint32_t* tmem_slot = (uint32_t*)(tiles_gen + S * CF::STAGE_BYTES + CF::STG_BYTES + 16 * S + 32);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -320,6 +385,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;
         const int cbeg = ((warp - 2) >> 2) * (BN / 2);
         constexpr int NCH = BN / 64;  // 32-column chunks per half
+        const uint32_t stg = stg_base + (uint32_t)(warp - 2) * 4096u;
         int lt = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, lt++) {
             const int split = tile / tiles_mn, r = tile % tiles_mn;
@@ -341,11 +407,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int c = 0; c < NCH; c++) {
                 if (c + 1 < NCH) tmem_ld32_async(taddr + (uint32_t)(32 * (c + 1)), buf[(c + 1) & 1]);
                 const int col = tn * BN + cbeg + 32 * c;
-                if (row < p.M && col < p.N) {
+                if (col < p.N) {
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(buf[c & 1][i]);
-                    epilogue32(p, row, col, min(32, p.N - col), v, split);
+                    epilogue_chunk(p, maps, tm * BM + q * 32, col, lane, v, split, stg);
                 }
                 if (c + 1 < NCH) tmem_wait32(buf[(c + 1) & 1]);
             }
@@ -353,6 +419,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + 8 * b);
         }
+        if (lane == 0) bulk_wait0();  // all bulk stores of this warp complete
+        __syncwarp();
     }
     __syncthreads();
     if (warp == 1) {
@@ -408,16 +476,52 @@ bool make_map(CUtensorMap* m, const void* base, long inner, long outer, long ld,
     return r == CUDA_SUCCESS;
 }
 
+bool make_map_epi(CUtensorMap* m, void* base, CUtensorMapDataType dt, int esz, int rank,
+                  const cuuint64_t* dims, const cuuint64_t* strides_bytes) {
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, rank, base, dims, strides_bytes, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          esz == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_epi_maps(EpiMaps* em, const GemmDesc& d, const TcParams& tp) {
+    memset(em, 0, sizeof(*em));
+    bool ok = true;
+    if (tp.epi == EPI_ACCUM_F32) {
+        cuuint64_t dims[2] = {(cuuint64_t)d.N, (cuuint64_t)d.M};
+        cuuint64_t st[1] = {(cuuint64_t)d.ldd * 4};
+        ok = make_map_epi(&em->d, d.D, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 2, dims, st);
+    } else if (tp.epi == EPI_PART_F32) {
+        cuuint64_t dims[3] = {(cuuint64_t)d.N, (cuuint64_t)d.M, (cuuint64_t)tp.splits};
+        cuuint64_t st[2] = {(cuuint64_t)d.N * 4, (cuuint64_t)d.N * d.M * 4};
+        ok = make_map_epi(&em->part, tp.part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 3, dims, st);
+    } else {
+        cuuint64_t dims[2] = {(cuuint64_t)d.N, (cuuint64_t)d.M};
+        cuuint64_t st[1] = {(cuuint64_t)d.ldd * 2};
+        ok = make_map_epi(&em->d, d.D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dims, st);
+        if (ok && tp.epi == EPI_GELU) {
+            cuuint64_t sx[1] = {(cuuint64_t)d.ldx * 2};
+            ok = make_map_epi(&em->aux, d.aux, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dims, sx);
+        }
+    }
+    return ok;
+}
+
 template <int BN, bool AM, bool BMN>
 cudaError_t launch(const GemmDesc& d, const TcParams& tp, int grid, cudaStream_t s) {
     CUtensorMap ma, mb;
+    EpiMaps em;
+    if (!make_epi_maps(&em, d, tp)) return cudaErrorInvalidValue;
     // A: K-major -> [M rows][K], box 64(K) x 128(M);  MN-major -> [K rows][M], box 64(M) x 64(K)
     bool ok = AM ? make_map(&ma, d.A, d.M, d.K, d.lda, 64)
                  : make_map(&ma, d.A, d.K, d.M, d.lda, BM);
     ok = ok && (BMN ? make_map(&mb, d.B, d.N, d.K, d.ldb, 64)
                     : make_map(&mb, d.B, d.K, d.N, d.ldb, BN));
     if (!ok) return cudaErrorInvalidValue;
-    k_gemm_tc<BN, AM, BMN><<<grid, NUM_THREADS, Cfg<BN>::SMEM, s>>>(ma, mb, tp);
+    k_gemm_tc<BN, AM, BMN><<<grid, NUM_THREADS, Cfg<BN>::SMEM, s>>>(ma, mb, em, tp);
     return cudaGetLastError();
 }
 
