@@ -242,33 +242,43 @@ template <typename T, int VEC, int IT>
 __global__ void __launch_bounds__(256) k_ln_bwd(T* dx, float* part, const T* dout, const T* x,
                                                 const T* w, const float* mean,
                                                 const float* rstd, int N, int C) {
-    extern __shared__ float sm[];  // [LNB_WARPS][2C]
-    int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    float* acc = sm + (size_t)warp * 2 * C;
-    for (int i = threadIdx.x; i < LNB_WARPS * 2 * C; i += blockDim.x) sm[i] = 0.f;
-    __syncthreads();
+    __shared__ float sm[2 * 2048];  // block fold of the dw/db partials (C <= 2048)
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    // this lane's dw, db partial sums for its columns, over this warp's rows
+    float aw[IT][VEC], ab[IT][VEC];
+#pragma unroll
+    for (int it = 0; it < IT; it++)
+#pragma unroll
+        for (int j = 0; j < VEC; j++) aw[it][j] = ab[it][j] = 0.f;
     for (int row = blockIdx.x * LNB_WARPS + warp; row < N; row += gridDim.x * LNB_WARPS) {
         const T* xr = x + (size_t)row * C;
         const T* dyr = dout + (size_t)row * C;
-        float m = mean[row], r = rstd[row];
-        float xh[IT][VEC], g[IT][VEC];
+        const float m = mean[row], r = rstd[row];
+        Vec<T, VEC> xv[IT], dv[IT];
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            const int c = (it * 32 + lane) * VEC;
+            if (c < C) {
+                xv[it] = *reinterpret_cast<const Vec<T, VEC>*>(xr + c);
+                dv[it] = *reinterpret_cast<const Vec<T, VEC>*>(dyr + c);
+            }
+        }
         float sg = 0.f, sgx = 0.f;
 #pragma unroll
         for (int it = 0; it < IT; it++) {
-            int c = (it * 32 + lane) * VEC;
+            const int c = (it * 32 + lane) * VEC;
             if (c < C) {
-                float xv[VEC], dy[VEC], wv[VEC];
-                load_vec_f<T, VEC>(xv, xr + c);
-                load_vec_f<T, VEC>(dy, dyr + c);
+                float wv[VEC];
                 load_vec_f<T, VEC>(wv, w + c);
 #pragma unroll
                 for (int j = 0; j < VEC; j++) {
-                    xh[it][j] = (xv[j] - m) * r;
-                    g[it][j] = dy[j] * wv[j];
-                    sg += g[it][j];
-                    sgx += g[it][j] * xh[it][j];
-                    acc[c + j] += dy[j] * xh[it][j];
-                    acc[C + c + j] += dy[j];
+                    const float xh = (to_f(xv[it].v[j]) - m) * r;
+                    const float dy = to_f(dv[it].v[j]);
+                    const float g = dy * wv[j];
+                    sg += g;
+                    sgx += g * xh;
+                    aw[it][j] += dy * xh;
+                    ab[it][j] += dy;
                 }
             }
         }
@@ -277,23 +287,44 @@ __global__ void __launch_bounds__(256) k_ln_bwd(T* dx, float* part, const T* dou
         T* dxr = dx + (size_t)row * C;
 #pragma unroll
         for (int it = 0; it < IT; it++) {
-            int c = (it * 32 + lane) * VEC;
+            const int c = (it * 32 + lane) * VEC;
             if (c < C) {
-                float d[VEC];
+                float wv[VEC], d[VEC];
+                load_vec_f<T, VEC>(wv, w + c);
                 load_vec_f<T, VEC>(d, dxr + c);
 #pragma unroll
-                for (int j = 0; j < VEC; j++) d[j] += r * (g[it][j] - sg - xh[it][j] * sgx);
+                for (int j = 0; j < VEC; j++) {
+                    const float xh = (to_f(xv[it].v[j]) - m) * r;
+                    const float g = to_f(dv[it].v[j]) * wv[j];
+                    d[j] += r * (g - sg - xh * sgx);
+                }
                 store_vec_f<T, VEC>(dxr + c, d);
             }
         }
     }
-    __syncthreads();
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
-        float a = 0.f;
+    // fold the 8 warps' partials in a fixed order (warp 0 first)
+    for (int wi = 0; wi < LNB_WARPS; wi++) {
+        if (warp == wi) {
 #pragma unroll
-        for (int wi = 0; wi < LNB_WARPS; wi++) a += sm[(size_t)wi * 2 * C + c];
-        part[(size_t)blockIdx.x * 2 * C + c] = a;
+            for (int it = 0; it < IT; it++) {
+                const int c = (it * 32 + lane) * VEC;
+                if (c < C) {
+#pragma unroll
+                    for (int j = 0; j < VEC; j++) {
+                        if (wi == 0) {
+                            sm[c + j] = aw[it][j];
+                            sm[C + c + j] = ab[it][j];
+                        } else {
+                            sm[c + j] += aw[it][j];
+                            sm[C + c + j] += ab[it][j];
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
     }
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) part[(size_t)blockIdx.x * 2 * C + c] = sm[c];
 }
 
 // out0[c] (c < n0) / out1[c - n0] (c >= n0) += sum_i part[i*ld + c], i in a
@@ -327,23 +358,26 @@ static cudaError_t ln_bwd_vec(void* dx, float* dw, float* db, const void* dout, 
                               const void* w, const float* mean, const float* rstd, int N, int C,
                               void* scratch, cudaStream_t s) {
     int it = cdiv(C, 32 * VEC);
-    int nb = cdiv(N, LNB_WARPS);
+    int nb = cdiv(N, LNB_WARPS * 4);
     if (nb > LNB_MAX_BLOCKS) nb = LNB_MAX_BLOCKS;
-    size_t smem = (size_t)LNB_WARPS * 2 * C * sizeof(float);
     float* part = (float*)scratch;
 #define LNB(I)                                                                                   \
-    do {                                                                                         \
-        auto kf = k_ln_bwd<T, VEC, I>;                                                           \
-        cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);        \
-        kf<<<nb, 256, smem, s>>>((T*)dx, part, (const T*)dout, (const T*)x, (const T*)w, mean,  \
-                                 rstd, N, C);                                                    \
-    } while (0)
-    if (it <= 1) LNB(1);
-    else if (it <= 2) LNB(2);
-    else if (it <= 4) LNB(4);
-    else if (it <= 8) LNB(8);
-    else if (it <= 16) LNB(16);
-    else return cudaErrorInvalidValue;
+    k_ln_bwd<T, VEC, I><<<nb, 256, 0, s>>>((T*)dx, part, (const T*)dout, (const T*)x,            \
+                                           (const T*)w, mean, rstd, N, C)
+    switch (it) {
+        case 1: LNB(1); break;
+        case 2: LNB(2); break;
+        case 3: LNB(3); break;
+        case 4: LNB(4); break;
+        case 5: LNB(5); break;
+        case 6: LNB(6); break;
+        case 7: LNB(7); break;
+        case 8: LNB(8); break;
+        default:
+            if (it <= 12) LNB(12);
+            else if (it <= 16) LNB(16);
+            else return cudaErrorInvalidValue;
+    }
 #undef LNB
     k_colsum<<<cdiv(2 * C, 32), 256, 0, s>>>(dw, db, C, 2 * C, part, nb, 2 * C);
     return cudaGetLastError();
@@ -359,7 +393,7 @@ static cudaError_t ln_bwd_t(void* dx, float* dw, float* db, const void* dout, co
 cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, const void* dout,
                                const void* x, const void* w, const float* mean,
                                const float* rstd, int N, int C, void* scratch, cudaStream_t s) {
-    if ((size_t)C * 2 * LNB_WARPS * sizeof(float) > 200 * 1024) return cudaErrorInvalidValue;
+    if (C > 2048) return cudaErrorInvalidValue;
     if (act == ACT_BF16)
         return ln_bwd_t<bf16>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
     return ln_bwd_t<float>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
@@ -371,23 +405,42 @@ cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, const vo
 // ===========================================================================
 #define BG_ROWS 64
 
+// block (32 x 8 threads): column vectors blockIdx.x*32 + tx, rows
+// [blockIdx.y*BG_ROWS, +BG_ROWS); thread row ty sums rows ty, ty+8, ... in
+// order, then the 8 row sums are added in order.
 template <typename T, int VEC>
-__global__ void k_bias_part(float* part, const T* dout, int N, int OC) {
-    int cg = blockIdx.x * blockDim.x + threadIdx.x;
-    int c = cg * VEC;
-    if (c >= OC) return;
-    int r0 = blockIdx.y * BG_ROWS, r1 = min(N, r0 + BG_ROWS);
+__global__ void __launch_bounds__(256) k_bias_part(float* part, const T* dout, int N, int OC) {
+    __shared__ float sh[8][32 * VEC + 1];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int c = (blockIdx.x * 32 + tx) * VEC;
+    const int r0 = blockIdx.y * BG_ROWS;
     float a[VEC];
 #pragma unroll
     for (int j = 0; j < VEC; j++) a[j] = 0.f;
-    for (int r = r0; r < r1; r++) {
-        float v[VEC];
-        load_vec_f<T, VEC>(v, dout + (size_t)r * OC + c);
+    if (c < OC) {
 #pragma unroll
-        for (int j = 0; j < VEC; j++) a[j] += v[j];
+        for (int k = 0; k < BG_ROWS / 8; k++) {
+            const int r = r0 + ty + 8 * k;
+            if (r < N) {
+                float v[VEC];
+                load_vec_f<T, VEC>(v, dout + (size_t)r * OC + c);
+#pragma unroll
+                for (int j = 0; j < VEC; j++) a[j] += v[j];
+            }
+        }
     }
 #pragma unroll
-    for (int j = 0; j < VEC; j++) part[(size_t)blockIdx.y * OC + c + j] = a[j];
+    for (int j = 0; j < VEC; j++) sh[ty][tx * VEC + j] = a[j];
+    __syncthreads();
+    if (ty == 0 && c < OC) {
+#pragma unroll
+        for (int j = 0; j < VEC; j++) {
+            float t = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; k++) t += sh[k][tx * VEC + j];
+            part[(size_t)blockIdx.y * OC + c + j] = t;
+        }
+    }
 }
 size_t bias_grad_scratch(int N, int OC) { return (size_t)cdiv(N, BG_ROWS) * OC * sizeof(float); }
 
@@ -398,11 +451,11 @@ static cudaError_t bias_grad_t(float* db, const void* dout, int N, int OC, void*
     int nch = cdiv(N, BG_ROWS);
     float* part = (float*)scratch;
     if (OC % VM == 0) {
-        dim3 grid(cdiv(OC / VM, 128), nch);
-        k_bias_part<T, VM><<<grid, 128, 0, s>>>(part, (const T*)dout, N, OC);
+        dim3 grid(cdiv(OC / VM, 32), nch);
+        k_bias_part<T, VM><<<grid, 256, 0, s>>>(part, (const T*)dout, N, OC);
     } else {
-        dim3 grid(cdiv(OC, 128), nch);
-        k_bias_part<T, 1><<<grid, 128, 0, s>>>(part, (const T*)dout, N, OC);
+        dim3 grid(cdiv(OC, 32), nch);
+        k_bias_part<T, 1><<<grid, 256, 0, s>>>(part, (const T*)dout, N, OC);
     }
     k_colsum<<<cdiv(OC, 32), 256, 0, s>>>(db, db, OC, OC, part, nch, OC);
     return cudaGetLastError();

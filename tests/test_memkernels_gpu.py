@@ -1,0 +1,200 @@
+"""Parity of the memory-bound kernels of the step against the oracle (fp64),
+at the full GPT-2 124M micro-batch (B=16, T=1024, C=768, V=50257) and at
+small ragged shapes: embedding forward/backward, LayerNorm forward/backward,
+bias gradient, fused softmax cross-entropy (loss + dlogits in place).
+
+Gathers and scatters are checked bit-exactly: the embedding forward in fp32 is
+one fp32 add (the fp32 build of the oracle does the same add), and the
+embedding backward is fed small integers, whose sums are exact in any order.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.pyoracle import Ops
+from scratch_gpt_step_train_b300 import inputs
+from scratch_gpt_step_train_b300 import kernels as K
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+ops = Ops("double")
+ops32 = Ops("float")
+FULL = dict(B=16, T=1024, C=768, V=50257)
+
+
+def _t(x, dtype):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dtype).cuda()
+
+
+def _np(t):
+    return t.double().cpu().numpy()
+
+
+# ------------------------------------------------------------------ embedding
+
+@pytest.mark.parametrize("B,T,C,V", [(2, 37, 40, 100), (16, 1024, 768, 50257)], ids=["small", "full"])
+def test_encoder_forward_fp32_bit_exact(B, T, C, V):
+    rng = np.random.default_rng(0)
+    wte = rng.normal(0, 0.02, (V, C)).astype(np.float32)
+    wpe = rng.normal(0, 0.02, (T, C)).astype(np.float32)
+    tok = inputs.zipf_batches(1, 1, B, T, V)[0][0]
+    out = torch.empty(B, T, C, device="cuda")
+    err = K.encoder_forward(out, torch.from_numpy(tok).cuda(), _t(wte, torch.float32),
+                            _t(wpe, torch.float32), V)
+    ref = ops32.encoder_forward(tok, wte, wpe)
+    assert np.array_equal(out.cpu().numpy(), ref)
+    assert int(err[0]) == 0
+
+
+def test_encoder_forward_bf16_and_range_flag():
+    B, T, C, V = 4, 64, 128, 1000
+    rng = np.random.default_rng(1)
+    wte = _t(rng.normal(0, 0.02, (V, C)), torch.bfloat16)
+    wpe = _t(rng.normal(0, 0.02, (T, C)), torch.bfloat16)
+    tok = inputs.uniform_batch(2, B, T, V)[0]
+    out = torch.empty(B, T, C, dtype=torch.bfloat16, device="cuda")
+    err = K.encoder_forward(out, torch.from_numpy(tok).cuda(), wte, wpe, V)
+    ref = ops.encoder_forward(tok, _np(wte), _np(wpe))
+    # one RNE rounding to bf16 (unit roundoff 2^-8) of the exact fp32 sum
+    assert np.all(np.abs(_np(out) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
+    assert int(err[0]) == 0
+    bad = tok.copy()
+    bad[1, 5] = V
+    err = K.encoder_forward(out, torch.from_numpy(bad).cuda(), wte, wpe, V)
+    assert int(err[0]) & 1
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_encoder_backward_full_size_exact_indexing(dtype):
+    """integer-valued dx: every row sum is exact, so any misrouted row shows"""
+    B, T, C, V = FULL["B"], FULL["T"], FULL["C"], FULL["V"]
+    Vp = ((V + 127) // 128) * 128
+    tok = inputs.zipf_batches(2, 1, B, T, V)[0][0]
+    rng = np.random.default_rng(3)
+    dx = rng.integers(-4, 5, (B, T, C)).astype(np.float32)
+    dwte0 = rng.integers(-3, 4, (Vp, C)).astype(np.float32)
+    dwpe0 = rng.integers(-3, 4, (T, C)).astype(np.float32)
+    dwte = torch.from_numpy(dwte0).cuda()
+    dwpe = torch.from_numpy(dwpe0).cuda()
+    K.encoder_backward(dwte, dwpe, _t(dx, dtype), torch.from_numpy(tok).cuda())
+    rwte, rwpe = ops.encoder_backward(dx.astype(np.float64), tok, Vp)
+    assert np.array_equal(dwte.cpu().numpy(), dwte0 + rwte)
+    assert np.array_equal(dwpe.cpu().numpy(), dwpe0 + rwpe)
+
+
+def test_encoder_backward_real_values_and_determinism():
+    B, T, C, V = 8, 200, 64, 300
+    Vp = 384
+    tok = inputs.zipf_batches(4, 1, B, T, V)[0][0]  # long buckets for the head ids
+    dx = np.random.default_rng(5).normal(0, 1, (B, T, C)).astype(np.float32)
+    outs = []
+    for _ in range(2):
+        dwte = torch.zeros(Vp, C, device="cuda")
+        dwpe = torch.zeros(T, C, device="cuda")
+        K.encoder_backward(dwte, dwpe, _t(dx, torch.float32), torch.from_numpy(tok).cuda())
+        outs.append((dwte.cpu().numpy(), dwpe.cpu().numpy()))
+    rwte, rwpe = ops.encoder_backward(dx.astype(np.float64), tok, Vp)
+    assert_close(outs[0][0], rwte, 1e-6, "dwte")
+    assert_close(outs[0][1], rwpe, 1e-6, "dwpe")
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+# ------------------------------------------------------------------ layernorm
+
+def _ln_inputs(N, C, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(0.2, 1.3, (N, C))
+    w = rng.normal(1, 0.1, C)
+    b = rng.normal(0, 0.1, C)
+    return x, w, b
+
+
+@pytest.mark.parametrize("N,C", [(37, 200), (16384, 768), (300, 1600)], ids=["small", "full", "c1600"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_layernorm_forward(N, C, dtype):
+    x, w, b = _ln_inputs(N, C, 1)
+    xt, wt, bt = _t(x, dtype), _t(w, dtype), _t(b, dtype)
+    out = torch.empty(N, C, dtype=dtype, device="cuda")
+    mean = torch.empty(N, device="cuda")
+    rstd = torch.empty(N, device="cuda")
+    K.layernorm_forward(out, mean, rstd, xt, wt, bt)
+    ref, rm, rr = ops.layernorm_forward(_np(xt), _np(wt), _np(bt))
+    if dtype == torch.float32:
+        assert_close(_np(out), ref, 1e-5, "y")
+    else:
+        assert np.all(np.abs(_np(out) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
+    assert np.abs(mean.double().cpu().numpy() - rm).max() <= 1e-5
+    assert np.all(np.abs(rstd.double().cpu().numpy() - rr) <= 1e-5 * rr)
+
+
+@pytest.mark.parametrize("N,C", [(37, 200), (16384, 768), (300, 1600)], ids=["small", "full", "c1600"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_layernorm_backward(N, C, dtype):
+    x, w, b = _ln_inputs(N, C, 2)
+    rng = np.random.default_rng(3)
+    dy = rng.normal(0, 1, (N, C))
+    dx0 = rng.normal(0, 1, (N, C))
+    xt, wt, bt, dyt = _t(x, dtype), _t(w, dtype), _t(b, dtype), _t(dy, dtype)
+    out = torch.empty(N, C, dtype=dtype, device="cuda")
+    mean = torch.empty(N, device="cuda")
+    rstd = torch.empty(N, device="cuda")
+    K.layernorm_forward(out, mean, rstd, xt, wt, bt)
+    dx = _t(dx0, dtype)
+    dx0r = _np(dx)
+    dw0 = rng.normal(0, 1, C).astype(np.float32)
+    db0 = rng.normal(0, 1, C).astype(np.float32)
+    dw = torch.from_numpy(dw0).cuda()
+    db = torch.from_numpy(db0).cuda()
+    K.layernorm_backward(dx, dw, db, dyt, xt, wt, mean, rstd)
+    _, rm, rr = ops.layernorm_forward(_np(xt), _np(wt), _np(bt))
+    rdx, rdw, rdb = ops.layernorm_backward(_np(dyt), _np(xt), _np(wt), rm, rr)
+    tol = 1e-4 if dtype == torch.float32 else 1e-2
+    assert_close(_np(dx) - dx0r, rdx, tol, "dx")
+    assert_close(dw.double().cpu().numpy() - dw0, rdw, 1e-4, "dw")
+    assert_close(db.double().cpu().numpy() - db0, rdb, 1e-4, "db")
+
+
+# -------------------------------------------------------------- bias gradient
+
+@pytest.mark.parametrize("N,OC", [(37, 200), (16384, 2304), (16384, 3072)], ids=["small", "qkv", "fc"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_bias_grad(N, OC, dtype):
+    rng = np.random.default_rng(4)
+    dout = _t(rng.normal(0, 1, (N, OC)), dtype)
+    db0 = rng.normal(0, 1, OC).astype(np.float32)
+    db = torch.from_numpy(db0).cuda()
+    K.bias_grad(db, dout)
+    # the oracle's linear backward with a single input column: its bias
+    # gradient is the column sum of dout
+    d64 = _np(dout)
+    _, _, rdb = ops.matmul_backward(d64, np.ones((N, 1)), np.ones((OC, 1)))
+    assert_close(db.double().cpu().numpy() - db0, rdb, 1e-5, "db")
+
+
+# ------------------------------------------------------------- cross-entropy
+
+@pytest.mark.parametrize("N,V", [(37, 1000), (16384, 50257)], ids=["small", "full"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_crossentropy_fused(N, V, dtype):
+    Vp = ((V + 127) // 128) * 128
+    g = torch.Generator(device="cuda").manual_seed(5)
+    logits = (torch.randn(N, Vp, generator=g, device="cuda") * 2.0).to(dtype)
+    logits[:, V:] = 0
+    tgt = torch.from_numpy(inputs.zipf_batches(6, 1, 1, N, V)[0][1].reshape(-1)).cuda()
+    rows = np.sort(np.random.default_rng(7).choice(N, min(N, 64), replace=False))
+    z = _np(logits[torch.from_numpy(rows).cuda()])
+    losses = torch.empty(N, device="cuda")
+    dloss = 1.0 / N
+    err = K.crossentropy(logits, losses, tgt, V, dloss)
+    probs, rloss = ops.crossentropy_forward(z, tgt.cpu().numpy()[rows], V)
+    rd = ops.crossentropy_backward(probs, tgt.cpu().numpy()[rows], dloss, V)
+    got_l = losses.double().cpu().numpy()[rows]
+    assert np.all(np.abs(got_l - rloss) <= 1e-4 * np.abs(rloss) + 1e-5)
+    got_d = _np(logits[torch.from_numpy(rows).cuda()])
+    assert np.all(got_d[:, V:] == 0)
+    if dtype == torch.float32:
+        # the kernel's fast exp is good to a few ulp (relative 1e-5 is loose for it)
+        assert np.all(np.abs(got_d - rd) <= 1e-5 * np.abs(rd) + 1e-6 * dloss)
+    else:
+        assert np.all(np.abs(got_d - rd) <= 2.0 ** -8 * np.abs(rd) + 1e-6 * dloss)
+    assert int(err[0]) == 0
