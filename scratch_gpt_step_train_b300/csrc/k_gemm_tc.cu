@@ -170,42 +170,58 @@ struct EpiMaps {
     CUtensorMap part; // fp32 [splits,M,N] box 32x32x1 SW128 (split-K partials)
 };
 
+// Row-wise operand of a chunk that comes from global memory (the residual for
+// EPI_RESID, the pre-activation for EPI_GELU_BWD): 32 bf16 of this lane's row,
+// loaded one chunk ahead so the load latency hides behind the previous chunk.
+__device__ __forceinline__ void epi_prefetch(const TcParams& p, int row, int col, uint4 (&pf)[4]) {
+    const bf16* src = nullptr;
+    if (p.epi == EPI_RESID) src = p.resid + (size_t)row * p.ldr + col;
+    else if (p.epi == EPI_GELU_BWD) src = p.aux + (size_t)row * p.ldx + col;
+    const int nv = min(32, p.N - col);
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+        pf[k] = (src && row < p.M && 8 * k < nv) ? *reinterpret_cast<const uint4*>(src + 8 * k)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void unpack8_bf16(float* f, uint4 u) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
 // One warp: the 32 x 32 chunk at rows [row0, row0+32), columns [col, col+32);
-// lane = row within the chunk; v = this lane's 32 accumulator values.
+// lane = row within the chunk; v = this lane's 32 accumulator values; pf =
+// this lane's prefetched row operand (see epi_prefetch).
 __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps& m, int row0,
                                                int col, int lane, float* v, int split,
-                                               uint32_t stg) {
-    const int row = row0 + lane;
-    const bool rin = row < p.M;
+                                               uint32_t stg, const uint4 (&pf)[4]) {
     const int nv = min(32, p.N - col);  // multiple of 8
     if (p.epi == EPI_GELU_BWD) {
-        const bf16* a = p.aux + (size_t)row * p.ldx + col;
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
+        for (int k = 0; k < 4; k++) {
             float pre[8];
-            if (rin && j < nv) ld8_bf16(pre, a + j);
-            else
+            unpack8_bf16(pre, pf[k]);
 #pragma unroll
-                for (int i = 0; i < 8; i++) pre[i] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; i++) v[j + i] *= gelu_grad_fast(pre[i]);
+            for (int i = 0; i < 8; i++) v[8 * k + i] *= gelu_grad_fast(pre[i]);
         }
     } else if (p.epi != EPI_ACCUM_F32 && p.epi != EPI_PART_F32) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-            if (j < nv) {
-                if (p.bias) {
-                    float b[8];
-                    ld8_bf16(b, p.bias + col + j);
+        for (int k = 0; k < 4; k++) {
+            if (p.bias && 8 * k < nv) {
+                float b[8];
+                ld8_bf16(b, p.bias + col + 8 * k);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) v[j + i] += b[i];
-                }
-                if (p.epi == EPI_RESID && rin) {
-                    float r8[8];
-                    ld8_bf16(r8, p.resid + (size_t)row * p.ldr + col + j);
+                for (int i = 0; i < 8; i++) v[8 * k + i] += b[i];
+            }
+            if (p.epi == EPI_RESID) {
+                float r8[8];
+                unpack8_bf16(r8, pf[k]);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) v[j + i] += r8[i];
-                }
+                for (int i = 0; i < 8; i++) v[8 * k + i] += r8[i];
             }
         }
     }
@@ -236,7 +252,10 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
 }
 
 // ------------------------------------------------------------------- kernel
-template <int BN, bool A_MN, bool B_MN>
+// MC: CTA pairs (cluster of 2) on adjacent 128-row tiles of the same output
+// columns; each CTA loads its own A tile and half of the B tile, multicast to
+// both, so the pair reads B once.
+template <int BN, bool A_MN, bool B_MN, bool MC>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const __grid_constant__ EpiMaps maps, TcParams p) {
@@ -258,7 +277,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(full + 8 * s, 1);
-            mbar_init(empty + 8 * s, 1);
+            mbar_init(empty + 8 * s, MC ? 2 : 1);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(tfull + 8 * b, 1);
@@ -275,9 +294,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
     }
     __syncthreads();
+    if (MC) cluster_sync_all();  // the peer's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int tiles_mn = p.tiles_m * p.tiles_n;
+    // work units: single tiles, or (with MC) pairs of vertically adjacent tiles
+    const int rank = MC ? (int)cluster_ctarank() : 0;
+    const int units_m = MC ? (p.tiles_m + 1) / 2 : p.tiles_m;
+    const int units_mn = units_m * p.tiles_n;
+    const int num_units = units_mn * p.splits;
+    const int unit0 = MC ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int ustep = MC ? (int)gridDim.x / 2 : (int)gridDim.x;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -286,9 +312,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued = 0;  // bit s: stage s has a load in flight or landed
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                const int split = tile / tiles_mn, r = tile % tiles_mn;
-                const int tm = r % p.tiles_m, tn = r / p.tiles_m;
+            for (int u = unit0; ok && u < num_units; u += ustep) {
+                const int split = u / units_mn, r = u % units_mn;
+                const int tm = MC ? 2 * (r % units_m) + rank : r % units_m, tn = r / units_m;
                 const int k0 = split * p.k_per_split;
                 const int k1 = min(p.K, k0 + p.k_per_split);
                 const int nkb = (k1 - k0 + BK - 1) / BK;
@@ -307,7 +333,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_2d(sa, &mapA, fb, tm * BM, kk);
                         tma_load_2d(sa + 8192, &mapA, fb, tm * BM + 64, kk);
                     }
-                    if (!B_MN) {
+                    if (MC) {
+                        if (!B_MN) {
+                            tma_load_2d_mc(sb + rank * (BN / 2) * 128, &mapB, fb, kk,
+                                           tn * BN + rank * (BN / 2), 3);
+                        } else {
+#pragma unroll
+                            for (int j = rank * (BN / 128); j < (rank + 1) * (BN / 128); j++)
+                                tma_load_2d_mc(sb + j * 8192, &mapB, fb, tn * BN + 64 * j, kk, 3);
+                        }
+                    } else if (!B_MN) {
                         tma_load_2d(sb, &mapB, fb, kk, tn * BN);
                     } else {
 #pragma unroll
@@ -341,8 +376,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t ph = 0;
             int lt = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, lt++) {
-                const int split = tile / tiles_mn;
+            for (int u = unit0; ok && u < num_units; u += ustep, lt++) {
+                const int split = u / units_mn;
                 const int k0 = split * p.k_per_split;
                 const int k1 = min(p.K, k0 + p.k_per_split);
                 const int nkb = (k1 - k0 + BK - 1) / BK;
@@ -369,7 +404,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             B_MN ? sdesc(sb + k * 2048, 8192, 1024) : sdesc(sb + k * 32, 0, 1024);
                         umma_bf16(dt, ad, bd, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(empty + 8 * s);
+                    if (MC) umma_commit_mc(empty + 8 * s, 3);
+                    else umma_commit(empty + 8 * s);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -386,18 +422,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int cbeg = ((warp - 2) >> 2) * (BN / 2);
         constexpr int NCH = BN / 64;  // 32-column chunks per half
         const uint32_t stg = stg_base + (uint32_t)(warp - 2) * 4096u;
+        const bool has_pf = p.epi == EPI_RESID || p.epi == EPI_GELU_BWD;
         int lt = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, lt++) {
-            const int split = tile / tiles_mn, r = tile % tiles_mn;
-            const int tm = r % p.tiles_m, tn = r / p.tiles_m;
+        for (int u = unit0; u < num_units; u += ustep, lt++) {
+            const int split = u / units_mn, r = u % units_mn;
+            const int tm = MC ? 2 * (r % units_m) + rank : r % units_m, tn = r / units_m;
             const int b = lt & 1;
             const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+            const int row = tm * BM + q * 32 + lane;
+            uint4 pf[2][4];
+            // the first chunk's row operand does not depend on the accumulator:
+            // fetch it before waiting for the tile
+            if (has_pf) epi_prefetch(p, row, tn * BN + cbeg, pf[0]);
             bool ok = true;
             if (lane == 0) ok = mbar_wait(tfull + 8 * b, aph, abort_flag, p.err);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
             tc_fence_after();
-            const int row = tm * BM + q * 32 + lane;
             const uint32_t taddr =
                 tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cbeg);
             uint32_t buf[2][32];
@@ -405,13 +446,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait32(buf[0]);
 #pragma unroll
             for (int c = 0; c < NCH; c++) {
-                if (c + 1 < NCH) tmem_ld32_async(taddr + (uint32_t)(32 * (c + 1)), buf[(c + 1) & 1]);
+                if (c + 1 < NCH) {
+                    tmem_ld32_async(taddr + (uint32_t)(32 * (c + 1)), buf[(c + 1) & 1]);
+                    if (has_pf) epi_prefetch(p, row, tn * BN + cbeg + 32 * (c + 1), pf[(c + 1) & 1]);
+                }
                 const int col = tn * BN + cbeg + 32 * c;
                 if (col < p.N) {
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(buf[c & 1][i]);
-                    epilogue_chunk(p, maps, tm * BM + q * 32, col, lane, v, split, stg);
+                    epilogue_chunk(p, maps, tm * BM + q * 32, col, lane, v, split, stg, pf[c & 1]);
                 }
                 if (c + 1 < NCH) tmem_wait32(buf[(c + 1) & 1]);
             }
@@ -423,6 +467,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     }
     __syncthreads();
+    if (MC) cluster_sync_all();  // no multicast or remote arrive targets an exited CTA
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -456,9 +501,9 @@ EncodeTiledFn g_encode = nullptr;
 int g_num_sms = 148;
 int g_state = -1;  // -1 unknown, 0 unavailable, 1 ready
 
-template <int BN, bool AM, bool BMN>
+template <int BN, bool AM, bool BMN, bool MC>
 void set_smem_attr() {
-    cudaFuncSetAttribute(k_gemm_tc<BN, AM, BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(k_gemm_tc<BN, AM, BMN, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg<BN>::SMEM);
 }
 
@@ -510,19 +555,42 @@ bool make_epi_maps(EpiMaps* em, const GemmDesc& d, const TcParams& tp) {
     return ok;
 }
 
-template <int BN, bool AM, bool BMN>
-cudaError_t launch(const GemmDesc& d, const TcParams& tp, int grid, cudaStream_t s) {
+int g_mc_clusters = 0;  // co-resident 2-CTA clusters of the multicast kernel
+
+template <int BN, bool AM, bool BMN, bool MC>
+cudaError_t launch(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     CUtensorMap ma, mb;
     EpiMaps em;
     if (!make_epi_maps(&em, d, tp)) return cudaErrorInvalidValue;
     // A: K-major -> [M rows][K], box 64(K) x 128(M);  MN-major -> [K rows][M], box 64(M) x 64(K)
     bool ok = AM ? make_map(&ma, d.A, d.M, d.K, d.lda, 64)
                  : make_map(&ma, d.A, d.K, d.M, d.lda, BM);
+    // B: K-major box 64(K) x BN rows (half of them per CTA with multicast)
     ok = ok && (BMN ? make_map(&mb, d.B, d.N, d.K, d.ldb, 64)
-                    : make_map(&mb, d.B, d.K, d.N, d.ldb, BN));
+                    : make_map(&mb, d.B, d.K, d.N, d.ldb, MC ? BN / 2 : BN));
     if (!ok) return cudaErrorInvalidValue;
-    k_gemm_tc<BN, AM, BMN><<<grid, NUM_THREADS, Cfg<BN>::SMEM, s>>>(ma, mb, em, tp);
-    return cudaGetLastError();
+    if (!MC) {
+        const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
+        k_gemm_tc<BN, AM, BMN, false><<<grid, NUM_THREADS, Cfg<BN>::SMEM, s>>>(ma, mb, em, tp);
+        return cudaGetLastError();
+    }
+    const int units = ((tp.tiles_m + 1) / 2) * tp.tiles_n * tp.splits;
+    int clusters = g_mc_clusters > 0 ? g_mc_clusters : g_num_sms / 2;
+    if (units < clusters) clusters = units;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, AM, BMN, true>, ma, mb, em, tp);
 }
 
 }  // namespace
@@ -545,14 +613,39 @@ bool gemm_tc_available() {
         return false;
     }
     g_encode = (EncodeTiledFn)fn;
-    set_smem_attr<256, false, false>();
-    set_smem_attr<256, false, true>();
-    set_smem_attr<256, true, false>();
-    set_smem_attr<256, true, true>();
-    set_smem_attr<128, false, false>();
-    set_smem_attr<128, false, true>();
-    set_smem_attr<128, true, false>();
-    set_smem_attr<128, true, true>();
+    set_smem_attr<256, false, false, false>();
+    set_smem_attr<256, false, true, false>();
+    set_smem_attr<256, true, false, false>();
+    set_smem_attr<256, true, true, false>();
+    set_smem_attr<128, false, false, false>();
+    set_smem_attr<128, false, true, false>();
+    set_smem_attr<128, true, false, false>();
+    set_smem_attr<128, true, true, false>();
+    set_smem_attr<256, false, false, true>();
+    set_smem_attr<256, false, true, true>();
+    set_smem_attr<256, true, false, true>();
+    set_smem_attr<256, true, true, true>();
+    {
+        // how many 2-CTA clusters of the multicast kernel fit at once
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(g_num_sms);
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = Cfg<256>::SMEM;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<256, false, false, true>, &cfg) ==
+                cudaSuccess &&
+            n > 0)
+            g_mc_clusters = n < g_num_sms / 2 ? n : g_num_sms / 2;
+        cudaGetLastError();
+    }
     if (cudaGetLastError() != cudaSuccess) return false;
     g_state = 1;
     return true;
@@ -584,8 +677,12 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     if (!gemm_tc_available()) return cudaErrorNotSupported;
     if (!gemm_tc_supported(d)) return cudaErrorInvalidValue;
     const int tiles_m = (d.M + BM - 1) / BM;
+    // 128 x 256 tiles halve the operand traffic per flop against 128 x 128;
+    // narrow outputs, and products with too few tiles that cannot be split
+    // along K, take 128 x 128 tiles
+    const bool can_split = d.epi == EPI_ACCUM_F32 && d.K >= 8 * BK && scratch;
     int BN = 256;
-    if ((long)tiles_m * ((d.N + 255) / 256) < 2L * g_num_sms || d.N <= 128) BN = 128;
+    if (d.N <= 128 || (!can_split && (long)tiles_m * ((d.N + 255) / 256) < g_num_sms)) BN = 128;
     const int tiles_n = (d.N + BN - 1) / BN;
     TcParams tp;
     tp.M = d.M; tp.N = d.N; tp.K = d.K;
@@ -601,7 +698,7 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     tp.part = (float*)scratch;
     tp.err = err;
     const long tiles = (long)tiles_m * tiles_n;
-    if (d.epi == EPI_ACCUM_F32 && tiles < g_num_sms && d.K >= 8 * BK && scratch) {
+    if (can_split && tiles < g_num_sms) {
         int splits = (int)((2L * g_num_sms + tiles - 1) / tiles);
         int kb = (d.K + BK - 1) / BK;
         if (splits > kb / 4) splits = kb / 4;
@@ -615,19 +712,24 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
         }
     }
     tp.num_tiles = (int)(tiles * tp.splits);
-    const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
     const bool am = !d.a_kmajor, bm = !d.b_kmajor;
+    const bool mc = BN == 256 && tiles_m >= 2;
     cudaError_t e;
-    if (BN == 256) {
-        if (!am && !bm) e = launch<256, false, false>(d, tp, grid, s);
-        else if (!am && bm) e = launch<256, false, true>(d, tp, grid, s);
-        else if (am && !bm) e = launch<256, true, false>(d, tp, grid, s);
-        else e = launch<256, true, true>(d, tp, grid, s);
+    if (BN == 256 && mc) {
+        if (!am && !bm) e = launch<256, false, false, true>(d, tp, s);
+        else if (!am && bm) e = launch<256, false, true, true>(d, tp, s);
+        else if (am && !bm) e = launch<256, true, false, true>(d, tp, s);
+        else e = launch<256, true, true, true>(d, tp, s);
+    } else if (BN == 256) {
+        if (!am && !bm) e = launch<256, false, false, false>(d, tp, s);
+        else if (!am && bm) e = launch<256, false, true, false>(d, tp, s);
+        else if (am && !bm) e = launch<256, true, false, false>(d, tp, s);
+        else e = launch<256, true, true, false>(d, tp, s);
     } else {
-        if (!am && !bm) e = launch<128, false, false>(d, tp, grid, s);
-        else if (!am && bm) e = launch<128, false, true>(d, tp, grid, s);
-        else if (am && !bm) e = launch<128, true, false>(d, tp, grid, s);
-        else e = launch<128, true, true>(d, tp, grid, s);
+        if (!am && !bm) e = launch<128, false, false, false>(d, tp, s);
+        else if (!am && bm) e = launch<128, false, true, false>(d, tp, s);
+        else if (am && !bm) e = launch<128, true, false, false>(d, tp, s);
+        else e = launch<128, true, true, false>(d, tp, s);
     }
     if (e != cudaSuccess) return e;
     if (nlaunch) *nlaunch = 1;
