@@ -37,13 +37,26 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `ns` nanoseconds pass, instead of spinning on the issue slots
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait for the phase of parity `parity` to complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* err) {
     if (mbar_try(bar, parity)) return true;
     long long t0 = clock64();
     while (true) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try_sleep(bar, parity, 200000u)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > WAIT_LIMIT) {
             *abort_flag = 1;
