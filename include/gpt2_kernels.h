@@ -70,6 +70,27 @@ int gpt2k_layernorm_backward(int dtype, void* dx, float* dw, float* db, const vo
                              const void* x, const void* w, const float* mean, const float* rstd,
                              int N, int C, void* scratch, void* stream);
 
+/* Allocation-free LayerNorm backward.  The pages have no counterpart: this
+ * is the same computation as gpt2k_layernorm_backward for callers that cannot
+ * allocate device memory -- their memory belongs to another allocator that
+ * gives them only the operation's tensors, or they run where cudaMalloc /
+ * cudaFree must not be called (both may synchronise the device).  Instead of
+ * caller scratch it uses a fixed array in device global memory (4.6 MiB,
+ * enough for rows of C <= 2048) that every GPU which loads the library holds
+ * until the process exits.  It allocates nothing and calls no allocating
+ * routine.
+ *  - Returns -1 (GPT2_ERR_ARG) for C > 2048 (beyond the fixed scratch) or a bad
+ *    shape, -2 if the array's device address cannot be found or a launch fails.
+ *  - The first call on each device looks up the array's address with that
+ *    device current; make that first call before any stream capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU (on
+ *    different streams) race.  Each call fully overwrites the part it uses, so
+ *    contents left by an earlier call are harmless. */
+int gpt2k_layernorm_backward_noalloc(int dtype, void* dx, float* dw, float* db,
+                                     const void* dout, const void* x, const void* w,
+                                     const float* mean, const float* rstd, int N, int C,
+                                     void* stream);
+
 /* Token + position embedding: out[b,t,:] = wte[tok[b,t],:] + wpe[t,:].
  * Backward ACCUMULATES dwte[tok[b,t],:] += dx[b,t,:] (each row's sum taken
  * in position order, no atomics) and dwpe[t,:] += sum_b dx[b,t,:]. */

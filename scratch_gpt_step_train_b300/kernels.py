@@ -20,6 +20,8 @@ SIGNATURES = {
     "gpt2k_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2k_layernorm_backward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp,
                                       _vp]),
+    "gpt2k_layernorm_backward_noalloc": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i,
+                                              _i, _vp]),
     "gpt2k_encoder_forward": (_i, [_i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "gpt2k_encoder_backward_scratch_bytes": (_sz, [_i, _i, _i, _i]),
     "gpt2k_encoder_backward": (_i, [_i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
@@ -128,6 +130,16 @@ def layernorm_backward(dx, dw, db, dout, x, w, mean, rstd):
     _ck(L.gpt2k_layernorm_backward(_dt(x), _p(dx), _p(dw), _p(db), _p(dout), _p(x), _p(w),
                                    _p(mean), _p(rstd), N, C, _p(scratch), _stream()),
         "layernorm_backward")
+
+
+def layernorm_backward_noalloc(dx, dw, db, dout, x, w, mean, rstd):
+    """As layernorm_backward, with the library's fixed device scratch instead
+    of an allocation (for callers that cannot allocate; C <= 2048)."""
+    N, C = x.shape
+    rc = klib().gpt2k_layernorm_backward_noalloc(_dt(x), _p(dx), _p(dw), _p(db), _p(dout),
+                                                 _p(x), _p(w), _p(mean), _p(rstd), N, C,
+                                                 _stream())
+    _ck(rc, "layernorm_backward_noalloc")
 
 
 def encoder_forward(out, tok, wte, wpe, V, err=None):
