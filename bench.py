@@ -58,6 +58,36 @@ def flops_per_token(w):
     return 6 * n_params(w["L"], w["C"], w["V"], w["T"]) + 6 * w["L"] * w["C"] * w["T"]
 
 
+def kernel_sources_hash():
+    """sha256 over the CUDA sources (file names and contents, sorted)"""
+    import hashlib
+    d = os.path.join(ROOT, "scratch_gpt_step_train_b300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch of each kernel class, from the committed ncu
+    summary; None when the kernels changed after the counters were taken."""
+    p = os.path.join(ROOT, "profiles", f"dram_traffic_gpt2_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    out, sha = {}, None
+    for line in open(p):
+        line = line.strip()
+        if line.startswith("# kernel_sources_sha256"):
+            sha = line.split()[-1]
+        elif line and not line.startswith("#"):
+            name, val = line.split()[:2]
+            out[name] = float(val)
+    if sha != kernel_sources_hash():
+        return None
+    return out
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -322,17 +352,20 @@ def main():
     mfu = value / world * fpt / (peak_tf * 1e12)
 
     dom, (dms, dn, dfl, dby) = r["dom"], r["dprof"]
+    traffic = load_traffic(args.workload)
+    traffic = traffic.get(dom) if traffic else None
     if dfl > 0:
         achieved = dfl / dn / (dms / dn / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
                 "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
-                "traffic": None, "peak_kind": f"bf16 sustained ({peak_kind})",
+                "traffic": traffic, "algorithmic_bytes": dby / dn,
+                "peak_kind": f"bf16 sustained ({peak_kind})",
                 "launches": dn, "avg_launch_ms": dms / dn}
     else:
         achieved = dby / dn / (dms / dn / 1e3) / 1e9
         hbm = peaks.get("hbm_gbs", 6400.0)
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
-                "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                 "peak_kind": f"hbm copy ({peak_kind})", "launches": dn,
                 "avg_launch_ms": dms / dn}
 

@@ -29,11 +29,18 @@ using namespace gk;
 // kernel classes for event timing
 // ---------------------------------------------------------------------------
 enum {
-    K_MM_FWD, K_MM_CLS_FWD, K_MM_DX, K_MM_DW, K_ATTN_FWD, K_ATTN_BWD, K_LN_FWD, K_LN_BWD,
-    K_XENT, K_EMB_FWD, K_EMB_BWD, K_BIAS, K_ADAM, K_ZERO, K_NCLASS
+    // linear layers, one class per (layer, direction)
+    K_QKV_FWD, K_PROJ_FWD, K_FC_FWD, K_FCPROJ_FWD, K_CLS_FWD,
+    K_QKV_DX, K_PROJ_DX, K_FC_DX, K_FCPROJ_DX, K_CLS_DX,
+    K_QKV_DW, K_PROJ_DW, K_FC_DW, K_FCPROJ_DW, K_CLS_DW,
+    K_ATTN_FWD, K_ATTN_BWD, K_LN_FWD, K_LN_BWD, K_XENT, K_EMB_FWD, K_EMB_BWD, K_BIAS, K_ADAM,
+    K_ZERO, K_NCLASS
 };
 static const char* kClassNames[K_NCLASS] = {
-    "matmul_fwd", "matmul_classifier_fwd", "matmul_bwd_dx", "matmul_bwd_dw", "attention_fwd",
+    "matmul_qkv_fwd", "matmul_proj_fwd", "matmul_fc_fwd", "matmul_fcproj_fwd",
+    "matmul_classifier_fwd", "matmul_qkv_dx", "matmul_proj_dx", "matmul_fc_dx",
+    "matmul_fcproj_dx", "matmul_classifier_dx", "matmul_qkv_dw", "matmul_proj_dw",
+    "matmul_fc_dw", "matmul_fcproj_dw", "matmul_classifier_dw", "attention_fwd",
     "attention_bwd", "layernorm_fwd", "layernorm_bwd", "crossentropy", "embedding_fwd",
     "embedding_bwd", "bias_grad", "adamw", "zero_grad"};
 
@@ -448,7 +455,7 @@ static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
         GemmDesc d = gd(BT, 3 * C, C, ln1, C, 1, pc_tensor(g, P_QKVW, l), C, 1, qkv, 3 * C,
                         EPI_STORE);
         d.bias = pc_tensor(g, P_QKVB, l);
-        RUN(mm(g, K_MM_FWD, d));
+        RUN(mm(g, K_QKV_FWD, d));
         // causal attention flops: QK^T and PV over the lower triangle
         double afl = 2.0 * 2.0 * B * H * ((double)T * (T + 1) / 2) * (C / H);
         LAUNCH(K_ATTN_FWD, 1, afl, as * 4.0 * bt * c + 4.0 * B * H * T,
@@ -457,7 +464,7 @@ static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
         d.bias = pc_tensor(g, P_PROJB, l);
         d.resid = resid;
         d.ldr = C;
-        RUN(mm(g, K_MM_FWD, d));
+        RUN(mm(g, K_PROJ_FWD, d));
         LAUNCH(K_LN_FWD, 1, 0, ln_bytes,
                layernorm_forward(g->act, ln2, g->ln2_mean + l * bt, g->ln2_rstd + l * bt, x1,
                                  pc_tensor(g, P_LN2W, l), pc_tensor(g, P_LN2B, l), BT, C,
@@ -466,13 +473,13 @@ static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
         d.bias = pc_tensor(g, P_FCB, l);
         d.aux = fch;
         d.ldx = 4 * C;
-        RUN(mm(g, K_MM_FWD, d));
+        RUN(mm(g, K_FC_FWD, d));
         d = gd(BT, C, 4 * C, fchg, 4 * C, 1, pc_tensor(g, P_FCPROJW, l), 4 * C, 1, x2, C,
                EPI_RESID);
         d.bias = pc_tensor(g, P_FCPROJB, l);
         d.resid = x1;
         d.ldr = C;
-        RUN(mm(g, K_MM_FWD, d));
+        RUN(mm(g, K_FCPROJ_FWD, d));
         resid = x2;
     }
     LAUNCH(K_LN_FWD, 1, 0, ln_bytes,
@@ -480,7 +487,7 @@ static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
                              pc_tensor(g, P_LNFW, 0), pc_tensor(g, P_LNFB, 0), BT, C, g->stream));
     GemmDesc d = gd(BT, Vp, C, g->lnf, C, 1, pc_tensor(g, P_WTE, 0), C, 1, g->logits, Vp,
                     EPI_STORE);
-    RUN(mm(g, K_MM_CLS_FWD, d));
+    RUN(mm(g, K_CLS_FWD, d));
     g->have_targets = with_targets ? 1 : 0;
     g->logits_valid = with_targets ? 0 : 1;
     g->have_fwd = 1;
@@ -536,10 +543,10 @@ extern "C" int gpt2_backward(gpt2_t* g) {
     // classifier: dlogits sit in the logits buffer
     GemmDesc d = gd(BT, C, Vp, g->logits, Vp, 1, pc_tensor(g, P_WTE, 0), C, 0, g->dln, C,
                     EPI_STORE);
-    RUN(mm(g, K_MM_DX, d));
+    RUN(mm(g, K_CLS_DX, d));
     d = gd(Vp, C, BT, g->logits, Vp, 0, g->lnf, C, 0, grad_tensor(g, P_WTE, 0), C,
            EPI_ACCUM_F32);
-    RUN(mm(g, K_MM_DW, d));
+    RUN(mm(g, K_CLS_DW, d));
     CK(cudaMemsetAsync(dres, 0, bt * c * as, g->stream));
     const void* xL = L > 0 ? act_at(g, g->x2, bt * c, L - 1) : g->encoded;
     double lnb_bytes = as * 4.0 * bt * c + 8.0 * bt;
@@ -560,7 +567,7 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         // MLP: x2 = x1 + fcproj(gelu(fc(ln2(x1))))
         d = gd(C, 4 * C, BT, dres, C, 0, fchg, 4 * C, 0, grad_tensor(g, P_FCPROJW, l), 4 * C,
                EPI_ACCUM_F32);
-        RUN(mm(g, K_MM_DW, d));
+        RUN(mm(g, K_FCPROJ_DW, d));
         LAUNCH(K_BIAS, 2, 0, as * bt * c,
                bias_grad(g->act, grad_tensor(g, P_FCPROJB, l), dres, BT, C, g->scratch,
                          g->stream));
@@ -568,16 +575,16 @@ extern "C" int gpt2_backward(gpt2_t* g) {
                EPI_GELU_BWD);
         d.aux = fch;
         d.ldx = 4 * C;
-        RUN(mm(g, K_MM_DX, d));
+        RUN(mm(g, K_FCPROJ_DX, d));
         d = gd(4 * C, C, BT, g->dbig, 4 * C, 0, ln2, C, 0, grad_tensor(g, P_FCW, l), C,
                EPI_ACCUM_F32);
-        RUN(mm(g, K_MM_DW, d));
+        RUN(mm(g, K_FC_DW, d));
         LAUNCH(K_BIAS, 2, 0, as * bt * 4 * c,
                bias_grad(g->act, grad_tensor(g, P_FCB, l), g->dbig, BT, 4 * C, g->scratch,
                          g->stream));
         d = gd(BT, C, 4 * C, g->dbig, 4 * C, 1, pc_tensor(g, P_FCW, l), C, 0, g->dln, C,
                EPI_STORE);
-        RUN(mm(g, K_MM_DX, d));
+        RUN(mm(g, K_FC_DX, d));
         LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
                layernorm_backward(g->act, dres, grad_tensor(g, P_LN2W, l),
                                   grad_tensor(g, P_LN2B, l), g->dln, x1, pc_tensor(g, P_LN2W, l),
@@ -585,25 +592,25 @@ extern "C" int gpt2_backward(gpt2_t* g) {
                                   g->stream));
         // attention: x1 = rin + proj(attn(qkv(ln1(rin))))
         d = gd(C, C, BT, dres, C, 0, atty, C, 0, grad_tensor(g, P_PROJW, l), C, EPI_ACCUM_F32);
-        RUN(mm(g, K_MM_DW, d));
+        RUN(mm(g, K_PROJ_DW, d));
         LAUNCH(K_BIAS, 2, 0, as * bt * c,
                bias_grad(g->act, grad_tensor(g, P_PROJB, l), dres, BT, C, g->scratch,
                          g->stream));
         d = gd(BT, C, C, dres, C, 1, pc_tensor(g, P_PROJW, l), C, 0, g->datty, C, EPI_STORE);
-        RUN(mm(g, K_MM_DX, d));
+        RUN(mm(g, K_PROJ_DX, d));
         double afl = 2.5 * 2.0 * 2.0 * B * H * ((double)T * (T + 1) / 2) * (C / H);
         LAUNCH(K_ATTN_BWD, 3, afl, as * 8.0 * bt * c,
                attention_backward(g->act, g->dqkv, g->datty, qkv, atty, lse, B, T, C, H,
                                   g->scratch, g->err, g->stream));
         d = gd(3 * C, C, BT, g->dqkv, 3 * C, 0, ln1, C, 0, grad_tensor(g, P_QKVW, l), C,
                EPI_ACCUM_F32);
-        RUN(mm(g, K_MM_DW, d));
+        RUN(mm(g, K_QKV_DW, d));
         LAUNCH(K_BIAS, 2, 0, as * bt * 3 * c,
                bias_grad(g->act, grad_tensor(g, P_QKVB, l), g->dqkv, BT, 3 * C, g->scratch,
                          g->stream));
         d = gd(BT, C, 3 * C, g->dqkv, 3 * C, 1, pc_tensor(g, P_QKVW, l), C, 0, g->dln, C,
                EPI_STORE);
-        RUN(mm(g, K_MM_DX, d));
+        RUN(mm(g, K_QKV_DX, d));
         LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
                layernorm_backward(g->act, dres, grad_tensor(g, P_LN1W, l),
                                   grad_tensor(g, P_LN1B, l), g->dln, rin, pc_tensor(g, P_LN1W, l),

@@ -62,6 +62,7 @@ struct Cfg {
 struct TcParams {
     int M, N, K;
     int tiles_m, tiles_n, splits, k_per_split, num_tiles;
+    int n_fastest;  // work-unit order: 1 = output-column tiles vary fastest
     int epi;
     void* D;
     long ldd;
@@ -314,7 +315,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int u = unit0; ok && u < num_units; u += ustep) {
                 const int split = u / units_mn, r = u % units_mn;
-                const int tm = MC ? 2 * (r % units_m) + rank : r % units_m, tn = r / units_m;
+                const int um = p.n_fastest ? r / p.tiles_n : r % units_m;
+                const int tn = p.n_fastest ? r % p.tiles_n : r / units_m;
+                const int tm = MC ? 2 * um + rank : um;
                 const int k0 = split * p.k_per_split;
                 const int k1 = min(p.K, k0 + p.k_per_split);
                 const int nkb = (k1 - k0 + BK - 1) / BK;
@@ -426,7 +429,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int lt = 0;
         for (int u = unit0; u < num_units; u += ustep, lt++) {
             const int split = u / units_mn, r = u % units_mn;
-            const int tm = MC ? 2 * (r % units_m) + rank : r % units_m, tn = r / units_m;
+            const int um = p.n_fastest ? r / p.tiles_n : r % units_m;
+            const int tn = p.n_fastest ? r % p.tiles_n : r / units_m;
+            const int tm = MC ? 2 * um + rank : um;
             const int b = lt & 1;
             const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
             const int row = tm * BM + q * 32 + lane;
@@ -690,6 +695,9 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     tp.tiles_n = tiles_n;
     tp.splits = 1;
     tp.k_per_split = ((d.K + BK - 1) / BK) * BK;
+    // the larger operand is streamed once when the tiles that share it run
+    // side by side: output-column tiles fastest when A (M x K) is the larger
+    tp.n_fastest = d.M > d.N ? 1 : 0;
     tp.epi = d.epi;
     tp.D = d.D; tp.ldd = d.ldd;
     tp.bias = (const bf16*)d.bias;

@@ -119,13 +119,19 @@ def test_matmul_accumulate_fp32(a_km, b_km, Kd):
 # bench runs them; the oracle computes a sample of 48 output rows.
 FULL = [
     ("qkv_fwd", 16384, 2304, 768, True, True, "store"),
+    ("proj_fwd", 16384, 768, 768, True, True, "resid"),
     ("fc_fwd", 16384, 3072, 768, True, True, "gelu"),
     ("fcproj_fwd", 16384, 768, 3072, True, True, "resid"),
     ("classifier_fwd", 16384, 50304, 768, True, True, "store"),
+    ("qkv_dx", 16384, 768, 2304, True, False, "store"),
+    ("proj_dx", 16384, 768, 768, True, False, "store"),
+    ("fc_dx", 16384, 768, 3072, True, False, "store"),
     ("fcproj_dx", 16384, 3072, 768, True, False, "gelu_bwd"),
     ("classifier_dx", 16384, 768, 50304, True, False, "store"),
-    ("fc_dw", 3072, 768, 16384, False, False, "accum_f32"),
+    ("qkv_dw", 2304, 768, 16384, False, False, "accum_f32"),
     ("proj_dw", 768, 768, 16384, False, False, "accum_f32"),
+    ("fc_dw", 3072, 768, 16384, False, False, "accum_f32"),
+    ("fcproj_dw", 768, 3072, 16384, False, False, "accum_f32"),
     ("classifier_dw", 50304, 768, 16384, False, False, "accum_f32"),
 ]
 
