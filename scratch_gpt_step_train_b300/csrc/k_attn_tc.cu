@@ -64,11 +64,12 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// lane 0 waits, the warp learns the outcome
+// lane 0 waits (polling: these waits are on the critical path), the warp
+// learns the outcome
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* err, int lane) {
     bool ok = true;
-    if (lane == 0) ok = mbar_wait(bar, parity, abort_flag, err);
+    if (lane == 0) ok = mbar_wait_spin(bar, parity, abort_flag, err);
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
@@ -88,8 +89,11 @@ __device__ __forceinline__ void st_row32(uint32_t tile, int r, int c0, const uin
     }
 }
 
-__global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_constant__ CUtensorMap map,
-                                                             AttnParams p) {
+constexpr int FWD_THREADS = 288;  // warp 0: TMA (lane 0) + MMA (lane 1); 8 softmax warps
+constexpr float RESCALE_SLACK = 8.0f;  // log2 units: P stays <= 2^8 between rescales
+
+__global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_constant__ CUtensorMap map,
+                                                                AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
     float* red = (float*)(base_gen + F_RED);  // [2 buffers][2 halves][128 rows]
     float* lsum = (float*)(base_gen + F_LS);  // [2 halves][128 rows]
     const uint32_t bar = base + F_BAR;
-    // full[3], empty[3] for the ring; q; s (S ready); pf (P ready); o (O_j ready)
+    // full[3], empty[3] for the ring; q; s (S ready); pf (P ready); o (P.V done)
     const uint32_t b_full = bar, b_empty = bar + 24, b_q = bar + 48, b_sfull = bar + 56,
                    b_pfull = bar + 64, b_ofull = bar + 72;
     uint32_t* tmem_slot = (uint32_t*)(base_gen + F_BAR + 128);
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map) : "memory");
     }
-    if (warp == 1) {
+    if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), 256);
         tmem_relinquish();
         tc_fence_before();
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 128;
+    const uint32_t tS = tmem, tO = tmem + 128;  // S [128 x 128], O [128 x 64] fp32
 
     if (warp == 0) {
         if (lane == 0) {
@@ -162,38 +166,40 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
                 while (!mbar_try(b_q, 0) && clock64() - t0 < WAIT_LIMIT) {
                 }
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
+        } else if (lane == 1) {
             // ----------------------------------------------------------- MMA
             constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
+            // descriptors are built once; a K step advances the start address
+            // field (bits 0..13, in 16-byte units) by a constant
+            const uint64_t dQ = sdesc(sQ, 0, 1024), dP = sdesc(sP, 0, 1024);
+            const uint64_t dRingK = sdesc(sRing, 0, 1024), dRingV = sdesc(sRing, 8192, 1024);
             auto issue_s = [&](int j) -> bool {
                 const int it = 2 * j, s = it % 3;
-                if (!mbar_wait(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) return false;
+                if (!mbar_wait_spin(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
-                const uint32_t sk = sRing + s * TILE_BYTES;
+                const uint64_t dK = dRingK + (uint64_t)((s * TILE_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
-                    umma_bf16(tS, sdesc(sQ + k * 32, 0, 1024), sdesc(sk + k * 32, 0, 1024), ID_S,
-                              k > 0);
+                    umma_bf16(tS, dQ + (uint64_t)(k * 2), dK + (uint64_t)(k * 2), ID_S, k > 0);
                 umma_commit(b_sfull);
                 umma_commit(b_empty + 8 * s);
                 return true;
             };
             bool ok = mbar_wait(b_q, 0, abort_flag, p.err) && issue_s(0);
             for (int j = 0; ok && j < nkt; j++) {
-                if (!mbar_wait(b_pfull, j & 1, abort_flag, p.err)) break;
+                if (!mbar_wait_spin(b_pfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 if (j + 1 < nkt && !issue_s(j + 1)) break;
                 const int it = 2 * j + 1, s = it % 3;
-                if (!mbar_wait(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) break;
+                if (!mbar_wait_spin(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                const uint32_t sv = sRing + s * TILE_BYTES;
+                const uint64_t dV = dRingV + (uint64_t)((s * TILE_BYTES) >> 4);
+                // O += P_j V_j (O starts at the first tile)
 #pragma unroll
                 for (int k = 0; k < TILE / 16; k++)
-                    umma_bf16(tO, sdesc(sP + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024),
-                              sdesc(sv + k * 2048, 8192, 1024), ID_O, k > 0);
+                    umma_bf16(tO, dP + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                              dV + (uint64_t)(k * 128), ID_O, (j > 0 || k > 0) ? 1u : 0u);
                 umma_commit(b_ofull);
                 umma_commit(b_empty + 8 * s);
             }
@@ -201,78 +207,72 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
     } else {
         // ------------------------------------------------------- softmax
         // warp pair (w, w+4) shares TMEM lane quarter w & 3: half 0 takes keys
-        // [0,64) of each tile and output columns [0,32), half 1 the rest
-        const int q = warp & 3, hf = (warp - 2) >> 2;
+        // [0,64) of each tile and output columns [0,32), half 1 the rest.
+        // O accumulates in TMEM; the running max m used for P is raised (and O,
+        // l rescaled) only when the row max exceeds it by more than 2^8, so P
+        // stays <= 256 and most tiles need no rescale.
+        const int q = warp & 3, hf = (warp - 1) >> 2;
         const int r = q * 32 + lane;
         const int qi = qt * TILE + r;
         const uint32_t loff = (uint32_t)(q * 32) << 16;
         const int kb = hf * 64;
-        float o[32];
-#pragma unroll
-        for (int i = 0; i < 32; i++) o[i] = 0.f;
-        float m2 = -INFINITY, l = 0.f;
+        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkt; j++) {
-            if (j > 0 && !warp_wait(b_ofull, (j - 1) & 1, abort_flag, p.err, lane)) {
-                ok = false;
-                break;
-            }
             if (!warp_wait(b_sfull, j & 1, abort_flag, p.err, lane)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            if (j > 0) {
+            uint32_t sv[2][32];
+            tmem_ld32_async(tS + loff + kb, sv[0]);
+            tmem_ld32_async(tS + loff + kb + 32, sv[1]);
+            tmem_wait32(sv[0]);
+            tmem_wait32(sv[1]);
+            if (j == qt) {  // causal mask of the diagonal tile: keys > row
+#pragma unroll
+                for (int c = 0; c < 2; c++)
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        if (kb + 32 * c + i > r) sv[c][i] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 2; c++)
+#pragma unroll
+                for (int i = 0; i < 32; i++) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
+            float* rb = red + (j & 1) * 256;
+            rb[hf * 128 + r] = mx;
+            named_sync_softmax();
+            const float mrow = fmaxf(rb[r], rb[128 + r]) * p.scale_log2;
+            const bool need = mrow > m_used + RESCALE_SLACK;
+            const float m_new = need ? mrow : m_used;
+            // P.V of the previous tile must be done: it reads the P buffer and
+            // writes O, which a rescale rewrites
+            if (j > 0 && !warp_wait(b_ofull, (j - 1) & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                const float corr = need ? ex2(m_used - m_new) : 1.f;
                 uint32_t t[32];
                 tmem_ld32_async(tO + loff + hf * 32, t);
                 tmem_wait32(t);
 #pragma unroll
-                for (int i = 0; i < 32; i++) o[i] += __uint_as_float(t[i]);
+                for (int i = 0; i < 32; i++) t[i] = __float_as_uint(__uint_as_float(t[i]) * corr);
+                tmem_st32(tO + loff + hf * 32, t);
+                l *= corr;
             }
-            // Only the diagonal tile needs the causal mask; the max is taken on
-            // raw scores (the scale is positive) and scaled once.
-            const bool diag = (j == qt);
-            float mx = -INFINITY;
+            m_used = m_new;
 #pragma unroll
             for (int c = 0; c < 2; c++) {
-                uint32_t sv[32];
-                tmem_ld32_async(tS + loff + kb + 32 * c, sv);
-                tmem_wait32(sv);
-                if (!diag) {
-#pragma unroll
-                    for (int i = 0; i < 32; i++) mx = fmaxf(mx, __uint_as_float(sv[i]));
-                } else {
-                    const int lim = r - (kb + 32 * c);  // keys i <= lim are visible
-#pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        mx = fmaxf(mx, i <= lim ? __uint_as_float(sv[i]) : -INFINITY);
-                }
-            }
-            float* rb = red + (j & 1) * 256;
-            rb[hf * 128 + r] = mx;
-            named_sync_softmax();
-            mx = fmaxf(rb[r], rb[128 + r]) * p.scale_log2;
-            const float mn = fmaxf(m2, mx);
-            const float corr = ex2(m2 - mn);
-            l *= corr;
-#pragma unroll
-            for (int i = 0; i < 32; i++) o[i] *= corr;
-            m2 = mn;
-#pragma unroll
-            for (int c = 0; c < 2; c++) {
-                uint32_t sv[32];
-                tmem_ld32_async(tS + loff + kb + 32 * c, sv);
-                tmem_wait32(sv);
                 uint32_t pk[16];
-                const int lim = diag ? r - (kb + 32 * c) : 64;
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
-                    float a = ex2(fmaf(__uint_as_float(sv[2 * i]), p.scale_log2, -mn));
-                    float e = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), p.scale_log2, -mn));
-                    if (diag) {
-                        a = 2 * i <= lim ? a : 0.f;
-                        e = 2 * i + 1 <= lim ? e : 0.f;
-                    }
+                    const float a = ex2(fmaf(__uint_as_float(sv[c][2 * i]), p.scale_log2, -m_used));
+                    const float e =
+                        ex2(fmaf(__uint_as_float(sv[c][2 * i + 1]), p.scale_log2, -m_used));
                     l += a + e;
                     pk[i] = pack_bf16x2(a, e);
                 }
@@ -284,13 +284,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
             if (lane == 0) mbar_arrive(b_pfull);
         }
         bool fin = ok && warp_wait(b_ofull, (nkt - 1) & 1, abort_flag, p.err, lane);
+        uint32_t t[32];
         if (fin) {
             tc_fence_after();
-            uint32_t t[32];
             tmem_ld32_async(tO + loff + hf * 32, t);
             tmem_wait32(t);
-#pragma unroll
-            for (int i = 0; i < 32; i++) o[i] += __uint_as_float(t[i]);
         }
         // fold the two halves' row sums (every softmax thread reaches this)
         lsum[hf * 128 + r] = l;
@@ -302,18 +300,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_fwd_tc(const __grid_con
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
                 uint4 u;
-                u.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
-                u.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
-                u.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
-                u.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
+                u.x = pack_bf16x2(__uint_as_float(t[i]) * inv, __uint_as_float(t[i + 1]) * inv);
+                u.y = pack_bf16x2(__uint_as_float(t[i + 2]) * inv, __uint_as_float(t[i + 3]) * inv);
+                u.z = pack_bf16x2(__uint_as_float(t[i + 4]) * inv, __uint_as_float(t[i + 5]) * inv);
+                u.w = pack_bf16x2(__uint_as_float(t[i + 6]) * inv, __uint_as_float(t[i + 7]) * inv);
                 *reinterpret_cast<uint4*>(dst + i) = u;
             }
-            if (hf == 0) p.lse[(size_t)bh * p.T + qi] = (m2 + log2f(lt)) * 0.6931471805599453f;
+            if (hf == 0) p.lse[(size_t)bh * p.T + qi] = (m_used + log2f(lt)) * 0.6931471805599453f;
         }
         tc_fence_before();
     }
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 0) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 256);
@@ -429,30 +427,31 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
+            // descriptors built once; K steps add constant start-address offsets
+            const uint64_t dK = sdesc(sK, 0, 1024), dV = sdesc(sV, 0, 1024);
+            const uint64_t dPT = sdesc(sPT, 0, 1024), dDST = sdesc(sDST, 0, 1024);
             bool ok = mbar_wait(b_kv, 0, abort_flag, p.err);
             for (int n = 0; ok && n < nq; n++) {
                 const int s = n & 1, u = n >> 1;
-                if (!mbar_wait(s ? b_qdf1 : b_qdf0, u & 1, abort_flag, p.err)) break;
+                if (!mbar_wait_spin(s ? b_qdf1 : b_qdf0, u & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t sq = base + (s ? B_Q1 : B_Q0), sd = base + (s ? B_DO1 : B_DO0);
+                const uint64_t dq_k = sdesc(sq, 0, 1024), dd_k = sdesc(sd, 0, 1024);
+                const uint64_t dq_m = sdesc(sq, 8192, 1024), dd_m = sdesc(sd, 8192, 1024);
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
-                    umma_bf16(tST, sdesc(sK + k * 32, 0, 1024), sdesc(sq + k * 32, 0, 1024), ID_S,
-                              k > 0);
+                    umma_bf16(tST, dK + (uint64_t)(2 * k), dq_k + (uint64_t)(2 * k), ID_S, k > 0);
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
-                    umma_bf16(tDPT, sdesc(sV + k * 32, 0, 1024), sdesc(sd + k * 32, 0, 1024),
-                              ID_S, k > 0);
+                    umma_bf16(tDPT, dV + (uint64_t)(2 * k), dd_k + (uint64_t)(2 * k), ID_S, k > 0);
                 umma_commit(b_sfull);
-                if (!mbar_wait(b_psfull, n & 1, abort_flag, p.err)) break;
+                if (!mbar_wait_spin(b_psfull, n & 1, abort_flag, p.err)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < TILE / 16; k++) {
-                    const uint32_t aoff = (k >> 2) * 16384 + (k & 3) * 32;
-                    umma_bf16(tDV, sdesc(sPT + aoff, 0, 1024), sdesc(sd + k * 2048, 8192, 1024),
-                              ID_O, (n > 0 || k > 0));
-                    umma_bf16(tDK, sdesc(sDST + aoff, 0, 1024), sdesc(sq + k * 2048, 8192, 1024),
-                              ID_O, (n > 0 || k > 0));
+                    const uint64_t aoff = (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+                    umma_bf16(tDV, dPT + aoff, dd_m + (uint64_t)(128 * k), ID_O, (n > 0 || k > 0));
+                    umma_bf16(tDK, dDST + aoff, dq_m + (uint64_t)(128 * k), ID_O, (n > 0 || k > 0));
                 }
                 umma_commit(s ? b_qde1 : b_qde0);
                 umma_commit(b_psfree);
@@ -659,27 +658,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
+            const uint64_t dQ = sdesc(sQ, 0, 1024), dDO = sdesc(sDO, 0, 1024);
+            const uint64_t dDS = sdesc(sDS, 0, 1024);
             bool ok = mbar_wait(b_q, 0, abort_flag, p.err);
             for (int j = 0; ok && j < nkt; j++) {
                 const int s = j & 1, u = j >> 1;
-                if (!mbar_wait(s ? b_kvf1 : b_kvf0, u & 1, abort_flag, p.err)) break;
+                if (!mbar_wait_spin(s ? b_kvf1 : b_kvf0, u & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t sk = base + (s ? Q_K1 : Q_K0), sv = base + (s ? Q_V1 : Q_V0);
+                const uint64_t dk_k = sdesc(sk, 0, 1024), dv_k = sdesc(sv, 0, 1024);
+                const uint64_t dk_m = sdesc(sk, 8192, 1024);
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
-                    umma_bf16(tS, sdesc(sQ + k * 32, 0, 1024), sdesc(sk + k * 32, 0, 1024), ID_S,
-                              k > 0);
+                    umma_bf16(tS, dQ + (uint64_t)(2 * k), dk_k + (uint64_t)(2 * k), ID_S, k > 0);
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
-                    umma_bf16(tDP, sdesc(sDO + k * 32, 0, 1024), sdesc(sv + k * 32, 0, 1024),
-                              ID_S, k > 0);
+                    umma_bf16(tDP, dDO + (uint64_t)(2 * k), dv_k + (uint64_t)(2 * k), ID_S, k > 0);
                 umma_commit(b_sfull);
-                if (!mbar_wait(b_dsfull, j & 1, abort_flag, p.err)) break;
+                if (!mbar_wait_spin(b_dsfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < TILE / 16; k++)
-                    umma_bf16(tDQ, sdesc(sDS + (k >> 2) * 16384 + (k & 3) * 32, 0, 1024),
-                              sdesc(sk + k * 2048, 8192, 1024), ID_O, (j > 0 || k > 0));
+                    umma_bf16(tDQ, dDS + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                              dk_m + (uint64_t)(128 * k), ID_O, (j > 0 || k > 0));
                 umma_commit(s ? b_kve1 : b_kve0);
                 umma_commit(b_dsfree);
             }
@@ -857,7 +858,7 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
     p.err = err;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
     dim3 grid(p.nqt, B * H);
-    k_attn_fwd_tc<<<grid, ATT_THREADS, F_SMEM, s>>>(map, p);
+    k_attn_fwd_tc<<<grid, FWD_THREADS, F_SMEM, s>>>(map, p);
     return cudaGetLastError();
 }
 

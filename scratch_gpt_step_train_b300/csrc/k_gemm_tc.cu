@@ -379,6 +379,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t ph = 0;
             int lt = 0;
             bool ok = true;
+            // stage-0 descriptors; stages and K steps add start-address offsets
+            const uint64_t dA0 = A_MN ? sdesc(tiles, 8192, 1024) : sdesc(tiles, 0, 1024);
+            const uint64_t dB0 = B_MN ? sdesc(tiles + CF::A_BYTES, 8192, 1024)
+                                      : sdesc(tiles + CF::A_BYTES, 0, 1024);
             for (int u = unit0; ok && u < num_units; u += ustep, lt++) {
                 const int split = u / units_mn;
                 const int k0 = split * p.k_per_split;
@@ -398,15 +402,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = tiles + s * CF::STAGE_BYTES, sb = sa + CF::A_BYTES;
+                    const uint64_t ad0 = dA0 + (uint64_t)((s * CF::STAGE_BYTES) >> 4);
+                    const uint64_t bd0 = dB0 + (uint64_t)((s * CF::STAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; k++) {
-                        const uint64_t ad =
-                            A_MN ? sdesc(sa + k * 2048, 8192, 1024) : sdesc(sa + k * 32, 0, 1024);
-                        const uint64_t bd =
-                            B_MN ? sdesc(sb + k * 2048, 8192, 1024) : sdesc(sb + k * 32, 0, 1024);
-                        umma_bf16(dt, ad, bd, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
-                    }
+                    for (int k = 0; k < BK / 16; k++)
+                        umma_bf16(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
+                                  bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
+                                  (kb > 0 || k > 0) ? 1u : 0u);
                     if (MC) umma_commit_mc(empty + 8 * s, 3);
                     else umma_commit(empty + 8 * s);
                     if (++s == S) {
