@@ -332,12 +332,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
 // Each CTA owns its outputs: no atomics, deterministic.  TMEM: 512 columns
 // (one CTA per SM).
 // ---------------------------------------------------------------------------
-constexpr int B_K = 0, B_V = 16384, B_Q0 = 32768, B_DO0 = 49152, B_Q1 = 65536, B_DO1 = 81920,
-              B_PT = 98304, B_DST = 131072, B_LSE = 163840, B_D = 164352, B_BAR = 164864;
-constexpr int B_SMEM = B_BAR + 256 + 1024;
+// The 128-row side of each kernel (keys in k_attn_dkv_tc, queries in
+// k_attn_dq_tc) is visited in steps of 64 on the other side, so every CTA
+// holds at most 256 TMEM columns and ~100 KB of shared memory: two CTAs share
+// an SM, and one CTA's softmax phase overlaps the other's products.
+constexpr int BWD_THREADS = 288;  // warp 0: TMA (lane 0) + MMA (lane 1); 8 softmax warps
+constexpr int SUB = 64;           // rows of the 64-wide side
+constexpr int SUB_BYTES = SUB * 128;
 
 struct AttnBwdParams {
-    int B, T, C, H, nqt;
+    int B, T, C, H, nqt, nsub;  // nsub = ceil(T / 64)
     const float* lse;  // [B,H,T] natural log
     const float* Dv;   // [B,H,T]
     bf16* dqkv;
@@ -346,26 +350,46 @@ struct AttnBwdParams {
     float scale;       // 1/sqrt(hd)
 };
 
-__global__ void __launch_bounds__(ATT_THREADS, 1)
-    k_attn_dkv_tc(const __grid_constant__ CUtensorMap map_qkv,
-                  const __grid_constant__ CUtensorMap map_do, AttnBwdParams p) {
+// row r, columns [c0, c0+32) of a 128 x 64 bf16 K-major tile (one 128-byte
+// swizzle atom column)
+__device__ __forceinline__ void st_row32_64(uint32_t tile, int r, int c0, const uint32_t* pk) {
+#pragma unroll
+    for (int cc = 0; cc < 4; cc++) {
+        const int chunk = (c0 >> 3) + cc;
+        st_shared_v4(tile + r * 128 + ((uint32_t)(chunk ^ (r & 7)) << 4), pk[4 * cc],
+                     pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+    }
+}
+
+struct BwdMaps {
+    CUtensorMap qkv128, qkv64, do128, do64;  // boxes 64 x 128 rows / 64 x 64 rows
+};
+
+// dK, dV: CTA = (128-key tile kt, batch, head); query steps of 64.
+constexpr int D_K = 0, D_V = 16384, D_Q0 = 32768, D_Q1 = 40960, D_DO0 = 49152, D_DO1 = 57344,
+              D_PT = 65536, D_DST = 81920, D_LSE = 98304, D_D = 98560, D_BAR = 98816;
+constexpr int D_SMEM = D_BAR + 256 + 1024;
+
+__global__ void __launch_bounds__(BWD_THREADS, 2)
+    k_attn_dkv_tc(const __grid_constant__ BwdMaps maps, AttnBwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw);
-    const uint32_t sK = base + B_K, sV = base + B_V, sPT = base + B_PT, sDST = base + B_DST;
-    float* lse_s = (float*)(base_gen + B_LSE);
-    float* d_s = (float*)(base_gen + B_D);
-    const uint32_t bar = base + B_BAR;
+    const uint32_t sK = base + D_K, sV = base + D_V, sPT = base + D_PT, sDST = base + D_DST;
+    float* lse_s = (float*)(base_gen + D_LSE);
+    float* d_s = (float*)(base_gen + D_D);
+    const uint32_t bar = base + D_BAR;
     const uint32_t b_kv = bar, b_qdf0 = bar + 8, b_qdf1 = bar + 16, b_qde0 = bar + 24,
                    b_qde1 = bar + 32, b_sfull = bar + 40, b_psfull = bar + 48,
                    b_psfree = bar + 56, b_acc = bar + 64;
-    uint32_t* tmem_slot = (uint32_t*)(base_gen + B_BAR + 128);
-    volatile int* abort_flag = (volatile int*)(base_gen + B_BAR + 132);
+    uint32_t* tmem_slot = (uint32_t*)(base_gen + D_BAR + 128);
+    volatile int* abort_flag = (volatile int*)(base_gen + D_BAR + 132);
 
-    const int kt = p.nqt - 1 - (int)blockIdx.x;  // fewest query tiles last
+    const int kt = p.nqt - 1 - (int)blockIdx.x;  // fewest query steps last
     const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-    const int nq = p.nqt - kt;  // query tiles kt..nqt-1
+    const int i0 = 2 * kt;       // first 64-query step that sees these keys
+    const int nq = p.nsub - i0;  // query steps
     const int row0 = b * p.T;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
 
@@ -382,52 +406,49 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
         tmem_relinquish();
         tc_fence_before();
     }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tST = tmem, tDPT = tmem + 128, tDV = tmem + 256, tDK = tmem + 320;
+    const uint32_t tST = tmem, tDPT = tmem + 64, tDV = tmem + 128, tDK = tmem + 192;
 
     if (warp == 0) {
         if (lane == 0) {
-            const int cq = h * HD, ck = p.C + h * HD, cv = 2 * p.C + h * HD;
+            const int ck = p.C + h * HD, cv = 2 * p.C + h * HD;
             mbar_expect_tx(b_kv, 2 * TILE_BYTES);
-            tma_load_2d(sK, &map_qkv, b_kv, ck, row0 + kt * TILE);
-            tma_load_2d(sV, &map_qkv, b_kv, cv, row0 + kt * TILE);
-            int issued[2] = {-1, -1};
+            tma_load_2d(sK, &maps.qkv128, b_kv, ck, row0 + kt * TILE);
+            tma_load_2d(sV, &maps.qkv128, b_kv, cv, row0 + kt * TILE);
+            int issued0 = -1, issued1 = -1;
             for (int n = 0; n < nq; n++) {
                 const int s = n & 1, u = n >> 1;
-                const uint32_t fe = s ? b_qde1 : b_qde0, ff = s ? b_qdf1 : b_qdf0;
-                if (!mbar_wait(fe, (u & 1) ^ 1, abort_flag, p.err)) break;
-                const uint32_t sq = base + (s ? B_Q1 : B_Q0), sd = base + (s ? B_DO1 : B_DO0);
-                const int qrow = row0 + (kt + n) * TILE;
-                mbar_expect_tx(ff, 2 * TILE_BYTES);
-                tma_load_2d(sq, &map_qkv, ff, cq, qrow);
-                tma_load_2d(sd, &map_do, ff, h * HD, qrow);
-                issued[s] = u;
+                if (!mbar_wait(s ? b_qde1 : b_qde0, (u & 1) ^ 1, abort_flag, p.err)) break;
+                const uint32_t ff = s ? b_qdf1 : b_qdf0;
+                const int qrow = row0 + (i0 + n) * SUB;
+                mbar_expect_tx(ff, 2 * SUB_BYTES);
+                tma_load_2d(base + (s ? D_Q1 : D_Q0), &maps.qkv64, ff, h * HD, qrow);
+                tma_load_2d(base + (s ? D_DO1 : D_DO0), &maps.do64, ff, h * HD, qrow);
+                if (s) issued1 = u;
+                else issued0 = u;
             }
             if (*abort_flag) {
                 for (int s = 0; s < 2; s++) {
-                    if (issued[s] < 0) continue;
+                    const int is = s ? issued1 : issued0;
+                    if (is < 0) continue;
                     long long t0 = clock64();
-                    while (!mbar_try(s ? b_qdf1 : b_qdf0, issued[s] & 1) &&
-                           clock64() - t0 < WAIT_LIMIT) {
+                    while (!mbar_try(s ? b_qdf1 : b_qdf0, is & 1) && clock64() - t0 < WAIT_LIMIT) {
                     }
                 }
                 long long t0 = clock64();
                 while (!mbar_try(b_kv, 0) && clock64() - t0 < WAIT_LIMIT) {
                 }
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
+        } else if (lane == 1) {
+            constexpr uint32_t ID_S = make_idesc(128, SUB, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
-            // descriptors built once; K steps add constant start-address offsets
             const uint64_t dK = sdesc(sK, 0, 1024), dV = sdesc(sV, 0, 1024);
             const uint64_t dPT = sdesc(sPT, 0, 1024), dDST = sdesc(sDST, 0, 1024);
             bool ok = mbar_wait(b_kv, 0, abort_flag, p.err);
@@ -435,9 +456,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 const int s = n & 1, u = n >> 1;
                 if (!mbar_wait_spin(s ? b_qdf1 : b_qdf0, u & 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                const uint32_t sq = base + (s ? B_Q1 : B_Q0), sd = base + (s ? B_DO1 : B_DO0);
+                const uint32_t sq = base + (s ? D_Q1 : D_Q0), sd = base + (s ? D_DO1 : D_DO0);
                 const uint64_t dq_k = sdesc(sq, 0, 1024), dd_k = sdesc(sd, 0, 1024);
                 const uint64_t dq_m = sdesc(sq, 8192, 1024), dd_m = sdesc(sd, 8192, 1024);
+                // S^T = K Q^T and dP^T = V dO^T (128 keys x 64 queries)
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
                     umma_bf16(tST, dK + (uint64_t)(2 * k), dq_k + (uint64_t)(2 * k), ID_S, k > 0);
@@ -447,11 +469,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 umma_commit(b_sfull);
                 if (!mbar_wait_spin(b_psfull, n & 1, abort_flag, p.err)) break;
                 tc_fence_after();
+                // dV += P^T dO, dK += dS^T Q (K = the 64 queries)
 #pragma unroll
-                for (int k = 0; k < TILE / 16; k++) {
-                    const uint64_t aoff = (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
-                    umma_bf16(tDV, dPT + aoff, dd_m + (uint64_t)(128 * k), ID_O, (n > 0 || k > 0));
-                    umma_bf16(tDK, dDST + aoff, dq_m + (uint64_t)(128 * k), ID_O, (n > 0 || k > 0));
+                for (int k = 0; k < SUB / 16; k++) {
+                    umma_bf16(tDV, dPT + (uint64_t)(2 * k), dd_m + (uint64_t)(128 * k), ID_O,
+                              (n > 0 || k > 0));
+                    umma_bf16(tDK, dDST + (uint64_t)(2 * k), dq_m + (uint64_t)(128 * k), ID_O,
+                              (n > 0 || k > 0));
                 }
                 umma_commit(s ? b_qde1 : b_qde0);
                 umma_commit(b_psfree);
@@ -459,19 +483,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             if (ok) umma_commit(b_acc);
         }
     } else {
-        // warp pair (w, w+4) shares TMEM lane quarter w & 3; half hf takes
-        // query columns [64 hf, 64 hf + 64) and output columns [32 hf, 32 hf + 32)
-        const int q = warp & 3, hf = (warp - 2) >> 2;
+        // warp pair (w, w+4) shares TMEM lane quarter w & 3; half hf takes query
+        // columns [32 hf, 32 hf + 32) of each step and output columns [32 hf, +32)
+        const int q = warp & 3, hf = (warp - 1) >> 2;
         const int r = q * 32 + lane;   // key row within the tile
         const int kj = kt * TILE + r;  // key index in the sequence
-        const int tid = threadIdx.x - 64;
+        const int tid = threadIdx.x - 32;
         const uint32_t loff = (uint32_t)(q * 32) << 16;
+        const int c0 = hf * 32;
         bool ok = true;
         for (int n = 0; n < nq; n++) {
-            const int i = kt + n;
+            const int qbase = (i0 + n) * SUB;
             named_sync_softmax();  // everyone is done with the previous lse/D
-            if (tid < TILE) {
-                const int qi = i * TILE + tid;
+            if (tid < SUB) {
+                const int qi = qbase + tid;
                 lse_s[tid] = qi < p.T ? p.lse[(size_t)bh * p.T + qi] * 1.4426950408889634f : 0.f;
                 d_s[tid] = qi < p.T ? p.Dv[(size_t)bh * p.T + qi] : 0.f;
             }
@@ -485,51 +510,46 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int qbase = i * TILE;
-            // off-diagonal query tiles that lie inside the sequence need no mask
-            const bool full = i > kt && qbase + TILE <= p.T;
-#pragma unroll 1
-            for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 32) {
-                uint32_t sv[32], dp[32];
-                tmem_ld32_async(tST + loff + c0, sv);
-                tmem_ld32_async(tDPT + loff + c0, dp);
-                tmem_wait32(sv);
-                tmem_wait32(dp);
-                uint32_t pp[16], dd[16];
-                if (full) {
+            uint32_t sv[32], dp[32];
+            tmem_ld32_async(tST + loff + c0, sv);
+            tmem_ld32_async(tDPT + loff + c0, dp);
+            tmem_wait32(sv);
+            tmem_wait32(dp);
+            // the whole step lies after this key tile and inside the sequence
+            const bool full = qbase >= kt * TILE + TILE && qbase + SUB <= p.T;
+            uint32_t pp[16], dd[16];
+            if (full) {
 #pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        const int c = c0 + 2 * e;
-                        const float p0 =
-                            ex2(fmaf(__uint_as_float(sv[2 * e]), p.scale_log2, -lse_s[c]));
-                        const float p1 =
-                            ex2(fmaf(__uint_as_float(sv[2 * e + 1]), p.scale_log2, -lse_s[c + 1]));
-                        pp[e] = pack_bf16x2(p0, p1);
-                        dd[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - d_s[c]),
-                                            p1 * (__uint_as_float(dp[2 * e + 1]) - d_s[c + 1]));
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        float pv[2], dv[2];
-#pragma unroll
-                        for (int z = 0; z < 2; z++) {
-                            const int c = c0 + 2 * e + z;
-                            const int qi = qbase + c;
-                            const bool live = qi < p.T && kj <= qi;
-                            const float pr = live ? ex2(fmaf(__uint_as_float(sv[2 * e + z]),
-                                                             p.scale_log2, -lse_s[c]))
-                                                  : 0.f;
-                            pv[z] = pr;
-                            dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - d_s[c]) : 0.f;
-                        }
-                        pp[e] = pack_bf16x2(pv[0], pv[1]);
-                        dd[e] = pack_bf16x2(dv[0], dv[1]);
-                    }
+                for (int e = 0; e < 16; e++) {
+                    const int c = c0 + 2 * e;
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), p.scale_log2, -lse_s[c]));
+                    const float p1 =
+                        ex2(fmaf(__uint_as_float(sv[2 * e + 1]), p.scale_log2, -lse_s[c + 1]));
+                    pp[e] = pack_bf16x2(p0, p1);
+                    dd[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - d_s[c]),
+                                        p1 * (__uint_as_float(dp[2 * e + 1]) - d_s[c + 1]));
                 }
-                st_row32(sPT, r, c0, pp);
-                st_row32(sDST, r, c0, dd);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int z = 0; z < 2; z++) {
+                        const int c = c0 + 2 * e + z;
+                        const int qi = qbase + c;
+                        const bool live = qi < p.T && kj <= qi;
+                        const float pr = live ? ex2(fmaf(__uint_as_float(sv[2 * e + z]),
+                                                         p.scale_log2, -lse_s[c]))
+                                              : 0.f;
+                        pv[z] = pr;
+                        dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - d_s[c]) : 0.f;
+                    }
+                    pp[e] = pack_bf16x2(pv[0], pv[1]);
+                    dd[e] = pack_bf16x2(dv[0], dv[1]);
+                }
             }
+            st_row32_64(sPT, r, c0, pp);
+            st_row32_64(sDST, r, c0, dd);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -547,20 +567,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
                     uint4 uv, uk;
-                    float f[8], g[8];
-#pragma unroll
-                    for (int z = 0; z < 8; z++) {
-                        f[z] = __uint_as_float(v[e + z]);
-                        g[z] = __uint_as_float(k[e + z]) * p.scale;
-                    }
-                    uv.x = pack_bf16x2(f[0], f[1]);
-                    uv.y = pack_bf16x2(f[2], f[3]);
-                    uv.z = pack_bf16x2(f[4], f[5]);
-                    uv.w = pack_bf16x2(f[6], f[7]);
-                    uk.x = pack_bf16x2(g[0], g[1]);
-                    uk.y = pack_bf16x2(g[2], g[3]);
-                    uk.z = pack_bf16x2(g[4], g[5]);
-                    uk.w = pack_bf16x2(g[6], g[7]);
+                    uv.x = pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+                    uv.y = pack_bf16x2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                    uv.z = pack_bf16x2(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+                    uv.w = pack_bf16x2(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+                    uk.x = pack_bf16x2(__uint_as_float(k[e]) * p.scale, __uint_as_float(k[e + 1]) * p.scale);
+                    uk.y = pack_bf16x2(__uint_as_float(k[e + 2]) * p.scale, __uint_as_float(k[e + 3]) * p.scale);
+                    uk.z = pack_bf16x2(__uint_as_float(k[e + 4]) * p.scale, __uint_as_float(k[e + 5]) * p.scale);
+                    uk.w = pack_bf16x2(__uint_as_float(k[e + 6]) * p.scale, __uint_as_float(k[e + 7]) * p.scale);
                     *reinterpret_cast<uint4*>(dst + 2 * p.C + e) = uv;
                     *reinterpret_cast<uint4*>(dst + p.C + e) = uk;
                 }
@@ -569,35 +583,35 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         tc_fence_before();
     }
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 0) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, 256);
     }
 }
 
-constexpr int Q_Q = 0, Q_DO = 16384, Q_K0 = 32768, Q_V0 = 49152, Q_K1 = 65536, Q_V1 = 81920,
-              Q_DS = 98304, Q_BAR = 131072;
-constexpr int Q_SMEM = Q_BAR + 256 + 1024;
+// dQ: CTA = (128-query tile qt, batch, head); key steps of 64.
+constexpr int E_Q = 0, E_DO = 16384, E_K0 = 32768, E_K1 = 40960, E_V0 = 49152, E_V1 = 57344,
+              E_DS = 65536, E_BAR = 81920;
+constexpr int E_SMEM = E_BAR + 256 + 1024;
 
-__global__ void __launch_bounds__(ATT_THREADS, 1)
-    k_attn_dq_tc(const __grid_constant__ CUtensorMap map_qkv,
-                 const __grid_constant__ CUtensorMap map_do, AttnBwdParams p) {
+__global__ void __launch_bounds__(BWD_THREADS, 2)
+    k_attn_dq_tc(const __grid_constant__ BwdMaps maps, AttnBwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw);
-    const uint32_t sQ = base + Q_Q, sDO = base + Q_DO, sDS = base + Q_DS;
-    const uint32_t bar = base + Q_BAR;
+    const uint32_t sQ = base + E_Q, sDO = base + E_DO, sDS = base + E_DS;
+    const uint32_t bar = base + E_BAR;
     const uint32_t b_q = bar, b_kvf0 = bar + 8, b_kvf1 = bar + 16, b_kve0 = bar + 24,
                    b_kve1 = bar + 32, b_sfull = bar + 40, b_dsfull = bar + 48,
                    b_dsfree = bar + 56, b_acc = bar + 64;
-    uint32_t* tmem_slot = (uint32_t*)(base_gen + Q_BAR + 128);
-    volatile int* abort_flag = (volatile int*)(base_gen + Q_BAR + 132);
+    uint32_t* tmem_slot = (uint32_t*)(base_gen + E_BAR + 128);
+    volatile int* abort_flag = (volatile int*)(base_gen + E_BAR + 132);
 
     const int qt = p.nqt - 1 - (int)blockIdx.x;
     const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-    const int nkt = qt + 1;
+    const int nk = min(2 * qt + 2, p.nsub);  // 64-key steps 0..nk-1
     const int row0 = b * p.T;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
 
@@ -614,60 +628,59 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
         tmem_relinquish();
         tc_fence_before();
     }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
+    const uint32_t tS = tmem, tDP = tmem + 64, tDQ = tmem + 128;
 
     if (warp == 0) {
         if (lane == 0) {
-            const int cq = h * HD, ck = p.C + h * HD, cv = 2 * p.C + h * HD;
+            const int ck = p.C + h * HD, cv = 2 * p.C + h * HD;
             mbar_expect_tx(b_q, 2 * TILE_BYTES);
-            tma_load_2d(sQ, &map_qkv, b_q, cq, row0 + qt * TILE);
-            tma_load_2d(sDO, &map_do, b_q, h * HD, row0 + qt * TILE);
-            int issued[2] = {-1, -1};
-            for (int j = 0; j < nkt; j++) {
+            tma_load_2d(sQ, &maps.qkv128, b_q, h * HD, row0 + qt * TILE);
+            tma_load_2d(sDO, &maps.do128, b_q, h * HD, row0 + qt * TILE);
+            int issued0 = -1, issued1 = -1;
+            for (int j = 0; j < nk; j++) {
                 const int s = j & 1, u = j >> 1;
-                const uint32_t fe = s ? b_kve1 : b_kve0, ff = s ? b_kvf1 : b_kvf0;
-                if (!mbar_wait(fe, (u & 1) ^ 1, abort_flag, p.err)) break;
-                const uint32_t sk = base + (s ? Q_K1 : Q_K0), sv = base + (s ? Q_V1 : Q_V0);
-                mbar_expect_tx(ff, 2 * TILE_BYTES);
-                tma_load_2d(sk, &map_qkv, ff, ck, row0 + j * TILE);
-                tma_load_2d(sv, &map_qkv, ff, cv, row0 + j * TILE);
-                issued[s] = u;
+                if (!mbar_wait(s ? b_kve1 : b_kve0, (u & 1) ^ 1, abort_flag, p.err)) break;
+                const uint32_t ff = s ? b_kvf1 : b_kvf0;
+                mbar_expect_tx(ff, 2 * SUB_BYTES);
+                tma_load_2d(base + (s ? E_K1 : E_K0), &maps.qkv64, ff, ck, row0 + j * SUB);
+                tma_load_2d(base + (s ? E_V1 : E_V0), &maps.qkv64, ff, cv, row0 + j * SUB);
+                if (s) issued1 = u;
+                else issued0 = u;
             }
             if (*abort_flag) {
                 for (int s = 0; s < 2; s++) {
-                    if (issued[s] < 0) continue;
+                    const int is = s ? issued1 : issued0;
+                    if (is < 0) continue;
                     long long t0 = clock64();
-                    while (!mbar_try(s ? b_kvf1 : b_kvf0, issued[s] & 1) &&
-                           clock64() - t0 < WAIT_LIMIT) {
+                    while (!mbar_try(s ? b_kvf1 : b_kvf0, is & 1) && clock64() - t0 < WAIT_LIMIT) {
                     }
                 }
                 long long t0 = clock64();
                 while (!mbar_try(b_q, 0) && clock64() - t0 < WAIT_LIMIT) {
                 }
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
+        } else if (lane == 1) {
+            constexpr uint32_t ID_S = make_idesc(128, SUB, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
             const uint64_t dQ = sdesc(sQ, 0, 1024), dDO = sdesc(sDO, 0, 1024);
             const uint64_t dDS = sdesc(sDS, 0, 1024);
             bool ok = mbar_wait(b_q, 0, abort_flag, p.err);
-            for (int j = 0; ok && j < nkt; j++) {
+            for (int j = 0; ok && j < nk; j++) {
                 const int s = j & 1, u = j >> 1;
                 if (!mbar_wait_spin(s ? b_kvf1 : b_kvf0, u & 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                const uint32_t sk = base + (s ? Q_K1 : Q_K0), sv = base + (s ? Q_V1 : Q_V0);
+                const uint32_t sk = base + (s ? E_K1 : E_K0), sv = base + (s ? E_V1 : E_V0);
                 const uint64_t dk_k = sdesc(sk, 0, 1024), dv_k = sdesc(sv, 0, 1024);
                 const uint64_t dk_m = sdesc(sk, 8192, 1024);
+                // S = Q K_j^T, dP = dO V_j^T (128 queries x 64 keys)
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
                     umma_bf16(tS, dQ + (uint64_t)(2 * k), dk_k + (uint64_t)(2 * k), ID_S, k > 0);
@@ -677,25 +690,27 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 umma_commit(b_sfull);
                 if (!mbar_wait_spin(b_dsfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
+                // dQ += dS K_j (K = the 64 keys)
 #pragma unroll
-                for (int k = 0; k < TILE / 16; k++)
-                    umma_bf16(tDQ, dDS + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
-                              dk_m + (uint64_t)(128 * k), ID_O, (j > 0 || k > 0));
+                for (int k = 0; k < SUB / 16; k++)
+                    umma_bf16(tDQ, dDS + (uint64_t)(2 * k), dk_m + (uint64_t)(128 * k), ID_O,
+                              (j > 0 || k > 0));
                 umma_commit(s ? b_kve1 : b_kve0);
                 umma_commit(b_dsfree);
             }
             if (ok) umma_commit(b_acc);
         }
     } else {
-        const int q = warp & 3, hf = (warp - 2) >> 2;
+        const int q = warp & 3, hf = (warp - 1) >> 2;
         const int r = q * 32 + lane;
         const int qi = qt * TILE + r;
         const uint32_t loff = (uint32_t)(q * 32) << 16;
+        const int c0 = hf * 32;
         const bool qlive = qi < p.T;
         const float lse2 = qlive ? p.lse[(size_t)bh * p.T + qi] * 1.4426950408889634f : 0.f;
         const float Dq = qlive ? p.Dv[(size_t)bh * p.T + qi] : 0.f;
         bool ok = true;
-        for (int j = 0; j < nkt; j++) {
+        for (int j = 0; j < nk; j++) {
             if (!warp_wait(b_sfull, j & 1, abort_flag, p.err, lane)) {
                 ok = false;
                 break;
@@ -705,42 +720,38 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int kbase = j * TILE;
-#pragma unroll 1
-            for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 32) {
-                uint32_t sv[32], dp[32];
-                tmem_ld32_async(tS + loff + c0, sv);
-                tmem_ld32_async(tDP + loff + c0, dp);
-                tmem_wait32(sv);
-                tmem_wait32(dp);
-                uint32_t dd[16];
-                if (j < qt) {
+            uint32_t sv[32], dp[32];
+            tmem_ld32_async(tS + loff + c0, sv);
+            tmem_ld32_async(tDP + loff + c0, dp);
+            tmem_wait32(sv);
+            tmem_wait32(dp);
+            const int kbase = j * SUB;
+            uint32_t dd[16];
+            if (kbase + SUB <= qt * TILE) {  // every key of the step precedes every query
 #pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), p.scale_log2, -lse2));
-                        const float p1 =
-                            ex2(fmaf(__uint_as_float(sv[2 * e + 1]), p.scale_log2, -lse2));
-                        dd[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - Dq),
-                                            p1 * (__uint_as_float(dp[2 * e + 1]) - Dq));
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        float dv[2];
-#pragma unroll
-                        for (int z = 0; z < 2; z++) {
-                            const int kk = kbase + c0 + 2 * e + z;
-                            const bool live = qlive && kk <= qi;
-                            const float pr = live ? ex2(fmaf(__uint_as_float(sv[2 * e + z]),
-                                                             p.scale_log2, -lse2))
-                                                  : 0.f;
-                            dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - Dq) : 0.f;
-                        }
-                        dd[e] = pack_bf16x2(dv[0], dv[1]);
-                    }
+                for (int e = 0; e < 16; e++) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), p.scale_log2, -lse2));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[2 * e + 1]), p.scale_log2, -lse2));
+                    dd[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - Dq),
+                                        p1 * (__uint_as_float(dp[2 * e + 1]) - Dq));
                 }
-                st_row32(sDS, r, c0, dd);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    float dv[2];
+#pragma unroll
+                    for (int z = 0; z < 2; z++) {
+                        const int kk = kbase + c0 + 2 * e + z;
+                        const bool live = qlive && kk <= qi;
+                        const float pr =
+                            live ? ex2(fmaf(__uint_as_float(sv[2 * e + z]), p.scale_log2, -lse2))
+                                 : 0.f;
+                        dv[z] = live ? pr * (__uint_as_float(dp[2 * e + z]) - Dq) : 0.f;
+                    }
+                    dd[e] = pack_bf16x2(dv[0], dv[1]);
+                }
             }
+            st_row32_64(sDS, r, c0, dd);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -755,14 +766,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             if (qlive) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
-                    float f[8];
-#pragma unroll
-                    for (int z = 0; z < 8; z++) f[z] = __uint_as_float(v[e + z]) * p.scale;
                     uint4 u;
-                    u.x = pack_bf16x2(f[0], f[1]);
-                    u.y = pack_bf16x2(f[2], f[3]);
-                    u.z = pack_bf16x2(f[4], f[5]);
-                    u.w = pack_bf16x2(f[6], f[7]);
+                    u.x = pack_bf16x2(__uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale);
+                    u.y = pack_bf16x2(__uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale);
+                    u.z = pack_bf16x2(__uint_as_float(v[e + 4]) * p.scale, __uint_as_float(v[e + 5]) * p.scale);
+                    u.w = pack_bf16x2(__uint_as_float(v[e + 6]) * p.scale, __uint_as_float(v[e + 7]) * p.scale);
                     *reinterpret_cast<uint4*>(dst + e) = u;
                 }
             }
@@ -770,10 +778,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         tc_fence_before();
     }
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 0) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, 256);
     }
 }
 
@@ -791,12 +799,12 @@ bool attention_tc_supported(int act, int B, int T, int C, int H, const void* qkv
     return tc_encode_fn() != nullptr;
 }
 
-static bool map_rows(CUtensorMap* m, const void* base, long width, long rows) {
+static bool map_rows(CUtensorMap* m, const void* base, long width, long rows, int box_rows) {
     EncodeTiledFn enc = (EncodeTiledFn)tc_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)width * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -809,17 +817,21 @@ cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv,
                                   cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_attn_dkv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM);
-        cudaFuncSetAttribute(k_attn_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM);
+        cudaFuncSetAttribute(k_attn_dkv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, D_SMEM);
+        cudaFuncSetAttribute(k_attn_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, E_SMEM);
         attr = true;
     }
     if (((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15)) return cudaErrorInvalidValue;
-    CUtensorMap mq, md;
-    if (!map_rows(&mq, qkv, 3L * C, (long)B * T) || !map_rows(&md, dout, C, (long)B * T))
+    BwdMaps maps;
+    const long rows = (long)B * T;
+    if (!map_rows(&maps.qkv128, qkv, 3L * C, rows, 128) ||
+        !map_rows(&maps.qkv64, qkv, 3L * C, rows, 64) ||
+        !map_rows(&maps.do128, dout, C, rows, 128) || !map_rows(&maps.do64, dout, C, rows, 64))
         return cudaErrorInvalidValue;
     AttnBwdParams p;
     p.B = B; p.T = T; p.C = C; p.H = H;
     p.nqt = (T + TILE - 1) / TILE;
+    p.nsub = (T + SUB - 1) / SUB;
     p.lse = lse;
     p.Dv = Dv;
     p.dqkv = (bf16*)dqkv;
@@ -827,8 +839,8 @@ cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv,
     p.scale = 1.0f / sqrtf((float)HD);
     p.scale_log2 = 1.4426950408889634f * p.scale;
     dim3 grid(p.nqt, B * H);
-    k_attn_dkv_tc<<<grid, ATT_THREADS, B_SMEM, s>>>(mq, md, p);
-    k_attn_dq_tc<<<grid, ATT_THREADS, Q_SMEM, s>>>(mq, md, p);
+    k_attn_dkv_tc<<<grid, BWD_THREADS, D_SMEM, s>>>(maps, p);
+    k_attn_dq_tc<<<grid, BWD_THREADS, E_SMEM, s>>>(maps, p);
     return cudaGetLastError();
 }
 
