@@ -61,17 +61,23 @@ int gpt2k_attention_backward(int dtype, void* dqkv, const void* dout, const void
                              void* scratch, void* stream);
 
 /* LayerNorm over rows of C (eps 1e-5, biased variance): out = (x-mean)*rstd*w + b,
- * mean/rstd [N] fp32 saved.  Backward ACCUMULATES into dx [N,C] (dtype) and
- * into dw, db [C] (fp32). */
+ * mean/rstd [N] fp32 saved.  Backward: dx [N,C] (dtype) receives the input
+ * gradient -- added to its contents if `accumulate` is nonzero, else written
+ * over them; dw, db [C] (fp32) ACCUMULATE sum_n dy*xhat and sum_n dy; if dxsum
+ * [C] (fp32) is not NULL it ACCUMULATES the column sums of the dx rows as
+ * written (the bias gradient of a linear layer whose output gradient is dx).
+ * Scratch from gpt2k_layernorm_backward_scratch_bytes covers the dxsum case. */
 int gpt2k_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* x,
                             const void* w, const void* b, int N, int C, void* stream);
 size_t gpt2k_layernorm_backward_scratch_bytes(int N, int C);
-int gpt2k_layernorm_backward(int dtype, void* dx, float* dw, float* db, const void* dout,
-                             const void* x, const void* w, const float* mean, const float* rstd,
-                             int N, int C, void* scratch, void* stream);
+int gpt2k_layernorm_backward(int dtype, void* dx, float* dw, float* db, float* dxsum,
+                             const void* dout, const void* x, const void* w, const float* mean,
+                             const float* rstd, int N, int C, int accumulate, void* scratch,
+                             void* stream);
 
 /* Allocation-free LayerNorm backward.  The pages have no counterpart: this
- * is the same computation as gpt2k_layernorm_backward for callers that cannot
+ * is the same computation as gpt2k_layernorm_backward (accumulating into dx,
+ * no dxsum) for callers that cannot
  * allocate device memory -- their memory belongs to another allocator that
  * gives them only the operation's tensors, or they run where cudaMalloc /
  * cudaFree must not be called (both may synchronise the device).  Instead of

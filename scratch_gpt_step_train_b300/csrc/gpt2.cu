@@ -161,7 +161,7 @@ struct Planner {
 
 static size_t scratch_need(int L, int H, int C, int Vp, int T, int B) {
     size_t BT = (size_t)B * T;
-    size_t s = layernorm_backward_scratch((int)BT, C);
+    size_t s = layernorm_backward_scratch((int)BT, C, true);
     size_t x;
     if ((x = bias_grad_scratch((int)BT, 4 * C)) > s) s = x;
     if ((x = encoder_backward_scratch(B, T, C, Vp)) > s) s = x;
@@ -547,13 +547,17 @@ extern "C" int gpt2_backward(gpt2_t* g) {
     d = gd(Vp, C, BT, g->logits, Vp, 0, g->lnf, C, 0, grad_tensor(g, P_WTE, 0), C,
            EPI_ACCUM_F32);
     RUN(mm(g, K_CLS_DW, d));
-    CK(cudaMemsetAsync(dres, 0, bt * c * as, g->stream));
     const void* xL = L > 0 ? act_at(g, g->x2, bt * c, L - 1) : g->encoded;
+    // the residual-stream gradient dres is written (not accumulated) by the
+    // final LayerNorm's backward; each LayerNorm backward that feeds a
+    // projection's output gradient also yields that projection's bias
+    // gradient as the column sums of dres
     double lnb_bytes = as * 4.0 * bt * c + 8.0 * bt;
-    LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
+    LAUNCH(K_LN_BWD, 2, 0, as * 3.0 * bt * c + 8.0 * bt,
            layernorm_backward(g->act, dres, grad_tensor(g, P_LNFW, 0), grad_tensor(g, P_LNFB, 0),
-                              g->dln, xL, pc_tensor(g, P_LNFW, 0), g->lnf_mean, g->lnf_rstd, BT,
-                              C, g->scratch, g->stream));
+                              L > 0 ? grad_tensor(g, P_FCPROJB, L - 1) : nullptr, g->dln, xL,
+                              pc_tensor(g, P_LNFW, 0), g->lnf_mean, g->lnf_rstd, BT, C, false,
+                              g->scratch, g->stream));
     for (int l = L - 1; l >= 0; l--) {
         const void* rin = l == 0 ? g->encoded : act_at(g, g->x2, bt * c, l - 1);
         void* ln1 = act_at(g, g->ln1, bt * c, l);
@@ -568,9 +572,6 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         d = gd(C, 4 * C, BT, dres, C, 0, fchg, 4 * C, 0, grad_tensor(g, P_FCPROJW, l), 4 * C,
                EPI_ACCUM_F32);
         RUN(mm(g, K_FCPROJ_DW, d));
-        LAUNCH(K_BIAS, 2, 0, as * bt * c,
-               bias_grad(g->act, grad_tensor(g, P_FCPROJB, l), dres, BT, C, g->scratch,
-                         g->stream));
         d = gd(BT, 4 * C, C, dres, C, 1, pc_tensor(g, P_FCPROJW, l), 4 * C, 0, g->dbig, 4 * C,
                EPI_GELU_BWD);
         d.aux = fch;
@@ -587,15 +588,12 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         RUN(mm(g, K_FC_DX, d));
         LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
                layernorm_backward(g->act, dres, grad_tensor(g, P_LN2W, l),
-                                  grad_tensor(g, P_LN2B, l), g->dln, x1, pc_tensor(g, P_LN2W, l),
-                                  g->ln2_mean + l * bt, g->ln2_rstd + l * bt, BT, C, g->scratch,
-                                  g->stream));
+                                  grad_tensor(g, P_LN2B, l), grad_tensor(g, P_PROJB, l), g->dln,
+                                  x1, pc_tensor(g, P_LN2W, l), g->ln2_mean + l * bt,
+                                  g->ln2_rstd + l * bt, BT, C, true, g->scratch, g->stream));
         // attention: x1 = rin + proj(attn(qkv(ln1(rin))))
         d = gd(C, C, BT, dres, C, 0, atty, C, 0, grad_tensor(g, P_PROJW, l), C, EPI_ACCUM_F32);
         RUN(mm(g, K_PROJ_DW, d));
-        LAUNCH(K_BIAS, 2, 0, as * bt * c,
-               bias_grad(g->act, grad_tensor(g, P_PROJB, l), dres, BT, C, g->scratch,
-                         g->stream));
         d = gd(BT, C, C, dres, C, 1, pc_tensor(g, P_PROJW, l), C, 0, g->datty, C, EPI_STORE);
         RUN(mm(g, K_PROJ_DX, d));
         double afl = 2.5 * 2.0 * 2.0 * B * H * ((double)T * (T + 1) / 2) * (C / H);
@@ -613,9 +611,10 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         RUN(mm(g, K_QKV_DX, d));
         LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
                layernorm_backward(g->act, dres, grad_tensor(g, P_LN1W, l),
-                                  grad_tensor(g, P_LN1B, l), g->dln, rin, pc_tensor(g, P_LN1W, l),
-                                  g->ln1_mean + l * bt, g->ln1_rstd + l * bt, BT, C, g->scratch,
-                                  g->stream));
+                                  grad_tensor(g, P_LN1B, l),
+                                  l > 0 ? grad_tensor(g, P_FCPROJB, l - 1) : nullptr, g->dln, rin,
+                                  pc_tensor(g, P_LN1W, l), g->ln1_mean + l * bt,
+                                  g->ln1_rstd + l * bt, BT, C, true, g->scratch, g->stream));
     }
     LAUNCH(K_EMB_BWD, 9, 0, as * bt * c + 8.0 * T * c,
            encoder_backward(g->act, grad_tensor(g, P_WTE, 0), grad_tensor(g, P_WPE, 0), dres,

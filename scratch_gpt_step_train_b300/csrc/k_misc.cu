@@ -15,8 +15,10 @@
 // on the same inputs gives the same bits.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 #include <math.h>
+#include <type_traits>
 
 namespace gk {
 
@@ -230,37 +232,62 @@ cudaError_t layernorm_forward(int act, void* out, float* mean, float* rstd, cons
 
 // ===========================================================================
 // LayerNorm backward.  Per row (xhat = (x-mean)*rstd, g = dy*w):
-//   dx += rstd * (g - mean(g) - xhat * mean(g*xhat))
-// dw, db column sums: each warp accumulates its rows into its own shared
-// memory slice, the block folds its 8 slices in order into one partial row,
-// and a second kernel sums the block partials in order.
+//   dx (+)= rstd * (g - mean(g) - xhat * mean(g*xhat))
+// One warp per row.  The column sums dw = sum dy*xhat, db = sum dy (and, when
+// asked, dxsum = sum of the written dx rows) are accumulated per lane in shared
+// memory: accumulator slot (it*VEC + j)*32 + lane of a warp's slice holds the
+// partial of column (it*32 + lane)*VEC + j, so each lane only ever touches its
+// own slots and the registers stay free for the row data.  At the end the
+// block folds its warps' slices in warp order into one partial row per
+// accumulator, and k_colsum adds the block partials in block order.
 // ===========================================================================
-#define LNB_WARPS 8
 #define LNB_MAX_BLOCKS 296
 
-template <typename T, int VEC, int IT>
-__global__ void __launch_bounds__(256) k_ln_bwd(T* dx, float* part, const T* dout, const T* x,
-                                                const T* w, const float* mean,
-                                                const float* rstd, int N, int C) {
-    __shared__ float sm[2 * 2048];  // block fold of the dw/db partials (C <= 2048)
+// Makes the compiler treat the vector's contents as changed here, so that it
+// recomputes what it derived from them before instead of keeping those values
+// live in registers (the row data packed as T is the cheaper thing to keep).
+template <typename T, int VEC>
+__device__ __forceinline__ void opaque(Vec<T, VEC>& v) {
+    if constexpr (sizeof(Vec<T, VEC>) % 4 == 0) {
+        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int k = 0; k < (int)(sizeof(Vec<T, VEC>) / 4); k++) asm volatile("" : "+r"(u[k]));
+    }
+}
+
+template <int VEC, int IT, int NACC>
+struct LnbCfg {
+    static constexpr int S = IT * VEC * 32;  // accumulator slots per warp
+    // 8 warps a block while two blocks' slices fit in shared memory, else 4
+    static constexpr int W = (2 * 8 * NACC * S * 4 <= 220 * 1024) ? 8 : 4;
+};
+
+template <typename T, int VEC, int IT, int NACC>
+__global__ void __launch_bounds__(LnbCfg<VEC, IT, NACC>::W * 32, 2)
+    k_ln_bwd(T* dx, float* part, const T* dout, const T* x, const T* w, const float* mean,
+             const float* rstd, int N, int C, int accum_dx) {
+    extern __shared__ float lsm[];  // [warps][NACC][S]
+    constexpr int S = LnbCfg<VEC, IT, NACC>::S;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    // this lane's dw, db partial sums for its columns, over this warp's rows
-    float aw[IT][VEC], ab[IT][VEC];
+    const int nwarps = blockDim.x / 32;
+    float* acc = lsm + (size_t)warp * NACC * S + lane;
 #pragma unroll
-    for (int it = 0; it < IT; it++)
-#pragma unroll
-        for (int j = 0; j < VEC; j++) aw[it][j] = ab[it][j] = 0.f;
-    for (int row = blockIdx.x * LNB_WARPS + warp; row < N; row += gridDim.x * LNB_WARPS) {
+    for (int k = 0; k < NACC * IT * VEC; k++) acc[k * 32] = 0.f;
+    for (int row = blockIdx.x * nwarps + warp; row < N; row += gridDim.x * nwarps) {
         const T* xr = x + (size_t)row * C;
         const T* dyr = dout + (size_t)row * C;
+        T* dxr = dx + (size_t)row * C;
         const float m = mean[row], r = rstd[row];
-        Vec<T, VEC> xv[IT], dv[IT];
+        // x, dy and the incoming dx of the row are independent loads: issue
+        // them together so that the row costs one memory latency
+        Vec<T, VEC> xv[IT], dv[IT], ov[IT];
 #pragma unroll
         for (int it = 0; it < IT; it++) {
             const int c = (it * 32 + lane) * VEC;
             if (c < C) {
                 xv[it] = *reinterpret_cast<const Vec<T, VEC>*>(xr + c);
                 dv[it] = *reinterpret_cast<const Vec<T, VEC>*>(dyr + c);
+                if (accum_dx) ov[it] = *reinterpret_cast<const Vec<T, VEC>*>(dxr + c);
             }
         }
         float sg = 0.f, sgx = 0.f;
@@ -277,60 +304,209 @@ __global__ void __launch_bounds__(256) k_ln_bwd(T* dx, float* part, const T* dou
                     const float g = dy * wv[j];
                     sg += g;
                     sgx += g * xh;
-                    aw[it][j] += dy * xh;
-                    ab[it][j] += dy;
+                    float* a = acc + (it * VEC + j) * 32;
+                    a[0] += dy * xh;
+                    a[S] += dy;
                 }
             }
         }
         sg = warp_sum(sg) / C;
         sgx = warp_sum(sgx) / C;
-        T* dxr = dx + (size_t)row * C;
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            opaque(xv[it]);
+            opaque(dv[it]);
+        }
+        asm volatile("" ::: "memory");  // reload w rather than hold it
 #pragma unroll
         for (int it = 0; it < IT; it++) {
             const int c = (it * 32 + lane) * VEC;
             if (c < C) {
-                float wv[VEC], d[VEC];
+                float wv[VEC];
                 load_vec_f<T, VEC>(wv, w + c);
-                load_vec_f<T, VEC>(d, dxr + c);
+                Vec<T, VEC> o;
 #pragma unroll
                 for (int j = 0; j < VEC; j++) {
                     const float xh = (to_f(xv[it].v[j]) - m) * r;
                     const float g = to_f(dv[it].v[j]) * wv[j];
-                    d[j] += r * (g - sg - xh * sgx);
+                    float d = r * (g - sg - xh * sgx);
+                    if (accum_dx) d += to_f(ov[it].v[j]);
+                    o.v[j] = from_f<T>(d);
+                    // the column sum is of the value as stored
+                    if (NACC == 3) acc[(2 * IT * VEC + it * VEC + j) * 32] += to_f(o.v[j]);
                 }
-                store_vec_f<T, VEC>(dxr + c, d);
+                *reinterpret_cast<Vec<T, VEC>*>(dxr + c) = o;
             }
         }
     }
-    // fold the 8 warps' partials in a fixed order (warp 0 first)
-    for (int wi = 0; wi < LNB_WARPS; wi++) {
-        if (warp == wi) {
-#pragma unroll
-            for (int it = 0; it < IT; it++) {
-                const int c = (it * 32 + lane) * VEC;
-                if (c < C) {
-#pragma unroll
-                    for (int j = 0; j < VEC; j++) {
-                        if (wi == 0) {
-                            sm[c + j] = aw[it][j];
-                            sm[C + c + j] = ab[it][j];
-                        } else {
-                            sm[c + j] += aw[it][j];
-                            sm[C + c + j] += ab[it][j];
-                        }
-                    }
-                }
-            }
+    __syncthreads();
+    // fold the warps' slices in warp order into this block's partial rows
+    for (int s = threadIdx.x; s < NACC * S; s += blockDim.x) {
+        const int k = s / S, q = s - k * S;
+        const int ln = q & 31, jj = (q >> 5) % VEC, itq = (q >> 5) / VEC;
+        const int c = (itq * 32 + ln) * VEC + jj;
+        if (c < C) {
+            float t = 0.f;
+            for (int wi = 0; wi < nwarps; wi++) t += lsm[(size_t)wi * NACC * S + s];
+            part[((size_t)blockIdx.x * NACC + k) * C + c] = t;
         }
-        __syncthreads();
     }
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) part[(size_t)blockIdx.x * 2 * C + c] = sm[c];
 }
 
-// out0[c] (c < n0) / out1[c - n0] (c >= n0) += sum_i part[i*ld + c], i in a
+// Rows of up to 768 bf16 columns (1024 without the dx sums): the same computation with the column sums
+// in registers (IT*8 columns per lane) and the row data staged through shared
+// memory by cp.async.  Each lane copies exactly the 16-byte vectors it later
+// reads, into a two-slot ring of its warp, so the copy of the warp's next row
+// is in flight while it works on the current one, and a lane only ever waits
+// for its own copies (cp.async.wait_group).  Registers hold no row data.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int NPEND>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(NPEND) : "memory");
+}
+__device__ __forceinline__ void bf16x8_to_f(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        f[2 * k] = __uint_as_float(w[k] << 16);
+        f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+}
+
+template <int IT, int NACC>
+__global__ void __launch_bounds__(256, 2)
+    k_ln_bwd_ring(bf16* dx, float* part, const bf16* dout, const bf16* x, const bf16* w,
+                  const float* mean, const float* rstd, int N, int C, int accum_dx) {
+    // ring: [warp][slot 0/1][x | dy | dx][IT*256 bf16]; reused for the fold
+    extern __shared__ __align__(16) unsigned char rsm[];
+    constexpr int ROWV = IT * 32;              // 16-byte vectors per row array (max)
+    constexpr int SLOT = 3 * ROWV * 16;        // bytes per slot
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x / 32;
+    const uint32_t ring = tc::smem_u32(rsm) + (uint32_t)warp * 2 * SLOT;
+    float wr[IT][8];
+    float acc[NACC][IT][8];
+#pragma unroll
+    for (int it = 0; it < IT; it++) {
+        const int c = (it * 32 + lane) * 8;
+        if (c < C) bf16x8_to_f(*reinterpret_cast<const uint4*>(w + c), wr[it]);
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            if (c >= C) wr[it][j] = 0.f;
+#pragma unroll
+            for (int a = 0; a < NACC; a++) acc[a][it][j] = 0.f;
+        }
+    }
+    const int stride = gridDim.x * nwarps;
+    auto issue = [&](int row, int slot) {
+        if (row < N) {
+            const uint32_t base = ring + slot * SLOT;
+#pragma unroll
+            for (int it = 0; it < IT; it++) {
+                const int c = (it * 32 + lane) * 8;
+                if (c < C) {
+                    const uint32_t o = (uint32_t)(it * 32 + lane) * 16;
+                    cp_async16(base + o, x + (size_t)row * C + c);
+                    cp_async16(base + ROWV * 16 + o, dout + (size_t)row * C + c);
+                    if (accum_dx) cp_async16(base + 2 * ROWV * 16 + o, dx + (size_t)row * C + c);
+                }
+            }
+        }
+        cp_async_commit();  // an empty group past the last row keeps the count uniform
+    };
+    int row = blockIdx.x * nwarps + warp;
+    issue(row, 0);
+    for (int k = 0; row < N; row += stride, k++) {
+        issue(row + stride, (k + 1) & 1);
+        cp_async_wait<1>();  // this lane's copies of `row` have landed
+        const unsigned char* sl = rsm + (size_t)warp * 2 * SLOT + (size_t)(k & 1) * SLOT;
+        const float m = mean[row], r = rstd[row], mr = -m * r;
+        float sg = 0.f, sgx = 0.f;
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            const int c = (it * 32 + lane) * 8;
+            if (c < C) {
+                float xf[8], df[8];
+                bf16x8_to_f(*reinterpret_cast<const uint4*>(sl + (it * 32 + lane) * 16), xf);
+                bf16x8_to_f(*reinterpret_cast<const uint4*>(sl + ROWV * 16 + (it * 32 + lane) * 16),
+                            df);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float xh = fmaf(xf[j], r, mr);
+                    const float g = df[j] * wr[it][j];
+                    sg += g;
+                    sgx = fmaf(g, xh, sgx);
+                    acc[0][it][j] = fmaf(df[j], xh, acc[0][it][j]);
+                    acc[1][it][j] += df[j];
+                }
+            }
+        }
+        sg = warp_sum(sg) / C;
+        sgx = warp_sum(sgx) / C;
+        bf16* dxr = dx + (size_t)row * C;
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            const int c = (it * 32 + lane) * 8;
+            if (c < C) {
+                float xf[8], df[8], of[8];
+                bf16x8_to_f(*reinterpret_cast<const uint4*>(sl + (it * 32 + lane) * 16), xf);
+                bf16x8_to_f(*reinterpret_cast<const uint4*>(sl + ROWV * 16 + (it * 32 + lane) * 16),
+                            df);
+                if (accum_dx)
+                    bf16x8_to_f(
+                        *reinterpret_cast<const uint4*>(sl + 2 * ROWV * 16 + (it * 32 + lane) * 16),
+                        of);
+                Vec<bf16, 8> o;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float xh = fmaf(xf[j], r, mr);
+                    const float g = df[j] * wr[it][j];
+                    float d = r * fmaf(-xh, sgx, g - sg);
+                    if (accum_dx) d += of[j];
+                    o.v[j] = from_f<bf16>(d);
+                    if (NACC == 3) acc[NACC - 1][it][j] += to_f(o.v[j]);
+                }
+                *reinterpret_cast<Vec<bf16, 8>*>(dxr + c) = o;
+            }
+        }
+    }
+    cp_async_wait<0>();  // nothing may still be landing in the ring
+    __syncthreads();
+    // fold: slot (a, it, j, lane) of warp w at ((w*NACC + a)*IT*8 + it*8 + j)*32 + lane
+    float* fs = reinterpret_cast<float*>(rsm);
+#pragma unroll
+    for (int a = 0; a < NACC; a++)
+#pragma unroll
+        for (int it = 0; it < IT; it++)
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                fs[(((size_t)warp * NACC + a) * IT * 8 + it * 8 + j) * 32 + lane] = acc[a][it][j];
+    __syncthreads();
+    constexpr int S = IT * 8 * 32;
+    for (int q = threadIdx.x; q < NACC * S; q += blockDim.x) {
+        const int a = q / S, rem = q - a * S;
+        const int ln = rem & 31, jj = (rem >> 5) & 7, itq = rem >> 8;
+        const int c = (itq * 32 + ln) * 8 + jj;
+        if (c < C) {
+            float t = 0.f;
+            for (int wi = 0; wi < nwarps; wi++) t += fs[((size_t)wi * NACC + a) * S + rem];
+            part[((size_t)blockIdx.x * NACC + a) * C + c] = t;
+        }
+    }
+}
+
+// outs[k][c] += sum_i part[i*ld + k*n0 + c] for column k*n0 + c < ncols, i in a
 // fixed order: thread row ty sums i = ty, ty+8, ..., then row 0 adds the 8
 // row sums in order.  32 consecutive columns per block (coalesced).
-__global__ void __launch_bounds__(256) k_colsum(float* out0, float* out1, int n0, int ncols,
+struct ColsumOut {
+    float* p[3];
+};
+__global__ void __launch_bounds__(256) k_colsum(ColsumOut outs, int n0, int ncols,
                                                 const float* part, int nparts, long ld) {
     __shared__ float sh[8][33];
     int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -344,89 +520,145 @@ __global__ void __launch_bounds__(256) k_colsum(float* out0, float* out1, int n0
         float t = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; k++) t += sh[k][tx];
-        if (c < n0) out0[c] += t;
-        else out1[c - n0] += t;
+        const int k = c / n0;
+        outs.p[k][c - k * n0] += t;
     }
 }
 
-size_t layernorm_backward_scratch(int N, int C) {
-    return (size_t)LNB_MAX_BLOCKS * 2 * C * sizeof(float);
+size_t layernorm_backward_scratch(int N, int C, bool dxsum) {
+    return (size_t)LNB_MAX_BLOCKS * (dxsum ? 3 : 2) * C * sizeof(float);
 }
 
-template <typename T, int VEC>
-static cudaError_t ln_bwd_vec(void* dx, float* dw, float* db, const void* dout, const void* x,
-                              const void* w, const float* mean, const float* rstd, int N, int C,
-                              void* scratch, cudaStream_t s) {
-    int it = cdiv(C, 32 * VEC);
-    int nb = cdiv(N, LNB_WARPS * 4);
+template <typename T, int VEC, int IT, int NACC>
+static cudaError_t ln_bwd_launch(T* dx, float* part, const T* dout, const T* x, const T* w,
+                                 const float* mean, const float* rstd, int N, int C, int accum,
+                                 int* nb_out, cudaStream_t s) {
+    if constexpr (std::is_same<T, bf16>::value && VEC == 8 && IT * NACC <= 9) {
+        // register column sums, cp.async-staged rows
+        constexpr size_t smem = (size_t)8 * 2 * 3 * IT * 32 * 16;
+        static_assert(smem >= (size_t)8 * NACC * IT * 256 * 4, "fold does not fit the ring");
+        auto kern = k_ln_bwd_ring<IT, NACC>;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        int nb = cdiv(N, 8 * 4);
+        if (nb > LNB_MAX_BLOCKS) nb = LNB_MAX_BLOCKS;
+        *nb_out = nb;
+        kern<<<nb, 256, smem, s>>>(dx, part, dout, x, w, mean, rstd, N, C, accum);
+        return cudaGetLastError();
+    }
+    constexpr int S = LnbCfg<VEC, IT, NACC>::S, W = LnbCfg<VEC, IT, NACC>::W;
+    constexpr size_t smem = (size_t)W * NACC * S * sizeof(float);
+    static_assert(smem <= 227 * 1024, "LayerNorm backward slices exceed shared memory");
+    auto kern = k_ln_bwd<T, VEC, IT, NACC>;
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    int nb = cdiv(N, W * 4);
     if (nb > LNB_MAX_BLOCKS) nb = LNB_MAX_BLOCKS;
-    float* part = (float*)scratch;
-#define LNB(I)                                                                                   \
-    k_ln_bwd<T, VEC, I><<<nb, 256, 0, s>>>((T*)dx, part, (const T*)dout, (const T*)x,            \
-                                           (const T*)w, mean, rstd, N, C)
-    switch (it) {
-        case 1: LNB(1); break;
-        case 2: LNB(2); break;
-        case 3: LNB(3); break;
-        case 4: LNB(4); break;
-        case 5: LNB(5); break;
-        case 6: LNB(6); break;
-        case 7: LNB(7); break;
-        case 8: LNB(8); break;
-        default:
-            if (it <= 12) LNB(12);
-            else if (it <= 16) LNB(16);
-            else return cudaErrorInvalidValue;
-    }
-#undef LNB
-    k_colsum<<<cdiv(2 * C, 32), 256, 0, s>>>(dw, db, C, 2 * C, part, nb, 2 * C);
+    *nb_out = nb;
+    kern<<<nb, W * 32, smem, s>>>(dx, part, dout, x, w, mean, rstd, N, C, accum);
     return cudaGetLastError();
 }
-template <typename T>
-static cudaError_t ln_bwd_t(void* dx, float* dw, float* db, const void* dout, const void* x,
-                            const void* w, const float* mean, const float* rstd, int N, int C,
-                            void* scratch, cudaStream_t s) {
-    constexpr int VM = 16 / sizeof(T);
-    if (C % VM == 0) return ln_bwd_vec<T, VM>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
-    return ln_bwd_vec<T, 1>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
+
+template <typename T, int VEC, int NACC>
+static cudaError_t ln_bwd_vec(T* dx, float* part, const T* dout, const T* x, const T* w,
+                              const float* mean, const float* rstd, int N, int C, int accum,
+                              int* nb, cudaStream_t s) {
+    const int it = cdiv(C, 32 * VEC);
+#define LNB(I)                                                                                   \
+    return ln_bwd_launch<T, VEC, I, NACC>(dx, part, dout, x, w, mean, rstd, N, C, accum, nb, s)
+    switch (it) {
+        case 1: LNB(1);
+        case 2: LNB(2);
+        case 3: LNB(3);
+        case 4: LNB(4);
+        case 5: LNB(5);
+        case 6: LNB(6);
+        case 7: LNB(7);
+        case 8: LNB(8);
+        default:
+            if (it <= 12) LNB(12);
+            if (it <= 16) LNB(16);
+            return cudaErrorInvalidValue;
+    }
+#undef LNB
 }
-cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, const void* dout,
-                               const void* x, const void* w, const float* mean,
-                               const float* rstd, int N, int C, void* scratch, cudaStream_t s) {
+
+template <typename T>
+static cudaError_t ln_bwd_t(void* dx, float* dw, float* db, float* dxsum, const void* dout,
+                            const void* x, const void* w, const float* mean, const float* rstd,
+                            int N, int C, int accum, void* scratch, cudaStream_t s) {
+    constexpr int VM = 16 / sizeof(T);
+    float* part = (float*)scratch;
+    int nb = 0;
+    cudaError_t e;
+#define LNV(V, A)                                                                                \
+    ln_bwd_vec<T, V, A>((T*)dx, part, (const T*)dout, (const T*)x, (const T*)w, mean, rstd, N,  \
+                        C, accum, &nb, s)
+    if (C % VM == 0) e = dxsum ? LNV(VM, 3) : LNV(VM, 2);
+    else e = dxsum ? LNV(1, 3) : LNV(1, 2);
+#undef LNV
+    if (e != cudaSuccess) return e;
+    const int nacc = dxsum ? 3 : 2;
+    ColsumOut o{{dw, db, dxsum}};
+    k_colsum<<<cdiv(nacc * C, 32), 256, 0, s>>>(o, C, nacc * C, part, nb, (long)nacc * C);
+    return cudaGetLastError();
+}
+cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, float* dxsum,
+                               const void* dout, const void* x, const void* w, const float* mean,
+                               const float* rstd, int N, int C, bool accum_dx, void* scratch,
+                               cudaStream_t s) {
     if (C > 2048) return cudaErrorInvalidValue;
     if (act == ACT_BF16)
-        return ln_bwd_t<bf16>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
-    return ln_bwd_t<float>(dx, dw, db, dout, x, w, mean, rstd, N, C, scratch, s);
+        return ln_bwd_t<bf16>(dx, dw, db, dxsum, dout, x, w, mean, rstd, N, C, accum_dx, scratch,
+                              s);
+    return ln_bwd_t<float>(dx, dw, db, dxsum, dout, x, w, mean, rstd, N, C, accum_dx, scratch,
+                           s);
 }
 
 // ===========================================================================
-// Bias gradient: db[o] += sum_n dout[n,o].  Stage 1: each block sums a chunk
-// of BG_ROWS rows for VEC-wide column groups; stage 2 sums chunks in order.
+// Bias gradient: db[o] += sum_n dout[n,o].  Rows are cut into chunks of
+// BG_ROWS; block (x, p) sums the chunks p, p + P, p + 2P, ... (P = gridDim.y)
+// for 32 column vectors into partial row p, and k_colsum adds the P partial
+// rows in order -- a fixed summation order whatever the grid's timing.  P is
+// chosen so that the grid fills the GPU about four blocks deep.
 // ===========================================================================
 #define BG_ROWS 64
 
-// block (32 x 8 threads): column vectors blockIdx.x*32 + tx, rows
-// [blockIdx.y*BG_ROWS, +BG_ROWS); thread row ty sums rows ty, ty+8, ... in
-// order, then the 8 row sums are added in order.
+// block (32 x 8 threads): thread row ty sums rows ty, ty+8, ... of each chunk
+// (the chunk's 8 loads issued together), then the 8 row sums are added in order
 template <typename T, int VEC>
-__global__ void __launch_bounds__(256) k_bias_part(float* part, const T* dout, int N, int OC) {
+__global__ void __launch_bounds__(256) k_bias_part(float* part, const T* dout, int N, int OC,
+                                                   int nch) {
     __shared__ float sh[8][32 * VEC + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     const int c = (blockIdx.x * 32 + tx) * VEC;
-    const int r0 = blockIdx.y * BG_ROWS;
     float a[VEC];
 #pragma unroll
     for (int j = 0; j < VEC; j++) a[j] = 0.f;
     if (c < OC) {
+        for (int q = blockIdx.y; q < nch; q += gridDim.y) {
+            const int r0 = q * BG_ROWS + ty;
+            Vec<T, VEC> v[BG_ROWS / 8];
 #pragma unroll
-        for (int k = 0; k < BG_ROWS / 8; k++) {
-            const int r = r0 + ty + 8 * k;
-            if (r < N) {
-                float v[VEC];
-                load_vec_f<T, VEC>(v, dout + (size_t)r * OC + c);
+            for (int k = 0; k < BG_ROWS / 8; k++) {
+                const int r = r0 + 8 * k;
+                if (r < N) {
+                    v[k] = *reinterpret_cast<const Vec<T, VEC>*>(dout + (size_t)r * OC + c);
+                } else {
 #pragma unroll
-                for (int j = 0; j < VEC; j++) a[j] += v[j];
+                    for (int j = 0; j < VEC; j++) v[k].v[j] = from_f<T>(0.f);
+                }
             }
+#pragma unroll
+            for (int k = 0; k < BG_ROWS / 8; k++)
+#pragma unroll
+                for (int j = 0; j < VEC; j++) a[j] += to_f(v[k].v[j]);
         }
     }
 #pragma unroll
@@ -448,16 +680,17 @@ template <typename T>
 static cudaError_t bias_grad_t(float* db, const void* dout, int N, int OC, void* scratch,
                                cudaStream_t s) {
     constexpr int VM = 16 / sizeof(T);
-    int nch = cdiv(N, BG_ROWS);
+    const int nch = cdiv(N, BG_ROWS);
+    const int vec = OC % VM == 0 ? VM : 1;
+    const int gx = cdiv(OC / vec, 32);
+    int P = cdiv(148 * 4, gx);
+    if (P > nch) P = nch;
     float* part = (float*)scratch;
-    if (OC % VM == 0) {
-        dim3 grid(cdiv(OC / VM, 32), nch);
-        k_bias_part<T, VM><<<grid, 256, 0, s>>>(part, (const T*)dout, N, OC);
-    } else {
-        dim3 grid(cdiv(OC, 32), nch);
-        k_bias_part<T, 1><<<grid, 256, 0, s>>>(part, (const T*)dout, N, OC);
-    }
-    k_colsum<<<cdiv(OC, 32), 256, 0, s>>>(db, db, OC, OC, part, nch, OC);
+    dim3 grid(gx, P);
+    if (vec == VM) k_bias_part<T, VM><<<grid, 256, 0, s>>>(part, (const T*)dout, N, OC, nch);
+    else k_bias_part<T, 1><<<grid, 256, 0, s>>>(part, (const T*)dout, N, OC, nch);
+    ColsumOut o{{db, nullptr, nullptr}};
+    k_colsum<<<cdiv(OC, 32), 256, 0, s>>>(o, OC, OC, part, P, OC);
     return cudaGetLastError();
 }
 cudaError_t bias_grad(int act, float* db, const void* dout, int N, int OC, void* scratch,
@@ -554,13 +787,162 @@ __global__ void __launch_bounds__(512) k_xent(T* logits, float* losses, const in
     }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 rows staged whole in shared memory.  One persistent block per SM walks
+// the rows blockIdx.x, blockIdx.x + gridDim.x, ...; while it works on one row,
+// a bulk copy (cp.async.bulk, completion counted on an mbarrier) brings the
+// next row into the other half of the double buffer, so each row is read from
+// HBM once and the next read is always in flight.  Per row: max over the V
+// real columns, sum of exp(z - max), lse = max + log(sum), loss, then the
+// in-place write of (softmax - onehot) * dloss with the pad columns zeroed.
+// ---------------------------------------------------------------------------
+#define XS_THREADS 1024
+#define XS_CHUNK 32768u  // bytes per bulk copy
+
+__device__ __forceinline__ float ex2f_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+// block-wide reduction (op 0 = max, 1 = sum) of one value per thread
+__device__ __forceinline__ float block_reduce(float v, int op, float* red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    v = op ? warp_sum(v) : warp_max(v);
+    __syncthreads();  // red[] may still be read by the previous reduction
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = red[lane];  // blockDim.x == 1024: 32 warps
+    return op ? warp_sum(v) : warp_max(v);
+}
+
+__global__ void __launch_bounds__(XS_THREADS, 1)
+    k_xent_staged(bf16* logits, float* losses, const int* tgt, int N, int V, int Vp, float dloss,
+                  unsigned* err) {
+    extern __shared__ __align__(128) unsigned char xsm[];
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ float red[32];
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x;
+    const uint32_t rowb = (uint32_t)Vp * 2u;
+    const uint32_t buf0 = tc::smem_u32(xsm);
+    const uint32_t bar0 = tc::smem_u32(&bars[0]);
+    auto issue = [&](int row, int b) {  // thread 0: bring `row` into half b
+        const uint32_t bar = bar0 + 8u * b, dst = buf0 + rowb * b;
+        const char* src = reinterpret_cast<const char*>(logits + (size_t)row * Vp);
+        tc::mbar_expect_tx(bar, rowb);
+        for (uint32_t o = 0; o < rowb; o += XS_CHUNK)
+            bulk_g2s(dst + o, src + o, rowb - o < XS_CHUNK ? rowb - o : XS_CHUNK, bar);
+    };
+    if (tid == 0) {
+        tc::mbar_init(bar0, 1);
+        tc::mbar_init(bar0 + 8, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if ((int)blockIdx.x < N) issue(blockIdx.x, 0);
+    }
+    __syncthreads();
+    int k = 0, row = blockIdx.x;
+    for (; row < N; row += gridDim.x, k++) {
+        const int b = k & 1;
+        const int nrow = row + gridDim.x;
+        if (tid == 0 && nrow < N) {
+            // half b^1 was last read in the previous iteration, which ended
+            // with a block barrier; order those reads before the async write
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(nrow, b ^ 1);
+        }
+        tc::mbar_wait(bar0 + 8u * b, (uint32_t)(k >> 1) & 1u, &abort_flag, err);
+        __syncthreads();
+        if (abort_flag) break;
+        const bf16* z = reinterpret_cast<const bf16*>(xsm + (size_t)rowb * b);
+        int y = tgt[row];
+        if (y < 0 || y >= V) {
+            if (tid == 0) atomicOr(err, GPT2_DEVERR_TOKEN);
+            y = 0;
+        }
+        // pass 1: row max over the real columns
+        float m = -INFINITY;
+        for (int j = tid * 8; j < V; j += XS_THREADS * 8) {
+            Vec<bf16, 8> v = *reinterpret_cast<const Vec<bf16, 8>*>(z + j);
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                if (j + e < V) m = fmaxf(m, to_f(v.v[e]));
+        }
+        m = block_reduce(m, 0, red);
+        // pass 2: sum of exp(z - max) (z - max is exact for bf16 z)
+        const float L2E = 1.4426950408889634f;
+        float sum = 0.f;
+        for (int j = tid * 8; j < V; j += XS_THREADS * 8) {
+            Vec<bf16, 8> v = *reinterpret_cast<const Vec<bf16, 8>*>(z + j);
+#pragma unroll
+            for (int e = 0; e < 8; e++)
+                if (j + e < V) sum += ex2f_approx((to_f(v.v[e]) - m) * L2E);
+        }
+        sum = block_reduce(sum, 1, red);
+        const float lse = m + logf(sum);
+        if (tid == 0) losses[row] = lse - to_f(z[y]);
+        if (dloss != 0.f) {
+            // pass 3: dlogits, written over the row in global memory
+            bf16* zo = logits + (size_t)row * Vp;
+            const float nl = -lse * L2E;
+            for (int j = tid * 8; j < Vp; j += XS_THREADS * 8) {
+                Vec<bf16, 8> v = *reinterpret_cast<const Vec<bf16, 8>*>(z + j);
+                Vec<bf16, 8> o;
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int col = j + e;
+                    const float p = ex2f_approx(fmaf(to_f(v.v[e]), L2E, nl));
+                    o.v[e] = from_f<bf16>(col < V ? (p - (col == y ? 1.f : 0.f)) * dloss : 0.f);
+                }
+                *reinterpret_cast<Vec<bf16, 8>*>(zo + j) = o;
+            }
+        }
+        __syncthreads();  // half b is free for the copy issued next iteration
+    }
+    if (abort_flag && tid == 0) {
+        // a wait ran out in iteration k: let this block's copies still in
+        // flight (row k's, and the prefetch of the next row if one was
+        // issued) land, within the same bound, before its shared memory is
+        // released
+        volatile int own = 0;
+        tc::mbar_wait(bar0 + 8u * (k & 1), (uint32_t)(k >> 1) & 1u, &own, nullptr);
+        own = 0;
+        if (row + (int)gridDim.x < N)
+            tc::mbar_wait(bar0 + 8u * ((k + 1) & 1), (uint32_t)((k + 1) >> 1) & 1u, &own,
+                          nullptr);
+    }
+}
+
 cudaError_t crossentropy_fused(int act, void* logits, float* losses, const int* tgt, int N,
                                int V, int Vp, float dloss, unsigned* err, cudaStream_t s) {
     if (Vp % 8) return cudaErrorInvalidValue;
-    if (act == ACT_BF16)
-        k_xent<bf16, 8><<<N, 512, 0, s>>>((bf16*)logits, losses, tgt, V, Vp, dloss, err);
-    else
+    if (act == ACT_BF16) {
+        const size_t smem = (size_t)4 * Vp;  // two bf16 rows
+        if (smem <= 200 * 1024 && ((uintptr_t)logits & 15) == 0) {
+            static_assert(XS_THREADS == 1024, "block_reduce assumes 32 warps");
+            int dev = 0, nsm = 148;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+            cudaError_t e = cudaFuncSetAttribute(
+                k_xent_staged, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            const int grid = N < nsm ? N : nsm;
+            k_xent_staged<<<grid, XS_THREADS, smem, s>>>((bf16*)logits, losses, tgt, N, V, Vp,
+                                                        dloss, err);
+        } else {
+            k_xent<bf16, 8><<<N, 512, 0, s>>>((bf16*)logits, losses, tgt, V, Vp, dloss, err);
+        }
+    } else {
         k_xent<float, 4><<<N, 512, 0, s>>>((float*)logits, losses, tgt, V, Vp, dloss, err);
+    }
     return cudaGetLastError();
 }
 

@@ -59,14 +59,14 @@ extern "C" int gpt2k_layernorm_backward_noalloc(int dtype, void* dx, float* dw, 
                                                 const float* mean, const float* rstd, int N,
                                                 int C, void* stream) {
     if ((dtype != gk::ACT_F32 && dtype != gk::ACT_BF16) || N < 1 || C < 1) return GPT2_ERR_ARG;
-    if (C > kMaxC || gk::layernorm_backward_scratch(N, C) > kScratchBytes)
+    if (C > kMaxC || gk::layernorm_backward_scratch(N, C, false) > kScratchBytes)
         return GPT2_ERR_ARG;  // wider than the fixed scratch serves
     void* scratch = scratch_on_current_device();
     if (!scratch) return GPT2_ERR_CUDA;
     // every block overwrites its own partial rows before they are summed, so
     // nothing left in the array by an earlier call needs clearing
-    cudaError_t e = gk::layernorm_backward(dtype, dx, dw, db, dout, x, w, mean, rstd, N, C,
-                                           scratch, (cudaStream_t)stream);
+    cudaError_t e = gk::layernorm_backward(dtype, dx, dw, db, nullptr, dout, x, w, mean, rstd, N,
+                                           C, true, scratch, (cudaStream_t)stream);
     if (e == cudaSuccess) return GPT2_OK;
     cudaGetLastError();
     return e == cudaErrorInvalidValue ? GPT2_ERR_ARG : GPT2_ERR_CUDA;

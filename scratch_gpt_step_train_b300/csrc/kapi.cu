@@ -70,16 +70,16 @@ extern "C" int gpt2k_layernorm_forward(int dtype, void* out, float* mean, float*
 }
 
 extern "C" size_t gpt2k_layernorm_backward_scratch_bytes(int N, int C) {
-    return layernorm_backward_scratch(N, C);
+    return layernorm_backward_scratch(N, C, true);
 }
 
-extern "C" int gpt2k_layernorm_backward(int dtype, void* dx, float* dw, float* db,
+extern "C" int gpt2k_layernorm_backward(int dtype, void* dx, float* dw, float* db, float* dxsum,
                                         const void* dout, const void* x, const void* w,
                                         const float* mean, const float* rstd, int N, int C,
-                                        void* scratch, void* stream) {
+                                        int accumulate, void* scratch, void* stream) {
     if (!dt_ok(dtype) || N < 1 || C < 1 || !scratch) return GPT2_ERR_ARG;
-    return rc_of(layernorm_backward(dtype, dx, dw, db, dout, x, w, mean, rstd, N, C, scratch,
-                                    (cudaStream_t)stream));
+    return rc_of(layernorm_backward(dtype, dx, dw, db, dxsum, dout, x, w, mean, rstd, N, C,
+                                    accumulate != 0, scratch, (cudaStream_t)stream));
 }
 
 extern "C" int gpt2k_encoder_forward(int dtype, void* out, const int32_t* tok, const void* wte,

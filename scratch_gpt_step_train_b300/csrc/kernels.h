@@ -47,11 +47,14 @@ cudaError_t encoder_backward(int act, float* dwte, float* dwpe, const void* dx, 
 // ---- layernorm ------------------------------------------------------------
 cudaError_t layernorm_forward(int act, void* out, float* mean, float* rstd, const void* x,
                               const void* w, const void* b, int N, int C, cudaStream_t s);
-size_t layernorm_backward_scratch(int N, int C);
-// dx (+=), dw (+=), db (+=); partial column sums go through scratch.
-cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, const void* dout,
-                               const void* x, const void* w, const float* mean,
-                               const float* rstd, int N, int C, void* scratch, cudaStream_t s);
+// scratch for the partial column sums (dxsum != NULL needs the larger size)
+size_t layernorm_backward_scratch(int N, int C, bool dxsum);
+// dx += (accum_dx) or = the LayerNorm input gradient; dw += sum dy*xhat,
+// db += sum dy; dxsum (if not NULL) += the column sums of the dx rows written.
+cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, float* dxsum,
+                               const void* dout, const void* x, const void* w, const float* mean,
+                               const float* rstd, int N, int C, bool accum_dx, void* scratch,
+                               cudaStream_t s);
 
 // ---- bias gradient: db[o] += sum_n dout[n,o] (deterministic, two stage) ---
 size_t bias_grad_scratch(int N, int OC);

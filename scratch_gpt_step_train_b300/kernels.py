@@ -18,8 +18,8 @@ SIGNATURES = {
     "gpt2k_attention_backward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "gpt2k_layernorm_forward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2k_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
-    "gpt2k_layernorm_backward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp,
-                                      _vp]),
+    "gpt2k_layernorm_backward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
+                                      _i, _vp, _vp]),
     "gpt2k_layernorm_backward_noalloc": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i,
                                               _i, _vp]),
     "gpt2k_encoder_forward": (_i, [_i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
@@ -123,13 +123,13 @@ def layernorm_forward(out, mean, rstd, x, w, b):
                                        N, C, _stream()), "layernorm_forward")
 
 
-def layernorm_backward(dx, dw, db, dout, x, w, mean, rstd):
+def layernorm_backward(dx, dw, db, dout, x, w, mean, rstd, dxsum=None, accumulate=True):
     L = klib()
     N, C = x.shape
     scratch = _scratch(L.gpt2k_layernorm_backward_scratch_bytes(N, C))
-    _ck(L.gpt2k_layernorm_backward(_dt(x), _p(dx), _p(dw), _p(db), _p(dout), _p(x), _p(w),
-                                   _p(mean), _p(rstd), N, C, _p(scratch), _stream()),
-        "layernorm_backward")
+    _ck(L.gpt2k_layernorm_backward(_dt(x), _p(dx), _p(dw), _p(db), _p(dxsum), _p(dout), _p(x),
+                                   _p(w), _p(mean), _p(rstd), N, C, int(accumulate), _p(scratch),
+                                   _stream()), "layernorm_backward")
 
 
 def layernorm_backward_noalloc(dx, dw, db, dout, x, w, mean, rstd):

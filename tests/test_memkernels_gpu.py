@@ -127,9 +127,10 @@ def test_layernorm_forward(N, C, dtype):
     assert np.all(np.abs(rstd.double().cpu().numpy() - rr) <= 1e-5 * rr)
 
 
+@pytest.mark.parametrize("mode", ["accum", "overwrite_dxsum"])
 @pytest.mark.parametrize("N,C", [(37, 200), (16384, 768), (300, 1600)], ids=["small", "full", "c1600"])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
-def test_layernorm_backward(N, C, dtype):
+def test_layernorm_backward(N, C, dtype, mode):
     x, w, b = _ln_inputs(N, C, 2)
     rng = np.random.default_rng(3)
     dy = rng.normal(0, 1, (N, C))
@@ -139,19 +140,32 @@ def test_layernorm_backward(N, C, dtype):
     mean = torch.empty(N, device="cuda")
     rstd = torch.empty(N, device="cuda")
     K.layernorm_forward(out, mean, rstd, xt, wt, bt)
+    accumulate = mode == "accum"
     dx = _t(dx0, dtype)
-    dx0r = _np(dx)
+    dx0r = _np(dx) if accumulate else np.zeros((N, C))
     dw0 = rng.normal(0, 1, C).astype(np.float32)
     db0 = rng.normal(0, 1, C).astype(np.float32)
     dw = torch.from_numpy(dw0).cuda()
     db = torch.from_numpy(db0).cuda()
-    K.layernorm_backward(dx, dw, db, dyt, xt, wt, mean, rstd)
+    dxsum = None
+    if not accumulate:
+        ds0 = rng.normal(0, 1, C).astype(np.float32)
+        dxsum = torch.from_numpy(ds0).cuda()
+    K.layernorm_backward(dx, dw, db, dyt, xt, wt, mean, rstd, dxsum=dxsum, accumulate=accumulate)
     _, rm, rr = ops.layernorm_forward(_np(xt), _np(wt), _np(bt))
     rdx, rdw, rdb = ops.layernorm_backward(_np(dyt), _np(xt), _np(wt), rm, rr)
     tol = 1e-4 if dtype == torch.float32 else 1e-2
     assert_close(_np(dx) - dx0r, rdx, tol, "dx")
     assert_close(dw.double().cpu().numpy() - dw0, rdw, 1e-4, "dw")
     assert_close(db.double().cpu().numpy() - db0, rdb, 1e-4, "db")
+    if dxsum is not None:
+        # dxsum is the column sum of the rows as written (dx itself is checked
+        # against the oracle above): exact up to fp32 summation, whose error is
+        # at most about N * 2^-24 * sum|dx| per column
+        st = _np(dx)
+        got = dxsum.double().cpu().numpy() - ds0.astype(np.float64)
+        bound = (N + 8) * 2.0 ** -24 * np.abs(st).sum(0) + 2.0 ** -24 * np.abs(ds0) * 4
+        assert np.all(np.abs(got - st.sum(0)) <= bound), "dxsum"
 
 
 # -------------------------------------------------------------- bias gradient
