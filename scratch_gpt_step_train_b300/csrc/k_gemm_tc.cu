@@ -684,12 +684,45 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     if (!gemm_tc_available()) return cudaErrorNotSupported;
     if (!gemm_tc_supported(d)) return cudaErrorInvalidValue;
     const int tiles_m = (d.M + BM - 1) / BM;
-    // 128 x 256 tiles halve the operand traffic per flop against 128 x 128;
-    // narrow outputs, and products with too few tiles that cannot be split
-    // along K, take 128 x 128 tiles
+    // 128 x 256 tiles halve the operand traffic per flop against 128 x 128
     const bool can_split = d.epi == EPI_ACCUM_F32 && d.K >= 8 * BK && scratch;
-    int BN = 256;
-    if (d.N <= 128 || (!can_split && (long)tiles_m * ((d.N + 255) / 256) < g_num_sms)) BN = 128;
+    const int kb = (d.K + BK - 1) / BK;
+    int BN = 256, splits = 1;
+    if (can_split) {
+        // Weight-gradient products (long K, few output tiles): pick the tile
+        // width and the K split from a time model -- whole waves of work units
+        // over the SMs, each unit's k-blocks at the tile width's rate, plus the
+        // fp32 traffic of the output (read-modify-write) and of the split's
+        // partial sums (written, then read back by the ordered reduction).
+        // The k-block rates are measured ones: a 128 x 128 tile needs twice
+        // the L2 bytes per flop of a 128 x 256 tile whose B half is shared by
+        // a CTA pair, and runs at about the same k-block time, i.e. half the
+        // flop rate.
+        const double kblock_us[2] = {0.30, 0.31};  // 128x256 (paired) / 128x128
+        const double bytes_per_us = 5.0e6;
+        const double mn4 = 4.0 * d.M * d.N;
+        double best = 1e30;
+        for (int w = 0; w < 2; w++) {
+            const int bn = w ? 128 : 256;
+            const long t = (long)tiles_m * ((d.N + bn - 1) / bn);
+            for (int sp = 1; sp <= 16 && (sp == 1 || sp <= kb / 4); sp++) {
+                if (sp > 1 && (size_t)sp * d.M * d.N * 4 > scratch_bytes) break;
+                const int kbs = (kb + sp - 1) / sp, sps = (kb + kbs - 1) / kbs;
+                if (sp > 1 && sps != sp) continue;
+                const long waves = (t * sps + g_num_sms - 1) / g_num_sms;
+                const double us = waves * kbs * kblock_us[w] +
+                                  (sps > 1 ? 2.0 * sps + 2.0 : 2.0) * mn4 / bytes_per_us;
+                if (us < best - 1e-9) {
+                    best = us;
+                    BN = bn;
+                    splits = sps;
+                }
+            }
+        }
+    } else if (d.N <= 128 || (long)tiles_m * ((d.N + 255) / 256) < g_num_sms) {
+        // narrow outputs, and products with too few 128 x 256 tiles
+        BN = 128;
+    }
     const int tiles_n = (d.N + BN - 1) / BN;
     TcParams tp;
     tp.M = d.M; tp.N = d.N; tp.K = d.K;
@@ -708,18 +741,11 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     tp.part = (float*)scratch;
     tp.err = err;
     const long tiles = (long)tiles_m * tiles_n;
-    if (can_split && tiles < g_num_sms) {
-        int splits = (int)((2L * g_num_sms + tiles - 1) / tiles);
-        int kb = (d.K + BK - 1) / BK;
-        if (splits > kb / 4) splits = kb / 4;
-        if (splits > 16) splits = 16;
-        while (splits > 1 && (size_t)splits * d.M * d.N * 4 > scratch_bytes) splits--;
-        if (splits > 1) {
-            int kbs = (kb + splits - 1) / splits;
-            tp.k_per_split = kbs * BK;
-            tp.splits = (kb + kbs - 1) / kbs;
-            tp.epi = EPI_PART_F32;
-        }
+    if (splits > 1) {
+        const int kbs = (kb + splits - 1) / splits;
+        tp.k_per_split = kbs * BK;
+        tp.splits = (kb + kbs - 1) / kbs;
+        tp.epi = EPI_PART_F32;
     }
     tp.num_tiles = (int)(tiles * tp.splits);
     const bool am = !d.a_kmajor, bm = !d.b_kmajor;
