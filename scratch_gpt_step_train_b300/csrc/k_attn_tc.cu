@@ -108,8 +108,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
     uint32_t* tmem_slot = (uint32_t*)(base_gen + F_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + F_BAR + 132);
 
-    const int qt = p.nqt - 1 - (int)blockIdx.x;  // longest rows first
-    const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+    // blocks launch in linear order, x fastest: every head's longest rows
+    // first, so that the short tiles fill in the tail
+    const int qt = p.nqt - 1 - (int)blockIdx.y;
+    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int nkt = qt + 1;
     const int row0 = b * p.T;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -386,8 +388,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     uint32_t* tmem_slot = (uint32_t*)(base_gen + D_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + D_BAR + 132);
 
-    const int kt = p.nqt - 1 - (int)blockIdx.x;  // fewest query steps last
-    const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+    const int kt = (int)blockIdx.y;  // most query steps first (x fastest: all heads)
+    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int i0 = 2 * kt;       // first 64-query step that sees these keys
     const int nq = p.nsub - i0;  // query steps
     const int row0 = b * p.T;
@@ -609,8 +611,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     uint32_t* tmem_slot = (uint32_t*)(base_gen + E_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + E_BAR + 132);
 
-    const int qt = p.nqt - 1 - (int)blockIdx.x;
-    const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+    const int qt = p.nqt - 1 - (int)blockIdx.y;  // most key steps first
+    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int nk = min(2 * qt + 2, p.nsub);  // 64-key steps 0..nk-1
     const int row0 = b * p.T;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -838,7 +840,7 @@ cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv,
     p.err = err;
     p.scale = 1.0f / sqrtf((float)HD);
     p.scale_log2 = 1.4426950408889634f * p.scale;
-    dim3 grid(p.nqt, B * H);
+    dim3 grid(B * H, p.nqt);
     k_attn_dkv_tc<<<grid, BWD_THREADS, D_SMEM, s>>>(maps, p);
     k_attn_dq_tc<<<grid, BWD_THREADS, E_SMEM, s>>>(maps, p);
     return cudaGetLastError();
@@ -869,7 +871,7 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
     p.lse = lse;
     p.err = err;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-    dim3 grid(p.nqt, B * H);
+    dim3 grid(B * H, p.nqt);
     k_attn_fwd_tc<<<grid, FWD_THREADS, F_SMEM, s>>>(map, p);
     return cudaGetLastError();
 }
