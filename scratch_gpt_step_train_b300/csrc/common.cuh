@@ -31,6 +31,17 @@ __device__ __forceinline__ double warp_sum_d(double v) {
     return v;
 }
 
+// Programmatic dependent launch: every kernel of the library is launched
+// allowed to start before the kernel ahead of it in the stream has finished
+// (launch_pdl); gdc_wait() blocks until that kernel has completed and its
+// memory is visible, and must come before the first global-memory access.
+// gdc_launch_dependents() then lets the next kernel's blocks be scheduled as
+// this grid's blocks finish, so its launch and setup overlap this grid's tail.
+__device__ __forceinline__ void gdc_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void gdc_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Vector of N elements of T moved as one 16-byte (or smaller) access.
 template <typename T, int N>
 struct alignas(sizeof(T) * N) Vec {

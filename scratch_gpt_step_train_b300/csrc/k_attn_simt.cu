@@ -24,6 +24,8 @@ namespace gk {
 template <typename T, int HD>
 __global__ void __launch_bounds__(AT_TILE) k_attn_fwd(T* out, float* lse, const T* qkv, int T_,
                                                       int C, int H) {
+    gdc_wait();
+    gdc_launch_dependents();
     extern __shared__ float sm[];
     float* Ks = sm;                      // [AT_TILE][HD]
     float* Vs = sm + AT_TILE * HD;       // [AT_TILE][HD]
@@ -87,6 +89,8 @@ __global__ void __launch_bounds__(AT_TILE) k_attn_fwd(T* out, float* lse, const 
 template <typename T>
 __global__ void k_attn_D(float* Dv, const T* dout, const T* out, int B, int T_, int C, int H,
                          int hd) {
+    gdc_wait();
+    gdc_launch_dependents();
     long idx = blockIdx.x * (long)blockDim.x + threadIdx.x;
     if (idx >= (long)B * H * T_) return;
     int t = (int)(idx % T_);
@@ -101,6 +105,8 @@ __global__ void k_attn_D(float* Dv, const T* dout, const T* out, int B, int T_, 
 // D for head size 64 in bf16: one thread per (row, head), 16-byte loads
 __global__ void k_attn_D64_bf16(float* Dv, const bf16* dout, const bf16* out, int B, int T_,
                                 int C, int H) {
+    gdc_wait();
+    gdc_launch_dependents();
     long idx = blockIdx.x * (long)blockDim.x + threadIdx.x;  // (row, head), head fastest
     if (idx >= (long)B * T_ * H) return;
     int h = (int)(idx % H);
@@ -129,6 +135,8 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(AT_TILE) k_attn_dq(T* dqkv, const T* dout, const T* qkv,
                                                      const float* lse, const float* Dv, int T_,
                                                      int C, int H) {
+    gdc_wait();
+    gdc_launch_dependents();
     extern __shared__ float sm[];
     const int P = HD + 1;
     float* Ks = sm;                    // [AT_TILE][HD]
@@ -185,6 +193,8 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(AT_TILE) k_attn_dkv(T* dqkv, const T* dout, const T* qkv,
                                                       const float* lse, const float* Dv, int T_,
                                                       int C, int H) {
+    gdc_wait();
+    gdc_launch_dependents();
     extern __shared__ float sm[];
     const int P = HD + 1;
     float* Ks = sm;                    // [AT_TILE][P]  this block's keys
@@ -254,7 +264,7 @@ static cudaError_t attn_fwd_hd(void* out, float* lse, const void* qkv, int B, in
     size_t smem = 2 * AT_TILE * HD * sizeof(float);
     auto kf = k_attn_fwd<T, HD>;
     cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kf<<<grid, AT_TILE, smem, s>>>((T*)out, lse, (const T*)qkv, T_, C, H);
+    launch_pdl(kf, grid, AT_TILE, smem, s, (T*)out, lse, (const T*)qkv, T_, C, H);
     return cudaGetLastError();
 }
 
@@ -263,18 +273,18 @@ static cudaError_t attn_bwd_hd(void* dqkv, const void* dout, const void* qkv, co
                                const float* lse, int B, int T_, int C, int H, float* Dv,
                                cudaStream_t s) {
     long n = (long)B * H * T_;
-    k_attn_D<T><<<(int)((n + 255) / 256), 256, 0, s>>>(Dv, (const T*)dout, (const T*)out, B, T_,
+    launch_pdl(k_attn_D<T>, (int)((n + 255) / 256), 256, 0, s, Dv, (const T*)dout, (const T*)out, B, T_,
                                                        C, H, HD);
     dim3 grid((T_ + AT_TILE - 1) / AT_TILE, B * H);
     const int P = HD + 1;
     size_t smq = (2 * AT_TILE * HD + 2 * AT_TILE * P) * sizeof(float);
     auto kq = k_attn_dq<T, HD>;
     cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
-    kq<<<grid, AT_TILE, smq, s>>>((T*)dqkv, (const T*)dout, (const T*)qkv, lse, Dv, T_, C, H);
+    launch_pdl(kq, grid, AT_TILE, smq, s, (T*)dqkv, (const T*)dout, (const T*)qkv, lse, Dv, T_, C, H);
     size_t smk = (2 * AT_TILE * P + 2 * AT_TILE * HD + 2 * AT_TILE) * sizeof(float);
     auto kk = k_attn_dkv<T, HD>;
     cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
-    kk<<<grid, AT_TILE, smk, s>>>((T*)dqkv, (const T*)dout, (const T*)qkv, lse, Dv, T_, C, H);
+    launch_pdl(kk, grid, AT_TILE, smk, s, (T*)dqkv, (const T*)dout, (const T*)qkv, lse, Dv, T_, C, H);
     return cudaGetLastError();
 }
 
@@ -309,7 +319,7 @@ cudaError_t attention_backward(int act, void* dqkv, const void* dout, const void
     float* Dv = (float*)scratch;
     if (attention_tc_supported(act, B, T_, C, H, qkv)) {
         long n = (long)B * H * T_;
-        k_attn_D64_bf16<<<(int)((n + 255) / 256), 256, 0, s>>>(Dv, (const bf16*)dout,
+        launch_pdl(k_attn_D64_bf16, (int)((n + 255) / 256), 256, 0, s, Dv, (const bf16*)dout,
                                                                (const bf16*)out, B, T_, C, H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    gdc_wait();  // setup above touches no global memory
+    gdc_launch_dependents();
     const uint32_t tS = tmem, tO = tmem + 128;  // S [128 x 128], O [128 x 64] fp32
 
     if (warp == 0) {
@@ -416,6 +418,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    gdc_wait();  // setup above touches no global memory
+    gdc_launch_dependents();
     const uint32_t tST = tmem, tDPT = tmem + 64, tDV = tmem + 128, tDK = tmem + 192;
 
     if (warp == 0) {
@@ -638,6 +642,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    gdc_wait();  // setup above touches no global memory
+    gdc_launch_dependents();
     const uint32_t tS = tmem, tDP = tmem + 64, tDQ = tmem + 128;
 
     if (warp == 0) {
@@ -841,8 +847,8 @@ cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv,
     p.scale = 1.0f / sqrtf((float)HD);
     p.scale_log2 = 1.4426950408889634f * p.scale;
     dim3 grid(B * H, p.nqt);
-    k_attn_dkv_tc<<<grid, BWD_THREADS, D_SMEM, s>>>(maps, p);
-    k_attn_dq_tc<<<grid, BWD_THREADS, E_SMEM, s>>>(maps, p);
+    launch_pdl(k_attn_dkv_tc, grid, BWD_THREADS, D_SMEM, s, maps, p);
+    launch_pdl(k_attn_dq_tc, grid, BWD_THREADS, E_SMEM, s, maps, p);
     return cudaGetLastError();
 }
 
@@ -872,7 +878,7 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
     p.err = err;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
     dim3 grid(B * H, p.nqt);
-    k_attn_fwd_tc<<<grid, FWD_THREADS, F_SMEM, s>>>(map, p);
+    launch_pdl(k_attn_fwd_tc, grid, FWD_THREADS, F_SMEM, s, map, p);
     return cudaGetLastError();
 }
 

@@ -19,6 +19,8 @@ namespace gk {
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_gemm_simt(GemmDesc d) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ float As[SG_BK][SG_BM + 4];
     __shared__ float Bs[SG_BK][SG_BN + 4];
     const T* A = (const T*)d.A;
@@ -115,8 +117,8 @@ cudaError_t gemm_simt(const GemmDesc& d, cudaStream_t s) {
     if (d.M <= 0 || d.N <= 0) return cudaSuccess;
     dim3 grid((d.N + SG_BN - 1) / SG_BN, (d.M + SG_BM - 1) / SG_BM);
     if (grid.y > 65535) return cudaErrorInvalidValue;
-    if (d.act == ACT_BF16) k_gemm_simt<bf16><<<grid, 256, 0, s>>>(d);
-    else k_gemm_simt<float><<<grid, 256, 0, s>>>(d);
+    if (d.act == ACT_BF16) launch_pdl(k_gemm_simt<bf16>, grid, 256, 0, s, d);
+    else launch_pdl(k_gemm_simt<float>, grid, 256, 0, s, d);
     return cudaGetLastError();
 }
 

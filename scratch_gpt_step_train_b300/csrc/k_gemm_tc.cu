@@ -298,6 +298,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (MC) cluster_sync_all();  // the peer's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    gdc_wait();  // setup above touches no global memory
+    gdc_launch_dependents();
     // work units: single tiles, or (with MC) pairs of vertically adjacent tiles
     const int rank = MC ? (int)cluster_ctarank() : 0;
     const int units_m = MC ? (p.tiles_m + 1) / 2 : p.tiles_m;
@@ -484,6 +486,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // split-K: D[m,n] += sum_s part[s][m][n], s in order
 __global__ void k_splitk_reduce(float* D, long ldd, const float* part, int M, int N, int splits) {
+    gdc_wait();
+    gdc_launch_dependents();
     long idx = blockIdx.x * (long)blockDim.x + threadIdx.x;
     long nv = (long)M * (N / 4);
     if (idx >= nv) return;
@@ -578,7 +582,7 @@ cudaError_t launch(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     if (!ok) return cudaErrorInvalidValue;
     if (!MC) {
         const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
-        k_gemm_tc<BN, AM, BMN, false><<<grid, NUM_THREADS, Cfg<BN>::SMEM, s>>>(ma, mb, em, tp);
+        launch_pdl(k_gemm_tc<BN, AM, BMN, false>, grid, NUM_THREADS, Cfg<BN>::SMEM, s, ma, mb, em, tp);
         return cudaGetLastError();
     }
     const int units = ((tp.tiles_m + 1) / 2) * tp.tiles_n * tp.splits;
@@ -590,13 +594,15 @@ cudaError_t launch(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, AM, BMN, true>, ma, mb, em, tp);
 }
 
@@ -772,7 +778,7 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     if (tp.splits > 1) {
         if (nlaunch) *nlaunch = 2;
         long nv = (long)d.M * (d.N / 4);
-        k_splitk_reduce<<<(int)((nv + 255) / 256), 256, 0, s>>>((float*)d.D, d.ldd, tp.part, d.M,
+        launch_pdl(k_splitk_reduce, (int)((nv + 255) / 256), 256, 0, s, (float*)d.D, d.ldd, tp.part, d.M,
                                                                 d.N, tp.splits);
         e = cudaGetLastError();
     }

@@ -55,6 +55,8 @@ __device__ __forceinline__ double unit_open(uint64_t x) {
 }
 
 __global__ void k_init_params(float* p, ParamLayout lay, uint64_t seed, double sd, double sd_res) {
+    gdc_wait();
+    gdc_launch_dependents();
     size_t n = lay.off[P_NUM];
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -83,17 +85,19 @@ __global__ void k_init_params(float* p, ParamLayout lay, uint64_t seed, double s
 }
 
 cudaError_t init_params(float* master, const ParamLayout& lay, uint64_t seed, cudaStream_t s) {
-    k_init_params<<<148 * 8, 256, 0, s>>>(master, lay, seed, 0.02, 0.02 / sqrt(2.0 * lay.L));
+    launch_pdl(k_init_params, 148 * 8, 256, 0, s, master, lay, seed, 0.02, 0.02 / sqrt(2.0 * lay.L));
     return cudaGetLastError();
 }
 
 __global__ void k_cast_bf16(bf16* dst, const float* src, size_t n) {
+    gdc_wait();
+    gdc_launch_dependents();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x)
         dst[i] = __float2bfloat16_rn(src[i]);
 }
 cudaError_t cast_to_bf16(void* dst, const float* src, size_t n, cudaStream_t s) {
-    k_cast_bf16<<<148 * 8, 256, 0, s>>>((bf16*)dst, src, n);
+    launch_pdl(k_cast_bf16, 148 * 8, 256, 0, s, (bf16*)dst, src, n);
     return cudaGetLastError();
 }
 
@@ -103,6 +107,8 @@ cudaError_t cast_to_bf16(void* dst, const float* src, size_t n, cudaStream_t s) 
 template <typename T, int VEC>
 __global__ void k_encoder_fwd(T* out, const int* tok, const T* wte, const T* wpe, int BT, int T_,
                               int C, int V, unsigned* err) {
+    gdc_wait();
+    gdc_launch_dependents();
     int cv = C / VEC;
     long total = (long)BT * cv;
     for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total;
@@ -130,12 +136,10 @@ static cudaError_t enc_fwd_t(void* out, const int* tok, const void* wte, const v
     constexpr int VM = 16 / sizeof(T);
     if (C % VM == 0) {
         long total = (long)BT * (C / VM);
-        k_encoder_fwd<T, VM><<<cdiv(total, 256) < 148 * 16 ? cdiv(total, 256) : 148 * 16, 256, 0,
-                              s>>>((T*)out, tok, (const T*)wte, (const T*)wpe, BT, T_, C, V, err);
+        launch_pdl(k_encoder_fwd<T, VM>, cdiv(total, 256) < 148 * 16 ? cdiv(total, 256) : 148 * 16, 256, 0, s, (T*)out, tok, (const T*)wte, (const T*)wpe, BT, T_, C, V, err);
     } else {
         long total = (long)BT * C;
-        k_encoder_fwd<T, 1><<<cdiv(total, 256) < 148 * 16 ? cdiv(total, 256) : 148 * 16, 256, 0,
-                             s>>>((T*)out, tok, (const T*)wte, (const T*)wpe, BT, T_, C, V, err);
+        launch_pdl(k_encoder_fwd<T, 1>, cdiv(total, 256) < 148 * 16 ? cdiv(total, 256) : 148 * 16, 256, 0, s, (T*)out, tok, (const T*)wte, (const T*)wpe, BT, T_, C, V, err);
     }
     return cudaGetLastError();
 }
@@ -152,6 +156,8 @@ cudaError_t encoder_forward(int act, void* out, const int* tok, const void* wte,
 template <typename T, int VEC, int IT>
 __global__ void __launch_bounds__(256) k_ln_fwd(T* out, float* mean, float* rstd, const T* x,
                                                 const T* w, const T* b, int N, int C) {
+    gdc_wait();
+    gdc_launch_dependents();
     int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     int lane = threadIdx.x & 31;
     if (row >= N) return;
@@ -206,7 +212,7 @@ static cudaError_t ln_fwd_vec(void* out, float* mean, float* rstd, const void* x
     int it = cdiv(C, 32 * VEC);
     dim3 grid(cdiv(N, 8)), blk(256);
 #define LNF(I)                                                                                   \
-    k_ln_fwd<T, VEC, I><<<grid, blk, 0, s>>>((T*)out, mean, rstd, (const T*)x, (const T*)w,     \
+    launch_pdl(k_ln_fwd<T, VEC, I>, grid, blk, 0, s, (T*)out, mean, rstd, (const T*)x, (const T*)w,     \
                                             (const T*)b, N, C)
     if (it <= 1) LNF(1);
     else if (it <= 2) LNF(2);
@@ -266,6 +272,8 @@ template <typename T, int VEC, int IT, int NACC>
 __global__ void __launch_bounds__(LnbCfg<VEC, IT, NACC>::W * 32, 2)
     k_ln_bwd(T* dx, float* part, const T* dout, const T* x, const T* w, const float* mean,
              const float* rstd, int N, int C, int accum_dx) {
+    gdc_wait();
+    gdc_launch_dependents();
     extern __shared__ float lsm[];  // [warps][NACC][S]
     constexpr int S = LnbCfg<VEC, IT, NACC>::S;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -382,6 +390,8 @@ template <int IT, int NACC>
 __global__ void __launch_bounds__(256, 2)
     k_ln_bwd_ring(bf16* dx, float* part, const bf16* dout, const bf16* x, const bf16* w,
                   const float* mean, const float* rstd, int N, int C, int accum_dx) {
+    gdc_wait();
+    gdc_launch_dependents();
     // ring: [warp][slot 0/1][x | dy | dx][IT*256 bf16]; reused for the fold
     extern __shared__ __align__(16) unsigned char rsm[];
     constexpr int ROWV = IT * 32;              // 16-byte vectors per row array (max)
@@ -508,6 +518,8 @@ struct ColsumOut {
 };
 __global__ void __launch_bounds__(256) k_colsum(ColsumOut outs, int n0, int ncols,
                                                 const float* part, int nparts, long ld) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ float sh[8][33];
     int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     int c = blockIdx.x * 32 + tx;
@@ -546,7 +558,7 @@ static cudaError_t ln_bwd_launch(T* dx, float* part, const T* dout, const T* x, 
         int nb = cdiv(N, 8 * 4);
         if (nb > LNB_MAX_BLOCKS) nb = LNB_MAX_BLOCKS;
         *nb_out = nb;
-        kern<<<nb, 256, smem, s>>>(dx, part, dout, x, w, mean, rstd, N, C, accum);
+        launch_pdl(kern, nb, 256, smem, s, dx, part, dout, x, w, mean, rstd, N, C, accum);
         return cudaGetLastError();
     }
     constexpr int S = LnbCfg<VEC, IT, NACC>::S, W = LnbCfg<VEC, IT, NACC>::W;
@@ -561,7 +573,7 @@ static cudaError_t ln_bwd_launch(T* dx, float* part, const T* dout, const T* x, 
     int nb = cdiv(N, W * 4);
     if (nb > LNB_MAX_BLOCKS) nb = LNB_MAX_BLOCKS;
     *nb_out = nb;
-    kern<<<nb, W * 32, smem, s>>>(dx, part, dout, x, w, mean, rstd, N, C, accum);
+    launch_pdl(kern, nb, W * 32, smem, s, dx, part, dout, x, w, mean, rstd, N, C, accum);
     return cudaGetLastError();
 }
 
@@ -606,7 +618,7 @@ static cudaError_t ln_bwd_t(void* dx, float* dw, float* db, float* dxsum, const 
     if (e != cudaSuccess) return e;
     const int nacc = dxsum ? 3 : 2;
     ColsumOut o{{dw, db, dxsum}};
-    k_colsum<<<cdiv(nacc * C, 32), 256, 0, s>>>(o, C, nacc * C, part, nb, (long)nacc * C);
+    launch_pdl(k_colsum, cdiv(nacc * C, 32), 256, 0, s, o, C, nacc * C, part, nb, (long)nacc * C);
     return cudaGetLastError();
 }
 cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, float* dxsum,
@@ -635,6 +647,8 @@ cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, float* d
 template <typename T, int VEC>
 __global__ void __launch_bounds__(256) k_bias_part(float* part, const T* dout, int N, int OC,
                                                    int nch) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ float sh[8][32 * VEC + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     const int c = (blockIdx.x * 32 + tx) * VEC;
@@ -687,10 +701,10 @@ static cudaError_t bias_grad_t(float* db, const void* dout, int N, int OC, void*
     if (P > nch) P = nch;
     float* part = (float*)scratch;
     dim3 grid(gx, P);
-    if (vec == VM) k_bias_part<T, VM><<<grid, 256, 0, s>>>(part, (const T*)dout, N, OC, nch);
-    else k_bias_part<T, 1><<<grid, 256, 0, s>>>(part, (const T*)dout, N, OC, nch);
+    if (vec == VM) launch_pdl(k_bias_part<T, VM>, grid, 256, 0, s, part, (const T*)dout, N, OC, nch);
+    else launch_pdl(k_bias_part<T, 1>, grid, 256, 0, s, part, (const T*)dout, N, OC, nch);
     ColsumOut o{{db, nullptr, nullptr}};
-    k_colsum<<<cdiv(OC, 32), 256, 0, s>>>(o, OC, OC, part, P, OC);
+    launch_pdl(k_colsum, cdiv(OC, 32), 256, 0, s, o, OC, OC, part, P, OC);
     return cudaGetLastError();
 }
 cudaError_t bias_grad(int act, float* db, const void* dout, int N, int OC, void* scratch,
@@ -716,6 +730,8 @@ __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s
 template <typename T, int VEC>
 __global__ void __launch_bounds__(512) k_xent(T* logits, float* losses, const int* tgt, int V,
                                               int Vp, float dloss, unsigned* err) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ float sm_m[32], sm_s[32];
     __shared__ float sh_lse;
     int row = blockIdx.x;
@@ -826,6 +842,8 @@ __device__ __forceinline__ float block_reduce(float v, int op, float* red) {
 __global__ void __launch_bounds__(XS_THREADS, 1)
     k_xent_staged(bf16* logits, float* losses, const int* tgt, int N, int V, int Vp, float dloss,
                   unsigned* err) {
+    gdc_wait();
+    gdc_launch_dependents();
     extern __shared__ __align__(128) unsigned char xsm[];
     __shared__ __align__(8) uint64_t bars[2];
     __shared__ float red[32];
@@ -935,18 +953,20 @@ cudaError_t crossentropy_fused(int act, void* logits, float* losses, const int* 
                 k_xent_staged, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             const int grid = N < nsm ? N : nsm;
-            k_xent_staged<<<grid, XS_THREADS, smem, s>>>((bf16*)logits, losses, tgt, N, V, Vp,
+            launch_pdl(k_xent_staged, grid, XS_THREADS, smem, s, (bf16*)logits, losses, tgt, N, V, Vp,
                                                         dloss, err);
         } else {
-            k_xent<bf16, 8><<<N, 512, 0, s>>>((bf16*)logits, losses, tgt, V, Vp, dloss, err);
+            launch_pdl(k_xent<bf16, 8>, N, 512, 0, s, (bf16*)logits, losses, tgt, V, Vp, dloss, err);
         }
     } else {
-        k_xent<float, 4><<<N, 512, 0, s>>>((float*)logits, losses, tgt, V, Vp, dloss, err);
+        launch_pdl(k_xent<float, 4>, N, 512, 0, s, (float*)logits, losses, tgt, V, Vp, dloss, err);
     }
     return cudaGetLastError();
 }
 
 __global__ void k_mean(float* out, const float* x, int n) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ double sh[32];
     double a = 0.0;
     for (int i = threadIdx.x; i < n; i += blockDim.x) a += (double)x[i];
@@ -960,7 +980,7 @@ __global__ void k_mean(float* out, const float* x, int n) {
     }
 }
 cudaError_t mean_reduce(float* out, const float* x, int n, cudaStream_t s) {
-    k_mean<<<1, 1024, 0, s>>>(out, x, n);
+    launch_pdl(k_mean, 1, 1024, 0, s, out, x, n);
     return cudaGetLastError();
 }
 
@@ -1030,6 +1050,8 @@ size_t encoder_backward_scratch(int B, int T_, int C, int Vp) {
 
 __global__ void __launch_bounds__(EMB_BLK) k_emb_rank(const int* tok, int BT, int Vp, int* lrank,
                                                       int* blkcnt) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ unsigned key[EMB_BLK];
     __shared__ int rs[EMB_BLK];
     int i = threadIdx.x, pos = blockIdx.x * EMB_BLK + i;
@@ -1080,6 +1102,8 @@ __global__ void __launch_bounds__(EMB_BLK) k_emb_rank(const int* tok, int BT, in
 }
 
 __global__ void k_emb_blockprefix(int* blkcnt, int* cnt, int nb, int Vp) {
+    gdc_wait();
+    gdc_launch_dependents();
     int v = blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= Vp) return;
     int run = 0;
@@ -1095,6 +1119,8 @@ __global__ void k_emb_blockprefix(int* blkcnt, int* cnt, int nb, int Vp) {
 // chunks_v over v in [0, Vp).
 __global__ void __launch_bounds__(1024) k_emb_scan(const int* cnt, int* start, int* itemoff,
                                                    int* poff, int Vp) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ int s0[1024], s1[1024], s2[1024];
     int per = (Vp + 1023) / 1024;
     int lo = threadIdx.x * per, hi = min(Vp, lo + per);
@@ -1143,6 +1169,8 @@ __global__ void __launch_bounds__(1024) k_emb_scan(const int* cnt, int* start, i
 
 __global__ void k_emb_place(const int* tok, int BT, int Vp, const int* start, const int* blkcnt,
                             const int* lrank, int* sorted) {
+    gdc_wait();
+    gdc_launch_dependents();
     int pos = blockIdx.x * blockDim.x + threadIdx.x;
     if (pos >= BT) return;
     int t = tok[pos];
@@ -1152,6 +1180,8 @@ __global__ void k_emb_place(const int* tok, int BT, int Vp, const int* start, co
 }
 
 __global__ void k_emb_items(const int* cnt, const int* itemoff, int2* items, int Vp) {
+    gdc_wait();
+    gdc_launch_dependents();
     int v = blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= Vp) return;
     int n = cnt[v];
@@ -1163,6 +1193,8 @@ template <typename T, int VEC, int IT>
 __global__ void k_emb_reduce2(float* dwte, float* part, const T* dx, const int* sorted,
                               const int* cnt, const int* start, const int* n_items,
                               const int* poff, const int2* items, int C) {
+    gdc_wait();
+    gdc_launch_dependents();
     int item = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     int lane = threadIdx.x & 31;
     if (item >= *n_items) return;
@@ -1206,6 +1238,8 @@ __global__ void k_emb_reduce2(float* dwte, float* part, const T* dx, const int* 
 
 __global__ void k_emb_fold(float* dwte, const float* part, const int* cnt, const int* poff,
                            const int* n_items, const int2* items, int C) {
+    gdc_wait();
+    gdc_launch_dependents();
     int item = blockIdx.x;
     if (item >= *n_items) return;
     int2 vc = items[item];
@@ -1223,6 +1257,8 @@ __global__ void k_emb_fold(float* dwte, const float* part, const int* cnt, const
 
 template <typename T, int VEC>
 __global__ void k_wpe_bwd(float* dwpe, const T* dx, int B, int T_, int C) {
+    gdc_wait();
+    gdc_launch_dependents();
     long idx = blockIdx.x * (long)blockDim.x + threadIdx.x;
     int cv = C / VEC;
     if (idx >= (long)T_ * cv) return;
@@ -1246,16 +1282,16 @@ static cudaError_t emb_bwd_vec(float* dwte, float* dwpe, const void* dx, const i
     int BT = B * T_;
     EmbScratch e = emb_carve(scratch, BT, C, Vp, nullptr);
     cudaMemsetAsync(e.blkcnt, 0, (size_t)e.nb * Vp * 4, s);
-    k_emb_rank<<<e.nb, EMB_BLK, 0, s>>>(tok, BT, Vp, e.lrank, e.blkcnt);
-    k_emb_blockprefix<<<cdiv(Vp, 256), 256, 0, s>>>(e.blkcnt, e.cnt, e.nb, Vp);
-    k_emb_scan<<<1, 1024, 0, s>>>(e.cnt, e.start, e.itemoff, e.poff, Vp);
-    k_emb_place<<<cdiv(BT, 256), 256, 0, s>>>(tok, BT, Vp, e.start, e.blkcnt, e.lrank, e.sorted);
-    k_emb_items<<<cdiv(Vp, 256), 256, 0, s>>>(e.cnt, e.itemoff, e.items, Vp);
+    launch_pdl(k_emb_rank, e.nb, EMB_BLK, 0, s, tok, BT, Vp, e.lrank, e.blkcnt);
+    launch_pdl(k_emb_blockprefix, cdiv(Vp, 256), 256, 0, s, e.blkcnt, e.cnt, e.nb, Vp);
+    launch_pdl(k_emb_scan, 1, 1024, 0, s, e.cnt, e.start, e.itemoff, e.poff, Vp);
+    launch_pdl(k_emb_place, cdiv(BT, 256), 256, 0, s, tok, BT, Vp, e.start, e.blkcnt, e.lrank, e.sorted);
+    launch_pdl(k_emb_items, cdiv(Vp, 256), 256, 0, s, e.cnt, e.itemoff, e.items, Vp);
     int it = cdiv(C, 32 * VEC);
     const int* n_items = e.itemoff + Vp;
     dim3 g(cdiv(e.max_items, 8));
 #define EMR(I)                                                                                   \
-    k_emb_reduce2<T, VEC, I><<<g, 256, 0, s>>>(dwte, e.part, (const T*)dx, e.sorted, e.cnt,      \
+    launch_pdl(k_emb_reduce2<T, VEC, I>, g, 256, 0, s, dwte, e.part, (const T*)dx, e.sorted, e.cnt,      \
                                                e.start, n_items, e.poff, e.items, C)
     if (it <= 1) EMR(1);
     else if (it <= 2) EMR(2);
@@ -1264,8 +1300,8 @@ static cudaError_t emb_bwd_vec(float* dwte, float* dwpe, const void* dx, const i
     else if (it <= 16) EMR(16);
     else return cudaErrorInvalidValue;
 #undef EMR
-    k_emb_fold<<<e.max_items, 256, 0, s>>>(dwte, e.part, e.cnt, e.poff, n_items, e.items, C);
-    k_wpe_bwd<T, VEC><<<cdiv((long)T_ * (C / VEC), 256), 256, 0, s>>>(dwpe, (const T*)dx, B, T_,
+    launch_pdl(k_emb_fold, e.max_items, 256, 0, s, dwte, e.part, e.cnt, e.poff, n_items, e.items, C);
+    launch_pdl(k_wpe_bwd<T, VEC>, cdiv((long)T_ * (C / VEC), 256), 256, 0, s, dwpe, (const T*)dx, B, T_,
                                                                        C);
     return cudaGetLastError();
 }
@@ -1294,6 +1330,8 @@ cudaError_t encoder_backward(int act, float* dwte, float* dwpe, const void* dx, 
 #define ADAM_NB 1184
 
 __global__ void __launch_bounds__(256) k_sumsq(const float* g, size_t n, double* part) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ double sh[8];
     size_t chunk = ((n + ADAM_NB - 1) / ADAM_NB + 3) & ~(size_t)3;
     size_t lo = (size_t)blockIdx.x * chunk, hi = lo + chunk < n ? lo + chunk : n;
@@ -1318,6 +1356,8 @@ __global__ void __launch_bounds__(256) k_sumsq(const float* g, size_t n, double*
 }
 
 __global__ void k_adam_norm(const double* part, float* state, float inv_accum, float clip) {
+    gdc_wait();
+    gdc_launch_dependents();
     __shared__ double sh[32];
     double a = 0.0;
     for (int i = threadIdx.x; i < ADAM_NB; i += blockDim.x) a += part[i];
@@ -1357,6 +1397,8 @@ __device__ __forceinline__ float adam_one(float& w, float& m, float& v, float g,
 __global__ void __launch_bounds__(256) k_adam(float* w, float* m, float* v, const float* g,
                                               bf16* wb, size_t n, AdamArgs a,
                                               const float* state) {
+    gdc_wait();
+    gdc_launch_dependents();
     if (state[2] == 0.f) return;
     float sc = state[1];
     size_t nv = n / 4;
@@ -1399,9 +1441,9 @@ size_t adamw_scratch() { return ADAM_NB * sizeof(double); }
 cudaError_t adamw_step(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
                        const AdamArgs& a, float* state, void* scratch, cudaStream_t s) {
     double* part = (double*)scratch;
-    k_sumsq<<<ADAM_NB, 256, 0, s>>>(g, n, part);
-    k_adam_norm<<<1, 1024, 0, s>>>(part, state, a.inv_accum, a.clip);
-    k_adam<<<148 * 8, 256, 0, s>>>(w, m, v, g, (bf16*)wbf16, n, a, state);
+    launch_pdl(k_sumsq, ADAM_NB, 256, 0, s, g, n, part);
+    launch_pdl(k_adam_norm, 1, 1024, 0, s, part, state, a.inv_accum, a.clip);
+    launch_pdl(k_adam, 148 * 8, 256, 0, s, w, m, v, g, (bf16*)wbf16, n, a, state);
     return cudaGetLastError();
 }
 

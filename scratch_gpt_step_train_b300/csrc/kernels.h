@@ -5,6 +5,7 @@
 // or ACT_BF16 (bf16).  Gradients of parameters are always fp32.
 #pragma once
 #include <cuda_runtime.h>
+#include <utility>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -14,6 +15,25 @@
 #define GPT2_DEVERR_SHAPE 4u    // a kernel was launched with a shape it cannot do
 
 namespace gk {
+
+// Launches kernel k with programmatic stream serialization allowed: it may
+// begin while the previous kernel in the stream drains; every kernel of the
+// library calls gdc_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
 
 enum { ACT_F32 = 0, ACT_BF16 = 1 };
 inline size_t act_size(int act) { return act == ACT_BF16 ? 2 : 4; }
