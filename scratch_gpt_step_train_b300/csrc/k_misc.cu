@@ -361,12 +361,14 @@ __global__ void __launch_bounds__(LnbCfg<VEC, IT, NACC>::W * 32, 2)
     }
 }
 
-// Rows of up to 768 bf16 columns (1024 without the dx sums): the same computation with the column sums
-// in registers (IT*8 columns per lane) and the row data staged through shared
-// memory by cp.async.  Each lane copies exactly the 16-byte vectors it later
-// reads, into a two-slot ring of its warp, so the copy of the warp's next row
-// is in flight while it works on the current one, and a lane only ever waits
-// for its own copies (cp.async.wait_group).  Registers hold no row data.
+// bf16 rows with C % 8 == 0: the same computation with the column sums in
+// registers and the row data staged through shared memory by cp.async.  A row
+// is handled by a team of RS warps, each owning a contiguous part of its
+// 16-byte column vectors (IT per lane); the team adds its parts' row sums in
+// part order through shared memory.  Each lane copies exactly the vectors it
+// later reads, into a two-slot ring of its warp, so the copy of the team's next
+// row is in flight while it works on the current one, and a lane only ever
+// waits for its own copies (cp.async.wait_group).  Registers hold no row data.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -385,51 +387,73 @@ __device__ __forceinline__ void bf16x8_to_f(const uint4& u, float* f) {
         f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
     }
 }
+// element h (0 = low half) of a packed bf16 pair, widened to fp32
+__device__ __forceinline__ float bf_half(uint32_t u, int h) {
+    return __uint_as_float(h ? (u & 0xffff0000u) : (u << 16));
+}
+__device__ __forceinline__ uint32_t pack2_bf16_rn(float lo, float hi) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
-template <int IT, int NACC>
+template <int IT, int NACC, int RS>
 __global__ void __launch_bounds__(256, 2)
     k_ln_bwd_ring(bf16* dx, float* part, const bf16* dout, const bf16* x, const bf16* w,
                   const float* mean, const float* rstd, int N, int C, int accum_dx) {
     gdc_wait();
     gdc_launch_dependents();
-    // ring: [warp][slot 0/1][x | dy | dx][IT*256 bf16]; reused for the fold
+    // ring: [warp][slot 0/1][x | dy | dx][IT*32 vectors]; reused for the fold
     extern __shared__ __align__(16) unsigned char rsm[];
-    constexpr int ROWV = IT * 32;              // 16-byte vectors per row array (max)
-    constexpr int SLOT = 3 * ROWV * 16;        // bytes per slot
+    __shared__ float xch[2][8][2];          // [row parity][warp] partial (sum g, sum g*xhat)
+    constexpr int ROWV = IT * 32;           // vectors per row part and array (max)
+    constexpr int SLOT = 3 * ROWV * 16;     // bytes per slot
+    constexpr bool WREG = IT * (NACC + 1) <= 9;  // w of the lane's columns kept in registers
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x / 32;
+    const int teams = nwarps / RS, team = warp / RS, pix = warp % RS;
+    const int nvec = C / 8, vpp = (nvec + RS - 1) / RS;
+    const int v0 = pix * vpp;
+    const int lim = min(nvec, v0 + vpp) - v0;  // vectors of this part: it*32 + lane < lim
     const uint32_t ring = tc::smem_u32(rsm) + (uint32_t)warp * 2 * SLOT;
-    float wr[IT][8];
+    float wr[WREG ? IT : 1][8];
     float acc[NACC][IT][8];
+    const bf16* wl = w + (v0 + lane) * 8;  // this lane's first vector of w
 #pragma unroll
     for (int it = 0; it < IT; it++) {
-        const int c = (it * 32 + lane) * 8;
-        if (c < C) bf16x8_to_f(*reinterpret_cast<const uint4*>(w + c), wr[it]);
+        const bool ok = it * 32 + lane < lim;
+        if (WREG && ok) bf16x8_to_f(*reinterpret_cast<const uint4*>(wl + it * 256), wr[it]);
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-            if (c >= C) wr[it][j] = 0.f;
+            if (WREG && !ok) wr[it][j] = 0.f;
 #pragma unroll
             for (int a = 0; a < NACC; a++) acc[a][it][j] = 0.f;
         }
     }
-    const int stride = gridDim.x * nwarps;
+    auto wpacked = [&](int it) -> uint4 {  // w of vector it, when not held in registers
+        if constexpr (WREG) return make_uint4(0u, 0u, 0u, 0u);
+        else return *reinterpret_cast<const uint4*>(wl + it * 256);
+    };
+    const int stride = gridDim.x * teams;
     auto issue = [&](int row, int slot) {
         if (row < N) {
-            const uint32_t base = ring + slot * SLOT;
+            const uint32_t base = ring + slot * SLOT + lane * 16;
+            const size_t g = (size_t)row * C + (v0 + lane) * 8;
 #pragma unroll
             for (int it = 0; it < IT; it++) {
-                const int c = (it * 32 + lane) * 8;
-                if (c < C) {
-                    const uint32_t o = (uint32_t)(it * 32 + lane) * 16;
-                    cp_async16(base + o, x + (size_t)row * C + c);
-                    cp_async16(base + ROWV * 16 + o, dout + (size_t)row * C + c);
-                    if (accum_dx) cp_async16(base + 2 * ROWV * 16 + o, dx + (size_t)row * C + c);
+                if (it * 32 + lane < lim) {
+                    const uint32_t o = it * 512;
+                    cp_async16(base + o, x + g + it * 256);
+                    cp_async16(base + ROWV * 16 + o, dout + g + it * 256);
+                    if (accum_dx) cp_async16(base + 2 * ROWV * 16 + o, dx + g + it * 256);
                 }
             }
         }
         cp_async_commit();  // an empty group past the last row keeps the count uniform
     };
-    int row = blockIdx.x * nwarps + warp;
+    int row = blockIdx.x * teams + team;
     issue(row, 0);
     for (int k = 0; row < N; row += stride, k++) {
         issue(row + stride, (k + 1) & 1);
@@ -437,57 +461,88 @@ __global__ void __launch_bounds__(256, 2)
         const unsigned char* sl = rsm + (size_t)warp * 2 * SLOT + (size_t)(k & 1) * SLOT;
         const float m = mean[row], r = rstd[row], mr = -m * r;
         float sg = 0.f, sgx = 0.f;
+        // packed bf16 pairs are widened one 32-bit word at a time
 #pragma unroll
         for (int it = 0; it < IT; it++) {
-            const int c = (it * 32 + lane) * 8;
-            if (c < C) {
-                float xf[8], df[8];
-                bf16x8_to_f(*reinterpret_cast<const uint4*>(sl + (it * 32 + lane) * 16), xf);
-                bf16x8_to_f(*reinterpret_cast<const uint4*>(sl + ROWV * 16 + (it * 32 + lane) * 16),
-                            df);
+            if (it * 32 + lane < lim) {
+                const uint4 ux = *reinterpret_cast<const uint4*>(sl + (it * 32 + lane) * 16);
+                const uint4 ud =
+                    *reinterpret_cast<const uint4*>(sl + ROWV * 16 + (it * 32 + lane) * 16);
+                const uint4 uw = wpacked(it);
+                const uint32_t xw[4] = {ux.x, ux.y, ux.z, ux.w}, dw4[4] = {ud.x, ud.y, ud.z, ud.w};
+                const uint32_t ww[4] = {uw.x, uw.y, uw.z, uw.w};
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
-                    const float xh = fmaf(xf[j], r, mr);
-                    const float g = df[j] * wr[it][j];
+                    const float xv = bf_half(xw[j >> 1], j & 1), dv = bf_half(dw4[j >> 1], j & 1);
+                    const float xh = fmaf(xv, r, mr);
+                    const float g = dv * (WREG ? wr[WREG ? it : 0][j] : bf_half(ww[j >> 1], j & 1));
                     sg += g;
                     sgx = fmaf(g, xh, sgx);
-                    acc[0][it][j] = fmaf(df[j], xh, acc[0][it][j]);
-                    acc[1][it][j] += df[j];
+                    acc[0][it][j] = fmaf(dv, xh, acc[0][it][j]);
+                    acc[1][it][j] += dv;
                 }
             }
         }
-        sg = warp_sum(sg) / C;
-        sgx = warp_sum(sgx) / C;
-        bf16* dxr = dx + (size_t)row * C;
+        sg = warp_sum(sg);
+        sgx = warp_sum(sgx);
+        if (RS > 1) {
+            // the row's sums: the team's parts added in part order
+            if (lane == 0) {
+                xch[k & 1][warp][0] = sg;
+                xch[k & 1][warp][1] = sgx;
+            }
+            named_bar_sync(1 + team, RS * 32);
+            sg = sgx = 0.f;
+#pragma unroll
+            for (int q = 0; q < RS; q++) {
+                sg += xch[k & 1][team * RS + q][0];
+                sgx += xch[k & 1][team * RS + q][1];
+            }
+        }
+        sg /= C;
+        sgx /= C;
+        bf16* dxr = dx + (size_t)row * C + (v0 + lane) * 8;
 #pragma unroll
         for (int it = 0; it < IT; it++) {
-            const int c = (it * 32 + lane) * 8;
-            if (c < C) {
-                float xf[8], df[8], of[8];
-                bf16x8_to_f(*reinterpret_cast<const uint4*>(sl + (it * 32 + lane) * 16), xf);
-                bf16x8_to_f(*reinterpret_cast<const uint4*>(sl + ROWV * 16 + (it * 32 + lane) * 16),
-                            df);
+            if (it * 32 + lane < lim) {
+                const uint4 ux = *reinterpret_cast<const uint4*>(sl + (it * 32 + lane) * 16);
+                const uint4 ud =
+                    *reinterpret_cast<const uint4*>(sl + ROWV * 16 + (it * 32 + lane) * 16);
+                uint4 uo = make_uint4(0u, 0u, 0u, 0u);
                 if (accum_dx)
-                    bf16x8_to_f(
-                        *reinterpret_cast<const uint4*>(sl + 2 * ROWV * 16 + (it * 32 + lane) * 16),
-                        of);
-                Vec<bf16, 8> o;
+                    uo = *reinterpret_cast<const uint4*>(sl + 2 * ROWV * 16 + (it * 32 + lane) * 16);
+                const uint4 uw = wpacked(it);
+                const uint32_t xw[4] = {ux.x, ux.y, ux.z, ux.w}, dw4[4] = {ud.x, ud.y, ud.z, ud.w};
+                const uint32_t ow[4] = {uo.x, uo.y, uo.z, uo.w}, ww[4] = {uw.x, uw.y, uw.z, uw.w};
+                uint32_t res[4];
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const float xh = fmaf(xf[j], r, mr);
-                    const float g = df[j] * wr[it][j];
-                    float d = r * fmaf(-xh, sgx, g - sg);
-                    if (accum_dx) d += of[j];
-                    o.v[j] = from_f<bf16>(d);
-                    if (NACC == 3) acc[NACC - 1][it][j] += to_f(o.v[j]);
+                for (int q = 0; q < 4; q++) {
+                    float d2[2];
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int j = 2 * q + h;
+                        const float xh = fmaf(bf_half(xw[q], h), r, mr);
+                        const float g = bf_half(dw4[q], h) *
+                                        (WREG ? wr[WREG ? it : 0][j] : bf_half(ww[q], h));
+                        // bf_half of a zero word is 0 when there is no incoming dx
+                        d2[h] = fmaf(r, fmaf(-xh, sgx, g - sg), bf_half(ow[q], h));
+                    }
+                    res[q] = pack2_bf16_rn(d2[0], d2[1]);
+                    if (NACC == 3) {
+                        // the column sum is of the value as stored
+                        acc[NACC - 1][it][2 * q] += bf_half(res[q], 0);
+                        acc[NACC - 1][it][2 * q + 1] += bf_half(res[q], 1);
+                    }
                 }
-                *reinterpret_cast<Vec<bf16, 8>*>(dxr + c) = o;
+                *reinterpret_cast<uint4*>(dxr + it * 256) = make_uint4(res[0], res[1], res[2], res[3]);
             }
         }
     }
     cp_async_wait<0>();  // nothing may still be landing in the ring
     __syncthreads();
-    // fold: slot (a, it, j, lane) of warp w at ((w*NACC + a)*IT*8 + it*8 + j)*32 + lane
+    // fold: slot (a, it, j, lane) of warp w at ((w*NACC + a)*IT*8 + it*8 + j)*32 + lane;
+    // column vector v0(part) + it*32 + lane is owned by one warp of every team
+    constexpr int S = IT * 8 * 32;
     float* fs = reinterpret_cast<float*>(rsm);
 #pragma unroll
     for (int a = 0; a < NACC; a++)
@@ -495,17 +550,18 @@ __global__ void __launch_bounds__(256, 2)
         for (int it = 0; it < IT; it++)
 #pragma unroll
             for (int j = 0; j < 8; j++)
-                fs[(((size_t)warp * NACC + a) * IT * 8 + it * 8 + j) * 32 + lane] = acc[a][it][j];
+                fs[((size_t)warp * NACC + a) * S + (it * 8 + j) * 32 + lane] = acc[a][it][j];
     __syncthreads();
-    constexpr int S = IT * 8 * 32;
-    for (int q = threadIdx.x; q < NACC * S; q += blockDim.x) {
-        const int a = q / S, rem = q - a * S;
-        const int ln = rem & 31, jj = (rem >> 5) & 7, itq = rem >> 8;
-        const int c = (itq * 32 + ln) * 8 + jj;
-        if (c < C) {
+    for (int q = threadIdx.x; q < NACC * RS * S; q += blockDim.x) {
+        const int a = q / (RS * S), rem = q - a * (RS * S);
+        const int pq = rem / S, sq = rem - pq * S;
+        const int ln = sq & 31, jj = (sq >> 5) & 7, itq = sq >> 8;
+        const int vi = pq * vpp + itq * 32 + ln;
+        if (itq * 32 + ln < vpp && vi < nvec) {
             float t = 0.f;
-            for (int wi = 0; wi < nwarps; wi++) t += fs[((size_t)wi * NACC + a) * S + rem];
-            part[((size_t)blockIdx.x * NACC + a) * C + c] = t;
+            for (int tt = 0; tt < teams; tt++)
+                t += fs[((size_t)(tt * RS + pq) * NACC + a) * S + sq];
+            part[((size_t)blockIdx.x * NACC + a) * C + vi * 8 + jj] = t;
         }
     }
 }
@@ -541,25 +597,46 @@ size_t layernorm_backward_scratch(int N, int C, bool dxsum) {
     return (size_t)LNB_MAX_BLOCKS * (dxsum ? 3 : 2) * C * sizeof(float);
 }
 
+template <int IT, int NACC, int RS>
+static cudaError_t ln_bwd_ring_launch(bf16* dx, float* part, const bf16* dout, const bf16* x,
+                                      const bf16* w, const float* mean, const float* rstd, int N,
+                                      int C, int accum, int* nb_out, cudaStream_t s) {
+    constexpr size_t smem = (size_t)8 * 2 * 3 * IT * 32 * 16;
+    static_assert(smem >= (size_t)8 * NACC * IT * 256 * 4, "fold does not fit the ring");
+    auto kern = k_ln_bwd_ring<IT, NACC, RS>;
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    int nb = cdiv(N, (8 / RS) * 4);
+    if (nb > LNB_MAX_BLOCKS) nb = LNB_MAX_BLOCKS;
+    *nb_out = nb;
+    launch_pdl(kern, nb, 256, smem, s, dx, part, dout, x, w, mean, rstd, N, C, accum);
+    return cudaGetLastError();
+}
+
 template <typename T, int VEC, int IT, int NACC>
 static cudaError_t ln_bwd_launch(T* dx, float* part, const T* dout, const T* x, const T* w,
                                  const float* mean, const float* rstd, int N, int C, int accum,
                                  int* nb_out, cudaStream_t s) {
-    if constexpr (std::is_same<T, bf16>::value && VEC == 8 && IT * NACC <= 9) {
-        // register column sums, cp.async-staged rows
-        constexpr size_t smem = (size_t)8 * 2 * 3 * IT * 32 * 16;
-        static_assert(smem >= (size_t)8 * NACC * IT * 256 * 4, "fold does not fit the ring");
-        auto kern = k_ln_bwd_ring<IT, NACC>;
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return e;
+    if constexpr (std::is_same<T, bf16>::value && VEC == 8) {
+        // register column sums, cp.async-staged rows: one warp per row while a
+        // lane's column sums fit in registers, else two warps per row
+        const int nvec = C / 8;
+        if constexpr (IT * NACC <= 9)
+            return ln_bwd_ring_launch<IT, NACC, 1>(dx, part, dout, x, w, mean, rstd, N, C, accum,
+                                                   nb_out, s);
+        const int it2 = cdiv(cdiv(nvec, 2), 32);
+        switch (it2) {
+            case 2: return ln_bwd_ring_launch<2, NACC, 2>(dx, part, dout, x, w, mean, rstd, N, C,
+                                                         accum, nb_out, s);
+            case 3: return ln_bwd_ring_launch<3, NACC, 2>(dx, part, dout, x, w, mean, rstd, N, C,
+                                                         accum, nb_out, s);
+            case 4: return ln_bwd_ring_launch<4, NACC, 2>(dx, part, dout, x, w, mean, rstd, N, C,
+                                                         accum, nb_out, s);
+            default: break;  // wider rows: shared-memory column sums below
         }
-        int nb = cdiv(N, 8 * 4);
-        if (nb > LNB_MAX_BLOCKS) nb = LNB_MAX_BLOCKS;
-        *nb_out = nb;
-        launch_pdl(kern, nb, 256, smem, s, dx, part, dout, x, w, mean, rstd, N, C, accum);
-        return cudaGetLastError();
     }
     constexpr int S = LnbCfg<VEC, IT, NACC>::S, W = LnbCfg<VEC, IT, NACC>::W;
     constexpr size_t smem = (size_t)W * NACC * S * sizeof(float);
