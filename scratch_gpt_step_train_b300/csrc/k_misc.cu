@@ -17,6 +17,7 @@
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
+#include <algorithm>
 #include <math.h>
 #include <type_traits>
 
@@ -150,78 +151,112 @@ cudaError_t encoder_forward(int act, void* out, const int* tok, const void* wte,
 }
 
 // ===========================================================================
-// LayerNorm forward: one warp per row, row cached in registers, VEC-wide loads.
-// mean, rstd = 1/sqrt(var + 1e-5) with the biased variance.
+// LayerNorm forward: one warp per row, mean, rstd = 1/sqrt(var + 1e-5) with
+// the biased variance.  Persistent warps walk the rows with a stride; the next
+// row's data (packed, VEC-wide loads) is in flight while the current row is
+// normalised.
 // ===========================================================================
 template <typename T, int VEC, int IT>
 __global__ void __launch_bounds__(256) k_ln_fwd(T* out, float* mean, float* rstd, const T* x,
                                                 const T* w, const T* b, int N, int C) {
     gdc_wait();
     gdc_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int nw = gridDim.x * (blockDim.x / 32);
     int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    int lane = threadIdx.x & 31;
-    if (row >= N) return;
-    const T* xr = x + (size_t)row * C;
-    float v[IT][VEC];
-    float s = 0.f;
+    Vec<T, VEC> cur[IT], nxt[IT];
+    auto load = [&](int r, Vec<T, VEC>* v) {
+        if (r < N) {
 #pragma unroll
-    for (int it = 0; it < IT; it++) {
-        int c = (it * 32 + lane) * VEC;
-        if (c < C) {
-            load_vec_f<T, VEC>(v[it], xr + c);
-#pragma unroll
-            for (int j = 0; j < VEC; j++) s += v[it][j];
-        }
-    }
-    float m = warp_sum(s) / C;
-    float ss = 0.f;
-#pragma unroll
-    for (int it = 0; it < IT; it++) {
-        int c = (it * 32 + lane) * VEC;
-        if (c < C) {
-#pragma unroll
-            for (int j = 0; j < VEC; j++) {
-                float d = v[it][j] - m;
-                ss += d * d;
+            for (int it = 0; it < IT; it++) {
+                const int c = (it * 32 + lane) * VEC;
+                if (c < C) v[it] = *reinterpret_cast<const Vec<T, VEC>*>(x + (size_t)r * C + c);
             }
         }
-    }
-    float r = rsqrtf(warp_sum(ss) / C + 1e-5f);
-    T* yr = out + (size_t)row * C;
+    };
+    load(row, cur);
+    for (; row < N; row += nw) {
+        load(row + nw, nxt);
+        float s = 0.f;
 #pragma unroll
-    for (int it = 0; it < IT; it++) {
-        int c = (it * 32 + lane) * VEC;
-        if (c < C) {
-            float wv[VEC], bv[VEC], y[VEC];
-            load_vec_f<T, VEC>(wv, w + c);
-            load_vec_f<T, VEC>(bv, b + c);
+        for (int it = 0; it < IT; it++) {
+            if ((it * 32 + lane) * VEC < C) {
 #pragma unroll
-            for (int j = 0; j < VEC; j++) y[j] = (v[it][j] - m) * r * wv[j] + bv[j];
-            store_vec_f<T, VEC>(yr + c, y);
+                for (int j = 0; j < VEC; j++) s += to_f(cur[it].v[j]);
+            }
         }
+        const float m = warp_sum(s) / C;
+        float ss = 0.f;
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            if ((it * 32 + lane) * VEC < C) {
+#pragma unroll
+                for (int j = 0; j < VEC; j++) {
+                    const float d = to_f(cur[it].v[j]) - m;
+                    ss += d * d;
+                }
+            }
+        }
+        const float r = rsqrtf(warp_sum(ss) / C + 1e-5f);
+        T* yr = out + (size_t)row * C;
+#pragma unroll
+        for (int it = 0; it < IT; it++) {
+            const int c = (it * 32 + lane) * VEC;
+            if (c < C) {
+                float wv[VEC], bv[VEC], y[VEC];
+                load_vec_f<T, VEC>(wv, w + c);
+                load_vec_f<T, VEC>(bv, b + c);
+#pragma unroll
+                for (int j = 0; j < VEC; j++) y[j] = (to_f(cur[it].v[j]) - m) * r * wv[j] + bv[j];
+                store_vec_f<T, VEC>(yr + c, y);
+            }
+        }
+        if (lane == 0) {
+            mean[row] = m;
+            rstd[row] = r;
+        }
+#pragma unroll
+        for (int it = 0; it < IT; it++) cur[it] = nxt[it];
     }
-    if (lane == 0) {
-        mean[row] = m;
-        rstd[row] = r;
-    }
+}
+
+template <typename T, int VEC, int IT>
+static cudaError_t ln_fwd_launch(void* out, float* mean, float* rstd, const void* x,
+                                 const void* w, const void* b, int N, int C, cudaStream_t s) {
+    auto kern = k_ln_fwd<T, VEC, IT>;
+    static int occ = 0;  // resident blocks per SM (same on every device of this build)
+    if (!occ && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 256, 0) != cudaSuccess ||
+                 occ < 1))
+        occ = 1;
+    int dev = 0, nsm = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int nb = std::min(cdiv(N, 8), nsm * occ);
+    launch_pdl(kern, nb, 256, 0, s, (T*)out, mean, rstd, (const T*)x, (const T*)w, (const T*)b, N,
+               C);
+    return cudaGetLastError();
 }
 
 template <typename T, int VEC>
 static cudaError_t ln_fwd_vec(void* out, float* mean, float* rstd, const void* x, const void* w,
                               const void* b, int N, int C, cudaStream_t s) {
-    int it = cdiv(C, 32 * VEC);
-    dim3 grid(cdiv(N, 8)), blk(256);
-#define LNF(I)                                                                                   \
-    launch_pdl(k_ln_fwd<T, VEC, I>, grid, blk, 0, s, (T*)out, mean, rstd, (const T*)x, (const T*)w,     \
-                                            (const T*)b, N, C)
-    if (it <= 1) LNF(1);
-    else if (it <= 2) LNF(2);
-    else if (it <= 4) LNF(4);
-    else if (it <= 8) LNF(8);
-    else if (it <= 16) LNF(16);
-    else return cudaErrorInvalidValue;
+    const int it = cdiv(C, 32 * VEC);
+#define LNF(I) return ln_fwd_launch<T, VEC, I>(out, mean, rstd, x, w, b, N, C, s)
+    switch (it) {
+        case 1: LNF(1);
+        case 2: LNF(2);
+        case 3: LNF(3);
+        case 4: LNF(4);
+        case 5: LNF(5);
+        case 6: LNF(6);
+        case 7: LNF(7);
+        case 8: LNF(8);
+        default:
+            if (it <= 12) LNF(12);
+            if (it <= 16) LNF(16);
+            return cudaErrorInvalidValue;
+    }
 #undef LNF
-    return cudaGetLastError();
 }
 template <typename T>
 static cudaError_t ln_fwd_t(void* out, float* mean, float* rstd, const void* x, const void* w,
@@ -774,8 +809,16 @@ static cudaError_t bias_grad_t(float* db, const void* dout, int N, int OC, void*
     const int nch = cdiv(N, BG_ROWS);
     const int vec = OC % VM == 0 ? VM : 1;
     const int gx = cdiv(OC / vec, 32);
-    int P = cdiv(148 * 4, gx);
-    if (P > nch) P = nch;
+    // P partial rows: as many as keep the whole grid resident (8 blocks of 256
+    // threads per SM), preferring a P that divides the chunk count so that
+    // every block sums the same number of chunks
+    const int pmax = std::max(1, std::min(nch, 148 * 8 / gx));
+    int P = pmax;
+    for (int q = pmax; q >= 1; q--)
+        if (nch % q == 0) {
+            if (2 * q >= pmax) P = q;
+            break;
+        }
     float* part = (float*)scratch;
     dim3 grid(gx, P);
     if (vec == VM) launch_pdl(k_bias_part<T, VM>, grid, 256, 0, s, part, (const T*)dout, N, OC, nch);
