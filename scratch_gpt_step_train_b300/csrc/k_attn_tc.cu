@@ -102,9 +102,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
     float* red = (float*)(base_gen + F_RED);  // [2 buffers][2 halves][128 rows]
     float* lsum = (float*)(base_gen + F_LS);  // [2 halves][128 rows]
     const uint32_t bar = base + F_BAR;
-    // full[3], empty[3] for the ring; q; s (S ready); pf (P ready); o (P.V done)
+    // full[3], empty[3] for the ring; q; s (S ready); pf (P ready); o (P.V done);
+    // sfree (S copied to registers: the next S may overwrite it)
     const uint32_t b_full = bar, b_empty = bar + 24, b_q = bar + 48, b_sfull = bar + 56,
-                   b_pfull = bar + 64, b_ofull = bar + 72;
+                   b_pfull = bar + 64, b_ofull = bar + 72, b_sfree = bar + 80;
     uint32_t* tmem_slot = (uint32_t*)(base_gen + F_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + F_BAR + 132);
 
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
         mbar_init(b_sfull, 1);
         mbar_init(b_pfull, 8);
         mbar_init(b_ofull, 1);
+        mbar_init(b_sfree, 8);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map) : "memory");
@@ -192,9 +194,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
             };
             bool ok = mbar_wait(b_q, 0, abort_flag, p.err) && issue_s(0);
             for (int j = 0; ok && j < nkt; j++) {
+                // S_{j+1} as soon as the softmax warps hold S_j in registers,
+                // so that it overlaps their work on tile j
+                if (j + 1 < nkt) {
+                    if (!mbar_wait_spin(b_sfree, j & 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+                    if (!issue_s(j + 1)) break;
+                }
                 if (!mbar_wait_spin(b_pfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                if (j + 1 < nkt && !issue_s(j + 1)) break;
                 const int it = 2 * j + 1, s = it % 3;
                 if (!mbar_wait_spin(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) break;
                 tc_fence_after();
@@ -233,6 +241,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
             tmem_ld32_async(tS + loff + kb + 32, sv[1]);
             tmem_wait32(sv[0]);
             tmem_wait32(sv[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_sfree);
             if (j == qt) {  // causal mask of the diagonal tile: keys > row
 #pragma unroll
                 for (int c = 0; c < 2; c++)
