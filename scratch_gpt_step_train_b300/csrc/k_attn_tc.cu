@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     const uint32_t bar = base + D_BAR;
     const uint32_t b_kv = bar, b_qdf0 = bar + 8, b_qdf1 = bar + 16, b_qde0 = bar + 24,
                    b_qde1 = bar + 32, b_sfull = bar + 40, b_psfull = bar + 48,
-                   b_psfree = bar + 56, b_acc = bar + 64;
+                   b_psfree = bar + 56, b_acc = bar + 64, b_sfree = bar + 72;
     uint32_t* tmem_slot = (uint32_t*)(base_gen + D_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + D_BAR + 132);
 
@@ -418,6 +418,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
         mbar_init(b_psfull, 8);
         mbar_init(b_psfree, 1);
         mbar_init(b_acc, 1);
+        mbar_init(b_sfree, 8);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -468,15 +469,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
             const uint64_t dK = sdesc(sK, 0, 1024), dV = sdesc(sV, 0, 1024);
             const uint64_t dPT = sdesc(sPT, 0, 1024), dDST = sdesc(sDST, 0, 1024);
-            bool ok = mbar_wait(b_kv, 0, abort_flag, p.err);
-            for (int n = 0; ok && n < nq; n++) {
+            // S^T = K Q_n^T and dP^T = V dO_n^T (128 keys x 64 queries)
+            auto issue_s = [&](int n) -> bool {
                 const int s = n & 1, u = n >> 1;
-                if (!mbar_wait_spin(s ? b_qdf1 : b_qdf0, u & 1, abort_flag, p.err)) break;
+                if (!mbar_wait_spin(s ? b_qdf1 : b_qdf0, u & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
                 const uint32_t sq = base + (s ? D_Q1 : D_Q0), sd = base + (s ? D_DO1 : D_DO0);
                 const uint64_t dq_k = sdesc(sq, 0, 1024), dd_k = sdesc(sd, 0, 1024);
-                const uint64_t dq_m = sdesc(sq, 8192, 1024), dd_m = sdesc(sd, 8192, 1024);
-                // S^T = K Q^T and dP^T = V dO^T (128 keys x 64 queries)
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
                     umma_bf16(tST, dK + (uint64_t)(2 * k), dq_k + (uint64_t)(2 * k), ID_S, k > 0);
@@ -484,6 +483,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 for (int k = 0; k < HD / 16; k++)
                     umma_bf16(tDPT, dV + (uint64_t)(2 * k), dd_k + (uint64_t)(2 * k), ID_S, k > 0);
                 umma_commit(b_sfull);
+                return true;
+            };
+            bool ok = mbar_wait(b_kv, 0, abort_flag, p.err) && issue_s(0);
+            for (int n = 0; ok && n < nq; n++) {
+                const int s = n & 1;
+                const uint32_t sq = base + (s ? D_Q1 : D_Q0), sd = base + (s ? D_DO1 : D_DO0);
+                const uint64_t dq_m = sdesc(sq, 8192, 1024), dd_m = sdesc(sd, 8192, 1024);
+                // the next step's products as soon as the softmax warps hold
+                // this step's S^T and dP^T in registers
+                if (n + 1 < nq) {
+                    if (!mbar_wait_spin(b_sfree, n & 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+                    if (!issue_s(n + 1)) break;
+                }
                 if (!mbar_wait_spin(b_psfull, n & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 // dV += P^T dO, dK += dS^T Q (K = the 64 queries)
@@ -522,16 +535,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 ok = false;
                 break;
             }
-            if (n > 0 && !warp_wait(b_psfree, (n - 1) & 1, abort_flag, p.err, lane)) {
-                ok = false;
-                break;
-            }
             tc_fence_after();
             uint32_t sv[32], dp[32];
             tmem_ld32_async(tST + loff + c0, sv);
             tmem_ld32_async(tDPT + loff + c0, dp);
             tmem_wait32(sv);
             tmem_wait32(dp);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_sfree);  // the next S^T, dP^T may land
             // the whole step lies after this key tile and inside the sequence
             const bool full = qbase >= kt * TILE + TILE && qbase + SUB <= p.T;
             uint32_t pp[16], dd[16];
@@ -564,6 +576,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                     pp[e] = pack_bf16x2(pv[0], pv[1]);
                     dd[e] = pack_bf16x2(dv[0], dv[1]);
                 }
+            }
+            // the previous step's products must be done reading the P^T, dS^T tiles
+            if (n > 0 && !warp_wait(b_psfree, (n - 1) & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
             }
             st_row32_64(sPT, r, c0, pp);
             st_row32_64(sDST, r, c0, dd);
@@ -622,7 +639,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     const uint32_t bar = base + E_BAR;
     const uint32_t b_q = bar, b_kvf0 = bar + 8, b_kvf1 = bar + 16, b_kve0 = bar + 24,
                    b_kve1 = bar + 32, b_sfull = bar + 40, b_dsfull = bar + 48,
-                   b_dsfree = bar + 56, b_acc = bar + 64;
+                   b_dsfree = bar + 56, b_acc = bar + 64, b_sfree = bar + 72;
     uint32_t* tmem_slot = (uint32_t*)(base_gen + E_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + E_BAR + 132);
 
@@ -642,6 +659,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
         mbar_init(b_dsfull, 8);
         mbar_init(b_dsfree, 1);
         mbar_init(b_acc, 1);
+        mbar_init(b_sfree, 8);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -691,15 +709,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
             const uint64_t dQ = sdesc(sQ, 0, 1024), dDO = sdesc(sDO, 0, 1024);
             const uint64_t dDS = sdesc(sDS, 0, 1024);
-            bool ok = mbar_wait(b_q, 0, abort_flag, p.err);
-            for (int j = 0; ok && j < nk; j++) {
+            // S = Q K_j^T, dP = dO V_j^T (128 queries x 64 keys)
+            auto issue_s = [&](int j) -> bool {
                 const int s = j & 1, u = j >> 1;
-                if (!mbar_wait_spin(s ? b_kvf1 : b_kvf0, u & 1, abort_flag, p.err)) break;
+                if (!mbar_wait_spin(s ? b_kvf1 : b_kvf0, u & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
                 const uint32_t sk = base + (s ? E_K1 : E_K0), sv = base + (s ? E_V1 : E_V0);
                 const uint64_t dk_k = sdesc(sk, 0, 1024), dv_k = sdesc(sv, 0, 1024);
-                const uint64_t dk_m = sdesc(sk, 8192, 1024);
-                // S = Q K_j^T, dP = dO V_j^T (128 queries x 64 keys)
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
                     umma_bf16(tS, dQ + (uint64_t)(2 * k), dk_k + (uint64_t)(2 * k), ID_S, k > 0);
@@ -707,6 +723,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 for (int k = 0; k < HD / 16; k++)
                     umma_bf16(tDP, dDO + (uint64_t)(2 * k), dv_k + (uint64_t)(2 * k), ID_S, k > 0);
                 umma_commit(b_sfull);
+                return true;
+            };
+            bool ok = mbar_wait(b_q, 0, abort_flag, p.err) && issue_s(0);
+            for (int j = 0; ok && j < nk; j++) {
+                const int s = j & 1;
+                const uint32_t sk = base + (s ? E_K1 : E_K0);
+                const uint64_t dk_m = sdesc(sk, 8192, 1024);
+                // the next step's products as soon as the softmax warps hold
+                // this step's S and dP in registers
+                if (j + 1 < nk) {
+                    if (!mbar_wait_spin(b_sfree, j & 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+                    if (!issue_s(j + 1)) break;
+                }
                 if (!mbar_wait_spin(b_dsfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 // dQ += dS K_j (K = the 64 keys)
@@ -734,16 +764,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 ok = false;
                 break;
             }
-            if (j > 0 && !warp_wait(b_dsfree, (j - 1) & 1, abort_flag, p.err, lane)) {
-                ok = false;
-                break;
-            }
             tc_fence_after();
             uint32_t sv[32], dp[32];
             tmem_ld32_async(tS + loff + c0, sv);
             tmem_ld32_async(tDP + loff + c0, dp);
             tmem_wait32(sv);
             tmem_wait32(dp);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_sfree);  // the next S, dP may land
             const int kbase = j * SUB;
             uint32_t dd[16];
             if (kbase + SUB <= qt * TILE) {  // every key of the step precedes every query
@@ -769,6 +798,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                     }
                     dd[e] = pack_bf16x2(dv[0], dv[1]);
                 }
+            }
+            // the previous step's product must be done reading the dS tile
+            if (j > 0 && !warp_wait(b_dsfree, (j - 1) & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                break;
             }
             st_row32_64(sDS, r, c0, dd);
             fence_proxy_async_smem();
