@@ -38,6 +38,9 @@ extern "C" {
  *   epi 2: D = resid[m,n] + acc (+ bias[n])
  *   epi 3: D (fp32) += acc                          (weight-gradient accumulate)
  *   epi 4: D = acc * gelu_tanh'(aux[m,n])           (MLP backward)
+ *   epi 5: x = acc + bias[n]; D = gelu_tanh(x), aux = gelu_tanh'(x)
+ *          (MLP forward keeping the derivative instead of x)
+ *   epi 6: D = acc * aux[m,n]                        (MLP backward with epi 5's aux)
  * impl: 0 = automatic (tensor cores for bf16 when the shape fits, else the
  * fp32-FFMA kernel), 1 = fp32-FFMA kernel, 2 = tensor cores (bf16 only;
  * returns -1 if the shape does not fit: N % 8, 16-byte aligned bases,

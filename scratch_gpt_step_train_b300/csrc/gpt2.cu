@@ -469,7 +469,7 @@ static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
                layernorm_forward(g->act, ln2, g->ln2_mean + l * bt, g->ln2_rstd + l * bt, x1,
                                  pc_tensor(g, P_LN2W, l), pc_tensor(g, P_LN2B, l), BT, C,
                                  g->stream));
-        d = gd(BT, 4 * C, C, ln2, C, 1, pc_tensor(g, P_FCW, l), C, 1, fchg, 4 * C, EPI_GELU);
+        d = gd(BT, 4 * C, C, ln2, C, 1, pc_tensor(g, P_FCW, l), C, 1, fchg, 4 * C, EPI_GELU_D);
         d.bias = pc_tensor(g, P_FCB, l);
         d.aux = fch;
         d.ldx = 4 * C;
@@ -573,7 +573,7 @@ extern "C" int gpt2_backward(gpt2_t* g) {
                EPI_ACCUM_F32);
         RUN(mm(g, K_FCPROJ_DW, d));
         d = gd(BT, 4 * C, C, dres, C, 1, pc_tensor(g, P_FCPROJW, l), 4 * C, 0, g->dbig, 4 * C,
-               EPI_GELU_BWD);
+               EPI_MUL_AUX);
         d.aux = fch;
         d.ldx = 4 * C;
         RUN(mm(g, K_FCPROJ_DX, d));

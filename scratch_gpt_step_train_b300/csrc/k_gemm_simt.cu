@@ -92,6 +92,19 @@ __global__ void __launch_bounds__(256) k_gemm_simt(GemmDesc d) {
                     ((T*)d.D)[(size_t)m * d.ldd + n] = from_f<T>(v * gelu_grad_f(pre));
                     break;
                 }
+                case EPI_MUL_AUX: {
+                    float dg = to_f(((const T*)d.aux)[(size_t)m * d.ldx + n]);
+                    ((T*)d.D)[(size_t)m * d.ldd + n] = from_f<T>(v * dg);
+                    break;
+                }
+                case EPI_GELU_D: {
+                    if (bias) v += to_f(bias[n]);
+                    float g, dg;
+                    gelu_and_grad_f(v, g, dg);
+                    ((T*)d.aux)[(size_t)m * d.ldx + n] = from_f<T>(dg);
+                    ((T*)d.D)[(size_t)m * d.ldd + n] = from_f<T>(g);
+                    break;
+                }
                 case EPI_GELU: {
                     if (bias) v += to_f(bias[n]);
                     ((T*)d.aux)[(size_t)m * d.ldx + n] = from_f<T>(v);

@@ -109,6 +109,16 @@ __device__ __forceinline__ float gelu_fast(float x) {
     float u = fmaxf(k * (x + 0.044715f * x * x * x), -40.0f);
     return __fdividef(x, 1.0f + __expf(-2.0f * u));
 }
+// gelu(x) and gelu'(x) sharing one sigmoid s = 1/(1 + e^{-2u}) (two MUFU
+// operations).  With u = k (x + c x^3), the derivative term 2 x du/dx equals
+// 6u - 4kx exactly, so gelu' = s + (s - s^2)(6u - 4kx) costs three FMAs.
+__device__ __forceinline__ void gelu_and_grad_fast(float x, float& g, float& dg) {
+    const float k = 0.7978845608028654f;
+    const float u = k * fmaf(0.044715f * x, x * x, x);
+    const float s = __fdividef(1.0f, 1.0f + __expf(-2.0f * fmaxf(u, -40.0f)));
+    g = x * s;
+    dg = fmaf(fmaf(-s, s, s), fmaf(-4.0f * k, x, 6.0f * u), s);
+}
 __device__ __forceinline__ float gelu_grad_fast(float x) {
     const float k = 0.7978845608028654f;
     float x2 = x * x;
@@ -167,7 +177,7 @@ __device__ __forceinline__ void stage_f32_row(uint32_t stg, int r, const float* 
 
 struct EpiMaps {
     CUtensorMap d;    // bf16 [M,N] box 32x32 SW64, or fp32 [M,N] box 32x32 SW128 (accumulate)
-    CUtensorMap aux;  // bf16 [M,N] box 32x32 SW64 (GELU pre-activation)
+    CUtensorMap aux;  // bf16 [M,N] box 32x32 SW64 (GELU pre-activation, or gelu')
     CUtensorMap part; // fp32 [splits,M,N] box 32x32x1 SW128 (split-K partials)
 };
 
@@ -177,7 +187,7 @@ struct EpiMaps {
 __device__ __forceinline__ void epi_prefetch(const TcParams& p, int row, int col, uint4 (&pf)[4]) {
     const bf16* src = nullptr;
     if (p.epi == EPI_RESID) src = p.resid + (size_t)row * p.ldr + col;
-    else if (p.epi == EPI_GELU_BWD) src = p.aux + (size_t)row * p.ldx + col;
+    else if (p.epi == EPI_GELU_BWD || p.epi == EPI_MUL_AUX) src = p.aux + (size_t)row * p.ldx + col;
     const int nv = min(32, p.N - col);
 #pragma unroll
     for (int k = 0; k < 4; k++)
@@ -209,6 +219,14 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
 #pragma unroll
             for (int i = 0; i < 8; i++) v[8 * k + i] *= gelu_grad_fast(pre[i]);
         }
+    } else if (p.epi == EPI_MUL_AUX) {
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            float dg[8];
+            unpack8_bf16(dg, pf[k]);
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[8 * k + i] *= dg[i];
+        }
     } else if (p.epi != EPI_ACCUM_F32 && p.epi != EPI_PART_F32) {
 #pragma unroll
         for (int k = 0; k < 4; k++) {
@@ -231,6 +249,12 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
     __syncwarp();
     if (p.epi == EPI_ACCUM_F32 || p.epi == EPI_PART_F32) {
         stage_f32_row(stg, lane, v);
+    } else if (p.epi == EPI_GELU_D) {
+        float dg[32];
+#pragma unroll
+        for (int i = 0; i < 32; i++) gelu_and_grad_fast(v[i], v[i], dg[i]);
+        stage_bf16_row(stg + 2048, lane, dg);  // gelu'
+        stage_bf16_row(stg, lane, v);
     } else if (p.epi == EPI_GELU) {
         stage_bf16_row(stg + 2048, lane, v);  // pre-activation
 #pragma unroll
@@ -246,7 +270,8 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
         else if (p.epi == EPI_PART_F32) tma_store_3d(&m.part, stg, col, row0, split);
         else {
             tma_store_2d(&m.d, stg, col, row0);
-            if (p.epi == EPI_GELU) tma_store_2d(&m.aux, stg + 2048, col, row0);
+            if (p.epi == EPI_GELU || p.epi == EPI_GELU_D)
+                tma_store_2d(&m.aux, stg + 2048, col, row0);
         }
         bulk_commit();
     }
@@ -429,7 +454,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int cbeg = ((warp - 2) >> 2) * (BN / 2);
         constexpr int NCH = BN / 64;  // 32-column chunks per half
         const uint32_t stg = stg_base + (uint32_t)(warp - 2) * 4096u;
-        const bool has_pf = p.epi == EPI_RESID || p.epi == EPI_GELU_BWD;
+        const bool has_pf = p.epi == EPI_RESID || p.epi == EPI_GELU_BWD || p.epi == EPI_MUL_AUX;
         int lt = 0;
         for (int u = unit0; u < num_units; u += ustep, lt++) {
             const int split = u / units_mn, r = u % units_mn;
@@ -558,7 +583,7 @@ bool make_epi_maps(EpiMaps* em, const GemmDesc& d, const TcParams& tp) {
         cuuint64_t dims[2] = {(cuuint64_t)d.N, (cuuint64_t)d.M};
         cuuint64_t st[1] = {(cuuint64_t)d.ldd * 2};
         ok = make_map_epi(&em->d, d.D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dims, st);
-        if (ok && tp.epi == EPI_GELU) {
+        if (ok && (tp.epi == EPI_GELU || tp.epi == EPI_GELU_D)) {
             cuuint64_t sx[1] = {(cuuint64_t)d.ldx * 2};
             ok = make_map_epi(&em->aux, d.aux, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 2, dims, sx);
         }
@@ -676,7 +701,9 @@ bool gemm_tc_supported(const GemmDesc& d) {
     if (d.a_kmajor ? d.lda < d.K : d.lda < d.M) return false;
     if (d.b_kmajor ? d.ldb < d.K : d.ldb < d.N) return false;
     if (d.epi == EPI_RESID && (!d.resid || !al16(d.resid) || d.ldr % 8)) return false;
-    if ((d.epi == EPI_GELU || d.epi == EPI_GELU_BWD) && (!d.aux || !al16(d.aux) || d.ldx % 8))
+    if ((d.epi == EPI_GELU || d.epi == EPI_GELU_BWD || d.epi == EPI_GELU_D ||
+         d.epi == EPI_MUL_AUX) &&
+        (!d.aux || !al16(d.aux) || d.ldx % 8))
         return false;
     if (d.bias && !al16(d.bias)) return false;
     return true;

@@ -25,9 +25,11 @@ extern "C" int gpt2k_matmul(int dtype, int impl, int M, int N, int K, const void
                             long ldx, int epi, void* scratch, size_t scratch_bytes,
                             unsigned* err, void* stream) {
     if (!dt_ok(dtype) || M < 1 || N < 1 || K < 1 || !A || !B || !D) return GPT2_ERR_ARG;
-    if (epi < EPI_STORE || epi > EPI_GELU_BWD) return GPT2_ERR_ARG;
+    if (epi < EPI_STORE || epi > EPI_MUL_AUX) return GPT2_ERR_ARG;
     if (epi == EPI_RESID && !resid) return GPT2_ERR_ARG;
-    if ((epi == EPI_GELU || epi == EPI_GELU_BWD) && !aux) return GPT2_ERR_ARG;
+    if ((epi == EPI_GELU || epi == EPI_GELU_BWD || epi == EPI_GELU_D || epi == EPI_MUL_AUX) &&
+        !aux)
+        return GPT2_ERR_ARG;
     GemmDesc d;
     d.M = M; d.N = N; d.K = K;
     d.A = A; d.lda = lda; d.a_kmajor = a_kmajor;

@@ -107,7 +107,9 @@ enum Epi {
     EPI_GELU = 1,       // aux = acc + bias; D = gelu(aux)
     EPI_RESID = 2,      // D = resid + acc + bias
     EPI_ACCUM_F32 = 3,  // D(fp32) += acc
-    EPI_GELU_BWD = 4    // D = acc * gelu'(aux)
+    EPI_GELU_BWD = 4,   // D = acc * gelu'(aux)
+    EPI_GELU_D = 5,     // x = acc + bias; D = gelu(x), aux = gelu'(x)
+    EPI_MUL_AUX = 6     // D = acc * aux  (aux holding gelu' from EPI_GELU_D)
 };
 struct GemmDesc {
     int M, N, K;
@@ -116,7 +118,7 @@ struct GemmDesc {
     void* D; long ldd;                      // D[m,n] at m*ldd+n
     const void* bias;                       // [N] act type, or NULL
     const void* resid; long ldr;            // EPI_RESID
-    void* aux; long ldx;                    // EPI_GELU out / EPI_GELU_BWD in
+    void* aux; long ldx;  // out: EPI_GELU, EPI_GELU_D; in: EPI_GELU_BWD, EPI_MUL_AUX
     int epi;
     int act;                                // element type of A, B, bias, resid, aux, D (non-accum)
 };

@@ -30,7 +30,8 @@ SIGNATURES = {
     "gpt2k_bias_grad": (_i, [_i, _vp, _vp, _i, _i, _vp, _vp]),
 }
 
-EPI = {"store": 0, "gelu": 1, "resid": 2, "accum_f32": 3, "gelu_bwd": 4}
+EPI = {"store": 0, "gelu": 1, "resid": 2, "accum_f32": 3, "gelu_bwd": 4, "gelu_d": 5,
+       "mul_aux": 6}
 _bound = False
 
 

@@ -96,6 +96,47 @@ def test_matmul_epilogues(a_km, b_km):
                   + 4e-7 * np.abs(acc) + 1e-30)
 
 
+# sup |gelu''| of the tanh-form GELU (attained at x = 0: 2 * 0.5 * sqrt(2/pi))
+GELU2_SUP = 0.8
+
+
+def test_gelu_second_derivative_bound():
+    x = np.linspace(-8, 8, 160001)
+    h = 1e-4
+    g2 = (ops.gelu_backward(x + h, np.ones_like(x)) - ops.gelu_backward(x - h, np.ones_like(x))) / (2 * h)
+    assert np.abs(g2).max() <= GELU2_SUP
+
+
+@pytest.mark.parametrize("a_km,b_km", LAYOUTS, ids=["AK-BK", "AK-BN", "AM-BK", "AM-BN"])
+@pytest.mark.parametrize("impl", [2, 1], ids=["tcgen05", "ffma"])
+def test_matmul_gelu_derivative_epilogues(a_km, b_km, impl):
+    """epi gelu_d: D = gelu(x), aux = gelu'(x) for x = acc + bias; epi mul_aux:
+    D = acc * aux -- together the MLP's GELU forward and backward"""
+    M, N, Kd = 296, 328, 200
+    rng = np.random.default_rng(11)
+    At, Bt, A64, B64 = _operands(M, N, Kd, 12, a_km, b_km)
+    bias = _bf(rng.normal(0, 1, N))
+    acc = ops.matmul_forward(A64, B64)
+    bnd = _bound(A64, B64, acc, Kd, out_bf16=False)
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    aux = torch.empty_like(D)
+    K.matmul(At, Bt, D, a_kmajor=a_km, b_kmajor=b_km, bias=bias, aux=aux, epi="gelu_d",
+             impl=impl, M=M, N=N, K=Kd)
+    pre = acc + _np(bias)
+    gl = ops.gelu_forward(pre)
+    assert np.all(np.abs(_np(D) - gl) <= 1.2 * bnd + 2.0 ** -8 * np.abs(gl) + 1e-30)
+    dg = ops.gelu_backward(pre, np.ones_like(pre))
+    # |gelu'(x~) - gelu'(x)| <= sup|gelu''| |x~ - x|, plus the fp32 evaluation
+    # of gelu' (its two terms cancel near x = -0.75) and the bf16 rounding
+    assert np.all(np.abs(_np(aux) - dg) <= GELU2_SUP * bnd + 4e-7 + 2.0 ** -8 * np.abs(dg))
+    auxin = _bf(rng.normal(0, 0.7, (M, N)))
+    K.matmul(At, Bt, D, a_kmajor=a_km, b_kmajor=b_km, aux=auxin, epi="mul_aux", impl=impl,
+             M=M, N=N, K=Kd)
+    ref = acc * _np(auxin)
+    assert np.all(np.abs(_np(D) - ref) <= np.abs(_np(auxin)) * bnd + 2.0 ** -8 * np.abs(ref)
+                  + 1e-30)
+
+
 @pytest.mark.parametrize("a_km,b_km", LAYOUTS, ids=["AK-BK", "AK-BN", "AM-BK", "AM-BN"])
 @pytest.mark.parametrize("Kd", [200, 2000], ids=["nosplit", "splitK"])
 def test_matmul_accumulate_fp32(a_km, b_km, Kd):
@@ -127,6 +168,8 @@ FULL = [
     ("proj_dx", 16384, 768, 768, True, False, "store"),
     ("fc_dx", 16384, 768, 3072, True, False, "store"),
     ("fcproj_dx", 16384, 3072, 768, True, False, "gelu_bwd"),
+    ("fc_fwd_gelu_d", 16384, 3072, 768, True, True, "gelu_d"),
+    ("fcproj_dx_mul_aux", 16384, 3072, 768, True, False, "mul_aux"),
     ("classifier_dx", 16384, 768, 50304, True, False, "store"),
     ("qkv_dw", 2304, 768, 16384, False, False, "accum_f32"),
     ("proj_dw", 768, 768, 16384, False, False, "accum_f32"),
@@ -159,11 +202,13 @@ def test_matmul_full_size_sampled(name, M, N, Kd, a_km, b_km, epi):
     D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     kw = {}
     ref = acc.copy()
-    if epi in ("store", "gelu", "resid"):
+    if epi in ("store", "gelu", "resid", "gelu_d"):
         kw["bias"] = bias
         ref = ref + _np(bias)
-    if epi == "gelu":
+    if epi in ("gelu", "gelu_d"):
         kw["aux"] = torch.empty_like(D)
+    if epi == "mul_aux":
+        kw["aux"] = (torch.randn(M, N, generator=g, device="cuda") * 0.7).to(torch.bfloat16)
     if epi == "resid":
         kw["resid"] = torch.randn(M, N, generator=g, device="cuda").to(torch.bfloat16)
         ref = ref + _np(kw["resid"][rt])
@@ -175,6 +220,16 @@ def test_matmul_full_size_sampled(name, M, N, Kd, a_km, b_km, epi):
         assert np.all(np.abs(_np(kw["aux"][rt]) - ref) <= bnd + 2.0 ** -8 * np.abs(ref) + 1e-30)
         ref = ops.gelu_forward(ref)
         bnd = 1.2 * bnd
+    if epi == "gelu_d":
+        dg = ops.gelu_backward(ref, np.ones_like(ref))
+        assert np.all(np.abs(_np(kw["aux"][rt]) - dg) <= GELU2_SUP * bnd + 4e-7
+                      + 2.0 ** -8 * np.abs(dg))
+        ref = ops.gelu_forward(ref)
+        bnd = 1.2 * bnd
+    if epi == "mul_aux":
+        a = _np(kw["aux"][rt])
+        ref = acc * a
+        bnd = np.abs(a) * bnd
     if epi == "gelu_bwd":
         pre = _np(kw["aux"][rt])
         ref = ops.gelu_backward(pre, acc)
