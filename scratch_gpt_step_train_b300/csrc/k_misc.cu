@@ -933,6 +933,12 @@ __global__ void __launch_bounds__(512) k_xent(T* logits, float* losses, const in
 // in-place write of (softmax - onehot) * dloss with the pad columns zeroed.
 // ---------------------------------------------------------------------------
 #define XS_THREADS 1024
+// a packed bf16 pair reinterpreted (register to register)
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t x) {
+    __nv_bfloat162 r;
+    memcpy(&r, &x, sizeof r);
+    return r;
+}
 #define XS_CHUNK 32768u  // bytes per bulk copy
 
 __device__ __forceinline__ float ex2f_approx(float x) {
@@ -1006,41 +1012,61 @@ __global__ void __launch_bounds__(XS_THREADS, 1)
             if (tid == 0) atomicOr(err, GPT2_DEVERR_TOKEN);
             y = 0;
         }
-        // pass 1: row max over the real columns
-        float m = -INFINITY;
-        for (int j = tid * 8; j < V; j += XS_THREADS * 8) {
-            Vec<bf16, 8> v = *reinterpret_cast<const Vec<bf16, 8>*>(z + j);
-#pragma unroll
-            for (int e = 0; e < 8; e++)
-                if (j + e < V) m = fmaxf(m, to_f(v.v[e]));
-        }
-        m = block_reduce(m, 0, red);
-        // pass 2: sum of exp(z - max) (z - max is exact for bf16 z)
+        // vectors of 8: [0, nfull) hold only real columns; the rest (the one
+        // straddling V, then pure padding) take per-element checks
+        const int nfull = V / 8, nvec = Vp / 8;
         const float L2E = 1.4426950408889634f;
-        float sum = 0.f;
-        for (int j = tid * 8; j < V; j += XS_THREADS * 8) {
-            Vec<bf16, 8> v = *reinterpret_cast<const Vec<bf16, 8>*>(z + j);
-#pragma unroll
-            for (int e = 0; e < 8; e++)
-                if (j + e < V) sum += ex2f_approx((to_f(v.v[e]) - m) * L2E);
+        // pass 1: row max over the real columns (packed bf16 pairs)
+        __nv_bfloat162 m2 = __float2bfloat162_rn(-INFINITY);
+        for (int j = tid; j < nfull; j += XS_THREADS) {
+            const uint4 u = *reinterpret_cast<const uint4*>(z + 8 * j);
+            m2 = __hmax2(m2, __hmax2(__hmax2(as_bf2(u.x), as_bf2(u.y)),
+                                     __hmax2(as_bf2(u.z), as_bf2(u.w))));
         }
+        float m = fmaxf(__low2float(m2), __high2float(m2));
+        for (int c = 8 * nfull + tid; c < V; c += XS_THREADS) m = fmaxf(m, to_f(z[c]));
+        m = block_reduce(m, 0, red);
+        // pass 2: sum of exp(z - max)
+        const float nm = -m * L2E;
+        float sum = 0.f;
+        for (int j = tid; j < nfull; j += XS_THREADS) {
+            const uint4 u = *reinterpret_cast<const uint4*>(z + 8 * j);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 8; e++) sum += ex2f_approx(fmaf(bf_half(w4[e >> 1], e & 1), L2E, nm));
+        }
+        for (int c = 8 * nfull + tid; c < V; c += XS_THREADS)
+            sum += ex2f_approx(fmaf(to_f(z[c]), L2E, nm));
         sum = block_reduce(sum, 1, red);
         const float lse = m + logf(sum);
         if (tid == 0) losses[row] = lse - to_f(z[y]);
         if (dloss != 0.f) {
-            // pass 3: dlogits, written over the row in global memory
+            // pass 3: dlogits = softmax * dloss over the row, then the target
+            // column minus dloss; written over the row in global memory
             bf16* zo = logits + (size_t)row * Vp;
             const float nl = -lse * L2E;
-            for (int j = tid * 8; j < Vp; j += XS_THREADS * 8) {
-                Vec<bf16, 8> v = *reinterpret_cast<const Vec<bf16, 8>*>(z + j);
+            for (int j = tid; j < nfull; j += XS_THREADS) {
+                const uint4 u = *reinterpret_cast<const uint4*>(z + 8 * j);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++)
+                    o[q] = pack2_bf16_rn(ex2f_approx(fmaf(bf_half(w4[q], 0), L2E, nl)) * dloss,
+                                         ex2f_approx(fmaf(bf_half(w4[q], 1), L2E, nl)) * dloss);
+                *reinterpret_cast<uint4*>(zo + 8 * j) = make_uint4(o[0], o[1], o[2], o[3]);
+                if (y >> 3 == j)  // the target column: rewritten by the same thread
+                    zo[y] = from_f<bf16>((ex2f_approx(fmaf(to_f(z[y]), L2E, nl)) - 1.f) * dloss);
+            }
+            for (int j = nfull + tid; j < nvec; j += XS_THREADS) {
+                Vec<bf16, 8> v = *reinterpret_cast<const Vec<bf16, 8>*>(z + 8 * j);
                 Vec<bf16, 8> o;
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
-                    const int col = j + e;
-                    const float p = ex2f_approx(fmaf(to_f(v.v[e]), L2E, nl));
-                    o.v[e] = from_f<bf16>(col < V ? (p - (col == y ? 1.f : 0.f)) * dloss : 0.f);
+                    const int col = 8 * j + e;
+                    const float pv = ex2f_approx(fmaf(to_f(v.v[e]), L2E, nl));
+                    o.v[e] = from_f<bf16>(col < V ? (pv - (col == y ? 1.f : 0.f)) * dloss : 0.f);
                 }
-                *reinterpret_cast<Vec<bf16, 8>*>(zo + j) = o;
+                *reinterpret_cast<Vec<bf16, 8>*>(zo + 8 * j) = o;
             }
         }
         __syncthreads();  // half b is free for the copy issued next iteration
@@ -1236,55 +1262,78 @@ __global__ void k_emb_blockprefix(int* blkcnt, int* cnt, int nb, int Vp) {
 }
 
 // One block of 1024 threads: exclusive scans of n_v, chunks_v, multi-chunk
-// chunks_v over v in [0, Vp).
+// chunks_v over v in [0, Vp), in tiles of 4096 consecutive v (coalesced: thread
+// t takes v = tile + 4t .. 4t+3), each tile a warp-shuffle block scan plus the
+// running total of the tiles before it.
 __global__ void __launch_bounds__(1024) k_emb_scan(const int* cnt, int* start, int* itemoff,
                                                    int* poff, int Vp) {
     gdc_wait();
     gdc_launch_dependents();
-    __shared__ int s0[1024], s1[1024], s2[1024];
-    int per = (Vp + 1023) / 1024;
-    int lo = threadIdx.x * per, hi = min(Vp, lo + per);
-    int a = 0, b = 0, c = 0;
-    for (int v = lo; v < hi; v++) {
-        int n = cnt[v], ch = (n + EMB_R - 1) / EMB_R;
-        a += n;
-        b += ch;
-        c += ch > 1 ? ch : 0;
-    }
-    s0[threadIdx.x] = a;
-    s1[threadIdx.x] = b;
-    s2[threadIdx.x] = c;
+    __shared__ int wsum[3][32];
+    __shared__ int carry[3];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (t < 3) carry[t] = 0;
     __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-        int x0 = s0[threadIdx.x], x1 = s1[threadIdx.x], x2 = s2[threadIdx.x];
-        if (threadIdx.x >= off) {
-            x0 += s0[threadIdx.x - off];
-            x1 += s1[threadIdx.x - off];
-            x2 += s2[threadIdx.x - off];
+    for (int base = 0; base < Vp; base += 4096) {
+        int n[4], ch[4];
+        int own[3] = {0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int v = base + 4 * t + k;
+            n[k] = v < Vp ? cnt[v] : 0;
+            ch[k] = (n[k] + EMB_R - 1) / EMB_R;
+            own[0] += n[k];
+            own[1] += ch[k];
+            own[2] += ch[k] > 1 ? ch[k] : 0;
+        }
+        int inc[3] = {own[0], own[1], own[2]};
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+            for (int q = 0; q < 3; q++) {
+                const int y = __shfl_up_sync(0xffffffffu, inc[q], off);
+                if (lane >= off) inc[q] += y;
+            }
+        }
+        if (lane == 31) {
+#pragma unroll
+            for (int q = 0; q < 3; q++) wsum[q][warp] = inc[q];
         }
         __syncthreads();
-        s0[threadIdx.x] = x0;
-        s1[threadIdx.x] = x1;
-        s2[threadIdx.x] = x2;
+        if (warp == 0) {
+#pragma unroll
+            for (int q = 0; q < 3; q++) {
+                int x = wsum[q][lane];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
+                }
+                wsum[q][lane] = x;  // inclusive over warps
+            }
+        }
+        __syncthreads();
+        int pre[3];
+#pragma unroll
+        for (int q = 0; q < 3; q++)
+            pre[q] = carry[q] + (warp ? wsum[q][warp - 1] : 0) + inc[q] - own[q];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int v = base + 4 * t + k;
+            if (v < Vp) {
+                start[v] = pre[0];
+                itemoff[v] = pre[1];
+                poff[v] = pre[2];
+            }
+            pre[0] += n[k];
+            pre[1] += ch[k];
+            pre[2] += ch[k] > 1 ? ch[k] : 0;
+        }
+        __syncthreads();  // every thread has read carry and wsum
+        if (t < 3) carry[t] += wsum[t][31];
         __syncthreads();
     }
-    a = threadIdx.x ? s0[threadIdx.x - 1] : 0;
-    b = threadIdx.x ? s1[threadIdx.x - 1] : 0;
-    c = threadIdx.x ? s2[threadIdx.x - 1] : 0;
-    for (int v = lo; v < hi; v++) {
-        int n = cnt[v], ch = (n + EMB_R - 1) / EMB_R;
-        start[v] = a;
-        itemoff[v] = b;
-        poff[v] = c;
-        a += n;
-        b += ch;
-        c += ch > 1 ? ch : 0;
-    }
-    if (threadIdx.x == 1023) {
-        start[Vp] = s0[1023];
-        itemoff[Vp] = s1[1023];
-        poff[Vp] = s2[1023];
-    }
+    if (t < 3) (t == 0 ? start : (t == 1 ? itemoff : poff))[Vp] = carry[t];
 }
 
 __global__ void k_emb_place(const int* tok, int BT, int Vp, const int* start, const int* blkcnt,
