@@ -9,18 +9,22 @@
 // "Code anatomy" item 2 and "Performance comparison"); here it is one fused
 // kernel per direction, written for tcgen05.
 //
-// Forward (one CTA per 128-query tile of one (batch, head); 192 threads):
-//   warp 0    TMA: the Q tile once, then K_j and V_j tiles (128 keys x 64)
-//   warp 1    TMEM (256 columns) + tcgen05.mma issue:
-//               S_j = Q K_j^T          M=128 N=128 K=64   -> TMEM cols [0,128)
-//               O_j = P_j V_j          M=128 N=64  K=128  -> TMEM cols [128,192)
-//   warps 2-5 one query row per thread: tcgen05.ld of S_j, online softmax in
-//             base 2 (running max m, sum l), P_j = exp2(S_j c - m) written as
-//             bf16 into a 128-byte-swizzled smem tile that is the A operand of
-//             the second product; O_j is read back and accumulated in
-//             registers as O = O * exp2(m_old - m_new) + O_j.
+// Forward (one CTA per 128-query tile of one (batch, head); 288 threads):
+//   warp 0, lane 0  TMA: the Q tile once, then K_j, V_j tiles (128 keys x 64)
+//                   through a ring of five shared-memory slots
+//   warp 0, lane 1  tcgen05.mma issue, TMEM (256 columns):
+//                     S_j = Q K_j^T   M=128 N=128 K=64   -> fp32 cols [0,128)
+//                     O  += P_j V_j   M=128 N=64  K=128  -> fp32 cols [128,192)
+//                   with P_j (bf16, two per column) read from cols [192,256);
+//                   S_{j+1} is issued as soon as the softmax warps hold S_j
+//   warps 1-8       two warps per TMEM lane quarter, each one half of the
+//                   keys of 32 rows: tcgen05.ld of S_j, row max (exchanged
+//                   between the halves), P_j = exp2(S_j c - m) in base 2,
+//                   tcgen05.st of P_j; the running max m is raised (and O, the
+//                   row sum rescaled in TMEM) only when a row max exceeds it
+//                   by more than 2^8.
 // Keys are visited in tiles 0..q (q = the query tile); only the diagonal tile
-// needs the causal mask.  Two CTAs fit on one SM (~82 KB smem, 256 TMEM
+// needs the causal mask.  Two CTAs fit on one SM (~100 KB smem, 256 TMEM
 // columns each), so one CTA's softmax overlaps the other's products.
 // Outputs: O [B,T,C] (bf16) and the row log-sum-exp [B,H,T] (fp32, natural
 // log), which the backward pass uses to recompute P.
@@ -38,10 +42,12 @@ constexpr int HD = 64;
 constexpr int TILE = 128;               // queries per CTA = keys per tile
 constexpr int TILE_BYTES = TILE * 128;  // 128 rows of 64 bf16
 constexpr int ATT_THREADS = 320;        // TMA warp, MMA warp, 8 softmax warps
-// forward smem: Q, a ring of 3 K/V slots (K_0 V_0 K_1 V_1 ... in order), P,
-// then the row-max exchange, the final row-sum exchange and the barriers
-constexpr int F_Q = 0, F_RING = 16384, F_P = 65536, F_RED = 98304, F_LS = 99328,
-              F_BAR = 100352;
+// forward smem: Q, a ring of F_NRING K/V slots (K_0 V_0 K_1 V_1 ... in order),
+// then the row-max exchange, the final row-sum exchange and the barriers (P
+// lives in TMEM)
+constexpr int F_NRING = 5;
+constexpr int F_Q = 0, F_RING = 16384, F_RED = F_RING + F_NRING * 16384, F_LS = F_RED + 1024,
+              F_BAR = F_LS + 1024;
 constexpr int F_SMEM = F_BAR + 256 + 1024;
 
 struct AttnParams {
@@ -78,17 +84,6 @@ __device__ __forceinline__ void named_sync_softmax() {
     asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
-// write 32 values (16 packed bf16 pairs) of row r, columns [c0, c0+32), into a
-// 128x128 bf16 K-major tile with 128-byte swizzle (two 64-column atoms)
-__device__ __forceinline__ void st_row32(uint32_t tile, int r, int c0, const uint32_t* pk) {
-#pragma unroll
-    for (int cc = 0; cc < 4; cc++) {
-        const int chunk = ((c0 & 63) >> 3) + cc;
-        const uint32_t addr = tile + (c0 >> 6) * 16384 + r * 128 + ((uint32_t)(chunk ^ (r & 7)) << 4);
-        st_shared_v4(addr, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-    }
-}
-
 constexpr int FWD_THREADS = 288;  // warp 0: TMA (lane 0) + MMA (lane 1); 8 softmax warps
 constexpr float RESCALE_SLACK = 8.0f;  // log2 units: P stays <= 2^8 between rescales
 
@@ -98,14 +93,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw);
-    const uint32_t sQ = base + F_Q, sRing = base + F_RING, sP = base + F_P;
+    const uint32_t sQ = base + F_Q, sRing = base + F_RING;
     float* red = (float*)(base_gen + F_RED);  // [2 buffers][2 halves][128 rows]
     float* lsum = (float*)(base_gen + F_LS);  // [2 halves][128 rows]
     const uint32_t bar = base + F_BAR;
-    // full[3], empty[3] for the ring; q; s (S ready); pf (P ready); o (P.V done);
-    // sfree (S copied to registers: the next S may overwrite it)
-    const uint32_t b_full = bar, b_empty = bar + 24, b_q = bar + 48, b_sfull = bar + 56,
-                   b_pfull = bar + 64, b_ofull = bar + 72, b_sfree = bar + 80;
+    // full[F_NRING], empty[F_NRING] for the ring; q; s (S ready); pf (P ready);
+    // o (P.V done); sfree (S copied to registers: the next S may overwrite it)
+    const uint32_t b_full = bar, b_empty = bar + 8 * F_NRING, b_q = bar + 16 * F_NRING,
+                   b_sfull = b_q + 8, b_pfull = b_q + 16, b_ofull = b_q + 24, b_sfree = b_q + 32;
     uint32_t* tmem_slot = (uint32_t*)(base_gen + F_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + F_BAR + 132);
 
@@ -118,7 +113,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 3; i++) {
+        for (int i = 0; i < F_NRING; i++) {
             mbar_init(b_full + 8 * i, 1);
             mbar_init(b_empty + 8 * i, 1);
         }
@@ -141,7 +136,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
     const uint32_t tmem = *tmem_slot;
     gdc_wait();  // setup above touches no global memory
     gdc_launch_dependents();
-    const uint32_t tS = tmem, tO = tmem + 128;  // S [128 x 128], O [128 x 64] fp32
+    // S [128 x 128] fp32, O [128 x 64] fp32, P [128 x 128] bf16 (64 columns)
+    const uint32_t tS = tmem, tO = tmem + 128, tP = tmem + 192;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -149,20 +145,19 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
             const int ck = p.C + h * HD, cv = 2 * p.C + h * HD;
             mbar_expect_tx(b_q, TILE_BYTES);
             tma_load_2d(sQ, &map, b_q, h * HD, row0 + qt * TILE);
-            int last0 = -1, last1 = -1, last2 = -1;  // use count of each slot's last load
+            int last[F_NRING];  // use count of each slot's last load
+            for (int s = 0; s < F_NRING; s++) last[s] = -1;
             for (int it = 0; it < 2 * nkt; it++) {
-                const int s = it % 3, u = it / 3;
+                const int s = it % F_NRING, u = it / F_NRING;
                 if (!mbar_wait(b_empty + 8 * s, (u & 1) ^ 1, abort_flag, p.err)) break;
                 mbar_expect_tx(b_full + 8 * s, TILE_BYTES);
                 tma_load_2d(sRing + s * TILE_BYTES, &map, b_full + 8 * s, (it & 1) ? cv : ck,
                             row0 + (it >> 1) * TILE);
-                if (s == 0) last0 = u;
-                else if (s == 1) last1 = u;
-                else last2 = u;
+                last[s] = u;
             }
             if (*abort_flag) {
-                for (int s = 0; s < 3; s++) {
-                    const int ls = s == 0 ? last0 : (s == 1 ? last1 : last2);
+                for (int s = 0; s < F_NRING; s++) {
+                    const int ls = last[s];
                     if (ls < 0) continue;
                     long long t0 = clock64();
                     while (!mbar_try(b_full + 8 * s, ls & 1) && clock64() - t0 < WAIT_LIMIT) {
@@ -178,11 +173,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
             // descriptors are built once; a K step advances the start address
             // field (bits 0..13, in 16-byte units) by a constant
-            const uint64_t dQ = sdesc(sQ, 0, 1024), dP = sdesc(sP, 0, 1024);
+            const uint64_t dQ = sdesc(sQ, 0, 1024);
             const uint64_t dRingK = sdesc(sRing, 0, 1024), dRingV = sdesc(sRing, 8192, 1024);
             auto issue_s = [&](int j) -> bool {
-                const int it = 2 * j, s = it % 3;
-                if (!mbar_wait_spin(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) return false;
+                const int it = 2 * j, s = it % F_NRING;
+                if (!mbar_wait_spin(b_full + 8 * s, (it / F_NRING) & 1, abort_flag, p.err))
+                    return false;
                 tc_fence_after();
                 const uint64_t dK = dRingK + (uint64_t)((s * TILE_BYTES) >> 4);
 #pragma unroll
@@ -203,15 +199,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
                 }
                 if (!mbar_wait_spin(b_pfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                const int it = 2 * j + 1, s = it % 3;
-                if (!mbar_wait_spin(b_full + 8 * s, (it / 3) & 1, abort_flag, p.err)) break;
+                const int it = 2 * j + 1, s = it % F_NRING;
+                if (!mbar_wait_spin(b_full + 8 * s, (it / F_NRING) & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint64_t dV = dRingV + (uint64_t)((s * TILE_BYTES) >> 4);
-                // O += P_j V_j (O starts at the first tile)
+                // O += P_j V_j (O starts at the first tile); P is read from TMEM,
+                // 16 keys (8 columns) per instruction
 #pragma unroll
                 for (int k = 0; k < TILE / 16; k++)
-                    umma_bf16(tO, dP + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
-                              dV + (uint64_t)(k * 128), ID_O, (j > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(tO, tP + (uint32_t)(8 * k), dV + (uint64_t)(k * 128), ID_O,
+                                     (j > 0 || k > 0) ? 1u : 0u);
                 umma_commit(b_ofull);
                 umma_commit(b_empty + 8 * s);
             }
@@ -251,19 +248,37 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
                     for (int i = 0; i < 32; i++)
                         if (kb + 32 * c + i > r) sv[c][i] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row max over the 64 columns as a tree (8 independent chains)
+            float m8[8];
 #pragma unroll
-            for (int c = 0; c < 2; c++)
+            for (int i = 0; i < 8; i++) m8[i] = __uint_as_float(sv[0][i]);
 #pragma unroll
-                for (int i = 0; i < 32; i++) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
+            for (int i = 8; i < 64; i++) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i >> 5][i & 31]));
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; i++) m8[i] = fmaxf(m8[i], m8[i + w]);
+            const float mx = m8[0];
             float* rb = red + (j & 1) * 256;
             rb[hf * 128 + r] = mx;
             named_sync_softmax();
             const float mrow = fmaxf(rb[r], rb[128 + r]) * p.scale_log2;
             const bool need = mrow > m_used + RESCALE_SLACK;
             const float m_new = need ? mrow : m_used;
-            // P.V of the previous tile must be done: it reads the P buffer and
-            // writes O, which a rescale rewrites
+            // P_j in registers first (exponentials relative to m_new)
+            uint32_t pk[32];
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};  // the tile's row sum in 4 chains
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+                const float a =
+                    ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i) & 31]), p.scale_log2, -m_new));
+                const float e =
+                    ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i + 1) & 31]), p.scale_log2, -m_new));
+                l4[i & 3] += a + e;
+                pk[i] = pack_bf16x2(a, e);
+            }
+            // P.V of the previous tile must be done: it reads the P columns of
+            // TMEM and writes O, which a rescale rewrites
             if (j > 0 && !warp_wait(b_ofull, (j - 1) & 1, abort_flag, p.err, lane)) {
                 ok = false;
                 break;
@@ -280,20 +295,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
                 l *= corr;
             }
             m_used = m_new;
-#pragma unroll
-            for (int c = 0; c < 2; c++) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const float a = ex2(fmaf(__uint_as_float(sv[c][2 * i]), p.scale_log2, -m_used));
-                    const float e =
-                        ex2(fmaf(__uint_as_float(sv[c][2 * i + 1]), p.scale_log2, -m_used));
-                    l += a + e;
-                    pk[i] = pack_bf16x2(a, e);
-                }
-                st_row32(sP, r, kb + 32 * c, pk);
-            }
-            fence_proxy_async_smem();
+            l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            // keys [kb, kb+64) of each row: 32 packed columns of P
+            tmem_st32(tP + loff + hf * 32, pk);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_pfull);
