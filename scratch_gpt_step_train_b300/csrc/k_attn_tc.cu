@@ -628,9 +628,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     }
 }
 
-// dQ: CTA = (128-query tile qt, batch, head); key steps of 64.
-constexpr int E_Q = 0, E_DO = 16384, E_K0 = 32768, E_K1 = 40960, E_V0 = 49152, E_V1 = 57344,
-              E_DS = 65536, E_BAR = 81920;
+// dQ: CTA = (128-query tile qt, batch, head); key steps of 64 through a ring of
+// E_NRING (K_j, V_j) slots; dS lives in TMEM.
+constexpr int E_NRING = 3;
+constexpr int E_Q = 0, E_DO = 16384, E_KV = 32768, E_BAR = E_KV + E_NRING * 2 * SUB_BYTES;
 constexpr int E_SMEM = E_BAR + 256 + 1024;
 
 __global__ void __launch_bounds__(BWD_THREADS, 2)
@@ -639,11 +640,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw);
-    const uint32_t sQ = base + E_Q, sDO = base + E_DO, sDS = base + E_DS;
+    const uint32_t sQ = base + E_Q, sDO = base + E_DO, sKV = base + E_KV;
     const uint32_t bar = base + E_BAR;
-    const uint32_t b_q = bar, b_kvf0 = bar + 8, b_kvf1 = bar + 16, b_kve0 = bar + 24,
-                   b_kve1 = bar + 32, b_sfull = bar + 40, b_dsfull = bar + 48,
-                   b_dsfree = bar + 56, b_acc = bar + 64, b_sfree = bar + 72;
+    // q; kv full[E_NRING]; kv empty[E_NRING]; s, ds full / free, acc, s consumed
+    const uint32_t b_q = bar, b_kvf = bar + 8, b_kve = bar + 8 + 8 * E_NRING,
+                   b_sfull = bar + 8 + 16 * E_NRING, b_dsfull = b_sfull + 8,
+                   b_dsfree = b_sfull + 16, b_acc = b_sfull + 24, b_sfree = b_sfull + 32;
     uint32_t* tmem_slot = (uint32_t*)(base_gen + E_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + E_BAR + 132);
 
@@ -655,10 +657,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
-        mbar_init(b_kvf0, 1);
-        mbar_init(b_kvf1, 1);
-        mbar_init(b_kve0, 1);
-        mbar_init(b_kve1, 1);
+        for (int i = 0; i < E_NRING; i++) {
+            mbar_init(b_kvf + 8 * i, 1);
+            mbar_init(b_kve + 8 * i, 1);
+        }
         mbar_init(b_sfull, 1);
         mbar_init(b_dsfull, 8);
         mbar_init(b_dsfree, 1);
@@ -677,7 +679,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     const uint32_t tmem = *tmem_slot;
     gdc_wait();  // setup above touches no global memory
     gdc_launch_dependents();
-    const uint32_t tS = tmem, tDP = tmem + 64, tDQ = tmem + 128;
+    // S, dP, dQ [128 x 64] fp32; dS [128 x 64] bf16 (32 columns)
+    const uint32_t tS = tmem, tDP = tmem + 64, tDQ = tmem + 128, tDS = tmem + 192;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -685,23 +688,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             mbar_expect_tx(b_q, 2 * TILE_BYTES);
             tma_load_2d(sQ, &maps.qkv128, b_q, h * HD, row0 + qt * TILE);
             tma_load_2d(sDO, &maps.do128, b_q, h * HD, row0 + qt * TILE);
-            int issued0 = -1, issued1 = -1;
+            int issued[E_NRING];
+            for (int s = 0; s < E_NRING; s++) issued[s] = -1;
             for (int j = 0; j < nk; j++) {
-                const int s = j & 1, u = j >> 1;
-                if (!mbar_wait(s ? b_kve1 : b_kve0, (u & 1) ^ 1, abort_flag, p.err)) break;
-                const uint32_t ff = s ? b_kvf1 : b_kvf0;
+                const int s = j % E_NRING, u = j / E_NRING;
+                if (!mbar_wait(b_kve + 8 * s, (u & 1) ^ 1, abort_flag, p.err)) break;
+                const uint32_t ff = b_kvf + 8 * s;
                 mbar_expect_tx(ff, 2 * SUB_BYTES);
-                tma_load_2d(base + (s ? E_K1 : E_K0), &maps.qkv64, ff, ck, row0 + j * SUB);
-                tma_load_2d(base + (s ? E_V1 : E_V0), &maps.qkv64, ff, cv, row0 + j * SUB);
-                if (s) issued1 = u;
-                else issued0 = u;
+                tma_load_2d(sKV + s * 2 * SUB_BYTES, &maps.qkv64, ff, ck, row0 + j * SUB);
+                tma_load_2d(sKV + s * 2 * SUB_BYTES + SUB_BYTES, &maps.qkv64, ff, cv,
+                            row0 + j * SUB);
+                issued[s] = u;
             }
             if (*abort_flag) {
-                for (int s = 0; s < 2; s++) {
-                    const int is = s ? issued1 : issued0;
+                for (int s = 0; s < E_NRING; s++) {
+                    const int is = issued[s];
                     if (is < 0) continue;
                     long long t0 = clock64();
-                    while (!mbar_try(s ? b_kvf1 : b_kvf0, is & 1) && clock64() - t0 < WAIT_LIMIT) {
+                    while (!mbar_try(b_kvf + 8 * s, is & 1) && clock64() - t0 < WAIT_LIMIT) {
                     }
                 }
                 long long t0 = clock64();
@@ -712,13 +716,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             constexpr uint32_t ID_S = make_idesc(128, SUB, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
             const uint64_t dQ = sdesc(sQ, 0, 1024), dDO = sdesc(sDO, 0, 1024);
-            const uint64_t dDS = sdesc(sDS, 0, 1024);
             // S = Q K_j^T, dP = dO V_j^T (128 queries x 64 keys)
             auto issue_s = [&](int j) -> bool {
-                const int s = j & 1, u = j >> 1;
-                if (!mbar_wait_spin(s ? b_kvf1 : b_kvf0, u & 1, abort_flag, p.err)) return false;
+                const int s = j % E_NRING, u = j / E_NRING;
+                if (!mbar_wait_spin(b_kvf + 8 * s, u & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
-                const uint32_t sk = base + (s ? E_K1 : E_K0), sv = base + (s ? E_V1 : E_V0);
+                const uint32_t sk = sKV + s * 2 * SUB_BYTES, sv = sk + SUB_BYTES;
                 const uint64_t dk_k = sdesc(sk, 0, 1024), dv_k = sdesc(sv, 0, 1024);
 #pragma unroll
                 for (int k = 0; k < HD / 16; k++)
@@ -731,8 +734,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             };
             bool ok = mbar_wait(b_q, 0, abort_flag, p.err) && issue_s(0);
             for (int j = 0; ok && j < nk; j++) {
-                const int s = j & 1;
-                const uint32_t sk = base + (s ? E_K1 : E_K0);
+                const int s = j % E_NRING;
+                const uint32_t sk = sKV + s * 2 * SUB_BYTES;
                 const uint64_t dk_m = sdesc(sk, 8192, 1024);
                 // the next step's products as soon as the softmax warps hold
                 // this step's S and dP in registers
@@ -743,12 +746,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 }
                 if (!mbar_wait_spin(b_dsfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                // dQ += dS K_j (K = the 64 keys)
+                // dQ += dS K_j (K = the 64 keys; dS read from TMEM, 8 columns
+                // = 16 keys per instruction)
 #pragma unroll
                 for (int k = 0; k < SUB / 16; k++)
-                    umma_bf16(tDQ, dDS + (uint64_t)(2 * k), dk_m + (uint64_t)(128 * k), ID_O,
-                              (j > 0 || k > 0));
-                umma_commit(s ? b_kve1 : b_kve0);
+                    umma_bf16_tmem_a(tDQ, tDS + (uint32_t)(8 * k), dk_m + (uint64_t)(128 * k),
+                                     ID_O, (j > 0 || k > 0));
+                umma_commit(b_kve + 8 * s);
                 umma_commit(b_dsfree);
             }
             if (ok) umma_commit(b_acc);
@@ -803,13 +807,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                     dd[e] = pack_bf16x2(dv[0], dv[1]);
                 }
             }
-            // the previous step's product must be done reading the dS tile
+            // the previous step's product must be done reading the dS columns
             if (j > 0 && !warp_wait(b_dsfree, (j - 1) & 1, abort_flag, p.err, lane)) {
                 ok = false;
                 break;
             }
-            st_row32_64(sDS, r, c0, dd);
-            fence_proxy_async_smem();
+            tc_fence_after();
+            tmem_st16(tDS + loff + (uint32_t)(c0 >> 1), dd);  // keys c0.. of the step
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_dsfull);
