@@ -102,33 +102,6 @@ __global__ void k_attn_D(float* Dv, const T* dout, const T* out, int B, int T_, 
     Dv[idx] = s;
 }
 
-// D for head size 64 in bf16: one thread per (row, head), 16-byte loads
-__global__ void k_attn_D64_bf16(float* Dv, const bf16* dout, const bf16* out, int B, int T_,
-                                int C, int H) {
-    gdc_wait();
-    gdc_launch_dependents();
-    long idx = blockIdx.x * (long)blockDim.x + threadIdx.x;  // (row, head), head fastest
-    if (idx >= (long)B * T_ * H) return;
-    int h = (int)(idx % H);
-    long row = idx / H;
-    int b = (int)(row / T_), t = (int)(row % T_);
-    const uint4* a = reinterpret_cast<const uint4*>(dout + row * C + h * 64);
-    const uint4* o = reinterpret_cast<const uint4*>(out + row * C + h * 64);
-    float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        uint4 x = a[k], y = o[k];
-        const __nv_bfloat162* xa = reinterpret_cast<const __nv_bfloat162*>(&x);
-        const __nv_bfloat162* ya = reinterpret_cast<const __nv_bfloat162*>(&y);
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            float2 u = __bfloat1622float2(xa[e]), v = __bfloat1622float2(ya[e]);
-            s = fmaf(u.x, v.x, s);
-            s = fmaf(u.y, v.y, s);
-        }
-    }
-    Dv[((size_t)b * H + h) * T_ + t] = s;
-}
 
 // dQ: one thread per query.
 template <typename T, int HD>
@@ -317,14 +290,8 @@ cudaError_t attention_backward(int act, void* dqkv, const void* dout, const void
                                const void* out, const float* lse, int B, int T_, int C, int H,
                                void* scratch, unsigned* err, cudaStream_t s) {
     float* Dv = (float*)scratch;
-    if (attention_tc_supported(act, B, T_, C, H, qkv)) {
-        long n = (long)B * H * T_;
-        launch_pdl(k_attn_D64_bf16, (int)((n + 255) / 256), 256, 0, s, Dv, (const bf16*)dout,
-                                                               (const bf16*)out, B, T_, C, H);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        return attention_backward_tc(dqkv, dout, qkv, lse, Dv, B, T_, C, H, err, s);
-    }
+    if (attention_tc_supported(act, B, T_, C, H, qkv))
+        return attention_backward_tc(dqkv, dout, qkv, out, lse, Dv, B, T_, C, H, err, s);
     if (act == ACT_BF16) {
         HD_DISPATCH(attn_bwd_hd, bf16, dqkv, dout, qkv, out, lse, B, T_, C, H, Dv, s)
     } else {

@@ -346,11 +346,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
 //   per key row forms P^T and dS^T (bf16, swizzled smem), then
 //   dV += P^T dO_i and dK += dS^T Q_i accumulate in TMEM (Q_i and dO_i tiles
 //   are read K-major for the first products and MN-major for the second).
-// k_attn_dq_tc: one CTA per (128-query tile, batch, head), visiting key tiles
-//   j <= query tile: S = Q K_j^T, dP = dO V_j^T, dS -> smem, dQ += dS K_j.
-// Each CTA owns its outputs: no atomics, deterministic.  TMEM: 512 columns
-// (one CTA per SM).
-// ---------------------------------------------------------------------------
+// k_attn_dq_tc (launched first): one CTA per (128-query tile, batch, head); it
+//   forms D of its queries from its dO and O tiles and writes it, then visits
+//   key tiles j <= query tile: S = Q K_j^T, dP = dO V_j^T, dS -> TMEM,
+//   dQ += dS K_j (dS read from TMEM as the A operand).
+// Each CTA owns its outputs: no atomics, deterministic.
 // The 128-row side of each kernel (keys in k_attn_dkv_tc, queries in
 // k_attn_dq_tc) is visited in steps of 64 on the other side, so every CTA
 // holds at most 256 TMEM columns and ~100 KB of shared memory: two CTAs share
@@ -362,7 +362,7 @@ constexpr int SUB_BYTES = SUB * 128;
 struct AttnBwdParams {
     int B, T, C, H, nqt, nsub;  // nsub = ceil(T / 64)
     const float* lse;  // [B,H,T] natural log
-    const float* Dv;   // [B,H,T]
+    float* Dv;         // [B,H,T] rowsum(dO o O): written by the dQ kernel, read by dK/dV
     bf16* dqkv;
     unsigned* err;
     float scale_log2;  // log2(e)/sqrt(hd)
@@ -381,7 +381,7 @@ __device__ __forceinline__ void st_row32_64(uint32_t tile, int r, int c0, const 
 }
 
 struct BwdMaps {
-    CUtensorMap qkv128, qkv64, do128, do64;  // boxes 64 x 128 rows / 64 x 64 rows
+    CUtensorMap qkv128, qkv64, do128, do64, o128;  // boxes 64 x 128 rows / 64 x 64 rows
 };
 
 // dK, dV: CTA = (128-key tile kt, batch, head); query steps of 64.
@@ -629,10 +629,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
 }
 
 // dQ: CTA = (128-query tile qt, batch, head); key steps of 64 through a ring of
-// E_NRING (K_j, V_j) slots; dS lives in TMEM.
+// E_NRING (K_j, V_j) slots; dS lives in TMEM.  The CTA also forms D =
+// rowsum(dO o O) of its queries (from its dO and O tiles) and writes it for
+// the dK/dV kernel, which runs after it.
 constexpr int E_NRING = 3;
-constexpr int E_Q = 0, E_DO = 16384, E_KV = 32768, E_BAR = E_KV + E_NRING * 2 * SUB_BYTES;
-constexpr int E_SMEM = E_BAR + 256 + 1024;
+constexpr int E_Q = 0, E_DO = 16384, E_O = 32768, E_KV = 49152,
+              E_BAR = E_KV + E_NRING * 2 * SUB_BYTES, E_DX = E_BAR + 256;
+constexpr int E_SMEM = E_DX + 1024 + 1024;
 
 __global__ void __launch_bounds__(BWD_THREADS, 2)
     k_attn_dq_tc(const __grid_constant__ BwdMaps maps, AttnBwdParams p) {
@@ -685,9 +688,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     if (warp == 0) {
         if (lane == 0) {
             const int ck = p.C + h * HD, cv = 2 * p.C + h * HD;
-            mbar_expect_tx(b_q, 2 * TILE_BYTES);
+            mbar_expect_tx(b_q, 3 * TILE_BYTES);
             tma_load_2d(sQ, &maps.qkv128, b_q, h * HD, row0 + qt * TILE);
             tma_load_2d(sDO, &maps.do128, b_q, h * HD, row0 + qt * TILE);
+            tma_load_2d(base + E_O, &maps.o128, b_q, h * HD, row0 + qt * TILE);
             int issued[E_NRING];
             for (int s = 0; s < E_NRING; s++) issued[s] = -1;
             for (int j = 0; j < nk; j++) {
@@ -765,8 +769,32 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
         const int c0 = hf * 32;
         const bool qlive = qi < p.T;
         const float lse2 = qlive ? p.lse[(size_t)bh * p.T + qi] * 1.4426950408889634f : 0.f;
-        const float Dq = qlive ? p.Dv[(size_t)bh * p.T + qi] : 0.f;
-        bool ok = true;
+        bool ok = warp_wait(b_q, 0, abort_flag, p.err, lane);
+        // D of this row: the half's 32 products from the swizzled dO and O
+        // tiles, then the two halves added in half order
+        float dpart = 0.f;
+        if (ok) {
+            const uint8_t* rdo = base_gen + E_DO + r * 128;
+            const uint8_t* ro = base_gen + E_O + r * 128;
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const int off = ((hf * 4 + c) ^ (r & 7)) << 4;
+                const uint4 a = *reinterpret_cast<const uint4*>(rdo + off);
+                const uint4 o = *reinterpret_cast<const uint4*>(ro + off);
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const float av = __uint_as_float((e & 1) ? (aw[e >> 1] & 0xffff0000u) : (aw[e >> 1] << 16));
+                    const float ov = __uint_as_float((e & 1) ? (ow[e >> 1] & 0xffff0000u) : (ow[e >> 1] << 16));
+                    dpart = fmaf(av, ov, dpart);
+                }
+            }
+        }
+        float* dx_s = reinterpret_cast<float*>(base_gen + E_DX);  // [2 halves][128 rows]
+        dx_s[hf * 128 + r] = dpart;
+        named_sync_softmax();
+        const float Dq = qlive ? dx_s[r] + dx_s[128 + r] : 0.f;
+        if (ok && hf == 0 && qlive) p.Dv[(size_t)bh * p.T + qi] = Dq;
         for (int j = 0; j < nk; j++) {
             if (!warp_wait(b_sfull, j & 1, abort_flag, p.err, lane)) {
                 ok = false;
@@ -873,8 +901,9 @@ static bool map_rows(CUtensorMap* m, const void* base, long width, long rows, in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const float* lse,
-                                  const float* Dv, int B, int T, int C, int H, unsigned* err,
+cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out,
+                                  const float* lse, float* Dv, int B, int T, int C, int H,
+                                  unsigned* err,
                                   cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
@@ -882,12 +911,14 @@ cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv,
         cudaFuncSetAttribute(k_attn_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, E_SMEM);
         attr = true;
     }
-    if (((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15)) return cudaErrorInvalidValue;
+    if (((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15) || ((uintptr_t)out & 15))
+        return cudaErrorInvalidValue;
     BwdMaps maps;
     const long rows = (long)B * T;
     if (!map_rows(&maps.qkv128, qkv, 3L * C, rows, 128) ||
         !map_rows(&maps.qkv64, qkv, 3L * C, rows, 64) ||
-        !map_rows(&maps.do128, dout, C, rows, 128) || !map_rows(&maps.do64, dout, C, rows, 64))
+        !map_rows(&maps.do128, dout, C, rows, 128) || !map_rows(&maps.do64, dout, C, rows, 64) ||
+        !map_rows(&maps.o128, out, C, rows, 128))
         return cudaErrorInvalidValue;
     AttnBwdParams p;
     p.B = B; p.T = T; p.C = C; p.H = H;
@@ -900,8 +931,9 @@ cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv,
     p.scale = 1.0f / sqrtf((float)HD);
     p.scale_log2 = 1.4426950408889634f * p.scale;
     dim3 grid(B * H, p.nqt);
-    launch_pdl(k_attn_dkv_tc, grid, BWD_THREADS, D_SMEM, s, maps, p);
+    // dQ first: it also writes D, which dK/dV reads
     launch_pdl(k_attn_dq_tc, grid, BWD_THREADS, E_SMEM, s, maps, p);
+    launch_pdl(k_attn_dkv_tc, grid, BWD_THREADS, D_SMEM, s, maps, p);
     return cudaGetLastError();
 }
 

@@ -133,9 +133,9 @@ cudaError_t attention_forward(int act, void* out, float* lse, const void* qkv, i
 bool attention_tc_supported(int act, int B, int T, int C, int H, const void* qkv);
 cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C,
                                  int H, unsigned* err, cudaStream_t s);
-cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const float* lse,
-                                  const float* Dv, int B, int T, int C, int H, unsigned* err,
-                                  cudaStream_t s);
+cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out,
+                                  const float* lse, float* Dv, int B, int T, int C, int H,
+                                  unsigned* err, cudaStream_t s);
 void* tc_encode_fn();
 size_t attention_backward_scratch(int B, int T, int H);
 // dqkv [B,T,3C] is overwritten
