@@ -601,9 +601,11 @@ __global__ void __launch_bounds__(256, 2)
     }
 }
 
-// outs[k][c] += sum_i part[i*ld + k*n0 + c] for column k*n0 + c < ncols, i in a
-// fixed order: thread row ty sums i = ty, ty+8, ..., then row 0 adds the 8
-// row sums in order.  32 consecutive columns per block (coalesced).
+// outs[k][c] += sum_i part[i*ld + k*n0 + c] for column k*n0 + c < ncols, in a
+// fixed order: thread row ty (of 8) sums the rows i = ty (mod 8) in four
+// interleaved chains (i = ty + 32q + {0, 8, 16, 24}) whose loads are in flight
+// together, adds the chains in order, then row 0 adds the 8 row sums in order.
+// 32 consecutive columns per block (coalesced).
 struct ColsumOut {
     float* p[3];
 };
@@ -612,12 +614,19 @@ __global__ void __launch_bounds__(256) k_colsum(ColsumOut outs, int n0, int ncol
     gdc_wait();
     gdc_launch_dependents();
     __shared__ float sh[8][33];
-    int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    int c = blockIdx.x * 32 + tx;
-    float a = 0.f;
-    if (c < ncols)
-        for (int i = ty; i < nparts; i += 8) a += part[(size_t)i * ld + c];
-    sh[ty][tx] = a;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + tx;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    if (c < ncols) {
+        for (int i = ty; i < nparts; i += 32) {
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) v[q] = i + 8 * q < nparts ? part[(size_t)(i + 8 * q) * ld + c] : 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; q++) a[q] += v[q];
+        }
+    }
+    sh[ty][tx] = (a[0] + a[1]) + (a[2] + a[3]);
     __syncthreads();
     if (ty == 0 && c < ncols) {
         float t = 0.f;
