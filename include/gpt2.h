@@ -62,7 +62,8 @@ enum {
     GPT2_ERR_STATE = -4,        /* call out of order (e.g. backward w/o forward)*/
     GPT2_ERR_TOKEN_RANGE = -5,  /* a token or target id outside [0, V)          */
     GPT2_ERR_NONFINITE = -6,    /* gradient norm not finite: update skipped     */
-    GPT2_ERR_TIMEOUT = -7       /* a bounded device-side wait ran out           */
+    GPT2_ERR_TIMEOUT = -7,      /* a bounded device-side wait ran out           */
+    GPT2_ERR_IO = -8            /* a checkpoint file could not be read/written  */
 };
 
 /* Bytes of device workspace a handle of this shape needs (0 if the shape is
@@ -143,6 +144,36 @@ int gpt2_get_opt_state(gpt2_t* g, float* h_m, float* h_v, int* h_step);
 /* AdamW first/second moments and the step count t (m, v: fp32, canonical
  * order, either may be NULL to leave it unchanged; step >= 0). */
 int gpt2_set_opt_state(gpt2_t* g, const float* h_m, const float* h_v, int step);
+/* ---- update skipping on loss / gradient-norm spikes ("Karpathy reproduces
+ * GPT-2 (1.6B) in llm.c", "Training": the flags -sl 5.0 -sg 5.0 skip the
+ * update on transient instabilities).  With the detector on, gpt2_adamw_step
+ * computes the step's mean micro-batch loss (the losses of the forwards
+ * followed by gpt2_backward since the last gpt2_zero_grad) and the gradient
+ * norm, their z-scores against the previous `window` steps ((x - mean)/std,
+ * population std; no z until `window` steps are recorded), and skips the
+ * update -- parameters, moments and step count unchanged -- when a z-score
+ * exceeds its threshold.  Every step's values are recorded, skipped or not.
+ * loss_z, grad_z <= 0 switch a criterion off; window 0 switches the detector
+ * off (the default); window 1 is rejected (GPT2_ERR_ARG).  Setting it clears
+ * the recorded window. */
+int gpt2_set_spike_skip(gpt2_t* g, float loss_z, float grad_z, int window);
+/* outcome of the last gpt2_adamw_step: skipped (0/1) and the two z-scores
+ * (NaN when the detector is off or its window is not yet full) */
+int gpt2_last_step_info(gpt2_t* g, int* skipped, float* z_loss, float* z_grad);
+
+/* ---- checkpoints: a file with the fp32 parameters, the AdamW moments and
+ * step count, and the spike detector's settings and window (this library's
+ * own format: an 88-byte header "GPT2B3CK", version 1, L H C V T mode,
+ * nparams, t, detector state; then params, m, v as fp32 in canonical order and
+ * the detector's two windows as float64).  A handle of the same L, H, C, V and
+ * T (any B, any mode) that loads it continues training bit for bit as the
+ * saving handle would have ("Karpathy reproduces GPT-2 (1.6B) in llm.c",
+ * "Training": -n saves checkpoints, -y 1 resumes bit-exactly).  Errors:
+ * GPT2_ERR_IO (open/read/write, not a checkpoint, truncated), GPT2_ERR_ARG (the
+ * checkpoint's shapes differ from the handle's). */
+int gpt2_save_checkpoint(gpt2_t* g, const char* path);
+int gpt2_load_checkpoint(gpt2_t* g, const char* path);
+
 /* logits [B,T,V] of the last forward WITHOUT targets (real columns only) */
 int gpt2_get_logits(gpt2_t* g, float* h_buf);
 int gpt2_get_loss(gpt2_t* g, float* h_loss);        /* mean loss, last fwd  */

@@ -79,6 +79,15 @@ struct gpt2 {
     int n_accum, t, have_targets, logits_valid, have_fwd;
     std::string last_err;
 
+    // update skipping on loss / gradient-norm spikes: z-scores of this step's
+    // mean loss and gradient norm against the previous sk_window steps
+    float sk_loss_z = 0.f, sk_grad_z = 0.f;  // thresholds (<= 0: criterion off)
+    int sk_window = 0;                       // 0: detector off
+    int sk_count = 0, sk_pos = 0;            // values recorded (<= window), ring position
+    std::vector<double> sk_loss_hist, sk_grad_hist;
+    int last_skipped = 0;
+    float last_zl = NAN, last_zg = NAN;
+
     long long launches;  // kernels launched by this handle
     unsigned prof_mask;  // classes timed with events
     bool prof_on, prof_cur;
@@ -619,6 +628,11 @@ extern "C" int gpt2_backward(gpt2_t* g) {
     LAUNCH(K_EMB_BWD, 9, 0, as * bt * c + 8.0 * T * c,
            encoder_backward(g->act, grad_tensor(g, P_WTE, 0), grad_tensor(g, P_WPE, 0), dres,
                             g->tok, B, T, C, Vp, g->scratch, g->stream));
+    if (g->sk_window > 0) {
+        // running sum of the micro-batch losses (loss[1]) for the spike detector
+        g->launches += 1;
+        CK(accumulate_scalar(g->loss + 1, g->loss, g->stream));
+    }
     g->n_accum++;
     g->have_fwd = 0;
     return GPT2_OK;
@@ -632,10 +646,26 @@ extern "C" int gpt2_zero_grad(gpt2_t* g) {
     cudaSetDevice(g->device);
     prof_begin(g, K_ZERO, 0, 4.0 * g->nparams);
     cudaError_t e = cudaMemsetAsync(g->grads, 0, g->nparams * 4, g->stream);
+    if (e == cudaSuccess && g->sk_window > 0) e = cudaMemsetAsync(g->loss + 1, 0, 4, g->stream);
     prof_end(g);
     if (e) return fail(g, GPT2_ERR_CUDA, "zero_grad: %s", cudaGetErrorString(e));
     g->n_accum = 0;
     return GPT2_OK;
+}
+
+// z-score of x against the recorded window: (x - mean) / std with the
+// population std of the window's values; NaN until the window is full; with a
+// zero std, 0 for x == mean and +-infinity otherwise
+static float spike_z(const gpt2* g, const std::vector<double>& hist, double x) {
+    if (g->sk_count < g->sk_window) return NAN;
+    double mean = 0.0;
+    for (int i = 0; i < g->sk_window; i++) mean += hist[i];
+    mean /= g->sk_window;
+    double var = 0.0;
+    for (int i = 0; i < g->sk_window; i++) var += (hist[i] - mean) * (hist[i] - mean);
+    const double sd = sqrt(var / g->sk_window);
+    if (sd == 0.0) return x == mean ? 0.f : (x > mean ? INFINITY : -INFINITY);
+    return (float)((x - mean) / sd);
 }
 
 extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float eps, float wd,
@@ -656,15 +686,171 @@ extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float ep
     a.dec_lo[2] = o[P_PROJW];   a.dec_hi[2] = o[P_PROJB];
     a.dec_lo[3] = o[P_FCW];     a.dec_hi[3] = o[P_FCB];
     a.dec_lo[4] = o[P_FCPROJW]; a.dec_hi[4] = o[P_FCPROJB];
-    LAUNCH(K_ADAM, 3, 0, 34.0 * g->nparams + (g->act == ACT_BF16 ? 2.0 * g->nparams : 0.0),
-           adamw_step(g->master, g->m, g->v, g->grads, g->act == ACT_BF16 ? g->pc : nullptr,
-                      g->nparams, a, g->adam_state, g->scratch, g->stream));
-    float st[3];
+    void* wb = g->act == ACT_BF16 ? g->pc : nullptr;
+    const double ad_bytes = 34.0 * g->nparams + (g->act == ACT_BF16 ? 2.0 * g->nparams : 0.0);
+    g->last_skipped = 0;
+    g->last_zl = g->last_zg = NAN;
+    if (g->sk_window <= 0) {
+        LAUNCH(K_ADAM, 3, 0, ad_bytes,
+               adamw_step(g->master, g->m, g->v, g->grads, wb, g->nparams, a, g->adam_state,
+                          g->scratch, g->stream));
+        float st[3];
+        CK(cudaMemcpyAsync(st, g->adam_state, 12, cudaMemcpyDeviceToHost, g->stream));
+        RUN(check_dev_err(g));
+        if (h_grad_norm) *h_grad_norm = st[0];
+        if (st[2] == 0.f)
+            return fail(g, GPT2_ERR_NONFINITE, "gradient norm is not finite (%g)", st[0]);
+        g->t = t;
+        return GPT2_OK;
+    }
+    // spike detector on: the norm pass, then the decision on the host, then
+    // the update (or not)
+    LAUNCH(K_ADAM, 2, 0, 4.0 * g->nparams,
+           adamw_norm(g->grads, g->nparams, a, g->adam_state, g->scratch, g->stream));
+    float st[3], lsum = 0.f;
     CK(cudaMemcpyAsync(st, g->adam_state, 12, cudaMemcpyDeviceToHost, g->stream));
-    RUN(check_dev_err(g));
+    CK(cudaMemcpyAsync(&lsum, g->loss + 1, 4, cudaMemcpyDeviceToHost, g->stream));
+    RUN(check_dev_err(g));  // synchronises the stream
     if (h_grad_norm) *h_grad_norm = st[0];
+    const double step_loss = (double)lsum / g->n_accum, norm = st[0];
+    g->last_zl = spike_z(g, g->sk_loss_hist, step_loss);
+    g->last_zg = spike_z(g, g->sk_grad_hist, norm);
+    const bool spike = (g->sk_loss_z > 0.f && g->last_zl > g->sk_loss_z) ||
+                       (g->sk_grad_z > 0.f && g->last_zg > g->sk_grad_z);
+    // every step's values enter the window, skipped or not
+    g->sk_loss_hist[g->sk_pos] = step_loss;
+    g->sk_grad_hist[g->sk_pos] = norm;
+    g->sk_pos = (g->sk_pos + 1) % g->sk_window;
+    if (g->sk_count < g->sk_window) g->sk_count++;
     if (st[2] == 0.f) return fail(g, GPT2_ERR_NONFINITE, "gradient norm is not finite (%g)", st[0]);
+    if (spike) {
+        g->last_skipped = 1;  // parameters, moments and the step count unchanged
+        return GPT2_OK;
+    }
+    LAUNCH(K_ADAM, 1, 0, ad_bytes - 4.0 * g->nparams,
+           adamw_update(g->master, g->m, g->v, g->grads, wb, g->nparams, a, g->adam_state,
+                        g->stream));
     g->t = t;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_set_spike_skip(gpt2_t* g, float loss_z, float grad_z, int window) {
+    if (!g || window < 0 || window == 1 || window > (1 << 20)) return GPT2_ERR_ARG;
+    g->sk_loss_z = loss_z;
+    g->sk_grad_z = grad_z;
+    g->sk_window = window;
+    g->sk_count = g->sk_pos = 0;
+    g->sk_loss_hist.assign(window, 0.0);
+    g->sk_grad_hist.assign(window, 0.0);
+    if (window > 0) {
+        cudaSetDevice(g->device);
+        CK(cudaMemsetAsync(g->loss + 1, 0, 4, g->stream));  // no partial sum carried in
+    }
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_last_step_info(gpt2_t* g, int* skipped, float* z_loss, float* z_grad) {
+    if (!g) return GPT2_ERR_ARG;
+    if (skipped) *skipped = g->last_skipped;
+    if (z_loss) *z_loss = g->last_zl;
+    if (z_grad) *z_grad = g->last_zg;
+    return GPT2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// checkpoints: fp32 parameters, AdamW moments and step count, and the spike
+// detector's window, so that a run resumed from a checkpoint continues bit for
+// bit as if it had not stopped
+// ---------------------------------------------------------------------------
+struct CkptHeader {  // 88 bytes, little-endian, no implicit padding
+    char magic[8];  // "GPT2B3CK"
+    uint32_t version;
+    int32_t L, H, C, V, T, mode;
+    uint32_t pad0;
+    uint64_t nparams;
+    int32_t t;
+    int32_t sk_window, sk_count, sk_pos;
+    float sk_loss_z, sk_grad_z;
+    uint32_t reserved[4];
+};
+static_assert(sizeof(CkptHeader) == 88, "checkpoint header layout");
+static const char kCkptMagic[8] = {'G', 'P', 'T', '2', 'B', '3', 'C', 'K'};
+
+extern "C" int gpt2_save_checkpoint(gpt2_t* g, const char* path) {
+    if (!g || !path) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    CkptHeader hd;
+    memset(&hd, 0, sizeof hd);
+    memcpy(hd.magic, kCkptMagic, 8);
+    hd.version = 1;
+    hd.L = g->L; hd.H = g->H; hd.C = g->C; hd.V = g->V; hd.T = g->T; hd.mode = g->mode;
+    hd.nparams = g->nparams;
+    hd.t = g->t;
+    hd.sk_window = g->sk_window; hd.sk_count = g->sk_count; hd.sk_pos = g->sk_pos;
+    hd.sk_loss_z = g->sk_loss_z; hd.sk_grad_z = g->sk_grad_z;
+    FILE* f = fopen(path, "wb");
+    if (!f) return fail(g, GPT2_ERR_IO, "cannot open %s for writing", path);
+    bool ok = fwrite(&hd, sizeof hd, 1, f) == 1;
+    std::vector<float> buf(ok ? g->nparams : 0);
+    const float* src[3] = {g->master, g->m, g->v};
+    for (int k = 0; ok && k < 3; k++) {
+        if (cudaMemcpy(buf.data(), src[k], g->nparams * 4, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            fclose(f);
+            return fail(g, GPT2_ERR_CUDA, "checkpoint: device read failed");
+        }
+        ok = fwrite(buf.data(), 4, g->nparams, f) == g->nparams;
+    }
+    if (ok && g->sk_window > 0)
+        ok = fwrite(g->sk_loss_hist.data(), 8, g->sk_window, f) == (size_t)g->sk_window &&
+             fwrite(g->sk_grad_hist.data(), 8, g->sk_window, f) == (size_t)g->sk_window;
+    if (fclose(f) != 0) ok = false;
+    return ok ? GPT2_OK : fail(g, GPT2_ERR_IO, "write to %s failed", path);
+}
+
+extern "C" int gpt2_load_checkpoint(gpt2_t* g, const char* path) {
+    if (!g || !path) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    FILE* f = fopen(path, "rb");
+    if (!f) return fail(g, GPT2_ERR_IO, "cannot open %s", path);
+    CkptHeader hd;
+    if (fread(&hd, sizeof hd, 1, f) != 1 || memcmp(hd.magic, kCkptMagic, 8) != 0 ||
+        hd.version != 1) {
+        fclose(f);
+        return fail(g, GPT2_ERR_IO, "%s is not a checkpoint of this library", path);
+    }
+    if (hd.L != g->L || hd.H != g->H || hd.C != g->C || hd.V != g->V || hd.T != g->T ||
+        hd.nparams != g->nparams || hd.t < 0 || hd.sk_window < 0 || hd.sk_window == 1 ||
+        hd.sk_window > (1 << 20) || hd.sk_count < 0 || hd.sk_count > hd.sk_window ||
+        hd.sk_pos < 0 || (hd.sk_window > 0 && hd.sk_pos >= hd.sk_window)) {
+        fclose(f);
+        return fail(g, GPT2_ERR_ARG, "checkpoint %s (L=%d H=%d C=%d V=%d T=%d) does not fit this model",
+                    path, hd.L, hd.H, hd.C, hd.V, hd.T);
+    }
+    std::vector<float> buf(g->nparams);
+    float* dst[3] = {g->master, g->m, g->v};
+    bool ok = true;
+    for (int k = 0; ok && k < 3; k++) {
+        ok = fread(buf.data(), 4, g->nparams, f) == g->nparams;
+        if (ok && cudaMemcpy(dst[k], buf.data(), g->nparams * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+            fclose(f);
+            return fail(g, GPT2_ERR_CUDA, "checkpoint: device write failed");
+        }
+    }
+    std::vector<double> lh(hd.sk_window), gh(hd.sk_window);
+    if (ok && hd.sk_window > 0)
+        ok = fread(lh.data(), 8, hd.sk_window, f) == (size_t)hd.sk_window &&
+             fread(gh.data(), 8, hd.sk_window, f) == (size_t)hd.sk_window;
+    fclose(f);
+    if (!ok) return fail(g, GPT2_ERR_IO, "%s is truncated", path);
+    if (g->act == ACT_BF16) CK(cast_to_bf16(g->pc, g->master, g->nparams, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    g->t = hd.t;
+    g->sk_window = hd.sk_window; g->sk_count = hd.sk_count; g->sk_pos = hd.sk_pos;
+    g->sk_loss_z = hd.sk_loss_z; g->sk_grad_z = hd.sk_grad_z;
+    g->sk_loss_hist = lh;
+    g->sk_grad_hist = gh;
+    g->last_skipped = 0;
+    g->last_zl = g->last_zg = NAN;
     return GPT2_OK;
 }
 

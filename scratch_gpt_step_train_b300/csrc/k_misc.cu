@@ -1616,12 +1616,33 @@ __global__ void __launch_bounds__(256) k_adam(float* w, float* m, float* v, cons
 
 size_t adamw_scratch() { return ADAM_NB * sizeof(double); }
 
-cudaError_t adamw_step(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
-                       const AdamArgs& a, float* state, void* scratch, cudaStream_t s) {
+cudaError_t adamw_norm(const float* g, size_t n, const AdamArgs& a, float* state, void* scratch,
+                       cudaStream_t s) {
     double* part = (double*)scratch;
     launch_pdl(k_sumsq, ADAM_NB, 256, 0, s, g, n, part);
     launch_pdl(k_adam_norm, 1, 1024, 0, s, part, state, a.inv_accum, a.clip);
+    return cudaGetLastError();
+}
+cudaError_t adamw_update(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
+                         const AdamArgs& a, const float* state, cudaStream_t s) {
     launch_pdl(k_adam, 148 * 8, 256, 0, s, w, m, v, g, (bf16*)wbf16, n, a, state);
+    return cudaGetLastError();
+}
+cudaError_t adamw_step(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
+                       const AdamArgs& a, float* state, void* scratch, cudaStream_t s) {
+    cudaError_t e = adamw_norm(g, n, a, state, scratch, s);
+    if (e != cudaSuccess) return e;
+    return adamw_update(w, m, v, g, wbf16, n, a, state, s);
+}
+
+// acc[0] += x[0] (the running sum of the micro-batch losses of a step)
+__global__ void k_accum1(float* acc, const float* x) {
+    gdc_wait();
+    gdc_launch_dependents();
+    if (threadIdx.x == 0) acc[0] += x[0];
+}
+cudaError_t accumulate_scalar(float* acc, const float* x, cudaStream_t s) {
+    launch_pdl(k_accum1, 1, 32, 0, s, acc, x);
     return cudaGetLastError();
 }
 

@@ -100,6 +100,13 @@ size_t adamw_scratch();
 // state[0] = norm, state[1] = total gradient scale, state[2] = finite flag
 cudaError_t adamw_step(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
                        const AdamArgs& a, float* state, void* scratch, cudaStream_t s);
+// the two halves of adamw_step: the norm pass (fills state) and the update
+cudaError_t adamw_norm(const float* g, size_t n, const AdamArgs& a, float* state, void* scratch,
+                       cudaStream_t s);
+cudaError_t adamw_update(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
+                         const AdamArgs& a, const float* state, cudaStream_t s);
+// acc[0] += x[0] on the device
+cudaError_t accumulate_scalar(float* acc, const float* x, cudaStream_t s);
 
 // ---- SIMT matmul (fp32 FFMA) ----------------------------------------------
 enum Epi {

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libgpt2b300.so")
 FP32, BF16 = 0, 1
 ERRORS = {0: "OK", -1: "GPT2_ERR_ARG", -2: "GPT2_ERR_CUDA", -3: "GPT2_ERR_OOM",
           -4: "GPT2_ERR_STATE", -5: "GPT2_ERR_TOKEN_RANGE", -6: "GPT2_ERR_NONFINITE",
-          -7: "GPT2_ERR_TIMEOUT"}
+          -7: "GPT2_ERR_TIMEOUT", -8: "GPT2_ERR_IO"}
 
 # name -> (restype, argtypes); every function declared in include/gpt2.h
 _vp, _i, _f, _sz = ct.c_void_p, ct.c_int, ct.c_float, ct.c_size_t
@@ -44,6 +44,10 @@ SIGNATURES = {
     "gpt2_get_logits": (_i, [_vp, _pf]),
     "gpt2_get_loss": (_i, [_vp, _pf]),
     "gpt2_get_losses": (_i, [_vp, _pf]),
+    "gpt2_set_spike_skip": (_i, [_vp, _f, _f, _i]),
+    "gpt2_last_step_info": (_i, [_vp, _pi, _pf, _pf]),
+    "gpt2_save_checkpoint": (_i, [_vp, ct.c_char_p]),
+    "gpt2_load_checkpoint": (_i, [_vp, ct.c_char_p]),
     "gpt2_prof_enable": (_i, [_vp, ct.c_uint]),
     "gpt2_launch_count": (ct.c_longlong, [_vp]),
     "gpt2_prof_reset": (_i, [_vp]),
@@ -211,6 +215,26 @@ class GPT2:
         v = np.ascontiguousarray(v, dtype=np.float32)
         assert m.size == self.n and v.size == self.n
         self._ck(self._lib.gpt2_set_opt_state(self.h, _fptr(m), _fptr(v), int(step)))
+
+    def set_spike_skip(self, loss_z=5.0, grad_z=5.0, window=128):
+        """Skip the update when the step's mean loss or gradient norm has a
+        z-score above its threshold against the previous `window` steps
+        (window 0: off)."""
+        self._ck(self._lib.gpt2_set_spike_skip(self.h, float(loss_z), float(grad_z), int(window)))
+
+    def last_step_info(self):
+        """(skipped, z_loss, z_grad) of the last adamw_step"""
+        sk = ct.c_int(0)
+        zl = ct.c_float(0.0)
+        zg = ct.c_float(0.0)
+        self._ck(self._lib.gpt2_last_step_info(self.h, ct.byref(sk), ct.byref(zl), ct.byref(zg)))
+        return bool(sk.value), zl.value, zg.value
+
+    def save_checkpoint(self, path):
+        self._ck(self._lib.gpt2_save_checkpoint(self.h, os.fsencode(path)))
+
+    def load_checkpoint(self, path):
+        self._ck(self._lib.gpt2_load_checkpoint(self.h, os.fsencode(path)))
 
     def get_logits(self):
         out = np.empty((self.B, self.T, self.V), np.float32)
