@@ -53,6 +53,19 @@ typedef struct gpt2 gpt2_t;
  *             softmax, loss.  This is the mixed-precision training mode of
  *             "Karpathy's llm.c ...", section "Code anatomy", item 3. */
 enum { GPT2_FP32 = 0, GPT2_BF16 = 1 };
+/* Activation recompute, OR-ed into `mode` ("Karpathy reproduces GPT-2 (1.6B)
+ * in llm.c", "Parameter guide" -r 1 / -r 2: recompute in the backward to save
+ * memory).
+ *  GPT2_RECOMPUTE_GELU: the MLP keeps only x = ln2 Wfc^T + b per layer; gelu(x)
+ *    lives in one buffer shared by all layers, filled by an elementwise GELU
+ *    kernel in the forward and refilled by the same kernel in the backward
+ *    (bit-identical), and the fcproj input gradient takes gelu'(x) from x.
+ *    Saves L-1 activations of B*T*4C.
+ *  GPT2_RECOMPUTE_LN (implies the above): the two LayerNorm outputs of each
+ *    layer are not kept either; the backward reruns the LayerNorm forward on
+ *    the kept residual stream (bit-identical).  Saves 2(L-1) of B*T*C more.
+ * In fp32 mode a recompute run is bit for bit the same as a run without. */
+enum { GPT2_RECOMPUTE_GELU = 0x10, GPT2_RECOMPUTE_LN = 0x20 };
 
 enum {
     GPT2_OK = 0,

@@ -119,6 +119,13 @@ int gpt2k_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx,
 int gpt2k_crossentropy(int dtype, void* logits, float* losses, const int32_t* tgt, int N, int V,
                        int Vp, float dloss, unsigned* err, void* stream);
 
+/* Elementwise tanh-form GELU, out[i] = gelu(in[i]) for i < n, the formula of
+ * the fp32 fused epilogue (sigmoid form, see epi 5): the recompute path of the
+ * MLP ("Karpathy reproduces GPT-2 (1.6B) in llm.c", "Parameter guide" -r 1)
+ * runs it in the forward and again in the backward on the same stored input,
+ * so both results are identical.  out and in may be the same buffer. */
+int gpt2k_gelu_forward(int dtype, void* out, const void* in, size_t n, void* stream);
+
 /* Bias gradient: db[o] += sum_n dout[n,o] (fixed summation order). */
 size_t gpt2k_bias_grad_scratch_bytes(int N, int OC);
 int gpt2k_bias_grad(int dtype, float* db, const void* dout, int N, int OC, void* scratch,

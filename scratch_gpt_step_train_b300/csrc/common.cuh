@@ -67,26 +67,25 @@ __device__ __forceinline__ void store_vec_f(T* dst, const float* src) {
 // evaluated through the exact identity 0.5 (1 + tanh(u)) = 1 / (1 + e^{-2u}),
 // which keeps full relative precision in the negative tail where 1 + tanh(u)
 // would cancel in fp32 (and 1 - tanh(u)^2 = 4 s (1 - s) with s that sigmoid).
-// gelu(x) and gelu'(x) together, sharing the sigmoid
+// gelu(x) and gelu'(x) together, sharing the sigmoid.  Every operation is an
+// explicitly rounded intrinsic (never contracted into an FMA differently by
+// the compiler), so all kernels that call it get the same bits for the same x.
 __device__ __forceinline__ void gelu_and_grad_f(float x, float& g, float& dg) {
     const float k = 0.7978845608028654f;
-    const float x2 = x * x;
-    const float u = k * (x + 0.044715f * x2 * x);
-    const float sg = 1.0f / (1.0f + expf(-2.0f * u));
-    const float du = k * (1.0f + 3.0f * 0.044715f * x2);
-    g = x * sg;
-    dg = sg + 2.0f * x * sg * (1.0f - sg) * du;
+    const float x2 = __fmul_rn(x, x);
+    const float u = __fmul_rn(k, __fmaf_rn(__fmul_rn(0.044715f, x2), x, x));
+    const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(__fmul_rn(-2.0f, u))));
+    const float du = __fmul_rn(k, __fmaf_rn(3.0f * 0.044715f, x2, 1.0f));
+    g = __fmul_rn(x, sg);
+    dg = __fmaf_rn(__fmul_rn(__fmul_rn(__fmul_rn(2.0f, x), sg), __fsub_rn(1.0f, sg)), du, sg);
 }
 __device__ __forceinline__ float gelu_f(float x) {
-    const float k = 0.7978845608028654f;  // sqrt(2/pi)
-    float u = k * (x + 0.044715f * x * x * x);
-    return x / (1.0f + expf(-2.0f * u));
+    float g, dg;
+    gelu_and_grad_f(x, g, dg);
+    return g;
 }
 __device__ __forceinline__ float gelu_grad_f(float x) {
-    const float k = 0.7978845608028654f;
-    float x2 = x * x;
-    float u = k * (x + 0.044715f * x2 * x);
-    float sg = 1.0f / (1.0f + expf(-2.0f * u));
-    float du = k * (1.0f + 3.0f * 0.044715f * x2);
-    return sg + 2.0f * x * sg * (1.0f - sg) * du;
+    float g, dg;
+    gelu_and_grad_f(x, g, dg);
+    return dg;
 }

@@ -34,7 +34,7 @@ enum {
     K_QKV_DX, K_PROJ_DX, K_FC_DX, K_FCPROJ_DX, K_CLS_DX,
     K_QKV_DW, K_PROJ_DW, K_FC_DW, K_FCPROJ_DW, K_CLS_DW,
     K_ATTN_FWD, K_ATTN_BWD, K_LN_FWD, K_LN_BWD, K_XENT, K_EMB_FWD, K_EMB_BWD, K_BIAS, K_ADAM,
-    K_ZERO, K_NCLASS
+    K_ZERO, K_RECOMP, K_NCLASS
 };
 static const char* kClassNames[K_NCLASS] = {
     "matmul_qkv_fwd", "matmul_proj_fwd", "matmul_fc_fwd", "matmul_fcproj_fwd",
@@ -42,7 +42,7 @@ static const char* kClassNames[K_NCLASS] = {
     "matmul_fcproj_dx", "matmul_classifier_dx", "matmul_qkv_dw", "matmul_proj_dw",
     "matmul_fc_dw", "matmul_fcproj_dw", "matmul_classifier_dw", "attention_fwd",
     "attention_bwd", "layernorm_fwd", "layernorm_bwd", "crossentropy", "embedding_fwd",
-    "embedding_bwd", "bias_grad", "adamw", "zero_grad"};
+    "embedding_bwd", "bias_grad", "adamw", "zero_grad", "recompute"};
 
 struct ProfRec {
     int cls;
@@ -52,6 +52,7 @@ struct ProfRec {
 
 struct gpt2 {
     int L, H, C, V, Vp, T, B, mode, act;
+    int recompute;  // 0: keep all activations; 1: GELU output recomputed; 2: and LN outputs
     size_t BT;
     ParamLayout lay;
     size_t nparams;
@@ -190,13 +191,15 @@ static void plan(gpt2* g, char* base, size_t* total) {
     g->v = (float*)p.take(N * 4);
     g->pc = g->act == ACT_BF16 ? p.take(N * 2) : (void*)g->master;
     g->encoded = p.take(BT * C * as);
-    g->ln1 = p.take(L * BT * C * as);
+    // with recompute, one layer's buffer serves every layer (refilled when needed)
+    const size_t Lln = g->recompute >= 2 ? 1 : L, Lg = g->recompute >= 1 ? 1 : L;
+    g->ln1 = p.take(Lln * BT * C * as);
     g->qkv = p.take(L * BT * 3 * C * as);
     g->atty = p.take(L * BT * C * as);
     g->x1 = p.take(L * BT * C * as);
-    g->ln2 = p.take(L * BT * C * as);
+    g->ln2 = p.take(Lln * BT * C * as);
     g->fch = p.take(L * BT * 4 * C * as);
-    g->fchg = p.take(L * BT * 4 * C * as);
+    g->fchg = p.take(Lg * BT * 4 * C * as);
     g->x2 = p.take(L * BT * C * as);
     g->lnf = p.take(BT * C * as);
     g->logits = p.take(BT * (size_t)g->Vp * as);
@@ -228,6 +231,8 @@ static bool shape_ok(int L, int H, int C, int V, int T, int B, int mode) {
     if (C % H) return false;
     int hd = C / H;
     if (hd != 8 && hd != 16 && hd != 32 && hd != 64 && hd != 128) return false;
+    if (mode & ~(0xF | GPT2_RECOMPUTE_GELU | GPT2_RECOMPUTE_LN)) return false;
+    mode &= 0xF;
     if (mode != GPT2_FP32 && mode != GPT2_BF16) return false;
     if (mode == GPT2_BF16 && C % 8) return false;
     if ((long)B * T > (1L << 30) / 4) return false;
@@ -240,7 +245,8 @@ extern "C" size_t gpt2_workspace_bytes(int L, int H, int C, int V, int T, int B,
     if (!shape_ok(L, H, C, V, T, B, mode)) return 0;
     gpt2 tmp;
     tmp.L = L; tmp.H = H; tmp.C = C; tmp.V = V; tmp.T = T; tmp.B = B; tmp.mode = mode;
-    tmp.act = mode == GPT2_BF16 ? ACT_BF16 : ACT_F32;
+    tmp.act = (mode & 0xF) == GPT2_BF16 ? ACT_BF16 : ACT_F32;
+    tmp.recompute = (mode & GPT2_RECOMPUTE_LN) ? 2 : ((mode & GPT2_RECOMPUTE_GELU) ? 1 : 0);
     tmp.Vp = ((V + 127) / 128) * 128;
     tmp.BT = (size_t)B * T;
     make_layout(&tmp.lay, L, C, V, T);
@@ -260,7 +266,8 @@ extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int 
     if (!shape_ok(L, H, C, V, T, B, mode)) return GPT2_ERR_ARG;
     gpt2* g = new gpt2();
     g->L = L; g->H = H; g->C = C; g->V = V; g->T = T; g->B = B; g->mode = mode;
-    g->act = mode == GPT2_BF16 ? ACT_BF16 : ACT_F32;
+    g->act = (mode & 0xF) == GPT2_BF16 ? ACT_BF16 : ACT_F32;
+    g->recompute = (mode & GPT2_RECOMPUTE_LN) ? 2 : ((mode & GPT2_RECOMPUTE_GELU) ? 1 : 0);
     g->Vp = ((V + 127) / 128) * 128;
     g->BT = (size_t)B * T;
     make_layout(&g->lay, L, C, V, T);
@@ -447,14 +454,15 @@ static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
                            pc_tensor(g, P_WPE, 0), B, T, C, g->V, g->err, g->stream));
     const void* resid = g->encoded;
     double ln_bytes = as * 2.0 * bt * c + 8.0 * bt;
+    const int lln = g->recompute >= 2 ? 0 : 1, lg = g->recompute >= 1 ? 0 : 1;
     for (int l = 0; l < L; l++) {
-        void* ln1 = act_at(g, g->ln1, bt * c, l);
+        void* ln1 = act_at(g, g->ln1, bt * c, l * lln);
         void* qkv = act_at(g, g->qkv, bt * 3 * c, l);
         void* atty = act_at(g, g->atty, bt * c, l);
         void* x1 = act_at(g, g->x1, bt * c, l);
-        void* ln2 = act_at(g, g->ln2, bt * c, l);
+        void* ln2 = act_at(g, g->ln2, bt * c, l * lln);
         void* fch = act_at(g, g->fch, bt * 4 * c, l);
-        void* fchg = act_at(g, g->fchg, bt * 4 * c, l);
+        void* fchg = act_at(g, g->fchg, bt * 4 * c, l * lg);
         void* x2 = act_at(g, g->x2, bt * c, l);
         float* lse = g->lse + (size_t)l * B * H * T;
         LAUNCH(K_LN_FWD, 1, 0, ln_bytes,
@@ -478,11 +486,22 @@ static int forward_impl(gpt2* g, bool with_targets, float* h_loss) {
                layernorm_forward(g->act, ln2, g->ln2_mean + l * bt, g->ln2_rstd + l * bt, x1,
                                  pc_tensor(g, P_LN2W, l), pc_tensor(g, P_LN2B, l), BT, C,
                                  g->stream));
-        d = gd(BT, 4 * C, C, ln2, C, 1, pc_tensor(g, P_FCW, l), C, 1, fchg, 4 * C, EPI_GELU_D);
-        d.bias = pc_tensor(g, P_FCB, l);
-        d.aux = fch;
-        d.ldx = 4 * C;
-        RUN(mm(g, K_FC_FWD, d));
+        if (g->recompute >= 1) {
+            // keep x = ln2 Wfc^T + b; gelu(x) goes to the shared buffer and is
+            // recomputed from x by the same kernel in the backward
+            d = gd(BT, 4 * C, C, ln2, C, 1, pc_tensor(g, P_FCW, l), C, 1, fch, 4 * C, EPI_STORE);
+            d.bias = pc_tensor(g, P_FCB, l);
+            RUN(mm(g, K_FC_FWD, d));
+            LAUNCH(K_RECOMP, 1, 0, as * 8.0 * bt * c,
+                   gelu_forward(g->act, fchg, fch, bt * 4 * c, g->stream));
+        } else {
+            d = gd(BT, 4 * C, C, ln2, C, 1, pc_tensor(g, P_FCW, l), C, 1, fchg, 4 * C,
+                   EPI_GELU_D);
+            d.bias = pc_tensor(g, P_FCB, l);
+            d.aux = fch;
+            d.ldx = 4 * C;
+            RUN(mm(g, K_FC_FWD, d));
+        }
         d = gd(BT, C, 4 * C, fchg, 4 * C, 1, pc_tensor(g, P_FCPROJW, l), 4 * C, 1, x2, C,
                EPI_RESID);
         d.bias = pc_tensor(g, P_FCPROJB, l);
@@ -567,25 +586,37 @@ extern "C" int gpt2_backward(gpt2_t* g) {
                               L > 0 ? grad_tensor(g, P_FCPROJB, L - 1) : nullptr, g->dln, xL,
                               pc_tensor(g, P_LNFW, 0), g->lnf_mean, g->lnf_rstd, BT, C, false,
                               g->scratch, g->stream));
+    const int lln = g->recompute >= 2 ? 0 : 1, lg = g->recompute >= 1 ? 0 : 1;
+    const double ln_bytes = as * 2.0 * bt * c + 8.0 * bt;
     for (int l = L - 1; l >= 0; l--) {
         const void* rin = l == 0 ? g->encoded : act_at(g, g->x2, bt * c, l - 1);
-        void* ln1 = act_at(g, g->ln1, bt * c, l);
+        void* ln1 = act_at(g, g->ln1, bt * c, l * lln);
         void* qkv = act_at(g, g->qkv, bt * 3 * c, l);
         void* atty = act_at(g, g->atty, bt * c, l);
         void* x1 = act_at(g, g->x1, bt * c, l);
-        void* ln2 = act_at(g, g->ln2, bt * c, l);
+        void* ln2 = act_at(g, g->ln2, bt * c, l * lln);
         void* fch = act_at(g, g->fch, bt * 4 * c, l);
-        void* fchg = act_at(g, g->fchg, bt * 4 * c, l);
+        void* fchg = act_at(g, g->fchg, bt * 4 * c, l * lg);
         float* lse = g->lse + (size_t)l * B * H * T;
         // MLP: x2 = x1 + fcproj(gelu(fc(ln2(x1))))
+        if (g->recompute >= 1)  // gelu(x) again, by the forward's kernel, from the kept x
+            LAUNCH(K_RECOMP, 1, 0, as * 8.0 * bt * c,
+                   gelu_forward(g->act, fchg, fch, bt * 4 * c, g->stream));
         d = gd(C, 4 * C, BT, dres, C, 0, fchg, 4 * C, 0, grad_tensor(g, P_FCPROJW, l), 4 * C,
                EPI_ACCUM_F32);
         RUN(mm(g, K_FCPROJ_DW, d));
+        // dx of fcproj times gelu'(x): kept by the forward (epilogue MUL_AUX), or
+        // evaluated from the kept x (GELU_BWD) when the GELU output is recomputed
         d = gd(BT, 4 * C, C, dres, C, 1, pc_tensor(g, P_FCPROJW, l), 4 * C, 0, g->dbig, 4 * C,
-               EPI_MUL_AUX);
+               g->recompute >= 1 ? EPI_GELU_BWD : EPI_MUL_AUX);
         d.aux = fch;
         d.ldx = 4 * C;
         RUN(mm(g, K_FCPROJ_DX, d));
+        if (g->recompute >= 2)  // ln2(x1) again (the same kernel on the same input)
+            LAUNCH(K_RECOMP, 1, 0, ln_bytes,
+                   layernorm_forward(g->act, ln2, g->ln2_mean + l * bt, g->ln2_rstd + l * bt, x1,
+                                     pc_tensor(g, P_LN2W, l), pc_tensor(g, P_LN2B, l), BT, C,
+                                     g->stream));
         d = gd(4 * C, C, BT, g->dbig, 4 * C, 0, ln2, C, 0, grad_tensor(g, P_FCW, l), C,
                EPI_ACCUM_F32);
         RUN(mm(g, K_FC_DW, d));
@@ -606,9 +637,15 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         d = gd(BT, C, C, dres, C, 1, pc_tensor(g, P_PROJW, l), C, 0, g->datty, C, EPI_STORE);
         RUN(mm(g, K_PROJ_DX, d));
         double afl = 2.5 * 2.0 * 2.0 * B * H * ((double)T * (T + 1) / 2) * (C / H);
-        LAUNCH(K_ATTN_BWD, 3, afl, as * 8.0 * bt * c,
+        const int attn_bwd_kernels = attention_tc_supported(g->act, B, T, C, H, qkv) ? 2 : 3;
+        LAUNCH(K_ATTN_BWD, attn_bwd_kernels, afl, as * 8.0 * bt * c,
                attention_backward(g->act, g->dqkv, g->datty, qkv, atty, lse, B, T, C, H,
                                   g->scratch, g->err, g->stream));
+        if (g->recompute >= 2)  // ln1(rin) again
+            LAUNCH(K_RECOMP, 1, 0, ln_bytes,
+                   layernorm_forward(g->act, ln1, g->ln1_mean + l * bt, g->ln1_rstd + l * bt, rin,
+                                     pc_tensor(g, P_LN1W, l), pc_tensor(g, P_LN1B, l), BT, C,
+                                     g->stream));
         d = gd(3 * C, C, BT, g->dqkv, 3 * C, 0, ln1, C, 0, grad_tensor(g, P_QKVW, l), C,
                EPI_ACCUM_F32);
         RUN(mm(g, K_QKV_DW, d));

@@ -151,6 +151,49 @@ cudaError_t encoder_forward(int act, void* out, const int* tok, const void* wte,
 }
 
 // ===========================================================================
+// Elementwise GELU, out = gelu(in), with the same device function
+// (gelu_and_grad_f) as the fp32 fused epilogue, so that an output recomputed
+// later from the same input is bit for bit the one computed first.
+// ===========================================================================
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) k_gelu_fwd(T* out, const T* in, size_t n) {
+    gdc_wait();
+    gdc_launch_dependents();
+    const size_t nv = n / VEC;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nv;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float x[VEC], y[VEC];
+        load_vec_f<T, VEC>(x, in + i * VEC);
+#pragma unroll
+        for (int j = 0; j < VEC; j++) {
+            float dg;
+            gelu_and_grad_f(x[j], y[j], dg);
+        }
+        store_vec_f<T, VEC>(out + i * VEC, y);
+    }
+    for (size_t e = nv * VEC + blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
+         e += (size_t)gridDim.x * blockDim.x) {
+        float y, dg;
+        gelu_and_grad_f(to_f(in[e]), y, dg);
+        out[e] = from_f<T>(y);
+    }
+}
+cudaError_t gelu_forward(int act, void* out, const void* in, size_t n, cudaStream_t s) {
+    if (act == ACT_BF16) {
+        if (((uintptr_t)out | (uintptr_t)in) & 15)
+            launch_pdl(k_gelu_fwd<bf16, 1>, 148 * 8, 256, 0, s, (bf16*)out, (const bf16*)in, n);
+        else
+            launch_pdl(k_gelu_fwd<bf16, 8>, 148 * 8, 256, 0, s, (bf16*)out, (const bf16*)in, n);
+    } else {
+        if (((uintptr_t)out | (uintptr_t)in) & 15)
+            launch_pdl(k_gelu_fwd<float, 1>, 148 * 8, 256, 0, s, (float*)out, (const float*)in, n);
+        else
+            launch_pdl(k_gelu_fwd<float, 4>, 148 * 8, 256, 0, s, (float*)out, (const float*)in, n);
+    }
+    return cudaGetLastError();
+}
+
+// ===========================================================================
 // LayerNorm forward: one warp per row, mean, rstd = 1/sqrt(var + 1e-5) with
 // the biased variance.  Persistent warps walk the rows with a stride; the next
 // row's data (packed, VEC-wide loads) is in flight while the current row is

@@ -112,6 +112,12 @@ extern "C" int gpt2k_crossentropy(int dtype, void* logits, float* losses, const 
                                     (cudaStream_t)stream));
 }
 
+extern "C" int gpt2k_gelu_forward(int dtype, void* out, const void* in, size_t n, void* stream) {
+    if (!dt_ok(dtype) || !out || !in) return GPT2_ERR_ARG;
+    if (n == 0) return GPT2_OK;
+    return rc_of(gelu_forward(dtype, out, in, n, (cudaStream_t)stream));
+}
+
 extern "C" size_t gpt2k_bias_grad_scratch_bytes(int N, int OC) { return bias_grad_scratch(N, OC); }
 
 extern "C" int gpt2k_bias_grad(int dtype, float* db, const void* dout, int N, int OC,

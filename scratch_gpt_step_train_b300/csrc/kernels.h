@@ -105,6 +105,8 @@ cudaError_t adamw_norm(const float* g, size_t n, const AdamArgs& a, float* state
                        cudaStream_t s);
 cudaError_t adamw_update(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
                          const AdamArgs& a, const float* state, cudaStream_t s);
+// out[i] = gelu(in[i]) for i < n (dtype act), the fused epilogue's formula
+cudaError_t gelu_forward(int act, void* out, const void* in, size_t n, cudaStream_t s);
 // acc[0] += x[0] on the device
 cudaError_t accumulate_scalar(float* acc, const float* x, cudaStream_t s);
 

@@ -26,6 +26,7 @@ SIGNATURES = {
     "gpt2k_encoder_backward_scratch_bytes": (_sz, [_i, _i, _i, _i]),
     "gpt2k_encoder_backward": (_i, [_i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "gpt2k_crossentropy": (_i, [_i, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
+    "gpt2k_gelu_forward": (_i, [_i, _vp, _vp, _sz, _vp]),
     "gpt2k_bias_grad_scratch_bytes": (_sz, [_i, _i]),
     "gpt2k_bias_grad": (_i, [_i, _vp, _vp, _i, _i, _vp, _vp]),
 }
@@ -167,6 +168,12 @@ def crossentropy(logits, losses, tgt, V, dloss, err=None):
     _ck(klib().gpt2k_crossentropy(_dt(logits), _p(logits), _p(losses), _p(tgt), N, V, Vp,
                                   float(dloss), _p(err), _stream()), "crossentropy")
     return err
+
+
+def gelu_forward(out, inp):
+    assert out.is_contiguous() and inp.is_contiguous() and out.numel() == inp.numel()
+    _ck(klib().gpt2k_gelu_forward(_dt(inp), _p(out), _p(inp), inp.numel(), _stream()),
+        "gelu_forward")
 
 
 def bias_grad(db, dout):

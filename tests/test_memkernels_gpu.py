@@ -212,3 +212,23 @@ def test_crossentropy_fused(N, V, dtype):
     else:
         assert np.all(np.abs(got_d - rd) <= 2.0 ** -8 * np.abs(rd) + 1e-6 * dloss)
     assert int(err[0]) == 0
+
+
+# ------------------------------------------------------------ elementwise GELU
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_gelu_forward(dtype):
+    """the recompute path's GELU (odd length: vector body plus scalar tail)"""
+    x = np.random.default_rng(9).normal(0, 2.5, 100003)
+    xt = _t(x, dtype)
+    out = torch.empty_like(xt)
+    K.gelu_forward(out, xt)
+    xin = _np(xt)
+    ref = ops.gelu_forward(xin)
+    got = _np(out)
+    # fp32: a few ulp of the sigmoid-form evaluation; bf16: plus one rounding.
+    # The oracle evaluates the tanh form, whose 1 + tanh(u) cancels in fp64 in
+    # the far negative tail (it returns 0 below x ~ -5.7): its own absolute
+    # error, about 2^-52 |x|, is part of the bar.
+    rel = 4e-6 if dtype == torch.float32 else 2.0 ** -8 + 4e-6
+    assert np.all(np.abs(got - ref) <= rel * np.abs(ref) + 2.0 ** -50 * np.abs(xin) + 1e-30)
