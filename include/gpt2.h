@@ -66,6 +66,15 @@ enum { GPT2_FP32 = 0, GPT2_BF16 = 1 };
  *    the kept residual stream (bit-identical).  Saves 2(L-1) of B*T*C more.
  * In fp32 mode a recompute run is bit for bit the same as a run without. */
 enum { GPT2_RECOMPUTE_GELU = 0x10, GPT2_RECOMPUTE_LN = 0x20 };
+/* Parameters without fp32 master weights, OR-ed into GPT2_BF16 ("Karpathy
+ * reproduces GPT-2 (1.6B) in llm.c", "Parameter guide" -w 0): the parameters
+ * exist only in bf16 (4 bytes/parameter less); AdamW (moments fp32) computes
+ * each new value in fp32 from the widened bf16 value and rounds it back
+ * stochastically: update t rounds parameter i with counter (t-1)*N + i of the
+ * SplitMix64 stream of seed ^ 0x5352000000000000 (the rounding rule of
+ * gpt2k_stochastic_round_bf16).  get/set_params widen exactly / round to
+ * nearest even; checkpoints hold the widened values. */
+enum { GPT2_NO_MASTER = 0x40 };
 
 enum {
     GPT2_OK = 0,
@@ -177,7 +186,9 @@ int gpt2_last_step_info(gpt2_t* g, int* skipped, float* z_loss, float* z_grad);
 /* ---- checkpoints: a file with the fp32 parameters, the AdamW moments and
  * step count, and the spike detector's settings and window (this library's
  * own format: an 88-byte header "GPT2B3CK", version 1, L H C V T mode,
- * nparams, t, detector state; then params, m, v as fp32 in canonical order and
+ * nparams, t, detector state, the handle's seed (the stochastic-rounding
+ * stream of GPT2_NO_MASTER continues from it); then params, m, v as fp32 in
+ * canonical order and
  * the detector's two windows as float64).  A handle of the same L, H, C, V and
  * T (any B, any mode) that loads it continues training bit for bit as the
  * saving handle would have ("Karpathy reproduces GPT-2 (1.6B) in llm.c",

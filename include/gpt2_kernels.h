@@ -126,6 +126,15 @@ int gpt2k_crossentropy(int dtype, void* logits, float* losses, const int32_t* tg
  * so both results are identical.  out and in may be the same buffer. */
 int gpt2k_gelu_forward(int dtype, void* out, const void* in, size_t n, void* stream);
 
+/* Stochastic rounding fp32 -> bf16 (the parameter update without fp32 master
+ * weights, "Karpathy reproduces GPT-2 (1.6B) in llm.c", "Parameter guide"
+ * -w 0): out[i] (bf16 bits) = (bits(in[i]) + r) >> 16 with r the top 16 bits
+ * of output number k0 + i (0-based) of the SplitMix64 stream of `seed`
+ * (Steele, Lea & Flood 2014: output k = mix(seed + (k+1) * 0x9E3779B97F4A7C15));
+ * |x| is rounded up with probability (low 16 bits of x)/65536.  NaN -> NaN. */
+int gpt2k_stochastic_round_bf16(void* out, const float* in, size_t n, uint64_t seed, uint64_t k0,
+                                void* stream);
+
 /* Bias gradient: db[o] += sum_n dout[n,o] (fixed summation order). */
 size_t gpt2k_bias_grad_scratch_bytes(int N, int OC);
 int gpt2k_bias_grad(int dtype, float* db, const void* dout, int N, int OC, void* scratch,

@@ -95,6 +95,29 @@ float og_normal_sample(uint64_t seed, uint64_t i, double std) {
     return (float)(z * std);
 }
 
+/* Stochastic rounding of fp32 to bf16 (the parameter update without fp32
+ * master weights, "Karpathy reproduces GPT-2 (1.6B) in llm.c", "Parameter
+ * guide" -w 0).  The bf16 value is the top half of the fp32 bit pattern; the
+ * bottom half (the fraction f / 65536 of the way from |x| truncated to the next
+ * bf16 magnitude) decides: round |x| up iff r < f, with r the top 16 bits of
+ * SplitMix64 output k0 + i -- i.e. with probability f / 65536.  Written as:
+ * up iff f + r >= 65536 (a carry out of the bottom half).  NaN gives the quiet
+ * NaN 0x7fc0. */
+void og_stochastic_round_bf16(uint16_t* out, const float* in, size_t n, uint64_t seed,
+                              uint64_t k0) {
+    for (size_t i = 0; i < n; i++) {
+        uint32_t b;
+        memcpy(&b, &in[i], 4);
+        if ((b & 0x7fffffffu) > 0x7f800000u) {
+            out[i] = 0x7fc0;
+            continue;
+        }
+        uint32_t r = (uint32_t)(og_splitmix64(seed, k0 + i) >> 48);
+        uint32_t top = b >> 16, f = b & 0xffffu;
+        out[i] = (uint16_t)(f + r >= 65536u ? top + 1u : top);
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* Parameter layout                                                    */
 /* ------------------------------------------------------------------ */

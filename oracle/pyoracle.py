@@ -72,6 +72,8 @@ def _lib(real="double"):
         "og_crossentropy_backward": (None, [pR, pR, pI, R, i, i, i]),
         "og_sumsq": (R, [pR, sz]),
         "og_adamw": (None, [pR, pR, pR, pR, sz, R, R, R, R, R, R, i, i]),
+        "og_stochastic_round_bf16": (None, [ct.POINTER(ct.c_uint16), ct.POINTER(ct.c_float), sz,
+                                            ct.c_uint64, ct.c_uint64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -230,6 +232,26 @@ class Ops:
         self.lib.og_adamw(self._pp(w), self._pp(m), self._pp(v), self._pp(g), w.size, gscale,
                           lr, b1, b2, eps, wd, int(decay), int(t))
         return w, m, v
+
+
+def stochastic_round_bf16(x, seed, k0=0):
+    """bf16 bit patterns (uint16) of the oracle's stochastic rounding of the
+    fp32 array x with SplitMix64 counters k0, k0+1, ..."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    out = np.empty(x.size, np.uint16)
+    _lib("double").og_stochastic_round_bf16(out.ctypes.data_as(ct.POINTER(ct.c_uint16)),
+                                            x.ctypes.data_as(ct.POINTER(ct.c_float)), x.size,
+                                            int(seed), int(k0))
+    return out
+
+
+def splitmix64(seed, j):
+    """output number j of SplitMix64 seeded with `seed`, as the oracle computes
+    it (for pins)"""
+    z = (seed + (j + 1) * 0x9E3779B97F4A7C15) % 2 ** 64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) % 2 ** 64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) % 2 ** 64
+    return z ^ (z >> 31)
 
 
 class Model:

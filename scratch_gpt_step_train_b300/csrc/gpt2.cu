@@ -53,6 +53,8 @@ struct ProfRec {
 struct gpt2 {
     int L, H, C, V, Vp, T, B, mode, act;
     int recompute;  // 0: keep all activations; 1: GELU output recomputed; 2: and LN outputs
+    bool no_master;  // parameters only in bf16, updated with stochastic rounding
+    uint64_t seed;
     size_t BT;
     ParamLayout lay;
     size_t nparams;
@@ -185,7 +187,7 @@ static void plan(gpt2* g, char* base, size_t* total) {
     Planner p{base, 0};
     size_t N = g->nparams, BT = g->BT, C = g->C, L = g->L;
     size_t as = act_size(g->act);
-    g->master = (float*)p.take(N * 4);
+    g->master = g->no_master ? nullptr : (float*)p.take(N * 4);
     g->grads = (float*)p.take(N * 4);
     g->m = (float*)p.take(N * 4);
     g->v = (float*)p.take(N * 4);
@@ -231,7 +233,8 @@ static bool shape_ok(int L, int H, int C, int V, int T, int B, int mode) {
     if (C % H) return false;
     int hd = C / H;
     if (hd != 8 && hd != 16 && hd != 32 && hd != 64 && hd != 128) return false;
-    if (mode & ~(0xF | GPT2_RECOMPUTE_GELU | GPT2_RECOMPUTE_LN)) return false;
+    if (mode & ~(0xF | GPT2_RECOMPUTE_GELU | GPT2_RECOMPUTE_LN | GPT2_NO_MASTER)) return false;
+    if ((mode & GPT2_NO_MASTER) && (mode & 0xF) != GPT2_BF16) return false;
     mode &= 0xF;
     if (mode != GPT2_FP32 && mode != GPT2_BF16) return false;
     if (mode == GPT2_BF16 && C % 8) return false;
@@ -247,6 +250,7 @@ extern "C" size_t gpt2_workspace_bytes(int L, int H, int C, int V, int T, int B,
     tmp.L = L; tmp.H = H; tmp.C = C; tmp.V = V; tmp.T = T; tmp.B = B; tmp.mode = mode;
     tmp.act = (mode & 0xF) == GPT2_BF16 ? ACT_BF16 : ACT_F32;
     tmp.recompute = (mode & GPT2_RECOMPUTE_LN) ? 2 : ((mode & GPT2_RECOMPUTE_GELU) ? 1 : 0);
+    tmp.no_master = (mode & GPT2_NO_MASTER) != 0;
     tmp.Vp = ((V + 127) / 128) * 128;
     tmp.BT = (size_t)B * T;
     make_layout(&tmp.lay, L, C, V, T);
@@ -268,6 +272,8 @@ extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int 
     g->L = L; g->H = H; g->C = C; g->V = V; g->T = T; g->B = B; g->mode = mode;
     g->act = (mode & 0xF) == GPT2_BF16 ? ACT_BF16 : ACT_F32;
     g->recompute = (mode & GPT2_RECOMPUTE_LN) ? 2 : ((mode & GPT2_RECOMPUTE_GELU) ? 1 : 0);
+    g->no_master = (mode & GPT2_NO_MASTER) != 0;
+    g->seed = seed;
     g->Vp = ((V + 127) / 128) * 128;
     g->BT = (size_t)B * T;
     make_layout(&g->lay, L, C, V, T);
@@ -318,9 +324,16 @@ extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int 
         if ((e = cudaMemsetAsync(g->m, 0, g->nparams * 4, g->stream))) break;
         if ((e = cudaMemsetAsync(g->v, 0, g->nparams * 4, g->stream))) break;
         if ((e = cudaMemsetAsync(g->err, 0, 16, g->stream))) break;
-        if ((e = init_params(g->master, g->lay, seed, g->stream))) break;
-        if (g->act == ACT_BF16 && (e = cast_to_bf16(g->pc, g->master, g->nparams, g->stream)))
-            break;
+        if (g->no_master) {
+            // the fp32 init passes through the gradient buffer, rounded to bf16
+            if ((e = init_params(g->grads, g->lay, seed, g->stream))) break;
+            if ((e = cast_to_bf16(g->pc, g->grads, g->nparams, g->stream))) break;
+            if ((e = cudaMemsetAsync(g->grads, 0, g->nparams * 4, g->stream))) break;
+        } else {
+            if ((e = init_params(g->master, g->lay, seed, g->stream))) break;
+            if (g->act == ACT_BF16 && (e = cast_to_bf16(g->pc, g->master, g->nparams, g->stream)))
+                break;
+        }
         e = cudaStreamSynchronize(g->stream);
     } while (0);
     if (e != cudaSuccess) {
@@ -705,6 +718,14 @@ static float spike_z(const gpt2* g, const std::vector<double>& hist, double x) {
     return (float)((x - mean) / sd);
 }
 
+// norm pass, then the update of bf16-only parameters with stochastic rounding
+static cudaError_t adamw_step_bf16_sr(gpt2* g, const AdamArgs& a) {
+    cudaError_t e = adamw_norm(g->grads, g->nparams, a, g->adam_state, g->scratch, g->stream);
+    if (e != cudaSuccess) return e;
+    return adamw_update_bf16_sr(g->pc, g->m, g->v, g->grads, g->nparams, a, g->adam_state,
+                                g->stream);
+}
+
 extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float eps, float wd,
                                float clip, float* h_grad_norm) {
     if (!g) return GPT2_ERR_ARG;
@@ -723,14 +744,20 @@ extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float ep
     a.dec_lo[2] = o[P_PROJW];   a.dec_hi[2] = o[P_PROJB];
     a.dec_lo[3] = o[P_FCW];     a.dec_hi[3] = o[P_FCB];
     a.dec_lo[4] = o[P_FCPROJW]; a.dec_hi[4] = o[P_FCPROJB];
+    a.t = t;
+    a.sr_seed = g->seed ^ 0x5352000000000000ull;  // "SR": the stochastic-rounding stream
     void* wb = g->act == ACT_BF16 ? g->pc : nullptr;
     const double ad_bytes = 34.0 * g->nparams + (g->act == ACT_BF16 ? 2.0 * g->nparams : 0.0);
     g->last_skipped = 0;
     g->last_zl = g->last_zg = NAN;
     if (g->sk_window <= 0) {
-        LAUNCH(K_ADAM, 3, 0, ad_bytes,
-               adamw_step(g->master, g->m, g->v, g->grads, wb, g->nparams, a, g->adam_state,
-                          g->scratch, g->stream));
+        if (g->no_master) {
+            LAUNCH(K_ADAM, 3, 0, ad_bytes - 6.0 * g->nparams, adamw_step_bf16_sr(g, a));
+        } else {
+            LAUNCH(K_ADAM, 3, 0, ad_bytes,
+                   adamw_step(g->master, g->m, g->v, g->grads, wb, g->nparams, a, g->adam_state,
+                              g->scratch, g->stream));
+        }
         float st[3];
         CK(cudaMemcpyAsync(st, g->adam_state, 12, cudaMemcpyDeviceToHost, g->stream));
         RUN(check_dev_err(g));
@@ -764,9 +791,14 @@ extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float ep
         g->last_skipped = 1;  // parameters, moments and the step count unchanged
         return GPT2_OK;
     }
-    LAUNCH(K_ADAM, 1, 0, ad_bytes - 4.0 * g->nparams,
-           adamw_update(g->master, g->m, g->v, g->grads, wb, g->nparams, a, g->adam_state,
-                        g->stream));
+    if (g->no_master)
+        LAUNCH(K_ADAM, 1, 0, ad_bytes - 10.0 * g->nparams,
+               adamw_update_bf16_sr(g->pc, g->m, g->v, g->grads, g->nparams, a, g->adam_state,
+                                    g->stream));
+    else
+        LAUNCH(K_ADAM, 1, 0, ad_bytes - 4.0 * g->nparams,
+               adamw_update(g->master, g->m, g->v, g->grads, wb, g->nparams, a, g->adam_state,
+                            g->stream));
     g->t = t;
     return GPT2_OK;
 }
@@ -794,6 +826,43 @@ extern "C" int gpt2_last_step_info(gpt2_t* g, int* skipped, float* z_loss, float
     return GPT2_OK;
 }
 
+// fp32 <-> the parameters: the master copy, or (no master) the bf16 values
+// widened exactly / rounded to nearest even, converted on the host
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    if ((b & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;
+    return (uint16_t)((b + 0x7fffu + ((b >> 16) & 1u)) >> 16);
+}
+static int params_to_host(gpt2* g, float* h) {
+    if (!g->no_master) {
+        CK(cudaMemcpyAsync(h, g->master, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
+        CK(cudaStreamSynchronize(g->stream));
+        return GPT2_OK;
+    }
+    std::vector<uint16_t> tmp(g->nparams);
+    CK(cudaMemcpyAsync(tmp.data(), g->pc, g->nparams * 2, cudaMemcpyDeviceToHost, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    for (size_t i = 0; i < g->nparams; i++) {
+        const uint32_t u = (uint32_t)tmp[i] << 16;
+        memcpy(&h[i], &u, 4);
+    }
+    return GPT2_OK;
+}
+static int params_from_host(gpt2* g, const float* h) {
+    if (!g->no_master) {
+        CK(cudaMemcpyAsync(g->master, h, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
+        if (g->act == ACT_BF16) CK(cast_to_bf16(g->pc, g->master, g->nparams, g->stream));
+        CK(cudaStreamSynchronize(g->stream));
+        return GPT2_OK;
+    }
+    std::vector<uint16_t> tmp(g->nparams);
+    for (size_t i = 0; i < g->nparams; i++) tmp[i] = f32_to_bf16_rne(h[i]);
+    CK(cudaMemcpyAsync(g->pc, tmp.data(), g->nparams * 2, cudaMemcpyHostToDevice, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    return GPT2_OK;
+}
+
 // ---------------------------------------------------------------------------
 // checkpoints: fp32 parameters, AdamW moments and step count, and the spike
 // detector's window, so that a run resumed from a checkpoint continues bit for
@@ -808,7 +877,8 @@ struct CkptHeader {  // 88 bytes, little-endian, no implicit padding
     int32_t t;
     int32_t sk_window, sk_count, sk_pos;
     float sk_loss_z, sk_grad_z;
-    uint32_t reserved[4];
+    uint64_t seed;  // the handle's seed: the stochastic-rounding stream continues from it
+    uint32_t reserved[2];
 };
 static_assert(sizeof(CkptHeader) == 88, "checkpoint header layout");
 static const char kCkptMagic[8] = {'G', 'P', 'T', '2', 'B', '3', 'C', 'K'};
@@ -825,13 +895,21 @@ extern "C" int gpt2_save_checkpoint(gpt2_t* g, const char* path) {
     hd.t = g->t;
     hd.sk_window = g->sk_window; hd.sk_count = g->sk_count; hd.sk_pos = g->sk_pos;
     hd.sk_loss_z = g->sk_loss_z; hd.sk_grad_z = g->sk_grad_z;
+    hd.seed = g->seed;
     FILE* f = fopen(path, "wb");
     if (!f) return fail(g, GPT2_ERR_IO, "cannot open %s for writing", path);
     bool ok = fwrite(&hd, sizeof hd, 1, f) == 1;
     std::vector<float> buf(ok ? g->nparams : 0);
-    const float* src[3] = {g->master, g->m, g->v};
+    const float* src[3] = {nullptr, g->m, g->v};  // params through params_to_host
     for (int k = 0; ok && k < 3; k++) {
-        if (cudaMemcpy(buf.data(), src[k], g->nparams * 4, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        if (k == 0) {
+            const int rc = params_to_host(g, buf.data());
+            if (rc != GPT2_OK) {
+                fclose(f);
+                return rc;
+            }
+        } else if (cudaMemcpy(buf.data(), src[k], g->nparams * 4, cudaMemcpyDeviceToHost) !=
+                   cudaSuccess) {
             fclose(f);
             return fail(g, GPT2_ERR_CUDA, "checkpoint: device read failed");
         }
@@ -864,11 +942,19 @@ extern "C" int gpt2_load_checkpoint(gpt2_t* g, const char* path) {
                     path, hd.L, hd.H, hd.C, hd.V, hd.T);
     }
     std::vector<float> buf(g->nparams);
-    float* dst[3] = {g->master, g->m, g->v};
+    float* dst[3] = {nullptr, g->m, g->v};  // params through params_from_host
     bool ok = true;
     for (int k = 0; ok && k < 3; k++) {
         ok = fread(buf.data(), 4, g->nparams, f) == g->nparams;
-        if (ok && cudaMemcpy(dst[k], buf.data(), g->nparams * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+        if (!ok) break;
+        if (k == 0) {
+            const int rc = params_from_host(g, buf.data());
+            if (rc != GPT2_OK) {
+                fclose(f);
+                return rc;
+            }
+        } else if (cudaMemcpy(dst[k], buf.data(), g->nparams * 4, cudaMemcpyHostToDevice) !=
+                   cudaSuccess) {
             fclose(f);
             return fail(g, GPT2_ERR_CUDA, "checkpoint: device write failed");
         }
@@ -879,13 +965,13 @@ extern "C" int gpt2_load_checkpoint(gpt2_t* g, const char* path) {
              fread(gh.data(), 8, hd.sk_window, f) == (size_t)hd.sk_window;
     fclose(f);
     if (!ok) return fail(g, GPT2_ERR_IO, "%s is truncated", path);
-    if (g->act == ACT_BF16) CK(cast_to_bf16(g->pc, g->master, g->nparams, g->stream));
     CK(cudaStreamSynchronize(g->stream));
     g->t = hd.t;
     g->sk_window = hd.sk_window; g->sk_count = hd.sk_count; g->sk_pos = hd.sk_pos;
     g->sk_loss_z = hd.sk_loss_z; g->sk_grad_z = hd.sk_grad_z;
     g->sk_loss_hist = lh;
     g->sk_grad_hist = gh;
+    g->seed = hd.seed;
     g->last_skipped = 0;
     g->last_zl = g->last_zg = NAN;
     return GPT2_OK;
@@ -900,17 +986,12 @@ extern "C" int gpt2_padded_vocab(gpt2_t* g) { return g ? g->Vp : 0; }
 extern "C" int gpt2_get_params(gpt2_t* g, float* h) {
     if (!g || !h) return GPT2_ERR_ARG;
     cudaSetDevice(g->device);
-    CK(cudaMemcpyAsync(h, g->master, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
-    CK(cudaStreamSynchronize(g->stream));
-    return GPT2_OK;
+    return params_to_host(g, h);
 }
 extern "C" int gpt2_set_params(gpt2_t* g, const float* h) {
     if (!g || !h) return GPT2_ERR_ARG;
     cudaSetDevice(g->device);
-    CK(cudaMemcpyAsync(g->master, h, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
-    if (g->act == ACT_BF16) CK(cast_to_bf16(g->pc, g->master, g->nparams, g->stream));
-    CK(cudaStreamSynchronize(g->stream));
-    return GPT2_OK;
+    return params_from_host(g, h);
 }
 extern "C" int gpt2_get_grads(gpt2_t* g, float* h) {
     if (!g || !h) return GPT2_ERR_ARG;

@@ -90,6 +90,31 @@ cudaError_t init_params(float* master, const ParamLayout& lay, uint64_t seed, cu
     return cudaGetLastError();
 }
 
+// ===========================================================================
+// Stochastic rounding fp32 -> bf16 with a counter-based random stream: the
+// element rounded with counter value k takes the top 16 bits r of the k-th
+// SplitMix64 output of seed s and becomes (bits(x) + r) >> 16.  Since the
+// formats are sign-magnitude, that rounds |x| up with probability
+// (low 16 bits of x) / 65536, down otherwise: unbiased.  NaN stays NaN.
+// ===========================================================================
+__device__ __forceinline__ uint16_t sround_bf16(float x, uint64_t word) {
+    const uint32_t b = __float_as_uint(x);
+    if ((b & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;  // NaN
+    return (uint16_t)((b + (uint32_t)(word >> 48)) >> 16);
+}
+__global__ void k_sround(uint16_t* out, const float* in, size_t n, uint64_t seed, uint64_t k0) {
+    gdc_wait();
+    gdc_launch_dependents();
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        out[i] = sround_bf16(in[i], sm64_at(seed, k0 + i));
+}
+cudaError_t stochastic_round_bf16(void* out, const float* in, size_t n, uint64_t seed,
+                                  uint64_t k0, cudaStream_t s) {
+    launch_pdl(k_sround, 148 * 8, 256, 0, s, (uint16_t*)out, in, n, seed, k0);
+    return cudaGetLastError();
+}
+
 __global__ void k_cast_bf16(bf16* dst, const float* src, size_t n) {
     gdc_wait();
     gdc_launch_dependents();
@@ -1655,6 +1680,33 @@ __global__ void __launch_bounds__(256) k_adam(float* w, float* m, float* v, cons
         v[e] = Vv;
         if (wb) wb[e] = __float2bfloat16_rn(W);
     }
+}
+
+// AdamW for parameters held only in bf16: the update in fp32 from the widened
+// bf16 value, then stochastic rounding back to bf16 with counter (t-1)*n + i
+// of the stream a.sr_seed (t = this update's step count).
+__global__ void __launch_bounds__(256) k_adam_bf16_sr(bf16* wb, float* m, float* v,
+                                                      const float* g, size_t n, AdamArgs a,
+                                                      const float* state) {
+    gdc_wait();
+    gdc_launch_dependents();
+    if (state[2] == 0.f) return;
+    const float sc = state[1];
+    const uint64_t k0 = (uint64_t)(a.t - 1) * (uint64_t)n;
+    uint16_t* wu = reinterpret_cast<uint16_t*>(wb);
+    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
+         e += (size_t)gridDim.x * blockDim.x) {
+        float W = __uint_as_float((uint32_t)wu[e] << 16), M = m[e], Vv = v[e];
+        adam_one(W, M, Vv, g[e], sc, a, decayed(e, a));
+        m[e] = M;
+        v[e] = Vv;
+        wu[e] = sround_bf16(W, sm64_at(a.sr_seed, k0 + e));
+    }
+}
+cudaError_t adamw_update_bf16_sr(void* wbf16, float* m, float* v, const float* g, size_t n,
+                                 const AdamArgs& a, const float* state, cudaStream_t s) {
+    launch_pdl(k_adam_bf16_sr, 148 * 8, 256, 0, s, (bf16*)wbf16, m, v, g, n, a, state);
+    return cudaGetLastError();
 }
 
 size_t adamw_scratch() { return ADAM_NB * sizeof(double); }

@@ -112,6 +112,13 @@ extern "C" int gpt2k_crossentropy(int dtype, void* logits, float* losses, const 
                                     (cudaStream_t)stream));
 }
 
+extern "C" int gpt2k_stochastic_round_bf16(void* out, const float* in, size_t n, uint64_t seed,
+                                           uint64_t k0, void* stream) {
+    if (!out || !in) return GPT2_ERR_ARG;
+    if (n == 0) return GPT2_OK;
+    return rc_of(stochastic_round_bf16(out, in, n, seed, k0, (cudaStream_t)stream));
+}
+
 extern "C" int gpt2k_gelu_forward(int dtype, void* out, const void* in, size_t n, void* stream) {
     if (!dt_ok(dtype) || !out || !in) return GPT2_ERR_ARG;
     if (n == 0) return GPT2_OK;

@@ -95,6 +95,8 @@ struct AdamArgs {
     float bc1, bc2;          // 1 - b1^t, 1 - b2^t
     float inv_accum, clip;
     size_t dec_lo[5], dec_hi[5];  // decayed index ranges [lo, hi)
+    int t;                        // this update's step count (1-based)
+    uint64_t sr_seed;             // stochastic-rounding stream (bf16-only parameters)
 };
 size_t adamw_scratch();
 // state[0] = norm, state[1] = total gradient scale, state[2] = finite flag
@@ -107,6 +109,12 @@ cudaError_t adamw_update(float* w, float* m, float* v, const float* g, void* wbf
                          const AdamArgs& a, const float* state, cudaStream_t s);
 // out[i] = gelu(in[i]) for i < n (dtype act), the fused epilogue's formula
 cudaError_t gelu_forward(int act, void* out, const void* in, size_t n, cudaStream_t s);
+// parameters held only in bf16: AdamW in fp32, stochastic rounding back
+cudaError_t adamw_update_bf16_sr(void* wbf16, float* m, float* v, const float* g, size_t n,
+                                 const AdamArgs& a, const float* state, cudaStream_t s);
+// out[i] = stochastic rounding of in[i] to bf16 with counter k0 + i of `seed`
+cudaError_t stochastic_round_bf16(void* out, const float* in, size_t n, uint64_t seed,
+                                  uint64_t k0, cudaStream_t s);
 // acc[0] += x[0] on the device
 cudaError_t accumulate_scalar(float* acc, const float* x, cudaStream_t s);
 

@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(HERE, "libgpt2b300.so")
 FP32, BF16 = 0, 1
 # activation recompute flags, OR-ed into the mode
 RECOMPUTE_GELU, RECOMPUTE_LN = 0x10, 0x20
+# parameters only in bf16, stochastic rounding in AdamW (with BF16)
+NO_MASTER = 0x40
 ERRORS = {0: "OK", -1: "GPT2_ERR_ARG", -2: "GPT2_ERR_CUDA", -3: "GPT2_ERR_OOM",
           -4: "GPT2_ERR_STATE", -5: "GPT2_ERR_TOKEN_RANGE", -6: "GPT2_ERR_NONFINITE",
           -7: "GPT2_ERR_TIMEOUT", -8: "GPT2_ERR_IO"}

@@ -27,6 +27,7 @@ SIGNATURES = {
     "gpt2k_encoder_backward": (_i, [_i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "gpt2k_crossentropy": (_i, [_i, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp]),
     "gpt2k_gelu_forward": (_i, [_i, _vp, _vp, _sz, _vp]),
+    "gpt2k_stochastic_round_bf16": (_i, [_vp, _vp, _sz, ct.c_uint64, ct.c_uint64, _vp]),
     "gpt2k_bias_grad_scratch_bytes": (_sz, [_i, _i]),
     "gpt2k_bias_grad": (_i, [_i, _vp, _vp, _i, _i, _vp, _vp]),
 }
@@ -174,6 +175,13 @@ def gelu_forward(out, inp):
     assert out.is_contiguous() and inp.is_contiguous() and out.numel() == inp.numel()
     _ck(klib().gpt2k_gelu_forward(_dt(inp), _p(out), _p(inp), inp.numel(), _stream()),
         "gelu_forward")
+
+
+def stochastic_round_bf16(out, inp, seed, k0=0):
+    """out (bf16) = stochastic rounding of inp (fp32) with stream counters k0.."""
+    assert out.is_contiguous() and inp.is_contiguous() and out.numel() == inp.numel()
+    _ck(klib().gpt2k_stochastic_round_bf16(_p(out), _p(inp), inp.numel(), int(seed), int(k0),
+                                           _stream()), "stochastic_round_bf16")
 
 
 def bias_grad(db, dout):

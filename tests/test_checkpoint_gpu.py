@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 from scratch_gpt_step_train_b300 import inputs
-from scratch_gpt_step_train_b300.gpt2 import BF16, FP32, GPT2, GPT2Error
+from scratch_gpt_step_train_b300.gpt2 import BF16, FP32, GPT2, NO_MASTER, GPT2Error
 
 pytestmark = pytest.mark.gpu
 CFG = dict(L=2, H=2, C=128, V=300, T=64, B=2)  # head size 64: tensor-core attention in bf16
@@ -35,7 +35,7 @@ def _state(gm):
     return gm.get_params(), m, v, t
 
 
-@pytest.mark.parametrize("mode", [FP32, BF16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("mode", [FP32, BF16, BF16 | NO_MASTER], ids=["fp32", "bf16", "bf16-nomaster"])
 def test_resume_from_checkpoint_is_bit_exact(tmp_path, mode):
     steps = [_batches(2, 100 + 10 * i) for i in range(5)]
     a = GPT2(**CFG, seed=1, mode=mode)

@@ -232,3 +232,18 @@ def test_gelu_forward(dtype):
     # error, about 2^-52 |x|, is part of the bar.
     rel = 4e-6 if dtype == torch.float32 else 2.0 ** -8 + 4e-6
     assert np.all(np.abs(got - ref) <= rel * np.abs(ref) + 2.0 ** -50 * np.abs(xin) + 1e-30)
+
+
+# ------------------------------------------------ stochastic rounding (-w 0)
+
+def test_stochastic_round_bf16_bit_exact():
+    from oracle.pyoracle import stochastic_round_bf16 as oracle_sr
+    rng = np.random.default_rng(31)
+    x = (rng.normal(0, 1, 300001) * np.exp(rng.uniform(-30, 30, 300001))).astype(np.float32)
+    x[:6] = [np.nan, np.inf, -np.inf, 0.0, -0.0, 3.3e38]
+    xt = torch.from_numpy(x).cuda()
+    out = torch.empty(x.size, dtype=torch.bfloat16, device="cuda")
+    seed, k0 = 0x5352000000000001, 123456789012
+    K.stochastic_round_bf16(out, xt, seed, k0)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle_sr(x, seed, k0))

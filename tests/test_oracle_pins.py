@@ -425,3 +425,39 @@ def test_toy_transition_table_brute_force_and_training():
         f = float(np.mean(nxt))
         if abs(f - 0.5) >= 0.3:
             assert abs(a50[s] - f) < abs(a0[s] - f) - 0.1, (s, f, a0[s], a50[s])
+
+
+# ------------------------------------------------ stochastic rounding (-w 0)
+
+def test_splitmix64_published_first_output():
+    from oracle.pyoracle import splitmix64
+    # the first output of SplitMix64 seeded with 0 (Steele, Lea & Flood 2014)
+    assert splitmix64(0, 0) == 0xE220A8397B1DCDAF
+
+
+def test_stochastic_round_bf16_oracle():
+    from oracle.pyoracle import splitmix64, stochastic_round_bf16
+    rng = np.random.default_rng(21)
+    x = (rng.normal(0, 1, 4096) * np.exp(rng.uniform(-20, 20, 4096))).astype(np.float32)
+    bits = x.view(np.uint32)
+    top = (bits >> 16).astype(np.uint32)
+    seed, k0 = 12345, 777
+    out = stochastic_round_bf16(x, seed, k0).astype(np.uint32)
+    # always one of the two bf16 neighbours of |x| (sign-magnitude)
+    assert np.all((out == top) | (out == top + 1))
+    # the decision follows the published generator: up iff f + r >= 2^16
+    for i in range(0, 4096, 97):
+        r = splitmix64(seed, k0 + i) >> 48
+        f = int(bits[i]) & 0xFFFF
+        assert int(out[i]) == int(top[i]) + (1 if f + r >= 65536 else 0)
+    # values on the bf16 grid stay put; NaN -> quiet NaN; inf stays inf
+    grid = (top.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(stochastic_round_bf16(grid, seed, k0).astype(np.uint32), top)
+    sp = np.array([np.nan, np.inf, -np.inf, 0.0, -0.0], np.float32)
+    assert list(stochastic_round_bf16(sp, 1)) == [0x7FC0, 0x7F80, 0xFF80, 0x0000, 0x8000]
+    # unbiased: 1 + 2^-9 lies a quarter of the way from 1 to 1 + 2^-7
+    n = 200000
+    y = stochastic_round_bf16(np.full(n, 1.0 + 2.0 ** -9, np.float32), 99, 0)
+    up = np.mean(y == 0x3F81)
+    assert np.all((y == 0x3F80) | (y == 0x3F81))
+    assert abs(up - 0.25) < 4 * np.sqrt(0.25 * 0.75 / n)
