@@ -183,6 +183,31 @@ int gpt2_set_spike_skip(gpt2_t* g, float loss_z, float grad_z, int window);
  * (NaN when the detector is off or its window is not yet full) */
 int gpt2_last_step_info(gpt2_t* g, int* skipped, float* z_loss, float* z_grad);
 
+/* ---- data parallelism ("Karpathy reproduces GPT-2 (1.6B) in llm.c",
+ * "Training": one process per GPU, gradients averaged over the ranks, the
+ * optimizer state sharded ZeRO-1 style).  One step on R ranks: every rank
+ * runs its micro-batches (forward + backward), sums the gradient vectors of
+ * all ranks into each (an all-reduce over gpt2_grads_buffer), sets the
+ * divisor to R x its micro-batch count (gpt2_set_grad_count), applies
+ * gpt2_adamw_step_shard to its own slice [lo, hi) of the canonical vector --
+ * the global norm and clip come from the whole summed gradient, so every rank
+ * takes the same decision -- and the ranks then exchange their updated slices
+ * of the parameters (the fp32 master and the bf16 copy of gpt2_params_buffer).
+ * The exchange itself is the caller's (NCCL through torch.distributed in the
+ * binding's DataParallel).  The moments are held for the whole vector but
+ * each rank only touches its slice.  Device pointers stay valid for the
+ * handle's life. */
+int gpt2_grads_buffer(gpt2_t* g, float** d_grads, size_t* n);
+/* master: NULL without fp32 master weights; bf16: NULL in GPT2_FP32 mode */
+int gpt2_params_buffer(gpt2_t* g, float** d_master, void** d_bf16, size_t* n);
+int gpt2_get_grad_count(gpt2_t* g, int* count);
+int gpt2_set_grad_count(gpt2_t* g, int count);  /* count >= 1 */
+/* AdamW on [lo, hi) of the canonical vector (lo, hi multiples of 4, hi may be
+ * N); the step count advances.  GPT2_ERR_STATE with the spike detector on
+ * (its decision needs every rank's loss). */
+int gpt2_adamw_step_shard(gpt2_t* g, size_t lo, size_t hi, float lr, float b1, float b2,
+                          float eps, float wd, float clip, float* h_grad_norm);
+
 /* ---- checkpoints: a file with the fp32 parameters, the AdamW moments and
  * step count, and the spike detector's settings and window (this library's
  * own format: an 88-byte header "GPT2B3CK", version 1, L H C V T mode,

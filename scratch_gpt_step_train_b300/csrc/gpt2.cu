@@ -719,19 +719,12 @@ static float spike_z(const gpt2* g, const std::vector<double>& hist, double x) {
 }
 
 // norm pass, then the update of bf16-only parameters with stochastic rounding
-static cudaError_t adamw_step_bf16_sr(gpt2* g, const AdamArgs& a) {
-    cudaError_t e = adamw_norm(g->grads, g->nparams, a, g->adam_state, g->scratch, g->stream);
-    if (e != cudaSuccess) return e;
-    return adamw_update_bf16_sr(g->pc, g->m, g->v, g->grads, g->nparams, a, g->adam_state,
-                                g->stream);
-}
-
-extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float eps, float wd,
-                               float clip, float* h_grad_norm) {
-    if (!g) return GPT2_ERR_ARG;
-    cudaSetDevice(g->device);
-    if (g->n_accum < 1) return fail(g, GPT2_ERR_STATE, "adamw_step without accumulated grads");
-    int t = g->t + 1;
+// AdamW arguments of step t (1-based): bias corrections, the 1/count of the
+// accumulated micro-batches, the weight-decayed ranges (the weight matrices and
+// both embedding tables: decay on 2-D tensors only), and the stochastic-rounding stream.  base is the
+// canonical index of the first element the update launch sees.
+static AdamArgs adam_args(const gpt2* g, int t, float lr, float b1, float b2, float eps, float wd,
+                          float clip, size_t base) {
     AdamArgs a;
     a.lr = lr; a.b1 = b1; a.b2 = b2; a.eps = eps; a.wd = wd;
     a.bc1 = (float)(1.0 - pow((double)b1, t));
@@ -746,6 +739,25 @@ extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float ep
     a.dec_lo[4] = o[P_FCPROJW]; a.dec_hi[4] = o[P_FCPROJB];
     a.t = t;
     a.sr_seed = g->seed ^ 0x5352000000000000ull;  // "SR": the stochastic-rounding stream
+    a.base = base;
+    a.n_total = g->nparams;
+    return a;
+}
+
+static cudaError_t adamw_step_bf16_sr(gpt2* g, const AdamArgs& a) {
+    cudaError_t e = adamw_norm(g->grads, g->nparams, a, g->adam_state, g->scratch, g->stream);
+    if (e != cudaSuccess) return e;
+    return adamw_update_bf16_sr(g->pc, g->m, g->v, g->grads, g->nparams, a, g->adam_state,
+                                g->stream);
+}
+
+extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float eps, float wd,
+                               float clip, float* h_grad_norm) {
+    if (!g) return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    if (g->n_accum < 1) return fail(g, GPT2_ERR_STATE, "adamw_step without accumulated grads");
+    const int t = g->t + 1;
+    const AdamArgs a = adam_args(g, t, lr, b1, b2, eps, wd, clip, 0);
     void* wb = g->act == ACT_BF16 ? g->pc : nullptr;
     const double ad_bytes = 34.0 * g->nparams + (g->act == ACT_BF16 ? 2.0 * g->nparams : 0.0);
     g->last_skipped = 0;
@@ -815,6 +827,69 @@ extern "C" int gpt2_set_spike_skip(gpt2_t* g, float loss_z, float grad_z, int wi
         cudaSetDevice(g->device);
         CK(cudaMemsetAsync(g->loss + 1, 0, 4, g->stream));  // no partial sum carried in
     }
+    return GPT2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// data parallelism: buffers for an external all-reduce / all-gather, the
+// gradient divisor, and the AdamW update of one shard of the parameters
+// ---------------------------------------------------------------------------
+extern "C" int gpt2_grads_buffer(gpt2_t* g, float** d_grads, size_t* n) {
+    if (!g) return GPT2_ERR_ARG;
+    if (d_grads) *d_grads = g->grads;
+    if (n) *n = g->nparams;
+    return GPT2_OK;
+}
+extern "C" int gpt2_params_buffer(gpt2_t* g, float** d_master, void** d_bf16, size_t* n) {
+    if (!g) return GPT2_ERR_ARG;
+    if (d_master) *d_master = g->master;  // NULL without master weights
+    if (d_bf16) *d_bf16 = g->act == ACT_BF16 ? g->pc : nullptr;
+    if (n) *n = g->nparams;
+    return GPT2_OK;
+}
+extern "C" int gpt2_get_grad_count(gpt2_t* g, int* count) {
+    if (!g || !count) return GPT2_ERR_ARG;
+    *count = g->n_accum;
+    return GPT2_OK;
+}
+extern "C" int gpt2_set_grad_count(gpt2_t* g, int count) {
+    if (!g || count < 1) return GPT2_ERR_ARG;
+    g->n_accum = count;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_adamw_step_shard(gpt2_t* g, size_t lo, size_t hi, float lr, float b1, float b2,
+                                     float eps, float wd, float clip, float* h_grad_norm) {
+    if (!g || lo > hi || hi > g->nparams || (lo % 4) || (hi % 4 && hi != g->nparams))
+        return GPT2_ERR_ARG;
+    cudaSetDevice(g->device);
+    if (g->n_accum < 1) return fail(g, GPT2_ERR_STATE, "adamw_step_shard without accumulated grads");
+    if (g->sk_window > 0)
+        return fail(g, GPT2_ERR_STATE, "the spike detector needs the whole update (not a shard)");
+    const int t = g->t + 1;
+    const AdamArgs a = adam_args(g, t, lr, b1, b2, eps, wd, clip, lo);
+    const size_t n = hi - lo;
+    // the norm (and the clip scale) over every gradient, the update on [lo, hi)
+    LAUNCH(K_ADAM, 2, 0, 4.0 * g->nparams,
+           adamw_norm(g->grads, g->nparams, a, g->adam_state, g->scratch, g->stream));
+    if (n > 0) {
+        const size_t as = act_size(g->act);
+        void* wb = g->act == ACT_BF16 ? (void*)((char*)g->pc + lo * as) : nullptr;
+        if (g->no_master)
+            LAUNCH(K_ADAM, 1, 0, 26.0 * n,
+                   adamw_update_bf16_sr(wb, g->m + lo, g->v + lo, g->grads + lo, n, a,
+                                        g->adam_state, g->stream));
+        else
+            LAUNCH(K_ADAM, 1, 0, 30.0 * n,
+                   adamw_update(g->master + lo, g->m + lo, g->v + lo, g->grads + lo, wb, n, a,
+                                g->adam_state, g->stream));
+    }
+    float st[3];
+    CK(cudaMemcpyAsync(st, g->adam_state, 12, cudaMemcpyDeviceToHost, g->stream));
+    RUN(check_dev_err(g));
+    if (h_grad_norm) *h_grad_norm = st[0];
+    if (st[2] == 0.f) return fail(g, GPT2_ERR_NONFINITE, "gradient norm is not finite (%g)", st[0]);
+    g->t = t;
     return GPT2_OK;
 }
 

@@ -1623,7 +1623,9 @@ __global__ void k_adam_norm(const double* part, float* state, float inv_accum, f
     }
 }
 
+// element i of the launch is canonical element a.base + i
 __device__ __forceinline__ bool decayed(size_t i, const AdamArgs& a) {
+    i += a.base;
 #pragma unroll
     for (int k = 0; k < 5; k++)
         if (i >= a.dec_lo[k] && i < a.dec_hi[k]) return true;
@@ -1692,7 +1694,7 @@ __global__ void __launch_bounds__(256) k_adam_bf16_sr(bf16* wb, float* m, float*
     gdc_launch_dependents();
     if (state[2] == 0.f) return;
     const float sc = state[1];
-    const uint64_t k0 = (uint64_t)(a.t - 1) * (uint64_t)n;
+    const uint64_t k0 = (uint64_t)(a.t - 1) * (uint64_t)a.n_total + a.base;
     uint16_t* wu = reinterpret_cast<uint16_t*>(wb);
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
          e += (size_t)gridDim.x * blockDim.x) {

@@ -97,6 +97,8 @@ struct AdamArgs {
     size_t dec_lo[5], dec_hi[5];  // decayed index ranges [lo, hi)
     int t;                        // this update's step count (1-based)
     uint64_t sr_seed;             // stochastic-rounding stream (bf16-only parameters)
+    size_t base;                  // canonical index of the first element updated (a shard)
+    size_t n_total;               // length of the whole canonical vector
 };
 size_t adamw_scratch();
 // state[0] = norm, state[1] = total gradient scale, state[2] = finite flag

@@ -48,6 +48,11 @@ SIGNATURES = {
     "gpt2_get_logits": (_i, [_vp, _pf]),
     "gpt2_get_loss": (_i, [_vp, _pf]),
     "gpt2_get_losses": (_i, [_vp, _pf]),
+    "gpt2_grads_buffer": (_i, [_vp, ct.POINTER(_vp), ct.POINTER(_sz)]),
+    "gpt2_params_buffer": (_i, [_vp, ct.POINTER(_vp), ct.POINTER(_vp), ct.POINTER(_sz)]),
+    "gpt2_get_grad_count": (_i, [_vp, _pi]),
+    "gpt2_set_grad_count": (_i, [_vp, _i]),
+    "gpt2_adamw_step_shard": (_i, [_vp, _sz, _sz] + [_f] * 6 + [_pf]),
     "gpt2_set_spike_skip": (_i, [_vp, _f, _f, _i]),
     "gpt2_last_step_info": (_i, [_vp, _pi, _pf, _pf]),
     "gpt2_save_checkpoint": (_i, [_vp, ct.c_char_p]),
@@ -219,6 +224,42 @@ class GPT2:
         v = np.ascontiguousarray(v, dtype=np.float32)
         assert m.size == self.n and v.size == self.n
         self._ck(self._lib.gpt2_set_opt_state(self.h, _fptr(m), _fptr(v), int(step)))
+
+    # ---- data parallelism (see dp.DataParallel) ----
+    def _ws_view(self, ptr, nbytes, dtype):
+        """torch view of device memory inside this handle's workspace"""
+        if self._ws is None or not ptr:
+            return None
+        off = ptr - self._ws.data_ptr()
+        assert 0 <= off and off + nbytes <= self._ws.numel()
+        return self._ws[off:off + nbytes].view(dtype)
+
+    def grads_tensor(self):
+        """the fp32 gradient vector (canonical order) as a torch view"""
+        p, n = _vp(), _sz()
+        self._ck(self._lib.gpt2_grads_buffer(self.h, ct.byref(p), ct.byref(n)))
+        return self._ws_view(p.value, n.value * 4, self._torch.float32)
+
+    def param_tensors(self):
+        """(fp32 master or None, bf16 compute copy or None) as torch views"""
+        pm, pb, n = _vp(), _vp(), _sz()
+        self._ck(self._lib.gpt2_params_buffer(self.h, ct.byref(pm), ct.byref(pb), ct.byref(n)))
+        return (self._ws_view(pm.value, n.value * 4, self._torch.float32),
+                self._ws_view(pb.value, n.value * 2, self._torch.bfloat16))
+
+    def grad_count(self):
+        c = ct.c_int(0)
+        self._ck(self._lib.gpt2_get_grad_count(self.h, ct.byref(c)))
+        return c.value
+
+    def set_grad_count(self, count):
+        self._ck(self._lib.gpt2_set_grad_count(self.h, int(count)))
+
+    def adamw_step_shard(self, lo, hi, lr, b1=0.9, b2=0.95, eps=1e-8, wd=0.1, clip=1.0):
+        norm = ct.c_float(0.0)
+        self._ck(self._lib.gpt2_adamw_step_shard(self.h, int(lo), int(hi), lr, b1, b2, eps, wd,
+                                                 clip, ct.byref(norm)))
+        return norm.value
 
     def set_spike_skip(self, loss_z=5.0, grad_z=5.0, window=128):
         """Skip the update when the step's mean loss or gradient norm has a

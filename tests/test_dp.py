@@ -1,0 +1,257 @@
+"""Data-parallel step with the optimizer update sharded over the ranks
+("Karpathy reproduces GPT-2 (1.6B) in llm.c", "Training": one process per
+GPU, gradients averaged over the ranks).
+
+CPU part: two gloo ranks drive dp.DataParallel over a stand-in model whose
+shard update is the oracle's AdamW; after three steps each rank's parameters
+must equal, bit for bit, one process updating the whole vector with the
+gradient summed over both ranks' micro-batches and divided by their total
+count.  GPU part: the same split done on one GPU by two handles (each updating
+its half, the halves then exchanged) equals the plain whole-vector step bit
+for bit, in fp32, bf16 and bf16 without master weights; and DataParallel over
+a one-rank NCCL group equals the plain step."""
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from scratch_gpt_step_train_b300.dp import DataParallel, shard_bounds
+
+HP = dict(lr=1e-2, b1=0.9, b2=0.95, eps=1e-8, wd=0.1, clip=1.0)
+N_PARAMS = 1000  # ragged over two ranks: slices [0, 512) and [512, 1000)
+MICRO = 2
+STEPS = 3
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_shard_bounds_cover_and_align():
+    for n in (0, 1, 63, 64, 1000, 124475904):
+        for world in (1, 2, 3, 8):
+            b = shard_bounds(n, world)
+            assert len(b) == world and b[0][0] == 0 and b[-1][1] == n
+            for (lo, hi), (lo2, _) in zip(b, b[1:]):
+                assert hi == lo2
+            for lo, hi in b:
+                assert 0 <= lo <= hi <= n
+                assert (lo % 64 == 0 or lo == n) and (hi % 64 == 0 or hi == n)
+    assert shard_bounds(10, 4) == [(0, 10), (10, 10), (10, 10), (10, 10)]
+
+
+class OracleShardModel:
+    """Stand-in for a GPT2 handle: fp64 CPU vectors, the update of a slice
+    done by the oracle's AdamW, the clip scale from the norm of the whole
+    summed gradient divided by the micro-batch count"""
+
+    def __init__(self, n, seed):
+        from oracle.pyoracle import Ops
+        self.ops = Ops("double")
+        g = torch.Generator().manual_seed(seed)
+        self.n = n
+        self.w = torch.randn(n, generator=g, dtype=torch.float64) * 0.02
+        self.m = torch.zeros(n, dtype=torch.float64)
+        self.v = torch.zeros(n, dtype=torch.float64)
+        self.g = torch.zeros(n, dtype=torch.float64)
+        self.count = 0
+        self.t = 0
+
+    def zero_grad(self):
+        self.g.zero_()
+        self.count = 0
+
+    def accumulate(self, grad):
+        self.g += grad
+        self.count += 1
+
+    def grads_tensor(self):
+        return self.g
+
+    def param_tensors(self):
+        return self.w, None
+
+    def grad_count(self):
+        return self.count
+
+    def set_grad_count(self, c):
+        self.count = c
+
+    def adamw_step_shard(self, lo, hi, lr, b1, b2, eps, wd, clip):
+        norm = float(torch.sqrt((self.g * self.g).sum())) / self.count
+        sc = (1.0 / self.count) * (clip / norm if clip > 0 and norm > clip else 1.0)
+        self.t += 1
+        if hi > lo:
+            w, m, v = self.ops.adamw(self.w[lo:hi].numpy(), self.m[lo:hi].numpy(),
+                                     self.v[lo:hi].numpy(), self.g[lo:hi].numpy(), sc, lr, b1,
+                                     b2, eps, wd, True, self.t)
+            self.w[lo:hi] = torch.from_numpy(w)
+            self.m[lo:hi] = torch.from_numpy(m)
+            self.v[lo:hi] = torch.from_numpy(v)
+        return norm
+
+
+def _micro_grad(rank, step, k):
+    g = torch.Generator().manual_seed(1000 * rank + 10 * step + k)
+    return torch.randn(N_PARAMS, generator=g, dtype=torch.float64)
+
+
+def _gloo_rank(rank, world, port, q):
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        model = OracleShardModel(N_PARAMS, seed=5)
+        dp = DataParallel(model)
+        norms = []
+        for step in range(STEPS):
+            model.zero_grad()
+            for k in range(MICRO):
+                model.accumulate(_micro_grad(rank, step, k))
+            norms.append(dp.step(**HP))
+        q.put((rank, model.w.numpy().copy(), model.m.numpy().copy(), norms))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_data_parallel_gloo_two_ranks_equals_one_process():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gloo_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(world):
+        rank, w, m, norms = q.get(timeout=120)
+        got[rank] = (w, m, norms)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+
+    ref = OracleShardModel(N_PARAMS, seed=5)
+    ref_norms = []
+    for step in range(STEPS):
+        ref.zero_grad()
+        per_rank = []
+        for r in range(world):
+            acc = torch.zeros(N_PARAMS, dtype=torch.float64)
+            for k in range(MICRO):
+                acc += _micro_grad(r, step, k)
+            per_rank.append(acc)
+        ref.g.copy_(per_rank[0] + per_rank[1])
+        ref.set_grad_count(world * MICRO)
+        ref_norms.append(ref.adamw_step_shard(0, N_PARAMS, **HP))
+    bounds = shard_bounds(N_PARAMS, world)
+    for r in range(world):
+        w, m, norms = got[r]
+        assert np.array_equal(w, ref.w.numpy())  # every slice, after the exchange
+        lo, hi = bounds[r]
+        assert np.array_equal(m[lo:hi], ref.m.numpy()[lo:hi])  # this rank's optimizer shard
+        assert norms == ref_norms
+
+
+# ---------------------------------------------------------------------------
+# GPU
+# ---------------------------------------------------------------------------
+CFG = dict(L=2, H=2, C=128, V=300, T=64, B=2)
+
+
+def _gpu_modes():
+    from scratch_gpt_step_train_b300.gpt2 import BF16, FP32, NO_MASTER
+    return [FP32, BF16, BF16 | NO_MASTER]
+
+
+def _batch(seed):
+    from scratch_gpt_step_train_b300 import inputs
+    return inputs.uniform_batch(seed, CFG["B"], CFG["T"], CFG["V"])
+
+
+def _micro(gm, seed):
+    tok, tgt = _batch(seed)
+    gm.forward(tok, tgt)
+    gm.backward()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mi", [0, 1, 2], ids=["fp32", "bf16", "bf16-nomaster"])
+def test_sharded_update_on_two_handles_equals_whole_step(mi):
+    from scratch_gpt_step_train_b300.gpt2 import GPT2
+    mode = _gpu_modes()[mi]
+    a = GPT2(**CFG, seed=3, mode=mode)
+    r = [GPT2(**CFG, seed=3, mode=mode) for _ in range(2)]
+    n = a.n
+    bounds = shard_bounds(n, 2)
+    for step in range(3):
+        # the reference: one micro-batch, count 1
+        a.zero_grad()
+        _micro(a, 40 + step)
+        na = a.adamw_step(**HP)
+        # two "ranks" with the same micro-batch: the summed gradient is exactly
+        # twice it and the count is 2, so the update is the same to the bit
+        for h in r:
+            h.zero_grad()
+            _micro(h, 40 + step)
+        g0, g1 = r[0].grads_tensor(), r[1].grads_tensor()
+        s = g0 + g1
+        g0.copy_(s)
+        g1.copy_(s)
+        norms = []
+        for h, (lo, hi) in zip(r, bounds):
+            h.set_grad_count(h.grad_count() * 2)
+            norms.append(h.adamw_step_shard(lo, hi, **HP))
+        for i, (lo, hi) in enumerate(bounds):
+            for dst, src in zip(r[1 - i].param_tensors(), r[i].param_tensors()):
+                if src is not None:
+                    dst[lo:hi].copy_(src[lo:hi])
+        torch.cuda.synchronize()
+        assert norms[0] == norms[1] == na
+    pa = a.get_params()
+    ma, va, ta = a.get_opt_state()
+    for i, h in enumerate(r):
+        assert np.array_equal(h.get_params(), pa)
+        m, v, t = h.get_opt_state()
+        lo, hi = bounds[i]
+        assert t == ta == 3
+        assert np.array_equal(m[lo:hi], ma[lo:hi]) and np.array_equal(v[lo:hi], va[lo:hi])
+    if mi > 0:  # the bf16 compute copies too
+        pb = a.param_tensors()[1]
+        for h in r:
+            assert torch.equal(h.param_tensors()[1].view(torch.int16), pb.view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_data_parallel_nccl_one_rank_equals_plain_step():
+    from scratch_gpt_step_train_b300.gpt2 import BF16, GPT2
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{_free_port()}", rank=0,
+                            world_size=1, device_id=torch.device("cuda:0"))
+    try:
+        a = GPT2(**CFG, seed=9, mode=BF16)
+        b = GPT2(**CFG, seed=9, mode=BF16)
+        dp = DataParallel(b)
+        for step in range(3):
+            for h in (a, b):
+                h.zero_grad()
+                _micro(h, 70 + 2 * step)
+                _micro(h, 71 + 2 * step)
+            na = a.adamw_step(**HP)
+            nb = dp.step(**HP)
+            assert na == nb
+        torch.cuda.synchronize()
+        assert np.array_equal(a.get_params(), b.get_params())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_shard_step_argument_errors_are_host_checks():
+    """the C-ABI rejects unaligned or out-of-range slices before any launch
+    (checked here through a null handle, which needs no GPU)"""
+    from scratch_gpt_step_train_b300.gpt2 import lib
+    L = lib()
+    assert L.gpt2_adamw_step_shard(None, 0, 4, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, None) == -1
+    assert L.gpt2_set_grad_count(None, 2) == -1
