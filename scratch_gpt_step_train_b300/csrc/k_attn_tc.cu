@@ -41,7 +41,6 @@ using namespace tc;
 constexpr int HD = 64;
 constexpr int TILE = 128;               // queries per CTA = keys per tile
 constexpr int TILE_BYTES = TILE * 128;  // 128 rows of 64 bf16
-constexpr int ATT_THREADS = 320;        // TMA warp, MMA warp, 8 softmax warps
 // forward smem: Q, a ring of F_NRING K/V slots (K_0 V_0 K_1 V_1 ... in order),
 // then the row-max exchange, the final row-sum exchange and the barriers (P
 // lives in TMEM)
@@ -70,18 +69,24 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// lane 0 waits (polling: these waits are on the critical path), the warp
-// learns the outcome
+// every lane of the warp waits (suspended in the barrier's try_wait until the
+// phase completes: no divergent polling loop); the warp goes on only if all
+// lanes saw the phase complete
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* err, int lane) {
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_spin(bar, parity, abort_flag, err);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    (void)lane;
+    const bool ok = mbar_wait(bar, parity, abort_flag, err);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // the 8 softmax warps (256 threads) synchronise among themselves
 __device__ __forceinline__ void named_sync_softmax() {
     asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+// the two softmax warps that share TMEM lane quarter q (warps q + 1 and
+// q + 5, counted from 1) synchronise: named barrier 2 + q, 64 threads
+__device__ __forceinline__ void pair_sync(int q) {
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory");
 }
 
 constexpr int FWD_THREADS = 288;  // warp 0: TMA (lane 0) + MMA (lane 1); 8 softmax warps
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
             const uint64_t dRingK = sdesc(sRing, 0, 1024), dRingV = sdesc(sRing, 8192, 1024);
             auto issue_s = [&](int j) -> bool {
                 const int it = 2 * j, s = it % F_NRING;
-                if (!mbar_wait_spin(b_full + 8 * s, (it / F_NRING) & 1, abort_flag, p.err))
+                if (!mbar_wait(b_full + 8 * s, (it / F_NRING) & 1, abort_flag, p.err))
                     return false;
                 tc_fence_after();
                 const uint64_t dK = dRingK + (uint64_t)((s * TILE_BYTES) >> 4);
@@ -193,14 +198,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
                 // S_{j+1} as soon as the softmax warps hold S_j in registers,
                 // so that it overlaps their work on tile j
                 if (j + 1 < nkt) {
-                    if (!mbar_wait_spin(b_sfree, j & 1, abort_flag, p.err)) break;
+                    if (!mbar_wait(b_sfree, j & 1, abort_flag, p.err)) break;
                     tc_fence_after();
                     if (!issue_s(j + 1)) break;
                 }
-                if (!mbar_wait_spin(b_pfull, j & 1, abort_flag, p.err)) break;
+                if (!mbar_wait(b_pfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const int it = 2 * j + 1, s = it % F_NRING;
-                if (!mbar_wait_spin(b_full + 8 * s, (it / F_NRING) & 1, abort_flag, p.err)) break;
+                if (!mbar_wait(b_full + 8 * s, (it / F_NRING) & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint64_t dV = dRingV + (uint64_t)((s * TILE_BYTES) >> 4);
                 // O += P_j V_j (O starts at the first tile); P is read from TMEM,
@@ -227,10 +232,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
         const int kb = hf * 64;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        // After a failed wait a warp keeps going round the loop without work,
+        // so that its partner warp still meets it at each barrier.
         for (int j = 0; j < nkt; j++) {
-            if (!warp_wait(b_sfull, j & 1, abort_flag, p.err, lane)) {
+            if (!ok || !warp_wait(b_sfull, j & 1, abort_flag, p.err, lane)) {
                 ok = false;
-                break;
+                pair_sync(q);
+                continue;
             }
             tc_fence_after();
             uint32_t sv[2][32];
@@ -248,7 +256,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
                     for (int i = 0; i < 32; i++)
                         if (kb + 32 * c + i > r) sv[c][i] = __float_as_uint(-INFINITY);
             }
-            // row max over the 64 columns as a tree (8 independent chains)
+            // row max over the 64 columns as a tree (8 independent chains),
+            // exchanged with the partner warp that holds the other 64
             float m8[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) m8[i] = __uint_as_float(sv[0][i]);
@@ -261,7 +270,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
             const float mx = m8[0];
             float* rb = red + (j & 1) * 256;
             rb[hf * 128 + r] = mx;
-            named_sync_softmax();
+            pair_sync(q);
             const float mrow = fmaxf(rb[r], rb[128 + r]) * p.scale_log2;
             const bool need = mrow > m_used + RESCALE_SLACK;
             const float m_new = need ? mrow : m_used;
@@ -281,7 +290,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
             // TMEM and writes O, which a rescale rewrites
             if (j > 0 && !warp_wait(b_ofull, (j - 1) & 1, abort_flag, p.err, lane)) {
                 ok = false;
-                break;
+                continue;
             }
             tc_fence_after();
             if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -311,7 +320,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
         }
         // fold the two halves' row sums (every softmax thread reaches this)
         lsum[hf * 128 + r] = l;
-        named_sync_softmax();
+        pair_sync(q);
         if (fin && qi < p.T) {
             const float lt = lsum[r] + lsum[128 + r];
             const float inv = 1.f / lt;
@@ -476,7 +485,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             // S^T = K Q_n^T and dP^T = V dO_n^T (128 keys x 64 queries)
             auto issue_s = [&](int n) -> bool {
                 const int s = n & 1, u = n >> 1;
-                if (!mbar_wait_spin(s ? b_qdf1 : b_qdf0, u & 1, abort_flag, p.err)) return false;
+                if (!mbar_wait(s ? b_qdf1 : b_qdf0, u & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
                 const uint32_t sq = base + (s ? D_Q1 : D_Q0), sd = base + (s ? D_DO1 : D_DO0);
                 const uint64_t dq_k = sdesc(sq, 0, 1024), dd_k = sdesc(sd, 0, 1024);
@@ -497,11 +506,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 // the next step's products as soon as the softmax warps hold
                 // this step's S^T and dP^T in registers
                 if (n + 1 < nq) {
-                    if (!mbar_wait_spin(b_sfree, n & 1, abort_flag, p.err)) break;
+                    if (!mbar_wait(b_sfree, n & 1, abort_flag, p.err)) break;
                     tc_fence_after();
                     if (!issue_s(n + 1)) break;
                 }
-                if (!mbar_wait_spin(b_psfull, n & 1, abort_flag, p.err)) break;
+                if (!mbar_wait(b_psfull, n & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 // dV += P^T dO, dK += dS^T Q (K = the 64 queries)
 #pragma unroll
@@ -535,9 +544,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 d_s[tid] = qi < p.T ? p.Dv[(size_t)bh * p.T + qi] : 0.f;
             }
             named_sync_softmax();
+            // after a failed wait a warp goes on round the loop without work,
+            // so that every softmax thread still meets each named barrier
+            if (!ok) continue;
             if (!warp_wait(b_sfull, n & 1, abort_flag, p.err, lane)) {
                 ok = false;
-                break;
+                continue;
             }
             tc_fence_after();
             uint32_t sv[32], dp[32];
@@ -584,7 +596,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             // the previous step's products must be done reading the P^T, dS^T tiles
             if (n > 0 && !warp_wait(b_psfree, (n - 1) & 1, abort_flag, p.err, lane)) {
                 ok = false;
-                break;
+                continue;
             }
             st_row32_64(sPT, r, c0, pp);
             st_row32_64(sDST, r, c0, dd);
@@ -723,7 +735,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             // S = Q K_j^T, dP = dO V_j^T (128 queries x 64 keys)
             auto issue_s = [&](int j) -> bool {
                 const int s = j % E_NRING, u = j / E_NRING;
-                if (!mbar_wait_spin(b_kvf + 8 * s, u & 1, abort_flag, p.err)) return false;
+                if (!mbar_wait(b_kvf + 8 * s, u & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
                 const uint32_t sk = sKV + s * 2 * SUB_BYTES, sv = sk + SUB_BYTES;
                 const uint64_t dk_k = sdesc(sk, 0, 1024), dv_k = sdesc(sv, 0, 1024);
@@ -744,11 +756,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 // the next step's products as soon as the softmax warps hold
                 // this step's S and dP in registers
                 if (j + 1 < nk) {
-                    if (!mbar_wait_spin(b_sfree, j & 1, abort_flag, p.err)) break;
+                    if (!mbar_wait(b_sfree, j & 1, abort_flag, p.err)) break;
                     tc_fence_after();
                     if (!issue_s(j + 1)) break;
                 }
-                if (!mbar_wait_spin(b_dsfull, j & 1, abort_flag, p.err)) break;
+                if (!mbar_wait(b_dsfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 // dQ += dS K_j (K = the 64 keys; dS read from TMEM, 8 columns
                 // = 16 keys per instruction)
@@ -846,10 +858,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(b_dsfull);
         }
-        if (ok && warp_wait(b_acc, 0, abort_flag, p.err, lane)) {
+        const bool fin = ok && warp_wait(b_acc, 0, abort_flag, p.err, lane);
+        uint32_t v[32];
+        if (fin) {
             tc_fence_after();
             bf16* dst = p.dqkv + (size_t)(row0 + qi) * 3 * p.C + h * HD + hf * 32;
-            uint32_t v[32];
             tmem_ld32_async(tDQ + loff + hf * 32, v);
             tmem_wait32(v);
             if (qlive) {
@@ -903,8 +916,7 @@ static bool map_rows(CUtensorMap* m, const void* base, long width, long rows, in
 
 cudaError_t attention_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out,
                                   const float* lse, float* Dv, int B, int T, int C, int H,
-                                  unsigned* err,
-                                  cudaStream_t s) {
+                                  unsigned* err, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_attn_dkv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, D_SMEM);

@@ -14,14 +14,18 @@
 // descriptor's transpose bits select the smem layout, so dX = dY W and
 // dW = dY^T X run without transposed copies.
 //
-// Kernel organisation (one persistent CTA per SM, 192 threads):
+// Kernel organisation (one persistent CTA per SM, 320 threads):
 //   warp 0    TMA producer: 2-D tiled loads, 128-byte swizzle, STAGES-deep
 //             ring of (A, B) stages guarded by full/empty mbarriers
 //   warp 1    allocates 2*BN TMEM columns; lane 0 issues tcgen05.mma
 //             (M=128, N=BN, K=16) and tcgen05.commit to free stages and to
 //             publish a finished accumulator
-//   warps 2-5 epilogue: tcgen05.ld of their 32-lane quarter of the
-//             accumulator, bias / GELU / residual / fp32 accumulate, stores
+//   warps 2-9 epilogue: warp w takes TMEM lane quarter w % 4 and one half of
+//             the tile's columns: tcgen05.ld in 32-column chunks, bias / GELU
+//             / residual / fp32 accumulate, staged in shared memory and
+//             written by TMA bulk stores
+// With MC, CTA pairs (clusters of 2) on vertically adjacent tiles share the
+// B tile: each loads one half and multicasts it to both.
 // Two TMEM accumulators let the epilogue of tile i overlap the mainloop of
 // tile i+1.  Every mbarrier wait is bounded (clock64 budget): on expiry the
 // CTA raises an abort flag, sets GPT2_DEVERR_TIMEOUT in the device error
@@ -468,9 +472,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // the first chunk's row operand does not depend on the accumulator:
             // fetch it before waiting for the tile
             if (has_pf) epi_prefetch(p, row, tn * BN + cbeg, pf[0]);
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(tfull + 8 * b, aph, abort_flag, p.err);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            // every lane waits (suspended in the barrier's try_wait until the
+            // phase completes); the warp goes on only if all saw it complete
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull + 8 * b, aph, abort_flag, p.err));
             if (!ok) break;
             tc_fence_after();
             const uint32_t taddr =

@@ -686,12 +686,15 @@ __global__ void __launch_bounds__(256) k_colsum(ColsumOut outs, int n0, int ncol
     const int c = blockIdx.x * 32 + tx;
     float a[4] = {0.f, 0.f, 0.f, 0.f};
     if (c < ncols) {
-        for (int i = ty; i < nparts; i += 32) {
-            float v[4];
+        // 16 independent loads in flight per thread: the partial rows are few
+        // (one per producer block), so latency, not bandwidth, sets the time
+        for (int i = ty; i < nparts; i += 128) {
+            float v[16];
 #pragma unroll
-            for (int q = 0; q < 4; q++) v[q] = i + 8 * q < nparts ? part[(size_t)(i + 8 * q) * ld + c] : 0.f;
+            for (int q = 0; q < 16; q++)
+                v[q] = i + 8 * q < nparts ? part[(size_t)(i + 8 * q) * ld + c] : 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; q++) a[q] += v[q];
+            for (int q = 0; q < 16; q++) a[q & 3] += v[q];
         }
     }
     sh[ty][tx] = (a[0] + a[1]) + (a[2] + a[3]);

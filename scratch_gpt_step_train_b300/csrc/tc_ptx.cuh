@@ -37,38 +37,6 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// non-blocking probe of the phase
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for a phase on a latency-critical path: polls with a short
-// nanosleep instead of suspending, so the waiter resumes within ~tens of cycles.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, unsigned* err) {
-    if (mbar_test(bar, parity)) return true;
-    long long t0 = clock64();
-    for (int it = 0;; it++) {
-        if (mbar_test(bar, parity)) return true;
-        __nanosleep(20);
-        if ((it & 63) == 63) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > WAIT_LIMIT) {
-                *abort_flag = 1;
-                if (err) atomicOr(err, GPT2_DEVERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
 // try_wait with a suspend-time hint: the thread sleeps until the phase
 // completes or about `ns` nanoseconds pass, instead of spinning on the issue slots
 __device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
