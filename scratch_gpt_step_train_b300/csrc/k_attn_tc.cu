@@ -45,8 +45,10 @@ constexpr int TILE_BYTES = TILE * 128;  // 128 rows of 64 bf16
 // then the row-max exchange, the final row-sum exchange and the barriers (P
 // lives in TMEM)
 constexpr int F_NRING = 5;
-constexpr int F_Q = 0, F_RING = 16384, F_RED = F_RING + F_NRING * 16384, F_LS = F_RED + 1024,
+constexpr int F_Q = 0, F_RING = 16384, F_RED = F_RING + F_NRING * 16384, F_LS = F_RED + 2048,
               F_BAR = F_LS + 1024;
+// the barriers sit below the TMEM address slot and the abort flag (offset 128)
+static_assert(16 * F_NRING + 40 <= 128, "forward barriers overlap the TMEM slot");
 constexpr int F_SMEM = F_BAR + 256 + 1024;
 
 struct AttnParams {
@@ -92,23 +94,6 @@ __device__ __forceinline__ void pair_sync(int q) {
 constexpr int FWD_THREADS = 288;  // warp 0: TMA (lane 0) + MMA (lane 1); 8 softmax warps
 constexpr float RESCALE_SLACK = 8.0f;  // log2 units: P stays <= 2^8 between rescales
 
-// Work items of the persistent attention kernels: item w is the (128-row
-// tile, batch*head) pair w, heaviest tiles first (row tile nt - 1 - w / BH,
-// batch*head w % BH).  CTA c of G takes item r*G + c in even rounds r and
-// r*G + G-1-c in odd ones (a snake), which evens out the per-CTA work.
-// (Everything is recomputed from the launch and the kernel parameters, which
-// the compiler can reload instead of holding in registers.)
-struct Items {
-    int B, H, nt;
-    __device__ __forceinline__ int at(int r) const {
-        const int G = (int)gridDim.x, c = (int)blockIdx.x;
-        const int w = r * G + ((r & 1) ? G - 1 - c : c);
-        return w < B * H * nt ? w : -1;
-    }
-    __device__ __forceinline__ int tile(int w) const { return nt - 1 - w / (B * H); }
-    __device__ __forceinline__ int bh(int w) const { return w % (B * H); }
-};
-
 __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_constant__ CUtensorMap map,
                                                                 AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -119,17 +104,19 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
     float* red = (float*)(base_gen + F_RED);  // [2 buffers][2 halves][128 rows]
     float* lsum = (float*)(base_gen + F_LS);  // [2 halves][128 rows]
     const uint32_t bar = base + F_BAR;
-    // full[F_NRING], empty[F_NRING] for the ring; q (Q landed); s (S ready);
-    // pf (P ready); o (P.V done); sfree (S copied to registers: the next S may
-    // overwrite it); qe (the item's last S issued: Q may be reloaded); of (the
-    // item's O read: the next item's first P.V may overwrite it)
+    // full[F_NRING], empty[F_NRING] for the ring; q; s (S ready); pf (P ready);
+    // o (P.V done); sfree (S copied to registers: the next S may overwrite it)
     const uint32_t b_full = bar, b_empty = bar + 8 * F_NRING, b_q = bar + 16 * F_NRING,
-                   b_sfull = b_q + 8, b_pfull = b_q + 16, b_ofull = b_q + 24, b_sfree = b_q + 32,
-                   b_qempty = b_q + 40, b_ofree = b_q + 48;
+                   b_sfull = b_q + 8, b_pfull = b_q + 16, b_ofull = b_q + 24, b_sfree = b_q + 32;
     uint32_t* tmem_slot = (uint32_t*)(base_gen + F_BAR + 128);
     volatile int* abort_flag = (volatile int*)(base_gen + F_BAR + 132);
 
-    const Items items{p.B, p.H, p.nqt};
+    // blocks launch in linear order, x fastest: every head's longest rows
+    // first, so that the short tiles fill in the tail
+    const int qt = p.nqt - 1 - (int)blockIdx.y;
+    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+    const int nkt = qt + 1;
+    const int row0 = b * p.T;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -142,8 +129,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
         mbar_init(b_pfull, 8);
         mbar_init(b_ofull, 1);
         mbar_init(b_sfree, 8);
-        mbar_init(b_qempty, 1);
-        mbar_init(b_ofree, 8);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map) : "memory");
@@ -164,33 +149,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------ producer
-            // per item: Q (once the previous item's last S has read the old
-            // one), then K_j, V_j through the ring, which runs on across items
+            const int ck = p.C + h * HD, cv = 2 * p.C + h * HD;
+            mbar_expect_tx(b_q, TILE_BYTES);
+            tma_load_2d(sQ, &map, b_q, h * HD, row0 + qt * TILE);
             int last[F_NRING];  // use count of each slot's last load
             for (int s = 0; s < F_NRING; s++) last[s] = -1;
-            int it = 0, qlast = -1;
-            bool ok = true;
-            for (int ic = 0; ok; ic++) {
-                const int w = items.at(ic);
-                if (w < 0) break;
-                const int qt = items.tile(w), bh = items.bh(w);
-                const int b = bh / p.H, h = bh % p.H, row0 = b * p.T;
-                const int ck = p.C + h * HD, cv = 2 * p.C + h * HD;
-                if (ic > 0 && !mbar_wait(b_qempty, (ic - 1) & 1, abort_flag, p.err)) break;
-                mbar_expect_tx(b_q, TILE_BYTES);
-                tma_load_2d(sQ, &map, b_q, h * HD, row0 + qt * TILE);
-                qlast = ic;
-                for (int t = 0; t < 2 * (qt + 1); t++, it++) {
-                    const int s = it % F_NRING, u = it / F_NRING;
-                    if (!mbar_wait(b_empty + 8 * s, (u & 1) ^ 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_expect_tx(b_full + 8 * s, TILE_BYTES);
-                    tma_load_2d(sRing + s * TILE_BYTES, &map, b_full + 8 * s, (t & 1) ? cv : ck,
-                                row0 + (t >> 1) * TILE);
-                    last[s] = u;
-                }
+            for (int it = 0; it < 2 * nkt; it++) {
+                const int s = it % F_NRING, u = it / F_NRING;
+                if (!mbar_wait(b_empty + 8 * s, (u & 1) ^ 1, abort_flag, p.err)) break;
+                mbar_expect_tx(b_full + 8 * s, TILE_BYTES);
+                tma_load_2d(sRing + s * TILE_BYTES, &map, b_full + 8 * s, (it & 1) ? cv : ck,
+                            row0 + (it >> 1) * TILE);
+                last[s] = u;
             }
             if (*abort_flag) {
                 for (int s = 0; s < F_NRING; s++) {
@@ -200,10 +170,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
                     while (!mbar_try(b_full + 8 * s, ls & 1) && clock64() - t0 < WAIT_LIMIT) {
                     }
                 }
-                if (qlast >= 0) {
-                    long long t0 = clock64();
-                    while (!mbar_try(b_q, qlast & 1) && clock64() - t0 < WAIT_LIMIT) {
-                    }
+                long long t0 = clock64();
+                while (!mbar_try(b_q, 0) && clock64() - t0 < WAIT_LIMIT) {
                 }
             }
         } else if (lane == 1) {
@@ -214,11 +182,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
             // field (bits 0..13, in 16-byte units) by a constant
             const uint64_t dQ = sdesc(sQ, 0, 1024);
             const uint64_t dRingK = sdesc(sRing, 0, 1024), dRingV = sdesc(sRing, 8192, 1024);
-            // S of global tile g (ring load 2g holds its K): item ic, local
-            // tile j of nkt
-            auto issue_s = [&](int g, int ic, int j, int nkt) -> bool {
-                if (j == 0 && !mbar_wait(b_q, ic & 1, abort_flag, p.err)) return false;
-                const int it = 2 * g, s = it % F_NRING;
+            auto issue_s = [&](int j) -> bool {
+                const int it = 2 * j, s = it % F_NRING;
                 if (!mbar_wait(b_full + 8 * s, (it / F_NRING) & 1, abort_flag, p.err))
                     return false;
                 tc_fence_after();
@@ -228,50 +193,31 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
                     umma_bf16(tS, dQ + (uint64_t)(k * 2), dK + (uint64_t)(k * 2), ID_S, k > 0);
                 umma_commit(b_sfull);
                 umma_commit(b_empty + 8 * s);
-                if (j == nkt - 1) umma_commit(b_qempty);  // the item's last read of Q
                 return true;
             };
-            int ic = 0, j = 0, w = items.at(0);
-            int nkt = w >= 0 ? items.tile(w) + 1 : 0;
-            bool ok = w >= 0 && issue_s(0, 0, 0, nkt);
-            for (int g = 0; ok; g++) {
-                // the next tile: this item's next, or the next item's first
-                int ic2 = ic, j2 = j + 1, nkt2 = nkt;
-                if (j2 == nkt) {
-                    ic2 = ic + 1;
-                    j2 = 0;
-                    const int w2 = items.at(ic2);
-                    nkt2 = w2 >= 0 ? items.tile(w2) + 1 : 0;
-                }
-                // S of the next tile as soon as the softmax warps hold this
-                // tile's S in registers, so that it overlaps their work
-                if (nkt2 > 0) {
-                    if (!mbar_wait(b_sfree, g & 1, abort_flag, p.err)) break;
+            bool ok = mbar_wait(b_q, 0, abort_flag, p.err) && issue_s(0);
+            for (int j = 0; ok && j < nkt; j++) {
+                // S_{j+1} as soon as the softmax warps hold S_j in registers,
+                // so that it overlaps their work on tile j
+                if (j + 1 < nkt) {
+                    if (!mbar_wait(b_sfree, j & 1, abort_flag, p.err)) break;
                     tc_fence_after();
-                    if (!issue_s(g + 1, ic2, j2, nkt2)) break;
+                    if (!issue_s(j + 1)) break;
                 }
-                if (!mbar_wait(b_pfull, g & 1, abort_flag, p.err)) break;
-                // a new item's first P.V overwrites O: the softmax warps must
-                // have read the previous item's
-                if (j == 0 && ic > 0 && !mbar_wait(b_ofree, (ic - 1) & 1, abort_flag, p.err))
-                    break;
+                if (!mbar_wait(b_pfull, j & 1, abort_flag, p.err)) break;
                 tc_fence_after();
-                const int it = 2 * g + 1, s = it % F_NRING;
+                const int it = 2 * j + 1, s = it % F_NRING;
                 if (!mbar_wait(b_full + 8 * s, (it / F_NRING) & 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint64_t dV = dRingV + (uint64_t)((s * TILE_BYTES) >> 4);
-                // O += P_j V_j (O starts at the item's first tile); P is read
-                // from TMEM, 16 keys (8 columns) per instruction
+                // O += P_j V_j (O starts at the first tile); P is read from TMEM,
+                // 16 keys (8 columns) per instruction
 #pragma unroll
                 for (int k = 0; k < TILE / 16; k++)
                     umma_bf16_tmem_a(tO, tP + (uint32_t)(8 * k), dV + (uint64_t)(k * 128), ID_O,
                                      (j > 0 || k > 0) ? 1u : 0u);
                 umma_commit(b_ofull);
                 umma_commit(b_empty + 8 * s);
-                if (nkt2 == 0) break;
-                ic = ic2;
-                j = j2;
-                nkt = nkt2;
             }
         }
     } else {
@@ -283,145 +229,114 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
         // stays <= 256 and most tiles need no rescale.
         const int q = warp & 3, hf = (warp - 1) >> 2;
         const int r = q * 32 + lane;
+        const int qi = qt * TILE + r;
         const uint32_t loff = (uint32_t)(q * 32) << 16;
         const int kb = hf * 64;
+        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        int g = 0;  // global tile count (barrier phases)
-        for (int ic = 0;; ic++) {
-            const int w = items.at(ic);
-            if (w < 0) break;
-            const int nkt = items.tile(w) + 1;  // the item's tile index is nkt - 1
-            float m_used = -INFINITY, l = 0.f;
-            // After a failed wait a warp keeps going round the loops without
-            // work, so that its partner warp still meets it at each barrier.
-            for (int j = 0; j < nkt; j++, g++) {
-                if (!ok || !warp_wait(b_sfull, g & 1, abort_flag, p.err, lane)) {
-                    ok = false;
-                    pair_sync(q);
-                    continue;
-                }
-                // two passes over S in TMEM, 32 columns at a time: the row max,
-                // then (after the exchange with the partner warp) the
-                // exponentials; S stays in TMEM until the second pass has read
-                // it, so only 32 of its columns occupy registers at once
-                tc_fence_after();
-                const bool diag = j == nkt - 1;  // causal mask: keys > row
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 2; c++) {
-                    uint32_t sv[32];
-                    tmem_ld32_async(tS + loff + kb + 32 * c, sv);
-                    tmem_wait32(sv);
-                    float m8[8];
-#pragma unroll
-                    for (int i = 0; i < 8; i++) m8[i] = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        const float v = (diag && kb + 32 * c + i > r) ? -INFINITY
-                                                                      : __uint_as_float(sv[i]);
-                        m8[i & 7] = fmaxf(m8[i & 7], v);
-                    }
-#pragma unroll
-                    for (int v = 4; v > 0; v >>= 1)
-#pragma unroll
-                        for (int i = 0; i < v; i++) m8[i] = fmaxf(m8[i], m8[i + v]);
-                    mx = fmaxf(mx, m8[0]);
-                }
-                float* rb = red + (g & 1) * 256;
-                rb[hf * 128 + r] = mx;
+        // After a failed wait a warp keeps going round the loop without work,
+        // so that its partner warp still meets it at each barrier.
+        for (int j = 0; j < nkt; j++) {
+            if (!ok || !warp_wait(b_sfull, j & 1, abort_flag, p.err, lane)) {
+                ok = false;
                 pair_sync(q);
-                const float mrow = fmaxf(rb[r], rb[128 + r]) * p.scale_log2;
-                const bool need = mrow > m_used + RESCALE_SLACK;
-                const float m_new = need ? mrow : m_used;
-                // P_j in registers (exponentials relative to m_new)
-                uint32_t pk[32];
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};  // the tile's row sum in 4 chains
-#pragma unroll
-                for (int c = 0; c < 2; c++) {
-                    uint32_t sv[32];
-                    tmem_ld32_async(tS + loff + kb + 32 * c, sv);
-                    tmem_wait32(sv);
-                    if (c == 1) {  // S is fully read: the next S may overwrite it
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(b_sfree);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const int k0 = kb + 32 * c + 2 * i;
-                        const float a = (diag && k0 > r)
-                                            ? 0.f
-                                            : ex2(fmaf(__uint_as_float(sv[2 * i]), p.scale_log2, -m_new));
-                        const float e = (diag && k0 + 1 > r)
-                                            ? 0.f
-                                            : ex2(fmaf(__uint_as_float(sv[2 * i + 1]), p.scale_log2, -m_new));
-                        l4[i & 3] += a + e;
-                        pk[16 * c + i] = pack_bf16x2(a, e);
-                    }
-                }
-                // P.V of the previous tile must be done: it reads the P columns
-                // of TMEM and writes O, which a rescale rewrites (an item's
-                // first tile follows the previous item's epilogue, which
-                // waited for its last P.V)
-                if (j > 0 && !warp_wait(b_ofull, (g - 1) & 1, abort_flag, p.err, lane)) {
-                    ok = false;
-                    continue;
-                }
-                tc_fence_after();
-                // keys [kb, kb+64) of each row: 32 packed columns of P (stored
-                // first, so that P's registers are free for a rescale of O)
-                tmem_st32(tP + loff + hf * 32, pk);
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    const float corr = need ? ex2(m_used - m_new) : 1.f;
-                    uint32_t t[32];
-                    tmem_ld32_async(tO + loff + hf * 32, t);
-                    tmem_wait32(t);
-#pragma unroll
-                    for (int i = 0; i < 32; i++) t[i] = __float_as_uint(__uint_as_float(t[i]) * corr);
-                    tmem_st32(tO + loff + hf * 32, t);
-                    l *= corr;
-                }
-                m_used = m_new;
-                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_pfull);
+                continue;
             }
-            const bool fin = ok && warp_wait(b_ofull, (g - 1) & 1, abort_flag, p.err, lane);
-            // fold the two halves' row sums (every softmax thread reaches this)
-            lsum[hf * 128 + r] = l;
+            tc_fence_after();
+            uint32_t sv[2][32];
+            tmem_ld32_async(tS + loff + kb, sv[0]);
+            tmem_ld32_async(tS + loff + kb + 32, sv[1]);
+            tmem_wait32(sv[0]);
+            tmem_wait32(sv[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_sfree);
+            if (j == qt) {  // causal mask of the diagonal tile: keys > row
+#pragma unroll
+                for (int c = 0; c < 2; c++)
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        if (kb + 32 * c + i > r) sv[c][i] = __float_as_uint(-INFINITY);
+            }
+            // row max over the 64 columns as a tree (8 independent chains),
+            // exchanged with the partner warp that holds the other 64
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) m8[i] = __uint_as_float(sv[0][i]);
+#pragma unroll
+            for (int i = 8; i < 64; i++) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i >> 5][i & 31]));
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; i++) m8[i] = fmaxf(m8[i], m8[i + w]);
+            const float mx = m8[0];
+            float* rb = red + (j & 1) * 256;
+            rb[hf * 128 + r] = mx;
             pair_sync(q);
-            const float lt = lsum[r] + lsum[128 + r];
-            const int qi = (nkt - 1) * TILE + r, bh = items.bh(w);
-            const bool st = fin && qi < p.T;
-            // fast reciprocal (MUFU, a few ulp; the output is rounded to bf16)
-            const float inv = __fdividef(1.f, lt);
-            bf16* dst = p.out + ((size_t)(bh / p.H * p.T + qi)) * p.C + bh % p.H * HD + hf * 32;
-            // O in two 16-column halves (fewer registers live at once)
-            if (fin) tc_fence_after();
+            const float mrow = fmaxf(rb[r], rb[128 + r]) * p.scale_log2;
+            const bool need = mrow > m_used + RESCALE_SLACK;
+            const float m_new = need ? mrow : m_used;
+            // P_j in registers first (exponentials relative to m_new)
+            uint32_t pk[32];
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};  // the tile's row sum in 4 chains
 #pragma unroll
-            for (int c = 0; c < 2; c++) {
-                uint32_t t[16];
-                if (fin) tmem_ld16(tO + loff + hf * 32 + 16 * c, t);
-                if (c == 1) {  // O is read: the next item's first P.V may overwrite it
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(b_ofree);
-                }
-                if (st) {
-#pragma unroll
-                    for (int i = 0; i < 16; i += 8) {
-                        uint4 u;
-                        u.x = pack_bf16x2(__uint_as_float(t[i]) * inv, __uint_as_float(t[i + 1]) * inv);
-                        u.y = pack_bf16x2(__uint_as_float(t[i + 2]) * inv, __uint_as_float(t[i + 3]) * inv);
-                        u.z = pack_bf16x2(__uint_as_float(t[i + 4]) * inv, __uint_as_float(t[i + 5]) * inv);
-                        u.w = pack_bf16x2(__uint_as_float(t[i + 6]) * inv, __uint_as_float(t[i + 7]) * inv);
-                        *reinterpret_cast<uint4*>(dst + 16 * c + i) = u;
-                    }
-                }
+            for (int i = 0; i < 32; i++) {
+                const float a =
+                    ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i) & 31]), p.scale_log2, -m_new));
+                const float e =
+                    ex2(fmaf(__uint_as_float(sv[i >> 4][(2 * i + 1) & 31]), p.scale_log2, -m_new));
+                l4[i & 3] += a + e;
+                pk[i] = pack_bf16x2(a, e);
             }
-            if (st && hf == 0)
-                p.lse[(size_t)bh * p.T + qi] = (m_used + __log2f(lt)) * 0.6931471805599453f;
+            // P.V of the previous tile must be done: it reads the P columns of
+            // TMEM and writes O, which a rescale rewrites
+            if (j > 0 && !warp_wait(b_ofull, (j - 1) & 1, abort_flag, p.err, lane)) {
+                ok = false;
+                continue;
+            }
+            tc_fence_after();
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                const float corr = need ? ex2(m_used - m_new) : 1.f;
+                uint32_t t[32];
+                tmem_ld32_async(tO + loff + hf * 32, t);
+                tmem_wait32(t);
+#pragma unroll
+                for (int i = 0; i < 32; i++) t[i] = __float_as_uint(__uint_as_float(t[i]) * corr);
+                tmem_st32(tO + loff + hf * 32, t);
+                l *= corr;
+            }
+            m_used = m_new;
+            l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            // keys [kb, kb+64) of each row: 32 packed columns of P
+            tmem_st32(tP + loff + hf * 32, pk);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pfull);
+        }
+        bool fin = ok && warp_wait(b_ofull, (nkt - 1) & 1, abort_flag, p.err, lane);
+        uint32_t t[32];
+        if (fin) {
+            tc_fence_after();
+            tmem_ld32_async(tO + loff + hf * 32, t);
+            tmem_wait32(t);
+        }
+        // fold the two halves' row sums (every softmax thread reaches this)
+        lsum[hf * 128 + r] = l;
+        pair_sync(q);
+        if (fin && qi < p.T) {
+            const float lt = lsum[r] + lsum[128 + r];
+            const float inv = 1.f / lt;
+            bf16* dst = p.out + ((size_t)(row0 + qi)) * p.C + h * HD + hf * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                uint4 u;
+                u.x = pack_bf16x2(__uint_as_float(t[i]) * inv, __uint_as_float(t[i + 1]) * inv);
+                u.y = pack_bf16x2(__uint_as_float(t[i + 2]) * inv, __uint_as_float(t[i + 3]) * inv);
+                u.z = pack_bf16x2(__uint_as_float(t[i + 4]) * inv, __uint_as_float(t[i + 5]) * inv);
+                u.w = pack_bf16x2(__uint_as_float(t[i + 6]) * inv, __uint_as_float(t[i + 7]) * inv);
+                *reinterpret_cast<uint4*>(dst + i) = u;
+            }
+            if (hf == 0) p.lse[(size_t)bh * p.T + qi] = (m_used + log2f(lt)) * 0.6931471805599453f;
         }
         tc_fence_before();
     }
@@ -1061,17 +976,7 @@ cudaError_t attention_forward_tc(void* out, float* lse, const void* qkv, int B, 
     p.lse = lse;
     p.err = err;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-    // persistent: every resident CTA slot takes a share of the work items
-    static int occ = 0;
-    if (!occ && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attn_fwd_tc, FWD_THREADS,
-                                                               F_SMEM) != cudaSuccess ||
-                 occ < 1))
-        occ = 1;
-    int dev = 0, nsm = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    const long nitems = (long)B * H * p.nqt;
-    const int grid = (int)std::min<long>(nitems, (long)nsm * occ);
+    dim3 grid(B * H, p.nqt);
     launch_pdl(k_attn_fwd_tc, grid, FWD_THREADS, F_SMEM, s, map, p);
     return cudaGetLastError();
 }
