@@ -8,8 +8,8 @@ activations (GBs) are far larger than the 126 MB L2, so no flush is needed.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 124M|350M|1558M]
     python bench.py --impl reference ...   # the CPU oracle, timed on host cores
 
-Under torchrun (N > 1) every rank trains its own replica (no collective: the
-data-parallel gradient exchange is not part of this one-GPU build); the
+Under torchrun (N > 1) every rank trains its own replica, with no collective
+(the data-parallel gradient exchange, dp.DataParallel, is not timed here); the
 timed region is bracketed by barriers and the slowest rank's time is used.
 """
 import argparse
@@ -47,7 +47,7 @@ DESCR = {
 # of many steps stays within minutes); the cpu_baseline of the GPU run times
 # one longer sample (about ten seconds of CPU work on the 124M architecture).
 CPU_SAMPLE = dict(B=1, T=32)
-BASELINE_SAMPLE = dict(B=1, T=256)
+CPU_BASELINE_SAMPLE = dict(B=1, T=256)
 
 
 def n_params(L, C, V, T):
@@ -336,10 +336,10 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, cores, times = cpu_oracle_step_rate(w, BASELINE_SAMPLE, steps=1, warmup=0)
+        rate, cores, times = cpu_oracle_step_rate(w, CPU_BASELINE_SAMPLE, steps=1, warmup=0)
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{args.workload} architecture, B={BASELINE_SAMPLE['B']} "
-                         f"T={BASELINE_SAMPLE['T']}, one full step (forward, backward, AdamW), "
+               "sample": f"{args.workload} architecture, B={CPU_BASELINE_SAMPLE['B']} "
+                         f"T={CPU_BASELINE_SAMPLE['T']}, one full step (forward, backward, AdamW), "
                          f"fp64 oracle, {statistics.mean(times):.1f} s",
                "cpu": cpu_model()}
 

@@ -292,7 +292,7 @@ template <typename T, int VEC, int IT>
 static cudaError_t ln_fwd_launch(void* out, float* mean, float* rstd, const void* x,
                                  const void* w, const void* b, int N, int C, cudaStream_t s) {
     auto kern = k_ln_fwd<T, VEC, IT>;
-    static int occ = 0;  // resident blocks per SM (same on every device of this build)
+    static int occ = 0;  // resident blocks per SM (the same on every device it runs on)
     if (!occ && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 256, 0) != cudaSuccess ||
                  occ < 1))
         occ = 1;
