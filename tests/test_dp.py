@@ -96,26 +96,69 @@ class OracleShardModel:
         return norm
 
 
-def _micro_grad(rank, step, k):
+def _micro_grad(rank, step, k, n=N_PARAMS):
     g = torch.Generator().manual_seed(1000 * rank + 10 * step + k)
-    return torch.randn(N_PARAMS, generator=g, dtype=torch.float64)
+    return torch.randn(n, generator=g, dtype=torch.float64)
 
 
-def _gloo_rank(rank, world, port, q):
+def _gloo_rank(rank, world, port, q, n=N_PARAMS):
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
                             world_size=world)
     try:
-        model = OracleShardModel(N_PARAMS, seed=5)
+        model = OracleShardModel(n, seed=5)
         dp = DataParallel(model)
         norms = []
         for step in range(STEPS):
             model.zero_grad()
             for k in range(MICRO):
-                model.accumulate(_micro_grad(rank, step, k))
+                model.accumulate(_micro_grad(rank, step, k, n))
             norms.append(dp.step(**HP))
         q.put((rank, model.w.numpy().copy(), model.m.numpy().copy(), norms))
     finally:
         dist.destroy_process_group()
+
+
+def _run_gloo(world, n):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gloo_rank, args=(r, world, port, q, n)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(world):
+        rank, w, m, norms = q.get(timeout=120)
+        got[rank] = (w, m, norms)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    return got
+
+
+@pytest.mark.parametrize("world,n", [(3, 1000), (4, 10)], ids=["3-ranks", "4-ranks-empty-shards"])
+def test_data_parallel_gloo_more_ranks(world, n):
+    """three ranks (ragged last slice) and four ranks over 10 parameters (one
+    64-aligned slice holds everything, the other ranks update nothing but still
+    take part): every rank ends with the one-process result; the all-reduce
+    of more than two ranks may add in another order, hence a tolerance"""
+    got = _run_gloo(world, n)
+    ref = OracleShardModel(n, seed=5)
+    for step in range(STEPS):
+        ref.zero_grad()
+        total = torch.zeros(n, dtype=torch.float64)
+        for r in range(world):
+            for k in range(MICRO):
+                total += _micro_grad(r, step, k, n)
+        ref.g.copy_(total)
+        ref.set_grad_count(world * MICRO)
+        ref.adamw_step_shard(0, n, **HP)
+    bounds = shard_bounds(n, world)
+    for r in range(world):
+        w, m, norms = got[r]
+        np.testing.assert_allclose(w, ref.w.numpy(), rtol=1e-12, atol=1e-15)
+        lo, hi = bounds[r]
+        np.testing.assert_allclose(m[lo:hi], ref.m.numpy()[lo:hi], rtol=1e-12, atol=1e-15)
+        assert all(got[q][2] == norms for q in range(world))  # one summed gradient everywhere
 
 
 def test_data_parallel_gloo_two_ranks_equals_one_process():
