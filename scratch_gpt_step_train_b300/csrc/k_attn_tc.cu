@@ -24,9 +24,9 @@
 //                   row sum rescaled in TMEM) only when a row max exceeds it
 //                   by more than 2^8.
 // Keys are visited in tiles 0..q (q = the query tile); only the diagonal tile
-// needs the causal mask.  Each CTA is sized so that two could share an SM
-// (~100 KB smem, 256 TMEM columns each, one CTA's softmax overlapping the
-// other's products); the occupancy query reports one per SM on this device.
+// needs the causal mask.  Two CTAs share an SM (~100 KB smem, 256 TMEM
+// columns and 96 registers a thread each), so one CTA's softmax overlaps the
+// other's products.
 // Outputs: O [B,T,C] (bf16) and the row log-sum-exp [B,H,T] (fp32, natural
 // log), which the backward pass uses to recompute P.
 #include "common.cuh"
@@ -365,8 +365,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
 // Each CTA owns its outputs: no atomics, deterministic.
 // The 128-row side of each kernel (keys in k_attn_dkv_tc, queries in
 // k_attn_dq_tc) is visited in steps of 64 on the other side, so every CTA
-// holds at most 256 TMEM columns and ~100 KB of shared memory, sized for two
-// CTAs per SM (the occupancy query reports one on this device).
+// holds at most 256 TMEM columns and ~100 KB of shared memory: two CTAs share
+// an SM, and one CTA's softmax phase overlaps the other's products.
 constexpr int BWD_THREADS = 288;  // warp 0: TMA (lane 0) + MMA (lane 1); 8 softmax warps
 constexpr int SUB = 64;           // rows of the 64-wide side
 constexpr int SUB_BYTES = SUB * 128;
