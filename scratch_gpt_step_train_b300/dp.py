@@ -5,7 +5,8 @@ in llm.c", "Training": one process per GPU, gradients averaged over the ranks.
 One process per GPU, each with its own GPT2 handle of the same shape and
 parameters.  A step is: every rank runs its micro-batches (forward +
 backward); then DataParallel.step() sums the gradient vectors of all ranks in
-place (all-reduce), sets the divisor to (ranks x micro-batches), lets every
+place (all-reduce), sets the divisor to the micro-batch count summed over the
+ranks, lets every
 rank update its own slice of the canonical parameter vector (the clip and the
 norm from the whole summed gradient, identical on every rank), and exchanges
 the updated slices (each rank broadcasts its slice of the fp32 master and of
@@ -54,7 +55,11 @@ class DataParallel:
         s = getattr(self.model, "stream", None)
         with torch.cuda.stream(s) if s is not None else nullcontext():
             dist.all_reduce(self.grads, op=dist.ReduceOp.SUM, group=self.group)
-            self.model.set_grad_count(self.model.grad_count() * self.world)
+            # the divisor: micro-batches summed over the ranks (they may differ)
+            count = torch.tensor([self.model.grad_count()], dtype=torch.int64,
+                                 device=self.grads.device)
+            dist.all_reduce(count, op=dist.ReduceOp.SUM, group=self.group)
+            self.model.set_grad_count(int(count.item()))
             lo, hi = self.bounds[self.rank]
             norm = self.model.adamw_step_shard(lo, hi, lr, b1, b2, eps, wd, clip)
             for r, (a, b) in enumerate(self.bounds):

@@ -101,7 +101,11 @@ def _micro_grad(rank, step, k, n=N_PARAMS):
     return torch.randn(n, generator=g, dtype=torch.float64)
 
 
-def _gloo_rank(rank, world, port, q, n=N_PARAMS):
+def _micro_count(rank, uneven):
+    return MICRO + rank if uneven else MICRO
+
+
+def _gloo_rank(rank, world, port, q, n=N_PARAMS, uneven=False):
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
                             world_size=world)
     try:
@@ -110,7 +114,7 @@ def _gloo_rank(rank, world, port, q, n=N_PARAMS):
         norms = []
         for step in range(STEPS):
             model.zero_grad()
-            for k in range(MICRO):
+            for k in range(_micro_count(rank, uneven)):
                 model.accumulate(_micro_grad(rank, step, k, n))
             norms.append(dp.step(**HP))
         q.put((rank, model.w.numpy().copy(), model.m.numpy().copy(), norms))
@@ -118,11 +122,12 @@ def _gloo_rank(rank, world, port, q, n=N_PARAMS):
         dist.destroy_process_group()
 
 
-def _run_gloo(world, n):
+def _run_gloo(world, n, uneven=False):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_gloo_rank, args=(r, world, port, q, n)) for r in range(world)]
+    procs = [ctx.Process(target=_gloo_rank, args=(r, world, port, q, n, uneven))
+             for r in range(world)]
     for p in procs:
         p.start()
     got = {}
@@ -135,22 +140,24 @@ def _run_gloo(world, n):
     return got
 
 
-@pytest.mark.parametrize("world,n", [(3, 1000), (4, 10)], ids=["3-ranks", "4-ranks-empty-shards"])
-def test_data_parallel_gloo_more_ranks(world, n):
-    """three ranks (ragged last slice) and four ranks over 10 parameters (one
+@pytest.mark.parametrize("world,n,uneven", [(3, 1000, False), (4, 10, False), (3, 1000, True)],
+                         ids=["3-ranks", "4-ranks-empty-shards", "3-ranks-uneven-micro-batches"])
+def test_data_parallel_gloo_more_ranks(world, n, uneven):
+    """three ranks (ragged last slice), four ranks over 10 parameters (one
     64-aligned slice holds everything, the other ranks update nothing but still
-    take part): every rank ends with the one-process result; the all-reduce
-    of more than two ranks may add in another order, hence a tolerance"""
-    got = _run_gloo(world, n)
+    take part), and three ranks with 2, 3 and 4 micro-batches (the divisor is
+    their sum): every rank ends with the one-process result; the all-reduce of
+    more than two ranks may add in another order, hence a tolerance"""
+    got = _run_gloo(world, n, uneven)
     ref = OracleShardModel(n, seed=5)
     for step in range(STEPS):
         ref.zero_grad()
         total = torch.zeros(n, dtype=torch.float64)
         for r in range(world):
-            for k in range(MICRO):
+            for k in range(_micro_count(r, uneven)):
                 total += _micro_grad(r, step, k, n)
         ref.g.copy_(total)
-        ref.set_grad_count(world * MICRO)
+        ref.set_grad_count(sum(_micro_count(r, uneven) for r in range(world)))
         ref.adamw_step_shard(0, n, **HP)
     bounds = shard_bounds(n, world)
     for r in range(world):
