@@ -29,6 +29,13 @@
 extern "C" {
 #endif
 
+/* The architecture the library's kernels were built for, as the CUDA runtime
+ * reports it for the loaded tensor-core matmul kernel on the current device
+ * (cudaFuncAttributes.binaryVersion: major*10 + minor, 103 for sm_103a), or
+ * -2 (GPT2_ERR_CUDA) if the kernel cannot be loaded on this device.  Needs a
+ * GPU; it launches nothing. */
+int gpt2k_binary_arch(void);
+
 /* Linear layer, forward and backward ("Karpathy's llm.c: understanding LLM
  * training from scratch in C/CUDA", "Code anatomy": the QKV / projection /
  * MLP / classifier matmuls):  D[M,N] = epi(sum_k A[m,k] B[n,k]).

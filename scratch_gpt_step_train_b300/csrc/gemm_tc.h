@@ -9,6 +9,8 @@ bool gemm_tc_available();
 // true if this descriptor's shape, strides and alignment fit the kernel:
 // bf16, N % 8 == 0, 16-byte aligned bases, leading dimensions % 8 == 0
 bool gemm_tc_supported(const GemmDesc& d);
+// binaryVersion of the loaded tensor-core GEMM kernel (major*10+minor), or -1
+int gemm_tc_binary_version();
 // bytes of scratch the split-K weight-gradient products may use
 size_t gemm_tc_scratch_bytes();
 // D = epilogue(A . B^T).  scratch: split-K partials (may be NULL: no split);

@@ -24,8 +24,6 @@
 //             the tile's columns: tcgen05.ld in 32-column chunks, bias / GELU
 //             / residual / fp32 accumulate, staged in shared memory and
 //             written by TMA bulk stores
-// With MC, CTA pairs (clusters of 2) on vertically adjacent tiles share the
-// B tile: each loads one half and multicasts it to both.
 // Two TMEM accumulators let the epilogue of tile i overlap the mainloop of
 // tile i+1.  Every mbarrier wait is bounded (clock64 budget): on expiry the
 // CTA raises an abort flag, sets GPT2_DEVERR_TIMEOUT in the device error
@@ -282,10 +280,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
 }
 
 // ------------------------------------------------------------------- kernel
-// MC: CTA pairs (cluster of 2) on adjacent 128-row tiles of the same output
-// columns; each CTA loads its own A tile and half of the B tile, multicast to
-// both, so the pair reads B once.
-template <int BN, bool A_MN, bool B_MN, bool MC>
+template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const __grid_constant__ EpiMaps maps, TcParams p) {
@@ -307,7 +302,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(full + 8 * s, 1);
-            mbar_init(empty + 8 * s, MC ? 2 : 1);
+            mbar_init(empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(tfull + 8 * b, 1);
@@ -324,18 +319,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
     }
     __syncthreads();
-    if (MC) cluster_sync_all();  // the peer's barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     gdc_wait();  // setup above touches no global memory
     gdc_launch_dependents();
-    // work units: single tiles, or (with MC) pairs of vertically adjacent tiles
-    const int rank = MC ? (int)cluster_ctarank() : 0;
-    const int units_m = MC ? (p.tiles_m + 1) / 2 : p.tiles_m;
+    // work units: output tiles (times K splits), strided over the CTAs
+    const int units_m = p.tiles_m;
     const int units_mn = units_m * p.tiles_n;
     const int num_units = units_mn * p.splits;
-    const int unit0 = MC ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-    const int ustep = MC ? (int)gridDim.x / 2 : (int)gridDim.x;
+    const int unit0 = (int)blockIdx.x;
+    const int ustep = (int)gridDim.x;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -348,7 +341,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int split = u / units_mn, r = u % units_mn;
                 const int um = p.n_fastest ? r / p.tiles_n : r % units_m;
                 const int tn = p.n_fastest ? r % p.tiles_n : r / units_m;
-                const int tm = MC ? 2 * um + rank : um;
+                const int tm = um;
                 const int k0 = split * p.k_per_split;
                 const int k1 = min(p.K, k0 + p.k_per_split);
                 const int nkb = (k1 - k0 + BK - 1) / BK;
@@ -367,16 +360,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_2d(sa, &mapA, fb, tm * BM, kk);
                         tma_load_2d(sa + 8192, &mapA, fb, tm * BM + 64, kk);
                     }
-                    if (MC) {
-                        if (!B_MN) {
-                            tma_load_2d_mc(sb + rank * (BN / 2) * 128, &mapB, fb, kk,
-                                           tn * BN + rank * (BN / 2), 3);
-                        } else {
-#pragma unroll
-                            for (int j = rank * (BN / 128); j < (rank + 1) * (BN / 128); j++)
-                                tma_load_2d_mc(sb + j * 8192, &mapB, fb, tn * BN + 64 * j, kk, 3);
-                        }
-                    } else if (!B_MN) {
+                    if (!B_MN) {
                         tma_load_2d(sb, &mapB, fb, kk, tn * BN);
                     } else {
 #pragma unroll
@@ -440,8 +424,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         umma_bf16(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
                                   bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
                                   (kb > 0 || k > 0) ? 1u : 0u);
-                    if (MC) umma_commit_mc(empty + 8 * s, 3);
-                    else umma_commit(empty + 8 * s);
+                    umma_commit(empty + 8 * s);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -464,7 +447,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int split = u / units_mn, r = u % units_mn;
             const int um = p.n_fastest ? r / p.tiles_n : r % units_m;
             const int tn = p.n_fastest ? r % p.tiles_n : r / units_m;
-            const int tm = MC ? 2 * um + rank : um;
+            const int tm = um;
             const int b = lt & 1;
             const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
             const int row = tm * BM + q * 32 + lane;
@@ -505,7 +488,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     }
     __syncthreads();
-    if (MC) cluster_sync_all();  // no multicast or remote arrive targets an exited CTA
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -541,9 +523,9 @@ EncodeTiledFn g_encode = nullptr;
 int g_num_sms = 148;
 int g_state = -1;  // -1 unknown, 0 unavailable, 1 ready
 
-template <int BN, bool AM, bool BMN, bool MC>
+template <int BN, bool AM, bool BMN>
 void set_smem_attr() {
-    cudaFuncSetAttribute(k_gemm_tc<BN, AM, BMN, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(k_gemm_tc<BN, AM, BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg<BN>::SMEM);
 }
 
@@ -595,9 +577,7 @@ bool make_epi_maps(EpiMaps* em, const GemmDesc& d, const TcParams& tp) {
     return ok;
 }
 
-int g_mc_clusters = 0;  // co-resident 2-CTA clusters of the multicast kernel
-
-template <int BN, bool AM, bool BMN, bool MC>
+template <int BN, bool AM, bool BMN>
 cudaError_t launch(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     CUtensorMap ma, mb;
     EpiMaps em;
@@ -605,34 +585,13 @@ cudaError_t launch(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     // A: K-major -> [M rows][K], box 64(K) x 128(M);  MN-major -> [K rows][M], box 64(M) x 64(K)
     bool ok = AM ? make_map(&ma, d.A, d.M, d.K, d.lda, 64)
                  : make_map(&ma, d.A, d.K, d.M, d.lda, BM);
-    // B: K-major box 64(K) x BN rows (half of them per CTA with multicast)
+    // B: K-major box 64(K) x BN rows;  N-major box 64(N) x 64(K)
     ok = ok && (BMN ? make_map(&mb, d.B, d.N, d.K, d.ldb, 64)
-                    : make_map(&mb, d.B, d.K, d.N, d.ldb, MC ? BN / 2 : BN));
+                    : make_map(&mb, d.B, d.K, d.N, d.ldb, BN));
     if (!ok) return cudaErrorInvalidValue;
-    if (!MC) {
-        const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
-        launch_pdl(k_gemm_tc<BN, AM, BMN, false>, grid, NUM_THREADS, Cfg<BN>::SMEM, s, ma, mb, em, tp);
-        return cudaGetLastError();
-    }
-    const int units = ((tp.tiles_m + 1) / 2) * tp.tiles_n * tp.splits;
-    int clusters = g_mc_clusters > 0 ? g_mc_clusters : g_num_sms / 2;
-    if (units < clusters) clusters = units;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, AM, BMN, true>, ma, mb, em, tp);
+    const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
+    launch_pdl(k_gemm_tc<BN, AM, BMN>, grid, NUM_THREADS, Cfg<BN>::SMEM, s, ma, mb, em, tp);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -655,42 +614,26 @@ bool gemm_tc_available() {
         return false;
     }
     g_encode = (EncodeTiledFn)fn;
-    set_smem_attr<256, false, false, false>();
-    set_smem_attr<256, false, true, false>();
-    set_smem_attr<256, true, false, false>();
-    set_smem_attr<256, true, true, false>();
-    set_smem_attr<128, false, false, false>();
-    set_smem_attr<128, false, true, false>();
-    set_smem_attr<128, true, false, false>();
-    set_smem_attr<128, true, true, false>();
-    set_smem_attr<256, false, false, true>();
-    set_smem_attr<256, false, true, true>();
-    set_smem_attr<256, true, false, true>();
-    set_smem_attr<256, true, true, true>();
-    {
-        // how many 2-CTA clusters of the multicast kernel fit at once
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(g_num_sms);
-        cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = Cfg<256>::SMEM;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<256, false, false, true>, &cfg) ==
-                cudaSuccess &&
-            n > 0)
-            g_mc_clusters = n < g_num_sms / 2 ? n : g_num_sms / 2;
-        cudaGetLastError();
-    }
+    set_smem_attr<256, false, false>();
+    set_smem_attr<256, false, true>();
+    set_smem_attr<256, true, false>();
+    set_smem_attr<256, true, true>();
+    set_smem_attr<128, false, false>();
+    set_smem_attr<128, false, true>();
+    set_smem_attr<128, true, false>();
+    set_smem_attr<128, true, true>();
     if (cudaGetLastError() != cudaSuccess) return false;
     g_state = 1;
     return true;
+}
+
+int gemm_tc_binary_version() {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, k_gemm_tc<256, false, false>) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return a.binaryVersion;
 }
 
 void* tc_encode_fn() { return gemm_tc_available() ? (void*)g_encode : nullptr; }
@@ -731,11 +674,9 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
         // over the SMs, each unit's k-blocks at the tile width's rate, plus the
         // fp32 traffic of the output (read-modify-write) and of the split's
         // partial sums (written, then read back by the ordered reduction).
-        // The k-block rates are measured ones: a 128 x 128 tile needs twice
-        // the L2 bytes per flop of a 128 x 256 tile whose B half is shared by
-        // a CTA pair, and runs at about the same k-block time, i.e. half the
-        // flop rate.
-        const double kblock_us[2] = {0.30, 0.31};  // 128x256 (paired) / 128x128
+        // The k-block rates are measured ones (128 x 256 and 128 x 128 tiles,
+        // each CTA loading its whole A and B tiles).
+        const double kblock_us[2] = {0.30, 0.31};  // 128x256 / 128x128
         const double bytes_per_us = 5.0e6;
         const double mn4 = 4.0 * d.M * d.N;
         double best = 1e30;
@@ -786,23 +727,17 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     }
     tp.num_tiles = (int)(tiles * tp.splits);
     const bool am = !d.a_kmajor, bm = !d.b_kmajor;
-    const bool mc = BN == 256 && tiles_m >= 2;
     cudaError_t e;
-    if (BN == 256 && mc) {
-        if (!am && !bm) e = launch<256, false, false, true>(d, tp, s);
-        else if (!am && bm) e = launch<256, false, true, true>(d, tp, s);
-        else if (am && !bm) e = launch<256, true, false, true>(d, tp, s);
-        else e = launch<256, true, true, true>(d, tp, s);
-    } else if (BN == 256) {
-        if (!am && !bm) e = launch<256, false, false, false>(d, tp, s);
-        else if (!am && bm) e = launch<256, false, true, false>(d, tp, s);
-        else if (am && !bm) e = launch<256, true, false, false>(d, tp, s);
-        else e = launch<256, true, true, false>(d, tp, s);
+    if (BN == 256) {
+        if (!am && !bm) e = launch<256, false, false>(d, tp, s);
+        else if (!am && bm) e = launch<256, false, true>(d, tp, s);
+        else if (am && !bm) e = launch<256, true, false>(d, tp, s);
+        else e = launch<256, true, true>(d, tp, s);
     } else {
-        if (!am && !bm) e = launch<128, false, false, false>(d, tp, s);
-        else if (!am && bm) e = launch<128, false, true, false>(d, tp, s);
-        else if (am && !bm) e = launch<128, true, false, false>(d, tp, s);
-        else e = launch<128, true, true, false>(d, tp, s);
+        if (!am && !bm) e = launch<128, false, false>(d, tp, s);
+        else if (!am && bm) e = launch<128, false, true>(d, tp, s);
+        else if (am && !bm) e = launch<128, true, false>(d, tp, s);
+        else e = launch<128, true, true>(d, tp, s);
     }
     if (e != cudaSuccess) return e;
     if (nlaunch) *nlaunch = 1;

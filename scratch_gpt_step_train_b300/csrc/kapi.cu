@@ -19,6 +19,11 @@ static bool dt_ok(int dtype) { return dtype == ACT_F32 || dtype == ACT_BF16; }
 
 extern "C" size_t gpt2k_matmul_scratch_bytes(void) { return gemm_tc_scratch_bytes(); }
 
+extern "C" int gpt2k_binary_arch(void) {
+    const int v = gemm_tc_binary_version();
+    return v < 0 ? GPT2_ERR_CUDA : v;
+}
+
 extern "C" int gpt2k_matmul(int dtype, int impl, int M, int N, int K, const void* A, long lda,
                             int a_kmajor, const void* B, long ldb, int b_kmajor, void* D,
                             long ldd, const void* bias, const void* resid, long ldr, void* aux,

@@ -10,6 +10,7 @@ from .gpt2 import GPT2Error, lib
 
 _vp, _i, _l, _sz, _f = ct.c_void_p, ct.c_int, ct.c_long, ct.c_size_t, ct.c_float
 SIGNATURES = {
+    "gpt2k_binary_arch": (_i, []),
     "gpt2k_matmul_scratch_bytes": (_sz, []),
     "gpt2k_matmul": (_i, [_i, _i, _i, _i, _i, _vp, _l, _i, _vp, _l, _i, _vp, _l, _vp, _vp, _l,
                           _vp, _l, _i, _vp, _sz, _vp, _vp]),

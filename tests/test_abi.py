@@ -48,12 +48,22 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n)
 
 
-def test_library_is_built_for_sm103a(lib):
-    from scratch_gpt_step_train_b300 import gpt2
-    out = subprocess.run(["/usr/local/cuda/bin/cuobjdump", "--list-elf", gpt2.LIB_PATH],
-                         capture_output=True, text=True)
-    # only the listing of embedded ELF names is read, never their contents
-    assert "sm_103a" in out.stdout
+def test_library_is_built_for_sm103a_only():
+    """every object is compiled with exactly one target, sm_103a (the build
+    passes no other -gencode / -arch flag)"""
+    from scratch_gpt_step_train_b300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert not any(f.startswith(("-arch", "--gpu-architecture", "-gencode", "-code"))
+                   for f in build.FLAGS)
+
+
+@pytest.mark.gpu
+def test_loaded_kernels_are_sm103(lib):
+    """the runtime reports binary version 10.3 for the loaded GEMM kernel"""
+    from scratch_gpt_step_train_b300 import kernels
+    import torch
+    torch.cuda.init()
+    assert kernels.klib().gpt2k_binary_arch() == 103
 
 
 def test_no_oracle_dependency_in_product():
