@@ -48,6 +48,7 @@ DESCR = {
 # one longer sample (about ten seconds of CPU work on the 124M architecture).
 CPU_SAMPLE = dict(B=1, T=32)
 CPU_BASELINE_SAMPLE = dict(B=1, T=256)
+CPU_SAMPLE_1558M = dict(B=1, T=128)
 
 
 def n_params(L, C, V, T):
@@ -101,10 +102,11 @@ def load_peaks():
 
 
 # --------------------------------------------------------------------------- CPU
-def cpu_oracle_step_rate(w, sample, steps=1, warmup=0):
-    """Time the oracle (fp64 build, all host cores) on `sample` tokens of the
-    workload's architecture: forward + backward + AdamW per step.  Runs in a
-    fresh interpreter so no CUDA context is shared with it."""
+def cpu_oracle_step_rate(w, sample, steps=1, warmup=0, threads=None):
+    """Time the oracle (fp64 build) on `sample` tokens of the workload's
+    architecture: forward + backward + AdamW per step, with `threads` OpenMP
+    threads (default: all host cores).  Runs in a fresh interpreter so no
+    CUDA context is shared with it.  Returns (tokens/s, threads, step times)."""
     code = f"""
 import json, os, sys, time
 sys.path.insert(0, {ROOT!r})
@@ -124,7 +126,7 @@ for i in range({steps + warmup}):
     times.append(time.perf_counter() - t0)
 print(json.dumps(dict(times=times[{warmup}:])))
 """
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     env = dict(os.environ, OMP_NUM_THREADS=str(cores))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
                        timeout=1800)
@@ -133,6 +135,51 @@ print(json.dumps(dict(times=times[{warmup}:])))
     times = json.loads(r.stdout.strip().splitlines()[-1])["times"]
     tok = sample["B"] * sample["T"]
     return tok * len(times) / sum(times), cores, times
+
+
+def oracle_bytes(w, sample):
+    """host memory the fp64 oracle holds for this architecture and sample:
+    params, grads, m, v and the activations it keeps for the backward"""
+    L, H, C, V, T, B = w["L"], w["H"], w["C"], w["V"], sample["T"], sample["B"]
+    Vp = ((V + 127) // 128) * 128
+    n = n_params(L, C, V, T)
+    act = L * (17 * B * T * C + B * H * T * T) + 3 * B * T * Vp + 16 * B * T * C
+    return 8 * (4 * n + act)
+
+
+def mem_available():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def cpu_baselines():
+    """The oracle, as it stands, on bounded samples of the workloads: the
+    124M architecture at all host cores and at one thread, and the 1558M
+    architecture at all cores (skipped, with the reason, when the host has
+    not the memory for it)."""
+    runs = []
+    for wl, sample, threads in (("124M", CPU_BASELINE_SAMPLE, None),
+                                ("124M", CPU_SAMPLE, 1),
+                                ("1558M", CPU_SAMPLE_1558M, None)):
+        w = WORKLOADS[wl]
+        need, have = oracle_bytes(w, sample), mem_available()
+        desc = (f"{wl} architecture, B={sample['B']} T={sample['T']}, one full step "
+                f"(forward, backward, AdamW), fp64 oracle")
+        if have is not None and need * 1.25 > have:
+            runs.append({"sample": desc, "skipped": f"needs {need / 2**30:.0f} GiB of host "
+                         f"memory, {have / 2**30:.0f} GiB available"})
+            continue
+        rate, cores, times = cpu_oracle_step_rate(w, sample, steps=1, warmup=0, threads=threads)
+        runs.append({"value": rate, "unit": "tokens/s", "cores": cores,
+                     "sample": f"{desc}, {statistics.mean(times):.1f} s"})
+    head = runs[0]
+    return {"value": head["value"], "unit": "tokens/s", "cores": head["cores"], "kind": "oracle",
+            "sample": head["sample"], "cpu": cpu_model(), "runs": runs}
 
 
 def cpu_model():
@@ -192,8 +239,19 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- GPU
-def run_gpu(args, w, rank, world):
-    import numpy as np
+def run_gpu(w, rank, world, steps, warmup, accum, rl_steps):
+    """Train the workload's model on this rank's GPU and time it.
+
+    1. warm-up steps (untimed);
+    2. the timed region: `steps` whole steps between CUDA events on the
+       handle's stream, no per-kernel instrumentation, clocks sampled;
+    3. a roofline pass (not part of the value): one step with events around
+       every kernel class picks the dominant class, then `rl_steps` steps with
+       events around that class alone give its average launch duration;
+    4. end to end through the public host-buffer call, the same number of
+       steps as the timed region: pinned host tokens copied every micro-step,
+       the loss read back every step (with the update's norm, clip state and
+       error word: 20 bytes), timed on the host clock."""
     import torch
     from scratch_gpt_step_train_b300 import inputs
     from scratch_gpt_step_train_b300.gpt2 import BF16, GPT2
@@ -201,14 +259,13 @@ def run_gpu(args, w, rank, world):
     dev = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream()
-    B, T, accum = w["B"], w["T"], args.accum or w["accum"]
+    B, T = w["B"], w["T"]
     hp = w["hp"]
     with torch.cuda.stream(stream):
         model = GPT2(w["L"], w["H"], w["C"], w["V"], T, B, seed=1, mode=BF16, stream=stream)
     # synthetic Zipf(1.1) tokens, resident on the device before timing
     zs = inputs.ZipfStream(2 + rank, B, T, w["V"])
-    nbuf = accum
-    host = [zs.next() for _ in range(nbuf)]
+    host = [zs.next() for _ in range(accum)]
     dtok = [torch.from_numpy(a).to(f"cuda:{dev}") for a, _ in host]
     dtgt = [torch.from_numpy(b).to(f"cuda:{dev}") for _, b in host]
     torch.cuda.synchronize()
@@ -224,19 +281,12 @@ def run_gpu(args, w, rank, world):
         if world > 1:
             torch.distributed.barrier()
 
-    # calibration pass: which kernel class dominates (events on every class)
-    model.prof_enable(None)
-    step()
     model.prof_enable([])
-    prof = model.prof_read()
-    dom = max(prof, key=lambda k: prof[k][0])
-    model.prof_reset()
-    for _ in range(max(0, args.warmup - 1)):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
 
-    # timed region: events around the dominant class only
-    model.prof_enable([dom])
+    # timed region
     clocks = ClockSampler(dev)
     barrier()
     torch.cuda.synchronize()
@@ -244,10 +294,9 @@ def run_gpu(args, w, rank, world):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    losses = []
     # an NVTX range marks the timed steps for profilers (a no-op otherwise)
     torch.cuda.nvtx.range_push("timed_steps")
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     torch.cuda.nvtx.range_pop()
     ev1.record(stream)
@@ -256,33 +305,46 @@ def run_gpu(args, w, rank, world):
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
     launches = model.launch_count() - launches0
-    model.prof_enable([])
-    dprof = model.prof_read()[dom]
     final_loss = model.get_loss()
 
-    # end to end through the public host-buffer call: pinned host tokens
-    # copied every micro-step, the loss read back every step
+    # roofline pass
+    model.prof_reset()
+    model.prof_enable(None)
+    step()
+    torch.cuda.synchronize()
+    prof = model.prof_read()
+    dom = max(prof, key=lambda k: prof[k][0])
+    model.prof_reset()
+    model.prof_enable([dom])
+    for _ in range(rl_steps):
+        step()
+    torch.cuda.synchronize()
+    model.prof_enable([])
+    dprof = model.prof_read()[dom]
+
+    # end to end
     ptok = [torch.from_numpy(a).pin_memory() for a, _ in host]
     ptgt = [torch.from_numpy(b).pin_memory() for _, b in host]
     htok = [p.numpy() for p in ptok]
     htgt = [p.numpy() for p in ptgt]
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    for _ in range(steps):
         model.zero_grad()
         for i in range(accum):
             model.forward(htok[i], htgt[i])
             model.backward()
         model.adamw_step(**hp)
-        losses.append(model.get_loss())
+        model.get_loss()
     torch.cuda.synchronize()
     barrier()
     e2e_s = time.perf_counter() - t0
+    model.close()
+    del model
+    torch.cuda.empty_cache()
     return dict(ms=ms, launches=launches, dom=dom, dprof=dprof, clocks=clk, e2e_s=e2e_s,
-                e2e_steps=e2e_steps, final_loss=final_loss, accum=accum,
-                h2d=accum * 2 * B * T * 4, d2h=24, prof=prof)
+                final_loss=final_loss, h2d=accum * 2 * B * T * 4, d2h=20, prof=prof)
 
 
 def max_over_ranks(x, world):
@@ -302,7 +364,11 @@ def main():
     ap.add_argument("--workload", default="124M", choices=sorted(WORKLOADS))
     ap.add_argument("--accum", type=int, default=0, help="override micro-batches per step")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--rl-steps", type=int, default=3,
+                    help="steps of the roofline pass (events around the dominant class)")
+    ap.add_argument("--secondary", default="1558M",
+                    help="a second workload timed after the first (1-GPU runs; '' for none)")
+    ap.add_argument("--secondary-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -312,7 +378,6 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     w = WORKLOADS[args.workload]
     peaks, peak_kind = load_peaks()
-    fpt = flops_per_token(w)
 
     if args.impl == "reference":
         # the CPU oracle as the reference arm; rank 0 alone
@@ -336,29 +401,42 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, cores, times = cpu_oracle_step_rate(w, CPU_BASELINE_SAMPLE, steps=1, warmup=0)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{args.workload} architecture, B={CPU_BASELINE_SAMPLE['B']} "
-                         f"T={CPU_BASELINE_SAMPLE['T']}, one full step (forward, backward, AdamW), "
-                         f"fp64 oracle, {statistics.mean(times):.1f} s",
-               "cpu": cpu_model()}
+        cpu = cpu_baselines()
 
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
-    r = run_gpu(args, w, rank, world)
+    line = workload_line(args.workload, w, args.steps, args.warmup, args.accum, args.rl_steps,
+                         rank, world, peaks, peak_kind)
+    if world == 1 and args.secondary and args.workload != args.secondary:
+        w2 = WORKLOADS[args.secondary]
+        sec = workload_line(args.secondary, w2, args.secondary_steps, 3, 0, 1, rank, world,
+                            peaks, peak_kind)
+        line["secondary"] = {k: sec[k] for k in (
+            "value", "unit", "ms_per_step", "steps", "warmup", "config", "bf16_mfu", "roofline",
+            "e2e", "gpu_launches", "clocks", "final_loss")}
+    if rank != 0:
+        return
+    line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def workload_line(name, w, steps, warmup, accum_override, rl_steps, rank, world, peaks,
+                  peak_kind):
+    accum = accum_override or w["accum"]
+    fpt = flops_per_token(w)
+    r = run_gpu(w, rank, world, steps, warmup, accum, rl_steps)
     ms = max_over_ranks(r["ms"], world)
     e2e_s = max_over_ranks(r["e2e_s"], world)
-    accum = r["accum"]
     tok_step = w["B"] * w["T"] * accum
-    value = world * tok_step * args.steps / (ms / 1e3)
-    e2e_value = world * tok_step * r["e2e_steps"] / e2e_s
+    value = world * tok_step * steps / (ms / 1e3)
+    e2e_value = world * tok_step * steps / e2e_s
     peak_tf = peaks.get("bf16_tflops", 1800.0)
     peak_sus = peaks.get("bf16_tflops_sustained", 1400.0)
     mfu = value / world * fpt / (peak_tf * 1e12)
 
     dom, (dms, dn, dfl, dby) = r["dom"], r["dprof"]
-    traffic = load_traffic(args.workload)
+    traffic = load_traffic(name)
     traffic = traffic.get(dom) if traffic else None
     if dfl > 0:
         achieved = dfl / dn / (dms / dn / 1e3) / 1e12
@@ -366,7 +444,8 @@ def main():
                 "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
                 "traffic": traffic, "algorithmic_bytes": dby / dn,
                 "peak_kind": f"bf16 sustained ({peak_kind})",
-                "launches": dn, "avg_launch_ms": dms / dn}
+                "launches": dn, "avg_launch_ms": dms / dn,
+                "frac_of_burst": achieved / peak_tf}
     else:
         achieved = dby / dn / (dms / dn / 1e3) / 1e9
         hbm = peaks.get("hbm_gbs", 6400.0)
@@ -374,17 +453,14 @@ def main():
                 "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                 "peak_kind": f"hbm copy ({peak_kind})", "launches": dn,
                 "avg_launch_ms": dms / dn}
-
-    if rank != 0:
-        return
-    line = {
+    descr = DESCR[name] if accum == w["accum"] else \
+        DESCR[name] + f" (accumulation overridden to {accum})"
+    return {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": DESCR[args.workload] if args.accum == 0 or args.accum == w["accum"]
-                   else DESCR[args.workload] + f" (accumulation overridden to {accum})",
-                   "tokens_per_step": tok_step * world, "seq_len": w["T"],
+        "config": {"workload": descr, "tokens_per_step": tok_step * world, "seq_len": w["T"],
                    "micro_batch": w["B"], "grad_accum": accum,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "working set (activations) far larger than L2; no flush"},
@@ -392,15 +468,13 @@ def main():
                      "peak_tflops": peak_tf, "peak_kind": f"bf16 burst ({peak_kind})",
                      "mfu_vs_sustained": value / world * fpt / (peak_sus * 1e12)},
         "roofline": roof,
-        "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
-                "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
+                "d2h_bytes_per_step": r["d2h"], "steps": steps},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "final_loss": r["final_loss"],
         "kernel_ms_calibration_step": {k: round(v[0], 3) for k, v in r["prof"].items() if v[1]},
     }
-    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

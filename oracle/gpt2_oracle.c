@@ -515,6 +515,8 @@ static real* G(og_model* g, int which, int l) {
 static void og_init_params(og_model* g, uint64_t seed) {
     double std = 0.02, std_res = 0.02 / sqrt(2.0 * g->L);
     for (int k = 0; k < P_COUNT; k++) {
+        /* each element depends only on (seed, its index): iterations are independent */
+#pragma omp parallel for schedule(static)
         for (size_t j = 0; j < g->sizes[k]; j++) {
             size_t i = g->offs[k] + j;
             real val;

@@ -73,3 +73,24 @@ def test_reference_arm_prints_the_contract_line():
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
     assert line["dtype"] == "f64" and line["data"] == "synthetic"
+
+
+def test_cpu_baselines_skip_a_sample_the_host_cannot_hold(monkeypatch):
+    """the 1558M oracle sample holds ~50 GB of fp64 state; with less host
+    memory it is reported as skipped, with the reason, not run"""
+    b = _bench()
+    w = b.WORKLOADS
+    need = b.oracle_bytes(w["1558M"], b.CPU_SAMPLE_1558M)
+    assert 4 * 8 * 1.55e9 < need < 4 * 8 * 1.6e9 + 8e9
+    calls = []
+
+    def fake_rate(wl, sample, steps=1, warmup=0, threads=None):
+        calls.append((wl["C"], sample["T"], threads))
+        return 100.0, threads or 8, [1.0]
+    monkeypatch.setattr(b, "cpu_oracle_step_rate", fake_rate)
+    monkeypatch.setattr(b, "mem_available", lambda: 16 << 30)
+    cb = b.cpu_baselines()
+    assert calls == [(768, 256, None), (768, 32, 1)]
+    assert cb["kind"] == "oracle" and cb["value"] == 100.0 and cb["cores"] == 8
+    assert [("skipped" in r) for r in cb["runs"]] == [False, False, True]
+    assert cb["runs"][1]["cores"] == 1
