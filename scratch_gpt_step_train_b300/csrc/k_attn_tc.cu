@@ -9,22 +9,25 @@
 // "Code anatomy" item 2 and "Performance comparison"); here it is one fused
 // kernel per direction, written for tcgen05.
 //
-// Forward (one CTA per 128-query tile of one (batch, head); 288 threads):
+// Forward (one CTA per 128-query tile of one (batch, head); 320 threads):
 //   warp 0, lane 0  TMA: the Q tile once, then K_j, V_j tiles (128 keys x 64)
 //                   through a ring of five shared-memory slots
-//   warp 0, lane 1  tcgen05.mma issue, TMEM (256 columns):
+//   warp 1, lane 0  tcgen05.mma issue, TMEM (256 columns):
 //                     S_j = Q K_j^T   M=128 N=128 K=64   -> fp32 cols [0,128)
 //                     O  += P_j V_j   M=128 N=64  K=128  -> fp32 cols [128,192)
 //                   with P_j (bf16, two per column) read from cols [192,256);
 //                   S_{j+1} is issued as soon as the softmax warps hold S_j
-//   warps 1-8       two warps per TMEM lane quarter, each one half of the
+//   warps 2-9       two warps per TMEM lane quarter, each one half of the
 //                   keys of 32 rows: tcgen05.ld of S_j, row max (exchanged
 //                   between the halves), P_j = exp2(S_j c - m) in base 2,
 //                   tcgen05.st of P_j; the running max m is raised (and O, the
 //                   row sum rescaled in TMEM) only when a row max exceeds it
 //                   by more than 2^8.
 // Keys are visited in tiles 0..q (q = the query tile); only the diagonal tile
-// needs the causal mask.  Two CTAs share an SM (~100 KB smem, 256 TMEM
+// needs the causal mask.  The TMA producer and the MMA issuer sit in warps of
+// their own: a thread issuing tcgen05.mma back to back is held for about a
+// hundred cycles per instruction, and sharing a warp with the producer's
+// waits costs a few percent more.  Two CTAs share an SM (~100 KB smem, 256 TMEM
 // columns and 96 registers a thread each), so one CTA's softmax overlaps the
 // other's products.
 // Outputs: O [B,T,C] (bf16) and the row log-sum-exp [B,H,T] (fp32, natural
@@ -86,13 +89,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ void named_sync_softmax() {
     asm volatile("bar.sync 1, 256;" ::: "memory");
 }
-// the two softmax warps that share TMEM lane quarter q (warps q + 1 and
-// q + 5, counted from 1) synchronise: named barrier 2 + q, 64 threads
+// the two softmax warps that share TMEM lane quarter q (warps w and w + 4 with
+// w % 4 == q, among warps 2-9) synchronise: named barrier 2 + q, 64 threads
 __device__ __forceinline__ void pair_sync(int q) {
     asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory");
 }
 
-constexpr int FWD_THREADS = 288;  // warp 0: TMA (lane 0) + MMA (lane 1); 8 softmax warps
+constexpr int FWD_THREADS = 320;  // warp 0: TMA (lane 0); warp 1: MMA (lane 0); 8 softmax warps
 constexpr float RESCALE_SLACK = 8.0f;  // log2 units: P stays <= 2^8 between rescales
 
 __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_constant__ CUtensorMap map,
@@ -175,7 +178,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
                 while (!mbar_try(b_q, 0) && clock64() - t0 < WAIT_LIMIT) {
                 }
             }
-        } else if (lane == 1) {
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
             // ----------------------------------------------------------- MMA
             constexpr uint32_t ID_S = make_idesc(128, 128, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
         // O accumulates in TMEM; the running max m used for P is raised (and O,
         // l rescaled) only when the row max exceeds it by more than 2^8, so P
         // stays <= 256 and most tiles need no rescale.
-        const int q = warp & 3, hf = (warp - 1) >> 2;
+        const int q = warp & 3, hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;
         const int qi = qt * TILE + r;
         const uint32_t loff = (uint32_t)(q * 32) << 16;
@@ -367,7 +372,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) k_attn_fwd_tc(const __grid_con
 // k_attn_dq_tc) is visited in steps of 64 on the other side, so every CTA
 // holds at most 256 TMEM columns and ~100 KB of shared memory: two CTAs share
 // an SM, and one CTA's softmax phase overlaps the other's products.
-constexpr int BWD_THREADS = 288;  // warp 0: TMA (lane 0) + MMA (lane 1); 8 softmax warps
+constexpr int BWD_THREADS = 320;  // warp 0: TMA (lane 0); warp 1: MMA (lane 0); 8 softmax warps
 constexpr int SUB = 64;           // rows of the 64-wide side
 constexpr int SUB_BYTES = SUB * 128;
 
@@ -480,7 +485,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 while (!mbar_try(b_kv, 0) && clock64() - t0 < WAIT_LIMIT) {
                 }
             }
-        } else if (lane == 1) {
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
             constexpr uint32_t ID_S = make_idesc(128, SUB, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
             const uint64_t dK = sdesc(sK, 0, 1024), dV = sdesc(sV, 0, 1024);
@@ -531,10 +538,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
     } else {
         // warp pair (w, w+4) shares TMEM lane quarter w & 3; half hf takes query
         // columns [32 hf, 32 hf + 32) of each step and output columns [32 hf, +32)
-        const int q = warp & 3, hf = (warp - 1) >> 2;
+        const int q = warp & 3, hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;   // key row within the tile
         const int kj = kt * TILE + r;  // key index in the sequence
-        const int tid = threadIdx.x - 32;
+        const int tid = threadIdx.x - 64;
         const uint32_t loff = (uint32_t)(q * 32) << 16;
         const int c0 = hf * 32;
         bool ok = true;
@@ -731,7 +738,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
                 while (!mbar_try(b_q, 0) && clock64() - t0 < WAIT_LIMIT) {
                 }
             }
-        } else if (lane == 1) {
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
             constexpr uint32_t ID_S = make_idesc(128, SUB, false, false);
             constexpr uint32_t ID_O = make_idesc(128, 64, false, true);
             const uint64_t dQ = sdesc(sQ, 0, 1024), dDO = sdesc(sDO, 0, 1024);
@@ -777,7 +786,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2)
             if (ok) umma_commit(b_acc);
         }
     } else {
-        const int q = warp & 3, hf = (warp - 1) >> 2;
+        const int q = warp & 3, hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;
         const int qi = qt * TILE + r;
         const uint32_t loff = (uint32_t)(q * 32) << 16;

@@ -157,7 +157,8 @@ def test_matmul_accumulate_fp32(a_km, b_km, Kd):
 
 
 # Full-size products of the GPT-2 124M step at micro-batch 16 x 1024, as the
-# bench runs them; the oracle computes a sample of 48 output rows.
+# bench runs them; the oracle computes a sample of 48 output rows (every
+# column of each).
 FULL = [
     ("qkv_fwd", 16384, 2304, 768, True, True, "store"),
     ("proj_fwd", 16384, 768, 768, True, True, "resid"),
@@ -179,7 +180,30 @@ FULL = [
 ]
 
 
-@pytest.mark.parametrize("name,M,N,Kd,a_km,b_km,epi", FULL, ids=[f[0] for f in FULL])
+# The same products at the GPT-2 1558M width (C=1600, 3C=4800, 4C=6400; none a
+# multiple of the 256-wide tiles) at micro-batch 16 x 1024.
+FULL_1558M = [
+    ("qkv_fwd", 16384, 4800, 1600, True, True, "store"),
+    ("proj_fwd", 16384, 1600, 1600, True, True, "resid"),
+    ("fc_fwd_gelu_d", 16384, 6400, 1600, True, True, "gelu_d"),
+    ("fcproj_fwd", 16384, 1600, 6400, True, True, "resid"),
+    ("classifier_fwd", 16384, 50304, 1600, True, True, "store"),
+    ("qkv_dx", 16384, 1600, 4800, True, False, "store"),
+    ("proj_dx", 16384, 1600, 1600, True, False, "store"),
+    ("fc_dx", 16384, 1600, 6400, True, False, "store"),
+    ("fcproj_dx_mul_aux", 16384, 6400, 1600, True, False, "mul_aux"),
+    ("classifier_dx", 16384, 1600, 50304, True, False, "store"),
+    ("qkv_dw", 4800, 1600, 16384, False, False, "accum_f32"),
+    ("proj_dw", 1600, 1600, 16384, False, False, "accum_f32"),
+    ("fc_dw", 6400, 1600, 16384, False, False, "accum_f32"),
+    ("fcproj_dw", 1600, 6400, 16384, False, False, "accum_f32"),
+    ("classifier_dw", 50304, 1600, 16384, False, False, "accum_f32"),
+]
+ALL_FULL = [("124M-" + f[0],) + f[1:] for f in FULL] + [("1558M-" + f[0],) + f[1:]
+                                                       for f in FULL_1558M]
+
+
+@pytest.mark.parametrize("name,M,N,Kd,a_km,b_km,epi", ALL_FULL, ids=[f[0] for f in ALL_FULL])
 def test_matmul_full_size_sampled(name, M, N, Kd, a_km, b_km, epi):
     g = torch.Generator(device="cuda").manual_seed(7)
     Ash = (M, Kd) if a_km else (Kd, M)

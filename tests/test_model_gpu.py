@@ -139,7 +139,7 @@ def test_fp32_toy_50_adamw_steps_stepwise():
         gm.backward()
         assert abs(lg - lo) <= 1e-4 * abs(lo)
         compare_tensors(gm.get_grads(), om.grads(), om, 1e-4, f"step {step} grad",
-                        f32_vec=o32.grads())
+                        f32_vec=o32.grads(), widen=("lnfb",))
         om.adamw_step(**hp)
         gm.adamw_step(**hp)
         assert_close(gm.get_params()[keep], om.params()[keep], 1e-4, f"step {step} params")
@@ -188,6 +188,70 @@ def test_toy_transition_table_gpu():
         if nxt and abs(np.mean(nxt) - 0.5) >= 0.3:
             f = float(np.mean(nxt))
             assert abs(a50[s] - f) < abs(a0[s] - f) - 0.1
+
+
+# the GPT-2 1558M layer width (C=1600, 25 heads of 64, 4C=6400) and the full
+# vocabulary, two layers, one sequence of 128 tokens
+WIDE = dict(L=2, H=25, C=1600, V=50257, T=128, B=1)
+WIDE_HP = dict(lr=6e-4, b1=0.9, b2=0.95, eps=1e-8, wd=0.1, clip=1.0)
+
+
+def test_fp32_1558M_width_two_steps():
+    """fp32 mode against the fp64 oracle from the same init and Zipf tokens,
+    two AdamW steps: logits, loss and the norm each update saw at rel 1e-4;
+    every gradient tensor at rel 1e-4 at the first step.  From the second
+    step the weights of any two fp32 evaluations differ (AdamW's first step
+    moves every weight by lr in the direction of its gradient's sign, however
+    small the gradient, so a gradient that is rounding noise moves its weight
+    by lr either way), and each gradient tensor is held to
+    max(1e-4, 4 x the error of the fp32 build of the oracle run alongside)."""
+    om = Model(**WIDE, seed=1)
+    o32 = Model(**WIDE, seed=1, real="float")
+    gm = GPT2(**WIDE, seed=1, mode=FP32)
+    gm.set_params(om.params())
+    o32.set_params(om.params())
+    stream = inputs.ZipfStream(2, WIDE["B"], WIDE["T"], WIDE["V"])
+    for step in range(2):
+        tok, tgt = stream.next()
+        om.forward(tok, None)
+        gm.forward(tok, None)
+        assert_close(gm.get_logits(), om.logits(), 1e-4, f"step {step} logits")
+        for m in (om, o32):
+            m.zero_grad()
+        lo = om.forward(tok, tgt)
+        om.backward()
+        o32.forward(tok, tgt)
+        o32.backward()
+        gm.zero_grad()
+        lg = gm.forward(tok, tgt, sync_loss=True)
+        assert abs(lg - lo) <= 1e-4 * abs(lo), (step, lg, lo)
+        gm.backward()
+        widen = () if step == 0 else tuple(om.tensor_slices())
+        compare_tensors(gm.get_grads(), om.grads(), om, 1e-4, f"step {step} grad",
+                        f32_vec=o32.grads(), widen=widen)
+        rc, no = om.adamw_step(**WIDE_HP)
+        o32.adamw_step(**WIDE_HP)
+        ng = gm.adamw_step(**WIDE_HP)
+        assert rc == 0 and abs(ng - no) <= 1e-4 * no, (step, ng, no)
+
+
+def test_bf16_1558M_width_two_steps():
+    """bf16-mixed mode at the same shape: |loss difference| <= 2e-2 per step"""
+    om = Model(**WIDE, seed=1)
+    gm = GPT2(**WIDE, seed=1, mode=BF16)
+    gm.set_params(om.params())
+    stream = inputs.ZipfStream(2, WIDE["B"], WIDE["T"], WIDE["V"])
+    for step in range(2):
+        tok, tgt = stream.next()
+        om.zero_grad()
+        lo = om.forward(tok, tgt)
+        om.backward()
+        om.adamw_step(**WIDE_HP)
+        gm.zero_grad()
+        lg = gm.forward(tok, tgt, sync_loss=True)
+        gm.backward()
+        gm.adamw_step(**WIDE_HP)
+        assert abs(lg - lo) <= 2e-2, (step, lg, lo)
 
 
 def test_fp32_accum_clip_decay_stepwise():
