@@ -185,28 +185,68 @@ int gpt2_last_step_info(gpt2_t* g, int* skipped, float* z_loss, float* z_grad);
 
 /* ---- data parallelism ("Karpathy reproduces GPT-2 (1.6B) in llm.c",
  * "Training": one process per GPU, gradients averaged over the ranks, the
- * optimizer state sharded ZeRO-1 style).  One step on R ranks: every rank
- * runs its micro-batches (forward + backward), sums the gradient vectors of
- * all ranks into each (an all-reduce over gpt2_grads_buffer), sets the
- * divisor to R x its micro-batch count (gpt2_set_grad_count), applies
- * gpt2_adamw_step_shard to its own slice [lo, hi) of the canonical vector --
- * the global norm and clip come from the whole summed gradient, so every rank
- * takes the same decision -- and the ranks then exchange their updated slices
- * of the parameters (the fp32 master and the bf16 copy of gpt2_params_buffer).
- * The exchange itself is the caller's (NCCL through torch.distributed in the
- * binding's DataParallel).  The moments are held for the whole vector but
- * each rank only touches its slice.  Device pointers stay valid for the
- * handle's life. */
+ * optimizer state sharded ZeRO-1 style, -z 1).  One step on R ranks: every
+ * rank runs its micro-batches (forward + backward), sums the gradient vectors
+ * of all ranks into each (an all-reduce over gpt2_grads_buffer), sets the
+ * divisor to the micro-batch count summed over the ranks (gpt2_set_grad_count
+ * from the host, or gpt2_set_grad_count_device from a device word that a
+ * collective summed), applies gpt2_adamw_step_shard to its own slice [lo, hi)
+ * of the canonical vector -- the global norm and clip come from the whole
+ * summed gradient, so every rank takes the same decision -- and the ranks then
+ * gather the updated slices of the parameters the forward reads (the bf16
+ * copy in GPT2_BF16 mode, the fp32 parameters in GPT2_FP32 mode: the d_bf16 or
+ * d_master pointer of gpt2_params_buffer).  The collectives are the caller's
+ * (NCCL through torch.distributed in the binding's DataParallel).  Device
+ * pointers stay valid for the handle's life. */
 int gpt2_grads_buffer(gpt2_t* g, float** d_grads, size_t* n);
-/* master: NULL without fp32 master weights; bf16: NULL in GPT2_FP32 mode */
+/* d_master: the fp32 parameters -- NULL without master weights and on a
+ * sharded bf16 handle (which holds only its slice of them); d_bf16: NULL in
+ * GPT2_FP32 mode.  *n = the number of parameters N. */
 int gpt2_params_buffer(gpt2_t* g, float** d_master, void** d_bf16, size_t* n);
 int gpt2_get_grad_count(gpt2_t* g, int* count);
 int gpt2_set_grad_count(gpt2_t* g, int count);  /* count >= 1 */
-/* AdamW on [lo, hi) of the canonical vector (lo, hi multiples of 4, hi may be
- * N); the step count advances.  GPT2_ERR_STATE with the spike detector on
- * (its decision needs every rank's loss). */
+/* The next update (gpt2_adamw_step or gpt2_adamw_step_shard) divides by the
+ * int32 at d_count (device memory of the handle's device, 4-byte aligned),
+ * read by the update's kernels in stream order -- so a count summed over the
+ * ranks by a collective never has to come back to the host.  The setting
+ * serves that one update, which clears it whatever its outcome; the host
+ * count (gpt2_get_grad_count) is left as it was.  A count of 0 on the device
+ * makes the norm non-finite: the update is skipped with GPT2_ERR_NONFINITE. */
+int gpt2_set_grad_count_device(gpt2_t* g, const int* d_count);
+/* AdamW on [lo, hi) of the canonical vector (lo a multiple of 4, hi a
+ * multiple of 4 or N); the step count advances.  On a sharded handle [lo, hi)
+ * must be its own slice.  GPT2_ERR_STATE with the spike detector on (its
+ * decision needs every rank's loss).  After a failed update (a non-finite
+ * norm) the gradient buffer still holds what the caller put there (after an
+ * all-reduce: the sum over the ranks): call gpt2_zero_grad before the next
+ * micro-batches. */
 int gpt2_adamw_step_shard(gpt2_t* g, size_t lo, size_t hi, float lr, float b1, float b2,
                           float eps, float wd, float clip, float* h_grad_norm);
+/* ZeRO-1 handles.  gpt2_create_shard is gpt2_create for a rank that owns the
+ * canonical slice [lo, hi) (lo a multiple of 4, hi a multiple of 4 or N): the
+ * handle holds the AdamW moments m, v of the slice alone and, in GPT2_BF16
+ * mode with master weights, the fp32 master of the slice alone (the forward
+ * reads the full bf16 copy; in GPT2_FP32 mode the fp32 parameters are what the
+ * forward reads, so they stay whole).  Per rank that saves 8 (N - (hi - lo))
+ * bytes of moments, plus 4 (N - (hi - lo)) of master in GPT2_BF16 mode, against
+ * gpt2_workspace_bytes (the pages' 1558M run keeps 1/8 of m, v and the master
+ * on each of 8 GPUs).  On such a handle: gpt2_adamw_step returns
+ * GPT2_ERR_STATE (use gpt2_adamw_step_shard on [lo, hi)); gpt2_get_params
+ * returns the parameters the forward reads (in GPT2_BF16 mode the bf16 copy,
+ * widened); gpt2_set_params sets the bf16 copy (rounded to nearest even) and
+ * the slice's master; gpt2_get/set_opt_state move hi - lo moments each;
+ * checkpoints return GPT2_ERR_STATE (a rank holds only its slice).
+ * gpt2_workspace_bytes_shard returns 0 for a shape or slice it rejects. */
+size_t gpt2_workspace_bytes_shard(int L, int H, int C, int V, int T, int B, int mode, size_t lo,
+                                  size_t hi);
+int gpt2_create_shard(gpt2_t** out, int L, int H, int C, int V, int T, int B, uint64_t seed,
+                      int mode, size_t lo, size_t hi, void* workspace, size_t ws_bytes,
+                      void* stream);
+/* [lo, hi) of a sharded handle; [0, N) otherwise */
+int gpt2_shard_bounds(gpt2_t* g, size_t* lo, size_t* hi);
+/* the fp32 master of the handle's slice (hi - lo values; the whole vector on
+ * an unsharded handle); GPT2_ERR_STATE without master weights */
+int gpt2_get_shard_master(gpt2_t* g, float* h);
 
 /* ---- checkpoints: a file with the fp32 parameters, the AdamW moments and
  * step count, and the spike detector's settings and window (this library's

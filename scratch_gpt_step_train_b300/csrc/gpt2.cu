@@ -67,6 +67,15 @@ struct gpt2 {
 
     float *master, *grads, *m, *v;
     void* pc;  // compute copy of the parameters (== master in fp32 mode)
+    // ZeRO-1 shard: the handle holds the AdamW moments (and, in bf16 mode,
+    // the fp32 master) of the canonical slice [sh_lo, sh_hi) only
+    bool sharded = false;
+    size_t sh_lo = 0, sh_hi = 0;
+    // the micro-batch count of the next update, read on the device (NULL: n_accum)
+    const int* d_count = nullptr;
+    // elements of the moment buffers, and of the master buffer
+    size_t n_state() const { return sharded ? sh_hi - sh_lo : nparams; }
+    bool master_sliced() const { return sharded && act == ACT_BF16 && !no_master; }
     // activations
     void *encoded, *ln1, *qkv, *atty, *x1, *ln2, *fch, *fchg, *x2, *lnf, *logits;
     float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lnf_mean, *lnf_rstd, *lse, *losses;
@@ -187,10 +196,11 @@ static void plan(gpt2* g, char* base, size_t* total) {
     Planner p{base, 0};
     size_t N = g->nparams, BT = g->BT, C = g->C, L = g->L;
     size_t as = act_size(g->act);
-    g->master = g->no_master ? nullptr : (float*)p.take(N * 4);
+    const size_t S = g->n_state();
+    g->master = g->no_master ? nullptr : (float*)p.take((g->master_sliced() ? S : N) * 4);
     g->grads = (float*)p.take(N * 4);
-    g->m = (float*)p.take(N * 4);
-    g->v = (float*)p.take(N * 4);
+    g->m = (float*)p.take(S * 4);
+    g->v = (float*)p.take(S * 4);
     g->pc = g->act == ACT_BF16 ? p.take(N * 2) : (void*)g->master;
     g->encoded = p.take(BT * C * as);
     // with recompute, one layer's buffer serves every layer (refilled when needed)
@@ -244,7 +254,12 @@ static bool shape_ok(int L, int H, int C, int V, int T, int B, int mode) {
     return true;
 }
 
-extern "C" size_t gpt2_workspace_bytes(int L, int H, int C, int V, int T, int B, int mode) {
+static bool shard_ok(size_t n, size_t lo, size_t hi) {
+    return lo <= hi && hi <= n && lo % 4 == 0 && (hi % 4 == 0 || hi == n);
+}
+
+static size_t workspace_bytes(int L, int H, int C, int V, int T, int B, int mode, bool sharded,
+                              size_t lo, size_t hi) {
     if (!shape_ok(L, H, C, V, T, B, mode)) return 0;
     gpt2 tmp;
     tmp.L = L; tmp.H = H; tmp.C = C; tmp.V = V; tmp.T = T; tmp.B = B; tmp.mode = mode;
@@ -255,16 +270,29 @@ extern "C" size_t gpt2_workspace_bytes(int L, int H, int C, int V, int T, int B,
     tmp.BT = (size_t)B * T;
     make_layout(&tmp.lay, L, C, V, T);
     tmp.nparams = tmp.lay.off[P_NUM];
+    if (sharded && !shard_ok(tmp.nparams, lo, hi)) return 0;
+    tmp.sharded = sharded;
+    tmp.sh_lo = lo;
+    tmp.sh_hi = hi;
     size_t total;
     plan(&tmp, nullptr, &total);
     return total;
 }
 
+extern "C" size_t gpt2_workspace_bytes(int L, int H, int C, int V, int T, int B, int mode) {
+    return workspace_bytes(L, H, C, V, T, B, mode, false, 0, 0);
+}
+extern "C" size_t gpt2_workspace_bytes_shard(int L, int H, int C, int V, int T, int B, int mode,
+                                             size_t lo, size_t hi) {
+    return workspace_bytes(L, H, C, V, T, B, mode, true, lo, hi);
+}
+
 // ---------------------------------------------------------------------------
 // create / destroy
 // ---------------------------------------------------------------------------
-extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int B, uint64_t seed,
-                           int mode, void* workspace, size_t ws_bytes, void* stream) {
+static int create(gpt2_t** out, int L, int H, int C, int V, int T, int B, uint64_t seed, int mode,
+                  bool sharded, size_t lo, size_t hi, void* workspace, size_t ws_bytes,
+                  void* stream) {
     if (!out) return GPT2_ERR_ARG;
     *out = nullptr;
     if (!shape_ok(L, H, C, V, T, B, mode)) return GPT2_ERR_ARG;
@@ -278,6 +306,13 @@ extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int 
     g->BT = (size_t)B * T;
     make_layout(&g->lay, L, C, V, T);
     g->nparams = g->lay.off[P_NUM];
+    if (sharded && !shard_ok(g->nparams, lo, hi)) {
+        delete g;
+        return GPT2_ERR_ARG;
+    }
+    g->sharded = sharded;
+    g->sh_lo = lo;
+    g->sh_hi = hi;
     g->stream = (cudaStream_t)stream;
     g->prof_on = false;
     g->prof_cur = false;
@@ -321,13 +356,18 @@ extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int 
     cudaError_t e;
     do {
         if ((e = cudaMemsetAsync(g->grads, 0, g->nparams * 4, g->stream))) break;
-        if ((e = cudaMemsetAsync(g->m, 0, g->nparams * 4, g->stream))) break;
-        if ((e = cudaMemsetAsync(g->v, 0, g->nparams * 4, g->stream))) break;
+        if ((e = cudaMemsetAsync(g->m, 0, g->n_state() * 4, g->stream))) break;
+        if ((e = cudaMemsetAsync(g->v, 0, g->n_state() * 4, g->stream))) break;
         if ((e = cudaMemsetAsync(g->err, 0, 16, g->stream))) break;
-        if (g->no_master) {
-            // the fp32 init passes through the gradient buffer, rounded to bf16
+        if (g->no_master || g->master_sliced()) {
+            // the fp32 init passes through the gradient buffer: rounded to
+            // bf16 for the compute copy, and its slice kept as the master
             if ((e = init_params(g->grads, g->lay, seed, g->stream))) break;
             if ((e = cast_to_bf16(g->pc, g->grads, g->nparams, g->stream))) break;
+            if (g->master_sliced() && g->n_state() &&
+                (e = cudaMemcpyAsync(g->master, g->grads + lo, g->n_state() * 4,
+                                     cudaMemcpyDeviceToDevice, g->stream)))
+                break;
             if ((e = cudaMemsetAsync(g->grads, 0, g->nparams * 4, g->stream))) break;
         } else {
             if ((e = init_params(g->master, g->lay, seed, g->stream))) break;
@@ -343,6 +383,16 @@ extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int 
     }
     *out = g;
     return GPT2_OK;
+}
+
+extern "C" int gpt2_create(gpt2_t** out, int L, int H, int C, int V, int T, int B, uint64_t seed,
+                           int mode, void* workspace, size_t ws_bytes, void* stream) {
+    return create(out, L, H, C, V, T, B, seed, mode, false, 0, 0, workspace, ws_bytes, stream);
+}
+extern "C" int gpt2_create_shard(gpt2_t** out, int L, int H, int C, int V, int T, int B,
+                                 uint64_t seed, int mode, size_t lo, size_t hi, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+    return create(out, L, H, C, V, T, B, seed, mode, true, lo, hi, workspace, ws_bytes, stream);
 }
 
 extern "C" void gpt2_destroy(gpt2_t* g) {
@@ -729,7 +779,8 @@ static AdamArgs adam_args(const gpt2* g, int t, float lr, float b1, float b2, fl
     a.lr = lr; a.b1 = b1; a.b2 = b2; a.eps = eps; a.wd = wd;
     a.bc1 = (float)(1.0 - pow((double)b1, t));
     a.bc2 = (float)(1.0 - pow((double)b2, t));
-    a.inv_accum = 1.0f / (float)g->n_accum;
+    a.inv_accum = g->n_accum > 0 ? 1.0f / (float)g->n_accum : 0.f;
+    a.d_count = nullptr;
     a.clip = clip;
     const size_t* o = g->lay.off;
     a.dec_lo[0] = o[P_WTE];     a.dec_hi[0] = o[P_LN1W];
@@ -755,9 +806,15 @@ extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float ep
                                float clip, float* h_grad_norm) {
     if (!g) return GPT2_ERR_ARG;
     cudaSetDevice(g->device);
-    if (g->n_accum < 1) return fail(g, GPT2_ERR_STATE, "adamw_step without accumulated grads");
+    // the device-side count (if any) serves this one update, whatever its outcome
+    const int* dc = g->d_count;
+    g->d_count = nullptr;
+    if (g->sharded)
+        return fail(g, GPT2_ERR_STATE, "a sharded handle updates its slice (gpt2_adamw_step_shard)");
+    if (!dc && g->n_accum < 1) return fail(g, GPT2_ERR_STATE, "adamw_step without accumulated grads");
     const int t = g->t + 1;
-    const AdamArgs a = adam_args(g, t, lr, b1, b2, eps, wd, clip, 0);
+    AdamArgs a = adam_args(g, t, lr, b1, b2, eps, wd, clip, 0);
+    a.d_count = dc;
     void* wb = g->act == ACT_BF16 ? g->pc : nullptr;
     const double ad_bytes = 34.0 * g->nparams + (g->act == ACT_BF16 ? 2.0 * g->nparams : 0.0);
     g->last_skipped = 0;
@@ -788,7 +845,7 @@ extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float ep
     CK(cudaMemcpyAsync(&lsum, g->loss + 1, 4, cudaMemcpyDeviceToHost, g->stream));
     RUN(check_dev_err(g));  // synchronises the stream
     if (h_grad_norm) *h_grad_norm = st[0];
-    const double step_loss = (double)lsum / g->n_accum, norm = st[0];
+    const double step_loss = (double)lsum / (g->n_accum > 0 ? g->n_accum : 1), norm = st[0];
     g->last_zl = spike_z(g, g->sk_loss_hist, step_loss);
     g->last_zg = spike_z(g, g->sk_grad_hist, norm);
     const bool spike = (g->sk_loss_z > 0.f && g->last_zl > g->sk_loss_z) ||
@@ -842,7 +899,8 @@ extern "C" int gpt2_grads_buffer(gpt2_t* g, float** d_grads, size_t* n) {
 }
 extern "C" int gpt2_params_buffer(gpt2_t* g, float** d_master, void** d_bf16, size_t* n) {
     if (!g) return GPT2_ERR_ARG;
-    if (d_master) *d_master = g->master;  // NULL without master weights
+    // NULL without master weights, or when the handle holds only its slice
+    if (d_master) *d_master = g->master_sliced() ? nullptr : g->master;
     if (d_bf16) *d_bf16 = g->act == ACT_BF16 ? g->pc : nullptr;
     if (n) *n = g->nparams;
     return GPT2_OK;
@@ -857,18 +915,48 @@ extern "C" int gpt2_set_grad_count(gpt2_t* g, int count) {
     g->n_accum = count;
     return GPT2_OK;
 }
+extern "C" int gpt2_set_grad_count_device(gpt2_t* g, const int* d_count) {
+    if (!g || !d_count || ((uintptr_t)d_count & 3)) return GPT2_ERR_ARG;
+    g->d_count = d_count;
+    return GPT2_OK;
+}
+extern "C" int gpt2_shard_bounds(gpt2_t* g, size_t* lo, size_t* hi) {
+    if (!g) return GPT2_ERR_ARG;
+    if (lo) *lo = g->sharded ? g->sh_lo : 0;
+    if (hi) *hi = g->sharded ? g->sh_hi : g->nparams;
+    return GPT2_OK;
+}
+extern "C" int gpt2_get_shard_master(gpt2_t* g, float* h) {
+    if (!g || !h) return GPT2_ERR_ARG;
+    if (!g->master) return fail(g, GPT2_ERR_STATE, "no fp32 master weights (GPT2_NO_MASTER)");
+    cudaSetDevice(g->device);
+    const float* src = g->master_sliced() ? g->master : g->master + (g->sharded ? g->sh_lo : 0);
+    CK(cudaMemcpyAsync(h, src, g->n_state() * 4, cudaMemcpyDeviceToHost, g->stream));
+    CK(cudaStreamSynchronize(g->stream));
+    return GPT2_OK;
+}
 
 extern "C" int gpt2_adamw_step_shard(gpt2_t* g, size_t lo, size_t hi, float lr, float b1, float b2,
                                      float eps, float wd, float clip, float* h_grad_norm) {
-    if (!g || lo > hi || hi > g->nparams || (lo % 4) || (hi % 4 && hi != g->nparams))
-        return GPT2_ERR_ARG;
+    if (!g || !shard_ok(g->nparams, lo, hi)) return GPT2_ERR_ARG;
+    if (g->sharded && (lo != g->sh_lo || hi != g->sh_hi)) return GPT2_ERR_ARG;
     cudaSetDevice(g->device);
-    if (g->n_accum < 1) return fail(g, GPT2_ERR_STATE, "adamw_step_shard without accumulated grads");
+    // the device-side count (if any) serves this one update, whatever its outcome
+    const int* dc = g->d_count;
+    g->d_count = nullptr;
+    if (!dc && g->n_accum < 1)
+        return fail(g, GPT2_ERR_STATE, "adamw_step_shard without accumulated grads");
     if (g->sk_window > 0)
         return fail(g, GPT2_ERR_STATE, "the spike detector needs the whole update (not a shard)");
     const int t = g->t + 1;
-    const AdamArgs a = adam_args(g, t, lr, b1, b2, eps, wd, clip, lo);
+    AdamArgs a = adam_args(g, t, lr, b1, b2, eps, wd, clip, lo);
+    a.d_count = dc;
     const size_t n = hi - lo;
+    // the slice's moments (and master): the whole buffers' [lo, hi), or all of
+    // a sharded handle's
+    float* ms = g->sharded ? g->m : g->m + lo;
+    float* vs = g->sharded ? g->v : g->v + lo;
+    float* ws = g->master_sliced() ? g->master : (g->master ? g->master + lo : nullptr);
     // the norm (and the clip scale) over every gradient, the update on [lo, hi)
     LAUNCH(K_ADAM, 2, 0, 4.0 * g->nparams,
            adamw_norm(g->grads, g->nparams, a, g->adam_state, g->scratch, g->stream));
@@ -877,12 +965,11 @@ extern "C" int gpt2_adamw_step_shard(gpt2_t* g, size_t lo, size_t hi, float lr, 
         void* wb = g->act == ACT_BF16 ? (void*)((char*)g->pc + lo * as) : nullptr;
         if (g->no_master)
             LAUNCH(K_ADAM, 1, 0, 26.0 * n,
-                   adamw_update_bf16_sr(wb, g->m + lo, g->v + lo, g->grads + lo, n, a,
-                                        g->adam_state, g->stream));
+                   adamw_update_bf16_sr(wb, ms, vs, g->grads + lo, n, a, g->adam_state,
+                                        g->stream));
         else
             LAUNCH(K_ADAM, 1, 0, 30.0 * n,
-                   adamw_update(g->master + lo, g->m + lo, g->v + lo, g->grads + lo, wb, n, a,
-                                g->adam_state, g->stream));
+                   adamw_update(ws, ms, vs, g->grads + lo, wb, n, a, g->adam_state, g->stream));
     }
     float st[3];
     CK(cudaMemcpyAsync(st, g->adam_state, 12, cudaMemcpyDeviceToHost, g->stream));
@@ -910,7 +997,7 @@ static uint16_t f32_to_bf16_rne(float f) {
     return (uint16_t)((b + 0x7fffu + ((b >> 16) & 1u)) >> 16);
 }
 static int params_to_host(gpt2* g, float* h) {
-    if (!g->no_master) {
+    if (!g->no_master && !g->master_sliced()) {
         CK(cudaMemcpyAsync(h, g->master, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
         CK(cudaStreamSynchronize(g->stream));
         return GPT2_OK;
@@ -925,7 +1012,10 @@ static int params_to_host(gpt2* g, float* h) {
     return GPT2_OK;
 }
 static int params_from_host(gpt2* g, const float* h) {
-    if (!g->no_master) {
+    if (g->master_sliced() && g->n_state())
+        CK(cudaMemcpyAsync(g->master, h + g->sh_lo, g->n_state() * 4, cudaMemcpyHostToDevice,
+                           g->stream));
+    if (!g->no_master && !g->master_sliced()) {
         CK(cudaMemcpyAsync(g->master, h, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
         if (g->act == ACT_BF16) CK(cast_to_bf16(g->pc, g->master, g->nparams, g->stream));
         CK(cudaStreamSynchronize(g->stream));
@@ -960,6 +1050,8 @@ static const char kCkptMagic[8] = {'G', 'P', 'T', '2', 'B', '3', 'C', 'K'};
 
 extern "C" int gpt2_save_checkpoint(gpt2_t* g, const char* path) {
     if (!g || !path) return GPT2_ERR_ARG;
+    if (g->sharded)
+        return fail(g, GPT2_ERR_STATE, "a sharded handle holds only its slice of the state");
     cudaSetDevice(g->device);
     CkptHeader hd;
     memset(&hd, 0, sizeof hd);
@@ -999,6 +1091,8 @@ extern "C" int gpt2_save_checkpoint(gpt2_t* g, const char* path) {
 
 extern "C" int gpt2_load_checkpoint(gpt2_t* g, const char* path) {
     if (!g || !path) return GPT2_ERR_ARG;
+    if (g->sharded)
+        return fail(g, GPT2_ERR_STATE, "a sharded handle holds only its slice of the state");
     cudaSetDevice(g->device);
     FILE* f = fopen(path, "rb");
     if (!f) return fail(g, GPT2_ERR_IO, "cannot open %s", path);
@@ -1086,8 +1180,8 @@ extern "C" int gpt2_set_grads(gpt2_t* g, const float* h) {
 extern "C" int gpt2_get_opt_state(gpt2_t* g, float* hm, float* hv, int* step) {
     if (!g) return GPT2_ERR_ARG;
     cudaSetDevice(g->device);
-    if (hm) CK(cudaMemcpyAsync(hm, g->m, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
-    if (hv) CK(cudaMemcpyAsync(hv, g->v, g->nparams * 4, cudaMemcpyDeviceToHost, g->stream));
+    if (hm) CK(cudaMemcpyAsync(hm, g->m, g->n_state() * 4, cudaMemcpyDeviceToHost, g->stream));
+    if (hv) CK(cudaMemcpyAsync(hv, g->v, g->n_state() * 4, cudaMemcpyDeviceToHost, g->stream));
     CK(cudaStreamSynchronize(g->stream));
     if (step) *step = g->t;
     return GPT2_OK;
@@ -1096,8 +1190,8 @@ extern "C" int gpt2_get_opt_state(gpt2_t* g, float* hm, float* hv, int* step) {
 extern "C" int gpt2_set_opt_state(gpt2_t* g, const float* hm, const float* hv, int step) {
     if (!g || step < 0) return GPT2_ERR_ARG;
     cudaSetDevice(g->device);
-    if (hm) CK(cudaMemcpyAsync(g->m, hm, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
-    if (hv) CK(cudaMemcpyAsync(g->v, hv, g->nparams * 4, cudaMemcpyHostToDevice, g->stream));
+    if (hm) CK(cudaMemcpyAsync(g->m, hm, g->n_state() * 4, cudaMemcpyHostToDevice, g->stream));
+    if (hv) CK(cudaMemcpyAsync(g->v, hv, g->n_state() * 4, cudaMemcpyHostToDevice, g->stream));
     CK(cudaStreamSynchronize(g->stream));
     g->t = step;
     return GPT2_OK;

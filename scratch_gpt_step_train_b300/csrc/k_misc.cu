@@ -1604,9 +1604,12 @@ __global__ void __launch_bounds__(256) k_sumsq(const float* g, size_t n, double*
     }
 }
 
-__global__ void k_adam_norm(const double* part, float* state, float inv_accum, float clip) {
+__global__ void k_adam_norm(const double* part, float* state, float inv_accum, float clip,
+                            const int* d_count) {
     gdc_wait();
     gdc_launch_dependents();
+    // the same correctly rounded quotient the host forms from its own count
+    if (d_count) inv_accum = __fdiv_rn(1.0f, (float)*d_count);
     __shared__ double sh[32];
     double a = 0.0;
     for (int i = threadIdx.x; i < ADAM_NB; i += blockDim.x) a += part[i];
@@ -1720,7 +1723,7 @@ cudaError_t adamw_norm(const float* g, size_t n, const AdamArgs& a, float* state
                        cudaStream_t s) {
     double* part = (double*)scratch;
     launch_pdl(k_sumsq, ADAM_NB, 256, 0, s, g, n, part);
-    launch_pdl(k_adam_norm, 1, 1024, 0, s, part, state, a.inv_accum, a.clip);
+    launch_pdl(k_adam_norm, 1, 1024, 0, s, part, state, a.inv_accum, a.clip, a.d_count);
     return cudaGetLastError();
 }
 cudaError_t adamw_update(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,

@@ -94,6 +94,7 @@ struct AdamArgs {
     float lr, b1, b2, eps, wd;
     float bc1, bc2;          // 1 - b1^t, 1 - b2^t
     float inv_accum, clip;
+    const int* d_count;           // if not NULL: the divisor is *d_count (on the device)
     size_t dec_lo[5], dec_hi[5];  // decayed index ranges [lo, hi)
     int t;                        // this update's step count (1-based)
     uint64_t sr_seed;             // stochastic-rounding stream (bf16-only parameters)

@@ -53,6 +53,12 @@ SIGNATURES = {
     "gpt2_get_grad_count": (_i, [_vp, _pi]),
     "gpt2_set_grad_count": (_i, [_vp, _i]),
     "gpt2_adamw_step_shard": (_i, [_vp, _sz, _sz] + [_f] * 6 + [_pf]),
+    "gpt2_set_grad_count_device": (_i, [_vp, _vp]),
+    "gpt2_workspace_bytes_shard": (_sz, [_i] * 7 + [_sz, _sz]),
+    "gpt2_create_shard": (_i, [ct.POINTER(_vp)] + [_i] * 6 + [ct.c_uint64, _i, _sz, _sz, _vp, _sz,
+                                                             _vp]),
+    "gpt2_shard_bounds": (_i, [_vp, ct.POINTER(_sz), ct.POINTER(_sz)]),
+    "gpt2_get_shard_master": (_i, [_vp, _pf]),
     "gpt2_set_spike_skip": (_i, [_vp, _f, _f, _i]),
     "gpt2_last_step_info": (_i, [_vp, _pi, _pf, _pf]),
     "gpt2_save_checkpoint": (_i, [_vp, ct.c_char_p]),
@@ -100,14 +106,20 @@ def padded_vocab(V):
     return ((V + 127) // 128) * 128
 
 
-def workspace_bytes(L, H, C, V, T, B, mode=FP32):
-    return lib().gpt2_workspace_bytes(L, H, C, V, T, B, mode)
+def workspace_bytes(L, H, C, V, T, B, mode=FP32, shard=None):
+    if shard is None:
+        return lib().gpt2_workspace_bytes(L, H, C, V, T, B, mode)
+    return lib().gpt2_workspace_bytes_shard(L, H, C, V, T, B, mode, int(shard[0]), int(shard[1]))
 
 
 class GPT2:
-    """One GPT-2 model + optimizer state on the current CUDA device."""
+    """One GPT-2 model + optimizer state on the current CUDA device.  With
+    shard=(lo, hi) the handle is one rank's ZeRO-1 handle: it holds the AdamW
+    moments (and in bf16 mode the fp32 master) of the canonical slice
+    [lo, hi) only (gpt2_create_shard)."""
 
-    def __init__(self, L, H, C, V, T, B, seed=0, mode=FP32, stream=None, torch_workspace=True):
+    def __init__(self, L, H, C, V, T, B, seed=0, mode=FP32, stream=None, torch_workspace=True,
+                 shard=None):
         import torch
         self.L, self.H, self.C, self.V, self.T, self.B = L, H, C, V, T, B
         self.mode = mode
@@ -116,7 +128,7 @@ class GPT2:
         if stream is None:
             stream = torch.cuda.current_stream()
         self.stream = stream
-        nbytes = self._lib.gpt2_workspace_bytes(L, H, C, V, T, B, mode)
+        nbytes = workspace_bytes(L, H, C, V, T, B, mode, shard)
         if nbytes == 0:
             raise GPT2Error(-1, f"shape rejected: L={L} H={H} C={C} V={V} T={T} B={B}")
         self._ws = None
@@ -126,12 +138,21 @@ class GPT2:
             base = self._ws.data_ptr()
             ws_ptr = (base + 255) & ~255
         h = _vp()
-        rc = self._lib.gpt2_create(ct.byref(h), L, H, C, V, T, B, seed, mode, ws_ptr,
-                                   nbytes if ws_ptr else 0, stream.cuda_stream)
+        if shard is None:
+            rc = self._lib.gpt2_create(ct.byref(h), L, H, C, V, T, B, seed, mode, ws_ptr,
+                                       nbytes if ws_ptr else 0, stream.cuda_stream)
+        else:
+            rc = self._lib.gpt2_create_shard(ct.byref(h), L, H, C, V, T, B, seed, mode,
+                                             int(shard[0]), int(shard[1]), ws_ptr,
+                                             nbytes if ws_ptr else 0, stream.cuda_stream)
         if rc != 0:
             raise GPT2Error(rc, "gpt2_create failed")
         self.h = h
         self.n = self._lib.gpt2_num_params(h)
+        lo, hi = _sz(), _sz()
+        self._ck(self._lib.gpt2_shard_bounds(h, ct.byref(lo), ct.byref(hi)))
+        self.shard = (lo.value, hi.value)
+        self.n_state = hi.value - lo.value
         self.Vp = self._lib.gpt2_padded_vocab(h)
         self.workspace_bytes = nbytes
 
@@ -213,8 +234,9 @@ class GPT2:
         self._ck(self._lib.gpt2_set_grads(self.h, _fptr(g)))
 
     def get_opt_state(self):
-        m = np.empty(self.n, np.float32)
-        v = np.empty(self.n, np.float32)
+        """(m, v, t); m and v cover the handle's slice (all N on an unsharded handle)"""
+        m = np.empty(self.n_state, np.float32)
+        v = np.empty(self.n_state, np.float32)
         t = ct.c_int(0)
         self._ck(self._lib.gpt2_get_opt_state(self.h, _fptr(m), _fptr(v), ct.byref(t)))
         return m, v, t.value
@@ -222,8 +244,14 @@ class GPT2:
     def set_opt_state(self, m, v, step):
         m = np.ascontiguousarray(m, dtype=np.float32)
         v = np.ascontiguousarray(v, dtype=np.float32)
-        assert m.size == self.n and v.size == self.n
+        assert m.size == self.n_state and v.size == self.n_state
         self._ck(self._lib.gpt2_set_opt_state(self.h, _fptr(m), _fptr(v), int(step)))
+
+    def get_shard_master(self):
+        """the fp32 master of the handle's slice"""
+        out = np.empty(self.n_state, np.float32)
+        self._ck(self._lib.gpt2_get_shard_master(self.h, _fptr(out)))
+        return out
 
     # ---- data parallelism (see dp.DataParallel) ----
     def _ws_view(self, ptr, nbytes, dtype):
@@ -254,6 +282,12 @@ class GPT2:
 
     def set_grad_count(self, count):
         self._ck(self._lib.gpt2_set_grad_count(self.h, int(count)))
+
+    def set_grad_count_device(self, count):
+        """the next update divides by the int32 in the CUDA tensor `count`"""
+        assert count.dtype == self._torch.int32 and count.is_cuda
+        self._count_ref = count  # kept alive until the update has read it
+        self._ck(self._lib.gpt2_set_grad_count_device(self.h, count.data_ptr()))
 
     def adamw_step_shard(self, lo, hi, lr, b1=0.9, b2=0.95, eps=1e-8, wd=0.1, clip=1.0):
         norm = ct.c_float(0.0)

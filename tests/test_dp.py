@@ -48,18 +48,22 @@ def test_shard_bounds_cover_and_align():
 class OracleShardModel:
     """Stand-in for a GPT2 handle: fp64 CPU vectors, the update of a slice
     done by the oracle's AdamW, the clip scale from the norm of the whole
-    summed gradient divided by the micro-batch count"""
+    summed gradient divided by the micro-batch count.  With shard=(lo, hi) it
+    holds the moments of that slice alone, as a ZeRO-1 handle does."""
 
-    def __init__(self, n, seed):
+    def __init__(self, n, seed, shard=None):
         from oracle.pyoracle import Ops
         self.ops = Ops("double")
         g = torch.Generator().manual_seed(seed)
         self.n = n
+        self.shard = tuple(shard) if shard is not None else (0, n)
+        ns = self.shard[1] - self.shard[0]
         self.w = torch.randn(n, generator=g, dtype=torch.float64) * 0.02
-        self.m = torch.zeros(n, dtype=torch.float64)
-        self.v = torch.zeros(n, dtype=torch.float64)
+        self.m = torch.zeros(ns, dtype=torch.float64)
+        self.v = torch.zeros(ns, dtype=torch.float64)
         self.g = torch.zeros(n, dtype=torch.float64)
         self.count = 0
+        self.dcount = None
         self.t = 0
 
     def zero_grad(self):
@@ -82,17 +86,24 @@ class OracleShardModel:
     def set_grad_count(self, c):
         self.count = c
 
+    def set_grad_count_device(self, t):
+        self.dcount = t  # read by the next update, then dropped
+
     def adamw_step_shard(self, lo, hi, lr, b1, b2, eps, wd, clip):
-        norm = float(torch.sqrt((self.g * self.g).sum())) / self.count
-        sc = (1.0 / self.count) * (clip / norm if clip > 0 and norm > clip else 1.0)
+        count = int(self.dcount.item()) if self.dcount is not None else self.count
+        self.dcount = None
+        norm = float(torch.sqrt((self.g * self.g).sum())) / count
+        sc = (1.0 / count) * (clip / norm if clip > 0 and norm > clip else 1.0)
         self.t += 1
+        s0 = self.shard[0]
+        assert self.shard == (0, self.n) or self.shard == (lo, hi)
         if hi > lo:
-            w, m, v = self.ops.adamw(self.w[lo:hi].numpy(), self.m[lo:hi].numpy(),
-                                     self.v[lo:hi].numpy(), self.g[lo:hi].numpy(), sc, lr, b1,
-                                     b2, eps, wd, True, self.t)
+            w, m, v = self.ops.adamw(self.w[lo:hi].numpy(), self.m[lo - s0:hi - s0].numpy(),
+                                     self.v[lo - s0:hi - s0].numpy(), self.g[lo:hi].numpy(), sc,
+                                     lr, b1, b2, eps, wd, True, self.t)
             self.w[lo:hi] = torch.from_numpy(w)
-            self.m[lo:hi] = torch.from_numpy(m)
-            self.v[lo:hi] = torch.from_numpy(v)
+            self.m[lo - s0:hi - s0] = torch.from_numpy(m)
+            self.v[lo - s0:hi - s0] = torch.from_numpy(v)
         return norm
 
 
@@ -109,7 +120,8 @@ def _gloo_rank(rank, world, port, q, n=N_PARAMS, uneven=False):
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
                             world_size=world)
     try:
-        model = OracleShardModel(n, seed=5)
+        # each rank holds the moments of its own slice only (ZeRO-1)
+        model = OracleShardModel(n, seed=5, shard=shard_bounds(n, world)[rank])
         dp = DataParallel(model)
         norms = []
         for step in range(STEPS):
@@ -164,7 +176,8 @@ def test_data_parallel_gloo_more_ranks(world, n, uneven):
         w, m, norms = got[r]
         np.testing.assert_allclose(w, ref.w.numpy(), rtol=1e-12, atol=1e-15)
         lo, hi = bounds[r]
-        np.testing.assert_allclose(m[lo:hi], ref.m.numpy()[lo:hi], rtol=1e-12, atol=1e-15)
+        assert m.size == hi - lo  # the rank holds its slice of the moments alone
+        np.testing.assert_allclose(m, ref.m.numpy()[lo:hi], rtol=1e-12, atol=1e-15)
         assert all(got[q][2] == norms for q in range(world))  # one summed gradient everywhere
 
 
@@ -202,7 +215,7 @@ def test_data_parallel_gloo_two_ranks_equals_one_process():
         w, m, norms = got[r]
         assert np.array_equal(w, ref.w.numpy())  # every slice, after the exchange
         lo, hi = bounds[r]
-        assert np.array_equal(m[lo:hi], ref.m.numpy()[lo:hi])  # this rank's optimizer shard
+        assert np.array_equal(m, ref.m.numpy()[lo:hi])  # this rank's optimizer shard
         assert norms == ref_norms
 
 
@@ -298,6 +311,86 @@ def test_data_parallel_nccl_one_rank_equals_plain_step():
         dist.destroy_process_group()
 
 
+def _slice_adamw_oracle(w, m, v, g, lo, hi, sc, t, offsets, hp):
+    """the oracle's AdamW over the canonical slice [lo, hi), tensor by tensor
+    (decay on the 2-D weights only)"""
+    from oracle.pyoracle import DECAYED, TENSOR_NAMES, Ops
+    ops = Ops("double")
+    w, m, v = (np.array(a, np.float64) for a in (w, m, v))
+    for name in TENSOR_NAMES:
+        a, b = max(lo, offsets[name].start), min(hi, offsets[name].stop)
+        if a >= b:
+            continue
+        i, j = a - lo, b - lo
+        w[i:j], m[i:j], v[i:j] = ops.adamw(w[i:j], m[i:j], v[i:j], g[a:b], sc, hp["lr"],
+                                           hp["b1"], hp["b2"], hp["eps"], hp["wd"],
+                                           name in DECAYED, t)
+    return w, m, v
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mi", [0, 1], ids=["fp32", "bf16"])
+def test_zero1_shard_handles_against_the_oracle(mi):
+    """Two ZeRO-1 handles on one GPU, each holding the moments (and in bf16
+    mode the fp32 master) of its half only: the workspace shrinks by the
+    slices it does not hold; over three steps each rank's update of its slice
+    (master, m, v) matches the oracle's AdamW applied to the same summed
+    gradient, state and clip scale at rel 1e-4, the bf16 copy of the slice is
+    the master rounded to nearest even, and after the gather both handles hold
+    the same parameters"""
+    from oracle.pyoracle import Model
+    from parity import assert_close
+    from scratch_gpt_step_train_b300.gpt2 import GPT2, workspace_bytes
+    mode = _gpu_modes()[mi]
+    full = workspace_bytes(**CFG, mode=mode)
+    r = []
+    probe = GPT2(**CFG, seed=3, mode=mode)
+    n = probe.n
+    bounds = shard_bounds(n, 2)
+    probe.close()
+    for lo, hi in bounds:
+        saved = (n - (hi - lo)) * (12 if mi else 8)  # m, v (+ the fp32 master in bf16 mode)
+        assert abs(full - workspace_bytes(**CFG, mode=mode, shard=(lo, hi)) - saved) < 1024
+        r.append(GPT2(**CFG, seed=3, mode=mode, shard=(lo, hi)))
+    offsets = Model(**CFG, seed=3).tensor_slices()
+    count = torch.tensor([2], dtype=torch.int32, device="cuda")
+    for step in range(3):
+        for h in r:
+            h.zero_grad()
+            _micro(h, 40 + step)
+        s = r[0].grads_tensor() + r[1].grads_tensor()
+        for h in r:
+            h.grads_tensor().copy_(s)
+        torch.cuda.synchronize()
+        gsum = s.double().cpu().numpy()
+        norm = np.linalg.norm(gsum) / 2
+        sc = 0.5 * (HP["clip"] / norm if norm > HP["clip"] else 1.0)
+        before = [(h.get_shard_master(), *h.get_opt_state()[:2]) for h in r]
+        for h, (lo, hi), (w0, m0, v0) in zip(r, bounds, before):
+            h.set_grad_count_device(count)
+            ng = h.adamw_step_shard(lo, hi, **HP)
+            assert abs(ng - norm) <= 1e-5 * norm
+            w1, m1, v1 = _slice_adamw_oracle(w0, m0, v0, gsum, lo, hi, sc, step + 1, offsets, HP)
+            m, v, t = h.get_opt_state()
+            assert t == step + 1 and m.size == hi - lo
+            assert_close(h.get_shard_master(), w1, 1e-4, f"step {step} master [{lo}, {hi})")
+            assert_close(m, m1, 1e-4, f"step {step} m")
+            assert_close(v, v1, 1e-4, f"step {step} v")
+            assert h.grad_count() == 1  # the device count served one update, the host's is kept
+            if mi:
+                bf = h.param_tensors()[1][lo:hi].float().cpu()
+                rne = torch.from_numpy(h.get_shard_master()).to(torch.bfloat16).float()
+                assert torch.equal(bf, rne)
+        # the all-gather: each handle's slice into the other
+        for i, (lo, hi) in enumerate(bounds):
+            src = r[i].param_tensors()[1 if mi else 0]
+            r[1 - i].param_tensors()[1 if mi else 0][lo:hi].copy_(src[lo:hi])
+    torch.cuda.synchronize()
+    assert np.array_equal(r[0].get_params(), r[1].get_params())
+    with pytest.raises(Exception):
+        r[0].adamw_step(**HP)  # a sharded handle updates its slice only
+
+
 def test_shard_step_argument_errors_are_host_checks():
     """the C-ABI rejects unaligned or out-of-range slices before any launch
     (checked here through a null handle, which needs no GPU)"""
@@ -305,3 +398,22 @@ def test_shard_step_argument_errors_are_host_checks():
     L = lib()
     assert L.gpt2_adamw_step_shard(None, 0, 4, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, None) == -1
     assert L.gpt2_set_grad_count(None, 2) == -1
+    assert L.gpt2_set_grad_count_device(None, None) == -1
+    assert L.gpt2_create_shard(None, 2, 2, 64, 100, 16, 2, 0, 0, 0, 4, None, 0, None) == -1
+
+
+def test_zero1_workspace_sizes():
+    """a rank's workspace drops the moments (and in bf16 mode the master) of
+    the slices it does not hold; bad slices are rejected with size 0"""
+    from scratch_gpt_step_train_b300.gpt2 import BF16, FP32, workspace_bytes
+    shape = dict(L=12, H=12, C=768, V=50257, T=1024, B=16)
+    n = 124475904
+    for mode, per in ((FP32, 8), (BF16, 12)):
+        full = workspace_bytes(**shape, mode=mode)
+        for world in (2, 8):
+            lo, hi = shard_bounds(n, world)[world - 1]
+            d = full - workspace_bytes(**shape, mode=mode, shard=(lo, hi))
+            assert abs(d - per * (n - (hi - lo))) < 1024
+    assert workspace_bytes(**shape, mode=BF16, shard=(2, 64)) == 0  # unaligned
+    assert workspace_bytes(**shape, mode=BF16, shard=(64, 0)) == 0  # empty the wrong way
+    assert workspace_bytes(**shape, mode=BF16, shard=(0, n + 4)) == 0  # beyond N
