@@ -87,6 +87,7 @@ struct gpt2 {
     int32_t *tok, *tgt;
     unsigned* err;
     float* adam_state;
+    unsigned* adam_bar;  // grid-barrier words of the single-launch AdamW (zero between launches)
 
     int n_accum, t, have_targets, logits_valid, have_fwd;
     std::string last_err;
@@ -188,6 +189,7 @@ static size_t scratch_need(int L, int H, int C, int Vp, int T, int B) {
     if ((x = encoder_backward_scratch(B, T, C, Vp)) > s) s = x;
     if ((x = attention_backward_scratch(B, T, H)) > s) s = x;
     if ((x = adamw_scratch()) > s) s = x;
+    if ((x = adamw_fused_scratch()) > s) s = x;
     if ((x = gemm_tc_scratch_bytes()) > s) s = x;
     return s;
 }
@@ -235,6 +237,7 @@ static void plan(gpt2* g, char* base, size_t* total) {
     g->tgt = (int32_t*)p.take(BT * 4);
     g->err = (unsigned*)p.take(16);
     g->adam_state = (float*)p.take(16);
+    g->adam_bar = (unsigned*)p.take(16);
     *total = p.off;
 }
 
@@ -359,6 +362,7 @@ static int create(gpt2_t** out, int L, int H, int C, int V, int T, int B, uint64
         if ((e = cudaMemsetAsync(g->m, 0, g->n_state() * 4, g->stream))) break;
         if ((e = cudaMemsetAsync(g->v, 0, g->n_state() * 4, g->stream))) break;
         if ((e = cudaMemsetAsync(g->err, 0, 16, g->stream))) break;
+        if ((e = cudaMemsetAsync(g->adam_bar, 0, 16, g->stream))) break;
         if (g->no_master || g->master_sliced()) {
             // the fp32 init passes through the gradient buffer: rounded to
             // bf16 for the compute copy, and its slice kept as the master
@@ -423,8 +427,11 @@ static int check_dev_err(gpt2* g) {
         CK(cudaMemsetAsync(g->err, 0, 4, g->stream));
         if (e & GPT2_DEVERR_TOKEN)
             return fail(g, GPT2_ERR_TOKEN_RANGE, "a token or target id is outside [0, V)");
-        if (e & GPT2_DEVERR_TIMEOUT)
+        if (e & GPT2_DEVERR_TIMEOUT) {
+            // a barrier left half-way must start from zero again
+            CK(cudaMemsetAsync(g->adam_bar, 0, 16, g->stream));
             return fail(g, GPT2_ERR_TIMEOUT, "a bounded device wait ran out");
+        }
         return fail(g, GPT2_ERR_CUDA, "device error word 0x%x", e);
     }
     return GPT2_OK;
@@ -795,13 +802,6 @@ static AdamArgs adam_args(const gpt2* g, int t, float lr, float b1, float b2, fl
     return a;
 }
 
-static cudaError_t adamw_step_bf16_sr(gpt2* g, const AdamArgs& a) {
-    cudaError_t e = adamw_norm(g->grads, g->nparams, a, g->adam_state, g->scratch, g->stream);
-    if (e != cudaSuccess) return e;
-    return adamw_update_bf16_sr(g->pc, g->m, g->v, g->grads, g->nparams, a, g->adam_state,
-                                g->stream);
-}
-
 extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float eps, float wd,
                                float clip, float* h_grad_norm) {
     if (!g) return GPT2_ERR_ARG;
@@ -820,12 +820,17 @@ extern "C" int gpt2_adamw_step(gpt2_t* g, float lr, float b1, float b2, float ep
     g->last_skipped = 0;
     g->last_zl = g->last_zg = NAN;
     if (g->sk_window <= 0) {
+        // norm, clip and update in one cooperative launch
         if (g->no_master) {
-            LAUNCH(K_ADAM, 3, 0, ad_bytes - 6.0 * g->nparams, adamw_step_bf16_sr(g, a));
+            LAUNCH(K_ADAM, 1, 0, ad_bytes - 6.0 * g->nparams,
+                   adamw_fused(nullptr, g->m, g->v, g->grads, g->pc, g->nparams, 0, g->nparams,
+                               true, a, g->adam_state, g->scratch, g->adam_bar, g->err,
+                               g->stream));
         } else {
-            LAUNCH(K_ADAM, 3, 0, ad_bytes,
-                   adamw_step(g->master, g->m, g->v, g->grads, wb, g->nparams, a, g->adam_state,
-                              g->scratch, g->stream));
+            LAUNCH(K_ADAM, 1, 0, ad_bytes,
+                   adamw_fused(g->master, g->m, g->v, g->grads, wb, g->nparams, 0, g->nparams,
+                               false, a, g->adam_state, g->scratch, g->adam_bar, g->err,
+                               g->stream));
         }
         float st[3];
         CK(cudaMemcpyAsync(st, g->adam_state, 12, cudaMemcpyDeviceToHost, g->stream));
@@ -957,19 +962,19 @@ extern "C" int gpt2_adamw_step_shard(gpt2_t* g, size_t lo, size_t hi, float lr, 
     float* ms = g->sharded ? g->m : g->m + lo;
     float* vs = g->sharded ? g->v : g->v + lo;
     float* ws = g->master_sliced() ? g->master : (g->master ? g->master + lo : nullptr);
-    // the norm (and the clip scale) over every gradient, the update on [lo, hi)
-    LAUNCH(K_ADAM, 2, 0, 4.0 * g->nparams,
-           adamw_norm(g->grads, g->nparams, a, g->adam_state, g->scratch, g->stream));
-    if (n > 0) {
+    // the norm (and the clip scale) over every gradient, the update on [lo, hi),
+    // in one cooperative launch
+    {
         const size_t as = act_size(g->act);
         void* wb = g->act == ACT_BF16 ? (void*)((char*)g->pc + lo * as) : nullptr;
         if (g->no_master)
-            LAUNCH(K_ADAM, 1, 0, 26.0 * n,
-                   adamw_update_bf16_sr(wb, ms, vs, g->grads + lo, n, a, g->adam_state,
-                                        g->stream));
+            LAUNCH(K_ADAM, 1, 0, 4.0 * g->nparams + 26.0 * n,
+                   adamw_fused(nullptr, ms, vs, g->grads, wb, g->nparams, lo, n, true, a,
+                               g->adam_state, g->scratch, g->adam_bar, g->err, g->stream));
         else
-            LAUNCH(K_ADAM, 1, 0, 30.0 * n,
-                   adamw_update(ws, ms, vs, g->grads + lo, wb, n, a, g->adam_state, g->stream));
+            LAUNCH(K_ADAM, 1, 0, 4.0 * g->nparams + 30.0 * n,
+                   adamw_fused(ws, ms, vs, g->grads, wb, g->nparams, lo, n, false, a,
+                               g->adam_state, g->scratch, g->adam_bar, g->err, g->stream));
     }
     float st[3];
     CK(cudaMemcpyAsync(st, g->adam_state, 12, cudaMemcpyDeviceToHost, g->stream));

@@ -1719,6 +1719,203 @@ cudaError_t adamw_update_bf16_sr(void* wbf16, float* m, float* v, const float* g
 
 size_t adamw_scratch() { return ADAM_NB * sizeof(double); }
 
+// ---------------------------------------------------------------------------
+// AdamW with the global norm and clip in one launch ("update_params" of
+// "Karpathy's llm.c ...", "Performance comparison": one kernel for the whole
+// parameter update).  A cooperative launch (every block resident at once):
+//   1. the blocks compute the square sums of the ADAM_NB chunks that k_sumsq
+//      would (virtual block b = blockIdx.x, blockIdx.x + gridDim.x, ...), in
+//      the same order, into part[];
+//   2. a grid barrier (a counter and a generation word in device memory; each
+//      waiting thread spins a bounded number of clock cycles, then sets
+//      GPT2_DEVERR_TIMEOUT and the flag that skips the update);
+//   3. every block folds part[] exactly as k_adam_norm does (1024 virtual
+//      threads, butterfly warp sums, warps in order), so every block holds the
+//      same norm and scale, bit for bit the three-kernel result; block 0
+//      writes state[];
+//   4. the update of [0, n_upd) as k_adam / k_adam_bf16_sr (element-wise).
+// ---------------------------------------------------------------------------
+constexpr long long ADAM_BAR_LIMIT = 4000000000LL;  // ~2 s of SM clock
+
+__device__ bool adam_grid_barrier(unsigned* bar, unsigned nblocks, unsigned* err) {
+    __shared__ int ok_s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile unsigned* gen = bar + 1;
+        const unsigned g0 = *gen;
+        __threadfence();
+        const unsigned arrived = atomicAdd(bar, 1u) + 1u;
+        int ok = 1;
+        if (arrived == nblocks) {
+            bar[0] = 0u;  // reset for the next barrier, before releasing the others
+            __threadfence();
+            atomicAdd(bar + 1, 1u);
+        } else {
+            const long long t0 = clock64();
+            while (*gen == g0) {
+                if (clock64() - t0 > ADAM_BAR_LIMIT) {
+                    ok = 0;
+                    if (err) atomicOr(err, GPT2_DEVERR_TIMEOUT);
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+        ok_s = ok;
+    }
+    __syncthreads();
+    return ok_s != 0;
+}
+
+template <bool SR>
+__global__ void __launch_bounds__(256) k_adam_fused(float* w, float* m, float* v, const float* g,
+                                                    void* wb, size_t n_total, size_t lo,
+                                                    size_t n_upd, AdamArgs a, float* state,
+                                                    double* part, unsigned* bar, unsigned* err) {
+    __shared__ double sh[32];
+    __shared__ float sc_s;
+    __shared__ int fin_s;
+    // 1. square sums of the ADAM_NB chunks of the whole gradient
+    const size_t chunk = ((n_total + ADAM_NB - 1) / ADAM_NB + 3) & ~(size_t)3;
+    for (int vb = blockIdx.x; vb < ADAM_NB; vb += gridDim.x) {
+        const size_t b0 = (size_t)vb * chunk, b1 = b0 + chunk < n_total ? b0 + chunk : n_total;
+        float acc = 0.f;
+        if (b0 < b1) {
+            const size_t nv = (b1 - b0) / 4;
+            const float4* g4 = reinterpret_cast<const float4*>(g + b0);
+            for (size_t i = threadIdx.x; i < nv; i += blockDim.x) {
+                const float4 x = g4[i];
+                acc += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+            }
+            for (size_t i = b0 + nv * 4 + threadIdx.x; i < b1; i += blockDim.x) acc += g[i] * g[i];
+        }
+        const double d = warp_sum_d((double)acc);
+        if ((threadIdx.x & 31) == 0) sh[threadIdx.x / 32] = d;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double t = 0.0;
+            for (int k = 0; k < 8; k++) t += sh[k];
+            part[vb] = t;
+        }
+        __syncthreads();
+    }
+    // 2. every partial written
+    const bool ok = adam_grid_barrier(bar, gridDim.x, err);
+    // 3. the fold of k_adam_norm, 1024 virtual threads over 256
+    for (int k = 0; k < 4; k++) {
+        const int vt = threadIdx.x + 256 * k;
+        double x = 0.0;
+        for (int i = vt; i < ADAM_NB; i += 1024) x += __ldcg(part + i);  // L2: other blocks' writes
+        x = warp_sum_d(x);
+        if ((threadIdx.x & 31) == 0) sh[vt / 32] = x;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int k = 0; k < 32; k++) t += sh[k];
+        float inv = a.d_count ? __fdiv_rn(1.0f, (float)*a.d_count) : a.inv_accum;
+        const float norm = (float)(sqrt(t) * (double)inv);
+        const int finite = isfinite(norm) ? 1 : 0;
+        float sc = inv;
+        if (finite && a.clip > 0.f && norm > a.clip) sc = inv * (a.clip / norm);
+        sc_s = sc;
+        fin_s = finite && ok;
+        if (blockIdx.x == 0) {
+            state[0] = norm;
+            state[1] = sc;
+            state[2] = (float)finite;
+        }
+    }
+    __syncthreads();
+    if (!fin_s) return;
+    const float sc = sc_s;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    if (!SR) {
+        // 4. the update of [lo, lo + n_upd): w, m, v at their offsets, the
+        // bf16 copy (if any) refreshed
+        float* W = w;
+        const float* G = g + lo;
+        bf16* WB = reinterpret_cast<bf16*>(wb);
+        const size_t nv = n_upd / 4;
+        for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nv; i += stride) {
+            float4 X = reinterpret_cast<float4*>(W)[i];
+            float4 M = reinterpret_cast<float4*>(m)[i];
+            float4 Vv = reinterpret_cast<float4*>(v)[i];
+            const float4 Gr = reinterpret_cast<const float4*>(G)[i];
+            const size_t e = i * 4;
+            adam_one(X.x, M.x, Vv.x, Gr.x, sc, a, decayed(e, a));
+            adam_one(X.y, M.y, Vv.y, Gr.y, sc, a, decayed(e + 1, a));
+            adam_one(X.z, M.z, Vv.z, Gr.z, sc, a, decayed(e + 2, a));
+            adam_one(X.w, M.w, Vv.w, Gr.w, sc, a, decayed(e + 3, a));
+            reinterpret_cast<float4*>(W)[i] = X;
+            reinterpret_cast<float4*>(m)[i] = M;
+            reinterpret_cast<float4*>(v)[i] = Vv;
+            if (WB) {
+                __nv_bfloat162 l2 = __floats2bfloat162_rn(X.x, X.y);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(X.z, X.w);
+                uint2 pk;
+                pk.x = *reinterpret_cast<unsigned*>(&l2);
+                pk.y = *reinterpret_cast<unsigned*>(&h2);
+                reinterpret_cast<uint2*>(WB)[i] = pk;
+            }
+        }
+        for (size_t e = nv * 4 + blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n_upd;
+             e += stride) {
+            float X = W[e], M = m[e], Vv = v[e];
+            adam_one(X, M, Vv, G[e], sc, a, decayed(e, a));
+            W[e] = X;
+            m[e] = M;
+            v[e] = Vv;
+            if (WB) WB[e] = __float2bfloat16_rn(X);
+        }
+    } else {
+        const uint64_t k0 = (uint64_t)(a.t - 1) * (uint64_t)a.n_total + a.base;
+        uint16_t* wu = reinterpret_cast<uint16_t*>(wb);
+        const float* G = g + lo;
+        for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n_upd; e += stride) {
+            float X = __uint_as_float((uint32_t)wu[e] << 16), M = m[e], Vv = v[e];
+            adam_one(X, M, Vv, G[e], sc, a, decayed(e, a));
+            m[e] = M;
+            v[e] = Vv;
+            wu[e] = sround_bf16(X, sm64_at(a.sr_seed, k0 + e));
+        }
+    }
+}
+
+size_t adamw_fused_scratch() { return ADAM_NB * sizeof(double) + 256; }
+
+template <bool SR>
+static int fused_grid() {
+    static int grid = 0;
+    if (grid == 0) {
+        int dev = 0, nsm = 148, per = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_adam_fused<SR>, 256, 0) !=
+                cudaSuccess ||
+            per < 1) {
+            cudaGetLastError();
+            per = 1;
+        }
+        grid = nsm * (per < 8 ? per : 8);
+    }
+    return grid;
+}
+
+cudaError_t adamw_fused(float* w, float* m, float* v, const float* g, void* wbf16,
+                        size_t n_total, size_t lo, size_t n_upd, bool sr, const AdamArgs& a,
+                        float* state, void* scratch, unsigned* bar, unsigned* err,
+                        cudaStream_t s) {
+    double* part = (double*)scratch;
+    const int grid = sr ? fused_grid<true>() : fused_grid<false>();
+    void* args[] = {&w, &m, &v, (void*)&g, &wbf16, &n_total, &lo, &n_upd, (void*)&a, &state,
+                    &part, &bar, &err};
+    return cudaLaunchCooperativeKernel(
+        sr ? (const void*)k_adam_fused<true> : (const void*)k_adam_fused<false>, dim3(grid),
+        dim3(256), args, 0, s);
+}
+
 cudaError_t adamw_norm(const float* g, size_t n, const AdamArgs& a, float* state, void* scratch,
                        cudaStream_t s) {
     double* part = (double*)scratch;

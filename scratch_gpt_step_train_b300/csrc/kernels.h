@@ -110,6 +110,18 @@ cudaError_t adamw_norm(const float* g, size_t n, const AdamArgs& a, float* state
                        cudaStream_t s);
 cudaError_t adamw_update(float* w, float* m, float* v, const float* g, void* wbf16, size_t n,
                          const AdamArgs& a, const float* state, cudaStream_t s);
+// the whole AdamW step in one cooperative launch: the global norm and clip
+// scale over g[0, n_total), the update of the n_upd elements at w, m, v (g
+// read from g + lo; a.base = the canonical index of the first), the bf16 copy
+// refreshed (sr: parameters only in bf16, stochastic rounding at wbf16).
+// Results are bit for bit those of adamw_norm + adamw_update.  scratch: at
+// least adamw_fused_scratch() bytes; bar: two words that are zero before the
+// first launch (the kernel leaves them so).
+size_t adamw_fused_scratch();
+cudaError_t adamw_fused(float* w, float* m, float* v, const float* g, void* wbf16,
+                        size_t n_total, size_t lo, size_t n_upd, bool sr, const AdamArgs& a,
+                        float* state, void* scratch, unsigned* bar, unsigned* err,
+                        cudaStream_t s);
 // out[i] = gelu(in[i]) for i < n (dtype act), the fused epilogue's formula
 cudaError_t gelu_forward(int act, void* out, const void* in, size_t n, cudaStream_t s);
 // parameters held only in bf16: AdamW in fp32, stochastic rounding back

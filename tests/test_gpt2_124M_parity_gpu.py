@@ -72,15 +72,23 @@ def _bar(e32, tol=1e-4, factor=4.0):
     return max(tol, factor * max(e32)) if e32 is not None else tol
 
 
+def _golden(p, how):
+    if not os.path.exists(p):
+        pytest.fail(f"stored oracle values missing: run oracle/make_golden_124M.py {how}")
+    return _load(p)
+
+
 @pytest.fixture(scope="module")
-def golden():
-    if not os.path.exists(G64) or not os.path.exists(G32):
-        pytest.fail("stored oracle values missing: run oracle/make_golden_124M.py")
-    return _load(G64), _load(G32)
+def g64():
+    return _golden(G64, "")
 
 
-def test_fp32_124M_ten_steps(golden):
-    g64, g32 = golden
+@pytest.fixture(scope="module")
+def g32():
+    return _golden(G32, "--real float")
+
+
+def test_fp32_124M_ten_steps(g64, g32):
     gm = GPT2(**CFG, seed=1, mode=FP32)
     sl = _offsets(gm)
     stream = inputs.ZipfStream(2, CFG["B"], CFG["T"], CFG["V"])
@@ -122,8 +130,7 @@ def test_fp32_124M_ten_steps(golden):
         assert abs(norm - no) <= 1e-4 * no, (s, norm, no)
 
 
-def test_bf16_124M_twenty_steps(golden):
-    g64, _ = golden
+def test_bf16_124M_twenty_steps(g64):
     gm = GPT2(**CFG, seed=1, mode=BF16)
     stream = inputs.ZipfStream(2, CFG["B"], CFG["T"], CFG["V"])
     worst = 0.0
