@@ -322,6 +322,16 @@ def run_gpu(w, rank, world, steps, warmup, accum, rl_steps):
     model.prof_enable([])
     dprof = model.prof_read()[dom]
 
+    # memory-bound classes: in-step GB/s (from the all-class step above)
+    # against a copy of the same bytes (half read, half written) measured now
+    mem = {}
+    for k, (cms, cn, cfl, cby) in prof.items():
+        if cn and cfl == 0 and cby > 0 and cms > 0:
+            mem[k] = {"bytes_per_launch": cby / cn, "gbs": cby / cn / (cms / cn / 1e3) / 1e9,
+                      "launches": cn}
+    for k, v in mem.items():
+        v["copy_gbs_same_bytes"] = copy_rate(int(v["bytes_per_launch"]), stream)
+
     # end to end
     ptok = [torch.from_numpy(a).pin_memory() for a, _ in host]
     ptgt = [torch.from_numpy(b).pin_memory() for _, b in host]
@@ -344,7 +354,28 @@ def run_gpu(w, rank, world, steps, warmup, accum, rl_steps):
     del model
     torch.cuda.empty_cache()
     return dict(ms=ms, launches=launches, dom=dom, dprof=dprof, clocks=clk, e2e_s=e2e_s,
-                final_loss=final_loss, h2d=accum * 2 * B * T * 4, d2h=20, prof=prof)
+                final_loss=final_loss, h2d=accum * 2 * B * T * 4, d2h=20, prof=prof, mem=mem)
+
+
+def copy_rate(nbytes, stream, reps=7):
+    """GB/s of torch's device copy moving nbytes in all (nbytes/2 read,
+    nbytes/2 written), median of `reps`, on the bench's stream: the ceiling a
+    memory-bound kernel of that size meets, ramp and tail included"""
+    import torch
+    n = max(16, nbytes // 2)
+    src = torch.empty(n, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    ts = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps + 2):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+    return 2 * n / (statistics.median(ts[2:]) / 1e3) / 1e9
 
 
 def max_over_ranks(x, world):
@@ -414,7 +445,7 @@ def main():
                             peaks, peak_kind)
         line["secondary"] = {k: sec[k] for k in (
             "value", "unit", "ms_per_step", "steps", "warmup", "config", "bf16_mfu", "roofline",
-            "e2e", "gpu_launches", "clocks", "final_loss")}
+            "e2e", "gpu_launches", "clocks", "final_loss", "memory_bound")}
     if rank != 0:
         return
     line["cpu_baseline"] = cpu
@@ -474,6 +505,12 @@ def workload_line(name, w, steps, warmup, accum_override, rl_steps, rank, world,
         "clocks": r["clocks"],
         "final_loss": r["final_loss"],
         "kernel_ms_calibration_step": {k: round(v[0], 3) for k, v in r["prof"].items() if v[1]},
+        "memory_bound": {k: {"gbs": round(v["gbs"], 1),
+                             "mb_per_launch": round(v["bytes_per_launch"] / 1e6, 2),
+                             "copy_gbs_same_bytes": round(v["copy_gbs_same_bytes"], 1),
+                             "frac_of_peak": round(v["gbs"] / peaks.get("hbm_gbs", 6400.0), 3),
+                             "frac_of_copy": round(v["gbs"] / v["copy_gbs_same_bytes"], 3)}
+                         for k, v in r["mem"].items()},
     }
 
 

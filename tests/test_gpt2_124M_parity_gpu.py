@@ -12,7 +12,8 @@ fp64 oracle's 20 steps, gpt2_124M_B4T1024_f32.npz the fp32 build's first 10.
 
 fp32 mode, 10 steps (rel 1e-4 read per tensor as ||d||_2 <= 1e-4 ||ref||_2
 and max|d| <= 1e-4 max|ref|):
-  * the loss and the gradient norm each update sees, at every step;
+  * the loss and the gradient norm each update sees, at every step (from the
+    second step under the bar below);
   * at step 1 (both sides hold the same weights): sampled logits, every
     element of the small gradient tensors and 8192 sampled elements of each
     large one, and every tensor's L2 norm and max |.|;
@@ -106,7 +107,8 @@ def test_fp32_124M_ten_steps(g64, g32):
         gm.zero_grad()
         loss = gm.forward(tok, tgt, sync_loss=True)
         lo = g64["loss"][s - 1]
-        assert abs(loss - lo) <= 1e-4 * abs(lo), (s, loss, lo)
+        e32 = None if s == 1 else (abs(g32["loss"][s - 1] - lo) / abs(lo),)
+        assert abs(loss - lo) <= _bar(e32) * abs(lo), (s, loss, lo, e32)
         gm.backward()
         g = gm.get_grads()
         for j, k in enumerate(TENSOR_NAMES):
@@ -127,7 +129,8 @@ def test_fp32_124M_ten_steps(g64, g32):
                 assert max(e) <= _bar(e32), (s, k, e, e32)
         norm = gm.adamw_step(**HP)
         no = g64["norm"][s - 1]
-        assert abs(norm - no) <= 1e-4 * no, (s, norm, no)
+        e32 = None if s == 1 else (abs(g32["norm"][s - 1] - no) / no,)
+        assert abs(norm - no) <= _bar(e32) * no, (s, norm, no, e32)
 
 
 def test_bf16_124M_twenty_steps(g64):
