@@ -33,467 +33,19 @@
 // Weight-gradient products have K = B*T (16384) and few output tiles; they
 // are split along K into fp32 partial tiles summed in a fixed order by a
 // second kernel (deterministic; no float atomics).
-#include <cuda.h>
-#include <string.h>
-
-#include "common.cuh"
-#include "gemm_tc.h"
-#include "tc_ptx.cuh"
+#include "gemm_tc_kernel.cuh"
 
 namespace gk {
+namespace tcg {
 
-namespace {
-
-using namespace tc;
-
-constexpr int BM = 128;
-constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int NUM_THREADS = 320;  // producer, MMA, 8 epilogue warps
-
-template <int BN>
-struct Cfg {
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STG_BYTES = 8 * 4096;  // epilogue staging: 4 KB per epilogue warp
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + STG_BYTES + 1024 + BAR_BYTES;
-};
-
-struct TcParams {
-    int M, N, K;
-    int tiles_m, tiles_n, splits, k_per_split, num_tiles;
-    int n_fastest;  // work-unit order: 1 = output-column tiles vary fastest
-    int epi;
-    void* D;
-    long ldd;
-    const bf16* bias;
-    const bf16* resid;
-    long ldr;
-    bf16* aux;
-    long ldx;
-    float* part;
-    unsigned* err;
-};
-
-enum { EPI_PART_F32 = 100 };
-
-// ------------------------------------------------------------------ epilogue
-__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ void ld8_bf16(float* f, const bf16* p) {
-    uint4 u = *reinterpret_cast<const uint4*>(p);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-__device__ __forceinline__ void st8_bf16(bf16* p, const float* f) {
-    uint4 u;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-    *reinterpret_cast<uint4*>(p) = u;
-}
-
-// GELU and GELU' for the bf16 epilogues: the same sigmoid form as gelu_f /
-// gelu_grad_f with the fast exp and divide intrinsics (a few fp32 ulp, far
-// below the bf16 rounding of the stored result); u is clamped at -40 so the
-// divisor stays finite.
-__device__ __forceinline__ float gelu_fast(float x) {
-    const float k = 0.7978845608028654f;
-    float u = fmaxf(k * (x + 0.044715f * x * x * x), -40.0f);
-    return __fdividef(x, 1.0f + __expf(-2.0f * u));
-}
-// gelu(x) and gelu'(x) sharing one sigmoid s = 1/(1 + e^{-2u}) (two MUFU
-// operations).  With u = k (x + c x^3), the derivative term 2 x du/dx equals
-// 6u - 4kx exactly, so gelu' = s + (s - s^2)(6u - 4kx) costs three FMAs.
-__device__ __forceinline__ void gelu_and_grad_fast(float x, float& g, float& dg) {
-    const float k = 0.7978845608028654f;
-    const float u = k * fmaf(0.044715f * x, x * x, x);
-    const float s = __fdividef(1.0f, 1.0f + __expf(-2.0f * fmaxf(u, -40.0f)));
-    g = x * s;
-    dg = fmaf(fmaf(-s, s, s), fmaf(-4.0f * k, x, 6.0f * u), s);
-}
-__device__ __forceinline__ float gelu_grad_fast(float x) {
-    const float k = 0.7978845608028654f;
-    float x2 = x * x;
-    float u = fmaxf(k * (x + 0.044715f * x2 * x), -40.0f);
-    float sg = __fdividef(1.0f, 1.0f + __expf(-2.0f * u));
-    float du = k * (1.0f + 3.0f * 0.044715f * x2);
-    return sg + 2.0f * x * sg * (1.0f - sg) * du;
-}
-
-// TMA bulk-store helpers (smem -> global through a tensor map)
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
-                 ::"l"((uint64_t)map), "r"(src), "r"(c0), "r"(c1)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
-                                             int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-        ::"l"((uint64_t)map), "r"(src), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int c0,
-                                                  int c1) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
-        ::"l"((uint64_t)map), "r"(src), "r"(c0), "r"(c1)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read0() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// row r of a 32 x 32 bf16 staging tile (64-byte rows, 64-byte swizzle)
-__device__ __forceinline__ void stage_bf16_row(uint32_t stg, int r, const float* x) {
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const float* f = x + 8 * k;
-        st_shared_v4(stg + r * 64 + ((uint32_t)(k ^ ((r >> 1) & 3)) << 4),
-                     pack2_bf16(f[0], f[1]), pack2_bf16(f[2], f[3]), pack2_bf16(f[4], f[5]),
-                     pack2_bf16(f[6], f[7]));
-    }
-}
-// row r of a 32 x 32 fp32 staging tile (128-byte rows, 128-byte swizzle)
-__device__ __forceinline__ void stage_f32_row(uint32_t stg, int r, const float* x) {
-#pragma unroll
-    for (int k = 0; k < 8; k++)
-        st_shared_v4(stg + r * 128 + ((uint32_t)(k ^ (r & 7)) << 4), __float_as_uint(x[4 * k]),
-                     __float_as_uint(x[4 * k + 1]), __float_as_uint(x[4 * k + 2]),
-                     __float_as_uint(x[4 * k + 3]));
-}
-
-struct EpiMaps {
-    CUtensorMap d;    // bf16 [M,N] box 32x32 SW64, or fp32 [M,N] box 32x32 SW128 (accumulate)
-    CUtensorMap aux;  // bf16 [M,N] box 32x32 SW64 (GELU pre-activation, or gelu')
-    CUtensorMap part; // fp32 [splits,M,N] box 32x32x1 SW128 (split-K partials)
-};
-
-// Row-wise operand of a chunk that comes from global memory (the residual for
-// EPI_RESID, the pre-activation for EPI_GELU_BWD): 32 bf16 of this lane's row,
-// loaded one chunk ahead so the load latency hides behind the previous chunk.
-__device__ __forceinline__ void epi_prefetch(const TcParams& p, int row, int col, uint4 (&pf)[4]) {
-    const bf16* src = nullptr;
-    if (p.epi == EPI_RESID) src = p.resid + (size_t)row * p.ldr + col;
-    else if (p.epi == EPI_GELU_BWD || p.epi == EPI_MUL_AUX) src = p.aux + (size_t)row * p.ldx + col;
-    const int nv = min(32, p.N - col);
-#pragma unroll
-    for (int k = 0; k < 4; k++)
-        pf[k] = (src && row < p.M && 8 * k < nv) ? *reinterpret_cast<const uint4*>(src + 8 * k)
-                                                  : make_uint4(0u, 0u, 0u, 0u);
-}
-__device__ __forceinline__ void unpack8_bf16(float* f, uint4 u) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-
-// One warp: the 32 x 32 chunk at rows [row0, row0+32), columns [col, col+32);
-// lane = row within the chunk; v = this lane's 32 accumulator values; pf =
-// this lane's prefetched row operand (see epi_prefetch).
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps& m, int row0,
-                                               int col, int lane, float* v, int split,
-                                               uint32_t stg, const uint4 (&pf)[4]) {
-    const int nv = min(32, p.N - col);  // multiple of 8
-    if (p.epi == EPI_GELU_BWD) {
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            float pre[8];
-            unpack8_bf16(pre, pf[k]);
-#pragma unroll
-            for (int i = 0; i < 8; i++) v[8 * k + i] *= gelu_grad_fast(pre[i]);
-        }
-    } else if (p.epi == EPI_MUL_AUX) {
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            float dg[8];
-            unpack8_bf16(dg, pf[k]);
-#pragma unroll
-            for (int i = 0; i < 8; i++) v[8 * k + i] *= dg[i];
-        }
-    } else if (p.epi != EPI_ACCUM_F32 && p.epi != EPI_PART_F32) {
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            if (p.bias && 8 * k < nv) {
-                float b[8];
-                ld8_bf16(b, p.bias + col + 8 * k);
-#pragma unroll
-                for (int i = 0; i < 8; i++) v[8 * k + i] += b[i];
-            }
-            if (p.epi == EPI_RESID) {
-                float r8[8];
-                unpack8_bf16(r8, pf[k]);
-#pragma unroll
-                for (int i = 0; i < 8; i++) v[8 * k + i] += r8[i];
-            }
-        }
-    }
-    // the previous chunk's bulk stores must have finished reading the staging tile
-    if (lane == 0) bulk_wait_read0();
-    __syncwarp();
-    if (p.epi == EPI_ACCUM_F32 || p.epi == EPI_PART_F32) {
-        stage_f32_row(stg, lane, v);
-    } else if (p.epi == EPI_GELU_D) {
-        float dg[32];
-#pragma unroll
-        for (int i = 0; i < 32; i++) gelu_and_grad_fast(v[i], v[i], dg[i]);
-        stage_bf16_row(stg + 2048, lane, dg);  // gelu'
-        stage_bf16_row(stg, lane, v);
-    } else if (p.epi == EPI_GELU) {
-        stage_bf16_row(stg + 2048, lane, v);  // pre-activation
-#pragma unroll
-        for (int i = 0; i < 32; i++) v[i] = gelu_fast(v[i]);
-        stage_bf16_row(stg, lane, v);
-    } else {
-        stage_bf16_row(stg, lane, v);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-        if (p.epi == EPI_ACCUM_F32) tma_reduce_add_2d(&m.d, stg, col, row0);
-        else if (p.epi == EPI_PART_F32) tma_store_3d(&m.part, stg, col, row0, split);
-        else {
-            tma_store_2d(&m.d, stg, col, row0);
-            if (p.epi == EPI_GELU || p.epi == EPI_GELU_D)
-                tma_store_2d(&m.aux, stg + 2048, col, row0);
-        }
-        bulk_commit();
-    }
-}
-
-// ------------------------------------------------------------------- kernel
-template <int BN, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-              const __grid_constant__ EpiMaps maps, TcParams p) {
-    using CF = Cfg<BN>;
-    constexpr int S = CF::STAGES;
-    constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t tiles = (raw + 1023u) & ~1023u;
-    uint8_t* tiles_gen = smem_raw + (tiles - raw);
-    const uint32_t stg_base = tiles + S * CF::STAGE_BYTES;  // 1024-aligned
-    const uint32_t bars = stg_base + CF::STG_BYTES;
-    const uint32_t full = bars, empty = bars + 8 * S, tfull = bars + 16 * S,
-                   tempty = tfull + 16;
-    uint32_t* tmem_slot = (uint32_t*)(tiles_gen + S * CF::STAGE_BYTES + CF::STG_BYTES + 16 * S + 32);
-    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-
-    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; s++) {
-            mbar_init(full + 8 * s, 1);
-            mbar_init(empty + 8 * s, 1);
-        }
-        for (int b = 0; b < 2; b++) {
-            mbar_init(tfull + 8 * b, 1);
-            mbar_init(tempty + 8 * b, 8);
-        }
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&mapA) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&mapB) : "memory");
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 2 * BN);
-        tmem_relinquish();
-        tc_fence_before();
-    }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-    gdc_wait();  // setup above touches no global memory
-    gdc_launch_dependents();
-    // work units: output tiles (times K splits), strided over the CTAs
-    const int units_m = p.tiles_m;
-    const int units_mn = units_m * p.tiles_n;
-    const int num_units = units_mn * p.splits;
-    const int unit0 = (int)blockIdx.x;
-    const int ustep = (int)gridDim.x;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------------------- producer
-            int s = 0;
-            uint32_t ph = 0;
-            uint32_t issued = 0;  // bit s: stage s has a load in flight or landed
-            bool ok = true;
-            for (int u = unit0; ok && u < num_units; u += ustep) {
-                const int split = u / units_mn, r = u % units_mn;
-                const int um = p.n_fastest ? r / p.tiles_n : r % units_m;
-                const int tn = p.n_fastest ? r % p.tiles_n : r / units_m;
-                const int tm = um;
-                const int k0 = split * p.k_per_split;
-                const int k1 = min(p.K, k0 + p.k_per_split);
-                const int nkb = (k1 - k0 + BK - 1) / BK;
-                for (int kb = 0; kb < nkb; kb++) {
-                    if (!mbar_wait(empty + 8 * s, ph ^ 1u, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sa = tiles + s * CF::STAGE_BYTES, sb = sa + CF::A_BYTES;
-                    const uint32_t fb = full + 8 * s;
-                    mbar_expect_tx(fb, CF::STAGE_BYTES);
-                    const int kk = k0 + kb * BK;
-                    if (!A_MN) {
-                        tma_load_2d(sa, &mapA, fb, kk, tm * BM);
-                    } else {
-                        tma_load_2d(sa, &mapA, fb, tm * BM, kk);
-                        tma_load_2d(sa + 8192, &mapA, fb, tm * BM + 64, kk);
-                    }
-                    if (!B_MN) {
-                        tma_load_2d(sb, &mapB, fb, kk, tn * BN);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < BN / 64; j++)
-                            tma_load_2d(sb + j * 8192, &mapB, fb, tn * BN + 64 * j, kk);
-                    }
-                    issued |= 1u << s;
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                // drain: wait (bounded, ignoring the abort flag) for every
-                // stage's most recent load so no copy lands after exit
-                for (int i = 0; i < S; i++) {
-                    if (!((issued >> i) & 1u)) continue;
-                    // the last issue of stage i used parity (ph if i < s else ph^1)
-                    uint32_t par = i < s ? ph : ph ^ 1u;
-                    long long t0 = clock64();
-                    while (!mbar_try(full + 8 * i, par) && clock64() - t0 < WAIT_LIMIT) {
-                    }
-                }
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // --------------------------------------------------------- MMA
-            int s = 0;
-            uint32_t ph = 0;
-            int lt = 0;
-            bool ok = true;
-            // stage-0 descriptors; stages and K steps add start-address offsets
-            const uint64_t dA0 = A_MN ? sdesc(tiles, 8192, 1024) : sdesc(tiles, 0, 1024);
-            const uint64_t dB0 = B_MN ? sdesc(tiles + CF::A_BYTES, 8192, 1024)
-                                      : sdesc(tiles + CF::A_BYTES, 0, 1024);
-            for (int u = unit0; ok && u < num_units; u += ustep, lt++) {
-                const int split = u / units_mn;
-                const int k0 = split * p.k_per_split;
-                const int k1 = min(p.K, k0 + p.k_per_split);
-                const int nkb = (k1 - k0 + BK - 1) / BK;
-                const int b = lt & 1;
-                const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
-                if (!mbar_wait(tempty + 8 * b, aph ^ 1u, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t dt = tmem_base + (uint32_t)(b * BN);
-                for (int kb = 0; kb < nkb; kb++) {
-                    if (!mbar_wait(full + 8 * s, ph, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t ad0 = dA0 + (uint64_t)((s * CF::STAGE_BYTES) >> 4);
-                    const uint64_t bd0 = dB0 + (uint64_t)((s * CF::STAGE_BYTES) >> 4);
-#pragma unroll
-                    for (int k = 0; k < BK / 16; k++)
-                        umma_bf16(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
-                                  bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
-                                  (kb > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(empty + 8 * s);
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                umma_commit(tfull + 8 * b);
-            }
-        }
-    } else {
-        // ------------------------------------------------------- epilogue
-        // warps 2..9: TMEM lane quarter (warp % 4) x column half
-        const int q = warp & 3;
-        const int cbeg = ((warp - 2) >> 2) * (BN / 2);
-        constexpr int NCH = BN / 64;  // 32-column chunks per half
-        const uint32_t stg = stg_base + (uint32_t)(warp - 2) * 4096u;
-        const bool has_pf = p.epi == EPI_RESID || p.epi == EPI_GELU_BWD || p.epi == EPI_MUL_AUX;
-        int lt = 0;
-        for (int u = unit0; u < num_units; u += ustep, lt++) {
-            const int split = u / units_mn, r = u % units_mn;
-            const int um = p.n_fastest ? r / p.tiles_n : r % units_m;
-            const int tn = p.n_fastest ? r % p.tiles_n : r / units_m;
-            const int tm = um;
-            const int b = lt & 1;
-            const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
-            const int row = tm * BM + q * 32 + lane;
-            uint4 pf[2][4];
-            // the first chunk's row operand does not depend on the accumulator:
-            // fetch it before waiting for the tile
-            if (has_pf) epi_prefetch(p, row, tn * BN + cbeg, pf[0]);
-            // every lane waits (suspended in the barrier's try_wait until the
-            // phase completes); the warp goes on only if all saw it complete
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull + 8 * b, aph, abort_flag, p.err));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cbeg);
-            uint32_t buf[2][32];
-            tmem_ld32_async(taddr, buf[0]);
-            tmem_wait32(buf[0]);
-#pragma unroll
-            for (int c = 0; c < NCH; c++) {
-                if (c + 1 < NCH) {
-                    tmem_ld32_async(taddr + (uint32_t)(32 * (c + 1)), buf[(c + 1) & 1]);
-                    if (has_pf) epi_prefetch(p, row, tn * BN + cbeg + 32 * (c + 1), pf[(c + 1) & 1]);
-                }
-                const int col = tn * BN + cbeg + 32 * c;
-                if (col < p.N) {
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(buf[c & 1][i]);
-                    epilogue_chunk(p, maps, tm * BM + q * 32, col, lane, v, split, stg, pf[c & 1]);
-                }
-                if (c + 1 < NCH) tmem_wait32(buf[(c + 1) & 1]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty + 8 * b);
-        }
-        if (lane == 0) bulk_wait0();  // all bulk stores of this warp complete
-        __syncwarp();
-    }
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem_base, 2 * BN);
-    }
-}
+GK_GEMM_EPI_EXTERN(EPI_STORE)
+GK_GEMM_EPI_EXTERN(EPI_RESID)
+GK_GEMM_EPI_EXTERN(EPI_GELU)
+GK_GEMM_EPI_EXTERN(EPI_GELU_D)
+GK_GEMM_EPI_EXTERN(EPI_GELU_BWD)
+GK_GEMM_EPI_EXTERN(EPI_MUL_AUX)
+GK_GEMM_EPI_EXTERN(EPI_ACCUM_F32)
+GK_GEMM_EPI_EXTERN(EPI_PART_F32)
 
 // split-K: D[m,n] += sum_s part[s][m][n], s in order
 __global__ void k_splitk_reduce(float* D, long ldd, const float* part, int M, int N, int splits) {
@@ -514,20 +66,12 @@ __global__ void k_splitk_reduce(float* D, long ldd, const float* part, int M, in
     *d = o;
 }
 
+
 // ----------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 int g_num_sms = 148;
 int g_state = -1;  // -1 unknown, 0 unavailable, 1 ready
 
-template <int BN, bool AM, bool BMN>
-void set_smem_attr() {
-    cudaFuncSetAttribute(k_gemm_tc<BN, AM, BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         Cfg<BN>::SMEM);
-}
 
 // 2-D bf16 tensor map: inner extent `inner` (contiguous), `outer` rows of
 // `ld` elements; box = 64 x box_outer; 128-byte swizzle; OOB reads give 0.
@@ -577,24 +121,11 @@ bool make_epi_maps(EpiMaps* em, const GemmDesc& d, const TcParams& tp) {
     return ok;
 }
 
-template <int BN, bool AM, bool BMN>
-cudaError_t launch(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
-    CUtensorMap ma, mb;
-    EpiMaps em;
-    if (!make_epi_maps(&em, d, tp)) return cudaErrorInvalidValue;
-    // A: K-major -> [M rows][K], box 64(K) x 128(M);  MN-major -> [K rows][M], box 64(M) x 64(K)
-    bool ok = AM ? make_map(&ma, d.A, d.M, d.K, d.lda, 64)
-                 : make_map(&ma, d.A, d.K, d.M, d.lda, BM);
-    // B: K-major box 64(K) x BN rows;  N-major box 64(N) x 64(K)
-    ok = ok && (BMN ? make_map(&mb, d.B, d.N, d.K, d.ldb, 64)
-                    : make_map(&mb, d.B, d.K, d.N, d.ldb, BN));
-    if (!ok) return cudaErrorInvalidValue;
-    const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
-    launch_pdl(k_gemm_tc<BN, AM, BMN>, grid, NUM_THREADS, Cfg<BN>::SMEM, s, ma, mb, em, tp);
-    return cudaGetLastError();
-}
 
-}  // namespace
+
+}  // namespace tcg
+
+using namespace tcg;
 
 bool gemm_tc_available() {
     if (g_state >= 0) return g_state == 1;
@@ -614,14 +145,6 @@ bool gemm_tc_available() {
         return false;
     }
     g_encode = (EncodeTiledFn)fn;
-    set_smem_attr<256, false, false>();
-    set_smem_attr<256, false, true>();
-    set_smem_attr<256, true, false>();
-    set_smem_attr<256, true, true>();
-    set_smem_attr<128, false, false>();
-    set_smem_attr<128, false, true>();
-    set_smem_attr<128, true, false>();
-    set_smem_attr<128, true, true>();
     if (cudaGetLastError() != cudaSuccess) return false;
     g_state = 1;
     return true;
@@ -629,7 +152,7 @@ bool gemm_tc_available() {
 
 int gemm_tc_binary_version() {
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, k_gemm_tc<256, false, false>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&a, k_splitk_reduce) != cudaSuccess) {
         cudaGetLastError();
         return -1;
     }
@@ -728,16 +251,16 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     tp.num_tiles = (int)(tiles * tp.splits);
     const bool am = !d.a_kmajor, bm = !d.b_kmajor;
     cudaError_t e;
-    if (BN == 256) {
-        if (!am && !bm) e = launch<256, false, false>(d, tp, s);
-        else if (!am && bm) e = launch<256, false, true>(d, tp, s);
-        else if (am && !bm) e = launch<256, true, false>(d, tp, s);
-        else e = launch<256, true, true>(d, tp, s);
-    } else {
-        if (!am && !bm) e = launch<128, false, false>(d, tp, s);
-        else if (!am && bm) e = launch<128, false, true>(d, tp, s);
-        else if (am && !bm) e = launch<128, true, false>(d, tp, s);
-        else e = launch<128, true, true>(d, tp, s);
+    switch (tp.epi) {  // one kernel per epilogue mode
+        case EPI_STORE: e = launch_epi<EPI_STORE>(BN, am, bm, d, tp, s); break;
+        case EPI_RESID: e = launch_epi<EPI_RESID>(BN, am, bm, d, tp, s); break;
+        case EPI_GELU: e = launch_epi<EPI_GELU>(BN, am, bm, d, tp, s); break;
+        case EPI_GELU_D: e = launch_epi<EPI_GELU_D>(BN, am, bm, d, tp, s); break;
+        case EPI_GELU_BWD: e = launch_epi<EPI_GELU_BWD>(BN, am, bm, d, tp, s); break;
+        case EPI_MUL_AUX: e = launch_epi<EPI_MUL_AUX>(BN, am, bm, d, tp, s); break;
+        case EPI_ACCUM_F32: e = launch_epi<EPI_ACCUM_F32>(BN, am, bm, d, tp, s); break;
+        case EPI_PART_F32: e = launch_epi<EPI_PART_F32>(BN, am, bm, d, tp, s); break;
+        default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
     if (nlaunch) *nlaunch = 1;

@@ -1333,10 +1333,17 @@ __global__ void k_emb_blockprefix(int* blkcnt, int* cnt, int nb, int Vp) {
     int v = blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= Vp) return;
     int run = 0;
-    for (int b = 0; b < nb; b++) {
-        int c = blkcnt[(size_t)b * Vp + v];
-        blkcnt[(size_t)b * Vp + v] = run;
-        run += c;
+    // 16 block counts at a time: independent loads in flight together, then
+    // the prefix over them in block order
+    for (int b0 = 0; b0 < nb; b0 += 16) {
+        int c[16];
+#pragma unroll
+        for (int k = 0; k < 16; k++) c[k] = b0 + k < nb ? blkcnt[(size_t)(b0 + k) * Vp + v] : 0;
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+            if (b0 + k < nb) blkcnt[(size_t)(b0 + k) * Vp + v] = run;
+            run += c[k];
+        }
     }
     cnt[v] = run;
 }
@@ -1354,13 +1361,21 @@ __global__ void __launch_bounds__(1024) k_emb_scan(const int* cnt, int* start, i
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     if (t < 3) carry[t] = 0;
     __syncthreads();
+    // the next tile's counts are loaded while this tile is scanned
+    int nx[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) nx[k] = 4 * t + k < Vp ? cnt[4 * t + k] : 0;
     for (int base = 0; base < Vp; base += 4096) {
         int n[4], ch[4];
         int own[3] = {0, 0, 0};
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            const int v = base + 4 * t + k;
-            n[k] = v < Vp ? cnt[v] : 0;
+            n[k] = nx[k];
+            const int vn = base + 4096 + 4 * t + k;
+            nx[k] = vn < Vp ? cnt[vn] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
             ch[k] = (n[k] + EMB_R - 1) / EMB_R;
             own[0] += n[k];
             own[1] += ch[k];
