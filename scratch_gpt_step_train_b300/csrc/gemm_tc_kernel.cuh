@@ -55,11 +55,15 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
 constexpr int NUM_THREADS = 320;  // producer, MMA, 8 epilogue warps
 
+// BN = 256 tiles run on CTA pairs (tcgen05 cta_group::2): the pair computes a
+// 256 x 256 tile, each CTA holding 128 rows of A and 128 rows (of N) of B, so
+// a stage is 32 KB per CTA and six fit; BN = 128 tiles run on single CTAs.
 template <int BN>
 struct Cfg {
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr bool PAIR = BN == 256;
+    static constexpr int STAGES = 6;
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STG_BYTES = 8 * 4096;  // epilogue staging: 4 KB per epilogue warp
     static constexpr int BAR_BYTES = 256;
@@ -188,6 +192,55 @@ struct EpiMaps {
     CUtensorMap part; // fp32 [splits,M,N] box 32x32x1 SW128 (split-K partials)
 };
 
+// ------------------------------------------------------- CTA-pair helpers
+// (tcgen05 cta_group::2: the pair's MMAs are issued by the leader, rank 0;
+// every load and every signal goes to one CTA's own barrier -- no multicast)
+__device__ __forceinline__ uint32_t pair_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// the address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t pair_mapa(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void pair_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+// TMA 2-D load into this CTA's shared memory whose completion is counted on
+// the mbarrier at cluster address `bar` (the leader's)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+// arrive (once the pair's MMAs issued so far complete) on the mbarrier at
+// cluster address `bar`
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
+}
+
 // Row-wise operand of a chunk that comes from global memory (the residual for
 // EPI_RESID, the pre-activation for EPI_GELU_BWD): 32 bf16 of this lane's row,
 // loaded one chunk ahead so the load latency hides behind the previous chunk.
@@ -292,8 +345,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const __grid_constant__ EpiMaps maps, TcParams p) {
     using CF = Cfg<BN>;
+    constexpr bool PAIR = CF::PAIR;
     constexpr int S = CF::STAGES;
-    constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC = make_idesc(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t tiles = (raw + 1023u) & ~1023u;
@@ -313,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(tfull + 8 * b, 1);
-            mbar_init(tempty + 8 * b, 8);
+            mbar_init(tempty + 8 * b, PAIR ? 16 : 8);  // both CTAs' epilogue warps
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -321,21 +375,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&mapB) : "memory");
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 2 * BN);
-        tmem_relinquish();
+        // a pair allocates together: one warp of each CTA
+        if (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(2 * BN)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+            tmem_relinquish();
+        }
         tc_fence_before();
     }
     __syncthreads();
+    if (PAIR) pair_sync();  // the peer's barriers exist before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     gdc_wait();  // setup above touches no global memory
     gdc_launch_dependents();
-    // work units: output tiles (times K splits), strided over the CTAs
-    const int units_m = p.tiles_m;
+    // work units: output tiles (times K splits), strided over the CTAs; a pair
+    // takes two vertically adjacent 128-row tiles, rank r the rows 128 r ..
+    const uint32_t rank = PAIR ? pair_rank() : 0u;
+    const bool leader = rank == 0;
+    const int units_m = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
     const int units_mn = units_m * p.tiles_n;
     const int num_units = units_mn * p.splits;
-    const int unit0 = (int)blockIdx.x;
-    const int ustep = (int)gridDim.x;
+    const int unit0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int ustep = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -348,10 +415,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int split = u / units_mn, r = u % units_mn;
                 const int um = p.n_fastest ? r / p.tiles_n : r % units_m;
                 const int tn = p.n_fastest ? r % p.tiles_n : r / units_m;
-                const int tm = um;
+                const int tm = PAIR ? 2 * um + (int)rank : um;
                 const int k0 = split * p.k_per_split;
                 const int k1 = min(p.K, k0 + p.k_per_split);
                 const int nkb = (k1 - k0 + BK - 1) / BK;
+                // a pair CTA loads its own rows of A and its half (of N) of B
+                const int bn0 = tn * BN + (PAIR ? (int)rank * (BN / 2) : 0);
                 for (int kb = 0; kb < nkb; kb++) {
                     if (!mbar_wait(empty + 8 * s, ph ^ 1u, abort_flag, p.err)) {
                         ok = false;
@@ -359,20 +428,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const uint32_t sa = tiles + s * CF::STAGE_BYTES, sb = sa + CF::A_BYTES;
                     const uint32_t fb = full + 8 * s;
-                    mbar_expect_tx(fb, CF::STAGE_BYTES);
                     const int kk = k0 + kb * BK;
-                    if (!A_MN) {
-                        tma_load_2d(sa, &mapA, fb, kk, tm * BM);
-                    } else {
-                        tma_load_2d(sa, &mapA, fb, tm * BM, kk);
-                        tma_load_2d(sa + 8192, &mapA, fb, tm * BM + 64, kk);
-                    }
-                    if (!B_MN) {
-                        tma_load_2d(sb, &mapB, fb, kk, tn * BN);
-                    } else {
+                    if (PAIR) {
+                        // both CTAs' bytes are counted on the leader's barrier
+                        if (leader) mbar_expect_tx(fb, 2 * CF::STAGE_BYTES);
+                        const uint32_t fl = pair_mapa(fb, 0);
+                        if (!A_MN) {
+                            tma_load_2d_pair(sa, &mapA, fl, kk, tm * BM);
+                        } else {
+                            tma_load_2d_pair(sa, &mapA, fl, tm * BM, kk);
+                            tma_load_2d_pair(sa + 8192, &mapA, fl, tm * BM + 64, kk);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d_pair(sb, &mapB, fl, kk, bn0);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; j++)
-                            tma_load_2d(sb + j * 8192, &mapB, fb, tn * BN + 64 * j, kk);
+                            for (int j = 0; j < BN / 128; j++)
+                                tma_load_2d_pair(sb + j * 8192, &mapB, fl, bn0 + 64 * j, kk);
+                        }
+                    } else {
+                        mbar_expect_tx(fb, CF::STAGE_BYTES);
+                        if (!A_MN) {
+                            tma_load_2d(sa, &mapA, fb, kk, tm * BM);
+                        } else {
+                            tma_load_2d(sa, &mapA, fb, tm * BM, kk);
+                            tma_load_2d(sa + 8192, &mapA, fb, tm * BM + 64, kk);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d(sb, &mapB, fb, kk, bn0);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BN / 64; j++)
+                                tma_load_2d(sb + j * 8192, &mapB, fb, bn0 + 64 * j, kk);
+                        }
                     }
                     issued |= 1u << s;
                     if (++s == S) {
@@ -381,9 +469,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 // drain: wait (bounded, ignoring the abort flag) for every
-                // stage's most recent load so no copy lands after exit
+                // stage's most recent load so no copy lands after exit (a
+                // pair's loads all complete on the leader's barriers; the
+                // pair synchronises before either CTA exits)
                 for (int i = 0; i < S; i++) {
                     if (!((issued >> i) & 1u)) continue;
                     // the last issue of stage i used parity (ph if i < s else ph^1)
@@ -395,8 +485,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // --------------------------------------------------------- MMA
+            // (a pair's products are issued by its leader: M = 256, each CTA's
+            // TMEM receiving its 128 rows)
             int s = 0;
             uint32_t ph = 0;
             int lt = 0;
@@ -427,18 +519,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t ad0 = dA0 + (uint64_t)((s * CF::STAGE_BYTES) >> 4);
                     const uint64_t bd0 = dB0 + (uint64_t)((s * CF::STAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; k++)
-                        umma_bf16(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
-                                  bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
-                                  (kb > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(empty + 8 * s);
+                    for (int k = 0; k < BK / 16; k++) {
+                        if (PAIR)
+                            umma_bf16_pair(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
+                                           bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
+                                           (kb > 0 || k > 0) ? 1u : 0u);
+                        else
+                            umma_bf16(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
+                                      bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
+                                      (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    if (PAIR) {  // the stage is free in both CTAs
+                        umma_commit_pair(pair_mapa(empty + 8 * s, 0));
+                        umma_commit_pair(pair_mapa(empty + 8 * s, 1));
+                    } else {
+                        umma_commit(empty + 8 * s);
+                    }
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull + 8 * b);
+                if (PAIR) {  // the accumulator is ready in both CTAs
+                    umma_commit_pair(pair_mapa(tfull + 8 * b, 0));
+                    umma_commit_pair(pair_mapa(tfull + 8 * b, 1));
+                } else {
+                    umma_commit(tfull + 8 * b);
+                }
             }
         }
     } else {
@@ -454,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int split = u / units_mn, r = u % units_mn;
             const int um = p.n_fastest ? r / p.tiles_n : r % units_m;
             const int tn = p.n_fastest ? r % p.tiles_n : r / units_m;
-            const int tm = um;
+            const int tm = PAIR ? 2 * um + (int)rank : um;
             const int b = lt & 1;
             const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
             const int row = tm * BM + q * 32 + lane;
@@ -489,16 +597,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty + 8 * b);
+            if (lane == 0) {  // the accumulator buffer is free (on the leader's barrier)
+                if (PAIR && !leader) mbar_arrive_cluster(pair_mapa(tempty + 8 * b, 0));
+                else mbar_arrive(tempty + 8 * b);
+            }
         }
         if (lane == 0) bulk_wait0();  // all bulk stores of this warp complete
         __syncwarp();
     }
     __syncthreads();
+    // a pair: no signal of either CTA may target a CTA that has exited, and
+    // the pair deallocates its TMEM together
+    if (PAIR) pair_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, 2 * BN);
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(2 * BN)
+                         : "memory");
+        else
+            tmem_dealloc(tmem_base, 2 * BN);
     }
 }
 
@@ -529,13 +648,58 @@ cudaError_t launch_one(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     // A: K-major -> [M rows][K], box 64(K) x 128(M);  MN-major -> [K rows][M], box 64(M) x 64(K)
     bool ok = AM ? make_map(&ma, d.A, d.M, d.K, d.lda, 64)
                  : make_map(&ma, d.A, d.K, d.M, d.lda, BM);
-    // B: K-major box 64(K) x BN rows;  N-major box 64(N) x 64(K)
+    // B: K-major box 64(K) x BN rows (a pair CTA: its BN/2);  N-major box 64(N) x 64(K)
+    constexpr bool PAIR = Cfg<BN>::PAIR;
     ok = ok && (BMN ? make_map(&mb, d.B, d.N, d.K, d.ldb, 64)
-                    : make_map(&mb, d.B, d.K, d.N, d.ldb, BN));
+                    : make_map(&mb, d.B, d.K, d.N, d.ldb, PAIR ? BN / 2 : BN));
     if (!ok) return cudaErrorInvalidValue;
-    const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
-    launch_pdl(k_gemm_tc<BN, AM, BMN, EPI>, grid, NUM_THREADS, Cfg<BN>::SMEM, s, ma, mb, em, tp);
-    return cudaGetLastError();
+    if (!PAIR) {
+        const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
+        launch_pdl(k_gemm_tc<BN, AM, BMN, EPI>, grid, NUM_THREADS, Cfg<BN>::SMEM, s, ma, mb, em, tp);
+        return cudaGetLastError();
+    }
+    // CTA pairs: clusters of 2, as many as can be resident at once
+    static int resident = 0;
+    if (resident == 0) {
+        cudaLaunchConfig_t oc;
+        memset(&oc, 0, sizeof oc);
+        oc.gridDim = dim3(g_num_sms);
+        oc.blockDim = dim3(NUM_THREADS);
+        oc.dynamicSmemBytes = Cfg<BN>::SMEM;
+        cudaLaunchAttribute ca[1];
+        ca[0].id = cudaLaunchAttributeClusterDimension;
+        ca[0].val.clusterDim.x = 2;
+        ca[0].val.clusterDim.y = 1;
+        ca[0].val.clusterDim.z = 1;
+        oc.attrs = ca;
+        oc.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<BN, AM, BMN, EPI>, &oc) != cudaSuccess ||
+            n < 1) {
+            cudaGetLastError();
+            n = g_num_sms / 2;
+        }
+        resident = n < g_num_sms / 2 ? n : g_num_sms / 2;
+    }
+    const int units = ((tp.tiles_m + 1) / 2) * tp.tiles_n * tp.splits;
+    int pairs = resident;
+    if (units < pairs) pairs = units;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute la[2];
+    la[0].id = cudaLaunchAttributeClusterDimension;
+    la[0].val.clusterDim.x = 2;
+    la[0].val.clusterDim.y = 1;
+    la[0].val.clusterDim.z = 1;
+    la[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, AM, BMN, EPI>, ma, mb, em, tp);
 }
 
 // the launch for epilogue mode EPI, tile width bn and operand layouts am, bm
