@@ -397,9 +397,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rl-steps", type=int, default=3,
                     help="steps of the roofline pass (events around the dominant class)")
-    ap.add_argument("--secondary", default="1558M",
-                    help="a second workload timed after the first (1-GPU runs; '' for none)")
-    ap.add_argument("--secondary-steps", type=int, default=3)
+    ap.add_argument("--secondary", default="1558M:3,350M:30",
+                    help="workloads timed after the first, NAME[:STEPS] separated by commas "
+                         "(1-GPU runs; '' for none): the first is reported as `secondary`, "
+                         "the others as `secondary_NAME`")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -439,17 +440,33 @@ def main():
         torch.distributed.init_process_group("nccl")
     line = workload_line(args.workload, w, args.steps, args.warmup, args.accum, args.rl_steps,
                          rank, world, peaks, peak_kind)
-    if world == 1 and args.secondary and args.workload != args.secondary:
-        w2 = WORKLOADS[args.secondary]
-        sec = workload_line(args.secondary, w2, args.secondary_steps, 3, 0, 1, rank, world,
-                            peaks, peak_kind)
-        line["secondary"] = {k: sec[k] for k in (
-            "value", "unit", "ms_per_step", "steps", "warmup", "config", "bf16_mfu", "roofline",
-            "e2e", "gpu_launches", "clocks", "final_loss", "memory_bound")}
+    if world == 1:
+        first = True
+        for name, steps in parse_secondary(args.secondary):
+            if name == args.workload:
+                continue
+            sec = workload_line(name, WORKLOADS[name], steps, 3, 0, 1, rank, world, peaks,
+                                peak_kind)
+            line["secondary" if first else "secondary_" + name] = {k: sec[k] for k in (
+                "value", "unit", "ms_per_step", "steps", "warmup", "config", "bf16_mfu",
+                "roofline", "e2e", "gpu_launches", "clocks", "final_loss", "memory_bound")}
+            first = False
     if rank != 0:
         return
     line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
+
+
+def parse_secondary(spec):
+    """'1558M:3,350M:30' -> [('1558M', 3), ('350M', 30)]; a name without a
+    step count gets 3 timed steps"""
+    out = []
+    for item in filter(None, (x.strip() for x in (spec or "").split(","))):
+        name, _, steps = item.partition(":")
+        if name not in WORKLOADS:
+            raise SystemExit(f"unknown workload {name!r} in --secondary")
+        out.append((name, int(steps) if steps else 3))
+    return out
 
 
 def workload_line(name, w, steps, warmup, accum_override, rl_steps, rank, world, peaks,

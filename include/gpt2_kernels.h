@@ -109,7 +109,10 @@ int gpt2k_layernorm_backward_noalloc(int dtype, void* dx, float* dw, float* db,
 
 /* Token + position embedding: out[b,t,:] = wte[tok[b,t],:] + wpe[t,:].
  * Backward ACCUMULATES dwte[tok[b,t],:] += dx[b,t,:] (each row's sum taken
- * in position order, no atomics) and dwpe[t,:] += sum_b dx[b,t,:]. */
+ * in position order, no atomics) and dwpe[t,:] += sum_b dx[b,t,:].  Vp (the
+ * rows of dwte) must be a multiple of 4, else GPT2_ERR_ARG; scratch holds
+ * gpt2k_encoder_backward_scratch_bytes(B, T, C, Vp) bytes, owned by the
+ * caller, not read before it is written. */
 int gpt2k_encoder_forward(int dtype, void* out, const int32_t* tok, const void* wte,
                           const void* wpe, int B, int T, int C, int V, unsigned* err,
                           void* stream);

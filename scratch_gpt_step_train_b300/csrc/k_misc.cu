@@ -719,7 +719,9 @@ static cudaError_t ln_bwd_ring_launch(bf16* dx, float* part, const bf16* dout, c
     constexpr size_t smem = (size_t)8 * 2 * 3 * IT * 32 * 16;
     static_assert(smem >= (size_t)8 * NACC * IT * 256 * 4, "fold does not fit the ring");
     auto kern = k_ln_bwd_ring<IT, NACC, RS>;
-    if (smem > 48 * 1024) {
+    // the opt-in always: with the kernel's static shared memory, a ring of
+    // exactly 48 KB (C = 1024 with the dxsum column) is already over the default
+    {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -757,7 +759,7 @@ static cudaError_t ln_bwd_launch(T* dx, float* part, const T* dout, const T* x, 
     constexpr size_t smem = (size_t)W * NACC * S * sizeof(float);
     static_assert(smem <= 227 * 1024, "LayerNorm backward slices exceed shared memory");
     auto kern = k_ln_bwd<T, VEC, IT, NACC>;
-    if (smem > 48 * 1024) {
+    {  // the opt-in always (dynamic plus static shared memory may pass 48 KB)
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -1216,8 +1218,9 @@ cudaError_t mean_reduce(float* out, const float* x, int n, cudaStream_t s) {
 //     shared memory (bitonic), giving each position its rank among equal
 //     tokens of the block and the block's count per token.
 //  2. k_emb_blockprefix: per token, exclusive prefix of the block counts.
-//  3. k_emb_scan: one block scans the per-token totals -> bucket starts, and
-//     the chunk counts (buckets split in chunks of EMB_R rows).
+//  3. k_emb_scan: exclusive scans of the per-token totals -> bucket starts,
+//     and of the chunk counts (buckets split in chunks of EMB_R rows); the
+//     list of tokens with more than one chunk.
 //  4. k_emb_place: stable placement -> positions sorted by (token, position).
 //  5. k_emb_items: list the (token, chunk) work items.
 //  6. k_emb_reduce: one warp per item sums its <= EMB_R rows in position
@@ -1238,7 +1241,8 @@ struct EmbScratch {
     int* sorted;   // [BT]
     int2* items;   // [max_items]
     float* part;   // [max_part][C]
-    int nb, max_items, max_part;
+    int* mlist;    // [1 + max_multi]: the count of tokens with more than one chunk, then they
+    int nb, max_items, max_part, max_multi;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1248,6 +1252,7 @@ static EmbScratch emb_carve(void* base, int BT, int C, int Vp, size_t* total) {
     e.nb = cdiv(BT, EMB_BLK);
     e.max_items = cdiv(BT, EMB_R) + (BT < Vp ? BT : Vp);
     e.max_part = 2 * cdiv(BT, EMB_R) + 1;
+    e.max_multi = cdiv(BT, EMB_R + 1);  // a multi-chunk token holds > EMB_R positions
     char* p = (char*)base;
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -1264,6 +1269,7 @@ static EmbScratch emb_carve(void* base, int BT, int C, int Vp, size_t* total) {
     e.sorted = (int*)take((size_t)BT * 4);
     e.items = (int2*)take((size_t)e.max_items * 8);
     e.part = (float*)take((size_t)e.max_part * C * 4);
+    e.mlist = (int*)take((size_t)(e.max_multi + 1) * 4);
     if (total) *total = o;
     return e;
 }
@@ -1348,87 +1354,103 @@ __global__ void k_emb_blockprefix(int* blkcnt, int* cnt, int nb, int Vp) {
     cnt[v] = run;
 }
 
-// One block of 1024 threads: exclusive scans of n_v, chunks_v, multi-chunk
-// chunks_v over v in [0, Vp), in tiles of 4096 consecutive v (coalesced: thread
-// t takes v = tile + 4t .. 4t+3), each tile a warp-shuffle block scan plus the
-// running total of the tiles before it.
+// Exclusive scans over v in [0, Vp) of n_v (bucket starts), chunks_v (work
+// item offsets), chunks_v of the multi-chunk tokens (partial-row offsets) and
+// [chunks_v > 1] (their place in mlist).  Block b scans v in [1024 b, 1024 b +
+// 1024) after summing every count below its range itself (at most Vp ints,
+// read as int4 from L2), so the blocks need no communication and the result
+// does not depend on their order.  Vp is a multiple of 4.
 __global__ void __launch_bounds__(1024) k_emb_scan(const int* cnt, int* start, int* itemoff,
-                                                   int* poff, int Vp) {
+                                                   int* poff, int* mlist, int Vp) {
     gdc_wait();
     gdc_launch_dependents();
-    __shared__ int wsum[3][32];
-    __shared__ int carry[3];
+    constexpr int Q = 4;
+    __shared__ int wpre[Q][32], wloc[Q][32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    if (t < 3) carry[t] = 0;
-    __syncthreads();
-    // the next tile's counts are loaded while this tile is scanned
-    int nx[4];
-#pragma unroll
-    for (int k = 0; k < 4; k++) nx[k] = 4 * t + k < Vp ? cnt[4 * t + k] : 0;
-    for (int base = 0; base < Vp; base += 4096) {
-        int n[4], ch[4];
-        int own[3] = {0, 0, 0};
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            n[k] = nx[k];
-            const int vn = base + 4096 + 4 * t + k;
-            nx[k] = vn < Vp ? cnt[vn] : 0;
-        }
+    const int base = blockIdx.x * 1024;
+    auto terms = [](int n, int* q) {
+        const int ch = (n + EMB_R - 1) / EMB_R;
+        q[0] = n;
+        q[1] = ch;
+        q[2] = ch > 1 ? ch : 0;
+        q[3] = ch > 1 ? 1 : 0;
+    };
+    // 1. this thread's share of the sums below `base` (v, v+1, v+2, v+3 < base
+    //    whenever v < base: both are multiples of 4)
+    int pre[Q] = {0, 0, 0, 0};
+    for (int v0 = 0; v0 < base; v0 += 4 * 4096) {
+        int4 c[4];
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            ch[k] = (n[k] + EMB_R - 1) / EMB_R;
-            own[0] += n[k];
-            own[1] += ch[k];
-            own[2] += ch[k] > 1 ? ch[k] : 0;
+            const int v = v0 + 4096 * k + 4 * t;
+            c[k] = v < base ? *reinterpret_cast<const int4*>(cnt + v) : make_int4(0, 0, 0, 0);
         }
-        int inc[3] = {own[0], own[1], own[2]};
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-#pragma unroll
-            for (int q = 0; q < 3; q++) {
-                const int y = __shfl_up_sync(0xffffffffu, inc[q], off);
-                if (lane >= off) inc[q] += y;
-            }
-        }
-        if (lane == 31) {
-#pragma unroll
-            for (int q = 0; q < 3; q++) wsum[q][warp] = inc[q];
-        }
-        __syncthreads();
-        if (warp == 0) {
-#pragma unroll
-            for (int q = 0; q < 3; q++) {
-                int x = wsum[q][lane];
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, x, off);
-                    if (lane >= off) x += y;
-                }
-                wsum[q][lane] = x;  // inclusive over warps
-            }
-        }
-        __syncthreads();
-        int pre[3];
-#pragma unroll
-        for (int q = 0; q < 3; q++)
-            pre[q] = carry[q] + (warp ? wsum[q][warp - 1] : 0) + inc[q] - own[q];
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            const int v = base + 4 * t + k;
-            if (v < Vp) {
-                start[v] = pre[0];
-                itemoff[v] = pre[1];
-                poff[v] = pre[2];
+            const int n4[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                int q[Q];
+                terms(n4[j], q);
+#pragma unroll
+                for (int i = 0; i < Q; i++) pre[i] += q[i];
             }
-            pre[0] += n[k];
-            pre[1] += ch[k];
-            pre[2] += ch[k] > 1 ? ch[k] : 0;
         }
-        __syncthreads();  // every thread has read carry and wsum
-        if (t < 3) carry[t] += wsum[t][31];
-        __syncthreads();
     }
-    if (t < 3) (t == 0 ? start : (t == 1 ? itemoff : poff))[Vp] = carry[t];
+    // 2. this block's own range: one token per thread
+    const int v = base + t;
+    int own[Q];
+    terms(v < Vp ? cnt[v] : 0, own);
+    int inc[Q];
+#pragma unroll
+    for (int i = 0; i < Q; i++) inc[i] = own[i];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+        for (int i = 0; i < Q; i++) {
+            const int y = __shfl_up_sync(0xffffffffu, inc[i], off);
+            if (lane >= off) inc[i] += y;
+            pre[i] += __shfl_xor_sync(0xffffffffu, pre[i], off);
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int i = 0; i < Q; i++) {
+            wloc[i][warp] = inc[i];
+            wpre[i][warp] = pre[i];
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < Q; i++) {
+            int x = wloc[i][lane], y = wpre[i][lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += u;
+                y += __shfl_xor_sync(0xffffffffu, y, off);
+            }
+            wloc[i][lane] = x;  // inclusive over the warps
+            wpre[i][lane] = y;  // every lane: the block's total below `base`
+        }
+    }
+    __syncthreads();
+    int ex[Q];
+#pragma unroll
+    for (int i = 0; i < Q; i++) ex[i] = wpre[i][0] + (warp ? wloc[i][warp - 1] : 0) + inc[i] - own[i];
+    if (v < Vp) {
+        start[v] = ex[0];
+        itemoff[v] = ex[1];
+        poff[v] = ex[2];
+        if (own[3]) mlist[1 + ex[3]] = v;
+    }
+    if (base + 1024 >= Vp && t == 0) {
+        start[Vp] = wpre[0][0] + wloc[0][31];
+        itemoff[Vp] = wpre[1][0] + wloc[1][31];
+        poff[Vp] = wpre[2][0] + wloc[2][31];
+        mlist[0] = wpre[3][0] + wloc[3][31];
+    }
 }
 
 __global__ void k_emb_place(const int* tok, int BT, int Vp, const int* start, const int* blkcnt,
@@ -1500,17 +1522,14 @@ __global__ void k_emb_reduce2(float* dwte, float* part, const T* dx, const int* 
     }
 }
 
+// one block per multi-chunk token: dwte[v] += its partial rows in chunk order
 __global__ void k_emb_fold(float* dwte, const float* part, const int* cnt, const int* poff,
-                           const int* n_items, const int2* items, int C) {
+                           const int* mlist, int C) {
     gdc_wait();
     gdc_launch_dependents();
-    int item = blockIdx.x;
-    if (item >= *n_items) return;
-    int2 vc = items[item];
-    if (vc.y != 0) return;
-    int v = vc.x, n = cnt[v];
-    if (n <= EMB_R) return;
-    int ch = (n + EMB_R - 1) / EMB_R;
+    if ((int)blockIdx.x >= mlist[0]) return;
+    const int v = mlist[1 + blockIdx.x], n = cnt[v];
+    const int ch = (n + EMB_R - 1) / EMB_R;
     const float* p = part + (size_t)poff[v] * C;
     for (int col = threadIdx.x; col < C; col += blockDim.x) {
         float a = 0.f;
@@ -1548,7 +1567,9 @@ static cudaError_t emb_bwd_vec(float* dwte, float* dwpe, const void* dx, const i
     cudaMemsetAsync(e.blkcnt, 0, (size_t)e.nb * Vp * 4, s);
     launch_pdl(k_emb_rank, e.nb, EMB_BLK, 0, s, tok, BT, Vp, e.lrank, e.blkcnt);
     launch_pdl(k_emb_blockprefix, cdiv(Vp, 256), 256, 0, s, e.blkcnt, e.cnt, e.nb, Vp);
-    launch_pdl(k_emb_scan, 1, 1024, 0, s, e.cnt, e.start, e.itemoff, e.poff, Vp);
+    if (Vp % 4) return cudaErrorInvalidValue;
+    launch_pdl(k_emb_scan, cdiv(Vp, 1024), 1024, 0, s, e.cnt, e.start, e.itemoff, e.poff, e.mlist,
+               Vp);
     launch_pdl(k_emb_place, cdiv(BT, 256), 256, 0, s, tok, BT, Vp, e.start, e.blkcnt, e.lrank, e.sorted);
     launch_pdl(k_emb_items, cdiv(Vp, 256), 256, 0, s, e.cnt, e.itemoff, e.items, Vp);
     int it = cdiv(C, 32 * VEC);
@@ -1564,7 +1585,7 @@ static cudaError_t emb_bwd_vec(float* dwte, float* dwpe, const void* dx, const i
     else if (it <= 16) EMR(16);
     else return cudaErrorInvalidValue;
 #undef EMR
-    launch_pdl(k_emb_fold, e.max_items, 256, 0, s, dwte, e.part, e.cnt, e.poff, n_items, e.items, C);
+    launch_pdl(k_emb_fold, e.max_multi, 256, 0, s, dwte, e.part, e.cnt, e.poff, e.mlist, C);
     launch_pdl(k_wpe_bwd<T, VEC>, cdiv((long)T_ * (C / VEC), 256), 256, 0, s, dwpe, (const T*)dx, B, T_,
                                                                        C);
     return cudaGetLastError();

@@ -74,14 +74,19 @@ def test_attention_forward_fp32(B, T, C, H):
     assert np.abs(lse.double().cpu().numpy() - _lse_ref(q64, att, C, H)).max() < 1e-4
 
 
-@pytest.mark.parametrize("C,H", [(768, 12), (1600, 25)], ids=["124M", "1558M"])
-def test_attention_forward_full_size_sampled(C, H):
-    """GPT-2 124M and 1558M widths at micro-batch 16 x 1024: the oracle
-    recomputes one sequence (every head)"""
-    B, T = 16, 1024
+# GPT-2 widths at the micro-batch each is trained with: (C, H, B), T = 1024
+FULL_WIDTHS = [(768, 12, 16), (1600, 25, 16), (1024, 16, 8)]
+FULL_IDS = ["124M", "1558M", "350M"]
+
+
+@pytest.mark.parametrize("C,H,B", FULL_WIDTHS, ids=FULL_IDS)
+def test_attention_forward_full_size_sampled(C, H, B):
+    """GPT-2 124M, 350M and 1558M widths at their micro-batches x 1024: the
+    oracle recomputes one sequence (every head)"""
+    T = 1024
     qkv, _ = _qkv(B, T, C, 3)
     out, lse = _fwd(qkv, B, T, C, H)
-    b = 9
+    b = 9 % B
     q64 = qkv[b:b + 1].double().cpu().numpy()
     ref, att = ops.attention_forward(q64, H)
     a = q64.copy()
@@ -176,17 +181,18 @@ def test_attention_backward_fp32(B, T, C, H):
     assert_close(dqkv.double().cpu().numpy(), ref, 1e-4, "dqkv")
 
 
-@pytest.mark.parametrize("C,H", [(768, 12), (1600, 25)], ids=["124M", "1558M"])
-def test_attention_backward_full_size_sampled(C, H):
-    """micro-batch 16 x 1024 at the 124M and 1558M widths; the oracle
-    recomputes one sequence (every head), each element against the bound"""
-    B, T = 16, 1024
+@pytest.mark.parametrize("C,H,B", FULL_WIDTHS, ids=FULL_IDS)
+def test_attention_backward_full_size_sampled(C, H, B):
+    """the 124M, 350M and 1558M widths at their micro-batches x 1024; the
+    oracle recomputes one sequence (every head), each element against the
+    bound"""
+    T = 1024
     qkv, _ = _qkv(B, T, C, 8)
     out, lse = _fwd(qkv, B, T, C, H)
     dout = (torch.randn(B, T, C, generator=torch.Generator(device="cuda").manual_seed(9),
                         device="cuda")).to(torch.bfloat16)
     dqkv = _bwd(qkv, dout, out, lse, B, T, C, H)
-    b = 13
+    b = 13 % B
     q64 = qkv[b:b + 1].double().cpu().numpy()
     d64 = dout[b:b + 1].double().cpu().numpy()
     _, att = ops.attention_forward(q64, H)

@@ -94,3 +94,12 @@ def test_cpu_baselines_skip_a_sample_the_host_cannot_hold(monkeypatch):
     assert cb["kind"] == "oracle" and cb["value"] == 100.0 and cb["cores"] == 8
     assert [("skipped" in r) for r in cb["runs"]] == [False, False, True]
     assert cb["runs"][1]["cores"] == 1
+
+
+def test_secondary_workload_list():
+    b = _bench()
+    assert b.parse_secondary("1558M:3,350M:30") == [("1558M", 3), ("350M", 30)]
+    assert b.parse_secondary("350M") == [("350M", 3)]
+    assert b.parse_secondary("") == [] and b.parse_secondary(None) == []
+    with pytest.raises(SystemExit):
+        b.parse_secondary("7B:1")

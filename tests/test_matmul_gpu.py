@@ -199,8 +199,29 @@ FULL_1558M = [
     ("fcproj_dw", 1600, 6400, 16384, False, False, "accum_f32"),
     ("classifier_dw", 50304, 1600, 16384, False, False, "accum_f32"),
 ]
-ALL_FULL = [("124M-" + f[0],) + f[1:] for f in FULL] + [("1558M-" + f[0],) + f[1:]
-                                                       for f in FULL_1558M]
+
+# The same products at the GPT-2 350M width (C=1024, 3C=3072, 4C=4096) at
+# micro-batch 8 x 1024 (M = 8192 rows).
+FULL_350M = [
+    ("qkv_fwd", 8192, 3072, 1024, True, True, "store"),
+    ("proj_fwd", 8192, 1024, 1024, True, True, "resid"),
+    ("fc_fwd_gelu_d", 8192, 4096, 1024, True, True, "gelu_d"),
+    ("fcproj_fwd", 8192, 1024, 4096, True, True, "resid"),
+    ("classifier_fwd", 8192, 50304, 1024, True, True, "store"),
+    ("qkv_dx", 8192, 1024, 3072, True, False, "store"),
+    ("proj_dx", 8192, 1024, 1024, True, False, "store"),
+    ("fc_dx", 8192, 1024, 4096, True, False, "store"),
+    ("fcproj_dx_mul_aux", 8192, 4096, 1024, True, False, "mul_aux"),
+    ("classifier_dx", 8192, 1024, 50304, True, False, "store"),
+    ("qkv_dw", 3072, 1024, 8192, False, False, "accum_f32"),
+    ("proj_dw", 1024, 1024, 8192, False, False, "accum_f32"),
+    ("fc_dw", 4096, 1024, 8192, False, False, "accum_f32"),
+    ("fcproj_dw", 1024, 4096, 8192, False, False, "accum_f32"),
+    ("classifier_dw", 50304, 1024, 8192, False, False, "accum_f32"),
+]
+ALL_FULL = ([("124M-" + f[0],) + f[1:] for f in FULL]
+            + [("1558M-" + f[0],) + f[1:] for f in FULL_1558M]
+            + [("350M-" + f[0],) + f[1:] for f in FULL_350M])
 
 
 @pytest.mark.parametrize("name,M,N,Kd,a_km,b_km,epi", ALL_FULL, ids=[f[0] for f in ALL_FULL])

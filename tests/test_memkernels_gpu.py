@@ -82,6 +82,28 @@ def test_encoder_backward_full_size_exact_indexing(dtype):
     assert np.array_equal(dwpe.cpu().numpy(), dwpe0 + rwpe)
 
 
+def test_encoder_backward_heavy_tokens_in_every_scan_block():
+    """Zipf tokens relabelled by a seeded permutation: the tokens with more
+    than one 32-row chunk lie all over [0, Vp), in every 1024-token block of
+    the bucket scan; integer-valued dx, so the sums are exact"""
+    B, T, C, V = 8, 1024, 256, 50257
+    Vp = ((V + 127) // 128) * 128
+    tok = inputs.zipf_batches(6, 1, B, T, V)[0][0]
+    perm = np.random.default_rng(7).permutation(V).astype(tok.dtype)
+    tok = perm[tok]
+    counts = np.bincount(tok.ravel(), minlength=Vp)
+    heavy = np.nonzero(counts > 32)[0]
+    assert len(np.unique(heavy // 1024)) >= 5  # the case this test is for
+    rng = np.random.default_rng(8)
+    dx = rng.integers(-4, 5, (B, T, C)).astype(np.float32)
+    dwte = torch.zeros(Vp, C, device="cuda")
+    dwpe = torch.zeros(T, C, device="cuda")
+    K.encoder_backward(dwte, dwpe, _t(dx, torch.float32), torch.from_numpy(tok).cuda())
+    rwte, rwpe = ops.encoder_backward(dx.astype(np.float64), tok, Vp)
+    assert np.array_equal(dwte.cpu().numpy(), rwte)
+    assert np.array_equal(dwpe.cpu().numpy(), rwpe)
+
+
 def test_encoder_backward_real_values_and_determinism():
     B, T, C, V = 8, 200, 64, 300
     Vp = 384
@@ -109,7 +131,8 @@ def _ln_inputs(N, C, seed):
     return x, w, b
 
 
-@pytest.mark.parametrize("N,C", [(37, 200), (16384, 768), (300, 1600)], ids=["small", "full", "c1600"])
+@pytest.mark.parametrize("N,C", [(37, 200), (16384, 768), (300, 1600), (8192, 1024)],
+                         ids=["small", "full", "c1600", "c1024"])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 def test_layernorm_forward(N, C, dtype):
     x, w, b = _ln_inputs(N, C, 1)
@@ -128,7 +151,8 @@ def test_layernorm_forward(N, C, dtype):
 
 
 @pytest.mark.parametrize("mode", ["accum", "overwrite_dxsum"])
-@pytest.mark.parametrize("N,C", [(37, 200), (16384, 768), (300, 1600)], ids=["small", "full", "c1600"])
+@pytest.mark.parametrize("N,C", [(37, 200), (16384, 768), (300, 1600), (8192, 1024)],
+                         ids=["small", "full", "c1600", "c1024"])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 def test_layernorm_backward(N, C, dtype, mode):
     x, w, b = _ln_inputs(N, C, 2)
@@ -170,7 +194,8 @@ def test_layernorm_backward(N, C, dtype, mode):
 
 # -------------------------------------------------------------- bias gradient
 
-@pytest.mark.parametrize("N,OC", [(37, 200), (16384, 2304), (16384, 3072)], ids=["small", "qkv", "fc"])
+@pytest.mark.parametrize("N,OC", [(37, 200), (16384, 2304), (16384, 3072), (8192, 3072), (8192, 4096)],
+                         ids=["small", "qkv", "fc", "qkv350M", "fc350M"])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
 def test_bias_grad(N, OC, dtype):
     rng = np.random.default_rng(4)

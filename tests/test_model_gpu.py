@@ -190,13 +190,16 @@ def test_toy_transition_table_gpu():
             assert abs(a50[s] - f) < abs(a0[s] - f) - 0.1
 
 
-# the GPT-2 1558M layer width (C=1600, 25 heads of 64, 4C=6400) and the full
-# vocabulary, two layers, one sequence of 128 tokens
-WIDE = dict(L=2, H=25, C=1600, V=50257, T=128, B=1)
+# the GPT-2 1558M layer width (C=1600, 25 heads of 64, 4C=6400) and the 350M
+# one (C=1024, 16 heads), the full vocabulary, two layers, one sequence of 128
+# tokens
+WIDTHS = {"1558M": dict(L=2, H=25, C=1600, V=50257, T=128, B=1),
+          "350M": dict(L=2, H=16, C=1024, V=50257, T=128, B=1)}
 WIDE_HP = dict(lr=6e-4, b1=0.9, b2=0.95, eps=1e-8, wd=0.1, clip=1.0)
 
 
-def test_fp32_1558M_width_two_steps():
+@pytest.mark.parametrize("width", sorted(WIDTHS))
+def test_fp32_wide_two_steps(width):
     """fp32 mode against the fp64 oracle from the same init and Zipf tokens,
     two AdamW steps: logits, loss and the norm each update saw at rel 1e-4;
     every gradient tensor at rel 1e-4 at the first step.  From the second
@@ -205,6 +208,7 @@ def test_fp32_1558M_width_two_steps():
     small the gradient, so a gradient that is rounding noise moves its weight
     by lr either way), and each gradient tensor is held to
     max(1e-4, 4 x the error of the fp32 build of the oracle run alongside)."""
+    WIDE = WIDTHS[width]
     om = Model(**WIDE, seed=1)
     o32 = Model(**WIDE, seed=1, real="float")
     gm = GPT2(**WIDE, seed=1, mode=FP32)
@@ -235,8 +239,10 @@ def test_fp32_1558M_width_two_steps():
         assert rc == 0 and abs(ng - no) <= 1e-4 * no, (step, ng, no)
 
 
-def test_bf16_1558M_width_two_steps():
-    """bf16-mixed mode at the same shape: |loss difference| <= 2e-2 per step"""
+@pytest.mark.parametrize("width", sorted(WIDTHS))
+def test_bf16_wide_two_steps(width):
+    """bf16-mixed mode at the same shapes: |loss difference| <= 2e-2 per step"""
+    WIDE = WIDTHS[width]
     om = Model(**WIDE, seed=1)
     gm = GPT2(**WIDE, seed=1, mode=BF16)
     gm.set_params(om.params())
