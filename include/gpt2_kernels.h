@@ -57,6 +57,22 @@ int gpt2k_matmul(int dtype, int impl, int M, int N, int K, const void* A, long l
                  const void* B, long ldb, int b_kmajor, void* D, long ldd, const void* bias,
                  const void* resid, long ldr, void* aux, long ldx, int epi, void* scratch,
                  size_t scratch_bytes, unsigned* err, void* stream);
+/* The MLP input gradient with the fc bias gradient of the same product (the
+ * bias gradient is the column sum of the pre-activation gradient, "Karpathy's
+ * llm.c: understanding LLM training from scratch in C/CUDA", "Code anatomy",
+ * the matmul backward): bf16 on the tensor cores, epi 6 (D = acc * aux) or
+ * epi 4 (D = acc * gelu_tanh'(aux)) as in gpt2k_matmul, and
+ *   dbias[n] += sum_m D[m,n]
+ * summed in fp32 from D's values before they are rounded to bf16, in a fixed
+ * order (32-row blocks, then the blocks in order).  dbias: N floats, device.
+ * scratch: at least ceil(M/32) * N * 4 bytes (gpt2k_matmul_scratch_bytes()
+ * covers M * N <= 512 Mi), owned by the caller and overwritten.  Returns -1
+ * for another epi, NULL pointers or a shape the tensor cores do not take
+ * (as impl 2 of gpt2k_matmul). */
+int gpt2k_matmul_bias_grad(int M, int N, int K, const void* A, long lda, int a_kmajor,
+                           const void* B, long ldb, int b_kmajor, void* D, long ldd, void* aux,
+                           long ldx, int epi, float* dbias, void* scratch, size_t scratch_bytes,
+                           unsigned* err, void* stream);
 
 /* Causal self-attention ("Getting started with LLMs from Andrej Karpathy's
  * talk", self-attention: softmax(Q K^T / sqrt(d_k)) V), query t attending to

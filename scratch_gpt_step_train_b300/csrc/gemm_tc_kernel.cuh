@@ -83,6 +83,9 @@ struct TcParams {
     bf16* aux;
     long ldx;
     float* part;
+    // EPI_MUL_AUX / EPI_GELU_BWD: column sums of each 32-row block of D (fp32,
+    // before rounding), [ceil(M/32)][N], or NULL
+    float* colpart;
     unsigned* err;
 };
 
@@ -305,6 +308,25 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
                 for (int i = 0; i < 8; i++) v[8 * k + i] += r8[i];
             }
         }
+    }
+    if ((EPI == EPI_MUL_AUX || EPI == EPI_GELU_BWD) && p.colpart) {
+        // column sums over the warp's 32 rows (lanes): a butterfly that halves
+        // the columns each lane keeps at every step, so that lane j ends with
+        // column j (a fixed order of additions); rows past M hold zeros
+        float cs[32];
+#pragma unroll
+        for (int i = 0; i < 32; i++) cs[i] = v[i];
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1) {
+            const bool up = (lane & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; i++) {
+                const float send = up ? cs[i] : cs[i + w];
+                const float keep = up ? cs[i + w] : cs[i];
+                cs[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+        }
+        if (row0 < p.M && lane < nv) p.colpart[(size_t)(row0 >> 5) * p.N + col + lane] = cs[0];
     }
     // the previous chunk's bulk stores must have finished reading the staging tile
     if (lane == 0) bulk_wait_read0();

@@ -681,6 +681,11 @@ extern "C" int gpt2_backward(gpt2_t* g) {
                g->recompute >= 1 ? EPI_GELU_BWD : EPI_MUL_AUX);
         d.aux = fch;
         d.ldx = 4 * C;
+        // the fc bias gradient (column sums of this product's output) comes
+        // out of the same kernel on the tensor cores
+        d.act = g->act;
+        const bool fused_fcb = g->use_tc && gemm_tc_supported(d);
+        if (fused_fcb) d.dbias = grad_tensor(g, P_FCB, l);
         RUN(mm(g, K_FCPROJ_DX, d));
         if (g->recompute >= 2)  // ln2(x1) again (the same kernel on the same input)
             LAUNCH(K_RECOMP, 1, 0, ln_bytes,
@@ -690,9 +695,10 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         d = gd(4 * C, C, BT, g->dbig, 4 * C, 0, ln2, C, 0, grad_tensor(g, P_FCW, l), C,
                EPI_ACCUM_F32);
         RUN(mm(g, K_FC_DW, d));
-        LAUNCH(K_BIAS, 2, 0, as * bt * 4 * c,
-               bias_grad(g->act, grad_tensor(g, P_FCB, l), g->dbig, BT, 4 * C, g->scratch,
-                         g->stream));
+        if (!fused_fcb)
+            LAUNCH(K_BIAS, 2, 0, as * bt * 4 * c,
+                   bias_grad(g->act, grad_tensor(g, P_FCB, l), g->dbig, BT, 4 * C, g->scratch,
+                             g->stream));
         d = gd(BT, C, 4 * C, g->dbig, 4 * C, 1, pc_tensor(g, P_FCW, l), C, 0, g->dln, C,
                EPI_STORE);
         RUN(mm(g, K_FC_DX, d));

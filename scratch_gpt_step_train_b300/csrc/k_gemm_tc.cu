@@ -240,7 +240,15 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     tp.resid = (const bf16*)d.resid; tp.ldr = d.ldr;
     tp.aux = (bf16*)d.aux; tp.ldx = d.ldx;
     tp.part = (float*)scratch;
+    tp.colpart = nullptr;
     tp.err = err;
+    const int row_blocks = (d.M + 31) / 32;
+    if (d.dbias) {
+        // column partial sums in scratch, then one ordered sum into dbias
+        if (d.epi != EPI_MUL_AUX && d.epi != EPI_GELU_BWD) return cudaErrorInvalidValue;
+        if (!scratch || (size_t)row_blocks * d.N * 4 > scratch_bytes) return cudaErrorInvalidValue;
+        tp.colpart = (float*)scratch;
+    }
     const long tiles = (long)tiles_m * tiles_n;
     if (splits > 1) {
         const int kbs = (kb + splits - 1) / splits;
@@ -264,6 +272,10 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     }
     if (e != cudaSuccess) return e;
     if (nlaunch) *nlaunch = 1;
+    if (tp.colpart) {
+        if (nlaunch) *nlaunch = 2;
+        return colsum_add(d.dbias, tp.colpart, row_blocks, d.N, s);
+    }
     if (tp.splits > 1) {
         if (nlaunch) *nlaunch = 2;
         long nv = (long)d.M * (d.N / 4);

@@ -708,6 +708,12 @@ __global__ void __launch_bounds__(256) k_colsum(ColsumOut outs, int n0, int ncol
     }
 }
 
+cudaError_t colsum_add(float* db, const float* part, int nparts, int ncols, cudaStream_t s) {
+    ColsumOut o{{db, nullptr, nullptr}};
+    launch_pdl(k_colsum, cdiv(ncols, 32), 256, 0, s, o, ncols, ncols, part, nparts, (long)ncols);
+    return cudaGetLastError();
+}
+
 size_t layernorm_backward_scratch(int N, int C, bool dxsum) {
     return (size_t)LNB_MAX_BLOCKS * (dxsum ? 3 : 2) * C * sizeof(float);
 }

@@ -5,6 +5,8 @@
 #include "gemm_tc.h"
 #include "kernels.h"
 
+#include <cstring>
+
 using namespace gk;
 
 static int rc_of(cudaError_t e) {
@@ -42,12 +44,35 @@ extern "C" int gpt2k_matmul(int dtype, int impl, int M, int N, int K, const void
     d.D = D; d.ldd = ldd;
     d.bias = bias; d.resid = resid; d.ldr = ldr; d.aux = aux; d.ldx = ldx;
     d.epi = epi; d.act = dtype;
+    d.dbias = nullptr;
     cudaStream_t s = (cudaStream_t)stream;
     bool tc = dtype == ACT_BF16 && gemm_tc_available() && gemm_tc_supported(d);
     if (impl == 2 && !tc) return GPT2_ERR_ARG;
     if (impl == 1 || !tc) return rc_of(gemm_simt(d, s));
     int nl;
     return rc_of(gemm_tc(d, scratch, scratch_bytes, err, s, &nl));
+}
+
+extern "C" int gpt2k_matmul_bias_grad(int M, int N, int K, const void* A, long lda,
+                                      int a_kmajor, const void* B, long ldb, int b_kmajor,
+                                      void* D, long ldd, void* aux, long ldx, int epi,
+                                      float* dbias, void* scratch, size_t scratch_bytes,
+                                      unsigned* err, void* stream) {
+    if (M < 1 || N < 1 || K < 1 || !A || !B || !D || !aux || !dbias || !scratch)
+        return GPT2_ERR_ARG;
+    if (epi != EPI_MUL_AUX && epi != EPI_GELU_BWD) return GPT2_ERR_ARG;
+    GemmDesc d;
+    memset(&d, 0, sizeof d);
+    d.M = M; d.N = N; d.K = K;
+    d.A = A; d.lda = lda; d.a_kmajor = a_kmajor;
+    d.B = B; d.ldb = ldb; d.b_kmajor = b_kmajor;
+    d.D = D; d.ldd = ldd;
+    d.aux = aux; d.ldx = ldx;
+    d.epi = epi; d.act = ACT_BF16;
+    d.dbias = dbias;
+    if (!gemm_tc_available() || !gemm_tc_supported(d)) return GPT2_ERR_ARG;
+    int nl;
+    return rc_of(gemm_tc(d, scratch, scratch_bytes, err, (cudaStream_t)stream, &nl));
 }
 
 extern "C" int gpt2k_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B,

@@ -78,6 +78,8 @@ cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, float* d
 
 // ---- bias gradient: db[o] += sum_n dout[n,o] (deterministic, two stage) ---
 size_t bias_grad_scratch(int N, int OC);
+// db[c] += sum_{i < nparts} part[i * ncols + c], rows in order (one launch)
+cudaError_t colsum_add(float* db, const float* part, int nparts, int ncols, cudaStream_t s);
 cudaError_t bias_grad(int act, float* db, const void* dout, int N, int OC, void* scratch,
                       cudaStream_t s);
 
@@ -153,6 +155,9 @@ struct GemmDesc {
     void* aux; long ldx;  // out: EPI_GELU, EPI_GELU_D; in: EPI_GELU_BWD, EPI_MUL_AUX
     int epi;
     int act;                                // element type of A, B, bias, resid, aux, D (non-accum)
+    // EPI_MUL_AUX / EPI_GELU_BWD on the tensor cores only, else NULL:
+    // dbias[n] += sum_m D[m,n] (the fp32 values before rounding to bf16)
+    float* dbias;
 };
 cudaError_t gemm_simt(const GemmDesc& d, cudaStream_t s);
 

@@ -14,6 +14,8 @@ SIGNATURES = {
     "gpt2k_matmul_scratch_bytes": (_sz, []),
     "gpt2k_matmul": (_i, [_i, _i, _i, _i, _i, _vp, _l, _i, _vp, _l, _i, _vp, _l, _vp, _vp, _l,
                           _vp, _l, _i, _vp, _sz, _vp, _vp]),
+    "gpt2k_matmul_bias_grad": (_i, [_i, _i, _i, _vp, _l, _i, _vp, _l, _i, _vp, _l, _vp, _l, _i,
+                                    _vp, _vp, _sz, _vp, _vp]),
     "gpt2k_attention_forward": (_i, [_i, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2k_attention_backward_scratch_bytes": (_sz, [_i, _i, _i, _i]),
     "gpt2k_attention_backward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
@@ -106,6 +108,26 @@ def matmul(A, B, D, *, a_kmajor=True, b_kmajor=True, bias=None, resid=None, aux=
                         aux.shape[1] if aux is not None else 0, EPI[epi], _p(scratch),
                         scratch.numel(), _p(err), _stream())
     _ck(rc, "gpt2k_matmul")
+    return err
+
+
+def matmul_bias_grad(A, B, D, aux, dbias, *, a_kmajor=True, b_kmajor=True, epi="mul_aux",
+                     err=None):
+    """D[M,N] = epi(A . B^T) (epi "mul_aux" or "gelu_bwd", bf16) and
+    dbias[n] += sum_m D[m,n] (fp32, before rounding)"""
+    L = klib()
+    M = A.shape[0] if a_kmajor else A.shape[1]
+    K = A.shape[1] if a_kmajor else A.shape[0]
+    N = B.shape[0] if b_kmajor else B.shape[1]
+    for t in (A, B, D, aux, dbias):
+        assert t.is_cuda and t.is_contiguous()
+    scratch = _scratch(L.gpt2k_matmul_scratch_bytes())
+    err = err if err is not None else err_word()
+    rc = L.gpt2k_matmul_bias_grad(M, N, K, _p(A), A.shape[1], int(a_kmajor), _p(B), B.shape[1],
+                                  int(b_kmajor), _p(D), D.shape[1], _p(aux), aux.shape[1],
+                                  EPI[epi], _p(dbias), _p(scratch), scratch.numel(), _p(err),
+                                  _stream())
+    _ck(rc, "gpt2k_matmul_bias_grad")
     return err
 
 

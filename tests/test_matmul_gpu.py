@@ -280,3 +280,66 @@ def test_matmul_full_size_sampled(name, M, N, Kd, a_km, b_km, epi):
         ref = ops.gelu_backward(pre, acc)
         bnd = np.abs(ops.gelu_backward(pre, np.ones_like(acc))) * bnd * 1.01 + 4e-7 * np.abs(acc)
     assert np.all(np.abs(got - ref) <= bnd + 2.0 ** -8 * np.abs(ref) + 1e-30)
+
+
+# ------------------------------------------------ MLP input gradient + fc bias gradient
+
+def _bias_grad_case(M, N, Kd, a_km, b_km, epi, seed):
+    rng = np.random.default_rng(seed)
+    At, Bt, A64, B64 = _operands(M, N, Kd, seed, a_km, b_km)
+    aux = _bf(rng.normal(0, 0.7, (M, N)) if epi == "mul_aux" else rng.normal(0, 1.5, (M, N)))
+    db0 = rng.normal(0, 1, N).astype(np.float32)
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    db = torch.from_numpy(db0.copy()).cuda()
+    K.matmul_bias_grad(At, Bt, D, aux, db, a_kmajor=a_km, b_kmajor=b_km, epi=epi)
+    torch.cuda.synchronize()
+    return At, Bt, A64, B64, aux, db0, D, db
+
+
+@pytest.mark.parametrize("a_km,b_km", LAYOUTS, ids=["AK-BK", "AK-BN", "AM-BK", "AM-BN"])
+@pytest.mark.parametrize("epi", ["mul_aux", "gelu_bwd"])
+def test_matmul_bias_grad_against_the_oracle(a_km, b_km, epi):
+    """D = acc * aux (or acc * gelu'(aux)) and dbias += sum over rows of D
+    (fp32, before rounding), at a size whose rows (1000: not a multiple of 32
+    or of the 128-row tiles) and columns (392 against 256-wide tiles) are
+    ragged.  Bound on dbias: the sum over rows of each element's fp32 error
+    plus an fp32 sum of M terms."""
+    M, N, Kd = 1000, 392, 200
+    At, Bt, A64, B64, aux, db0, D, db = _bias_grad_case(M, N, Kd, a_km, b_km, epi, 11)
+    acc = ops.matmul_forward(A64, B64)
+    bnd = _bound(A64, B64, acc, Kd, out_bf16=False)
+    x = _np(aux)
+    if epi == "mul_aux":
+        ref = acc * x
+        ebnd = np.abs(x) * bnd + 2.0 ** -24 * np.abs(ref)
+    else:
+        ref = ops.gelu_backward(x, acc)
+        gp = np.abs(ops.gelu_backward(x, np.ones_like(acc)))
+        ebnd = gp * bnd * 1.01 + 4e-7 * np.abs(acc) + 2.0 ** -24 * np.abs(ref)
+    assert np.all(np.abs(_np(D) - ref) <= ebnd + 2.0 ** -8 * np.abs(ref) + 1e-30)
+    want = db0.astype(np.float64) + ref.sum(axis=0)
+    tol = ebnd.sum(axis=0) + (M + 2) * 2.0 ** -24 * (np.abs(ref).sum(axis=0) + np.abs(db0)) + 1e-30
+    got = db.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - want) <= tol), np.max(np.abs(got - want) / tol)
+
+
+@pytest.mark.parametrize("C", [768, 1600], ids=["124M", "1558M"])
+def test_matmul_bias_grad_full_size(C):
+    """the fcproj input gradient of a micro-batch of 16 x 1024 (A = dres
+    [BT, C] K-major, B = W_fcproj stored [C, 4C]): dbias against the fp64 sum
+    of D's bf16 values, which differ from the fp32 values summed by at most
+    half a bf16 step each"""
+    M, N, Kd = 16384, 4 * C, C
+    At, Bt, A64, B64, aux, db0, D, db = _bias_grad_case(M, N, Kd, True, False, "mul_aux", 12)
+    Dd = D.double()
+    want = torch.from_numpy(db0).cuda().double() + Dd.sum(dim=0)
+    tol = (2.0 ** -8 + (M + 2) * 2.0 ** -24) * Dd.abs().sum(dim=0) + 1e-6
+    assert bool(((db.double() - want).abs() <= tol).all())
+    # and D itself on sampled rows against the oracle
+    rows = np.sort(np.random.default_rng(13).choice(M, 24, replace=False))
+    acc = ops.matmul_forward(A64[rows], B64)
+    x = _np(aux[torch.from_numpy(rows).cuda()])
+    ref = acc * x
+    bnd = np.abs(x) * _bound(A64, B64, acc, Kd, out_bf16=False, rows=rows)
+    assert np.all(np.abs(_np(D[torch.from_numpy(rows).cuda()]) - ref)
+                  <= bnd + 2.0 ** -8 * np.abs(ref) + 1e-30)
