@@ -63,8 +63,8 @@ int gpt2k_matmul(int dtype, int impl, int M, int N, int K, const void* A, long l
  * the matmul backward): bf16 on the tensor cores, epi 6 (D = acc * aux) or
  * epi 4 (D = acc * gelu_tanh'(aux)) as in gpt2k_matmul, and
  *   dbias[n] += sum_m D[m,n]
- * summed in fp32 from D's values before they are rounded to bf16, in a fixed
- * order (32-row blocks, then the blocks in order).  dbias: N floats, device.
+ * summed in fp32 over D's bf16 values, in a fixed order (32-row blocks, then
+ * the blocks in order).  dbias: N floats, device.
  * scratch: at least ceil(M/32) * N * 4 bytes (gpt2k_matmul_scratch_bytes()
  * covers M * N <= 512 Mi), owned by the caller and overwritten.  Returns -1
  * for another epi, NULL pointers or a shape the tensor cores do not take

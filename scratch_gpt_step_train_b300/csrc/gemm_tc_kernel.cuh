@@ -83,8 +83,8 @@ struct TcParams {
     bf16* aux;
     long ldx;
     float* part;
-    // EPI_MUL_AUX / EPI_GELU_BWD: column sums of each 32-row block of D (fp32,
-    // before rounding), [ceil(M/32)][N], or NULL
+    // EPI_MUL_AUX / EPI_GELU_BWD: column sums of each 32-row block of D (its
+    // bf16 values, summed in fp32), [ceil(M/32)][N], or NULL
     float* colpart;
     unsigned* err;
 };
@@ -309,25 +309,6 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
             }
         }
     }
-    if ((EPI == EPI_MUL_AUX || EPI == EPI_GELU_BWD) && p.colpart) {
-        // column sums over the warp's 32 rows (lanes): a butterfly that halves
-        // the columns each lane keeps at every step, so that lane j ends with
-        // column j (a fixed order of additions); rows past M hold zeros
-        float cs[32];
-#pragma unroll
-        for (int i = 0; i < 32; i++) cs[i] = v[i];
-#pragma unroll
-        for (int w = 16; w >= 1; w >>= 1) {
-            const bool up = (lane & w) != 0;
-#pragma unroll
-            for (int i = 0; i < w; i++) {
-                const float send = up ? cs[i] : cs[i + w];
-                const float keep = up ? cs[i + w] : cs[i];
-                cs[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-            }
-        }
-        if (row0 < p.M && lane < nv) p.colpart[(size_t)(row0 >> 5) * p.N + col + lane] = cs[0];
-    }
     // the previous chunk's bulk stores must have finished reading the staging tile
     if (lane == 0) bulk_wait_read0();
     __syncwarp();
@@ -358,6 +339,28 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
                 tma_store_2d(&m.aux, stg + 2048, col, row0);
         }
         bulk_commit();
+    }
+    if ((EPI == EPI_MUL_AUX || EPI == EPI_GELU_BWD) && p.colpart) {
+        // column sums of the staged (bf16) piece, read back from shared memory
+        // beside the bulk store: lane l takes columns 2(l & 15), 2(l & 15) + 1
+        // over rows 16(l >> 4) .. +15 in order, then the two row halves are
+        // added (a fixed order); rows past M hold zeros
+        const int cp = lane & 15, rh = lane >> 4;
+        const uint32_t unit = (uint32_t)(cp >> 2), wb = (uint32_t)(cp & 3) * 4u;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const int r = 16 * rh + i;
+            const uint32_t u =
+                ld_shared_u32(stg + (uint32_t)(r * 64) + ((unit ^ (uint32_t)((r >> 1) & 3)) << 4) + wb);
+            s0 += __uint_as_float(u << 16);
+            s1 += __uint_as_float(u & 0xffff0000u);
+        }
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+        if (rh == 0 && row0 < p.M && 2 * cp < nv)
+            *reinterpret_cast<float2*>(p.colpart + (size_t)(row0 >> 5) * p.N + col + 2 * cp) =
+                make_float2(s0, s1);
     }
 }
 

@@ -156,7 +156,7 @@ struct GemmDesc {
     int epi;
     int act;                                // element type of A, B, bias, resid, aux, D (non-accum)
     // EPI_MUL_AUX / EPI_GELU_BWD on the tensor cores only, else NULL:
-    // dbias[n] += sum_m D[m,n] (the fp32 values before rounding to bf16)
+    // dbias[n] += sum_m D[m,n] (D's bf16 values, summed in fp32)
     float* dbias;
 };
 cudaError_t gemm_simt(const GemmDesc& d, cudaStream_t s);

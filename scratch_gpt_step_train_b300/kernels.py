@@ -114,7 +114,7 @@ def matmul(A, B, D, *, a_kmajor=True, b_kmajor=True, bias=None, resid=None, aux=
 def matmul_bias_grad(A, B, D, aux, dbias, *, a_kmajor=True, b_kmajor=True, epi="mul_aux",
                      err=None):
     """D[M,N] = epi(A . B^T) (epi "mul_aux" or "gelu_bwd", bf16) and
-    dbias[n] += sum_m D[m,n] (fp32, before rounding)"""
+    dbias[n] += sum_m D[m,n] (D's bf16 values summed in fp32)"""
     L = klib()
     M = A.shape[0] if a_kmajor else A.shape[1]
     K = A.shape[1] if a_kmajor else A.shape[0]

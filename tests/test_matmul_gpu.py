@@ -299,11 +299,11 @@ def _bias_grad_case(M, N, Kd, a_km, b_km, epi, seed):
 @pytest.mark.parametrize("a_km,b_km", LAYOUTS, ids=["AK-BK", "AK-BN", "AM-BK", "AM-BN"])
 @pytest.mark.parametrize("epi", ["mul_aux", "gelu_bwd"])
 def test_matmul_bias_grad_against_the_oracle(a_km, b_km, epi):
-    """D = acc * aux (or acc * gelu'(aux)) and dbias += sum over rows of D
-    (fp32, before rounding), at a size whose rows (1000: not a multiple of 32
-    or of the 128-row tiles) and columns (392 against 256-wide tiles) are
-    ragged.  Bound on dbias: the sum over rows of each element's fp32 error
-    plus an fp32 sum of M terms."""
+    """D = acc * aux (or acc * gelu'(aux)) and dbias += sum over rows of D's
+    bf16 values, at a size whose rows (1000: not a multiple of 32 or of the
+    128-row tiles) and columns (392 against 256-wide tiles) are ragged.
+    Bound on dbias: the sum over rows of each element's bound plus an fp32
+    sum of M terms."""
     M, N, Kd = 1000, 392, 200
     At, Bt, A64, B64, aux, db0, D, db = _bias_grad_case(M, N, Kd, a_km, b_km, epi, 11)
     acc = ops.matmul_forward(A64, B64)
@@ -318,7 +318,8 @@ def test_matmul_bias_grad_against_the_oracle(a_km, b_km, epi):
         ebnd = gp * bnd * 1.01 + 4e-7 * np.abs(acc) + 2.0 ** -24 * np.abs(ref)
     assert np.all(np.abs(_np(D) - ref) <= ebnd + 2.0 ** -8 * np.abs(ref) + 1e-30)
     want = db0.astype(np.float64) + ref.sum(axis=0)
-    tol = ebnd.sum(axis=0) + (M + 2) * 2.0 ** -24 * (np.abs(ref).sum(axis=0) + np.abs(db0)) + 1e-30
+    tol = ((ebnd + 2.0 ** -8 * np.abs(ref)).sum(axis=0)
+           + (M + 2) * 2.0 ** -24 * (1.01 * np.abs(ref).sum(axis=0) + np.abs(db0)) + 1e-30)
     got = db.cpu().numpy().astype(np.float64)
     assert np.all(np.abs(got - want) <= tol), np.max(np.abs(got - want) / tol)
 
@@ -327,13 +328,12 @@ def test_matmul_bias_grad_against_the_oracle(a_km, b_km, epi):
 def test_matmul_bias_grad_full_size(C):
     """the fcproj input gradient of a micro-batch of 16 x 1024 (A = dres
     [BT, C] K-major, B = W_fcproj stored [C, 4C]): dbias against the fp64 sum
-    of D's bf16 values, which differ from the fp32 values summed by at most
-    half a bf16 step each"""
+    of D's bf16 values (the values the kernel sums), to an fp32 sum's error"""
     M, N, Kd = 16384, 4 * C, C
     At, Bt, A64, B64, aux, db0, D, db = _bias_grad_case(M, N, Kd, True, False, "mul_aux", 12)
     Dd = D.double()
     want = torch.from_numpy(db0).cuda().double() + Dd.sum(dim=0)
-    tol = (2.0 ** -8 + (M + 2) * 2.0 ** -24) * Dd.abs().sum(dim=0) + 1e-6
+    tol = (M + 2) * 2.0 ** -24 * (Dd.abs().sum(dim=0) + abs(torch.from_numpy(db0).cuda().double())) + 1e-30
     assert bool(((db.double() - want).abs() <= tol).all())
     # and D itself on sampled rows against the oracle
     rows = np.sort(np.random.default_rng(13).choice(M, 24, replace=False))
