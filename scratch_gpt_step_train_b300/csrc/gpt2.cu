@@ -20,6 +20,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <string>
 #include <vector>
 
@@ -34,7 +35,7 @@ enum {
     K_QKV_DX, K_PROJ_DX, K_FC_DX, K_FCPROJ_DX, K_CLS_DX,
     K_QKV_DW, K_PROJ_DW, K_FC_DW, K_FCPROJ_DW, K_CLS_DW,
     K_ATTN_FWD, K_ATTN_BWD, K_LN_FWD, K_LN_BWD, K_XENT, K_EMB_FWD, K_EMB_BWD, K_BIAS, K_ADAM,
-    K_ZERO, K_RECOMP, K_NCLASS
+    K_ZERO, K_RECOMP, K_COLSUM, K_NCLASS
 };
 static const char* kClassNames[K_NCLASS] = {
     "matmul_qkv_fwd", "matmul_proj_fwd", "matmul_fc_fwd", "matmul_fcproj_fwd",
@@ -42,7 +43,7 @@ static const char* kClassNames[K_NCLASS] = {
     "matmul_fcproj_dx", "matmul_classifier_dx", "matmul_qkv_dw", "matmul_proj_dw",
     "matmul_fc_dw", "matmul_fcproj_dw", "matmul_classifier_dw", "attention_fwd",
     "attention_bwd", "layernorm_fwd", "layernorm_bwd", "crossentropy", "embedding_fwd",
-    "embedding_bwd", "bias_grad", "adamw", "zero_grad", "recompute"};
+    "embedding_bwd", "bias_grad", "adamw", "zero_grad", "recompute", "grad_colsum"};
 
 struct ProfRec {
     int cls;
@@ -84,6 +85,12 @@ struct gpt2 {
     void *dres, *dbig, *dln, *datty, *dqkv;
     void* scratch;
     size_t scratch_bytes;
+    // column partials of the LayerNorm-weight and bias gradients of one
+    // backward pass, one region per producer, summed by one batched launch
+    // at its end: (2L+1) LayerNorm regions, then L qkv-bias, then L fc-bias
+    float* dpart;
+    size_t ln_part_bytes, qkvb_part_bytes, fcb_part_bytes;
+    std::vector<ColsumTask> ctasks;
     int32_t *tok, *tgt;
     unsigned* err;
     float* adam_state;
@@ -233,6 +240,13 @@ static void plan(gpt2* g, char* base, size_t* total) {
     g->dqkv = p.take(BT * 3 * C * as);
     g->scratch_bytes = scratch_need(g->L, g->H, g->C, g->Vp, g->T, g->B);
     g->scratch = p.take(g->scratch_bytes);
+    auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+    g->ln_part_bytes = al(layernorm_backward_scratch((int)BT, (int)C, true));
+    g->qkvb_part_bytes = al(bias_grad_scratch((int)BT, (int)(3 * C)));
+    g->fcb_part_bytes = al(std::max((BT + 31) / 32 * 4 * C * 4,
+                                    bias_grad_scratch((int)BT, (int)(4 * C))));
+    g->dpart = (float*)p.take((2 * L + 1) * g->ln_part_bytes +
+                              L * (g->qkvb_part_bytes + g->fcb_part_bytes));
     g->tok = (int32_t*)p.take(BT * 4);
     g->tgt = (int32_t*)p.take(BT * 4);
     g->err = (unsigned*)p.take(16);
@@ -651,11 +665,26 @@ extern "C" int gpt2_backward(gpt2_t* g) {
     // projection's output gradient also yields that projection's bias
     // gradient as the column sums of dres
     double lnb_bytes = as * 4.0 * bt * c + 8.0 * bt;
-    LAUNCH(K_LN_BWD, 2, 0, as * 3.0 * bt * c + 8.0 * bt,
-           layernorm_backward(g->act, dres, grad_tensor(g, P_LNFW, 0), grad_tensor(g, P_LNFB, 0),
-                              L > 0 ? grad_tensor(g, P_FCPROJB, L - 1) : nullptr, g->dln, xL,
-                              pc_tensor(g, P_LNFW, 0), g->lnf_mean, g->lnf_rstd, BT, C, false,
-                              g->scratch, g->stream));
+    // the column sums (LayerNorm weights, biases) of the whole pass are
+    // gathered as tasks and summed by one batched launch at its end
+    g->ctasks.clear();
+    int np = 0;
+    auto ln_task = [&](int idx, float* dw, float* db, float* dxsum) {
+        float* part = (float*)((char*)g->dpart + (size_t)idx * g->ln_part_bytes);
+        g->ctasks.push_back(ColsumTask{part, {dw, db, dxsum}, np, (dxsum ? 3 : 2) * C, C});
+        return part;
+    };
+    char* const qkvb_base = (char*)g->dpart + (size_t)(2 * L + 1) * g->ln_part_bytes;
+    char* const fcb_base = qkvb_base + (size_t)L * g->qkvb_part_bytes;
+    {
+        float* dxs = L > 0 ? grad_tensor(g, P_FCPROJB, L - 1) : nullptr;
+        float* part = (float*)g->dpart;
+        LAUNCH(K_LN_BWD, 1, 0, as * 3.0 * bt * c + 8.0 * bt,
+               layernorm_backward_rows(g->act, dres, dxs != nullptr, g->dln, xL,
+                                       pc_tensor(g, P_LNFW, 0), g->lnf_mean, g->lnf_rstd, BT, C,
+                                       false, part, &np, g->stream));
+        ln_task(0, grad_tensor(g, P_LNFW, 0), grad_tensor(g, P_LNFB, 0), dxs);
+    }
     const int lln = g->recompute >= 2 ? 0 : 1, lg = g->recompute >= 1 ? 0 : 1;
     const double ln_bytes = as * 2.0 * bt * c + 8.0 * bt;
     for (int l = L - 1; l >= 0; l--) {
@@ -681,11 +710,16 @@ extern "C" int gpt2_backward(gpt2_t* g) {
                g->recompute >= 1 ? EPI_GELU_BWD : EPI_MUL_AUX);
         d.aux = fch;
         d.ldx = 4 * C;
-        // the fc bias gradient (column sums of this product's output) comes
-        // out of the same kernel on the tensor cores
+        // the fc bias gradient (column sums of this product's output): its
+        // partials come out of the same kernel on the tensor cores
         d.act = g->act;
+        float* fcb_part = (float*)(fcb_base + (size_t)l * g->fcb_part_bytes);
         const bool fused_fcb = g->use_tc && gemm_tc_supported(d);
-        if (fused_fcb) d.dbias = grad_tensor(g, P_FCB, l);
+        if (fused_fcb) {
+            d.colpart = fcb_part;
+            g->ctasks.push_back(ColsumTask{fcb_part, {grad_tensor(g, P_FCB, l), nullptr, nullptr},
+                                           (BT + 31) / 32, 4 * C, 4 * C});
+        }
         RUN(mm(g, K_FCPROJ_DX, d));
         if (g->recompute >= 2)  // ln2(x1) again (the same kernel on the same input)
             LAUNCH(K_RECOMP, 1, 0, ln_bytes,
@@ -695,18 +729,25 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         d = gd(4 * C, C, BT, g->dbig, 4 * C, 0, ln2, C, 0, grad_tensor(g, P_FCW, l), C,
                EPI_ACCUM_F32);
         RUN(mm(g, K_FC_DW, d));
-        if (!fused_fcb)
-            LAUNCH(K_BIAS, 2, 0, as * bt * 4 * c,
-                   bias_grad(g->act, grad_tensor(g, P_FCB, l), g->dbig, BT, 4 * C, g->scratch,
-                             g->stream));
+        if (!fused_fcb) {
+            LAUNCH(K_BIAS, 1, 0, as * bt * 4 * c,
+                   bias_grad_rows(g->act, fcb_part, g->dbig, BT, 4 * C, &np, g->stream));
+            g->ctasks.push_back(ColsumTask{fcb_part, {grad_tensor(g, P_FCB, l), nullptr, nullptr},
+                                           np, 4 * C, 4 * C});
+        }
         d = gd(BT, C, 4 * C, g->dbig, 4 * C, 1, pc_tensor(g, P_FCW, l), C, 0, g->dln, C,
                EPI_STORE);
         RUN(mm(g, K_FC_DX, d));
-        LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
-               layernorm_backward(g->act, dres, grad_tensor(g, P_LN2W, l),
-                                  grad_tensor(g, P_LN2B, l), grad_tensor(g, P_PROJB, l), g->dln,
-                                  x1, pc_tensor(g, P_LN2W, l), g->ln2_mean + l * bt,
-                                  g->ln2_rstd + l * bt, BT, C, true, g->scratch, g->stream));
+        {
+            float* part = (float*)((char*)g->dpart + (size_t)(1 + 2 * l) * g->ln_part_bytes);
+            LAUNCH(K_LN_BWD, 1, 0, lnb_bytes,
+                   layernorm_backward_rows(g->act, dres, true, g->dln, x1,
+                                           pc_tensor(g, P_LN2W, l), g->ln2_mean + l * bt,
+                                           g->ln2_rstd + l * bt, BT, C, true, part, &np,
+                                           g->stream));
+            ln_task(1 + 2 * l, grad_tensor(g, P_LN2W, l), grad_tensor(g, P_LN2B, l),
+                    grad_tensor(g, P_PROJB, l));
+        }
         // attention: x1 = rin + proj(attn(qkv(ln1(rin))))
         d = gd(C, C, BT, dres, C, 0, atty, C, 0, grad_tensor(g, P_PROJW, l), C, EPI_ACCUM_F32);
         RUN(mm(g, K_PROJ_DW, d));
@@ -725,18 +766,34 @@ extern "C" int gpt2_backward(gpt2_t* g) {
         d = gd(3 * C, C, BT, g->dqkv, 3 * C, 0, ln1, C, 0, grad_tensor(g, P_QKVW, l), C,
                EPI_ACCUM_F32);
         RUN(mm(g, K_QKV_DW, d));
-        LAUNCH(K_BIAS, 2, 0, as * bt * 3 * c,
-               bias_grad(g->act, grad_tensor(g, P_QKVB, l), g->dqkv, BT, 3 * C, g->scratch,
-                         g->stream));
+        {
+            float* part = (float*)(qkvb_base + (size_t)l * g->qkvb_part_bytes);
+            LAUNCH(K_BIAS, 1, 0, as * bt * 3 * c,
+                   bias_grad_rows(g->act, part, g->dqkv, BT, 3 * C, &np, g->stream));
+            g->ctasks.push_back(ColsumTask{part, {grad_tensor(g, P_QKVB, l), nullptr, nullptr},
+                                           np, 3 * C, 3 * C});
+        }
         d = gd(BT, C, 3 * C, g->dqkv, 3 * C, 1, pc_tensor(g, P_QKVW, l), C, 0, g->dln, C,
                EPI_STORE);
         RUN(mm(g, K_QKV_DX, d));
-        LAUNCH(K_LN_BWD, 2, 0, lnb_bytes,
-               layernorm_backward(g->act, dres, grad_tensor(g, P_LN1W, l),
-                                  grad_tensor(g, P_LN1B, l),
-                                  l > 0 ? grad_tensor(g, P_FCPROJB, l - 1) : nullptr, g->dln, rin,
-                                  pc_tensor(g, P_LN1W, l), g->ln1_mean + l * bt,
-                                  g->ln1_rstd + l * bt, BT, C, true, g->scratch, g->stream));
+        {
+            float* dxs = l > 0 ? grad_tensor(g, P_FCPROJB, l - 1) : nullptr;
+            float* part = (float*)((char*)g->dpart + (size_t)(2 + 2 * l) * g->ln_part_bytes);
+            LAUNCH(K_LN_BWD, 1, 0, lnb_bytes,
+                   layernorm_backward_rows(g->act, dres, dxs != nullptr, g->dln, rin,
+                                           pc_tensor(g, P_LN1W, l), g->ln1_mean + l * bt,
+                                           g->ln1_rstd + l * bt, BT, C, true, part, &np,
+                                           g->stream));
+            ln_task(2 + 2 * l, grad_tensor(g, P_LN1W, l), grad_tensor(g, P_LN1B, l), dxs);
+        }
+    }
+    {
+        double cby = 0;
+        for (const ColsumTask& t : g->ctasks) cby += 4.0 * t.ncols * (t.nparts + 2.0);
+        const int nk = ((int)g->ctasks.size() + 95) / 96;
+        int nl = 0;
+        LAUNCH(K_COLSUM, nk, 0, cby,
+               colsum_batch(g->ctasks.data(), (int)g->ctasks.size(), g->stream, &nl));
     }
     LAUNCH(K_EMB_BWD, 9, 0, as * bt * c + 8.0 * T * c,
            encoder_backward(g->act, grad_tensor(g, P_WTE, 0), grad_tensor(g, P_WPE, 0), dres,

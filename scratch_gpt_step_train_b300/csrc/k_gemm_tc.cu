@@ -243,11 +243,13 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     tp.colpart = nullptr;
     tp.err = err;
     const int row_blocks = (d.M + 31) / 32;
-    if (d.dbias) {
-        // column partial sums in scratch, then one ordered sum into dbias
+    if (d.dbias || d.colpart) {
+        // column partial sums (in scratch, then one ordered sum into dbias;
+        // or in the caller's region, summed later)
         if (d.epi != EPI_MUL_AUX && d.epi != EPI_GELU_BWD) return cudaErrorInvalidValue;
-        if (!scratch || (size_t)row_blocks * d.N * 4 > scratch_bytes) return cudaErrorInvalidValue;
-        tp.colpart = (float*)scratch;
+        if (d.dbias && (!scratch || (size_t)row_blocks * d.N * 4 > scratch_bytes))
+            return cudaErrorInvalidValue;
+        tp.colpart = d.dbias ? (float*)scratch : d.colpart;
     }
     const long tiles = (long)tiles_m * tiles_n;
     if (splits > 1) {
@@ -272,7 +274,7 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     }
     if (e != cudaSuccess) return e;
     if (nlaunch) *nlaunch = 1;
-    if (tp.colpart) {
+    if (d.dbias) {
         if (nlaunch) *nlaunch = 2;
         return colsum_add(d.dbias, tp.colpart, row_blocks, d.N, s);
     }

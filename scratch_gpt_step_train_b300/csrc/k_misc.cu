@@ -677,13 +677,11 @@ __global__ void __launch_bounds__(256, 2)
 struct ColsumOut {
     float* p[3];
 };
-__global__ void __launch_bounds__(256) k_colsum(ColsumOut outs, int n0, int ncols,
-                                                const float* part, int nparts, long ld) {
-    gdc_wait();
-    gdc_launch_dependents();
+__device__ __forceinline__ void colsum_cols(const ColsumOut& outs, int n0, int ncols,
+                                            const float* part, int nparts, long ld, int cblock) {
     __shared__ float sh[8][33];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int c = blockIdx.x * 32 + tx;
+    const int c = cblock * 32 + tx;
     float a[4] = {0.f, 0.f, 0.f, 0.f};
     if (c < ncols) {
         // 16 independent loads in flight per thread: the partial rows are few
@@ -706,6 +704,51 @@ __global__ void __launch_bounds__(256) k_colsum(ColsumOut outs, int n0, int ncol
         const int k = c / n0;
         outs.p[k][c - k * n0] += t;
     }
+}
+__global__ void __launch_bounds__(256) k_colsum(ColsumOut outs, int n0, int ncols,
+                                                const float* part, int nparts, long ld) {
+    gdc_wait();
+    gdc_launch_dependents();
+    colsum_cols(outs, n0, ncols, part, nparts, ld, blockIdx.x);
+}
+
+// Many column sums in one launch: task i owns blocks [blk0[i], blk0[i+1]),
+// each summing 32 columns exactly as k_colsum does.
+#define COLSUM_MAX_TASKS 96
+struct ColsumBatch {
+    ColsumTask t[COLSUM_MAX_TASKS];
+    int blk0[COLSUM_MAX_TASKS + 1];
+    int ntasks;
+};
+__global__ void __launch_bounds__(256) k_colsum_batch(const __grid_constant__ ColsumBatch b) {
+    gdc_wait();
+    gdc_launch_dependents();
+    int lo = 0, hi = b.ntasks - 1;  // the last task whose first block <= blockIdx.x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (b.blk0[mid] <= (int)blockIdx.x) lo = mid;
+        else hi = mid - 1;
+    }
+    const ColsumTask& t = b.t[lo];
+    ColsumOut o{{t.out[0], t.out[1], t.out[2]}};
+    colsum_cols(o, t.n0, t.ncols, t.part, t.nparts, (long)t.ncols, (int)blockIdx.x - b.blk0[lo]);
+}
+cudaError_t colsum_batch(const ColsumTask* tasks, int n, cudaStream_t s, int* nlaunch) {
+    if (nlaunch) *nlaunch = 0;
+    for (int i0 = 0; i0 < n; i0 += COLSUM_MAX_TASKS) {
+        ColsumBatch b;
+        b.ntasks = std::min(COLSUM_MAX_TASKS, n - i0);
+        int nb = 0;
+        for (int i = 0; i < b.ntasks; i++) {
+            b.t[i] = tasks[i0 + i];
+            b.blk0[i] = nb;
+            nb += cdiv(b.t[i].ncols, 32);
+        }
+        b.blk0[b.ntasks] = nb;
+        launch_pdl(k_colsum_batch, nb, 256, 0, s, b);
+        if (nlaunch) ++*nlaunch;
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t colsum_add(float* db, const float* part, int nparts, int ncols, cudaStream_t s) {
@@ -801,36 +844,44 @@ static cudaError_t ln_bwd_vec(T* dx, float* part, const T* dout, const T* x, con
 #undef LNB
 }
 
+// the row kernel alone: per-block column partials [nb][nacc * C] into part
 template <typename T>
-static cudaError_t ln_bwd_t(void* dx, float* dw, float* db, float* dxsum, const void* dout,
-                            const void* x, const void* w, const float* mean, const float* rstd,
-                            int N, int C, int accum, void* scratch, cudaStream_t s) {
+static cudaError_t ln_bwd_rows(void* dx, bool dxsum, const void* dout, const void* x,
+                               const void* w, const float* mean, const float* rstd, int N, int C,
+                               int accum, float* part, int* nb, cudaStream_t s) {
     constexpr int VM = 16 / sizeof(T);
-    float* part = (float*)scratch;
-    int nb = 0;
-    cudaError_t e;
+    *nb = 0;
 #define LNV(V, A)                                                                                \
     ln_bwd_vec<T, V, A>((T*)dx, part, (const T*)dout, (const T*)x, (const T*)w, mean, rstd, N,  \
-                        C, accum, &nb, s)
-    if (C % VM == 0) e = dxsum ? LNV(VM, 3) : LNV(VM, 2);
-    else e = dxsum ? LNV(1, 3) : LNV(1, 2);
+                        C, accum, nb, s)
+    if (C % VM == 0) return dxsum ? LNV(VM, 3) : LNV(VM, 2);
+    return dxsum ? LNV(1, 3) : LNV(1, 2);
 #undef LNV
-    if (e != cudaSuccess) return e;
-    const int nacc = dxsum ? 3 : 2;
-    ColsumOut o{{dw, db, dxsum}};
-    launch_pdl(k_colsum, cdiv(nacc * C, 32), 256, 0, s, o, C, nacc * C, part, nb, (long)nacc * C);
-    return cudaGetLastError();
+}
+cudaError_t layernorm_backward_rows(int act, void* dx, bool dxsum, const void* dout,
+                                    const void* x, const void* w, const float* mean,
+                                    const float* rstd, int N, int C, bool accum_dx, float* part,
+                                    int* nparts, cudaStream_t s) {
+    if (C > 2048) return cudaErrorInvalidValue;
+    if (act == ACT_BF16)
+        return ln_bwd_rows<bf16>(dx, dxsum, dout, x, w, mean, rstd, N, C, accum_dx, part, nparts,
+                                 s);
+    return ln_bwd_rows<float>(dx, dxsum, dout, x, w, mean, rstd, N, C, accum_dx, part, nparts,
+                              s);
 }
 cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, float* dxsum,
                                const void* dout, const void* x, const void* w, const float* mean,
                                const float* rstd, int N, int C, bool accum_dx, void* scratch,
                                cudaStream_t s) {
-    if (C > 2048) return cudaErrorInvalidValue;
-    if (act == ACT_BF16)
-        return ln_bwd_t<bf16>(dx, dw, db, dxsum, dout, x, w, mean, rstd, N, C, accum_dx, scratch,
-                              s);
-    return ln_bwd_t<float>(dx, dw, db, dxsum, dout, x, w, mean, rstd, N, C, accum_dx, scratch,
-                           s);
+    float* part = (float*)scratch;
+    int nb = 0;
+    cudaError_t e = layernorm_backward_rows(act, dx, dxsum != nullptr, dout, x, w, mean, rstd, N,
+                                            C, accum_dx, part, &nb, s);
+    if (e != cudaSuccess) return e;
+    const int nacc = dxsum ? 3 : 2;
+    ColsumOut o{{dw, db, dxsum}};
+    launch_pdl(k_colsum, cdiv(nacc * C, 32), 256, 0, s, o, C, nacc * C, part, nb, (long)nacc * C);
+    return cudaGetLastError();
 }
 
 // ===========================================================================
@@ -891,8 +942,8 @@ __global__ void __launch_bounds__(256) k_bias_part(float* part, const T* dout, i
 size_t bias_grad_scratch(int N, int OC) { return (size_t)cdiv(N, BG_ROWS) * OC * sizeof(float); }
 
 template <typename T>
-static cudaError_t bias_grad_t(float* db, const void* dout, int N, int OC, void* scratch,
-                               cudaStream_t s) {
+static cudaError_t bias_grad_rows_t(float* part, const void* dout, int N, int OC, int* nparts,
+                                    cudaStream_t s) {
     constexpr int VM = 16 / sizeof(T);
     const int nch = cdiv(N, BG_ROWS);
     const int vec = OC % VM == 0 ? VM : 1;
@@ -907,18 +958,26 @@ static cudaError_t bias_grad_t(float* db, const void* dout, int N, int OC, void*
             if (2 * q >= pmax) P = q;
             break;
         }
-    float* part = (float*)scratch;
     dim3 grid(gx, P);
     if (vec == VM) launch_pdl(k_bias_part<T, VM>, grid, 256, 0, s, part, (const T*)dout, N, OC, nch);
     else launch_pdl(k_bias_part<T, 1>, grid, 256, 0, s, part, (const T*)dout, N, OC, nch);
-    ColsumOut o{{db, nullptr, nullptr}};
-    launch_pdl(k_colsum, cdiv(OC, 32), 256, 0, s, o, OC, OC, part, P, OC);
+    *nparts = P;
     return cudaGetLastError();
+}
+cudaError_t bias_grad_rows(int act, float* part, const void* dout, int N, int OC, int* nparts,
+                           cudaStream_t s) {
+    if (act == ACT_BF16) return bias_grad_rows_t<bf16>(part, dout, N, OC, nparts, s);
+    return bias_grad_rows_t<float>(part, dout, N, OC, nparts, s);
 }
 cudaError_t bias_grad(int act, float* db, const void* dout, int N, int OC, void* scratch,
                       cudaStream_t s) {
-    if (act == ACT_BF16) return bias_grad_t<bf16>(db, dout, N, OC, scratch, s);
-    return bias_grad_t<float>(db, dout, N, OC, scratch, s);
+    float* part = (float*)scratch;
+    int P = 0;
+    cudaError_t e = bias_grad_rows(act, part, dout, N, OC, &P, s);
+    if (e != cudaSuccess) return e;
+    ColsumOut o{{db, nullptr, nullptr}};
+    launch_pdl(k_colsum, cdiv(OC, 32), 256, 0, s, o, OC, OC, part, P, OC);
+    return cudaGetLastError();
 }
 
 // ===========================================================================

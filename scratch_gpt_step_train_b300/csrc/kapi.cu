@@ -45,6 +45,7 @@ extern "C" int gpt2k_matmul(int dtype, int impl, int M, int N, int K, const void
     d.bias = bias; d.resid = resid; d.ldr = ldr; d.aux = aux; d.ldx = ldx;
     d.epi = epi; d.act = dtype;
     d.dbias = nullptr;
+    d.colpart = nullptr;
     cudaStream_t s = (cudaStream_t)stream;
     bool tc = dtype == ACT_BF16 && gemm_tc_available() && gemm_tc_supported(d);
     if (impl == 2 && !tc) return GPT2_ERR_ARG;

@@ -75,11 +75,31 @@ cudaError_t layernorm_backward(int act, void* dx, float* dw, float* db, float* d
                                const void* dout, const void* x, const void* w, const float* mean,
                                const float* rstd, int N, int C, bool accum_dx, void* scratch,
                                cudaStream_t s);
+// its row kernel alone: partials [nparts][(dxsum ? 3 : 2) * C] (dw | db |
+// dxsum columns) into part (layernorm_backward_scratch bytes)
+cudaError_t layernorm_backward_rows(int act, void* dx, bool dxsum, const void* dout,
+                                    const void* x, const void* w, const float* mean,
+                                    const float* rstd, int N, int C, bool accum_dx, float* part,
+                                    int* nparts, cudaStream_t s);
 
 // ---- bias gradient: db[o] += sum_n dout[n,o] (deterministic, two stage) ---
 size_t bias_grad_scratch(int N, int OC);
 // db[c] += sum_{i < nparts} part[i * ncols + c], rows in order (one launch)
 cudaError_t colsum_add(float* db, const float* part, int nparts, int ncols, cudaStream_t s);
+// Deferred column sums.  The *_rows producers write their per-block column
+// partials [nparts][ncols] into a caller's region and report nparts; one
+// colsum_batch call then adds every task's sums into its outputs: out[k][c]
+// += sum_i part[i * ncols + k * n0 + c] (k < ncols / n0), the same order of
+// additions as the immediate forms.
+struct ColsumTask {
+    const float* part;
+    float* out[3];
+    int nparts, ncols, n0;
+};
+cudaError_t colsum_batch(const ColsumTask* tasks, int n, cudaStream_t s, int* nlaunch);
+// the bias gradient's row kernel alone: partials [nparts][OC], nparts <= ceil(N / 64)
+cudaError_t bias_grad_rows(int act, float* part, const void* dout, int N, int OC, int* nparts,
+                           cudaStream_t s);
 cudaError_t bias_grad(int act, float* db, const void* dout, int N, int OC, void* scratch,
                       cudaStream_t s);
 
@@ -158,6 +178,9 @@ struct GemmDesc {
     // EPI_MUL_AUX / EPI_GELU_BWD on the tensor cores only, else NULL:
     // dbias[n] += sum_m D[m,n] (D's bf16 values, summed in fp32)
     float* dbias;
+    // instead of dbias (same modes): the column sums of each 32-row block,
+    // [ceil(M/32)][N], written here for a later colsum_batch
+    float* colpart;
 };
 cudaError_t gemm_simt(const GemmDesc& d, cudaStream_t s);
 
