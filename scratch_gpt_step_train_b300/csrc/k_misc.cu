@@ -1587,7 +1587,8 @@ __global__ void k_emb_reduce2(float* dwte, float* part, const T* dx, const int* 
     }
 }
 
-// one block per multi-chunk token: dwte[v] += its partial rows in chunk order
+// block (x, y): multi-chunk token x, columns [256 y, 256 y + 256): dwte[v] +=
+// its partial rows added in chunk order (eight loads in flight at a time)
 __global__ void k_emb_fold(float* dwte, const float* part, const int* cnt, const int* poff,
                            const int* mlist, int C) {
     gdc_wait();
@@ -1596,11 +1597,18 @@ __global__ void k_emb_fold(float* dwte, const float* part, const int* cnt, const
     const int v = mlist[1 + blockIdx.x], n = cnt[v];
     const int ch = (n + EMB_R - 1) / EMB_R;
     const float* p = part + (size_t)poff[v] * C;
-    for (int col = threadIdx.x; col < C; col += blockDim.x) {
-        float a = 0.f;
-        for (int k = 0; k < ch; k++) a += p[(size_t)k * C + col];
-        dwte[(size_t)v * C + col] += a;
+    const int col = blockIdx.y * 256 + threadIdx.x;
+    if (col >= C) return;
+    float a = 0.f;
+    for (int k0 = 0; k0 < ch; k0 += 8) {
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) x[k] = k0 + k < ch ? p[(size_t)(k0 + k) * C + col] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            if (k0 + k < ch) a += x[k];
     }
+    dwte[(size_t)v * C + col] += a;
 }
 
 template <typename T, int VEC>
@@ -1650,7 +1658,8 @@ static cudaError_t emb_bwd_vec(float* dwte, float* dwpe, const void* dx, const i
     else if (it <= 16) EMR(16);
     else return cudaErrorInvalidValue;
 #undef EMR
-    launch_pdl(k_emb_fold, e.max_multi, 256, 0, s, dwte, e.part, e.cnt, e.poff, e.mlist, C);
+    launch_pdl(k_emb_fold, dim3(e.max_multi, cdiv(C, 256)), 256, 0, s, dwte, e.part, e.cnt, e.poff,
+               e.mlist, C);
     launch_pdl(k_wpe_bwd<T, VEC>, cdiv((long)T_ * (C / VEC), 256), 256, 0, s, dwpe, (const T*)dx, B, T_,
                                                                        C);
     return cudaGetLastError();
