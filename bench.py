@@ -62,14 +62,22 @@ def flops_per_token(w):
     return 6 * n_params(w["L"], w["C"], w["V"], w["T"]) + 6 * w["L"] * w["C"] * w["T"]
 
 
+# the sources of the kernels whose DRAM traffic profiles/dram_traffic_*.txt
+# records (the products and attention), with the headers they include
+TRAFFIC_SOURCES = ("gemm_tc_kernel.cuh", "gemm_tc.h", "tc_ptx.cuh", "common.cuh", "kernels.h",
+                   "k_attn_tc.cu")
+
+
 def kernel_sources_hash():
-    """sha256 over the CUDA sources (file names and contents, sorted)"""
+    """sha256 over the sources of the product and attention kernels (file
+    names and contents, sorted)"""
     import hashlib
     d = os.path.join(ROOT, "scratch_gpt_step_train_b300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
-        h.update(f.encode())
-        h.update(open(os.path.join(d, f), "rb").read())
+        if f in TRAFFIC_SOURCES or f.startswith("k_gemm_tc"):
+            h.update(f.encode())
+            h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()
 
 

@@ -46,14 +46,17 @@ def test_stale_traffic_counters_are_dropped(tmp_path, monkeypatch):
     b = _bench()
     csrc = tmp_path / "scratch_gpt_step_train_b300" / "csrc"
     csrc.mkdir(parents=True)
-    (csrc / "k.cu").write_text("// kernel v1\n")
+    (csrc / "k_attn_tc.cu").write_text("// kernel v1\n")
+    (csrc / "k_misc.cu").write_text("// other kernels v1\n")
     (tmp_path / "profiles").mkdir()
     monkeypatch.setattr(b, "ROOT", os.fspath(tmp_path))
     sha = b.kernel_sources_hash()
     (tmp_path / "profiles" / "dram_traffic_gpt2_124M.txt").write_text(
         f"# counters\n# kernel_sources_sha256 {sha}\nattention_bwd 270392320\nmatmul_qkv_fwd 52000000\n")
     assert b.load_traffic("124M") == {"attention_bwd": 270392320.0, "matmul_qkv_fwd": 52000000.0}
-    (csrc / "k.cu").write_text("// kernel v2\n")  # the kernels changed after the capture
+    (csrc / "k_misc.cu").write_text("// other kernels v2\n")  # not a recorded kernel
+    assert b.load_traffic("124M") == {"attention_bwd": 270392320.0, "matmul_qkv_fwd": 52000000.0}
+    (csrc / "k_attn_tc.cu").write_text("// kernel v2\n")  # the kernels changed after the capture
     assert b.load_traffic("124M") is None
     assert b.load_traffic("350M") is None  # no capture at all
 
