@@ -114,7 +114,9 @@ int gpt2k_layernorm_backward(int dtype, void* dx, float* dw, float* db, float* d
  *  - Returns -1 (GPT2_ERR_ARG) for C > 2048 (beyond the fixed scratch) or a bad
  *    shape, -2 if the array's device address cannot be found or a launch fails.
  *  - The first call on each device looks up the array's address with that
- *    device current; make that first call before any stream capture.
+ *    device current and keeps it for the process: it assumes one primary
+ *    context per device for the process's life (after cudaDeviceReset the
+ *    kept address is stale).  Make that first call before any stream capture.
  *  - All calls share the one array: calls whose work overlaps on the GPU (on
  *    different streams) race.  Each call fully overwrites the part it uses, so
  *    contents left by an earlier call are harmless. */

@@ -197,7 +197,8 @@ struct EpiMaps {
 
 // ------------------------------------------------------- CTA-pair helpers
 // (tcgen05 cta_group::2: the pair's MMAs are issued by the leader, rank 0;
-// every load and every signal goes to one CTA's own barrier -- no multicast)
+// every load and every signal goes to one CTA's own barrier, one copy per
+// destination)
 __device__ __forceinline__ uint32_t pair_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -93,6 +93,8 @@ class OracleShardModel:
         count = int(self.dcount.item()) if self.dcount is not None else self.count
         self.dcount = None
         norm = float(torch.sqrt((self.g * self.g).sum())) / count
+        if not np.isfinite(norm):  # the library's GPT2_ERR_NONFINITE: nothing updated
+            raise FloatingPointError("gradient norm is not finite")
         sc = (1.0 / count) * (clip / norm if clip > 0 and norm > clip else 1.0)
         self.t += 1
         s0 = self.shard[0]
@@ -179,6 +181,71 @@ def test_data_parallel_gloo_more_ranks(world, n, uneven):
         assert m.size == hi - lo  # the rank holds its slice of the moments alone
         np.testing.assert_allclose(m, ref.m.numpy()[lo:hi], rtol=1e-12, atol=1e-15)
         assert all(got[q][2] == norms for q in range(world))  # one summed gradient everywhere
+
+
+def _gloo_rank_poisoned(rank, world, port, q):
+    """rank 1 feeds a NaN into step 1's gradient; every rank must see the step
+    fail, clear its gradients and go on"""
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        model = OracleShardModel(N_PARAMS, seed=5, shard=shard_bounds(N_PARAMS, world)[rank])
+        dp = DataParallel(model)
+        failed = []
+        for step in range(STEPS):
+            model.zero_grad()
+            for k in range(MICRO):
+                g = _micro_grad(rank, step, k)
+                if step == 1 and rank == 1 and k == 0:
+                    g[7] = float("nan")
+                model.accumulate(g)
+            try:
+                dp.step(**HP)
+                failed.append(False)
+            except FloatingPointError:
+                failed.append(True)
+        q.put((rank, model.w.numpy().copy(), failed))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_data_parallel_gloo_non_finite_step_fails_on_every_rank():
+    """a non-finite gradient on one rank reaches every rank through the
+    all-reduce: the step fails alike everywhere, updates nothing, and after
+    zero_grad the next step equals one process that skipped it"""
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gloo_rank_poisoned, args=(r, world, port, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(world):
+        rank, w, failed = q.get(timeout=120)
+        got[rank] = (w, failed)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    ref = OracleShardModel(N_PARAMS, seed=5)
+    for step in range(STEPS):
+        if step == 1:
+            continue
+        ref.zero_grad()
+        per_rank = []
+        for r in range(world):  # each rank's own sum, then the two ranks' (the all-reduce)
+            acc = torch.zeros(N_PARAMS, dtype=torch.float64)
+            for k in range(MICRO):
+                acc += _micro_grad(r, step, k)
+            per_rank.append(acc)
+        ref.g.copy_(per_rank[0] + per_rank[1])
+        ref.set_grad_count(world * MICRO)
+        ref.adamw_step_shard(0, N_PARAMS, **HP)
+    for r in range(world):
+        w, failed = got[r]
+        assert failed == [False, True, False]
+        assert np.array_equal(w, ref.w.numpy())
 
 
 def test_data_parallel_gloo_two_ranks_equals_one_process():
