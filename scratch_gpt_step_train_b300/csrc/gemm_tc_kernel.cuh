@@ -58,13 +58,17 @@ constexpr int NUM_THREADS = 320;  // producer, MMA, 8 epilogue warps
 // BN = 256 tiles run on CTA pairs (tcgen05 cta_group::2): the pair computes a
 // 256 x 256 tile, each CTA holding 128 rows of A and 128 rows (of N) of B, so
 // a stage is 32 KB per CTA and six fit; BN = 128 tiles run on single CTAs.
-template <int BN>
+template <int BN, int KB>
 struct Cfg {
     static constexpr bool PAIR = BN == 256;
-    static constexpr int STAGES = 6;
+    // KB k-blocks (64 deep) per pipeline stage: two halve the stage barriers
+    // and commits per instruction, which pays on the long-K products
+    static constexpr int KB2 = KB;
+    static constexpr int STAGES = 6 / KB2;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int HALF_BYTES = A_BYTES + B_BYTES;  // one k-block
+    static constexpr int STAGE_BYTES = KB2 * HALF_BYTES;
     static constexpr int STG_BYTES = 8 * 4096;  // epilogue staging: 4 KB per epilogue warp
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = STAGES * STAGE_BYTES + STG_BYTES + 1024 + BAR_BYTES;
@@ -366,11 +370,11 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const EpiMaps&
 }
 
 // ------------------------------------------------------------------- kernel
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, int KB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const __grid_constant__ EpiMaps maps, TcParams p) {
-    using CF = Cfg<BN>;
+    using CF = Cfg<BN, KB>;
     constexpr bool PAIR = CF::PAIR;
     constexpr int S = CF::STAGES;
     constexpr uint32_t IDESC = make_idesc(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
@@ -447,45 +451,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int nkb = (k1 - k0 + BK - 1) / BK;
                 // a pair CTA loads its own rows of A and its half (of N) of B
                 const int bn0 = tn * BN + (PAIR ? (int)rank * (BN / 2) : 0);
-                for (int kb = 0; kb < nkb; kb++) {
+                for (int kb2 = 0; kb2 < nkb; kb2 += CF::KB2) {
                     if (!mbar_wait(empty + 8 * s, ph ^ 1u, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = tiles + s * CF::STAGE_BYTES, sb = sa + CF::A_BYTES;
+                    const int nh = min(CF::KB2, nkb - kb2);
                     const uint32_t fb = full + 8 * s;
-                    const int kk = k0 + kb * BK;
                     if (PAIR) {
-                        // both CTAs' bytes are counted on the leader's barrier
-                        if (leader) mbar_expect_tx(fb, 2 * CF::STAGE_BYTES);
-                        const uint32_t fl = pair_mapa(fb, 0);
-                        if (!A_MN) {
-                            tma_load_2d_pair(sa, &mapA, fl, kk, tm * BM);
-                        } else {
-                            tma_load_2d_pair(sa, &mapA, fl, tm * BM, kk);
-                            tma_load_2d_pair(sa + 8192, &mapA, fl, tm * BM + 64, kk);
-                        }
-                        if (!B_MN) {
-                            tma_load_2d_pair(sb, &mapB, fl, kk, bn0);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < BN / 128; j++)
-                                tma_load_2d_pair(sb + j * 8192, &mapB, fl, bn0 + 64 * j, kk);
-                        }
+                        if (leader) mbar_expect_tx(fb, 2 * nh * CF::HALF_BYTES);
                     } else {
-                        mbar_expect_tx(fb, CF::STAGE_BYTES);
-                        if (!A_MN) {
-                            tma_load_2d(sa, &mapA, fb, kk, tm * BM);
-                        } else {
-                            tma_load_2d(sa, &mapA, fb, tm * BM, kk);
-                            tma_load_2d(sa + 8192, &mapA, fb, tm * BM + 64, kk);
-                        }
-                        if (!B_MN) {
-                            tma_load_2d(sb, &mapB, fb, kk, bn0);
-                        } else {
+                        mbar_expect_tx(fb, nh * CF::HALF_BYTES);
+                    }
+                    for (int hh = 0; hh < nh; hh++) {
+                        const uint32_t sa = tiles + s * CF::STAGE_BYTES + hh * CF::HALF_BYTES,
+                                       sb = sa + CF::A_BYTES;
+                        const int kk = k0 + (kb2 + hh) * BK;
+                        if (PAIR) {
+                            // both CTAs' bytes are counted on the leader's barrier
+                            const uint32_t fl = pair_mapa(fb, 0);
+                            if (!A_MN) {
+                                tma_load_2d_pair(sa, &mapA, fl, kk, tm * BM);
+                            } else {
+                                tma_load_2d_pair(sa, &mapA, fl, tm * BM, kk);
+                                tma_load_2d_pair(sa + 8192, &mapA, fl, tm * BM + 64, kk);
+                            }
+                            if (!B_MN) {
+                                tma_load_2d_pair(sb, &mapB, fl, kk, bn0);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < BN / 64; j++)
-                                tma_load_2d(sb + j * 8192, &mapB, fb, bn0 + 64 * j, kk);
+                                for (int j = 0; j < BN / 128; j++)
+                                    tma_load_2d_pair(sb + j * 8192, &mapB, fl, bn0 + 64 * j, kk);
+                            }
+                        } else {
+                            if (!A_MN) {
+                                tma_load_2d(sa, &mapA, fb, kk, tm * BM);
+                            } else {
+                                tma_load_2d(sa, &mapA, fb, tm * BM, kk);
+                                tma_load_2d(sa + 8192, &mapA, fb, tm * BM + 64, kk);
+                            }
+                            if (!B_MN) {
+                                tma_load_2d(sb, &mapB, fb, kk, bn0);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < BN / 64; j++)
+                                    tma_load_2d(sb + j * 8192, &mapB, fb, bn0 + 64 * j, kk);
+                            }
                         }
                     }
                     issued |= 1u << s;
@@ -536,24 +547,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t dt = tmem_base + (uint32_t)(b * BN);
-                for (int kb = 0; kb < nkb; kb++) {
+                for (int kb2 = 0; kb2 < nkb; kb2 += CF::KB2) {
                     if (!mbar_wait(full + 8 * s, ph, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad0 = dA0 + (uint64_t)((s * CF::STAGE_BYTES) >> 4);
-                    const uint64_t bd0 = dB0 + (uint64_t)((s * CF::STAGE_BYTES) >> 4);
+                    const int nh = min(CF::KB2, nkb - kb2);
+                    for (int hh = 0; hh < nh; hh++) {
+                        const int kb = kb2 + hh;
+                        const uint64_t ad0 =
+                            dA0 + (uint64_t)((s * CF::STAGE_BYTES + hh * CF::HALF_BYTES) >> 4);
+                        const uint64_t bd0 =
+                            dB0 + (uint64_t)((s * CF::STAGE_BYTES + hh * CF::HALF_BYTES) >> 4);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; k++) {
-                        if (PAIR)
-                            umma_bf16_pair(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
-                                           bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
-                                           (kb > 0 || k > 0) ? 1u : 0u);
-                        else
-                            umma_bf16(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
-                                      bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
-                                      (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < BK / 16; k++) {
+                            if (PAIR)
+                                umma_bf16_pair(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
+                                               bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
+                                               (kb > 0 || k > 0) ? 1u : 0u);
+                            else
+                                umma_bf16(dt, ad0 + (uint64_t)(k * (A_MN ? 128 : 2)),
+                                          bd0 + (uint64_t)(k * (B_MN ? 128 : 2)), IDESC,
+                                          (kb > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     if (PAIR) {  // the stage is free in both CTAs
                         umma_commit_pair(pair_mapa(empty + 8 * s, 0));
@@ -658,13 +675,13 @@ extern int g_num_sms;
 bool make_map(CUtensorMap* m, const void* base, long inner, long outer, long ld, int box_outer);
 bool make_epi_maps(EpiMaps* em, const GemmDesc& d, const TcParams& tp);
 
-template <int BN, bool AM, bool BMN, int EPI>
+template <int BN, bool AM, bool BMN, int EPI, int KB>
 cudaError_t launch_one(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     static bool attr = false;  // the dynamic shared-memory size, set once per kernel
     if (!attr) {
-        if (cudaFuncSetAttribute(k_gemm_tc<BN, AM, BMN, EPI>,
+        if (cudaFuncSetAttribute(k_gemm_tc<BN, AM, BMN, EPI, KB>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg<BN>::SMEM) != cudaSuccess)
+                                 Cfg<BN, KB>::SMEM) != cudaSuccess)
             return cudaGetLastError();
         attr = true;
     }
@@ -675,13 +692,13 @@ cudaError_t launch_one(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     bool ok = AM ? make_map(&ma, d.A, d.M, d.K, d.lda, 64)
                  : make_map(&ma, d.A, d.K, d.M, d.lda, BM);
     // B: K-major box 64(K) x BN rows (a pair CTA: its BN/2);  N-major box 64(N) x 64(K)
-    constexpr bool PAIR = Cfg<BN>::PAIR;
+    constexpr bool PAIR = Cfg<BN, KB>::PAIR;
     ok = ok && (BMN ? make_map(&mb, d.B, d.N, d.K, d.ldb, 64)
                     : make_map(&mb, d.B, d.K, d.N, d.ldb, PAIR ? BN / 2 : BN));
     if (!ok) return cudaErrorInvalidValue;
     if (!PAIR) {
         const int grid = tp.num_tiles < g_num_sms ? tp.num_tiles : g_num_sms;
-        launch_pdl(k_gemm_tc<BN, AM, BMN, EPI>, grid, NUM_THREADS, Cfg<BN>::SMEM, s, ma, mb, em, tp);
+        launch_pdl(k_gemm_tc<BN, AM, BMN, EPI, KB>, grid, NUM_THREADS, Cfg<BN, KB>::SMEM, s, ma, mb, em, tp);
         return cudaGetLastError();
     }
     // CTA pairs: clusters of 2, as many as can be resident at once
@@ -691,7 +708,7 @@ cudaError_t launch_one(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
         memset(&oc, 0, sizeof oc);
         oc.gridDim = dim3(g_num_sms);
         oc.blockDim = dim3(NUM_THREADS);
-        oc.dynamicSmemBytes = Cfg<BN>::SMEM;
+        oc.dynamicSmemBytes = Cfg<BN, KB>::SMEM;
         cudaLaunchAttribute ca[1];
         ca[0].id = cudaLaunchAttributeClusterDimension;
         ca[0].val.clusterDim.x = 2;
@@ -700,7 +717,7 @@ cudaError_t launch_one(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
         oc.attrs = ca;
         oc.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<BN, AM, BMN, EPI>, &oc) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<BN, AM, BMN, EPI, KB>, &oc) != cudaSuccess ||
             n < 1) {
             cudaGetLastError();
             n = g_num_sms / 2;
@@ -714,7 +731,7 @@ cudaError_t launch_one(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<BN, KB>::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute la[2];
     la[0].id = cudaLaunchAttributeClusterDimension;
@@ -725,30 +742,45 @@ cudaError_t launch_one(const GemmDesc& d, const TcParams& tp, cudaStream_t s) {
     la[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, AM, BMN, EPI>, ma, mb, em, tp);
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, AM, BMN, EPI, KB>, ma, mb, em, tp);
 }
 
 // the launch for epilogue mode EPI, tile width bn and operand layouts am, bm
+// modes whose 256-wide products take two k-blocks per stage when K is long
+// (measured: 2-6% faster there; the multiply-by-aux epilogue and the split
+// partials were not)
+constexpr bool kb2_mode(int epi) {
+    return epi == EPI_STORE || epi == EPI_RESID || epi == EPI_GELU || epi == EPI_GELU_D ||
+           epi == EPI_ACCUM_F32;
+}
 template <int EPI>
-cudaError_t launch_epi(int bn, bool am, bool bm, const GemmDesc& d, const TcParams& tp,
+cudaError_t launch_epi(int bn, bool am, bool bm, bool kb2, const GemmDesc& d, const TcParams& tp,
                        cudaStream_t s) {
     if (bn == 256) {
-        if (!am && !bm) return launch_one<256, false, false, EPI>(d, tp, s);
-        if (!am && bm) return launch_one<256, false, true, EPI>(d, tp, s);
-        if (am && !bm) return launch_one<256, true, false, EPI>(d, tp, s);
-        return launch_one<256, true, true, EPI>(d, tp, s);
+        if constexpr (kb2_mode(EPI)) {
+            if (kb2) {
+                if (!am && !bm) return launch_one<256, false, false, EPI, 2>(d, tp, s);
+                if (!am && bm) return launch_one<256, false, true, EPI, 2>(d, tp, s);
+                if (am && !bm) return launch_one<256, true, false, EPI, 2>(d, tp, s);
+                return launch_one<256, true, true, EPI, 2>(d, tp, s);
+            }
+        }
+        if (!am && !bm) return launch_one<256, false, false, EPI, 1>(d, tp, s);
+        if (!am && bm) return launch_one<256, false, true, EPI, 1>(d, tp, s);
+        if (am && !bm) return launch_one<256, true, false, EPI, 1>(d, tp, s);
+        return launch_one<256, true, true, EPI, 1>(d, tp, s);
     }
-    if (!am && !bm) return launch_one<128, false, false, EPI>(d, tp, s);
-    if (!am && bm) return launch_one<128, false, true, EPI>(d, tp, s);
-    if (am && !bm) return launch_one<128, true, false, EPI>(d, tp, s);
-    return launch_one<128, true, true, EPI>(d, tp, s);
+    if (!am && !bm) return launch_one<128, false, false, EPI, 1>(d, tp, s);
+    if (!am && bm) return launch_one<128, false, true, EPI, 1>(d, tp, s);
+    if (am && !bm) return launch_one<128, true, false, EPI, 1>(d, tp, s);
+    return launch_one<128, true, true, EPI, 1>(d, tp, s);
 }
 
 #define GK_GEMM_EPI_EXTERN(E)                                                                 \
-    extern template cudaError_t launch_epi<E>(int, bool, bool, const GemmDesc&, const TcParams&, \
-                                              cudaStream_t);
+    extern template cudaError_t launch_epi<E>(int, bool, bool, bool, const GemmDesc&,              \
+                                              const TcParams&, cudaStream_t);
 #define GK_GEMM_EPI_INSTANTIATE(E)                                                          \
-    template cudaError_t launch_epi<E>(int, bool, bool, const GemmDesc&, const TcParams&,     \
+    template cudaError_t launch_epi<E>(int, bool, bool, bool, const GemmDesc&, const TcParams&, \
                                        cudaStream_t);
 
 }  // namespace tcg

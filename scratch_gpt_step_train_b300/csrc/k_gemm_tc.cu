@@ -260,16 +260,18 @@ cudaError_t gemm_tc(const GemmDesc& d, void* scratch, size_t scratch_bytes, unsi
     }
     tp.num_tiles = (int)(tiles * tp.splits);
     const bool am = !d.a_kmajor, bm = !d.b_kmajor;
+    // two k-blocks per pipeline stage for the long-K products
+    const bool kb2 = tp.splits == 1 && d.K >= 1536;
     cudaError_t e;
     switch (tp.epi) {  // one kernel per epilogue mode
-        case EPI_STORE: e = launch_epi<EPI_STORE>(BN, am, bm, d, tp, s); break;
-        case EPI_RESID: e = launch_epi<EPI_RESID>(BN, am, bm, d, tp, s); break;
-        case EPI_GELU: e = launch_epi<EPI_GELU>(BN, am, bm, d, tp, s); break;
-        case EPI_GELU_D: e = launch_epi<EPI_GELU_D>(BN, am, bm, d, tp, s); break;
-        case EPI_GELU_BWD: e = launch_epi<EPI_GELU_BWD>(BN, am, bm, d, tp, s); break;
-        case EPI_MUL_AUX: e = launch_epi<EPI_MUL_AUX>(BN, am, bm, d, tp, s); break;
-        case EPI_ACCUM_F32: e = launch_epi<EPI_ACCUM_F32>(BN, am, bm, d, tp, s); break;
-        case EPI_PART_F32: e = launch_epi<EPI_PART_F32>(BN, am, bm, d, tp, s); break;
+        case EPI_STORE: e = launch_epi<EPI_STORE>(BN, am, bm, kb2, d, tp, s); break;
+        case EPI_RESID: e = launch_epi<EPI_RESID>(BN, am, bm, kb2, d, tp, s); break;
+        case EPI_GELU: e = launch_epi<EPI_GELU>(BN, am, bm, kb2, d, tp, s); break;
+        case EPI_GELU_D: e = launch_epi<EPI_GELU_D>(BN, am, bm, kb2, d, tp, s); break;
+        case EPI_GELU_BWD: e = launch_epi<EPI_GELU_BWD>(BN, am, bm, kb2, d, tp, s); break;
+        case EPI_MUL_AUX: e = launch_epi<EPI_MUL_AUX>(BN, am, bm, kb2, d, tp, s); break;
+        case EPI_ACCUM_F32: e = launch_epi<EPI_ACCUM_F32>(BN, am, bm, kb2, d, tp, s); break;
+        case EPI_PART_F32: e = launch_epi<EPI_PART_F32>(BN, am, bm, kb2, d, tp, s); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
