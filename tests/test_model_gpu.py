@@ -357,3 +357,26 @@ def test_errors_are_reported():
     gm.zero_grad()
     rc, _ = gm.adamw_step_rc(1e-3)
     assert rc == -4
+
+
+def test_bf16_gradients_near_the_oracle():
+    """bf16-mixed mode, one forward/backward at the mid shape (head size 64:
+    the tensor-core attention and products, the fc bias gradient out of the
+    fcproj product's epilogue, the batched column sums): every gradient
+    tensor within a relative L2 error of 5e-2 of the fp64 oracle, and the
+    bias and LayerNorm tensors (summed by the batched column sums) within the
+    same bar.  The bar: every stored activation and gradient is rounded to
+    bf16 (relative 2^-8); a 2-layer model stores about a dozen of them on any
+    path from the loss to a parameter, a few percent at most."""
+    om, gm = _pair(MID, BF16, seed=3, perturb=5)
+    tok, tgt = inputs.uniform_batch(7, MID["B"], MID["T"], MID["V"])
+    om.zero_grad()
+    om.forward(tok, tgt)
+    om.backward()
+    gm.zero_grad()
+    gm.forward(tok, tgt, sync_loss=True)
+    gm.backward()
+    got, ref = om.split(gm.get_grads().astype(np.float64)), om.split(om.grads())
+    errs = {k: float(np.linalg.norm(got[k] - ref[k]) / np.linalg.norm(ref[k])) for k in ref}
+    assert all(np.isfinite(v) for v in errs.values()), errs
+    assert max(errs.values()) <= 5e-2, errs
